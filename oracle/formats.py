@@ -1,0 +1,87 @@
+"""Number formats: E2M1 elements, E4M3 inner scales, UE8M0 FP8-slice scales.
+
+Test infrastructure only (see the package docstring).
+
+TetraJet-v2 technical summary §2.A: NVFP4 stores 4-bit values in groups of 16
+with an 8-bit scale.  The 4-bit value format is E2M1 (sign, 2 exponent bits,
+1 mantissa bit); its magnitudes are the grid below, which is the format's own
+definition (the lay explainer's "only 0 or 0.5" example is its first step).
+The 8-bit group scale is E4M3 (bias 7, no infinities, max 448, the all-ones
+mantissa at exponent 15 is NaN).  The FP8 outlier slice of §2.C uses E4M3
+values with a power-of-two UE8M0 scale per 32 elements (reading: the pages
+only say "e.g. FP8").
+"""
+import numpy as np
+
+# E2M1 magnitudes, indexed by the 3 low bits of a code; bit 3 is the sign.
+E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float32)
+E2M1_MAX = np.float32(6.0)
+E4M3_MAX = np.float32(448.0)
+
+
+def e4m3_decode(byte):
+    """Value of an E4M3 byte (array of uint8) as float64; NaN for 0x7F/0xFF."""
+    b = np.asarray(byte, dtype=np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = b & 0x7
+    sub = m.astype(np.float64) * 2.0 ** -9           # e == 0: m/8 * 2^(1-7)
+    nor = (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0)
+    val = np.where(e == 0, sub, nor)
+    val = np.where((e == 15) & (m == 7), np.nan, val)
+    return sign * val
+
+
+# All non-negative finite E4M3 values with their byte, in increasing order.
+_E4M3_POS_BYTES = np.arange(0, 0x7F, dtype=np.uint8)          # 0x00 .. 0x7E
+_E4M3_POS_VALS = e4m3_decode(_E4M3_POS_BYTES)                  # strictly increasing
+
+
+def e4m3_ceil_byte(t):
+    """Smallest E4M3 value >= t (t >= 0, fp32), clamped to 448; returns the byte.
+
+    Reading (inner-scale rounding): the inner scale is rounded UP onto the
+    E4M3 grid so that every scaled element stays within the E2M1 range and
+    stochastic rounding needs no clipping (this keeps §2.A's E[round(x)] = x
+    exact).  t == 0 gives byte 0.
+    """
+    t = np.asarray(t, dtype=np.float64)
+    idx = np.searchsorted(_E4M3_POS_VALS, t, side="left")
+    idx = np.minimum(idx, len(_E4M3_POS_VALS) - 1)               # clamp to 448
+    return _E4M3_POS_BYTES[idx]
+
+
+def e4m3_rne_satfinite_byte(x):
+    """Nearest finite E4M3 value to fp32 x, ties to even mantissa, |x|>448 -> 448.
+
+    Used for the FP8 outlier slice (§2.C).  Returns the byte (sign in bit 7).
+    Zero and values that round to zero give +0 / -0 by the sign of x.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    vals = _E4M3_POS_VALS
+    hi = np.searchsorted(vals, a, side="left")                   # vals[hi] >= a
+    hi = np.minimum(hi, len(vals) - 1)
+    lo = np.maximum(hi - 1, 0)
+    v_hi = vals[hi]
+    v_lo = vals[lo]
+    exact = v_hi == a
+    d_lo = a - v_lo
+    d_hi = v_hi - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((_E4M3_POS_BYTES[hi] & 1) == 0))
+    byte = np.where(exact | pick_hi, _E4M3_POS_BYTES[hi], _E4M3_POS_BYTES[lo])
+    byte = np.where(a >= 448.0, np.uint8(0x7E), byte)               # satfinite
+    sign = np.where(np.signbit(x), 0x80, 0x00).astype(np.uint8)
+    return (byte.astype(np.uint8) | sign).astype(np.uint8)
+
+
+def ue8m0_decode(byte):
+    """UE8M0 scale byte -> 2^(byte-127) as float64."""
+    return np.exp2(np.asarray(byte, dtype=np.float64) - 127.0)
+
+
+def e2m1_decode(code):
+    """Signed E2M1 value of a code (low 4 bits), as float64."""
+    c = np.asarray(code, dtype=np.int64)
+    mag = E2M1_GRID[c & 7].astype(np.float64)
+    return np.where(c & 8, -mag, mag)

@@ -1,0 +1,147 @@
+"""NVFP4 linear layer: forward Y = X W^T, backward dX = dY W, dW = dY^T X.
+
+Test infrastructure only (see the package docstring).
+
+TetraJet-v2 technical summary §2 (all linear layers take NVFP4 activations,
+weights and gradients), §2.A (backward "aligned": it estimates with X-hat, the
+dequantized forward operand, not X; SR in the backward; 1x16 weight groups, so
+the transposed weight is re-grouped along the new contraction axis) and §2.C
+(RHT on the backward contractions; a static top-p% set of outlier channels kept
+in FP8 in forward and backward).
+
+Notation: X [M, K], W [N, K], dY [M, N].  O = outlier channels (sorted), k = |O|;
+NC = the other channels, ascending, K_N = K - k.  Readings:
+  * channels are the input features K; normal channels are compacted in
+    ascending order before blocking;
+  * both operands of an outlier-slice product are MXFP8 (RTN, no RHT);
+  * the backward re-quantizes the fp32 dequantized forward operands;
+  * SR tags: 1 = dY rows (dX), 2 = dY^T rows (dW), 3 = W-hat^T, 4 = X-hat^T;
+    RHT sign tags 0x100 (dX) and 0x101 (dW); alpha = 2^-7 undoes H^T H = 128 I.
+All products are accumulated in fp64 on exactly dequantized operands.
+"""
+import numpy as np
+
+from . import quant as Q
+from .philox import rht_signs
+from .rht import rht_f32
+
+F32 = np.float32
+TAG_DY_ROW, TAG_DY_COL, TAG_WT, TAG_XT = 1, 2, 3, 4
+TAG_RHT_DX, TAG_RHT_DW = 0x100, 0x101
+ALPHA_RHT = 2.0 ** -7
+
+
+def normal_channels(K, outlier_idx):
+    """Ascending complement of the outlier set in 0..K-1."""
+    mask = np.ones(K, dtype=bool)
+    mask[np.asarray(outlier_idx, dtype=np.int64)] = False
+    return np.nonzero(mask)[0].astype(np.int64)
+
+
+def quantize_forward_operand(A, outlier_idx):
+    """Forward quantization of an operand [rows, K] along K (X or W).
+
+    Returns dict(q=(codes, sf, outer) of the normal channels, RTN double-block,
+                 q8=(codes, scales) MXFP8 of the outlier channels or None).
+    """
+    A = np.asarray(A, dtype=F32)
+    K = A.shape[1]
+    o = np.asarray(outlier_idx, dtype=np.int64)
+    nc = normal_channels(K, o)
+    q = Q.quantize_nvfp4(A[:, nc], Q.RTN)
+    q8 = Q.quantize_mxfp8(A[:, o]) if len(o) else None
+    return {"q": q, "q8": q8, "K_N": len(nc), "k": len(o)}
+
+
+def gemm_fp4(qa, qb, alpha=1.0):
+    """alpha * deq(A) deq(B)^T in fp64 for two double-block operands (same Lp)."""
+    a = Q.dequantize_nvfp4_f64(*qa)
+    b = Q.dequantize_nvfp4_f64(*qb)
+    return alpha * (a @ b.T)
+
+
+def gemm_fp8(qa, qb):
+    """deq(A) deq(B)^T in fp64 for two MXFP8 operands."""
+    return Q.dequantize_mxfp8_f64(*qa) @ Q.dequantize_mxfp8_f64(*qb).T
+
+
+def forward(X, W, outlier_idx):
+    """Y = X-hat W-hat^T (fp64), plus the saved quantized forward operands."""
+    fx = quantize_forward_operand(X, outlier_idx)
+    fw = quantize_forward_operand(W, outlier_idx)
+    Y = gemm_fp4(fx["q"], fw["q"])
+    if fx["q8"] is not None:
+        Y = Y + gemm_fp8(fx["q8"], fw["q8"])
+    return Y, fx, fw
+
+
+def sr_rht_rows(A, seed, sr_tag, rht_tag, row_ids=None):
+    """SR double-block quantization of RHT(rows of A) along the row (zero-padded to 128)."""
+    Ap = Q.pad_cols(A, Q.OUTER)
+    d = rht_signs(seed, rht_tag)
+    return Q.quantize_nvfp4(rht_f32(Ap, d), Q.SR, seed=seed, tag=sr_tag, row_ids=row_ids)
+
+
+def deq_normal_f32(fq):
+    """fp32 X-hat / W-hat of the normal channels, [rows, K_N] (padding dropped)."""
+    return Q.dequantize_nvfp4_f32(*fq["q"])[:, : fq["K_N"]]
+
+
+def deq_outlier_f32(fq):
+    """fp32 dequantized outlier slice, [rows, k]."""
+    return Q.dequantize_mxfp8_f32(*fq["q8"])[:, : fq["k"]]
+
+
+def bwd_dx_operands(dY, fw, seed):
+    """Quantized operands of dX: (S_dY, S_W, Q8(dY), Q8(W-hat_O^T))."""
+    s_dy = sr_rht_rows(dY, seed, TAG_DY_ROW, TAG_RHT_DX)
+    s_w = sr_rht_rows(deq_normal_f32(fw).T, seed, TAG_WT, TAG_RHT_DX)
+    if fw["k"]:
+        q8_dy = Q.quantize_mxfp8(dY)
+        q8_w = Q.quantize_mxfp8(deq_outlier_f32(fw).T)
+    else:
+        q8_dy = q8_w = None
+    return s_dy, s_w, q8_dy, q8_w
+
+
+def bwd_dx(dY, fw, outlier_idx, seed):
+    """dX [M, K] = 2^-7 S_dY S_W^T on the normal channels, FP8 slice on the outliers."""
+    dY = np.asarray(dY, dtype=F32)
+    M = dY.shape[0]
+    o = np.asarray(outlier_idx, dtype=np.int64)
+    K = fw["K_N"] + fw["k"]
+    nc = normal_channels(K, o)
+    s_dy, s_w, q8_dy, q8_w = bwd_dx_operands(dY, fw, seed)
+    dX = np.zeros((M, K), dtype=np.float64)
+    dX[:, nc] = gemm_fp4(s_dy, s_w, ALPHA_RHT)[:, : len(nc)]
+    if len(o):
+        dX[:, o] = gemm_fp8(q8_dy, q8_w)[:, : len(o)]
+    return dX
+
+
+def bwd_dw_operands(dY, fx, seed):
+    """Quantized operands of dW: (S_dY^T, S_X, Q8(dY^T), Q8(X-hat_O^T))."""
+    dYt = np.ascontiguousarray(np.asarray(dY, dtype=F32).T)
+    s_dy = sr_rht_rows(dYt, seed, TAG_DY_COL, TAG_RHT_DW)
+    s_x = sr_rht_rows(deq_normal_f32(fx).T, seed, TAG_XT, TAG_RHT_DW)
+    if fx["k"]:
+        q8_dy = Q.quantize_mxfp8(dYt)
+        q8_x = Q.quantize_mxfp8(deq_outlier_f32(fx).T)
+    else:
+        q8_dy = q8_x = None
+    return s_dy, s_x, q8_dy, q8_x
+
+
+def bwd_dw(dY, fx, outlier_idx, seed):
+    """dW [N, K] = 2^-7 S_dY^T S_X^T on the normal channels, FP8 slice on the outliers."""
+    dY = np.asarray(dY, dtype=F32)
+    N = dY.shape[1]
+    o = np.asarray(outlier_idx, dtype=np.int64)
+    K = fx["K_N"] + fx["k"]
+    nc = normal_channels(K, o)
+    s_dy, s_x, q8_dy, q8_x = bwd_dw_operands(dY, fx, seed)
+    dW = np.zeros((N, K), dtype=np.float64)
+    dW[:, nc] = gemm_fp4(s_dy, s_x, ALPHA_RHT)[:, : len(nc)]
+    if len(o):
+        dW[:, o] = gemm_fp8(q8_dy, q8_x)[:, : len(o)]
+    return dW

@@ -1,0 +1,63 @@
+"""OsciReset: oscillation tracking and reset of master weights.
+
+Test infrastructure only (see the package docstring).
+
+TetraJet-v2 technical summary §2.B: follow each weight's optimisation
+trajectory; the oscillation risk is dist_Q / dist_M, the distance travelled by
+the quantized weight over the distance travelled by the master weight.  When
+the learning rate is low and the risk exceeds a threshold, the master weight
+of the oscillating element is set to the centre of its current quantization
+bin.
+
+Readings:
+  * distances are cumulative L1 path lengths in fp32, summed step by step
+    from the start of tracking and zeroed on a reset;
+  * Q-hat is the fp32 dequantized RTN double-block quantization of the master
+    weight, rows quantized along their length (the forward weight layout,
+    without an outlier split);
+  * "bin centre" is the grid point itself, i.e. Q-hat, so a reset never
+    changes which bin the weight is in;
+  * reset  <=>  track and lr < lr_thr and dist_M > 0 and dist_Q > r * dist_M
+    (fp32 product); 0/0 never resets;
+  * after the step, w_prev <- w and Q-hat_prev <- Q-hat.
+"""
+import numpy as np
+
+from . import quant as Q
+
+F32 = np.float32
+
+
+def qhat_f32(w):
+    """fp32 Q-hat of a master weight matrix [rows, cols] (cols padded to 128 internally)."""
+    w = np.asarray(w, dtype=F32)
+    c, s, o = Q.quantize_nvfp4(w, Q.RTN)
+    return Q.dequantize_nvfp4_f32(c, s, o)[:, : w.shape[1]], (c, s, o)
+
+
+def init_state(w0):
+    """State at the start of tracking: w_prev = w0, Q-hat_prev = Q-hat(w0), distances 0."""
+    w0 = np.asarray(w0, dtype=F32)
+    qh, _ = qhat_f32(w0)
+    z = np.zeros_like(w0)
+    return {"w_prev": w0.copy(), "qhat_prev": qh, "dist_q": z.copy(), "dist_m": z.copy()}
+
+
+def osci_reset_step(w, state, lr, lr_thr, risk_thr, track=True):
+    """One OsciReset pass after an optimizer step.  Returns (w_new, state_new, mask, q).
+
+    q is the RTN double-block quantization (codes, sf, outer) of the
+    pre-reset w, i.e. the next forward's weight operand.
+    """
+    w = np.asarray(w, dtype=F32)
+    dist_m = (state["dist_m"] + np.abs((w - state["w_prev"]).astype(F32))).astype(F32)
+    qh, q = qhat_f32(w)
+    dist_q = (state["dist_q"] + np.abs((qh - state["qhat_prev"]).astype(F32))).astype(F32)
+    lr_low = bool(np.float32(lr) < np.float32(lr_thr))
+    risky = (dist_m > 0) & (dist_q > (F32(risk_thr) * dist_m).astype(F32))
+    mask = risky & bool(track) & lr_low
+    w_new = np.where(mask, qh, w).astype(F32)
+    dist_q = np.where(mask, F32(0.0), dist_q).astype(F32)
+    dist_m = np.where(mask, F32(0.0), dist_m).astype(F32)
+    new_state = {"w_prev": w_new.copy(), "qhat_prev": qh, "dist_q": dist_q, "dist_m": dist_m}
+    return w_new, new_state, mask, q

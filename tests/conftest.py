@@ -1,0 +1,23 @@
+"""Shared pytest configuration.
+
+Markers: ``gpu`` marks a test that needs a CUDA device (the parity tests that
+call the CUDA library through its C ABI).  CPU-only runs use ``-m "not gpu"``.
+"""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    config.addinivalue_line("markers", "slow: full-size parity case (minutes of oracle time)")
+
+
+@pytest.fixture(scope="session")
+def golden_dir():
+    return os.path.join(ROOT, "tests", "golden")
