@@ -1,0 +1,254 @@
+/*
+ * tj.h - C ABI of the GB300 (sm_103a) TetraJet-v2 NVFP4 linear-layer library.
+ *
+ * The method: arXiv 2510.27527, "TetraJet-v2: Accurate NVFP4 Training for Large
+ * Language Models with Oscillation Suppression and Outlier Control", as given
+ * by its technical summary pages (gist.science, nl/es/ja; sections cited as
+ * §2.A double-block quantization, §2.B OsciReset, §2.C OutControl).
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates or frees device memory; scratch space is passed in as
+ *     `workspace` with its size from tj_workspace_size().
+ *   - Pointers must be 16-byte aligned and leading dimensions (`ld`, in
+ *     elements) multiples of 8; violations return TJ_ERR_ALIGN before any launch.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and never synchronize.  Argument/shape errors are detected on the
+ *     host before any launch and leave outputs untouched; a failed launch maps to
+ *     TJ_ERR_CUDA.  Device-side bounded waits that run out set a sticky device
+ *     flag read by tj_get_device_status().
+ *   - Inputs must be finite.  Padded regions of outputs are written (zeros).
+ *
+ * Data layouts in HBM
+ *   NVFP4 double-block tensor (tj_nvfp4), logical [rows, cols] quantized along
+ *   cols (the contraction dimension of the GEMM that consumes it);
+ *   rows_p = roundup(rows, 128), cols_p = roundup(cols, 128):
+ *     codes  uint8 [rows_p][cols_p/2]   E2M1; element 2j in the LOW nibble of byte j;
+ *                                        bit 3 of a code is the sign.
+ *     sf     uint8 [rows_p*cols_p/16]   E4M3 inner scales (one per 1x16 group) in the
+ *                                        MMA tile layout below.
+ *     outer  float [cols_p/128][rows_p] FP32 outer scales (one per 1x128 block),
+ *                                        block-major so one block's scales for 128
+ *                                        consecutive rows are contiguous.
+ *   MXFP8 outlier slice (tj_mxfp8), logical [rows, cols] along cols:
+ *     codes  uint8 [rows_p][cols_p]     E4M3 values.
+ *     sf     uint8 [rows_p*cols_p/32]   UE8M0 scales (one per 1x32 group), tile layout.
+ *   Scale tile layout (both formats; B = 16 for NVFP4, 32 for MXFP8): the scales
+ *   form tiles of 128 rows x 4 consecutive groups; tile (rt, kt) starts at byte
+ *   (rt * (cols_p / (4*B)) + kt) * 512; inside it, the scale of row
+ *   rt*128 + 32*i + j (i < 4, j < 32) and group 4*kt + q sits at byte 16*j + 4*i + q.
+ *   This is the order in which the block-scaled tensor-core MMA reads its scale
+ *   factors from tensor memory, so the GEMM copies tiles without rearranging.
+ *
+ * Number formats (§2.A): E2M1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}; E4M3 inner
+ * scales; FP32 outer scale s_o = amax_128 / 2688 (2688 = 6 * 448); inner scale =
+ * smallest E4M3 >= amax_16 / (6 s_o) (clamped to 448); elements x * (1/(s_i s_o))
+ * clamped to 6, rounded to nearest-even (forward) or stochastically (backward).
+ */
+#ifndef TJ_H
+#define TJ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TJ_OK = 0,
+    TJ_ERR_INVALID_ARG = 1,   /* null pointer, bad enum, negative size */
+    TJ_ERR_SHAPE = 2,         /* inconsistent or unsupported sizes */
+    TJ_ERR_ALIGN = 3,         /* pointer or leading dimension misaligned */
+    TJ_ERR_UNSUPPORTED = 4,   /* device is not sm_103a-class, or feature not built */
+    TJ_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
+    TJ_ERR_TIMEOUT = 6,       /* a device-side bounded wait ran out (sticky) */
+    TJ_ERR_WORKSPACE = 7      /* workspace pointer null or smaller than required */
+} tj_status;
+
+typedef enum { TJ_RTN = 0, TJ_SR = 1 } tj_round;
+typedef enum { TJ_BF16 = 0, TJ_FP32 = 1 } tj_dtype;
+
+/* NVFP4 double-block tensor (caller-owned device buffers; layout above). */
+typedef struct {
+    uint8_t *codes;
+    uint8_t *sf;
+    float *outer;
+    int64_t rows;
+    int64_t cols;
+} tj_nvfp4;
+
+/* MXFP8 outlier slice (caller-owned device buffers; layout above). */
+typedef struct {
+    uint8_t *codes;
+    uint8_t *sf;
+    int64_t rows;
+    int64_t cols;
+} tj_mxfp8;
+
+/* Philox tags used inside the backward calls (documented for reproducibility):
+ * stochastic rounding of dY rows (dX operand), of dY^T rows (dW operand), of the
+ * re-aligned W-hat^T and X-hat^T, and the RHT sign vectors of dX and dW. */
+#define TJ_TAG_DY_ROW 1u
+#define TJ_TAG_DY_COL 2u
+#define TJ_TAG_WT 3u
+#define TJ_TAG_XT 4u
+#define TJ_TAG_RHT_DX 0x100u
+#define TJ_TAG_RHT_DW 0x101u
+
+/* ---------------------------------------------------------------------------
+ * tj_quantize_nvfp4 - double-block NVFP4 quantization (§2.A), optionally after a
+ * 128-point random Hadamard transform (§2.C).
+ *
+ *   x          device [rows_x, cols_x] bf16 or fp32 (dtype), row stride ld elements.
+ *   along_cols 0: output row r = input row r, quantized along the input columns.
+ *              1: transposed alignment (§2.A, 1x16 groups of the transposed
+ *                 operand): output row c = input column c, quantized along the
+ *                 input rows.
+ *   sel, n_sel optional (sel may be NULL -> all columns, n_sel ignored): ascending
+ *              int32 input-column indices to keep (OutControl's normal channels).
+ *              along_cols=0: they form the compacted contraction (out->cols = n_sel);
+ *              along_cols=1: they are the output rows (out->rows = n_sel).
+ *   mode       TJ_RTN or TJ_SR.  SR draws 16 bits per element from Philox4x32-10
+ *              with key = seed, counter = (e >> 3, tag, 0), e = out_row*cols_p + col.
+ *   rht        0/1: apply y = H128 * (d .* x) per 128-block of the quantized axis
+ *              (zero-padded), d from Philox(key = seed, counter = (0, 0, rht_tag, 0)).
+ *   out        caller-filled tj_nvfp4 whose rows/cols must equal the output shape.
+ * Errors: TJ_ERR_INVALID_ARG, TJ_ERR_SHAPE, TJ_ERR_ALIGN, TJ_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+tj_status tj_quantize_nvfp4(const void *x, int dtype, int64_t rows_x, int64_t cols_x, int64_t ld,
+                            int along_cols, const int32_t *sel, int64_t n_sel, int mode,
+                            int rht, uint64_t seed, uint32_t tag, uint32_t rht_tag,
+                            tj_nvfp4 *out, void *stream);
+
+/* tj_quantize_mxfp8 - FP8 outlier slice (§2.C "kept in higher precision, e.g.
+ * FP8"): E4M3 values with a UE8M0 scale 2^E per 1x32 group, E the smallest
+ * integer with 448*2^E >= amax_32, values rounded to nearest-even and saturated.
+ * Same x / along_cols / sel conventions as tj_quantize_nvfp4 (no RHT, no SR). */
+tj_status tj_quantize_mxfp8(const void *x, int dtype, int64_t rows_x, int64_t cols_x, int64_t ld,
+                            int along_cols, const int32_t *sel, int64_t n_sel,
+                            tj_mxfp8 *out, void *stream);
+
+/* tj_rht - standalone random Hadamard transform (§2.C): for each row of x (fp32,
+ * [rows, cols], cols a multiple of 128, contiguous) y = H128 * (d .* x) per
+ * 128-block, unnormalised, fp32 butterflies in stage order 1, 2, ..., 64.
+ * d from Philox(key = seed, counter = (0, 0, tag, 0)).  y may alias x. */
+tj_status tj_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,
+                 void *stream);
+
+/* tj_dequantize_nvfp4 - fp32 X-hat = (G * s_i) * s_o of a tj_nvfp4 into y
+ * [rows, cols] (row stride ldy).  The value the aligned backward re-quantizes. */
+tj_status tj_dequantize_nvfp4(const tj_nvfp4 *q, float *y, int64_t ldy, void *stream);
+
+/* tj_gemm_nvfp4 - block-scaled FP4 GEMM with FP32 outer-scale promotion:
+ *   D[m, n] = alpha * sum_kb sA[m,kb] sB[n,kb] * (sum over the 128 elements of
+ *             block kb of  (a s_iA)(b s_iB))  [+ sum over the FP8 slice a8 b8]
+ * A [M, K] and B [N, K] are both quantized along K (tcgen05 kind::mxf4nvf4,
+ * UE4M3 per 16; optional FP8 part kind::mxf8f6f4, UE8M0 per 32, accumulated into
+ * the same tile).  a8/b8 may be NULL (no FP8 part).  D is row-major [M, N] with
+ * row stride ldd, fp32 or bf16 (out_dtype); col_map (may be NULL) scatters
+ * column n of the product to column col_map[n] of D.  The product of one 16-group
+ * is exact; the FP32 accumulation is the only rounding (within 2e-3 sum|a||b|). */
+tj_status tj_gemm_nvfp4(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8, const tj_mxfp8 *b8,
+                        float alpha, void *d, int out_dtype, int64_t ldd, const int32_t *col_map,
+                        void *stream);
+
+/* tj_gemm_mxfp8 - FP8 slice GEMM alone: D[m, col_map[n]] = sum a8 b8 (used for the
+ * outlier columns of dX and dW, whose outputs are distinct columns). */
+tj_status tj_gemm_mxfp8(const tj_mxfp8 *a8, const tj_mxfp8 *b8, void *d, int out_dtype, int64_t ldd,
+                        const int32_t *col_map, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * tj_linear_fwd - forward of the NVFP4 linear layer (§2: NVFP4 for activations,
+ * weights and gradients of every linear layer; §2.A RTN double-block quantization;
+ * §2.C static outlier channels kept in FP8):
+ *   Y[M, N] = Q(X[:, NC]) Q(W[:, NC])^T + Q8(X[:, O]) Q8(W[:, O])^T
+ * x           bf16 [M, K], row stride ldx.
+ * wq, w8      W's forward operands: NVFP4 [N, K_N] and FP8 slice [N, k] (w8 NULL iff
+ *             k == 0), e.g. from tj_quantize_nvfp4/_mxfp8 with sel = normal_idx /
+ *             outlier_idx, or wq from tj_osci_reset when k == 0.
+ * normal_idx  int32 [K_N] ascending, outlier_idx int32 [k] ascending (device); both
+ *             NULL with k == 0 means no OutControl (K_N = K).
+ * xq, x8      caller buffers receiving the saved context X-hat: NVFP4 [M, K_N] and FP8
+ *             [M, k] (x8 NULL iff k == 0); the backward reads them (alignment, §2.A).
+ * y           [M, N] bf16 or fp32 (out_dtype), row stride ldy.
+ * ------------------------------------------------------------------------- */
+tj_status tj_linear_fwd(const void *x, int64_t M, int64_t K, int64_t ldx, const tj_nvfp4 *wq,
+                        const tj_mxfp8 *w8, const int32_t *normal_idx, const int32_t *outlier_idx,
+                        int64_t k, tj_nvfp4 *xq, tj_mxfp8 *x8, void *y, int out_dtype, int64_t ldy,
+                        void *stream);
+
+/* tj_linear_bwd_dx - input gradient (§2.A aligned backward with SR; §2.C RHT and
+ * FP8 outlier columns):
+ *   dX[:, NC] = 2^-7 SR(RHT(dY)) SR(RHT(W-hat_NC^T))^T   (RHT along N, tags above)
+ *   dX[:, O]  = Q8(dY) Q8(W-hat_O^T)^T                   (RTN, no RHT)
+ * W-hat is read from the forward operands wq / w8 (never the master weight).
+ * dy bf16 [M, N] (lddy); dx [M, K] bf16 or fp32 (lddx); seed = per-step Philox key.
+ * workspace: at least tj_workspace_size(TJ_OP_BWD_DX, M, N, K, k) bytes, 256-aligned.
+ * On return the workspace holds the quantized operands, each buffer starting on a
+ * 256-byte boundary in this order: S_dY (tj_nvfp4 [M, N]: codes, sf, outer),
+ * S_W (tj_nvfp4 [K_N, N]), and when k > 0 Q8(dY) (tj_mxfp8 [M, N]: codes, sf) and
+ * Q8(W-hat_O^T) (tj_mxfp8 [k, N]). */
+tj_status tj_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, const tj_nvfp4 *wq,
+                           const tj_mxfp8 *w8, const int32_t *normal_idx, const int32_t *outlier_idx,
+                           int64_t k, uint64_t seed, void *dx, int out_dtype, int64_t lddx,
+                           void *workspace, size_t ws_bytes, void *stream);
+
+/* tj_linear_bwd_dw - weight gradient:
+ *   dW[:, NC] = 2^-7 SR(RHT(dY^T)) SR(RHT(X-hat_NC^T))^T  (RHT along M)
+ *   dW[:, O]  = Q8(dY^T) Q8(X-hat_O^T)^T
+ * xq / x8 are the saved forward context of tj_linear_fwd.  dw fp32 [N, K] (lddw).
+ * The workspace then holds S_dY^T (tj_nvfp4 [N, M]), S_X (tj_nvfp4 [K_N, M]) and when
+ * k > 0 Q8(dY^T) (tj_mxfp8 [N, M]) and Q8(X-hat_O^T) (tj_mxfp8 [k, M]), laid out as for dX. */
+tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, const tj_nvfp4 *xq,
+                           const tj_mxfp8 *x8, const int32_t *normal_idx, const int32_t *outlier_idx,
+                           int64_t k, uint64_t seed, float *dw, int64_t lddw, void *workspace,
+                           size_t ws_bytes, void *stream);
+
+#define TJ_OP_BWD_DX 1
+#define TJ_OP_BWD_DW 2
+/* Bytes of workspace the backward call `op` needs for these sizes (K = K_N + k). */
+size_t tj_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t k);
+
+/* ---------------------------------------------------------------------------
+ * tj_outlier_calibrate - OutControl's static outlier selection (§2.C: the top p%
+ * channels by norm, found once in a short calibration window).
+ * If x != NULL: sumsq[c] += sum over the batch of x[t, c]^2, fp64, in a fixed order
+ * (each 128-token chunk summed in token order, then the chunks in order), so the
+ * result is reproducible bit for bit.  x bf16/fp32 [M, K] (ld); M <= 2^20.
+ * If finalize: the k channels with the largest sumsq (ties -> lower index) are
+ * written ascending to outlier_idx [k], the rest ascending to normal_idx [K - k].
+ * sumsq: device fp64 [K], zeroed by the caller before the first batch.
+ * ------------------------------------------------------------------------- */
+tj_status tj_outlier_calibrate(const void *x, int dtype, int64_t M, int64_t K, int64_t ld,
+                               double *sumsq, int finalize, int64_t k, int32_t *outlier_idx,
+                               int32_t *normal_idx, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * tj_osci_reset - OsciReset (§2.B) over master weights w [rows, cols] (fp32,
+ * contiguous), one pass after each optimizer step:
+ *   dist_M += |w - w_prev|;  Q = RTN double-block quantization of w (rows along
+ *   cols, written to q_out: the next forward's weight operand when k == 0);
+ *   dist_Q += |Q-hat - Q-hat_prev| (Q-hat_prev decoded from q_prev);
+ *   reset iff track && lr < lr_thr && dist_M > 0 && dist_Q > risk_thr * dist_M:
+ *     w <- Q-hat (the centre of its bin), dist_Q = dist_M = 0, mask bit set;
+ *   then w_prev <- w.  All in fp32.
+ * reset_mask: uint32 [rows][ceil(cols/32)], bit c&31 of word c>>5 of row r; every
+ * word is written.  q_out may equal q_prev.  Start tracking with w_prev = w,
+ * dist = 0 and q_prev = tj_quantize_nvfp4(w, RTN).
+ * ------------------------------------------------------------------------- */
+tj_status tj_osci_reset(float *w, float *w_prev, float *dist_q, float *dist_m, const tj_nvfp4 *q_prev,
+                        tj_nvfp4 *q_out, uint32_t *reset_mask, int64_t rows, int64_t cols, float lr,
+                        float lr_thr, float risk_thr, int track, void *stream);
+
+/* Reads (synchronously) and clears the sticky device error flag: TJ_OK, or
+ * TJ_ERR_TIMEOUT if a bounded device wait ran out since the last query. */
+tj_status tj_get_device_status(void);
+
+/* Static description of a status code. */
+const char *tj_status_str(tj_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TJ_H */

@@ -1,0 +1,317 @@
+// api.cu - the C ABI of libtj (declared and documented in include/tj.h):
+// argument validation, workspace carving and the composition of the linear
+// layer's forward / backward out of the kernels (TetraJet-v2 technical summary
+// §2.A aligned backward with SR, §2.C RHT and FP8 outlier channels).
+#include <cstring>
+
+#include "tj_common.cuh"
+#include "tj_internal.h"
+
+using namespace tj;
+
+namespace {
+
+inline bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+tj_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TJ_OK : TJ_ERR_CUDA; }
+
+#define TJ_TRY(expr)                          \
+    do {                                      \
+        const cudaError_t e_ = (expr);        \
+        if (e_ != cudaSuccess) return TJ_ERR_CUDA; \
+    } while (0)
+
+tj_status check_nv(const tj_nvfp4 *q, int64_t rows, int64_t cols) {
+    if (q == nullptr || q->codes == nullptr || q->sf == nullptr || q->outer == nullptr) return TJ_ERR_INVALID_ARG;
+    if (q->rows != rows || q->cols != cols || rows < 0 || cols < 0) return TJ_ERR_SHAPE;
+    if (!al16(q->codes) || !al16(q->sf) || !al16(q->outer)) return TJ_ERR_ALIGN;
+    return TJ_OK;
+}
+
+tj_status check_mx(const tj_mxfp8 *q, int64_t rows, int64_t cols) {
+    if (q == nullptr || q->codes == nullptr || q->sf == nullptr) return TJ_ERR_INVALID_ARG;
+    if (q->rows != rows || q->cols != cols || rows < 0 || cols < 0) return TJ_ERR_SHAPE;
+    if (!al16(q->codes) || !al16(q->sf)) return TJ_ERR_ALIGN;
+    return TJ_OK;
+}
+
+int64_t nv_bytes(int64_t rows, int64_t cols) {
+    const int64_t rp = round_up(rows, 128), cp = round_up(cols, 128);
+    return round_up(rp * cp / 2, 256) + round_up(rp * cp / 16, 256) + round_up(rp * (cp / 128) * 4, 256);
+}
+int64_t mx_bytes(int64_t rows, int64_t cols) {
+    const int64_t rp = round_up(rows, 128), cp = round_up(cols, 128);
+    return round_up(rp * cp, 256) + round_up(rp * cp / 32, 256);
+}
+
+// Carve an NVFP4 / MXFP8 tensor out of a workspace cursor.
+tj_nvfp4 carve_nv(uint8_t *&cur, int64_t rows, int64_t cols) {
+    const int64_t rp = round_up(rows, 128), cp = round_up(cols, 128);
+    tj_nvfp4 q;
+    q.codes = cur;
+    cur += round_up(rp * cp / 2, 256);
+    q.sf = cur;
+    cur += round_up(rp * cp / 16, 256);
+    q.outer = reinterpret_cast<float *>(cur);
+    cur += round_up(rp * (cp / 128) * 4, 256);
+    q.rows = rows;
+    q.cols = cols;
+    return q;
+}
+tj_mxfp8 carve_mx(uint8_t *&cur, int64_t rows, int64_t cols) {
+    const int64_t rp = round_up(rows, 128), cp = round_up(cols, 128);
+    tj_mxfp8 q;
+    q.codes = cur;
+    cur += round_up(rp * cp, 256);
+    q.sf = cur;
+    cur += round_up(rp * cp / 32, 256);
+    q.rows = rows;
+    q.cols = cols;
+    return q;
+}
+
+bool dense_ok(const void *x, int dtype, int64_t ld, int64_t cols) {
+    return x != nullptr && (dtype == TJ_BF16 || dtype == TJ_FP32) && ld >= cols;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *tj_status_str(tj_status s) {
+    switch (s) {
+        case TJ_OK: return "ok";
+        case TJ_ERR_INVALID_ARG: return "invalid argument";
+        case TJ_ERR_SHAPE: return "inconsistent or unsupported shape";
+        case TJ_ERR_ALIGN: return "pointer or leading dimension misaligned";
+        case TJ_ERR_UNSUPPORTED: return "unsupported device or feature";
+        case TJ_ERR_CUDA: return "CUDA error";
+        case TJ_ERR_TIMEOUT: return "device-side wait timed out";
+        case TJ_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+tj_status tj_get_device_status(void) {
+    const unsigned int v = read_and_clear_device_error();
+    if (v == 0xFFFFFFFFu) return TJ_ERR_CUDA;
+    return v ? TJ_ERR_TIMEOUT : TJ_OK;
+}
+
+tj_status tj_quantize_nvfp4(const void *x, int dtype, int64_t rows_x, int64_t cols_x, int64_t ld, int along_cols,
+                            const int32_t *sel, int64_t n_sel, int mode, int rht, uint64_t seed, uint32_t tag,
+                            uint32_t rht_tag, tj_nvfp4 *out, void *stream) {
+    if (rows_x < 0 || cols_x < 0 || (mode != TJ_RTN && mode != TJ_SR) || out == nullptr) return TJ_ERR_INVALID_ARG;
+    if (!dense_ok(x, dtype, ld, cols_x)) return TJ_ERR_INVALID_ARG;
+    if (!al16(x) || (ld % 8) != 0) return TJ_ERR_ALIGN;
+    const int64_t ncols = sel ? n_sel : cols_x;
+    if (sel && (n_sel < 0 || n_sel > cols_x)) return TJ_ERR_SHAPE;
+    const int64_t orows = along_cols ? ncols : rows_x, ocols = along_cols ? rows_x : ncols;
+    const tj_status st = check_nv(out, orows, ocols);
+    if (st != TJ_OK) return st;
+    return cuda_status(launch_quant_nv_dense(x, dtype, rows_x, ncols, ld, along_cols, sel, mode, rht, seed, tag,
+                                             rht_tag, *out, static_cast<cudaStream_t>(stream)));
+}
+
+tj_status tj_quantize_mxfp8(const void *x, int dtype, int64_t rows_x, int64_t cols_x, int64_t ld, int along_cols,
+                            const int32_t *sel, int64_t n_sel, tj_mxfp8 *out, void *stream) {
+    if (rows_x < 0 || cols_x < 0 || out == nullptr) return TJ_ERR_INVALID_ARG;
+    if (!dense_ok(x, dtype, ld, cols_x)) return TJ_ERR_INVALID_ARG;
+    if (!al16(x) || (ld % 8) != 0) return TJ_ERR_ALIGN;
+    const int64_t ncols = sel ? n_sel : cols_x;
+    if (sel && (n_sel < 0 || n_sel > cols_x)) return TJ_ERR_SHAPE;
+    const int64_t orows = along_cols ? ncols : rows_x, ocols = along_cols ? rows_x : ncols;
+    const tj_status st = check_mx(out, orows, ocols);
+    if (st != TJ_OK) return st;
+    return cuda_status(launch_quant_mx_dense(x, dtype, rows_x, ncols, ld, along_cols, sel, *out,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+tj_status tj_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, void *stream) {
+    if (x == nullptr || y == nullptr || rows < 0 || cols < 0) return TJ_ERR_INVALID_ARG;
+    if (cols % 128 != 0) return TJ_ERR_SHAPE;
+    if (!al16(x) || !al16(y)) return TJ_ERR_ALIGN;
+    if (rows == 0 || cols == 0) return TJ_OK;
+    return cuda_status(launch_rht(x, y, rows, cols, seed, tag, static_cast<cudaStream_t>(stream)));
+}
+
+tj_status tj_dequantize_nvfp4(const tj_nvfp4 *q, float *y, int64_t ldy, void *stream) {
+    if (q == nullptr || y == nullptr) return TJ_ERR_INVALID_ARG;
+    const tj_status st = check_nv(q, q->rows, q->cols);
+    if (st != TJ_OK) return st;
+    if (ldy < q->cols) return TJ_ERR_SHAPE;
+    return cuda_status(launch_dequant_nv(*q, y, ldy, static_cast<cudaStream_t>(stream)));
+}
+
+tj_status tj_gemm_nvfp4(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8, const tj_mxfp8 *b8, float alpha,
+                        void *d, int out_dtype, int64_t ldd, const int32_t *col_map, void *stream) {
+    if (a == nullptr || b == nullptr || d == nullptr) return TJ_ERR_INVALID_ARG;
+    if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
+    tj_status st = check_nv(a, a->rows, a->cols);
+    if (st == TJ_OK) st = check_nv(b, b->rows, a->cols);
+    if (st != TJ_OK) return st;
+    if ((a8 == nullptr) != (b8 == nullptr)) return TJ_ERR_INVALID_ARG;
+    if (a8 != nullptr) {
+        st = check_mx(a8, a->rows, a8->cols);
+        if (st == TJ_OK) st = check_mx(b8, b->rows, a8->cols);
+        if (st != TJ_OK) return st;
+    }
+    if (ldd < (col_map ? 1 : b->rows) || !al16(d)) return ldd < 1 ? TJ_ERR_SHAPE : TJ_ERR_ALIGN;
+    return cuda_status(launch_gemm(a, b, a8, b8, alpha, d, out_dtype, ldd, a->rows, b->rows, col_map,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+tj_status tj_gemm_mxfp8(const tj_mxfp8 *a8, const tj_mxfp8 *b8, void *d, int out_dtype, int64_t ldd,
+                        const int32_t *col_map, void *stream) {
+    if (a8 == nullptr || b8 == nullptr || d == nullptr) return TJ_ERR_INVALID_ARG;
+    if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
+    tj_status st = check_mx(a8, a8->rows, a8->cols);
+    if (st == TJ_OK) st = check_mx(b8, b8->rows, a8->cols);
+    if (st != TJ_OK) return st;
+    if (!al16(d)) return TJ_ERR_ALIGN;
+    return cuda_status(launch_gemm(nullptr, nullptr, a8, b8, 1.0f, d, out_dtype, ldd, a8->rows, b8->rows, col_map,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+size_t tj_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t k) {
+    if (M < 0 || N < 0 || K < 0 || k < 0 || k > K) return 0;
+    const int64_t kn = K - k;
+    int64_t b = 0;
+    if (op == TJ_OP_BWD_DX) {
+        b = nv_bytes(M, N) + nv_bytes(kn, N);
+        if (k > 0) b += mx_bytes(M, N) + mx_bytes(k, N);
+    } else if (op == TJ_OP_BWD_DW) {
+        b = nv_bytes(N, M) + nv_bytes(kn, M);
+        if (k > 0) b += mx_bytes(N, M) + mx_bytes(k, M);
+    }
+    return (size_t)b;
+}
+
+tj_status tj_linear_fwd(const void *x, int64_t M, int64_t K, int64_t ldx, const tj_nvfp4 *wq, const tj_mxfp8 *w8,
+                        const int32_t *normal_idx, const int32_t *outlier_idx, int64_t k, tj_nvfp4 *xq,
+                        tj_mxfp8 *x8, void *y, int out_dtype, int64_t ldy, void *stream) {
+    if (x == nullptr || wq == nullptr || xq == nullptr || y == nullptr || M < 0 || K < 0 || k < 0 || k > K)
+        return TJ_ERR_INVALID_ARG;
+    if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
+    if (k > 0 && (normal_idx == nullptr || outlier_idx == nullptr || w8 == nullptr || x8 == nullptr))
+        return TJ_ERR_INVALID_ARG;
+    if (!al16(x) || (ldx % 8) != 0 || !al16(y)) return TJ_ERR_ALIGN;
+    if (ldx < K) return TJ_ERR_SHAPE;
+    const int64_t kn = K - k, N = wq->rows;
+    tj_status st = check_nv(wq, N, kn);
+    if (st == TJ_OK) st = check_nv(xq, M, kn);
+    if (st == TJ_OK && k > 0) st = check_mx(w8, N, k);
+    if (st == TJ_OK && k > 0) st = check_mx(x8, M, k);
+    if (st != TJ_OK) return st;
+    if (ldy < N) return TJ_ERR_SHAPE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    TJ_TRY(launch_quant_nv_dense(x, TJ_BF16, M, kn, ldx, 0, k > 0 ? normal_idx : nullptr, TJ_RTN, 0, 0, 0, 0, *xq, s));
+    if (k > 0) TJ_TRY(launch_quant_mx_dense(x, TJ_BF16, M, k, ldx, 0, outlier_idx, *x8, s));
+    TJ_TRY(launch_gemm(xq, wq, k > 0 ? x8 : nullptr, k > 0 ? w8 : nullptr, 1.0f, y, out_dtype, ldy, M, N, nullptr, s));
+    return TJ_OK;
+}
+
+tj_status tj_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, const tj_nvfp4 *wq,
+                           const tj_mxfp8 *w8, const int32_t *normal_idx, const int32_t *outlier_idx, int64_t k,
+                           uint64_t seed, void *dx, int out_dtype, int64_t lddx, void *workspace, size_t ws_bytes,
+                           void *stream) {
+    if (dy == nullptr || wq == nullptr || dx == nullptr || M < 0 || N < 0 || k < 0) return TJ_ERR_INVALID_ARG;
+    if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
+    if (k > 0 && (normal_idx == nullptr || outlier_idx == nullptr || w8 == nullptr)) return TJ_ERR_INVALID_ARG;
+    if (!al16(dy) || (lddy % 8) != 0 || !al16(dx)) return TJ_ERR_ALIGN;
+    const int64_t kn = wq->cols, K = kn + k;
+    tj_status st = check_nv(wq, N, kn);
+    if (st == TJ_OK && k > 0) st = check_mx(w8, N, k);
+    if (st != TJ_OK) return st;
+    if (lddy < N || lddx < K) return TJ_ERR_SHAPE;
+    const size_t need = tj_workspace_size(TJ_OP_BWD_DX, M, N, K, k);
+    if (workspace == nullptr || ws_bytes < need) return TJ_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return TJ_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *cur = static_cast<uint8_t *>(workspace);
+    tj_nvfp4 s_dy = carve_nv(cur, M, N);
+    tj_nvfp4 s_w = carve_nv(cur, kn, N);
+    // dY rows: RHT along N + SR (the dX operand); W-hat^T re-aligned with the same signs
+    TJ_TRY(launch_quant_nv_dense(dy, TJ_BF16, M, N, lddy, 0, nullptr, TJ_SR, 1, seed, TJ_TAG_DY_ROW, TJ_TAG_RHT_DX,
+                                 s_dy, s));
+    TJ_TRY(launch_realign_nv(*wq, s_w, TJ_SR, 1, seed, TJ_TAG_WT, TJ_TAG_RHT_DX, s));
+    TJ_TRY(launch_gemm(&s_dy, &s_w, nullptr, nullptr, 0.0078125f, dx, out_dtype, lddx, M, kn,
+                       k > 0 ? normal_idx : nullptr, s));
+    if (k > 0) {
+        tj_mxfp8 q8_dy = carve_mx(cur, M, N);
+        tj_mxfp8 q8_w = carve_mx(cur, k, N);
+        TJ_TRY(launch_quant_mx_dense(dy, TJ_BF16, M, N, lddy, 0, nullptr, q8_dy, s));
+        TJ_TRY(launch_realign_mx(*w8, q8_w, s));
+        TJ_TRY(launch_gemm(nullptr, nullptr, &q8_dy, &q8_w, 1.0f, dx, out_dtype, lddx, M, k, outlier_idx, s));
+    }
+    return TJ_OK;
+}
+
+tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, const tj_nvfp4 *xq,
+                           const tj_mxfp8 *x8, const int32_t *normal_idx, const int32_t *outlier_idx, int64_t k,
+                           uint64_t seed, float *dw, int64_t lddw, void *workspace, size_t ws_bytes, void *stream) {
+    if (dy == nullptr || xq == nullptr || dw == nullptr || M < 0 || N < 0 || k < 0) return TJ_ERR_INVALID_ARG;
+    if (k > 0 && (normal_idx == nullptr || outlier_idx == nullptr || x8 == nullptr)) return TJ_ERR_INVALID_ARG;
+    if (!al16(dy) || (lddy % 8) != 0 || !al16(dw)) return TJ_ERR_ALIGN;
+    const int64_t kn = xq->cols, K = kn + k;
+    tj_status st = check_nv(xq, M, kn);
+    if (st == TJ_OK && k > 0) st = check_mx(x8, M, k);
+    if (st != TJ_OK) return st;
+    if (lddy < N || lddw < K) return TJ_ERR_SHAPE;
+    const size_t need = tj_workspace_size(TJ_OP_BWD_DW, M, N, K, k);
+    if (workspace == nullptr || ws_bytes < need) return TJ_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return TJ_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *cur = static_cast<uint8_t *>(workspace);
+    tj_nvfp4 s_dy = carve_nv(cur, N, M);
+    tj_nvfp4 s_x = carve_nv(cur, kn, M);
+    // dY^T rows (RHT along M + SR) and X-hat^T re-aligned with the same signs
+    TJ_TRY(launch_quant_nv_dense(dy, TJ_BF16, M, N, lddy, 1, nullptr, TJ_SR, 1, seed, TJ_TAG_DY_COL, TJ_TAG_RHT_DW,
+                                 s_dy, s));
+    TJ_TRY(launch_realign_nv(*xq, s_x, TJ_SR, 1, seed, TJ_TAG_XT, TJ_TAG_RHT_DW, s));
+    TJ_TRY(launch_gemm(&s_dy, &s_x, nullptr, nullptr, 0.0078125f, dw, TJ_FP32, lddw, N, kn,
+                       k > 0 ? normal_idx : nullptr, s));
+    if (k > 0) {
+        tj_mxfp8 q8_dy = carve_mx(cur, N, M);
+        tj_mxfp8 q8_x = carve_mx(cur, k, M);
+        TJ_TRY(launch_quant_mx_dense(dy, TJ_BF16, M, N, lddy, 1, nullptr, q8_dy, s));
+        TJ_TRY(launch_realign_mx(*x8, q8_x, s));
+        TJ_TRY(launch_gemm(nullptr, nullptr, &q8_dy, &q8_x, 1.0f, dw, TJ_FP32, lddw, N, k, outlier_idx, s));
+    }
+    return TJ_OK;
+}
+
+tj_status tj_outlier_calibrate(const void *x, int dtype, int64_t M, int64_t K, int64_t ld, double *sumsq,
+                               int finalize, int64_t k, int32_t *outlier_idx, int32_t *normal_idx, void *stream) {
+    if (sumsq == nullptr || M < 0 || K <= 0 || K > (int64_t)1 << 24) return TJ_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (x != nullptr) {
+        if (dtype != TJ_BF16 && dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
+        if (ld < K || M > ((int64_t)1 << 20)) return TJ_ERR_SHAPE;
+        if (!al16(x)) return TJ_ERR_ALIGN;
+        TJ_TRY(launch_calib_accumulate(x, dtype, M, K, ld, sumsq, s));
+    }
+    if (finalize) {
+        if (k < 0 || k > K) return TJ_ERR_SHAPE;
+        if ((k > 0 && outlier_idx == nullptr) || (k < K && normal_idx == nullptr)) return TJ_ERR_INVALID_ARG;
+        TJ_TRY(launch_calib_select(sumsq, K, k, outlier_idx, normal_idx, s));
+    }
+    return TJ_OK;
+}
+
+tj_status tj_osci_reset(float *w, float *w_prev, float *dist_q, float *dist_m, const tj_nvfp4 *q_prev,
+                        tj_nvfp4 *q_out, uint32_t *reset_mask, int64_t rows, int64_t cols, float lr, float lr_thr,
+                        float risk_thr, int track, void *stream) {
+    if (w == nullptr || w_prev == nullptr || dist_q == nullptr || dist_m == nullptr || reset_mask == nullptr ||
+        rows < 0 || cols < 0)
+        return TJ_ERR_INVALID_ARG;
+    tj_status st = check_nv(q_prev, rows, cols);
+    if (st == TJ_OK) st = check_nv(q_out, rows, cols);
+    if (st != TJ_OK) return st;
+    if (!al16(w) || !al16(w_prev) || !al16(dist_q) || !al16(dist_m) || !al16(reset_mask)) return TJ_ERR_ALIGN;
+    if (rows == 0 || cols == 0) return TJ_OK;
+    return cuda_status(launch_osci_reset(w, w_prev, dist_q, dist_m, *q_prev, *q_out, reset_mask, rows, cols, lr,
+                                         lr_thr, risk_thr, track, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

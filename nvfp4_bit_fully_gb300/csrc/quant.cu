@@ -1,0 +1,342 @@
+// quant.cu - quantize kernels (sm_103a): row-wise and transposed-alignment
+// double-block NVFP4 (RTN / SR, optional RHT), the MXFP8 outlier slice, the
+// standalone RHT and fp32 dequantization.  TetraJet-v2 technical summary §2.A
+// (double-block quantization, SR, 1x16 groups re-aligned for the transposed
+// operand) and §2.C (RHT, FP8 outlier channels).
+//
+// HBM-bound kernels: every input byte is read once with coalesced loads, every
+// output written once; no intermediate fp32/bf16 tensor is materialised.
+#include "quant_core.cuh"
+#include "tj_internal.h"
+
+namespace tj {
+
+// ---------------------------------------------------------------------------
+// Sources.  elem(r, c) is the fp32 value at input row r and (selected) column c;
+// rows beyond `rows` or columns beyond the selection read as 0 (zero padding).
+// ---------------------------------------------------------------------------
+template <typename T>
+struct SrcDense {
+    const T *p;
+    int64_t ld, rows, cols;   // cols = number of (selected) columns
+    const int32_t *sel;       // nullptr: identity
+    __device__ __forceinline__ float load(int64_t r, int64_t c) const {
+        if (r >= rows || c >= cols) return 0.0f;
+        const int64_t ci = sel ? (int64_t)sel[c] : c;
+        return to_f(p[r * ld + ci]);
+    }
+    __device__ static __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+    __device__ static __forceinline__ float to_f(float v) { return v; }
+};
+
+// NVFP4 tensor [rows, cols] read back as its fp32 dequantization (G * s_i) * s_o.
+struct SrcNv {
+    const uint8_t *codes, *sf;
+    const float *outer;
+    int64_t rows, cols, rows_p, cols_p;
+    __device__ __forceinline__ float load(int64_t r, int64_t c) const {
+        if (r >= rows || c >= cols) return 0.0f;
+        const uint32_t byte = codes[r * (cols_p / 2) + (c >> 1)];
+        const uint32_t code = (c & 1) ? (byte >> 4) : (byte & 15u);
+        const int64_t g = c >> 4;
+        const uint32_t sb = sf[sf_word_offset(r, g >> 2, cols_p / 64) + (g & 3)];
+        const uint32_t mag = code & 7u;
+        const float gv = mag < 4u ? __fmul_rn((float)mag, 0.5f)
+                                  : (mag == 4u ? 2.0f : (mag == 5u ? 3.0f : (mag == 6u ? 4.0f : 6.0f)));
+        const float v = __fmul_rn(__fmul_rn(gv, e4m3_to_float(sb)), outer[(c >> 7) * rows_p + r]);
+        return (code & 8u) ? -v : v;
+    }
+};
+
+// MXFP8 slice [rows, cols] read back as fp32 (E4M3 value times 2^(byte-127)).
+struct SrcMx {
+    const uint8_t *codes, *sf;
+    int64_t rows, cols, rows_p, cols_p;
+    __device__ __forceinline__ float load(int64_t r, int64_t c) const {
+        if (r >= rows || c >= cols) return 0.0f;
+        const float v = e4m3_to_float(codes[r * cols_p + c]);
+        const int64_t g = c >> 5;
+        const int e = (int)sf[sf_word_offset(r, g >> 2, cols_p / 128) + (g & 3)] - 127;
+        const float s = e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x400000u);
+        return __fmul_rn(v, s);
+    }
+};
+
+// Fast path of the row kernel: 32 consecutive bf16 of one row, 64-byte aligned.
+__device__ __forceinline__ void load32_bf16_vec(const __nv_bfloat16 *p, float (&x)[32]) {
+    const uint4 *q = reinterpret_cast<const uint4 *>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint4 v = __ldg(q + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x[8 * i + 2 * k] = bf16_bits_to_float(w[k] & 0xFFFFu);
+            x[8 * i + 2 * k + 1] = bf16_bits_to_float(w[k] >> 16);
+        }
+    }
+}
+
+template <typename Src>
+__device__ __forceinline__ void load_row32(const Src &src, int64_t r, int64_t c0, float (&x)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = src.load(r, c0 + j);
+}
+
+__device__ __forceinline__ void load_row32(const SrcDense<__nv_bfloat16> &src, int64_t r, int64_t c0,
+                                           float (&x)[32]) {
+    if (src.sel == nullptr && r < src.rows && c0 + 32 <= src.cols && (src.ld & 31) == 0 &&
+        ((reinterpret_cast<uintptr_t>(src.p) & 63) == 0)) {
+        load32_bf16_vec(src.p + r * src.ld + c0, x);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = src.load(r, c0 + j);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Row-wise kernel: output row r = input row r, quantized along the columns.
+// One quad per (row, 128-block); a warp covers 8 consecutive segments.
+// FMT 0 = NVFP4, 1 = MXFP8.
+// ---------------------------------------------------------------------------
+template <typename Src, int FMT, bool SR, bool RHT>
+__global__ void __launch_bounds__(256) k_quant_rows(Src src, OutNv onv, OutMx omx, int64_t nseg, uint64_t seed,
+                                                    uint32_t tag, uint32_t rht_tag) {
+    const int lane = threadIdx.x & 31;
+    const int t = lane & 3;
+    const int64_t rows_p = FMT == 0 ? onv.rows_p : omx.rows_p;
+    const int64_t cols_p = FMT == 0 ? onv.cols_p : omx.cols_p;
+    const int64_t total = rows_p * nseg;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    uint32_t sign_word = 0u;
+    if (RHT) {
+        const uint4 sb = rht_sign_bits(seed, rht_tag);
+        sign_word = t == 0 ? sb.x : (t == 1 ? sb.y : (t == 2 ? sb.z : sb.w));
+    }
+    for (int64_t base = warp0 * 8; base < total; base += nwarps * 8) {   // warp-uniform loop
+        const int64_t seg = base + (lane >> 2);
+        const bool valid = seg < total;
+        const int64_t row = valid ? seg / nseg : 0;
+        const int64_t kb = valid ? seg % nseg : 0;
+        float x[32];
+        if (valid) load_row32(src, row, kb * 128 + 32 * t, x);
+        else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = 0.0f;
+        }
+        if (FMT == 0) {
+            if (RHT) rht128_quad(x, sign_word, t);
+            const NvSeg s = quant_nvfp4_seg<SR>(x, (uint64_t)(row * cols_p + kb * 128 + 32 * t), seed, tag);
+            store_nv_seg(onv, row, kb, t, s, valid);
+        } else {
+            const MxSeg s = quant_mxfp8_group(x);
+            store_mx_seg(omx, row, kb, t, s, valid);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Transposed-alignment kernel: output row c = input column c, quantized along
+// the input rows.  A CTA stages a 128 (input rows = one output block) x 64
+// (output rows) fp32 tile in shared memory, then each quad quantizes one output
+// row's 128-segment.  The tile is XOR-swizzled so that both the row-major fill
+// and the column reads (lanes = 8 columns x 4 quad lanes) are conflict-free:
+// element (r, c) sits at r*64 + (c ^ (((r >> 5) & 3) << 3)).
+// ---------------------------------------------------------------------------
+template <typename Src, int FMT, bool SR, bool RHT>
+__global__ void __launch_bounds__(256) k_quant_cols(Src src, OutNv onv, OutMx omx, uint64_t seed, uint32_t tag,
+                                                    uint32_t rht_tag) {
+    __shared__ float tile[128 * 64];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t c0 = (int64_t)blockIdx.x * 64;      // first output row of the tile
+    const int64_t kb = blockIdx.y;                    // 128-block along the input rows
+    const int64_t r0 = kb * 128;
+    // fill: warp w loads rows w, w+8, ...; lane l loads columns l and l+32
+    for (int rr = warp; rr < 128; rr += 8) {
+        const int sw = ((rr >> 5) & 3) << 3;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int cc = lane + 32 * h;
+            tile[rr * 64 + (cc ^ sw)] = src.load(r0 + rr, c0 + cc);
+        }
+    }
+    __syncthreads();
+    const int t = lane & 3;
+    const int cl = warp * 8 + (lane >> 2);            // output row within the tile
+    float x[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = tile[(32 * t + j) * 64 + (cl ^ (t << 3))];
+    const int64_t row = c0 + cl;
+    const int64_t rows_p = FMT == 0 ? onv.rows_p : omx.rows_p;
+    const int64_t cols_p = FMT == 0 ? onv.cols_p : omx.cols_p;
+    const bool valid = row < rows_p;
+    if (FMT == 0) {
+        if (RHT) {
+            const uint4 sb = rht_sign_bits(seed, rht_tag);
+            rht128_quad(x, t == 0 ? sb.x : (t == 1 ? sb.y : (t == 2 ? sb.z : sb.w)), t);
+        }
+        const NvSeg s = quant_nvfp4_seg<SR>(x, (uint64_t)(row * cols_p + r0 + 32 * t), seed, tag);
+        store_nv_seg(onv, row, kb, t, s, valid);
+    } else {
+        const MxSeg s = quant_mxfp8_group(x);
+        store_mx_seg(omx, row, kb, t, s, valid);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Standalone RHT (fp32 -> fp32), one quad per 128-block, same butterfly as the
+// fused quantizers.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t seed,
+                                             uint32_t tag) {
+    const int lane = threadIdx.x & 31, t = lane & 3;
+    const int64_t nseg = cols / 128, total = rows * nseg;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const uint4 sb = rht_sign_bits(seed, tag);
+    const uint32_t sign_word = t == 0 ? sb.x : (t == 1 ? sb.y : (t == 2 ? sb.z : sb.w));
+    for (int64_t base = warp0 * 8; base < total; base += nwarps * 8) {
+        const int64_t seg = base + (lane >> 2);
+        const bool valid = seg < total;
+        const int64_t off = valid ? (seg / nseg) * cols + (seg % nseg) * 128 + 32 * t : 0;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 f = valid ? reinterpret_cast<const float4 *>(x + off)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+        }
+        rht128_quad(v, sign_word, t);
+        if (valid) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                reinterpret_cast<float4 *>(y + off)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+    }
+}
+
+// fp32 dequantization of an NVFP4 tensor, one thread per element.
+__global__ void k_dequant_nv(SrcNv src, float *y, int64_t ldy) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= src.rows * src.cols) return;
+    const int64_t r = i / src.cols, c = i % src.cols;
+    y[r * ldy + c] = src.load(r, c);
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kThreads = 256;
+
+int64_t row_grid(int64_t total_segments) {
+    const int64_t ctas = (total_segments + 63) / 64;          // 64 segments per CTA pass
+    return ctas < 152 * 32 ? (ctas > 0 ? ctas : 1) : 152 * 32;
+}
+
+OutNv out_nv(const tj_nvfp4 &q) {
+    return OutNv{q.codes, q.sf, q.outer, round_up(q.rows, 128), round_up(q.cols, 128)};
+}
+OutMx out_mx(const tj_mxfp8 &q) { return OutMx{q.codes, q.sf, round_up(q.rows, 128), round_up(q.cols, 128)}; }
+
+template <typename Src>
+cudaError_t rows_nv(const Src &src, const OutNv &o, int mode, int rht, uint64_t seed, uint32_t tag,
+                    uint32_t rht_tag, cudaStream_t s) {
+    const int64_t nseg = o.cols_p / 128, grid = row_grid(o.rows_p * nseg);
+    const OutMx none{};
+    if (mode == TJ_SR && rht)  k_quant_rows<Src, 0, true, true><<<grid, kThreads, 0, s>>>(src, o, none, nseg, seed, tag, rht_tag);
+    else if (mode == TJ_SR)    k_quant_rows<Src, 0, true, false><<<grid, kThreads, 0, s>>>(src, o, none, nseg, seed, tag, rht_tag);
+    else if (rht)              k_quant_rows<Src, 0, false, true><<<grid, kThreads, 0, s>>>(src, o, none, nseg, seed, tag, rht_tag);
+    else                       k_quant_rows<Src, 0, false, false><<<grid, kThreads, 0, s>>>(src, o, none, nseg, seed, tag, rht_tag);
+    return cudaGetLastError();
+}
+
+template <typename Src>
+cudaError_t cols_nv(const Src &src, const OutNv &o, int mode, int rht, uint64_t seed, uint32_t tag,
+                    uint32_t rht_tag, cudaStream_t s) {
+    const dim3 grid((unsigned)(o.rows_p / 64), (unsigned)(o.cols_p / 128));
+    const OutMx none{};
+    if (mode == TJ_SR && rht)  k_quant_cols<Src, 0, true, true><<<grid, kThreads, 0, s>>>(src, o, none, seed, tag, rht_tag);
+    else if (mode == TJ_SR)    k_quant_cols<Src, 0, true, false><<<grid, kThreads, 0, s>>>(src, o, none, seed, tag, rht_tag);
+    else if (rht)              k_quant_cols<Src, 0, false, true><<<grid, kThreads, 0, s>>>(src, o, none, seed, tag, rht_tag);
+    else                       k_quant_cols<Src, 0, false, false><<<grid, kThreads, 0, s>>>(src, o, none, seed, tag, rht_tag);
+    return cudaGetLastError();
+}
+
+template <typename Src>
+cudaError_t rows_mx(const Src &src, const OutMx &o, cudaStream_t s) {
+    const int64_t nseg = o.cols_p / 128, grid = row_grid(o.rows_p * nseg);
+    k_quant_rows<Src, 1, false, false><<<grid, kThreads, 0, s>>>(src, OutNv{}, o, nseg, 0, 0, 0);
+    return cudaGetLastError();
+}
+
+template <typename Src>
+cudaError_t cols_mx(const Src &src, const OutMx &o, cudaStream_t s) {
+    const dim3 grid((unsigned)(o.rows_p / 64), (unsigned)(o.cols_p / 128));
+    k_quant_cols<Src, 1, false, false><<<grid, kThreads, 0, s>>>(src, OutNv{}, o, 0, 0, 0);
+    return cudaGetLastError();
+}
+}  // namespace
+
+SrcNv src_nv(const tj_nvfp4 &q) {
+    return SrcNv{q.codes, q.sf, q.outer, q.rows, q.cols, round_up(q.rows, 128), round_up(q.cols, 128)};
+}
+SrcMx src_mx(const tj_mxfp8 &q) {
+    return SrcMx{q.codes, q.sf, q.rows, q.cols, round_up(q.rows, 128), round_up(q.cols, 128)};
+}
+
+// Dense input (bf16 / fp32) -> NVFP4, either orientation.  n_cols_sel = number of
+// selected input columns (cols_x when sel == nullptr).
+cudaError_t launch_quant_nv_dense(const void *x, int dtype, int64_t rows_x, int64_t n_cols_sel, int64_t ld,
+                                  int along_cols, const int32_t *sel, int mode, int rht, uint64_t seed,
+                                  uint32_t tag, uint32_t rht_tag, const tj_nvfp4 &out, cudaStream_t s) {
+    const OutNv o = out_nv(out);
+    if (dtype == TJ_BF16) {
+        const SrcDense<__nv_bfloat16> src{static_cast<const __nv_bfloat16 *>(x), ld, rows_x, n_cols_sel, sel};
+        return along_cols ? cols_nv(src, o, mode, rht, seed, tag, rht_tag, s)
+                          : rows_nv(src, o, mode, rht, seed, tag, rht_tag, s);
+    }
+    const SrcDense<float> src{static_cast<const float *>(x), ld, rows_x, n_cols_sel, sel};
+    return along_cols ? cols_nv(src, o, mode, rht, seed, tag, rht_tag, s)
+                      : rows_nv(src, o, mode, rht, seed, tag, rht_tag, s);
+}
+
+cudaError_t launch_quant_mx_dense(const void *x, int dtype, int64_t rows_x, int64_t n_cols_sel, int64_t ld,
+                                  int along_cols, const int32_t *sel, const tj_mxfp8 &out, cudaStream_t s) {
+    const OutMx o = out_mx(out);
+    if (dtype == TJ_BF16) {
+        const SrcDense<__nv_bfloat16> src{static_cast<const __nv_bfloat16 *>(x), ld, rows_x, n_cols_sel, sel};
+        return along_cols ? cols_mx(src, o, s) : rows_mx(src, o, s);
+    }
+    const SrcDense<float> src{static_cast<const float *>(x), ld, rows_x, n_cols_sel, sel};
+    return along_cols ? cols_mx(src, o, s) : rows_mx(src, o, s);
+}
+
+// Re-alignment of a forward NVFP4 operand for the backward (§2.A "estimate
+// X-hat instead of X", 1x16 groups of the transposed weight): dequantize, read
+// transposed, optional RHT along the new contraction axis, SR re-quantize.
+cudaError_t launch_realign_nv(const tj_nvfp4 &in, const tj_nvfp4 &out, int mode, int rht, uint64_t seed,
+                              uint32_t tag, uint32_t rht_tag, cudaStream_t s) {
+    return cols_nv(src_nv(in), out_nv(out), mode, rht, seed, tag, rht_tag, s);
+}
+
+// The FP8 outlier slice of a forward operand, transposed and re-quantized (RTN).
+cudaError_t launch_realign_mx(const tj_mxfp8 &in, const tj_mxfp8 &out, cudaStream_t s) {
+    return cols_mx(src_mx(in), out_mx(out), s);
+}
+
+cudaError_t launch_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,
+                       cudaStream_t s) {
+    const int64_t grid = row_grid(rows * (cols / 128));
+    k_rht<<<grid, kThreads, 0, s>>>(x, y, rows, cols, seed, tag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_nv(const tj_nvfp4 &q, float *y, int64_t ldy, cudaStream_t s) {
+    const int64_t n = q.rows * q.cols;
+    if (n == 0) return cudaSuccess;
+    k_dequant_nv<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(src_nv(q), y, ldy);
+    return cudaGetLastError();
+}
+
+}  // namespace tj

@@ -1,0 +1,203 @@
+// quant_core.cuh - the per-segment quantizers used by every quantize kernel.
+//
+// Work split: one 128-element segment of the quantized axis (one outer block of
+// TetraJet-v2 §2.A) is held by a quad of 4 adjacent lanes, 32 consecutive elements
+// per lane (lane t of the quad holds elements 32t .. 32t+31).  So each lane owns
+// two whole 16-element inner groups, one whole 32-element FP8 group, four whole
+// Philox calls (8 elements each), and the 128-point Hadamard butterfly needs only
+// two cross-lane stages.
+#pragma once
+#include "tj_common.cuh"
+
+namespace tj {
+
+// 128-point unnormalised Walsh-Hadamard transform of a quad's segment, after
+// multiplying by the random +-1 diagonal (bit j of `sign_word` set -> negate
+// element j of this lane).  Stages h = 1, 2, 4, 8, 16 run inside the lane, h = 32
+// and h = 64 pair lanes t^1 and t^2; every stage maps (a, b) -> (a + b, a - b) in
+// fp32, in the fixed order h = 1, 2, ..., 64 (TetraJet-v2 §2.C RHT).
+__device__ __forceinline__ void rht128_quad(float (&x)[32], uint32_t sign_word, int t) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        if ((sign_word >> j) & 1u) x[j] = -x[j];
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if ((j & h) == 0) {
+                const float a = x[j], b = x[j + h];
+                x[j] = __fadd_rn(a, b);
+                x[j + h] = __fsub_rn(a, b);
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float p = __shfl_xor_sync(0xffffffffu, x[j], m);
+            x[j] = (t & m) ? __fsub_rn(p, x[j]) : __fadd_rn(x[j], p);
+        }
+    }
+}
+
+struct NvSeg {
+    uint4 codes;    // 32 E2M1 codes, element 2j in the low nibble of byte j
+    uint32_t sf2;   // inner scale bytes of this lane's groups (low byte = first group)
+    float s_o;      // the segment's FP32 outer scale (same in all 4 lanes)
+};
+
+// Double-block NVFP4 quantization of one 128-segment (§2.A), readings as in tj.h:
+// s_o = amax/2688 (2^-149 if that underflows), s_i = E4M3 ceiling of
+// amax_16 / (6 s_o), element index = RTN(min(|x * (1/(s_i s_o))|, 6)) or SR with
+// the 16-bit uniforms of Philox call (elem0 + 8q) >> 3.  elem0 = index of x[0] in
+// the operand's quantized layout (row * cols_p + col), a multiple of 8.
+template <bool SR>
+__device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t elem0, uint64_t seed,
+                                                 uint32_t tag) {
+    float a_i[2];
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(x[16 * g + j]));
+        a_i[g] = m;
+    }
+    float a_o = fmaxf(a_i[0], a_i[1]);
+    a_o = fmaxf(a_o, __shfl_xor_sync(0xffffffffu, a_o, 1));
+    a_o = fmaxf(a_o, __shfl_xor_sync(0xffffffffu, a_o, 2));
+
+    float s_o = __fdiv_rn(a_o, 2688.0f);
+    if (a_o > 0.0f && s_o == 0.0f) s_o = __uint_as_float(1u);     // 2^-149
+    const float m6 = __fmul_rn(s_o, 6.0f);
+
+    NvSeg out;
+    out.s_o = s_o;
+    out.sf2 = 0u;
+    uint32_t words[4] = {0u, 0u, 0u, 0u};
+    uint4 rnd[4];
+    if (SR) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) rnd[q] = sr_bits8((elem0 >> 3) + (uint64_t)q, seed, tag);
+    }
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        uint32_t sb = 0u;
+        if (a_i[g] > 0.0f) sb = e4m3_ceil_byte(__fdiv_rn(a_i[g], m6));
+        out.sf2 |= sb << (8 * g);
+        const float s = __fmul_rn(e4m3_to_float(sb), s_o);
+        const float r = s > 0.0f ? __fdiv_rn(1.0f, s) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int e = 16 * g + j;
+            const float xv = x[e];
+            const float a = fminf(fabsf(__fmul_rn(xv, r)), 6.0f);
+            uint32_t idx;
+            if (SR) {
+                const uint4 w4 = rnd[e >> 3];
+                const int wi = (e & 7) >> 1;
+                const uint32_t w = wi == 0 ? w4.x : (wi == 1 ? w4.y : (wi == 2 ? w4.z : w4.w));
+                idx = e2m1_sr(a, (w >> (16 * (e & 1))) & 0xFFFFu);
+            } else {
+                idx = e2m1_rtn(a);
+            }
+            uint32_t code = (xv < 0.0f) ? (idx | 8u) : idx;
+            if (xv == 0.0f || !(s > 0.0f)) code = 0u;
+            words[e >> 3] |= code << (4 * (e & 7));
+        }
+    }
+    out.codes = make_uint4(words[0], words[1], words[2], words[3]);
+    return out;
+}
+
+struct MxSeg {
+    uint4 codes[2];  // 32 E4M3 bytes
+    uint32_t e8;     // UE8M0 scale byte
+};
+
+// MXFP8 quantization of one 32-element group (this lane's elements), §2.C FP8
+// slice: E = smallest integer with 448 * 2^E >= amax (clamped to [-127, 127],
+// 0 for an all-zero group), values x * 2^-E rounded to nearest-even E4M3 with
+// saturation at +-448.
+__device__ __forceinline__ MxSeg quant_mxfp8_group(const float (&x)[32]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(x[j]));
+    int E = 0;
+    if (amax > 0.0f) {
+        uint32_t b = __float_as_uint(amax);
+        int ex = (int)(b >> 23) - 127;
+        if (ex == -127) {                               // fp32 subnormal: renormalise
+            b = __float_as_uint(__fmul_rn(amax, 4294967296.0f));
+            ex = (int)(b >> 23) - 127 - 32;
+        }
+        const uint32_t man = b & 0x7FFFFFu;             // amax = 1.man * 2^ex; 448 = 1.75 * 2^8
+        E = (man <= 0x600000u) ? ex - 8 : ex - 7;
+        E = E < -127 ? -127 : (E > 127 ? 127 : E);
+    }
+    const int e2 = -E;                                  // 2^-E as an exact float
+    const float inv = e2 >= -126 ? __uint_as_float((uint32_t)(e2 + 127) << 23) : __uint_as_float(0x400000u);
+    MxSeg out;
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t word = 0u;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float2 f = make_float2(__fmul_rn(x[4 * i + 2 * h], inv), __fmul_rn(x[4 * i + 2 * h + 1], inv));
+            const __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+            word |= (uint32_t)p << (16 * h);
+        }
+        w[i] = word;
+    }
+    out.codes[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    out.codes[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    out.e8 = (uint32_t)(E + 127);
+    return out;
+}
+
+// Output descriptors (device pointers and padded sizes).
+struct OutNv {
+    uint8_t *codes;
+    uint8_t *sf;
+    float *outer;
+    int64_t rows_p, cols_p;
+};
+struct OutMx {
+    uint8_t *codes;
+    uint8_t *sf;
+    int64_t rows_p, cols_p;
+};
+
+// Store one quad's NVFP4 segment (row, block kb).  Lane t writes its 16 code
+// bytes; lanes 0 and 2 write the two 4-byte scale words (groups 8kb..8kb+3 and
+// 8kb+4..8kb+7); lane 0 writes the outer scale.  All 4 lanes must call.
+__device__ __forceinline__ void store_nv_seg(const OutNv &o, int64_t row, int64_t kb, int t, const NvSeg &s,
+                                             bool valid) {
+    const uint32_t other = __shfl_xor_sync(0xffffffffu, s.sf2, 1);
+    if (!valid) return;
+    *reinterpret_cast<uint4 *>(o.codes + row * (o.cols_p / 2) + kb * 64 + 16 * t) = s.codes;
+    if ((t & 1) == 0) {
+        const uint32_t word = (s.sf2 & 0xFFFFu) | (other << 16);
+        *reinterpret_cast<uint32_t *>(o.sf + sf_word_offset(row, 2 * kb + (t >> 1), o.cols_p / 64)) = word;
+    }
+    if (t == 0) o.outer[kb * o.rows_p + row] = s.s_o;
+}
+
+// Store one quad's MXFP8 segment (row, 128-block kb): lane t owns group 4kb+t.
+__device__ __forceinline__ void store_mx_seg(const OutMx &o, int64_t row, int64_t kb, int t, const MxSeg &s,
+                                             bool valid) {
+    const uint32_t b1 = __shfl_xor_sync(0xffffffffu, s.e8, 1);
+    const uint32_t b2 = __shfl_xor_sync(0xffffffffu, s.e8, 2);
+    const uint32_t b3 = __shfl_xor_sync(0xffffffffu, s.e8, 3);
+    if (!valid) return;
+    uint4 *dst = reinterpret_cast<uint4 *>(o.codes + row * o.cols_p + kb * 128 + 32 * t);
+    dst[0] = s.codes[0];
+    dst[1] = s.codes[1];
+    if (t == 0) {
+        const uint32_t word = s.e8 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        *reinterpret_cast<uint32_t *>(o.sf + sf_word_offset(row, kb, o.cols_p / 128)) = word;
+    }
+}
+
+}  // namespace tj

@@ -1,0 +1,128 @@
+// tj_common.cuh - device helpers shared by the sm_103a kernels of libtj.
+//
+// Number formats and rounding follow the TetraJet-v2 technical summary §2.A
+// (NVFP4: E2M1 values, 16-element groups with an 8-bit E4M3 scale, a 128-element
+// outer block with an FP32 scale; RTN forward, stochastic rounding backward) and
+// §2.C (128-point random Hadamard transform in the backward; FP8 outlier slice).
+// Every arithmetic step that decides a code is an explicit IEEE fp32 operation
+// (__fmul_rn / __fdiv_rn / __fadd_rn) so that no FMA contraction or reordering
+// can change a rounding.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "tj.h"
+
+namespace tj {
+
+constexpr int kOuter = 128;  // outer block (FP32 scale)
+constexpr int kInner = 16;   // inner group (E4M3 scale)
+constexpr int kMx = 32;      // FP8 slice group (UE8M0 scale)
+
+__host__ __device__ inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of two 32x32->64
+// multiplications with the constants 0xD2511F53 / 0xCD9E8D57, the high halves
+// xored with the other counter words and the round key, the key advanced by the
+// Weyl increments 0x9E3779B9 / 0xBB67AE85 after every round.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// Random bits for stochastic rounding: element e (row * cols_p + col of the
+// quantized operand) takes 16 bits of Philox(counter = (e>>3, tag, 0), key = seed);
+// elements 8g .. 8g+7 share call g: word (e&7)>>1, low half for even e.
+__device__ __forceinline__ uint4 sr_bits8(uint64_t g, uint64_t seed, uint32_t tag) {
+    return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), tag, 0u), (uint32_t)seed,
+                         (uint32_t)(seed >> 32));
+}
+
+// The +-1 diagonal of the RHT as 128 sign bits (bit i set -> d[i] = -1):
+// one Philox call with counter (0, 0, tag, 0) and key = seed.
+__device__ __forceinline__ uint4 rht_sign_bits(uint64_t seed, uint32_t tag) {
+    return philox4x32_10(make_uint4(0u, 0u, tag, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+// ---------------------------------------------------------------------------
+// E4M3 (bias 7, max 448, subnormal step 2^-9) helpers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float e4m3_to_float(uint32_t b) {
+    const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+    float v = (e == 0) ? __fmul_rn((float)m, 0.001953125f)                   // m * 2^-9
+                       : __uint_as_float(((e + 120u) << 23) | (m << 20));    // (1+m/8) 2^(e-7)
+    return (b & 0x80u) ? -v : v;
+}
+
+// Smallest E4M3 value >= t (t >= 0), clamped to 448; returns its byte.
+// Inner-scale reading: rounding the group scale UP keeps |x / s| <= 6, so no
+// element is clipped and stochastic rounding stays unbiased.
+__device__ __forceinline__ uint32_t e4m3_ceil_byte(float t) {
+    if (!(t > 0.0f)) return 0u;
+    if (t >= 448.0f) return 0x7Eu;
+    const uint32_t bits = __float_as_uint(t);
+    const int ex = (int)((bits >> 23) & 0xFFu) - 127;
+    if (ex < -6) {                                   // below the smallest normal 2^-6
+        const float s = __fmul_rn(t, 512.0f);        // t / 2^-9, exact
+        const uint32_t k = (uint32_t)ceilf(s);       // 1 .. 8
+        return k >= 8u ? 0x08u : (k == 0u ? 1u : k);
+    }
+    uint32_t m3 = (bits >> 20) & 7u;
+    uint32_t eb = (uint32_t)(ex + 7);
+    if (bits & 0xFFFFFu) {                           // not exactly representable: round up
+        if (++m3 == 8u) { m3 = 0u; ++eb; }
+    }
+    const uint32_t byte = (eb << 3) | m3;
+    return byte > 0x7Eu ? 0x7Eu : byte;
+}
+
+// ---------------------------------------------------------------------------
+// E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6}: rounding of a magnitude a in [0, 6].
+// ---------------------------------------------------------------------------
+// Nearest grid point, ties to the even code (the midpoints .25, .75, 1.25, 1.75,
+// 2.5, 3.5, 5 go to codes 0, 2, 2, 4, 4, 6, 6).
+__device__ __forceinline__ uint32_t e2m1_rtn(float a) {
+    return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+           (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
+           (uint32_t)(a > 5.0f);
+}
+
+// Stochastic rounding between the grid neighbours lo <= a <= hi: up with
+// probability p = (a - lo) / (hi - lo), decided as float(u16) < p * 65536.
+// a - lo is exact (Sterbenz) and 1/(hi - lo) a power of two, so p is exact.
+__device__ __forceinline__ uint32_t e2m1_sr(float a, uint32_t u16) {
+    const uint32_t lo = (uint32_t)(a >= 0.5f) + (uint32_t)(a >= 1.0f) + (uint32_t)(a >= 1.5f) +
+                        (uint32_t)(a >= 2.0f) + (uint32_t)(a >= 3.0f) + (uint32_t)(a >= 4.0f) +
+                        (uint32_t)(a >= 6.0f);
+    // grid value and reciprocal gap of index lo
+    const float g = lo < 4u ? __fmul_rn((float)lo, 0.5f) : (lo == 4u ? 2.0f : (lo == 5u ? 3.0f : (lo == 6u ? 4.0f : 6.0f)));
+    if (lo == 7u || a == g) return lo;
+    const float inv_gap = lo < 4u ? 2.0f : (lo < 6u ? 1.0f : 0.5f);
+    const float p = __fmul_rn(__fsub_rn(a, g), inv_gap);
+    return lo + ((float)u16 < __fmul_rn(p, 65536.0f) ? 1u : 0u);
+}
+
+// ---------------------------------------------------------------------------
+// Scale tile layout of the block-scaled MMA (see tj.h): byte offset of the scale
+// of (row, group) for a tensor with `ntile_k` = cols_p / (4 * group) tiles per row
+// tile.  Groups 4kt..4kt+3 of one row are 4 consecutive bytes.
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ int64_t sf_word_offset(int64_t row, int64_t kt, int64_t ntile_k) {
+    const int64_t rt = row >> 7, rr = row & 127;
+    return (rt * ntile_k + kt) * 512 + 16 * (rr & 31) + 4 * (rr >> 5);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
+
+}  // namespace tj

@@ -1,0 +1,39 @@
+// tj_internal.h - launchers shared between the kernel files and the C ABI layer.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "tj.h"
+
+namespace tj {
+
+cudaError_t launch_quant_nv_dense(const void *x, int dtype, int64_t rows_x, int64_t n_cols_sel, int64_t ld,
+                                  int along_cols, const int32_t *sel, int mode, int rht, uint64_t seed,
+                                  uint32_t tag, uint32_t rht_tag, const tj_nvfp4 &out, cudaStream_t s);
+cudaError_t launch_quant_mx_dense(const void *x, int dtype, int64_t rows_x, int64_t n_cols_sel, int64_t ld,
+                                  int along_cols, const int32_t *sel, const tj_mxfp8 &out, cudaStream_t s);
+cudaError_t launch_realign_nv(const tj_nvfp4 &in, const tj_nvfp4 &out, int mode, int rht, uint64_t seed,
+                              uint32_t tag, uint32_t rht_tag, cudaStream_t s);
+cudaError_t launch_realign_mx(const tj_mxfp8 &in, const tj_mxfp8 &out, cudaStream_t s);
+cudaError_t launch_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,
+                       cudaStream_t s);
+cudaError_t launch_dequant_nv(const tj_nvfp4 &q, float *y, int64_t ldy, cudaStream_t s);
+
+// GEMM: D = alpha * A_fp4 B_fp4^T (+ A8 B8^T); a/b may be null for an FP8-only GEMM.
+cudaError_t launch_gemm(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8, const tj_mxfp8 *b8,
+                        float alpha, void *d, int out_dtype, int64_t ldd, int64_t M, int64_t N,
+                        const int32_t *col_map, cudaStream_t s);
+
+cudaError_t launch_osci_reset(float *w, float *w_prev, float *dist_q, float *dist_m, const tj_nvfp4 &q_prev,
+                              const tj_nvfp4 &q_out, uint32_t *mask, int64_t rows, int64_t cols, float lr,
+                              float lr_thr, float risk_thr, int track, cudaStream_t s);
+
+cudaError_t launch_calib_accumulate(const void *x, int dtype, int64_t M, int64_t K, int64_t ld, double *sumsq,
+                                    cudaStream_t s);
+cudaError_t launch_calib_select(const double *sumsq, int64_t K, int64_t k, int32_t *outlier_idx,
+                                int32_t *normal_idx, cudaStream_t s);
+
+// Sticky device error flag (set by bounded waits that run out).
+unsigned int read_and_clear_device_error();
+
+}  // namespace tj

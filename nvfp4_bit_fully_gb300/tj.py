@@ -1,0 +1,297 @@
+"""ctypes binding of libtj (the C ABI in include/tj.h).
+
+Argument marshalling only: every step of the NVFP4 linear path runs in the
+CUDA kernels of libtj.  torch provides device memory and streams.  There is no
+CPU fallback: if libtj.so is missing or no CUDA device is present, the calls
+raise.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtj.so")
+
+TJ_OK = 0
+TJ_RTN, TJ_SR = 0, 1
+TJ_BF16, TJ_FP32 = 0, 1
+TJ_OP_BWD_DX, TJ_OP_BWD_DW = 1, 2
+TAG_DY_ROW, TAG_DY_COL, TAG_WT, TAG_XT = 1, 2, 3, 4
+TAG_RHT_DX, TAG_RHT_DW = 0x100, 0x101
+STATUS = {0: "ok", 1: "invalid argument", 2: "shape", 3: "alignment", 4: "unsupported", 5: "CUDA error",
+          6: "device wait timed out", 7: "workspace"}
+
+
+class TjError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__("%s failed: %s (%d)" % (fn, STATUS.get(code, "?"), code))
+        self.code = code
+
+
+class CNvfp4(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("sf", ctypes.c_void_p), ("outer", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64)]
+
+
+class CMxfp8(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("sf", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+_U32 = ctypes.c_uint32
+_U64 = ctypes.c_uint64
+_F = ctypes.c_float
+_SIGS = {
+    "tj_quantize_nvfp4": [_P, _I, _I64, _I64, _I64, _I, _P, _I64, _I, _I, _U64, _U32, _U32, ctypes.POINTER(CNvfp4), _P],
+    "tj_quantize_mxfp8": [_P, _I, _I64, _I64, _I64, _I, _P, _I64, ctypes.POINTER(CMxfp8), _P],
+    "tj_rht": [_P, _P, _I64, _I64, _U64, _U32, _P],
+    "tj_dequantize_nvfp4": [ctypes.POINTER(CNvfp4), _P, _I64, _P],
+    "tj_gemm_nvfp4": [ctypes.POINTER(CNvfp4), ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8),
+                      ctypes.POINTER(CMxfp8), _F, _P, _I, _I64, _P, _P],
+    "tj_gemm_mxfp8": [ctypes.POINTER(CMxfp8), ctypes.POINTER(CMxfp8), _P, _I, _I64, _P, _P],
+    "tj_linear_fwd": [_P, _I64, _I64, _I64, ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P, _P, _I64,
+                      ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P, _I, _I64, _P],
+    "tj_linear_bwd_dx": [_P, _I64, _I64, _I64, ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P, _P, _I64, _U64,
+                         _P, _I, _I64, _P, ctypes.c_size_t, _P],
+    "tj_linear_bwd_dw": [_P, _I64, _I64, _I64, ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P, _P, _I64, _U64,
+                         _P, _I64, _P, ctypes.c_size_t, _P],
+    "tj_workspace_size": [_I, _I64, _I64, _I64, _I64],
+    "tj_outlier_calibrate": [_P, _I, _I64, _I64, _I64, _P, _I, _I64, _P, _P, _P],
+    "tj_osci_reset": [_P, _P, _P, _P, ctypes.POINTER(CNvfp4), ctypes.POINTER(CNvfp4), _P, _I64, _I64, _F, _F, _F,
+                      _I, _P],
+    "tj_get_device_status": [],
+    "tj_status_str": [_I],
+}
+EXPORTED = sorted(_SIGS)
+
+
+def load(path=LIB_PATH):
+    """Load libtj.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError("libtj.so not built (run __graft_entry__.build()); no CPU fallback exists")
+        lib = ctypes.CDLL(path)
+        for name, args in _SIGS.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = ctypes.c_size_t if name == "tj_workspace_size" else (
+                ctypes.c_char_p if name == "tj_status_str" else ctypes.c_int)
+        _lib = lib
+    return _lib
+
+
+def _call(name, *args):
+    code = getattr(load(), name)(*args)
+    if code != TJ_OK:
+        raise TjError(name, code)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _round_up(v, m):
+    return (v + m - 1) // m * m
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return TJ_BF16
+    if t.dtype == torch.float32:
+        return TJ_FP32
+    raise TypeError("bf16 or fp32 tensor expected, got %s" % t.dtype)
+
+
+class NVFP4:
+    """Device buffers of a double-block NVFP4 tensor (layout documented in tj.h)."""
+
+    def __init__(self, codes, sf, outer, rows, cols):
+        self.codes, self.sf, self.outer, self.rows, self.cols = codes, sf, outer, rows, cols
+
+    @staticmethod
+    def empty(rows, cols, device="cuda"):
+        rp, cp = _round_up(rows, 128), _round_up(cols, 128)
+        return NVFP4(torch.empty(rp * cp // 2, dtype=torch.uint8, device=device),
+                     torch.empty(rp * cp // 16, dtype=torch.uint8, device=device),
+                     torch.empty((cp // 128) * rp, dtype=torch.float32, device=device), rows, cols)
+
+    def c(self):
+        return CNvfp4(self.codes.data_ptr(), self.sf.data_ptr(), self.outer.data_ptr(), self.rows, self.cols)
+
+
+class MXFP8:
+    """Device buffers of an MXFP8 outlier slice (layout documented in tj.h)."""
+
+    def __init__(self, codes, sf, rows, cols):
+        self.codes, self.sf, self.rows, self.cols = codes, sf, rows, cols
+
+    @staticmethod
+    def empty(rows, cols, device="cuda"):
+        rp, cp = _round_up(rows, 128), _round_up(cols, 128)
+        return MXFP8(torch.empty(rp * cp, dtype=torch.uint8, device=device),
+                     torch.empty(rp * cp // 32, dtype=torch.uint8, device=device), rows, cols)
+
+    def c(self):
+        return CMxfp8(self.codes.data_ptr(), self.sf.data_ptr(), self.rows, self.cols)
+
+
+def _ref(obj):
+    return None if obj is None else ctypes.byref(obj)
+
+
+def quantize_nvfp4(x, along_cols=False, sel=None, mode=TJ_RTN, rht=False, seed=0, tag=0, rht_tag=0, out=None,
+                   stream=None):
+    """Double-block NVFP4 quantization of a 2-D bf16/fp32 CUDA tensor (tj_quantize_nvfp4)."""
+    rows_x, cols_x = x.shape
+    ncols = cols_x if sel is None else sel.numel()
+    orows, ocols = (ncols, rows_x) if along_cols else (rows_x, ncols)
+    out = out if out is not None else NVFP4.empty(orows, ocols, x.device)
+    c = out.c()
+    _call("tj_quantize_nvfp4", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols), _ptr(sel),
+          0 if sel is None else sel.numel(), mode, int(rht), seed, tag, rht_tag, ctypes.byref(c), _stream(stream))
+    return out
+
+
+def quantize_mxfp8(x, along_cols=False, sel=None, out=None, stream=None):
+    """MXFP8 quantization (tj_quantize_mxfp8)."""
+    rows_x, cols_x = x.shape
+    ncols = cols_x if sel is None else sel.numel()
+    orows, ocols = (ncols, rows_x) if along_cols else (rows_x, ncols)
+    out = out if out is not None else MXFP8.empty(orows, ocols, x.device)
+    c = out.c()
+    _call("tj_quantize_mxfp8", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols), _ptr(sel),
+          0 if sel is None else sel.numel(), ctypes.byref(c), _stream(stream))
+    return out
+
+
+def rht(x, seed, tag, out=None, stream=None):
+    """128-point random Hadamard transform of each 128-block of the rows of x (fp32)."""
+    out = out if out is not None else torch.empty_like(x)
+    _call("tj_rht", _ptr(x), _ptr(out), x.shape[0], x.shape[1], seed, tag, _stream(stream))
+    return out
+
+
+def dequantize_nvfp4(q, stream=None):
+    y = torch.empty(q.rows, q.cols, dtype=torch.float32, device=q.codes.device)
+    c = q.c()
+    _call("tj_dequantize_nvfp4", ctypes.byref(c), _ptr(y), q.cols, _stream(stream))
+    return y
+
+
+def gemm_nvfp4(a, b, a8=None, b8=None, alpha=1.0, out=None, out_dtype=torch.float32, col_map=None, stream=None):
+    """D = alpha * A B^T (+ A8 B8^T), block-scaled FP4 on the tensor cores."""
+    if out is None:
+        out = torch.empty(a.rows, b.rows, dtype=out_dtype, device=a.codes.device)
+    ca, cb = a.c(), b.c()
+    c8a = a8.c() if a8 is not None else None
+    c8b = b8.c() if b8 is not None else None
+    _call("tj_gemm_nvfp4", ctypes.byref(ca), ctypes.byref(cb), _ref(c8a), _ref(c8b), alpha, _ptr(out),
+          _dtype_code(out), out.stride(0), _ptr(col_map), _stream(stream))
+    return out
+
+
+def gemm_mxfp8(a8, b8, out=None, out_dtype=torch.float32, col_map=None, stream=None):
+    if out is None:
+        out = torch.empty(a8.rows, b8.rows, dtype=out_dtype, device=a8.codes.device)
+    ca, cb = a8.c(), b8.c()
+    _call("tj_gemm_mxfp8", ctypes.byref(ca), ctypes.byref(cb), _ptr(out), _dtype_code(out), out.stride(0),
+          _ptr(col_map), _stream(stream))
+    return out
+
+
+def workspace_size(op, M, N, K, k):
+    return int(load().tj_workspace_size(op, M, N, K, k))
+
+
+def linear_fwd(x, wq, w8=None, normal_idx=None, outlier_idx=None, out_dtype=torch.bfloat16, xq=None, x8=None,
+               out=None, stream=None):
+    """Forward Y = X W^T of the NVFP4 linear layer; returns (Y, X-hat NVFP4, X-hat FP8 slice)."""
+    M, K = x.shape
+    k = 0 if outlier_idx is None else outlier_idx.numel()
+    xq = xq if xq is not None else NVFP4.empty(M, K - k, x.device)
+    if k and x8 is None:
+        x8 = MXFP8.empty(M, k, x.device)
+    out = out if out is not None else torch.empty(M, wq.rows, dtype=out_dtype, device=x.device)
+    cw, cx = wq.c(), xq.c()
+    cw8 = w8.c() if k else None
+    cx8 = x8.c() if k else None
+    _call("tj_linear_fwd", _ptr(x), M, K, x.stride(0), ctypes.byref(cw), _ref(cw8), _ptr(normal_idx),
+          _ptr(outlier_idx), k, ctypes.byref(cx), _ref(cx8), _ptr(out), _dtype_code(out), out.stride(0),
+          _stream(stream))
+    return out, xq, (x8 if k else None)
+
+
+def linear_bwd_dx(dy, wq, w8=None, normal_idx=None, outlier_idx=None, seed=0, out_dtype=torch.bfloat16,
+                  workspace=None, out=None, stream=None):
+    M, N = dy.shape
+    k = 0 if outlier_idx is None else outlier_idx.numel()
+    K = wq.cols + k
+    ws_bytes = workspace_size(TJ_OP_BWD_DX, M, N, K, k)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dy.device)
+    out = out if out is not None else torch.empty(M, K, dtype=out_dtype, device=dy.device)
+    cw = wq.c()
+    cw8 = w8.c() if k else None
+    _call("tj_linear_bwd_dx", _ptr(dy), M, N, dy.stride(0), ctypes.byref(cw), _ref(cw8), _ptr(normal_idx),
+          _ptr(outlier_idx), k, seed, _ptr(out), _dtype_code(out), out.stride(0), _ptr(workspace),
+          workspace.numel(), _stream(stream))
+    return out
+
+
+def linear_bwd_dw(dy, xq, x8=None, normal_idx=None, outlier_idx=None, seed=0, workspace=None, out=None,
+                  stream=None):
+    M, N = dy.shape
+    k = 0 if outlier_idx is None else outlier_idx.numel()
+    K = xq.cols + k
+    ws_bytes = workspace_size(TJ_OP_BWD_DW, M, N, K, k)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dy.device)
+    out = out if out is not None else torch.empty(N, K, dtype=torch.float32, device=dy.device)
+    cx = xq.c()
+    cx8 = x8.c() if k else None
+    _call("tj_linear_bwd_dw", _ptr(dy), M, N, dy.stride(0), ctypes.byref(cx), _ref(cx8), _ptr(normal_idx),
+          _ptr(outlier_idx), k, seed, _ptr(out), out.stride(0), _ptr(workspace), workspace.numel(),
+          _stream(stream))
+    return out
+
+
+def outlier_calibrate(x, sumsq, finalize=False, k=0, stream=None):
+    """Accumulate per-channel sums of squares (x may be None); on finalize return
+    (outlier_idx [k], normal_idx [K-k]) as int32 CUDA tensors."""
+    K = sumsq.numel()
+    outl = torch.empty(max(k, 1), dtype=torch.int32, device=sumsq.device)
+    norm = torch.empty(max(K - k, 1), dtype=torch.int32, device=sumsq.device)
+    if x is not None:
+        _call("tj_outlier_calibrate", _ptr(x), _dtype_code(x), x.shape[0], x.shape[1], x.stride(0), _ptr(sumsq), 0,
+              0, None, None, _stream(stream))
+    if finalize:
+        _call("tj_outlier_calibrate", None, TJ_BF16, 0, K, K, _ptr(sumsq), 1, k, _ptr(outl), _ptr(norm),
+              _stream(stream))
+        return outl[:k], norm[:K - k]
+    return None
+
+
+def osci_reset(w, w_prev, dist_q, dist_m, q_prev, q_out, mask, lr, lr_thr, risk_thr, track=True, stream=None):
+    """One OsciReset pass (tj_osci_reset); w, w_prev, dist_q, dist_m updated in place."""
+    rows, cols = w.shape
+    cp, co = q_prev.c(), q_out.c()
+    _call("tj_osci_reset", _ptr(w), _ptr(w_prev), _ptr(dist_q), _ptr(dist_m), ctypes.byref(cp), ctypes.byref(co),
+          _ptr(mask), rows, cols, lr, lr_thr, risk_thr, int(track), _stream(stream))
+
+
+def device_status():
+    """Reads and clears the sticky device flag; raises TjError on a timed-out device wait."""
+    code = load().tj_get_device_status()
+    if code != TJ_OK:
+        raise TjError("tj_get_device_status", code)

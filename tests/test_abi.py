@@ -1,0 +1,89 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library builds, loads, and exports every function include/tj.h declares;
+the ctypes binding knows each of them; argument and shape errors are reported
+by status code before any launch (these calls return before touching a device).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "tj.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tj_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+
+    path = __graft_entry__.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("tj_quantize_nvfp4", "tj_rht", "tj_linear_fwd", "tj_linear_bwd_dx", "tj_linear_bwd_dw",
+              "tj_outlier_calibrate", "tj_osci_reset"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_symbol():
+    from nvfp4_bit_fully_gb300 import tj
+
+    assert set(_declared()) <= set(tj.EXPORTED)
+
+
+def test_status_strings_and_workspace(lib):
+    from nvfp4_bit_fully_gb300 import tj
+
+    l = tj.load()
+    assert l.tj_status_str(0) == b"ok"
+    assert l.tj_status_str(7) == b"workspace missing or too small"
+    # dX workspace for 16384x4096x1024 with 103 outlier channels
+    rp = lambda v: (v + 127) // 128 * 128
+    def nv(r, c):
+        return rp(r) * rp(c) // 2 + rp(r) * rp(c) // 16 + rp(r) * rp(c) // 128 * 4
+    def mx(r, c):
+        return rp(r) * rp(c) + rp(r) * rp(c) // 32
+    assert tj.workspace_size(1, 16384, 4096, 1024, 103) == nv(16384, 4096) + nv(921, 4096) + mx(16384, 4096) + mx(103, 4096)
+    assert tj.workspace_size(2, 256, 512, 512, 0) == nv(512, 256) + nv(512, 256)
+    assert tj.workspace_size(1, 16, 16, 8, 9) == 0                       # k > K
+
+
+def test_argument_errors_before_launch(lib):
+    from nvfp4_bit_fully_gb300 import tj
+
+    l = tj.load()
+    q = tj.CNvfp4(0, 0, 0, 128, 128)
+    # null input
+    assert l.tj_quantize_nvfp4(None, 0, 128, 128, 128, 0, None, 0, 0, 0, 0, 0, 0, ctypes.byref(q), None) == 1
+    # bad rounding mode
+    assert l.tj_quantize_nvfp4(ctypes.c_void_p(256), 0, 128, 128, 128, 0, None, 0, 5, 0, 0, 0, 0,
+                               ctypes.byref(q), None) == 1
+    # misaligned input pointer
+    assert l.tj_quantize_nvfp4(ctypes.c_void_p(258), 0, 128, 128, 128, 0, None, 0, 0, 0, 0, 0, 0,
+                               ctypes.byref(q), None) == 3
+    # output descriptor with null buffers
+    assert l.tj_quantize_nvfp4(ctypes.c_void_p(256), 0, 128, 128, 128, 0, None, 0, 0, 0, 0, 0, 0,
+                               ctypes.byref(q), None) == 1
+    # RHT needs whole 128-blocks
+    assert l.tj_rht(ctypes.c_void_p(256), ctypes.c_void_p(256), 4, 100, 0, 0, None) == 2
+    # backward without workspace
+    w = tj.CNvfp4(256, 256, 256, 128, 128)
+    assert l.tj_linear_bwd_dx(ctypes.c_void_p(256), 128, 128, 128, ctypes.byref(w), None, None, None, 0, 1,
+                              ctypes.c_void_p(256), 0, 128, None, 0, None) == 7
+    # calibration: k larger than K
+    assert l.tj_outlier_calibrate(None, 0, 0, 8, 8, ctypes.c_void_p(256), 1, 9, ctypes.c_void_p(256),
+                                  ctypes.c_void_p(256), None) == 2

@@ -1,0 +1,103 @@
+"""GPU parity: the tcgen05 block-scaled GEMM vs the oracle's fp64 product.
+
+The operands are quantized on the GPU (bit-exact against the oracle, checked
+here again), then |D_gpu - D_oracle| <= 2e-3 * sum_k |a_mk||b_nk| per output.
+Shapes cover one tile, several tiles, an odd number of 128-K blocks (a half
+pipeline stage), ragged M / N, the FP8 slice alone and combined, column
+scatter and bf16 output.
+"""
+import numpy as np
+import pytest
+import torch
+
+from layouts import abs_product, abs_product_fp8, assert_gemm_close, assert_mxfp8_equal, assert_nvfp4_equal
+from oracle import linear as OL
+from oracle import quant as Q
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tj():
+    from nvfp4_bit_fully_gb300 import tj as _tj
+
+    _tj.load()
+    return _tj
+
+
+def _rand(rows, cols, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(rows, cols, generator=g) * scale
+    x[:, torch.randperm(cols, generator=g)[: max(1, cols // 64)]] *= 20
+    return x.to(torch.bfloat16)
+
+
+def _operands(tj, M, N, K, mode=0, seed=0):
+    A = _rand(M, K, seed + 1)
+    B = _rand(N, K, seed + 2, 0.05)
+    qa = tj.quantize_nvfp4(A.cuda(), mode=mode, seed=seed, tag=1)
+    qb = tj.quantize_nvfp4(B.cuda(), mode=mode, seed=seed, tag=2)
+    ra = Q.quantize_nvfp4(A.float().numpy(), mode, seed=seed, tag=1)
+    rb = Q.quantize_nvfp4(B.float().numpy(), mode, seed=seed, tag=2)
+    torch.cuda.synchronize()
+    assert_nvfp4_equal(qa, ra, "A")
+    assert_nvfp4_equal(qb, rb, "B")
+    return qa, qb, ra, rb
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 512), (128, 128, 384), (200, 300, 640),
+                                   (512, 256, 1024)])
+def test_gemm_fp4(tj, M, N, K):
+    qa, qb, ra, rb = _operands(tj, M, N, K, mode=1, seed=M + N + K)
+    d = tj.gemm_nvfp4(qa, qb)
+    torch.cuda.synchronize()
+    tj.device_status()
+    ref = OL.gemm_fp4(ra, rb)
+    assert_gemm_close(d.cpu().numpy(), ref, abs_product(ra, rb), what="fp4 %dx%dx%d" % (M, N, K))
+
+
+def test_gemm_fp4_alpha_bf16_and_scatter(tj):
+    M, N, K = 256, 200, 256
+    qa, qb, ra, rb = _operands(tj, M, N, K, seed=9)
+    cmap = torch.randperm(300, generator=torch.Generator().manual_seed(2))[:N].to(torch.int32)
+    out = torch.full((M, 300), -7.0, dtype=torch.bfloat16, device="cuda")
+    tj.gemm_nvfp4(qa, qb, alpha=2.0 ** -7, out=out, col_map=cmap.cuda())
+    torch.cuda.synchronize()
+    ref = OL.gemm_fp4(ra, rb, 2.0 ** -7)
+    got = out.float().cpu().numpy()
+    assert_gemm_close(got[:, cmap.numpy()], ref, abs_product(ra, rb, 2.0 ** -7), bf16=True, what="scatter")
+    untouched = np.setdiff1d(np.arange(300), cmap.numpy())
+    assert np.all(got[:, untouched] == -7.0)
+
+
+def _fp8_operands(tj, M, N, k, seed):
+    A = _rand(M, k, seed + 5, 30.0)
+    B = _rand(N, k, seed + 6, 0.05)
+    a8 = tj.quantize_mxfp8(A.cuda())
+    b8 = tj.quantize_mxfp8(B.cuda())
+    ra = Q.quantize_mxfp8(A.float().numpy())
+    rb = Q.quantize_mxfp8(B.float().numpy())
+    torch.cuda.synchronize()
+    assert_mxfp8_equal(a8, ra, "A8")
+    assert_mxfp8_equal(b8, rb, "B8")
+    return a8, b8, ra, rb
+
+
+@pytest.mark.parametrize("M,N,k", [(128, 128, 128), (256, 103, 103), (300, 410, 410)])
+def test_gemm_fp8_slice(tj, M, N, k):
+    a8, b8, ra, rb = _fp8_operands(tj, M, N, k, seed=k)
+    d = tj.gemm_mxfp8(a8, b8)
+    torch.cuda.synchronize()
+    ref = OL.gemm_fp8(ra, rb)
+    assert_gemm_close(d.cpu().numpy(), ref, abs_product_fp8(ra, rb), what="fp8")
+
+
+def test_gemm_fp4_plus_fp8_same_tile(tj):
+    M, N, K, k = 256, 256, 384, 40
+    qa, qb, ra, rb = _operands(tj, M, N, K, seed=3)
+    a8, b8, ra8, rb8 = _fp8_operands(tj, M, N, k, seed=4)
+    d = tj.gemm_nvfp4(qa, qb, a8, b8)
+    torch.cuda.synchronize()
+    ref = OL.gemm_fp4(ra, rb) + OL.gemm_fp8(ra8, rb8)
+    bound = abs_product(ra, rb) + abs_product_fp8(ra8, rb8)
+    assert_gemm_close(d.cpu().numpy(), ref, bound, what="fp4+fp8")

@@ -1,0 +1,122 @@
+"""GPU parity: the NVFP4 linear layer (forward, dX, dW) through the C ABI.
+
+Every quantized operand the calls produce (saved X-hat, the SR + RHT operands
+of the backward, the re-aligned W-hat^T / X-hat^T, the FP8 slices) is compared
+bit for bit with the oracle; the products are compared within
+2e-3 * sum|a||b| of the oracle's fp64 GEMM on those same operands.
+"""
+import numpy as np
+import pytest
+import torch
+
+from layouts import (abs_product, abs_product_fp8, assert_gemm_close, assert_mxfp8_equal, assert_nvfp4_equal,
+                     carve_workspace)
+from nvfp4_bit_fully_gb300 import workloads
+from oracle import linear as OL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tj():
+    from nvfp4_bit_fully_gb300 import tj as _tj
+
+    _tj.load()
+    return _tj
+
+
+def _setup(tj, X, W, outl):
+    K = X.shape[1]
+    if len(outl):
+        normal = OL.normal_channels(K, outl)
+        ni = torch.from_numpy(normal.astype(np.int32)).cuda()
+        oi = torch.from_numpy(np.asarray(outl, np.int32)).cuda()
+        wq = tj.quantize_nvfp4(W.cuda(), sel=ni)
+        w8 = tj.quantize_mxfp8(W.cuda(), sel=oi)
+    else:
+        ni = oi = None
+        wq = tj.quantize_nvfp4(W.cuda())
+        w8 = None
+    return ni, oi, wq, w8
+
+
+def _run_and_check(tj, X, W, dY, outl, seed):
+    M, K = X.shape
+    N = W.shape[0]
+    k = len(outl)
+    ni, oi, wq, w8 = _setup(tj, X, W, outl)
+    y, xq, x8 = tj.linear_fwd(X.cuda(), wq, w8, ni, oi, out_dtype=torch.float32)
+    ws_dx = torch.empty(tj.workspace_size(tj.TJ_OP_BWD_DX, M, N, K, k), dtype=torch.uint8, device="cuda")
+    ws_dw = torch.empty(tj.workspace_size(tj.TJ_OP_BWD_DW, M, N, K, k), dtype=torch.uint8, device="cuda")
+    dx = tj.linear_bwd_dx(dY.cuda(), wq, w8, ni, oi, seed=seed, out_dtype=torch.float32, workspace=ws_dx)
+    dw = tj.linear_bwd_dw(dY.cuda(), xq, x8, ni, oi, seed=seed, workspace=ws_dw)
+    torch.cuda.synchronize()
+    tj.device_status()
+
+    Xf, Wf, dYf = X.float().numpy(), W.float().numpy(), dY.float().numpy()
+    Y_ref, fx, fw = OL.forward(Xf, Wf, outl)
+    # forward: saved context bit-exact, product within tolerance
+    assert_nvfp4_equal(xq, fx["q"], "X-hat")
+    bound = abs_product(fx["q"], fw["q"])
+    if k:
+        assert_mxfp8_equal(x8, fx["q8"], "X-hat FP8 slice")
+        bound = bound + abs_product_fp8(fx["q8"], fw["q8"])
+    assert_gemm_close(y.cpu().numpy(), Y_ref, bound, what="Y")
+
+    # dX: operands in the workspace bit-exact, product within tolerance
+    K_N = K - k
+    s_dy, s_w, q8_dy, q8_w = OL.bwd_dx_operands(dYf, fw, seed)
+    parts = [("nv", M, N), ("nv", K_N, N)] + ([("mx", M, N), ("mx", k, N)] if k else [])
+    views = carve_workspace(ws_dx, parts)
+    assert_nvfp4_equal(views[0], s_dy, "S_dY")
+    assert_nvfp4_equal(views[1], s_w, "S_W (re-aligned W-hat^T)")
+    if k:
+        assert_mxfp8_equal(views[2], q8_dy, "Q8(dY)")
+        assert_mxfp8_equal(views[3], q8_w, "Q8(W-hat_O^T)")
+    dx_ref = OL.bwd_dx(dYf, fw, outl, seed)
+    nc = OL.normal_channels(K, outl)
+    bx = np.zeros((M, K))
+    bx[:, nc] = abs_product(s_dy, s_w, OL.ALPHA_RHT)[:, :K_N]
+    if k:
+        bx[:, outl] = abs_product_fp8(q8_dy, q8_w)[:, :k]
+    assert_gemm_close(dx.cpu().numpy(), dx_ref, bx, what="dX")
+
+    # dW
+    s_dyt, s_x, q8_dyt, q8_x = OL.bwd_dw_operands(dYf, fx, seed)
+    parts = [("nv", N, M), ("nv", K_N, M)] + ([("mx", N, M), ("mx", k, M)] if k else [])
+    views = carve_workspace(ws_dw, parts)
+    assert_nvfp4_equal(views[0], s_dyt, "S_dY^T")
+    assert_nvfp4_equal(views[1], s_x, "S_X (re-aligned X-hat^T)")
+    if k:
+        assert_mxfp8_equal(views[2], q8_dyt, "Q8(dY^T)")
+        assert_mxfp8_equal(views[3], q8_x, "Q8(X-hat_O^T)")
+    dw_ref = OL.bwd_dw(dYf, fx, outl, seed)
+    bw = np.zeros((N, K))
+    bw[:, nc] = abs_product(s_dyt, s_x, OL.ALPHA_RHT)[:, :K_N]
+    if k:
+        bw[:, outl] = abs_product_fp8(q8_dyt, q8_x)[:, :k]
+    assert_gemm_close(dw.cpu().numpy(), dw_ref, bw, what="dW")
+
+
+def test_tiny_linear_no_outliers(tj):
+    X, W, dY = workloads.tiny(seed=0)
+    _run_and_check(tj, X, W, dY, np.array([], dtype=np.int64), seed=0)
+
+
+def test_tiny_linear_with_outcontrol(tj):
+    X, W, dY = workloads.tiny(seed=0)
+    heavy = workloads.heavy_columns(512, 8, 0, 1 + 7919).numpy()
+    s = (X.float() ** 2).sum(dim=0).numpy()
+    outl = np.sort(np.argsort(-s, kind="stable")[:52])          # top 10% channels
+    assert set(heavy) <= set(outl)
+    _run_and_check(tj, X, W, dY, outl, seed=5)
+
+
+def test_ragged_linear(tj):
+    g = torch.Generator().manual_seed(11)
+    M, N, K = 200, 136, 328
+    X = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    W = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16)
+    dY = (torch.randn(M, N, generator=g) * 1e-3).to(torch.bfloat16)
+    outl = np.array([3, 40, 41, 200, 327])
+    _run_and_check(tj, X, W, dY, outl, seed=17)

@@ -1,0 +1,112 @@
+"""GPU parity: OsciReset and OutControl calibration, bit for bit.
+
+OsciReset: several steps of a synthetic trajectory whose learning rate crosses
+the threshold; every piece of state (master weight, w_prev, dist_Q, dist_M, the
+emitted forward NVFP4 weight, the reset mask) must equal the oracle's exactly.
+Calibration: fixed-order fp64 sums of squares over ragged batches, and the
+top-k selection with its tie rule.
+"""
+import numpy as np
+import pytest
+import torch
+
+from layouts import assert_nvfp4_equal
+from oracle import calib as OC
+from oracle import osci as OO
+from oracle import quant as Q
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tj():
+    from nvfp4_bit_fully_gb300 import tj as _tj
+
+    _tj.load()
+    return _tj
+
+
+def _mask_bits(mask_words, rows, cols):
+    w = mask_words.cpu().numpy().view(np.uint32).reshape(rows, -1)
+    bits = (w[:, :, None] >> np.arange(32, dtype=np.uint32)) & 1
+    return bits.reshape(rows, -1)[:, :cols].astype(bool)
+
+
+@pytest.mark.parametrize("rows,cols", [(64, 256), (100, 200)])
+def test_osci_reset_trajectory_bit_exact(tj, rows, cols):
+    rng = np.random.default_rng(rows + cols)
+    w0 = (rng.standard_normal((rows, cols)) * 0.02).astype(np.float32)
+    # make some elements oscillate around bin midpoints: alternate +-d
+    osc = rng.random((rows, cols)) < 0.05
+    state = OO.init_state(w0)
+    w_dev = torch.from_numpy(w0.copy()).cuda()
+    w_prev = w_dev.clone()
+    dq = torch.zeros_like(w_dev)
+    dm = torch.zeros_like(w_dev)
+    q_prev = tj.quantize_nvfp4(w_dev)
+    q_out = tj.NVFP4.empty(rows, cols)
+    mask = torch.empty(rows * ((cols + 31) // 32), dtype=torch.int32, device="cuda")
+    w = w0
+    lrs = [1e-3, 8e-4, 5e-4, 2e-4, 9e-5, 5e-5, 2e-5, 1e-5]
+    for t, lr in enumerate(lrs):
+        step = (rng.standard_normal((rows, cols)) * lr).astype(np.float32)
+        step = np.where(osc, np.float32(3e-4 * (1 if t % 2 == 0 else -1)), step).astype(np.float32)
+        w = (w + step).astype(np.float32)
+        w_dev.copy_(torch.from_numpy(w))
+        w, state, m_ref, q_ref = OO.osci_reset_step(w, state, lr, 1e-4, 4.0)
+        tj.osci_reset(w_dev, w_prev, dq, dm, q_prev, q_out, mask, lr, 1e-4, 4.0)
+        torch.cuda.synchronize()
+        assert np.array_equal(w_dev.cpu().numpy(), w), t
+        assert np.array_equal(w_prev.cpu().numpy(), state["w_prev"]), t
+        assert np.array_equal(dq.cpu().numpy(), state["dist_q"]), t
+        assert np.array_equal(dm.cpu().numpy(), state["dist_m"]), t
+        assert np.array_equal(_mask_bits(mask, rows, cols), m_ref), t
+        assert_nvfp4_equal(q_out, q_ref, "Q step %d" % t)
+        q_prev, q_out = q_out, q_prev
+    assert state["dist_m"].max() > 0
+
+
+def test_osci_reset_in_place_q(tj):
+    """q_out may be the same tensor as q_prev: it then holds Q of the new weights."""
+    rows, cols = 32, 128
+    w = torch.randn(rows, cols, device="cuda") * 0.02
+    q = tj.quantize_nvfp4(w)
+    w_prev = w.clone()
+    w2 = w + 1e-4
+    w2_before = w2.cpu().numpy().copy()
+    dq = torch.zeros_like(w)
+    dm = torch.zeros_like(w)
+    mask = torch.empty(rows * 4, dtype=torch.int32, device="cuda")
+    tj.osci_reset(w2, w_prev, dq, dm, q, q, mask, 1e-5, 1e-4, 4.0)
+    torch.cuda.synchronize()
+    assert_nvfp4_equal(q, Q.quantize_nvfp4(w2_before, 0), "in-place Q")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_calibration_bit_exact(tj, dtype):
+    g = torch.Generator().manual_seed(5)
+    K = 300
+    heavy = torch.randperm(K, generator=g)[:12]
+    sumsq = torch.zeros(K, dtype=torch.float64, device="cuda")
+    s_ref = np.zeros(K)
+    for b, M in enumerate((1000, 300, 4096)):
+        x = torch.randn(M, K, generator=g)
+        x[:, heavy] *= 40
+        x = x.to(dtype)
+        tj.outlier_calibrate(x.cuda(), sumsq)
+        s_ref = OC.accumulate_sumsq(x.float().numpy(), s_ref)
+    k = OC.outlier_count(K, 10)
+    outl, normal = tj.outlier_calibrate(None, sumsq, finalize=True, k=k)
+    torch.cuda.synchronize()
+    assert np.array_equal(sumsq.cpu().numpy(), s_ref)
+    o_ref, n_ref = OC.top_k_channels(s_ref, k)
+    assert np.array_equal(outl.cpu().numpy(), o_ref)
+    assert np.array_equal(normal.cpu().numpy(), n_ref)
+    assert set(heavy.numpy()) <= set(o_ref)
+
+
+def test_calibration_ties(tj):
+    s = torch.tensor([5.0, 7.0, 7.0, 1.0, 7.0, 0.0], dtype=torch.float64, device="cuda")
+    outl, normal = tj.outlier_calibrate(None, s, finalize=True, k=2)
+    torch.cuda.synchronize()
+    assert outl.cpu().tolist() == [1, 2] and normal.cpu().tolist() == [0, 3, 4, 5]
