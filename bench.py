@@ -1,0 +1,520 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 TetraJet-v2 NVFP4 linear path.
+
+One step = the ~370M-class decoder-layer linear set on 16384 tokens (QKV
+1024->3072, out-proj 1024->1024, SwiGLU gate/up 1024->2x4096, down 4096->1024;
+10% of each layer's input channels kept in FP8 by OutControl), forward + dX + dW
+through the C ABI, followed by one OsciReset pass over 369,098,752 fp32 master
+weights (cosine learning-rate schedule 1e-3 -> 1e-5 over 200 steps, reset
+threshold lr < 1e-4 and risk > 4).
+
+value  = linear-set fwd+bwd algorithmic TFLOP/s (6 * M * sum N*K per step) over
+         the time of the linear calls, inputs resident in HBM;
+e2e    = the same with X and dY copied host->device from pinned memory and dW
+         copied back every step;
+parts  = per-call times; the OsciReset pass and the quantize sweep in GB/s.
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "NVFP4 linear fwd+bwd TFLOP/s & quantize GB/s, as fraction of GB300 roofline"
+WORKLOAD = ("layer_set_370M: decoder-layer linear set QKV 1024->3072, out 1024->1024, gate/up 1024->8192, "
+            "down 4096->1024 on 16384 tokens, 10% FP8 outlier channels, fwd+dX+dW; plus OsciReset over "
+            "369,098,752 fp32 master weights per step")
+TOKENS = 16384
+OUTLIER_PCT = 10
+LR_THR, RISK_THR = 1e-4, 4.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def linear_flops(M=TOKENS):
+    from nvfp4_bit_fully_gb300.workloads import LAYER_SET
+
+    return 6.0 * M * sum(n * k for _, n, k in LAYER_SET)
+
+
+def osci_bytes_per_elem():
+    # read w, w_prev, dist_Q, dist_M (4 B each) + previous Q (0.5 + 1/16 + 4/128 B);
+    # write w_prev, dist_Q, dist_M + new Q + 1 mask bit (w itself only on reset)
+    q = 0.5 + 1.0 / 16 + 4.0 / 128
+    return (16 + q) + (12 + q + 1.0 / 8)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1].split()[0]))
+                    smax.append(float(parts[2].split()[0]))
+                    power.append(float(parts[3].split()[0]))
+                except ValueError:
+                    continue
+                for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                     parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# the step
+# ---------------------------------------------------------------------------
+class Timeline:
+    """CUDA events around every C-ABI call of a step, on the launching stream."""
+
+    def __init__(self, stream):
+        self.stream = stream
+        self.records = []
+
+    def time(self, name, fn):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(self.stream)
+        out = fn()
+        e.record(self.stream)
+        self.records.append((name, s, e))
+        return out
+
+    def summary(self):
+        agg = {}
+        for name, s, e in self.records:
+            agg.setdefault(name, []).append(s.elapsed_time(e))
+        return {k: (float(np.sum(v)), len(v)) for k, v in agg.items()}
+
+
+class Linear:
+    """One linear of the layer set: inputs, calibrated outlier set, forward
+    weight operands and every output / workspace buffer, all resident in HBM."""
+
+    def __init__(self, tj, wl, name, N, K, dev, seed):
+        self.name, self.N, self.K = name, N, K
+        self.X, W, self.dY = wl.device_layer_set_linear(name, N, K, seed=seed, M=TOKENS, device=dev)
+        self.k = (OUTLIER_PCT * K + 99) // 100
+        # OutControl calibration: 4 warm-up batches with fixed heavy channels (cold path)
+        sumsq = torch.zeros(K, dtype=torch.float64, device=dev)
+        for b in range(4):
+            xb = wl.device_calibration_batch(K, TOKENS, 20, b, seed, 700 + K, dev)
+            tj.outlier_calibrate(xb, sumsq)
+            del xb
+        self.oi, self.ni = tj.outlier_calibrate(None, sumsq, finalize=True, k=self.k)
+        self.wq = tj.quantize_nvfp4(W, sel=self.ni)
+        self.w8 = tj.quantize_mxfp8(W, sel=self.oi)
+        M, kn = TOKENS, K - self.k
+        self.xq = tj.NVFP4.empty(M, kn, dev)
+        self.x8 = tj.MXFP8.empty(M, self.k, dev)
+        self.Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        self.dX = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        self.dW = torch.empty(N, K, dtype=torch.float32, device=dev)
+        self.ws_dx = torch.empty(tj.workspace_size(tj.TJ_OP_BWD_DX, M, N, K, self.k), dtype=torch.uint8, device=dev)
+        self.ws_dw = torch.empty(tj.workspace_size(tj.TJ_OP_BWD_DW, M, N, K, self.k), dtype=torch.uint8, device=dev)
+        self.flops = 6.0 * M * N * K
+
+    def run(self, tj, seed, tl, stream):
+        tl.time(self.name + ".fwd", lambda: tj.linear_fwd(self.X, self.wq, self.w8, self.ni, self.oi, xq=self.xq,
+                                                          x8=self.x8, out=self.Y, stream=stream))
+        tl.time(self.name + ".bwd_dx", lambda: tj.linear_bwd_dx(self.dY, self.wq, self.w8, self.ni, self.oi, seed=seed,
+                                                                workspace=self.ws_dx, out=self.dX, stream=stream))
+        tl.time(self.name + ".bwd_dw", lambda: tj.linear_bwd_dw(self.dY, self.xq, self.x8, self.ni, self.oi, seed=seed,
+                                                                workspace=self.ws_dw, out=self.dW, stream=stream))
+
+
+class OsciState:
+    """OsciReset state of the master weights: w, w_prev, dist_Q, dist_M, Q double buffer, mask."""
+
+    def __init__(self, tj, wl, n, dev, seed):
+        self.w = wl.device_master_weights(n, seed=seed, device=dev)
+        rows, cols = self.w.shape
+        self.w_prev = self.w.clone()
+        self.dq = torch.zeros_like(self.w)
+        self.dm = torch.zeros_like(self.w)
+        self.q = [tj.quantize_nvfp4(self.w), tj.NVFP4.empty(rows, cols, dev)]
+        self.mask = torch.empty(rows * ((cols + 31) // 32), dtype=torch.int32, device=dev)
+        self.n = rows * cols
+
+    def run(self, tj, lr, tl, stream):
+        tl.time("osci_reset", lambda: tj.osci_reset(self.w, self.w_prev, self.dq, self.dm, self.q[0], self.q[1],
+                                                    self.mask, lr, LR_THR, RISK_THR, True, stream=stream))
+        self.q.reverse()
+
+
+LAUNCHES_PER_LINEAR = {True: 15, False: 7}     # with / without an FP8 outlier slice
+
+
+# ---------------------------------------------------------------------------
+# secondary measurements (outside the timed step loop)
+# ---------------------------------------------------------------------------
+def time_kernel(fn, stream, reps, flush=None, warmup=3):
+    """Average ms of fn() over reps launches, L2 flushed before each (outside the events)."""
+    for _ in range(warmup):
+        fn()
+    total = 0.0
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        e.synchronize()
+        total += s.elapsed_time(e)
+    return total / reps
+
+
+def quantize_sweep(tj, dev, stream, hbm_peak, flush):
+    """The quantize-only sweep: 4096x1024, 8192x2048, 16384x4096 bf16 inputs, RTN and SR,
+    row-wise and transposed alignment; bytes = 2 (read) + 0.59375 (write) per element."""
+    from nvfp4_bit_fully_gb300 import workloads as wl
+
+    out = []
+    for rows, cols in ((4096, 1024), (8192, 2048), (16384, 4096)):
+        x = wl.device_heavy_columns((rows, cols), 1.0, 30.0, math.ceil(cols / 100), 0, 11, dev)
+        for along in (False, True):
+            q = tj.NVFP4.empty(cols if along else rows, rows if along else cols, dev)
+            for mode in (tj.TJ_RTN, tj.TJ_SR):
+                ms = time_kernel(lambda: tj.quantize_nvfp4(x, along_cols=along, mode=mode, seed=1, tag=1, out=q,
+                                                           stream=stream), stream, 10, flush)
+                gbs = rows * cols * (2 + 0.59375) / (ms * 1e-3) / 1e9
+                out.append({"shape": [rows, cols], "align": "col" if along else "row",
+                            "mode": "SR" if mode else "RTN", "ms": round(ms, 4), "GB/s": round(gbs, 1),
+                            "frac": round(gbs / hbm_peak, 3)})
+        del x
+    return out
+
+
+def gemm_alone(tj, lin, stream, fp4_peak, fp8_peak):
+    """The largest forward GEMM (FP4 part + FP8 slice in one tile) timed alone."""
+    M, N, K, k = TOKENS, lin.N, lin.K, lin.k
+    ms = time_kernel(lambda: tj.gemm_nvfp4(lin.xq, lin.wq, lin.x8, lin.w8, out=lin.Y, stream=stream), stream, 20)
+    f4 = 2.0 * M * N * (K - k)
+    f8 = 2.0 * M * N * k
+    t_star = f4 / (fp4_peak * 1e12) + f8 / (fp8_peak * 1e12)          # time at the dtype-weighted peak
+    return {"shape": [M, N, K], "k_fp8": k, "ms": round(ms, 4), "TFLOP/s": round((f4 + f8) / (ms * 1e-3) / 1e12, 1),
+            "frac_of_peak": round(t_star / (ms * 1e-3), 3)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle as a CPU baseline (bounded sample of the same workload)
+# ---------------------------------------------------------------------------
+def oracle_sample(tokens, names=None):
+    """Oracle fwd+bwd of the linear set (or the named linears) on `tokens` tokens;
+    returns (seconds, flops)."""
+    from nvfp4_bit_fully_gb300 import workloads as wl
+    from oracle import calib as OC
+    from oracle import linear as OL
+
+    secs = 0.0
+    flops = 0.0
+    for name, N, K in wl.LAYER_SET:
+        if names is not None and name not in names:
+            continue
+        X, W, dY = wl.layer_set_linear(name, N, K, seed=3, M=tokens)
+        Xf, Wf, dYf = X.float().numpy(), W.float().numpy(), dY.float().numpy()
+        t0 = time.perf_counter()
+        k = OC.outlier_count(K, OUTLIER_PCT)
+        outl, _ = OC.top_k_channels(OC.accumulate_sumsq(Xf, np.zeros(K)), k)
+        _, fx, fw = OL.forward(Xf, Wf, outl)
+        OL.bwd_dx(dYf, fw, outl, 7)
+        OL.bwd_dw(dYf, fx, outl, 7)
+        secs += time.perf_counter() - t0
+        flops += 6.0 * tokens * N * K
+    return secs, flops
+
+
+def cpu_baseline():
+    secs, flops = oracle_sample(128)
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "oracle fwd+dX+dW (calibration, quantize, RHT+SR, re-alignment, fp64 GEMMs) of all four "
+                      "linears of the set on 128 of the 16384 tokens; %.1f s of CPU time (numpy elementwise "
+                      "single-threaded, fp64 matmul via multithreaded BLAS)" % secs}
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the oracle (CPU) timed on bounded samples of the same workload."""
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        oracle_sample(128, ("out",))
+    secs, flops = 0.0, 0.0
+    for _ in range(args.steps):
+        s, f = oracle_sample(128, ("out",))
+        secs += s
+        flops += f
+    value = flops / secs / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (fp32 quantizer)",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample_per_step": "out-proj 1024->1024, 128 tokens"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": "each step: oracle fwd+dX+dW of the out-proj linear (1024->1024, 10% FP8 "
+                                       "outliers) on 128 of the 16384 tokens"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the quantize sweep / GEMM-alone / e2e parts")
+    ap.add_argument("--osci-params", type=int, default=0, help="override the OsciReset size (profiling only)")
+    ap.add_argument("--only", choices=["all", "osci", "linear"], default="all",
+                    help="run one part of the step (for small profiler captures; not a bench line)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from nvfp4_bit_fully_gb300 import tj
+    from nvfp4_bit_fully_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    peaks, peak_src = load_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    bf16_burst = float(peaks["bf16_tflops"])
+    fp4_peak, fp8_peak = bf16_burst * 13.5 / 2.25, bf16_burst * 4.5 / 2.25      # nominal dtype ratios
+
+    with torch.cuda.stream(stream):
+        linears = [Linear(tj, wl, n, N, K, dev, seed=3 + rank) for n, N, K in wl.LAYER_SET] \
+            if args.only != "osci" else []
+        osci_n = args.osci_params or wl.OSCI_PARAMS
+        osci = OsciState(tj, wl, osci_n, dev, seed=3 + rank) if args.only != "linear" else None
+    torch.cuda.synchronize()
+
+    step_counter = [0]
+
+    def step(tl):
+        t = step_counter[0]
+        seed = 1000 + t
+        for lin in linears:
+            lin.run(tj, seed, tl, stream)
+        if osci is not None:
+            osci.run(tj, float(wl.cosine_lr(t % 200)), tl, stream)
+        step_counter[0] += 1
+
+    for _ in range(args.warmup):
+        step(Timeline(stream))
+    torch.cuda.synchronize()
+    tj.device_status()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.25)
+    tl = Timeline(stream)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(tl)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    tj.device_status()
+
+    total_ms = max_over_ranks(world, t_start.elapsed_time(t_end))
+    summ = tl.summary()
+    if args.only != "all":
+        if rank == 0:
+            print(json.dumps({"profiling_case": args.only, "ms_per_step": total_ms / args.steps,
+                              "parts": {k: v[0] / v[1] for k, v in summ.items()}}), flush=True)
+        return 0
+    lin_ms = max_over_ranks(world, sum(v[0] for k, v in summ.items() if k != "osci_reset"))
+    osci_ms = summ["osci_reset"][0] / summ["osci_reset"][1]
+    flops_step = sum(l.flops for l in linears)
+    value = world * flops_step * args.steps / (lin_ms * 1e-3) / 1e12
+    osci_bytes = osci.n * osci_bytes_per_elem()
+    osci_gbs = osci_bytes / (osci_ms * 1e-3) / 1e9
+    parts = {k: {"ms": round(v[0] / v[1], 4)} for k, v in sorted(summ.items())}
+    for lin in linears:
+        for kind, frac in (("fwd", 1 / 3), ("bwd_dx", 1 / 3), ("bwd_dw", 1 / 3)):
+            p = parts[lin.name + "." + kind]
+            p["TFLOP/s"] = round(lin.flops * frac / (p["ms"] * 1e-3) / 1e12, 1)
+    parts["osci_reset"]["GB/s"] = round(osci_gbs, 1)
+    # dominant call of the step (largest total time)
+    dom = max(summ.items(), key=lambda kv: kv[1][0])[0]
+    if dom == "osci_reset":
+        roof = {"kernel": "k_osci_reset (tj_osci_reset)", "bound": "hbm", "achieved": round(osci_gbs, 1),
+                "peak": hbm_peak, "unit": "GB/s", "frac": round(osci_gbs / hbm_peak, 3), "traffic": None,
+                "algorithmic_bytes_per_launch": int(osci_bytes), "peak_source": peak_src + " (hbm_gbs)"}
+    else:
+        p = parts[dom]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": p["TFLOP/s"], "peak": round(fp4_peak, 1),
+                "unit": "TFLOP/s", "frac": round(p["TFLOP/s"] / fp4_peak, 3), "traffic": None,
+                "peak_source": peak_src + " bf16 burst x 6 (nominal fp4/bf16 ratio)"}
+    launches = args.steps * (sum(LAUNCHES_PER_LINEAR[l.k > 0] for l in linears) + 1)
+
+    extras = {}
+    if not args.no_extras and rank == 0:
+        flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # 512 MB > L2
+        extras["quantize_sweep"] = quantize_sweep(tj, dev, stream, hbm_peak, flush)
+        big = max(linears, key=lambda l: l.N * l.K)
+        extras["gemm_fwd_alone"] = gemm_alone(tj, big, stream, fp4_peak, fp8_peak)
+        del flush
+    e2e = None
+    if not args.no_extras:
+        e2e = measure_e2e(tj, linears, stream, max(3, args.steps // 4), world)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3 x fp32 scales) + fp8 slice, fp32 acc",
+                "data": "synthetic (seeded CUDA generator; shapes and distributions of the pages' OLMo-2 370M linears)",
+                "config": {"workload": WORKLOAD, "tokens": TOKENS, "outlier_pct": OUTLIER_PCT,
+                           "osci_reset_params": osci.n, "parallelism": "replicas" if world > 1 else "single GPU",
+                           "l2": "no flush: per-step working set ~13 GB (OsciReset state 10.8 GB) >> 129 MB L2"},
+                "linear_ms_per_step": round(lin_ms / args.steps, 4),
+                "osci_reset": {"ms": round(osci_ms, 4), "GB/s": round(osci_gbs, 1), "frac": round(osci_gbs / hbm_peak, 3)},
+                "roofline": roof, "parts": parts, "gpu_launches": launches, "clocks": clk}
+        line.update(extras)
+        if e2e is not None:
+            line["e2e"] = e2e
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(tj, linears, stream, steps, world):
+    """Same metric through the public API with host buffers: X and dY of every linear copied
+    host->device from pinned memory and every dW copied back, inside the timed region."""
+    hx = [l.X.cpu().pin_memory() for l in linears]
+    hdy = [l.dY.cpu().pin_memory() for l in linears]
+    hdw = [torch.empty(l.dW.shape, dtype=l.dW.dtype).pin_memory() for l in linears]
+    h2d = sum(t.numel() * t.element_size() for t in hx + hdy)
+    d2h = sum(t.numel() * t.element_size() for t in hdw)
+    dummy = Timeline(stream)
+
+    def one(seed):
+        with torch.cuda.stream(stream):
+            for i, l in enumerate(linears):
+                l.X.copy_(hx[i], non_blocking=True)
+                l.dY.copy_(hdy[i], non_blocking=True)
+                l.run(tj, seed, dummy, stream)
+                hdw[i].copy_(l.dW, non_blocking=True)
+
+    for w in range(2):
+        one(5000 + w)
+    torch.cuda.synchronize()
+    barrier(world)
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for t in range(steps):
+        one(6000 + t)
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(world, s.elapsed_time(e))
+    flops = world * sum(l.flops for l in linears) * steps
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 4)}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

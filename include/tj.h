@@ -10,8 +10,11 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
  *     never allocates or frees device memory; scratch space is passed in as
  *     `workspace` with its size from tj_workspace_size().
- *   - Pointers must be 16-byte aligned and leading dimensions (`ld`, in
- *     elements) multiples of 8; violations return TJ_ERR_ALIGN before any launch.
+ *   - Dense bf16/fp32 inputs (x, dy) need only their element alignment; rows that
+ *     start on 64-byte boundaries (ld a multiple of 32) take a vectorised load path.
+ *     Every other pointer (quantized tensors, outputs, workspace) must be 16-byte
+ *     aligned (the workspace 256-byte); violations return TJ_ERR_ALIGN before any
+ *     launch.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and never synchronize.  Argument/shape errors are detected on the
  *     host before any launch and leave outputs untouched; a failed launch maps to

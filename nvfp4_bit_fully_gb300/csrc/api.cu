@@ -12,6 +12,11 @@ using namespace tj;
 namespace {
 
 inline bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+// Dense inputs need only their element alignment (the kernels take a vectorised
+// path by themselves when rows are 64-byte aligned).
+inline bool al_elem(const void *p, int dtype) {
+    return (reinterpret_cast<uintptr_t>(p) & (dtype == TJ_FP32 ? 3 : 1)) == 0;
+}
 
 tj_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TJ_OK : TJ_ERR_CUDA; }
 
@@ -103,7 +108,7 @@ tj_status tj_quantize_nvfp4(const void *x, int dtype, int64_t rows_x, int64_t co
                             uint32_t rht_tag, tj_nvfp4 *out, void *stream) {
     if (rows_x < 0 || cols_x < 0 || (mode != TJ_RTN && mode != TJ_SR) || out == nullptr) return TJ_ERR_INVALID_ARG;
     if (!dense_ok(x, dtype, ld, cols_x)) return TJ_ERR_INVALID_ARG;
-    if (!al16(x) || (ld % 8) != 0) return TJ_ERR_ALIGN;
+    if (!al_elem(x, dtype)) return TJ_ERR_ALIGN;
     const int64_t ncols = sel ? n_sel : cols_x;
     if (sel && (n_sel < 0 || n_sel > cols_x)) return TJ_ERR_SHAPE;
     const int64_t orows = along_cols ? ncols : rows_x, ocols = along_cols ? rows_x : ncols;
@@ -117,7 +122,7 @@ tj_status tj_quantize_mxfp8(const void *x, int dtype, int64_t rows_x, int64_t co
                             const int32_t *sel, int64_t n_sel, tj_mxfp8 *out, void *stream) {
     if (rows_x < 0 || cols_x < 0 || out == nullptr) return TJ_ERR_INVALID_ARG;
     if (!dense_ok(x, dtype, ld, cols_x)) return TJ_ERR_INVALID_ARG;
-    if (!al16(x) || (ld % 8) != 0) return TJ_ERR_ALIGN;
+    if (!al_elem(x, dtype)) return TJ_ERR_ALIGN;
     const int64_t ncols = sel ? n_sel : cols_x;
     if (sel && (n_sel < 0 || n_sel > cols_x)) return TJ_ERR_SHAPE;
     const int64_t orows = along_cols ? ncols : rows_x, ocols = along_cols ? rows_x : ncols;
@@ -195,7 +200,7 @@ tj_status tj_linear_fwd(const void *x, int64_t M, int64_t K, int64_t ldx, const 
     if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
     if (k > 0 && (normal_idx == nullptr || outlier_idx == nullptr || w8 == nullptr || x8 == nullptr))
         return TJ_ERR_INVALID_ARG;
-    if (!al16(x) || (ldx % 8) != 0 || !al16(y)) return TJ_ERR_ALIGN;
+    if (!al_elem(x, TJ_BF16) || !al16(y)) return TJ_ERR_ALIGN;
     if (ldx < K) return TJ_ERR_SHAPE;
     const int64_t kn = K - k, N = wq->rows;
     tj_status st = check_nv(wq, N, kn);
@@ -218,7 +223,7 @@ tj_status tj_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, c
     if (dy == nullptr || wq == nullptr || dx == nullptr || M < 0 || N < 0 || k < 0) return TJ_ERR_INVALID_ARG;
     if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
     if (k > 0 && (normal_idx == nullptr || outlier_idx == nullptr || w8 == nullptr)) return TJ_ERR_INVALID_ARG;
-    if (!al16(dy) || (lddy % 8) != 0 || !al16(dx)) return TJ_ERR_ALIGN;
+    if (!al_elem(dy, TJ_BF16) || !al16(dx)) return TJ_ERR_ALIGN;
     const int64_t kn = wq->cols, K = kn + k;
     tj_status st = check_nv(wq, N, kn);
     if (st == TJ_OK && k > 0) st = check_mx(w8, N, k);
@@ -252,7 +257,7 @@ tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, c
                            uint64_t seed, float *dw, int64_t lddw, void *workspace, size_t ws_bytes, void *stream) {
     if (dy == nullptr || xq == nullptr || dw == nullptr || M < 0 || N < 0 || k < 0) return TJ_ERR_INVALID_ARG;
     if (k > 0 && (normal_idx == nullptr || outlier_idx == nullptr || x8 == nullptr)) return TJ_ERR_INVALID_ARG;
-    if (!al16(dy) || (lddy % 8) != 0 || !al16(dw)) return TJ_ERR_ALIGN;
+    if (!al_elem(dy, TJ_BF16) || !al16(dw)) return TJ_ERR_ALIGN;
     const int64_t kn = xq->cols, K = kn + k;
     tj_status st = check_nv(xq, M, kn);
     if (st == TJ_OK && k > 0) st = check_mx(x8, M, k);
@@ -288,7 +293,7 @@ tj_status tj_outlier_calibrate(const void *x, int dtype, int64_t M, int64_t K, i
     if (x != nullptr) {
         if (dtype != TJ_BF16 && dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
         if (ld < K || M > ((int64_t)1 << 20)) return TJ_ERR_SHAPE;
-        if (!al16(x)) return TJ_ERR_ALIGN;
+        if (!al_elem(x, dtype)) return TJ_ERR_ALIGN;
         TJ_TRY(launch_calib_accumulate(x, dtype, M, K, ld, sumsq, s));
     }
     if (finalize) {

@@ -103,3 +103,66 @@ def layer_set_linear(name, N, K, seed=3, M=16384):
 def cosine_lr(step, total=200, lr_max=1e-3, lr_min=1e-5):
     """Cosine-decayed learning rate of the synthetic AdamW trajectory."""
     return lr_min + 0.5 * (lr_max - lr_min) * (1.0 + math.cos(math.pi * step / total))
+
+
+# ---------------------------------------------------------------------------
+# Device-side generation for the benchmark (same distributions, drawn with a
+# seeded CUDA generator so that multi-GB inputs appear in seconds).
+# ---------------------------------------------------------------------------
+OSCI_PARAMS = 22 * sum(n * k for _, n, k in LAYER_SET)       # 369,098,752 master weights
+
+
+def _cuda_gen(seed, stream, device):
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000003 + int(stream))
+    return g
+
+
+def device_heavy_columns(shape, std, factor, count, seed, stream, device):
+    g = _cuda_gen(seed, stream, device)
+    x = torch.randn(*shape, generator=g, device=device, dtype=torch.float32) * std
+    cols = torch.randperm(shape[1], generator=g, device=device)[:count]
+    x[:, cols] *= factor
+    return x.to(torch.bfloat16)
+
+
+def device_student_t_rows(rows, cols, scale, nu, seed, stream, device):
+    g = _cuda_gen(seed, stream, device)
+    z = torch.randn(rows, generator=g, device=device, dtype=torch.float64)
+    chi2 = (torch.randn(rows, nu, generator=g, device=device, dtype=torch.float64) ** 2).sum(dim=1)
+    t = (z / torch.sqrt(chi2 / nu)).abs().to(torch.float32)
+    out = torch.empty(rows, cols, dtype=torch.bfloat16, device=device)
+    for r0 in range(0, rows, 4096):                      # chunked: bounded fp32 temporaries
+        r1 = min(rows, r0 + 4096)
+        out[r0:r1] = (torch.randn(r1 - r0, cols, generator=g, device=device) * (scale * t[r0:r1, None])).to(torch.bfloat16)
+    return out
+
+
+def device_layer_set_linear(name, N, K, seed=3, M=16384, device="cuda"):
+    """(X [M,K], W [N,K], dY [M,N]) of one linear of the layer set, on the device."""
+    s = 40 + 10 * [n for n, _, _ in LAYER_SET].index(name)
+    X = device_heavy_columns((M, K), 1.0, 30.0, math.ceil(K / 100), seed, s, device)
+    g = _cuda_gen(seed, s + 1, device)
+    W = (torch.randn(N, K, generator=g, device=device) * 0.02).to(torch.bfloat16)
+    dY = device_student_t_rows(M, N, 1e-3, 3, seed, s + 2, device)
+    return X, W, dY
+
+
+def device_calibration_batch(K, M, heavy_count, b, seed, stream, device):
+    """A calibration batch X [M,K] N(0,1) whose heavy channels (fixed per stream) are x40."""
+    g = _cuda_gen(seed, stream, device)
+    heavy = torch.randperm(K, generator=g, device=device)[:heavy_count]
+    g2 = _cuda_gen(seed, stream + 100 + b, device)
+    x = torch.randn(M, K, generator=g2, device=device)
+    x[:, heavy] *= 40.0
+    return x.to(torch.bfloat16)
+
+
+def device_master_weights(n, seed=3, device="cuda", cols=1024):
+    """OsciReset master weights w0 ~ N(0, 0.02) as [n/cols, cols] fp32."""
+    g = _cuda_gen(seed, 900, device)
+    w = torch.empty(n // cols, cols, dtype=torch.float32, device=device)
+    for r0 in range(0, w.shape[0], 65536):
+        r1 = min(w.shape[0], r0 + 65536)
+        w[r0:r1].normal_(0.0, 0.02, generator=g)
+    return w
