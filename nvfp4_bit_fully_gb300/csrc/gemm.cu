@@ -11,13 +11,17 @@
 // The FP8 slice (kind::mxf8f6f4, UE8M0 per 32) has only power-of-two scales and
 // accumulates over its whole K into one tensor-memory buffer added at the end.
 //
-// CTA = 128 x 128 output tile, 10 warps:
+// Persistent CTAs (one per SM) walk the 128 x 128 output tiles; 12 warps:
 //   warp 0     TMA producer (one lane): operand tiles (128 B rows, 128-byte swizzle)
-//              and scale-factor tiles (bulk copies) into a 4-stage ring;
+//              and scale-factor tiles into a 3-stage ring, and the FP32 outer
+//              scales of every 128-K block into an 8-slot ring (bulk copies);
 //   warp 1     tensor-memory owner and MMA issuer (one lane): tcgen05.cp of the
 //              scale tiles, tcgen05.mma into the double-buffered partials;
-//   warps 2-9  promotion + epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
-//              (its rows) and columns 64*((w-2)/4) .. +63.
+//   warps 2-9  promotion: warp w reads TMEM lanes 32*(w%4) .. +31 (its rows) and
+//              columns 64*((w-2)/4) .. +63, accumulates in registers with packed
+//              f32x2 FMAs, and hands the finished tile to a padded staging buffer;
+//   warps 10-11 stores: coalesced row writes of the staged tile (bf16 / fp32,
+//              optional column scatter), overlapping the next tile's promotion.
 // Tensor memory (512 columns): P0 [0,128), P1 [128,256), FP8 accumulator
 // [256,384), scale factors 32 columns per ring slot [384,512).
 // Every mbarrier wait is bounded; a wait that runs out sets the sticky device
@@ -39,22 +43,27 @@ __device__ unsigned int g_tj_dev_error = 0u;
 
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 3;                     // operand ring (2 x 128-K blocks per stage)
+constexpr int kScaleSlots = 8;                 // FP32 outer-scale ring (one 128-K block per slot)
 constexpr int kTileBytes = 128 * 128;          // one operand tile: 128 rows x 128 bytes
 constexpr int kSfStageBytes = 2048;            // 4 scale tiles of 512 bytes
+constexpr int kStageRow = 132;                 // staging row stride in floats (bank-conflict padding)
 constexpr int kSmemA = 0;
 constexpr int kSmemB = kSmemA + kStages * kTileBytes;
 constexpr int kSmemSfa = kSmemB + kStages * kTileBytes;
 constexpr int kSmemSfb = kSmemSfa + kStages * kSfStageBytes;
-constexpr int kSmemBar = kSmemSfb + kStages * kSfStageBytes;
-constexpr int kSmemBytes = kSmemBar + 256;
-constexpr int kThreadsGemm = 320;
+constexpr int kSmemOuter = kSmemSfb + kStages * kSfStageBytes;      // [slot][A 128 | B 128] floats
+constexpr int kSmemStage = kSmemOuter + kScaleSlots * 1024;        // 128 x kStageRow floats
+constexpr int kSmemBar = kSmemStage + 128 * kStageRow * 4;
+constexpr int kSmemBytes = kSmemBar + 512;
+constexpr int kThreadsGemm = 384;
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColP = 0, kColAcc8 = 256, kColSf = 384;
 
 struct GemmArgs {
     int64_t M, N;                 // logical output size
+    int tiles_m, tiles_n;         // 128 x 128 output tiles
     int nkb4;                     // 128-K blocks of the FP4 part (0: none)
     int nk8;                      // 128-K stages of the FP8 part (0: none)
     const uint8_t *sfa4, *sfb4;   // scale tiles, FP4 operands
@@ -71,7 +80,10 @@ struct GemmArgs {
 };
 
 struct Bars {
-    uint64_t full[kStages], empty[kStages], pfull[2], pempty[2], acc8, drain;
+    uint64_t full[kStages], empty[kStages];
+    uint64_t pfull[2], pempty[2];
+    uint64_t sfull[kScaleSlots], sempty[kScaleSlots];
+    uint64_t a8full, a8empty, stfull, stempty, drain;
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -99,16 +111,14 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, Bar
     return false;
 }
 
-// Warp-uniform bounded wait: lane 0 waits, the verdict is broadcast, and on
-// success every lane observes the completed phase (an immediate re-check)
-// before the warp-collective tensor-memory loads that follow.
+// Warp-uniform bounded wait: every lane waits (lane 0 first), the verdict is
+// agreed by vote, so warp-collective operations that follow see one decision.
 __device__ __forceinline__ bool warp_wait_bounded(uint64_t *bar, uint32_t parity, Bars *bars, int lane) {
     int ok = 0;
     if (lane == 0) ok = wait_bounded(bar, parity, bars) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok && lane != 0) ok = wait_bounded(bar, parity, bars) ? 1 : 0;
-    ok = __all_sync(0xffffffffu, ok);
-    return ok != 0;
+    return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // Instruction descriptors (bits: 4-5 B scale id, 7-9 A format, 10-12 B format,
@@ -122,6 +132,26 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t sf_id) {
            (sf_id << 29);
 }
 
+// Packed fp32 pair helpers (two accumulator columns per instruction).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    return ((uint64_t)__float_as_uint(hi) << 32) | (uint64_t)__float_as_uint(lo);
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __global__ void __launch_bounds__(kThreadsGemm, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tm_a4, const __grid_constant__ CUtensorMap tm_b4,
                  const __grid_constant__ CUtensorMap tm_a8, const __grid_constant__ CUtensorMap tm_b8,
@@ -129,8 +159,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars *bars = reinterpret_cast<Bars *>(smem + kSmemBar);
+    float *outer_s = reinterpret_cast<float *>(smem + kSmemOuter);
+    float *stage_s = reinterpret_cast<float *>(smem + kSmemStage);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t m0 = (int64_t)blockIdx.y * 128, n0 = (int64_t)blockIdx.x * 128;
+    const int ntiles = args.tiles_m * args.tiles_n;
     const int nst4 = (args.nkb4 + 1) / 2;
     const int nstages = nst4 + args.nk8;
 
@@ -143,7 +175,14 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             ptx::mbar_init(&bars->pfull[p], 1);
             ptx::mbar_init(&bars->pempty[p], 8);
         }
-        ptx::mbar_init(&bars->acc8, 1);
+        for (int s = 0; s < kScaleSlots; ++s) {
+            ptx::mbar_init(&bars->sfull[s], 1);
+            ptx::mbar_init(&bars->sempty[s], 8);
+        }
+        ptx::mbar_init(&bars->a8full, 1);
+        ptx::mbar_init(&bars->a8empty, 8);
+        ptx::mbar_init(&bars->stfull, 8);
+        ptx::mbar_init(&bars->stempty, 2);
         ptx::mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         ptx::fence_mbar_init();
@@ -159,170 +198,246 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         if (lane == 0) {
             if (args.nkb4 > 0) { ptx::prefetch_tmap(&tm_a4); ptx::prefetch_tmap(&tm_b4); }
             if (args.nk8 > 0) { ptx::prefetch_tmap(&tm_a8); ptx::prefetch_tmap(&tm_b8); }
-            const int64_t rta = m0 / 128, rtb = n0 / 128;
-            int it = 0;
-            for (; it < nstages; ++it) {
-                const int slot = it % kStages;
-                if (it >= kStages && !wait_bounded(&bars->empty[slot], ((it / kStages) - 1) & 1, bars)) break;
-                uint8_t *sa = smem + kSmemA + slot * kTileBytes;
-                uint8_t *sb = smem + kSmemB + slot * kTileBytes;
-                uint8_t *sfa = smem + kSmemSfa + slot * kSfStageBytes;
-                uint8_t *sfb = smem + kSmemSfb + slot * kSfStageBytes;
-                if (it < nst4) {
-                    const int nkbs = min(2, args.nkb4 - 2 * it);
-                    const uint32_t sfbytes = (uint32_t)nkbs * 1024u;
-                    ptx::mbar_arrive_expect_tx(&bars->full[slot], 2u * kTileBytes + 2u * sfbytes);
-                    ptx::tma_load_2d(sa, &tm_a4, it * 128, (int32_t)m0, &bars->full[slot]);
-                    ptx::tma_load_2d(sb, &tm_b4, it * 128, (int32_t)n0, &bars->full[slot]);
-                    ptx::bulk_load(sfa, args.sfa4 + (rta * args.ntk_a4 + 4 * it) * 512, sfbytes, &bars->full[slot]);
-                    ptx::bulk_load(sfb, args.sfb4 + (rtb * args.ntk_b4 + 4 * it) * 512, sfbytes, &bars->full[slot]);
-                } else {
-                    const int s8 = it - nst4;
-                    ptx::mbar_arrive_expect_tx(&bars->full[slot], 2u * kTileBytes + 1024u);
-                    ptx::tma_load_2d(sa, &tm_a8, s8 * 128, (int32_t)m0, &bars->full[slot]);
-                    ptx::tma_load_2d(sb, &tm_b8, s8 * 128, (int32_t)n0, &bars->full[slot]);
-                    ptx::bulk_load(sfa, args.sfa8 + (rta * args.ntk_a8 + s8) * 512, 512u, &bars->full[slot]);
-                    ptx::bulk_load(sfb, args.sfb8 + (rtb * args.ntk_b8 + s8) * 512, 512u, &bars->full[slot]);
+            int it = 0, sk = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                const int64_t m0 = (int64_t)(tile / args.tiles_n) * 128, n0 = (int64_t)(tile % args.tiles_n) * 128;
+                const int64_t rta = m0 / 128, rtb = n0 / 128;
+                for (int st = 0; st < nstages; ++st, ++it) {
+                    const int slot = it % kStages;
+                    if (it >= kStages && !wait_bounded(&bars->empty[slot], ((it / kStages) - 1) & 1, bars)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sa = smem + kSmemA + slot * kTileBytes;
+                    uint8_t *sb = smem + kSmemB + slot * kTileBytes;
+                    uint8_t *sfa = smem + kSmemSfa + slot * kSfStageBytes;
+                    uint8_t *sfb = smem + kSmemSfb + slot * kSfStageBytes;
+                    if (st < nst4) {
+                        const int nkbs = min(2, args.nkb4 - 2 * st);
+                        const uint32_t sfbytes = (uint32_t)nkbs * 1024u;
+                        ptx::mbar_arrive_expect_tx(&bars->full[slot], 2u * kTileBytes + 2u * sfbytes);
+                        ptx::tma_load_2d(sa, &tm_a4, st * 128, (int32_t)m0, &bars->full[slot]);
+                        ptx::tma_load_2d(sb, &tm_b4, st * 128, (int32_t)n0, &bars->full[slot]);
+                        ptx::bulk_load(sfa, args.sfa4 + (rta * args.ntk_a4 + 4 * st) * 512, sfbytes, &bars->full[slot]);
+                        ptx::bulk_load(sfb, args.sfb4 + (rtb * args.ntk_b4 + 4 * st) * 512, sfbytes, &bars->full[slot]);
+                        // the FP32 outer scales of these blocks, for the promotion warps
+                        for (int j = 0; j < nkbs && ok; ++j, ++sk) {
+                            const int ss = sk % kScaleSlots;
+                            if (sk >= kScaleSlots &&
+                                !wait_bounded(&bars->sempty[ss], ((sk / kScaleSlots) - 1) & 1, bars)) {
+                                ok = false;
+                                break;
+                            }
+                            const int64_t kb = 2 * st + j;
+                            ptx::mbar_arrive_expect_tx(&bars->sfull[ss], 1024u);
+                            ptx::bulk_load(outer_s + ss * 256, args.outa + kb * args.rpa + m0, 512u, &bars->sfull[ss]);
+                            ptx::bulk_load(outer_s + ss * 256 + 128, args.outb + kb * args.rpb + n0, 512u,
+                                           &bars->sfull[ss]);
+                        }
+                        if (!ok) { ++it; break; }
+                    } else {
+                        const int s8 = st - nst4;
+                        ptx::mbar_arrive_expect_tx(&bars->full[slot], 2u * kTileBytes + 1024u);
+                        ptx::tma_load_2d(sa, &tm_a8, s8 * 128, (int32_t)m0, &bars->full[slot]);
+                        ptx::tma_load_2d(sb, &tm_b8, s8 * 128, (int32_t)n0, &bars->full[slot]);
+                        ptx::bulk_load(sfa, args.sfa8 + (rta * args.ntk_a8 + s8) * 512, 512u, &bars->full[slot]);
+                        ptx::bulk_load(sfb, args.sfb8 + (rtb * args.ntk_b8 + s8) * 512, 512u, &bars->full[slot]);
+                    }
                 }
             }
-            // drain: every fill issued must have landed before the CTA exits
+            // drain: every copy issued must have landed before the CTA exits
             for (int j = (it > kStages ? it - kStages : 0); j < it; ++j)
                 wait_bounded(&bars->full[j % kStages], (j / kStages) & 1, bars);
+            for (int j = (sk > kScaleSlots ? sk - kScaleSlots : 0); j < sk; ++j)
+                wait_bounded(&bars->sfull[j % kScaleSlots], (j / kScaleSlots) & 1, bars);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc4 = idesc_nvf4();
-            int pcount = 0;
+            int it = 0, pcount = 0, a8count = 0;
             bool ok = true;
-            for (int it = 0; it < nstages && ok; ++it) {
-                const int slot = it % kStages;
-                if (!wait_bounded(&bars->full[slot], (it / kStages) & 1, bars)) { ok = false; break; }
-                ptx::tc_fence_after();
-                const uint32_t sa = ptx::smem_u32(smem + kSmemA + slot * kTileBytes);
-                const uint32_t sb = ptx::smem_u32(smem + kSmemB + slot * kTileBytes);
-                const uint32_t sfa = ptx::smem_u32(smem + kSmemSfa + slot * kSfStageBytes);
-                const uint32_t sfb = ptx::smem_u32(smem + kSmemSfb + slot * kSfStageBytes);
-                const uint32_t sfcol = tbase + kColSf + 32u * slot;
-                if (it < nst4) {
-                    const int nkbs = min(2, args.nkb4 - 2 * it);
-                    for (int j = 0; j < 2 * nkbs; ++j) {   // one 512-byte scale tile per K = 64 MMA
-                        ptx::tc_cp_32x128b_warpx4(sfcol + 4 * j, ptx::smem_desc(sfa + 512 * j, 0, 128, 0));
-                        ptx::tc_cp_32x128b_warpx4(sfcol + 16 + 4 * j, ptx::smem_desc(sfb + 512 * j, 0, 128, 0));
-                    }
-                    for (int kbl = 0; kbl < nkbs; ++kbl) {
-                        const int pb = pcount & 1;
-                        if (pcount >= 2 && !wait_bounded(&bars->pempty[pb], ((pcount >> 1) - 1) & 1, bars)) {
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                for (int st = 0; st < nstages; ++st, ++it) {
+                    const int slot = it % kStages;
+                    if (!wait_bounded(&bars->full[slot], (it / kStages) & 1, bars)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_u32(smem + kSmemA + slot * kTileBytes);
+                    const uint32_t sb = ptx::smem_u32(smem + kSmemB + slot * kTileBytes);
+                    const uint32_t sfa = ptx::smem_u32(smem + kSmemSfa + slot * kSfStageBytes);
+                    const uint32_t sfb = ptx::smem_u32(smem + kSmemSfb + slot * kSfStageBytes);
+                    const uint32_t sfcol = tbase + kColSf + 32u * slot;
+                    if (st < nst4) {
+                        const int nkbs = min(2, args.nkb4 - 2 * st);
+                        for (int j = 0; j < 2 * nkbs; ++j) {   // one 512-byte scale tile per K = 64 MMA
+                            ptx::tc_cp_32x128b_warpx4(sfcol + 4 * j, ptx::smem_desc(sfa + 512 * j, 0, 128, 0));
+                            ptx::tc_cp_32x128b_warpx4(sfcol + 16 + 4 * j, ptx::smem_desc(sfb + 512 * j, 0, 128, 0));
+                        }
+                        for (int kbl = 0; kbl < nkbs; ++kbl) {
+                            const int pb = pcount & 1;
+                            if (pcount >= 2 && !wait_bounded(&bars->pempty[pb], ((pcount >> 1) - 1) & 1, bars)) {
+                                ok = false;
+                                break;
+                            }
+                            ptx::tc_fence_after();
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                const uint32_t koff = 64u * kbl + 32u * j;
+                                ptx::mma_nvf4(tbase + kColP + 128u * pb, ptx::smem_desc(sa + koff, 16, 1024, 2),
+                                              ptx::smem_desc(sb + koff, 16, 1024, 2), idesc4,
+                                              sfcol + 4 * (2 * kbl + j), sfcol + 16 + 4 * (2 * kbl + j), (uint32_t)j);
+                            }
+                            ptx::tc_commit(&bars->pfull[pb]);
+                            ++pcount;
+                        }
+                        if (!ok) break;
+                    } else {
+                        const int s8 = st - nst4;
+                        if (s8 == 0 && a8count >= 1 &&
+                            !wait_bounded(&bars->a8empty, (a8count - 1) & 1, bars)) {
                             ok = false;
                             break;
                         }
                         ptx::tc_fence_after();
+                        ptx::tc_cp_32x128b_warpx4(sfcol, ptx::smem_desc(sfa, 0, 128, 0));
+                        ptx::tc_cp_32x128b_warpx4(sfcol + 16, ptx::smem_desc(sfb, 0, 128, 0));
 #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            const uint32_t koff = 64u * kbl + 32u * j;
-                            ptx::mma_nvf4(tbase + kColP + 128u * pb, ptx::smem_desc(sa + koff, 16, 1024, 2),
-                                          ptx::smem_desc(sb + koff, 16, 1024, 2), idesc4, sfcol + 4 * (2 * kbl + j),
-                                          sfcol + 16 + 4 * (2 * kbl + j), (uint32_t)j);
+                        for (int j = 0; j < 4; ++j) {
+                            ptx::mma_mxf8(tbase + kColAcc8, ptx::smem_desc(sa + 32u * j, 16, 1024, 2),
+                                          ptx::smem_desc(sb + 32u * j, 16, 1024, 2), idesc_mxf8((uint32_t)j), sfcol,
+                                          sfcol + 16, (uint32_t)(s8 > 0 || j > 0));
                         }
-                        ptx::tc_commit(&bars->pfull[pb]);
-                        ++pcount;
+                        if (s8 == args.nk8 - 1) {
+                            ptx::tc_commit(&bars->a8full);
+                            ++a8count;
+                        }
                     }
-                    if (!ok) break;
-                } else {
-                    const int s8 = it - nst4;
-                    ptx::tc_cp_32x128b_warpx4(sfcol, ptx::smem_desc(sfa, 0, 128, 0));
-                    ptx::tc_cp_32x128b_warpx4(sfcol + 16, ptx::smem_desc(sfb, 0, 128, 0));
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        ptx::mma_mxf8(tbase + kColAcc8, ptx::smem_desc(sa + 32u * j, 16, 1024, 2),
-                                      ptx::smem_desc(sb + 32u * j, 16, 1024, 2), idesc_mxf8((uint32_t)j), sfcol,
-                                      sfcol + 16, (uint32_t)(s8 > 0 || j > 0));
-                    }
+                    ptx::tc_commit(&bars->empty[slot]);
                 }
-                ptx::tc_commit(&bars->empty[slot]);
             }
-            if (ok && args.nk8 > 0) ptx::tc_commit(&bars->acc8);
             // drain: all MMAs / copies issued by this thread complete before TMEM is freed
             ptx::tc_commit(&bars->drain);
             wait_bounded(&bars->drain, 0, bars);
         }
-    } else {
-        // ------------------------------------------------------------ promotion + epilogue
+    } else if (warp < 10) {
+        // ------------------------------------------------------------ promotion
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
         const int h = (warp - 2) >> 2;          // column half
         const int row_l = 32 * q + lane;
         const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-        float acc[64];
-#pragma unroll
-        for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+        int kbc = 0, a8c = 0, tc = 0;
         bool ok = true;
-        for (int kb = 0; kb < args.nkb4; ++kb) {
-            const int pb = kb & 1;
-            const float sa = args.outa[(int64_t)kb * args.rpa + m0 + row_l] * args.alpha;
-            if (!warp_wait_bounded(&bars->pfull[pb], (kb >> 1) & 1, bars, lane)) { ok = false; break; }
-            ptx::tc_fence_after();
-            uint32_t p0[32], p1[32];
-            ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColP + 128u * pb + 64u * h, p0);
-            ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColP + 128u * pb + 64u * h + 32u, p1);
-            ptx::tmem_wait_ld();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&bars->pempty[pb]);
-            const float4 *sbp = reinterpret_cast<const float4 *>(args.outb + (int64_t)kb * args.rpb + n0 + 64 * h);
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tc) {
+            uint64_t acc[32];                  // 64 fp32 accumulators as packed pairs
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float sbv[32];
+            for (int j = 0; j < 32; ++j) acc[j] = 0ull;
+            for (int kb = 0; kb < args.nkb4; ++kb, ++kbc) {
+                const int pb = kbc & 1;
+                const int ss = kbc % kScaleSlots;
+                if (!warp_wait_bounded(&bars->pfull[pb], (kbc >> 1) & 1, bars, lane)) { ok = false; break; }
+                ptx::tc_fence_after();
+                uint32_t p0[32], p1[32];
+                ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColP + 128u * pb + 64u * h, p0);
+                ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColP + 128u * pb + 64u * h + 32u, p1);
+                ptx::tmem_wait_ld();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&bars->pempty[pb]);
+                if (!warp_wait_bounded(&bars->sfull[ss], (kbc / kScaleSlots) & 1, bars, lane)) { ok = false; break; }
+                const float sa = outer_s[ss * 256 + row_l] * args.alpha;
+                const uint64_t sa2 = pack2(sa, sa);
+                const float4 *sbp = reinterpret_cast<const float4 *>(outer_s + ss * 256 + 128 + 64 * h);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 f = __ldg(sbp + 8 * c + i);
-                    sbv[4 * i] = f.x; sbv[4 * i + 1] = f.y; sbv[4 * i + 2] = f.z; sbv[4 * i + 3] = f.w;
+                for (int i = 0; i < 16; ++i) {
+                    const float4 sbv = sbp[i];            // broadcast read: all lanes, same address
+                    const uint64_t c01 = mul2(sa2, pack2(sbv.x, sbv.y));
+                    const uint64_t c23 = mul2(sa2, pack2(sbv.z, sbv.w));
+                    const int j = 4 * i;   // columns j .. j+3 of this half
+                    const uint32_t *pp = j < 32 ? p0 : p1;
+                    const int jj = j & 31;
+                    acc[2 * i] = fma2(pack2(__uint_as_float(pp[jj]), __uint_as_float(pp[jj + 1])), c01, acc[2 * i]);
+                    acc[2 * i + 1] =
+                        fma2(pack2(__uint_as_float(pp[jj + 2]), __uint_as_float(pp[jj + 3])), c23, acc[2 * i + 1]);
                 }
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float pv = __uint_as_float(c == 0 ? p0[j] : p1[j]);
-                    acc[32 * c + j] = fmaf(pv, sa * sbv[j], acc[32 * c + j]);
-                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&bars->sempty[ss]);
             }
-        }
-        if (ok && args.nk8 > 0) {
-            if (warp_wait_bounded(&bars->acc8, 0, bars, lane)) {
+            if (!ok) break;
+            if (args.nk8 > 0) {
+                if (!warp_wait_bounded(&bars->a8full, a8c & 1, bars, lane)) { ok = false; break; }
                 ptx::tc_fence_after();
                 uint32_t p0[32], p1[32];
                 ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColAcc8 + 64u * h, p0);
                 ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColAcc8 + 64u * h + 32u, p1);
                 ptx::tmem_wait_ld();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&bars->a8empty);
+                ++a8c;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    acc[j] += __uint_as_float(p0[j]);
-                    acc[32 + j] += __uint_as_float(p1[j]);
+                for (int i = 0; i < 16; ++i) {
+                    acc[i] = add2(acc[i], pack2(__uint_as_float(p0[2 * i]), __uint_as_float(p0[2 * i + 1])));
+                    acc[16 + i] = add2(acc[16 + i], pack2(__uint_as_float(p1[2 * i]), __uint_as_float(p1[2 * i + 1])));
                 }
             }
+            // hand the tile to the store warps through the padded staging buffer
+            if (tc >= 1 && !warp_wait_bounded(&bars->stempty, (tc - 1) & 1, bars, lane)) { ok = false; break; }
+            float4 *dst = reinterpret_cast<float4 *>(stage_s + row_l * kStageRow + 64 * h);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint64_t a = acc[2 * i], b = acc[2 * i + 1];
+                dst[i] = make_float4(__uint_as_float((uint32_t)a), __uint_as_float((uint32_t)(a >> 32)),
+                                     __uint_as_float((uint32_t)b), __uint_as_float((uint32_t)(b >> 32)));
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bars->stfull);
         }
-        // epilogue: row-major D, optional column scatter
-        const int64_t row = m0 + row_l;
-        if (row < args.M && !bars->abort_flag) {
-            const int64_t nb = n0 + 64 * h;
-            if (args.col_map == nullptr && nb + 64 <= args.N && !args.out_bf16 && (args.ldd & 3) == 0) {
-                float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(args.d) + row * args.ldd + nb);
+    } else {
+        // ------------------------------------------------------------ stores (warps 10, 11)
+        const int sw = warp - 10;
+        int tc = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tc) {
+            if (!warp_wait_bounded(&bars->stfull, tc & 1, bars, lane)) break;
+            const int64_t m0 = (int64_t)(tile / args.tiles_n) * 128, n0 = (int64_t)(tile % args.tiles_n) * 128;
+            const int64_t n = n0 + 4 * lane;
+            const bool full4 = n + 4 <= args.N && (args.ldd & 3) == 0;
+            int64_t cols[4];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-            } else {
+            for (int c = 0; c < 4; ++c) cols[c] = args.col_map ? (n + c < args.N ? (int64_t)args.col_map[n + c] : -1) : n + c;
+#pragma unroll 4
+            for (int r = sw; r < 128; r += 2) {
+                const int64_t row = m0 + r;
+                if (row >= args.M) break;
+                const float4 v = *reinterpret_cast<const float4 *>(stage_s + r * kStageRow + 4 * lane);
+                if (args.col_map == nullptr && full4) {
+                    if (args.out_bf16) {
+                        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+                        uint2 u;
+                        u.x = *reinterpret_cast<uint32_t *>(&lo);
+                        u.y = *reinterpret_cast<uint32_t *>(&hi);
+                        *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(args.d) + row * args.ldd + n) = u;
+                    } else {
+                        *reinterpret_cast<float4 *>(static_cast<float *>(args.d) + row * args.ldd + n) = v;
+                    }
+                } else {
+                    const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const int64_t n = nb + j;
-                    if (n < args.N) {
-                        const int64_t col = args.col_map ? (int64_t)args.col_map[n] : n;
-                        if (args.out_bf16)
-                            static_cast<__nv_bfloat16 *>(args.d)[row * args.ldd + col] = __float2bfloat16_rn(acc[j]);
-                        else
-                            static_cast<float *>(args.d)[row * args.ldd + col] = acc[j];
+                    for (int c = 0; c < 4; ++c) {
+                        if (n + c < args.N) {
+                            if (args.out_bf16)
+                                static_cast<__nv_bfloat16 *>(args.d)[row * args.ldd + cols[c]] = __float2bfloat16_rn(vv[c]);
+                            else
+                                static_cast<float *>(args.d)[row * args.ldd + cols[c]] = vv[c];
+                        }
                     }
                 }
             }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bars->stempty);
         }
-        ptx::tc_fence_before();
     }
+    ptx::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
@@ -330,9 +445,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     }
 }
 
+}  // namespace
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
+namespace {
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -414,8 +533,18 @@ cudaError_t launch_gemm(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8
         if (!make_tile_map(&tm[2], a8->codes, rows_pa, kp8) || !make_tile_map(&tm[3], b8->codes, rows_pb, kp8))
             return cudaErrorInvalidValue;
     }
-    const dim3 grid((unsigned)(round_up(N, 128) / 128), (unsigned)(round_up(M, 128) / 128));
-    if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+    g.tiles_m = (int)(round_up(M, 128) / 128);
+    g.tiles_n = (int)(round_up(N, 128) / 128);
+    const int ntiles = g.tiles_m * g.tiles_n;
+    if (ntiles == 0) return cudaSuccess;
+    static int num_sms = 0;
+    if (num_sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (num_sms <= 0) num_sms = 148;
+    }
+    const int grid = ntiles < num_sms ? ntiles : num_sms;     // persistent CTAs, one per SM
     k_gemm_nvfp4<<<grid, kThreadsGemm, kSmemBytes + 1024, s>>>(tm[0], tm[1], tm[2], tm[3], g);
     return cudaGetLastError();
 }

@@ -15,11 +15,13 @@ namespace tj {
 // multiplying by the random +-1 diagonal (bit j of `sign_word` set -> negate
 // element j of this lane).  Stages h = 1, 2, 4, 8, 16 run inside the lane, h = 32
 // and h = 64 pair lanes t^1 and t^2; every stage maps (a, b) -> (a + b, a - b) in
-// fp32, in the fixed order h = 1, 2, ..., 64 (TetraJet-v2 §2.C RHT).
+// fp32, in the fixed order h = 1, 2, ..., 64 (TetraJet-v2 §2.C RHT).  The
+// cross-lane stages use one FMA with a +-1 factor: s*x + p is exact before its
+// single rounding, so it rounds exactly like x + p or p - x.
 __device__ __forceinline__ void rht128_quad(float (&x)[32], uint32_t sign_word, int t) {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-        if ((sign_word >> j) & 1u) x[j] = -x[j];
+        x[j] = __uint_as_float(__float_as_uint(x[j]) ^ ((sign_word << (31 - j)) & 0x80000000u));
 #pragma unroll
     for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll
@@ -33,10 +35,11 @@ __device__ __forceinline__ void rht128_quad(float (&x)[32], uint32_t sign_word, 
     }
 #pragma unroll
     for (int m = 1; m <= 2; m <<= 1) {
+        const float sgn = (t & m) ? -1.0f : 1.0f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const float p = __shfl_xor_sync(0xffffffffu, x[j], m);
-            x[j] = (t & m) ? __fsub_rn(p, x[j]) : __fadd_rn(x[j], p);
+            x[j] = __fmaf_rn(sgn, x[j], p);
         }
     }
 }
@@ -49,9 +52,11 @@ struct NvSeg {
 
 // Double-block NVFP4 quantization of one 128-segment (§2.A), readings as in tj.h:
 // s_o = amax/2688 (2^-149 if that underflows), s_i = E4M3 ceiling of
-// amax_16 / (6 s_o), element index = RTN(min(|x * (1/(s_i s_o))|, 6)) or SR with
-// the 16-bit uniforms of Philox call (elem0 + 8q) >> 3.  elem0 = index of x[0] in
-// the operand's quantized layout (row * cols_p + col), a multiple of 8.
+// amax_16 / (6 s_o), v = x * (1/(s_i s_o)); RTN = nearest E2M1 value, ties even,
+// saturated at 6 (hardware conversion); SR = exact integer test on min(|v|, 6)
+// with the 16-bit uniforms of Philox call (elem0 + 8q) >> 3.  A zero element,
+// or any element of a group whose scale is zero, gets code 0.  elem0 = index of
+// x[0] in the operand's quantized layout (row * cols_p + col), a multiple of 8.
 template <bool SR>
 __device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t elem0, uint64_t seed,
                                                  uint32_t tag) {
@@ -87,23 +92,30 @@ __device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t 
         out.sf2 |= sb << (8 * g);
         const float s = __fmul_rn(e4m3_to_float(sb), s_o);
         const float r = s > 0.0f ? __fdiv_rn(1.0f, s) : 0.0f;
+        if (!(s > 0.0f)) continue;                         // zero group: codes stay 0
+        if (SR) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int e = 16 * g + j;
-            const float xv = x[e];
-            const float a = fminf(fabsf(__fmul_rn(xv, r)), 6.0f);
-            uint32_t idx;
-            if (SR) {
+            for (int j = 0; j < 16; ++j) {
+                const int e = 16 * g + j;
+                const float xv = x[e];
+                const float a = fminf(fabsf(__fmul_rn(xv, r)), 6.0f);
                 const uint4 w4 = rnd[e >> 3];
                 const int wi = (e & 7) >> 1;
                 const uint32_t w = wi == 0 ? w4.x : (wi == 1 ? w4.y : (wi == 2 ? w4.z : w4.w));
-                idx = e2m1_sr(a, (w >> (16 * (e & 1))) & 0xFFFFu);
-            } else {
-                idx = e2m1_rtn(a);
+                uint32_t code = e2m1_sr(a, (w >> (16 * (e & 1))) & 0xFFFFu) | (xv < 0.0f ? 8u : 0u);
+                if (xv == 0.0f) code = 0u;
+                words[e >> 3] |= code << (4 * (e & 7));
             }
-            uint32_t code = (xv < 0.0f) ? (idx | 8u) : idx;
-            if (xv == 0.0f || !(s > 0.0f)) code = 0u;
-            words[e >> 3] |= code << (4 * (e & 7));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                const int e = 16 * g + j;
+                const float x0 = x[e], x1 = x[e + 1];
+                uint32_t byte = e2m1x2_rn(__fmul_rn(x0, r), __fmul_rn(x1, r));
+                if (x0 == 0.0f) byte &= 0xF0u;                 // -0 or 0 input -> code 0
+                if (x1 == 0.0f) byte &= 0x0Fu;
+                words[e >> 3] |= byte << (4 * (e & 7));
+            }
         }
     }
     out.codes = make_uint4(words[0], words[1], words[2], words[3]);

@@ -91,26 +91,41 @@ __device__ __forceinline__ uint32_t e4m3_ceil_byte(float t) {
 // E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6}: rounding of a magnitude a in [0, 6].
 // ---------------------------------------------------------------------------
 // Nearest grid point, ties to the even code (the midpoints .25, .75, 1.25, 1.75,
-// 2.5, 3.5, 5 go to codes 0, 2, 2, 4, 4, 6, 6).
+// 2.5, 3.5, 5 go to codes 0, 2, 2, 4, 4, 6, 6).  Reference form, used by the
+// scalar paths; the vector paths use the hardware E2M1 conversion, which rounds
+// to nearest-even on the same grid and saturates at 6.
 __device__ __forceinline__ uint32_t e2m1_rtn(float a) {
     return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
            (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
            (uint32_t)(a > 5.0f);
 }
 
-// Stochastic rounding between the grid neighbours lo <= a <= hi: up with
-// probability p = (a - lo) / (hi - lo), decided as float(u16) < p * 65536.
-// a - lo is exact (Sterbenz) and 1/(hi - lo) a power of two, so p is exact.
+// Two signed values -> one byte of E2M1 codes (lo in the low nibble), rounded
+// to nearest-even and saturated to +-6 by cvt.rn.satfinite.e2m1x2.f32.
+__device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
+    uint16_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+        : "=h"(r)
+        : "f"(hi), "f"(lo));
+    return (uint32_t)r & 0xFFu;
+}
+
+// Stochastic rounding of a in [0, 6] between its grid neighbours lo <= a <= hi:
+// up with probability p = (a - lo) / (hi - lo), decided as float(u16) < p * 65536.
+// Integer form of that same test: for a >= 1 in the binade [2^e, 2^(e+1)) the grid
+// keeps 1 mantissa bit, so p = r / 2^22 with r the 22 lower mantissa bits and the
+// test is 64 * u16 < r; on [0.5, 1) p = m / 2^23 (test 128 * u16 < m); below 0.5
+// lo = 0 and p * 65536 = a * 2^17 exactly.  Returns the grid index (0..7).
 __device__ __forceinline__ uint32_t e2m1_sr(float a, uint32_t u16) {
-    const uint32_t lo = (uint32_t)(a >= 0.5f) + (uint32_t)(a >= 1.0f) + (uint32_t)(a >= 1.5f) +
-                        (uint32_t)(a >= 2.0f) + (uint32_t)(a >= 3.0f) + (uint32_t)(a >= 4.0f) +
-                        (uint32_t)(a >= 6.0f);
-    // grid value and reciprocal gap of index lo
-    const float g = lo < 4u ? __fmul_rn((float)lo, 0.5f) : (lo == 4u ? 2.0f : (lo == 5u ? 3.0f : (lo == 6u ? 4.0f : 6.0f)));
-    if (lo == 7u || a == g) return lo;
-    const float inv_gap = lo < 4u ? 2.0f : (lo < 6u ? 1.0f : 0.5f);
-    const float p = __fmul_rn(__fsub_rn(a, g), inv_gap);
-    return lo + ((float)u16 < __fmul_rn(p, 65536.0f) ? 1u : 0u);
+    const uint32_t A = __float_as_uint(a);
+    const bool big = A >= 0x3F800000u;             // a >= 1
+    const bool mid = A >= 0x3F000000u;             // a >= 0.5
+    const uint32_t lo = big ? (A >> 22) - 252u : (mid ? 1u : 0u);
+    bool up;
+    if (big) up = (u16 << 6) < (A & 0x3FFFFFu);
+    else if (mid) up = (u16 << 7) < (A & 0x7FFFFFu);
+    else up = (float)u16 < __fmul_rn(a, 131072.0f);
+    return lo + (up ? 1u : 0u);
 }
 
 // ---------------------------------------------------------------------------
