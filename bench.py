@@ -202,21 +202,24 @@ LAUNCHES_PER_LINEAR = {True: 15, False: 7}     # with / without an FP8 outlier s
 # secondary measurements (outside the timed step loop)
 # ---------------------------------------------------------------------------
 def time_kernel(fn, stream, reps, flush=None, warmup=3):
-    """Average ms of fn() over reps launches, L2 flushed before each (outside the events)."""
+    """Average device ms of fn() over reps launches, the L2 flushed before each
+    (outside the events).  Every rep is enqueued before the first is waited on,
+    so host launch latency never shows up as device time."""
     for _ in range(warmup):
         fn()
-    total = 0.0
+    evs = []
     for _ in range(reps):
         if flush is not None:
-            flush.zero_()
+            with torch.cuda.stream(stream):
+                flush.zero_()
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record(stream)
         fn()
         e.record(stream)
-        e.synchronize()
-        total += s.elapsed_time(e)
-    return total / reps
+        evs.append((s, e))
+    torch.cuda.synchronize()
+    return sum(s.elapsed_time(e) for s, e in evs) / reps
 
 
 def quantize_sweep(tj, dev, stream, hbm_peak, flush):
