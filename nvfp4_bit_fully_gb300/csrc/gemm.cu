@@ -98,6 +98,7 @@ __device__ __forceinline__ uint64_t global_ns() {
 // soon as another role has aborted), setting the sticky device error flag and
 // the CTA's abort flag.  No wait in this kernel can spin forever.
 __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, Bars *bars) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;         // fast path: no clock read
     const uint64_t t0 = global_ns();
     for (uint32_t i = 0;; ++i) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -405,10 +406,11 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             int64_t cols[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) cols[c] = args.col_map ? (n + c < args.N ? (int64_t)args.col_map[n + c] : -1) : n + c;
-#pragma unroll 4
+            const int rows_here = (int)(args.M - m0 < 128 ? args.M - m0 : 128);
+#pragma unroll 8
             for (int r = sw; r < 128; r += 2) {
                 const int64_t row = m0 + r;
-                if (row >= args.M) break;
+                if (r >= rows_here) continue;
                 const float4 v = *reinterpret_cast<const float4 *>(stage_s + r * kStageRow + 4 * lane);
                 if (args.col_map == nullptr && full4) {
                     if (args.out_bf16) {
