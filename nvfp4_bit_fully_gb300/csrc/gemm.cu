@@ -11,19 +11,18 @@
 // The FP8 slice (kind::mxf8f6f4, UE8M0 per 32) has only power-of-two scales and
 // accumulates over its whole K into one tensor-memory buffer added at the end.
 //
-// Persistent CTAs (one per SM) walk the 128 x 128 output tiles; 12 warps:
+// Persistent CTAs (one per SM) walk the 128 x 128 output tiles; 18 warps:
 //   warp 0     TMA producer (one lane): operand tiles (128 B rows, 128-byte swizzle)
-//              and scale-factor tiles into a 3-stage ring, and the FP32 outer
-//              scales of every 128-K block into an 8-slot ring (bulk copies);
+//              and scale-factor tiles into a 5-stage ring, and the FP32 outer
+//              scales of every 128-K block into a 12-slot ring (bulk copies);
 //   warp 1     tensor-memory owner and MMA issuer (one lane): tcgen05.cp of the
-//              scale tiles, tcgen05.mma into the double-buffered partials;
-//   warps 2-9  promotion: warp w reads TMEM lanes 32*(w%4) .. +31 (its rows) and
-//              columns 64*((w-2)/4) .. +63, accumulates in registers with packed
-//              f32x2 FMAs, and hands the finished tile to a padded staging buffer;
-//   warps 10-11 stores: coalesced row writes of the staged tile (bf16 / fp32,
-//              optional column scatter), overlapping the next tile's promotion.
+//              scale tiles into a 3-slot tensor-memory ring, tcgen05.mma into the
+//              double-buffered partials;
+//   warps 2-17 promotion + epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (its
+//              rows) and columns 32*((w-2)/4) .. +31, accumulates in registers with
+//              packed f32x2 FMAs and writes its row segment with 16-byte stores.
 // Tensor memory (512 columns): P0 [0,128), P1 [128,256), FP8 accumulator
-// [256,384), scale factors 32 columns per ring slot [384,512).
+// [256,384), scale factors 32 columns per slot [384,480).
 // Every mbarrier wait is bounded; a wait that runs out sets the sticky device
 // error flag and an abort flag that makes every role leave its loop, after which
 // in-flight copies and MMAs are drained (bounded) and tensor memory is freed.
@@ -43,20 +42,20 @@ __device__ unsigned int g_tj_dev_error = 0u;
 
 namespace {
 
-constexpr int kStages = 3;                     // operand ring (2 x 128-K blocks per stage)
-constexpr int kScaleSlots = 8;                 // FP32 outer-scale ring (one 128-K block per slot)
+constexpr int kStages = 5;                     // operand ring (2 x 128-K blocks per stage)
+constexpr int kSfSlots = 3;                    // tensor-memory scale-factor slots (stages in flight)
+constexpr int kScaleSlots = 12;                // FP32 outer-scale ring (one 128-K block per slot)
+constexpr int kPromoWarps = 16;                // 4 per TMEM lane quadrant, 32 columns each
 constexpr int kTileBytes = 128 * 128;          // one operand tile: 128 rows x 128 bytes
 constexpr int kSfStageBytes = 2048;            // 4 scale tiles of 512 bytes
-constexpr int kStageRow = 132;                 // staging row stride in floats (bank-conflict padding)
 constexpr int kSmemA = 0;
 constexpr int kSmemB = kSmemA + kStages * kTileBytes;
 constexpr int kSmemSfa = kSmemB + kStages * kTileBytes;
 constexpr int kSmemSfb = kSmemSfa + kStages * kSfStageBytes;
 constexpr int kSmemOuter = kSmemSfb + kStages * kSfStageBytes;      // [slot][A 128 | B 128] floats
-constexpr int kSmemStage = kSmemOuter + kScaleSlots * 1024;        // 128 x kStageRow floats
-constexpr int kSmemBar = kSmemStage + 128 * kStageRow * 4;
+constexpr int kSmemBar = kSmemOuter + kScaleSlots * 1024;
 constexpr int kSmemBytes = kSmemBar + 512;
-constexpr int kThreadsGemm = 384;
+constexpr int kThreadsGemm = 32 * (2 + kPromoWarps);
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColP = 0, kColAcc8 = 256, kColSf = 384;
@@ -83,7 +82,7 @@ struct Bars {
     uint64_t full[kStages], empty[kStages];
     uint64_t pfull[2], pempty[2];
     uint64_t sfull[kScaleSlots], sempty[kScaleSlots];
-    uint64_t a8full, a8empty, stfull, stempty, drain;
+    uint64_t a8full, a8empty, drain;
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -161,7 +160,6 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars *bars = reinterpret_cast<Bars *>(smem + kSmemBar);
     float *outer_s = reinterpret_cast<float *>(smem + kSmemOuter);
-    float *stage_s = reinterpret_cast<float *>(smem + kSmemStage);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntiles = args.tiles_m * args.tiles_n;
     const int nst4 = (args.nkb4 + 1) / 2;
@@ -174,16 +172,14 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         }
         for (int p = 0; p < 2; ++p) {
             ptx::mbar_init(&bars->pfull[p], 1);
-            ptx::mbar_init(&bars->pempty[p], 8);
+            ptx::mbar_init(&bars->pempty[p], kPromoWarps);
         }
         for (int s = 0; s < kScaleSlots; ++s) {
             ptx::mbar_init(&bars->sfull[s], 1);
-            ptx::mbar_init(&bars->sempty[s], 8);
+            ptx::mbar_init(&bars->sempty[s], kPromoWarps);
         }
         ptx::mbar_init(&bars->a8full, 1);
-        ptx::mbar_init(&bars->a8empty, 8);
-        ptx::mbar_init(&bars->stfull, 8);
-        ptx::mbar_init(&bars->stempty, 2);
+        ptx::mbar_init(&bars->a8empty, kPromoWarps);
         ptx::mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         ptx::fence_mbar_init();
@@ -268,7 +264,18 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     const uint32_t sb = ptx::smem_u32(smem + kSmemB + slot * kTileBytes);
                     const uint32_t sfa = ptx::smem_u32(smem + kSmemSfa + slot * kSfStageBytes);
                     const uint32_t sfb = ptx::smem_u32(smem + kSmemSfb + slot * kSfStageBytes);
-                    const uint32_t sfcol = tbase + kColSf + 32u * slot;
+                    // scale-factor slot it % kSfSlots was last read by the MMAs of stage
+                    // it - kSfSlots; those have completed once that stage's ring slot was
+                    // released (its empty barrier phase)
+                    if (it >= kSfSlots) {
+                        const int prev = it - kSfSlots;
+                        if (!wait_bounded(&bars->empty[prev % kStages], (prev / kStages) & 1, bars)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                    }
+                    const uint32_t sfcol = tbase + kColSf + 32u * (uint32_t)(it % kSfSlots);
                     if (st < nst4) {
                         const int nkbs = min(2, args.nkb4 - 2 * st);
                         for (int j = 0; j < 2 * nkbs; ++j) {   // one 512-byte scale tile per K = 64 MMA
@@ -321,26 +328,26 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             ptx::tc_commit(&bars->drain);
             wait_bounded(&bars->drain, 0, bars);
         }
-    } else if (warp < 10) {
-        // ------------------------------------------------------------ promotion
+    } else {
+        // ------------------------------------------------------------ promotion + epilogue
+        const int pw = warp - 2;
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
-        const int h = (warp - 2) >> 2;          // column half
+        const int cq = pw >> 2;                 // column quarter: columns 32*cq .. +31
         const int row_l = 32 * q + lane;
         const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-        int kbc = 0, a8c = 0, tc = 0;
+        int kbc = 0, a8c = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tc) {
-            uint64_t acc[32];                  // 64 fp32 accumulators as packed pairs
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            uint64_t acc[16];                  // 32 fp32 accumulators as packed pairs
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = 0ull;
+            for (int j = 0; j < 16; ++j) acc[j] = 0ull;
             for (int kb = 0; kb < args.nkb4; ++kb, ++kbc) {
                 const int pb = kbc & 1;
                 const int ss = kbc % kScaleSlots;
                 if (!warp_wait_bounded(&bars->pfull[pb], (kbc >> 1) & 1, bars, lane)) { ok = false; break; }
                 ptx::tc_fence_after();
-                uint32_t p0[32], p1[32];
-                ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColP + 128u * pb + 64u * h, p0);
-                ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColP + 128u * pb + 64u * h + 32u, p1);
+                uint32_t pv[32];
+                ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColP + 128u * pb + 32u * cq, pv);
                 ptx::tmem_wait_ld();
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -348,95 +355,78 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                 if (!warp_wait_bounded(&bars->sfull[ss], (kbc / kScaleSlots) & 1, bars, lane)) { ok = false; break; }
                 const float sa = outer_s[ss * 256 + row_l] * args.alpha;
                 const uint64_t sa2 = pack2(sa, sa);
-                const float4 *sbp = reinterpret_cast<const float4 *>(outer_s + ss * 256 + 128 + 64 * h);
+                const float4 *sbp = reinterpret_cast<const float4 *>(outer_s + ss * 256 + 128 + 32 * cq);
+                float4 sbv[8];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float4 sbv = sbp[i];            // broadcast read: all lanes, same address
-                    const uint64_t c01 = mul2(sa2, pack2(sbv.x, sbv.y));
-                    const uint64_t c23 = mul2(sa2, pack2(sbv.z, sbv.w));
-                    const int j = 4 * i;   // columns j .. j+3 of this half
-                    const uint32_t *pp = j < 32 ? p0 : p1;
-                    const int jj = j & 31;
-                    acc[2 * i] = fma2(pack2(__uint_as_float(pp[jj]), __uint_as_float(pp[jj + 1])), c01, acc[2 * i]);
-                    acc[2 * i + 1] =
-                        fma2(pack2(__uint_as_float(pp[jj + 2]), __uint_as_float(pp[jj + 3])), c23, acc[2 * i + 1]);
-                }
+                for (int i = 0; i < 8; ++i) sbv[i] = sbp[i];    // broadcast reads: all lanes, same address
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&bars->sempty[ss]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint64_t c01 = mul2(sa2, pack2(sbv[i].x, sbv[i].y));
+                    const uint64_t c23 = mul2(sa2, pack2(sbv[i].z, sbv[i].w));
+                    acc[2 * i] = fma2(pack2(__uint_as_float(pv[4 * i]), __uint_as_float(pv[4 * i + 1])), c01, acc[2 * i]);
+                    acc[2 * i + 1] =
+                        fma2(pack2(__uint_as_float(pv[4 * i + 2]), __uint_as_float(pv[4 * i + 3])), c23, acc[2 * i + 1]);
+                }
             }
             if (!ok) break;
             if (args.nk8 > 0) {
                 if (!warp_wait_bounded(&bars->a8full, a8c & 1, bars, lane)) { ok = false; break; }
                 ptx::tc_fence_after();
-                uint32_t p0[32], p1[32];
-                ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColAcc8 + 64u * h, p0);
-                ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColAcc8 + 64u * h + 32u, p1);
+                uint32_t pv[32];
+                ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColAcc8 + 32u * cq, pv);
                 ptx::tmem_wait_ld();
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&bars->a8empty);
                 ++a8c;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    acc[i] = add2(acc[i], pack2(__uint_as_float(p0[2 * i]), __uint_as_float(p0[2 * i + 1])));
-                    acc[16 + i] = add2(acc[16 + i], pack2(__uint_as_float(p1[2 * i]), __uint_as_float(p1[2 * i + 1])));
-                }
+                for (int i = 0; i < 16; ++i)
+                    acc[i] = add2(acc[i], pack2(__uint_as_float(pv[2 * i]), __uint_as_float(pv[2 * i + 1])));
             }
-            // hand the tile to the store warps through the padded staging buffer
-            if (tc >= 1 && !warp_wait_bounded(&bars->stempty, (tc - 1) & 1, bars, lane)) { ok = false; break; }
-            float4 *dst = reinterpret_cast<float4 *>(stage_s + row_l * kStageRow + 64 * h);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint64_t a = acc[2 * i], b = acc[2 * i + 1];
-                dst[i] = make_float4(__uint_as_float((uint32_t)a), __uint_as_float((uint32_t)(a >> 32)),
-                                     __uint_as_float((uint32_t)b), __uint_as_float((uint32_t)(b >> 32)));
-            }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&bars->stfull);
-        }
-    } else {
-        // ------------------------------------------------------------ stores (warps 10, 11)
-        const int sw = warp - 10;
-        int tc = 0;
-        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tc) {
-            if (!warp_wait_bounded(&bars->stfull, tc & 1, bars, lane)) break;
+            // epilogue: this thread's row segment of 32 columns, written with 16-byte stores
             const int64_t m0 = (int64_t)(tile / args.tiles_n) * 128, n0 = (int64_t)(tile % args.tiles_n) * 128;
-            const int64_t n = n0 + 4 * lane;
-            const bool full4 = n + 4 <= args.N && (args.ldd & 3) == 0;
-            int64_t cols[4];
+            const int64_t row = m0 + row_l;
+            const int64_t nb = n0 + 32 * cq;
+            if (row < args.M) {
+                float v[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) cols[c] = args.col_map ? (n + c < args.N ? (int64_t)args.col_map[n + c] : -1) : n + c;
-            const int rows_here = (int)(args.M - m0 < 128 ? args.M - m0 : 128);
-#pragma unroll 8
-            for (int r = sw; r < 128; r += 2) {
-                const int64_t row = m0 + r;
-                if (r >= rows_here) continue;
-                const float4 v = *reinterpret_cast<const float4 *>(stage_s + r * kStageRow + 4 * lane);
-                if (args.col_map == nullptr && full4) {
-                    if (args.out_bf16) {
-                        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-                        uint2 u;
-                        u.x = *reinterpret_cast<uint32_t *>(&lo);
-                        u.y = *reinterpret_cast<uint32_t *>(&hi);
-                        *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(args.d) + row * args.ldd + n) = u;
-                    } else {
-                        *reinterpret_cast<float4 *>(static_cast<float *>(args.d) + row * args.ldd + n) = v;
+                for (int i = 0; i < 16; ++i) {
+                    v[2 * i] = __uint_as_float((uint32_t)acc[i]);
+                    v[2 * i + 1] = __uint_as_float((uint32_t)(acc[i] >> 32));
+                }
+                const bool fast = args.col_map == nullptr && nb + 32 <= args.N && (args.ldd & 7) == 0;
+                if (fast && args.out_bf16) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.d) + row * args.ldd + nb);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * i + 2 * k], v[8 * i + 2 * k + 1]);
+                            w4[k] = *reinterpret_cast<uint32_t *>(&b2);
+                        }
+                        dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
-                } else {
-                    const float vv[4] = {v.x, v.y, v.z, v.w};
+                } else if (fast) {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(args.d) + row * args.ldd + nb);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (n + c < args.N) {
+                    for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int64_t n = nb + j;
+                        if (n < args.N) {
+                            const int64_t col = args.col_map ? (int64_t)args.col_map[n] : n;
                             if (args.out_bf16)
-                                static_cast<__nv_bfloat16 *>(args.d)[row * args.ldd + cols[c]] = __float2bfloat16_rn(vv[c]);
+                                static_cast<__nv_bfloat16 *>(args.d)[row * args.ldd + col] = __float2bfloat16_rn(v[j]);
                             else
-                                static_cast<float *>(args.d)[row * args.ldd + cols[c]] = vv[c];
+                                static_cast<float *>(args.d)[row * args.ldd + col] = v[j];
                         }
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&bars->stempty);
         }
     }
     ptx::tc_fence_before();
