@@ -208,6 +208,27 @@ tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, c
                            int64_t k, uint64_t seed, float *dw, int64_t lddw, void *workspace,
                            size_t ws_bytes, void *stream);
 
+/* tj_linear_bwd_dx_noalloc - the same input gradient as tj_linear_bwd_dx, for callers
+ * that cannot allocate device memory when the backward runs (code below the framework's
+ * allocator, or deployments that only hand out buffers registered up front).  The paper
+ * has no counterpart: this is an interface convenience of the library.
+ *   - Takes the same arguments as tj_linear_bwd_dx minus the workspace: the scratch is a
+ *     fixed array inside the library, tj_noalloc_scratch_bytes() = 16 MiB, kept resident
+ *     on every GPU that loads the library until the process exits.
+ *   - Problems whose tj_workspace_size(TJ_OP_BWD_DX, ...) exceeds it return
+ *     TJ_ERR_WORKSPACE before any launch.
+ *   - Allocates nothing (no cudaMalloc / cudaFree, no allocating library routine).
+ *   - The first call on each device looks up the scratch's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one scratch array, which keeps the last call's contents; calls
+ *     whose executions overlap on the GPU (other streams, other threads) race on it, so
+ *     serialise them.  Nothing needs clearing: each call writes all scratch it reads. */
+tj_status tj_linear_bwd_dx_noalloc(const void *dy, int64_t M, int64_t N, int64_t lddy, const tj_nvfp4 *wq,
+                                   const tj_mxfp8 *w8, const int32_t *normal_idx, const int32_t *outlier_idx,
+                                   int64_t k, uint64_t seed, void *dx, int out_dtype, int64_t lddx, void *stream);
+size_t tj_noalloc_scratch_bytes(void);
+
 #define TJ_OP_BWD_DX 1
 #define TJ_OP_BWD_DW 2
 /* Bytes of workspace the backward call `op` needs for these sizes (K = K_N + k). */

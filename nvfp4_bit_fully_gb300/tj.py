@@ -64,6 +64,9 @@ _SIGS = {
     "tj_outlier_calibrate": [_P, _I, _I64, _I64, _I64, _P, _I, _I64, _P, _P, _P],
     "tj_osci_reset": [_P, _P, _P, _P, ctypes.POINTER(CNvfp4), ctypes.POINTER(CNvfp4), _P, _I64, _I64, _F, _F, _F,
                       _I, _P],
+    "tj_linear_bwd_dx_noalloc": [_P, _I64, _I64, _I64, ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P, _P, _I64,
+                                 _U64, _P, _I, _I64, _P],
+    "tj_noalloc_scratch_bytes": [],
     "tj_get_device_status": [],
     "tj_status_str": [_I],
 }
@@ -80,7 +83,7 @@ def load(path=LIB_PATH):
         for name, args in _SIGS.items():
             f = getattr(lib, name)
             f.argtypes = args
-            f.restype = ctypes.c_size_t if name == "tj_workspace_size" else (
+            f.restype = ctypes.c_size_t if name in ("tj_workspace_size", "tj_noalloc_scratch_bytes") else (
                 ctypes.c_char_p if name == "tj_status_str" else ctypes.c_int)
         _lib = lib
     return _lib
@@ -263,6 +266,20 @@ def linear_bwd_dw(dy, xq, x8=None, normal_idx=None, outlier_idx=None, seed=0, wo
     _call("tj_linear_bwd_dw", _ptr(dy), M, N, dy.stride(0), ctypes.byref(cx), _ref(cx8), _ptr(normal_idx),
           _ptr(outlier_idx), k, seed, _ptr(out), out.stride(0), _ptr(workspace), workspace.numel(),
           _stream(stream))
+    return out
+
+
+def linear_bwd_dx_noalloc(dy, wq, w8=None, normal_idx=None, outlier_idx=None, seed=0, out_dtype=torch.bfloat16,
+                          out=None, stream=None):
+    """dX like linear_bwd_dx, with the library's fixed internal scratch instead of a workspace
+    (for callers that cannot allocate device memory when the backward runs)."""
+    M, N = dy.shape
+    k = 0 if outlier_idx is None else outlier_idx.numel()
+    out = out if out is not None else torch.empty(M, wq.cols + k, dtype=out_dtype, device=dy.device)
+    cw = wq.c()
+    cw8 = w8.c() if k else None
+    _call("tj_linear_bwd_dx_noalloc", _ptr(dy), M, N, dy.stride(0), ctypes.byref(cw), _ref(cw8), _ptr(normal_idx),
+          _ptr(outlier_idx), k, seed, _ptr(out), _dtype_code(out), out.stride(0), _stream(stream))
     return out
 
 

@@ -1,0 +1,99 @@
+"""GPU test of tj_linear_bwd_dx_noalloc, the input-gradient entry point for callers
+that cannot allocate device memory when the backward runs (code below the
+framework's allocator, or deployments that only use buffers registered up front).
+It uses a fixed scratch array inside the library instead of a caller workspace.
+
+Through the C ABI, two calls in a row must each give the same dX as the regular
+tj_linear_bwd_dx with a caller workspace, within the GEMM tolerance the other
+tests use (2e-3 * sum|a||b| against the oracle's operands) and in fact bit for bit;
+a problem larger than the fixed scratch is rejected before any launch.  This file
+is named to be collected last, and passes alone or after the other tests.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from layouts import abs_product, assert_gemm_close
+from nvfp4_bit_fully_gb300 import workloads
+from oracle import linear as OL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tj():
+    from nvfp4_bit_fully_gb300 import tj as _tj
+
+    _tj.load()
+    return _tj
+
+
+def _call_noalloc(tj, dy, wq, w8, ni, oi, seed, out):
+    """Call the entry point directly through ctypes (no Python-side buffers besides dX)."""
+    lib = tj.load()
+    k = 0 if oi is None else oi.numel()
+    cw = wq.c()
+    cw8 = w8.c() if k else None
+    code = lib.tj_linear_bwd_dx_noalloc(
+        ctypes.c_void_p(dy.data_ptr()), dy.shape[0], dy.shape[1], dy.stride(0), ctypes.byref(cw),
+        ctypes.byref(cw8) if cw8 is not None else None,
+        ctypes.c_void_p(ni.data_ptr()) if ni is not None else None,
+        ctypes.c_void_p(oi.data_ptr()) if oi is not None else None, k, seed,
+        ctypes.c_void_p(out.data_ptr()), tj.TJ_FP32, out.stride(0),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert code == 0, tj.STATUS.get(code, code)
+
+
+@pytest.mark.parametrize("with_outliers", [False, True])
+def test_noalloc_matches_workspace_version_twice(tj, with_outliers):
+    X, W, dY = workloads.tiny(seed=0)
+    K = W.shape[1]
+    if with_outliers:
+        outl = np.arange(3, K, 10)[:52]
+        normal = OL.normal_channels(K, outl)
+        ni = torch.from_numpy(normal.astype(np.int32)).cuda()
+        oi = torch.from_numpy(outl.astype(np.int32)).cuda()
+        wq = tj.quantize_nvfp4(W.cuda(), sel=ni)
+        w8 = tj.quantize_mxfp8(W.cuda(), sel=oi)
+    else:
+        outl = np.array([], dtype=np.int64)
+        ni = oi = w8 = None
+        wq = tj.quantize_nvfp4(W.cuda())
+    dyd = dY.cuda()
+    seed = 77
+    ref = tj.linear_bwd_dx(dyd, wq, w8, ni, oi, seed=seed, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ref_np = ref.cpu().numpy()
+    # tolerance as in the other GEMM tests: 2e-3 * sum|a||b| over the quantized operands
+    _, _, fw = OL.forward(X.float().numpy(), W.float().numpy(), outl)
+    s_dy, s_w, _, _ = OL.bwd_dx_operands(dY.float().numpy(), fw, seed)
+    bound = np.zeros(ref_np.shape)
+    bound[:, OL.normal_channels(K, outl)] = abs_product(s_dy, s_w, OL.ALPHA_RHT)[:, : K - len(outl)]
+    if len(outl):
+        from layouts import abs_product_fp8
+        from oracle import quant as Q
+        q8_dy = Q.quantize_mxfp8(dY.float().numpy())
+        q8_w = Q.quantize_mxfp8(OL.deq_outlier_f32(fw).T)
+        bound[:, outl] = abs_product_fp8(q8_dy, q8_w)[:, : len(outl)]
+    for call in range(2):                                      # two calls in a row share the scratch
+        out = torch.full_like(ref, float("nan"))
+        _call_noalloc(tj, dyd, wq, w8, ni, oi, seed, out)
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        assert_gemm_close(got, ref_np, bound, what="noalloc call %d" % call)
+        assert np.array_equal(got, ref_np)
+    tj.device_status()
+
+
+def test_noalloc_rejects_problems_beyond_the_scratch(tj):
+    lib = tj.load()
+    limit = int(lib.tj_noalloc_scratch_bytes())
+    assert limit == 16 << 20
+    M, N, K = 16384, 4096, 1024                               # needs ~45 MB of scratch
+    assert tj.workspace_size(tj.TJ_OP_BWD_DX, M, N, K, 0) > limit
+    wq = tj.CNvfp4(256, 256, 256, N, K)
+    code = lib.tj_linear_bwd_dx_noalloc(ctypes.c_void_p(256), M, N, N, ctypes.byref(wq), None, None, None, 0, 1,
+                                        ctypes.c_void_p(256), tj.TJ_FP32, K, None)
+    assert code == 7                                           # TJ_ERR_WORKSPACE, before any launch
