@@ -140,9 +140,26 @@ class Timeline:
         return {k: (float(np.sum(v)), len(v)) for k, v in agg.items()}
 
 
+# kernel behind each step call (for per-kernel aggregation of the live event times)
+CALL_KERNEL = {
+    "quant_x": "k_quant_rows (NVFP4)", "quant_dy_row": "k_quant_rows (NVFP4)",
+    "quant_x8": "k_quant_rows (MXFP8)", "quant_dy_row8": "k_quant_rows (MXFP8)",
+    "quant_dy_col": "k_quant_cols (NVFP4)", "quant_dy_col8": "k_quant_cols (MXFP8)",
+    "requant_w": "k_quant_cols<SrcNv> (re-align)", "requant_x": "k_quant_cols<SrcNv> (re-align)",
+    "requant_w8": "k_quant_cols<SrcMx> (re-align)", "requant_x8": "k_quant_cols<SrcMx> (re-align)",
+    "gemm_fwd": "k_gemm_nvfp4", "gemm_dx": "k_gemm_nvfp4", "gemm_dw": "k_gemm_nvfp4",
+    "gemm_dx8": "k_gemm_nvfp4", "gemm_dw8": "k_gemm_nvfp4",
+    "osci_reset": "k_osci_reset",
+}
+
+
 class Linear:
-    """One linear of the layer set: inputs, calibrated outlier set, forward
-    weight operands and every output / workspace buffer, all resident in HBM."""
+    """One linear of the layer set: inputs, calibrated outlier set, forward weight
+    operands and every output / intermediate buffer, all resident in HBM.
+
+    run() issues the step as the individual C-ABI calls that tj_linear_fwd /
+    tj_linear_bwd_dx / tj_linear_bwd_dw make internally (same kernels, same order),
+    so every kernel gets its own CUDA events in the timed region."""
 
     def __init__(self, tj, wl, name, N, K, dev, seed):
         self.name, self.N, self.K = name, N, K
@@ -157,23 +174,65 @@ class Linear:
         self.oi, self.ni = tj.outlier_calibrate(None, sumsq, finalize=True, k=self.k)
         self.wq = tj.quantize_nvfp4(W, sel=self.ni)
         self.w8 = tj.quantize_mxfp8(W, sel=self.oi)
-        M, kn = TOKENS, K - self.k
-        self.xq = tj.NVFP4.empty(M, kn, dev)
-        self.x8 = tj.MXFP8.empty(M, self.k, dev)
+        M, kn, k = TOKENS, K - self.k, self.k
+        self.xq, self.x8 = tj.NVFP4.empty(M, kn, dev), tj.MXFP8.empty(M, k, dev)
+        self.s_dy, self.s_w = tj.NVFP4.empty(M, N, dev), tj.NVFP4.empty(kn, N, dev)
+        self.q8_dy, self.q8_w = tj.MXFP8.empty(M, N, dev), tj.MXFP8.empty(k, N, dev)
+        self.s_dyt, self.s_x = tj.NVFP4.empty(N, M, dev), tj.NVFP4.empty(kn, M, dev)
+        self.q8_dyt, self.q8_x = tj.MXFP8.empty(N, M, dev), tj.MXFP8.empty(k, M, dev)
         self.Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         self.dX = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
         self.dW = torch.empty(N, K, dtype=torch.float32, device=dev)
-        self.ws_dx = torch.empty(tj.workspace_size(tj.TJ_OP_BWD_DX, M, N, K, self.k), dtype=torch.uint8, device=dev)
-        self.ws_dw = torch.empty(tj.workspace_size(tj.TJ_OP_BWD_DW, M, N, K, self.k), dtype=torch.uint8, device=dev)
+        self.ws_dx = torch.empty(tj.workspace_size(tj.TJ_OP_BWD_DX, M, N, K, k), dtype=torch.uint8, device=dev)
+        self.ws_dw = torch.empty(tj.workspace_size(tj.TJ_OP_BWD_DW, M, N, K, k), dtype=torch.uint8, device=dev)
         self.flops = 6.0 * M * N * K
+        # algorithmic work of every call: (FP4 flops, FP8 flops) or bytes
+        f4 = lambda a, b, c: 2.0 * a * b * c
+        self.work = {
+            "gemm_fwd": (f4(M, N, kn), f4(M, N, k)), "gemm_dx": (f4(M, kn, N), 0.0), "gemm_dx8": (0.0, f4(M, k, N)),
+            "gemm_dw": (f4(N, kn, M), 0.0), "gemm_dw8": (0.0, f4(N, k, M)),
+            "quant_x": M * kn * (2 + NV_B), "quant_x8": M * k * (2 + MX_B), "quant_dy_row": M * N * (2 + NV_B),
+            "quant_dy_row8": M * N * (2 + MX_B), "quant_dy_col": M * N * (2 + NV_B), "quant_dy_col8": M * N * (2 + MX_B),
+            "requant_w": 2 * kn * N * NV_B, "requant_w8": 2 * k * N * MX_B, "requant_x": 2 * kn * M * NV_B,
+            "requant_x8": 2 * k * M * MX_B,
+        }
 
     def run(self, tj, seed, tl, stream):
-        tl.time(self.name + ".fwd", lambda: tj.linear_fwd(self.X, self.wq, self.w8, self.ni, self.oi, xq=self.xq,
-                                                          x8=self.x8, out=self.Y, stream=stream))
-        tl.time(self.name + ".bwd_dx", lambda: tj.linear_bwd_dx(self.dY, self.wq, self.w8, self.ni, self.oi, seed=seed,
-                                                                workspace=self.ws_dx, out=self.dX, stream=stream))
-        tl.time(self.name + ".bwd_dw", lambda: tj.linear_bwd_dw(self.dY, self.xq, self.x8, self.ni, self.oi, seed=seed,
-                                                                workspace=self.ws_dw, out=self.dW, stream=stream))
+        T = lambda name, fn: tl.time(self.name + "." + name, fn)
+        s = stream
+        SR = tj.TJ_SR
+        # forward (tj_linear_fwd)
+        T("quant_x", lambda: tj.quantize_nvfp4(self.X, sel=self.ni, out=self.xq, stream=s))
+        T("quant_x8", lambda: tj.quantize_mxfp8(self.X, sel=self.oi, out=self.x8, stream=s))
+        T("gemm_fwd", lambda: tj.gemm_nvfp4(self.xq, self.wq, self.x8, self.w8, out=self.Y, stream=s))
+        # input gradient (tj_linear_bwd_dx)
+        T("quant_dy_row", lambda: tj.quantize_nvfp4(self.dY, mode=SR, rht=True, seed=seed, tag=tj.TAG_DY_ROW,
+                                                    rht_tag=tj.TAG_RHT_DX, out=self.s_dy, stream=s))
+        T("requant_w", lambda: tj.requantize_nvfp4(self.wq, SR, True, seed, tj.TAG_WT, tj.TAG_RHT_DX, out=self.s_w,
+                                                   stream=s))
+        T("gemm_dx", lambda: tj.gemm_nvfp4(self.s_dy, self.s_w, alpha=2.0 ** -7, out=self.dX, col_map=self.ni,
+                                           stream=s))
+        T("quant_dy_row8", lambda: tj.quantize_mxfp8(self.dY, out=self.q8_dy, stream=s))
+        T("requant_w8", lambda: tj.requantize_mxfp8(self.w8, out=self.q8_w, stream=s))
+        T("gemm_dx8", lambda: tj.gemm_mxfp8(self.q8_dy, self.q8_w, out=self.dX, col_map=self.oi, stream=s))
+        # weight gradient (tj_linear_bwd_dw)
+        T("quant_dy_col", lambda: tj.quantize_nvfp4(self.dY, along_cols=True, mode=SR, rht=True, seed=seed,
+                                                    tag=tj.TAG_DY_COL, rht_tag=tj.TAG_RHT_DW, out=self.s_dyt, stream=s))
+        T("requant_x", lambda: tj.requantize_nvfp4(self.xq, SR, True, seed, tj.TAG_XT, tj.TAG_RHT_DW, out=self.s_x,
+                                                   stream=s))
+        T("gemm_dw", lambda: tj.gemm_nvfp4(self.s_dyt, self.s_x, alpha=2.0 ** -7, out=self.dW, col_map=self.ni,
+                                           stream=s))
+        T("quant_dy_col8", lambda: tj.quantize_mxfp8(self.dY, along_cols=True, out=self.q8_dyt, stream=s))
+        T("requant_x8", lambda: tj.requantize_mxfp8(self.x8, out=self.q8_x, stream=s))
+        T("gemm_dw8", lambda: tj.gemm_mxfp8(self.q8_dyt, self.q8_x, out=self.dW, col_map=self.oi, stream=s))
+
+    def run_api(self, tj, seed, stream):
+        """The same step through the user-facing calls (tj_linear_fwd / bwd_dx / bwd_dw)."""
+        tj.linear_fwd(self.X, self.wq, self.w8, self.ni, self.oi, xq=self.xq, x8=self.x8, out=self.Y, stream=stream)
+        tj.linear_bwd_dx(self.dY, self.wq, self.w8, self.ni, self.oi, seed=seed, workspace=self.ws_dx, out=self.dX,
+                         stream=stream)
+        tj.linear_bwd_dw(self.dY, self.xq, self.x8, self.ni, self.oi, seed=seed, workspace=self.ws_dw, out=self.dW,
+                         stream=stream)
 
 
 class OsciState:
@@ -181,6 +240,7 @@ class OsciState:
 
     def __init__(self, tj, wl, n, dev, seed):
         self.w = wl.device_master_weights(n, seed=seed, device=dev)
+        self.bytes = n * osci_bytes_per_elem()
         rows, cols = self.w.shape
         self.w_prev = self.w.clone()
         self.dq = torch.zeros_like(self.w)
@@ -195,7 +255,12 @@ class OsciState:
         self.q.reverse()
 
 
-LAUNCHES_PER_LINEAR = {True: 15, False: 7}     # with / without an FP8 outlier slice
+# DRAM bytes per launch measured by ncu for the HBM-bound kernels (profiles/), valid for the
+# kernel version they were taken on; None until a capture of the current version exists.
+TRAFFIC = {}
+NV_B = 0.5 + 1.0 / 16 + 4.0 / 128      # bytes per NVFP4 element (codes + E4M3 + FP32 scales)
+MX_B = 1.0 + 1.0 / 32                   # bytes per MXFP8 element (E4M3 + UE8M0)
+LAUNCHES_PER_LINEAR = 15                # with an FP8 outlier slice: fwd 3, dX 6, dW 6
 
 
 # ---------------------------------------------------------------------------
@@ -428,26 +493,58 @@ def main():
     osci_ms = summ["osci_reset"][0] / summ["osci_reset"][1]
     flops_step = sum(l.flops for l in linears)
     value = world * flops_step * args.steps / (lin_ms * 1e-3) / 1e12
-    osci_bytes = osci.n * osci_bytes_per_elem()
-    osci_gbs = osci_bytes / (osci_ms * 1e-3) / 1e9
-    parts = {k: {"ms": round(v[0] / v[1], 4)} for k, v in sorted(summ.items())}
-    for lin in linears:
-        for kind, frac in (("fwd", 1 / 3), ("bwd_dx", 1 / 3), ("bwd_dw", 1 / 3)):
-            p = parts[lin.name + "." + kind]
-            p["TFLOP/s"] = round(lin.flops * frac / (p["ms"] * 1e-3) / 1e12, 1)
-    parts["osci_reset"]["GB/s"] = round(osci_gbs, 1)
-    # dominant call of the step (largest total time)
-    dom = max(summ.items(), key=lambda kv: kv[1][0])[0]
-    if dom == "osci_reset":
-        roof = {"kernel": "k_osci_reset (tj_osci_reset)", "bound": "hbm", "achieved": round(osci_gbs, 1),
-                "peak": hbm_peak, "unit": "GB/s", "frac": round(osci_gbs / hbm_peak, 3), "traffic": None,
-                "algorithmic_bytes_per_launch": int(osci_bytes), "peak_source": peak_src + " (hbm_gbs)"}
+    osci_gbs = osci.bytes / (osci_ms * 1e-3) / 1e9
+    # per call: average ms and throughput against its algorithmic work
+    parts = {}
+    kern = {}                       # kernel -> [total ms, flops4, flops8, bytes, launches]
+    for name, (ms_tot, n) in sorted(summ.items()):
+        call = name.split(".")[-1]
+        p = {"ms": round(ms_tot / n, 4)}
+        agg = kern.setdefault(CALL_KERNEL[call], [0.0, 0.0, 0.0, 0.0, 0])
+        agg[0] += ms_tot
+        agg[4] += n
+        if call == "osci_reset":
+            p["GB/s"] = round(osci_gbs, 1)
+            agg[3] += osci.bytes * n
+        else:
+            lin = next(l for l in linears if l.name == name.split(".")[0])
+            w = lin.work[call]
+            if isinstance(w, tuple):
+                p["TFLOP/s"] = round((w[0] + w[1]) / (ms_tot / n * 1e-3) / 1e12, 1)
+                agg[1] += w[0] * n
+                agg[2] += w[1] * n
+            else:
+                p["GB/s"] = round(w / (ms_tot / n * 1e-3) / 1e9, 1)
+                agg[3] += w * n
+        parts[name] = p
+    kernels = {}
+    for kname, (ms_tot, f4, f8, by, n) in kern.items():
+        e = {"launches_per_step": n // args.steps, "ms_per_step": round(ms_tot / args.steps, 4),
+             "share": round(ms_tot / (total_ms * world / world), 3)}
+        if f4 + f8 > 0:
+            t_star = f4 / (fp4_peak * 1e12) + f8 / (fp8_peak * 1e12)       # time at the dtype-weighted peak
+            e.update({"TFLOP/s": round((f4 + f8) / (ms_tot * 1e-3) / 1e12, 1),
+                      "frac": round(t_star / (ms_tot * 1e-3), 4)})
+        else:
+            e.update({"GB/s": round(by / (ms_tot * 1e-3) / 1e9, 1), "frac": round(by / (ms_tot * 1e-3) / 1e9 / hbm_peak, 3)})
+        kernels[kname] = e
+    # dominant kernel of the step (largest total time), with its roofline
+    dom = max(kern.items(), key=lambda kv: kv[1][0])[0]
+    ms_tot, f4, f8, by, n = kern[dom]
+    if f4 + f8 > 0:
+        peak_mix = (f4 + f8) / (f4 / fp4_peak + f8 / fp8_peak)           # dtype-weighted peak, TFLOP/s
+        achieved = (f4 + f8) / (ms_tot * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak_mix, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / peak_mix, 4), "traffic": None,
+                "algorithmic_flops_per_launch": round((f4 + f8) / n),
+                "peak_source": "%s bf16 burst %.1f x nominal fp4 (x6) / fp8 (x2) ratios, weighted by the FP4 / FP8 "
+                               "flop mix" % (peak_src, bf16_burst)}
     else:
-        p = parts[dom]
-        roof = {"kernel": dom, "bound": "tensor", "achieved": p["TFLOP/s"], "peak": round(fp4_peak, 1),
-                "unit": "TFLOP/s", "frac": round(p["TFLOP/s"] / fp4_peak, 3), "traffic": None,
-                "peak_source": peak_src + " bf16 burst x 6 (nominal fp4/bf16 ratio)"}
-    launches = args.steps * (sum(LAUNCHES_PER_LINEAR[l.k > 0] for l in linears) + 1)
+        achieved = by / (ms_tot * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 3), "traffic": TRAFFIC.get(dom),
+                "algorithmic_bytes_per_launch": round(by / n), "peak_source": peak_src + " hbm_gbs"}
+    launches = args.steps * (LAUNCHES_PER_LINEAR * len(linears) + 1)
 
     extras = {}
     if not args.no_extras and rank == 0:
@@ -470,7 +567,7 @@ def main():
                            "l2": "no flush: per-step working set ~13 GB (OsciReset state 10.8 GB) >> 129 MB L2"},
                 "linear_ms_per_step": round(lin_ms / args.steps, 4),
                 "osci_reset": {"ms": round(osci_ms, 4), "GB/s": round(osci_gbs, 1), "frac": round(osci_gbs / hbm_peak, 3)},
-                "roofline": roof, "parts": parts, "gpu_launches": launches, "clocks": clk}
+                "roofline": roof, "kernels": kernels, "parts": parts, "gpu_launches": launches, "clocks": clk}
         line.update(extras)
         if e2e is not None:
             line["e2e"] = e2e
@@ -492,14 +589,13 @@ def measure_e2e(tj, linears, stream, steps, world):
     hdw = [torch.empty(l.dW.shape, dtype=l.dW.dtype).pin_memory() for l in linears]
     h2d = sum(t.numel() * t.element_size() for t in hx + hdy)
     d2h = sum(t.numel() * t.element_size() for t in hdw)
-    dummy = Timeline(stream)
 
     def one(seed):
         with torch.cuda.stream(stream):
             for i, l in enumerate(linears):
                 l.X.copy_(hx[i], non_blocking=True)
                 l.dY.copy_(hdy[i], non_blocking=True)
-                l.run(tj, seed, dummy, stream)
+                l.run_api(tj, seed, stream)
                 hdw[i].copy_(l.dW, non_blocking=True)
 
     for w in range(2):

@@ -132,6 +132,19 @@ tj_status tj_quantize_mxfp8(const void *x, int dtype, int64_t rows_x, int64_t co
                             int along_cols, const int32_t *sel, int64_t n_sel,
                             tj_mxfp8 *out, void *stream);
 
+/* tj_requantize_nvfp4 - transposed re-alignment of a forward NVFP4 operand for the
+ * backward (§2.A: the backward estimates with X-hat, the dequantized forward operand, and
+ * the 1x16 groups of the transposed weight are re-formed along the new contraction axis):
+ * out[c, r] = Q(RHT(X-hat[:, c])) along r, with X-hat[r, c] = (G s_i) s_o of `in`
+ * [rows, cols].  out is [cols, rows]; mode / rht / seed / tags as in tj_quantize_nvfp4
+ * (element index e = out_row * roundup(rows, 128) + r).  Used inside tj_linear_bwd_*. */
+tj_status tj_requantize_nvfp4(const tj_nvfp4 *in, int mode, int rht, uint64_t seed, uint32_t tag, uint32_t rht_tag,
+                              tj_nvfp4 *out, void *stream);
+
+/* tj_requantize_mxfp8 - the same re-alignment for an FP8 outlier slice: out[c, r] =
+ * Q8(X-hat_O[:, c]) along r (RTN, no RHT), in [rows, cols] -> out [cols, rows]. */
+tj_status tj_requantize_mxfp8(const tj_mxfp8 *in, tj_mxfp8 *out, void *stream);
+
 /* tj_rht - standalone random Hadamard transform (§2.C): for each row of x (fp32,
  * [rows, cols], cols a multiple of 128, contiguous) y = H128 * (d .* x) per
  * 128-block, unnormalised, fp32 butterflies in stage order 1, 2, ..., 64.

@@ -132,6 +132,23 @@ tj_status tj_quantize_mxfp8(const void *x, int dtype, int64_t rows_x, int64_t co
                                              static_cast<cudaStream_t>(stream)));
 }
 
+tj_status tj_requantize_nvfp4(const tj_nvfp4 *in, int mode, int rht, uint64_t seed, uint32_t tag, uint32_t rht_tag,
+                              tj_nvfp4 *out, void *stream) {
+    if (in == nullptr || out == nullptr || (mode != TJ_RTN && mode != TJ_SR)) return TJ_ERR_INVALID_ARG;
+    tj_status st = check_nv(in, in->rows, in->cols);
+    if (st == TJ_OK) st = check_nv(out, in->cols, in->rows);
+    if (st != TJ_OK) return st;
+    return cuda_status(launch_realign_nv(*in, *out, mode, rht, seed, tag, rht_tag, static_cast<cudaStream_t>(stream)));
+}
+
+tj_status tj_requantize_mxfp8(const tj_mxfp8 *in, tj_mxfp8 *out, void *stream) {
+    if (in == nullptr || out == nullptr) return TJ_ERR_INVALID_ARG;
+    tj_status st = check_mx(in, in->rows, in->cols);
+    if (st == TJ_OK) st = check_mx(out, in->cols, in->rows);
+    if (st != TJ_OK) return st;
+    return cuda_status(launch_realign_mx(*in, *out, static_cast<cudaStream_t>(stream)));
+}
+
 tj_status tj_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, void *stream) {
     if (x == nullptr || y == nullptr || rows < 0 || cols < 0) return TJ_ERR_INVALID_ARG;
     if (cols % 128 != 0) return TJ_ERR_SHAPE;

@@ -37,12 +37,12 @@ __device__ __forceinline__ uint32_t spread4(uint32_t b) {
     return b;
 }
 
-constexpr int kBlocksPerWarp = 4;   // 128-element blocks per warp iteration (memory-level parallelism)
+constexpr int kBlocksPerWarp = 2;   // 128-element blocks per warp iteration (memory-level parallelism)
 
 // One warp per 128-element block: lane l holds elements 4l .. 4l+3, so every
 // load and store of the fp32 state is a fully coalesced 512-byte warp access.
 // A 16-element inner group is 4 lanes; the outer block is the whole warp.
-__global__ void __launch_bounds__(256) k_osci_reset(float *w, float *w_prev, float *dist_q, float *dist_m,
+__global__ void __launch_bounds__(256, 3) k_osci_reset(float *w, float *w_prev, float *dist_q, float *dist_m,
                                                     const uint8_t *qp_codes, const uint8_t *qp_sf,
                                                     const float *qp_outer, OutNv qo, uint32_t *mask, int64_t rows,
                                                     int64_t cols, int lr_low, float risk_thr, int track) {
@@ -194,7 +194,7 @@ cudaError_t launch_osci_reset(float *w, float *w_prev, float *dist_q, float *dis
     const OutNv qo{q_out.codes, q_out.sf, q_out.outer, round_up(rows, 128), round_up(cols, 128)};
     const int64_t total = qo.rows_p * (qo.cols_p / 128);
     int64_t grid = (total + 8 * kBlocksPerWarp - 1) / (8 * kBlocksPerWarp);
-    if (grid > 152 * 8) grid = 152 * 8;
+    if (grid > 152 * 12) grid = 152 * 12;
     if (grid < 1) grid = 1;
     k_osci_reset<<<(unsigned)grid, 256, 0, s>>>(w, w_prev, dist_q, dist_m, q_prev.codes, q_prev.sf, q_prev.outer, qo,
                                                  mask, rows, cols, (lr < lr_thr) ? 1 : 0, risk_thr, track);

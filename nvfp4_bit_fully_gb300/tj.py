@@ -49,6 +49,8 @@ _F = ctypes.c_float
 _SIGS = {
     "tj_quantize_nvfp4": [_P, _I, _I64, _I64, _I64, _I, _P, _I64, _I, _I, _U64, _U32, _U32, ctypes.POINTER(CNvfp4), _P],
     "tj_quantize_mxfp8": [_P, _I, _I64, _I64, _I64, _I, _P, _I64, ctypes.POINTER(CMxfp8), _P],
+    "tj_requantize_nvfp4": [ctypes.POINTER(CNvfp4), _I, _I, _U64, _U32, _U32, ctypes.POINTER(CNvfp4), _P],
+    "tj_requantize_mxfp8": [ctypes.POINTER(CMxfp8), ctypes.POINTER(CMxfp8), _P],
     "tj_rht": [_P, _P, _I64, _I64, _U64, _U32, _P],
     "tj_dequantize_nvfp4": [ctypes.POINTER(CNvfp4), _P, _I64, _P],
     "tj_gemm_nvfp4": [ctypes.POINTER(CNvfp4), ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8),
@@ -175,6 +177,23 @@ def quantize_mxfp8(x, along_cols=False, sel=None, out=None, stream=None):
     c = out.c()
     _call("tj_quantize_mxfp8", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols), _ptr(sel),
           0 if sel is None else sel.numel(), ctypes.byref(c), _stream(stream))
+    return out
+
+
+def requantize_nvfp4(q, mode=TJ_SR, rht=True, seed=0, tag=0, rht_tag=0, out=None, stream=None):
+    """Transposed re-alignment of a forward NVFP4 operand [rows, cols] -> [cols, rows]."""
+    out = out if out is not None else NVFP4.empty(q.cols, q.rows, q.codes.device)
+    ci, co = q.c(), out.c()
+    _call("tj_requantize_nvfp4", ctypes.byref(ci), mode, int(rht), seed, tag, rht_tag, ctypes.byref(co),
+          _stream(stream))
+    return out
+
+
+def requantize_mxfp8(q, out=None, stream=None):
+    """Transposed re-alignment of an FP8 slice [rows, cols] -> [cols, rows] (RTN)."""
+    out = out if out is not None else MXFP8.empty(q.cols, q.rows, q.codes.device)
+    ci, co = q.c(), out.c()
+    _call("tj_requantize_mxfp8", ctypes.byref(ci), ctypes.byref(co), _stream(stream))
     return out
 
 

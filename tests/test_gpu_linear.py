@@ -120,3 +120,36 @@ def test_ragged_linear(tj):
     dY = (torch.randn(M, N, generator=g) * 1e-3).to(torch.bfloat16)
     outl = np.array([3, 40, 41, 200, 327])
     _run_and_check(tj, X, W, dY, outl, seed=17)
+
+
+def test_linear_calls_equal_their_steps(tj):
+    """tj_linear_fwd / bwd_dx / bwd_dw give bit-identical results to the sequence of
+    public step calls (quantize, requantize, GEMM) that the benchmark times one by one."""
+    g = torch.Generator().manual_seed(12)
+    M, N, K = 256, 384, 520
+    X = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    W = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16).cuda()
+    dY = (torch.randn(M, N, generator=g) * 1e-3).to(torch.bfloat16).cuda()
+    outl = np.sort(np.random.default_rng(3).choice(K, 52, replace=False))
+    ni, oi, wq, w8 = _setup(tj, X.cpu(), W.cpu(), outl)
+    seed = 99
+    y, xq, x8 = tj.linear_fwd(X, wq, w8, ni, oi, out_dtype=torch.float32)
+    dx = tj.linear_bwd_dx(dY, wq, w8, ni, oi, seed=seed, out_dtype=torch.float32)
+    dw = tj.linear_bwd_dw(dY, xq, x8, ni, oi, seed=seed)
+    # the same step, call by call
+    xq2 = tj.quantize_nvfp4(X, sel=ni)
+    x82 = tj.quantize_mxfp8(X, sel=oi)
+    y2 = tj.gemm_nvfp4(xq2, wq, x82, w8)
+    s_dy = tj.quantize_nvfp4(dY, mode=tj.TJ_SR, rht=True, seed=seed, tag=tj.TAG_DY_ROW, rht_tag=tj.TAG_RHT_DX)
+    s_w = tj.requantize_nvfp4(wq, tj.TJ_SR, True, seed, tj.TAG_WT, tj.TAG_RHT_DX)
+    dx2 = torch.zeros(M, K, device="cuda")
+    tj.gemm_nvfp4(s_dy, s_w, alpha=2.0 ** -7, out=dx2, col_map=ni)
+    tj.gemm_mxfp8(tj.quantize_mxfp8(dY), tj.requantize_mxfp8(w8), out=dx2, col_map=oi)
+    s_dyt = tj.quantize_nvfp4(dY, along_cols=True, mode=tj.TJ_SR, rht=True, seed=seed, tag=tj.TAG_DY_COL,
+                              rht_tag=tj.TAG_RHT_DW)
+    s_x = tj.requantize_nvfp4(xq2, tj.TJ_SR, True, seed, tj.TAG_XT, tj.TAG_RHT_DW)
+    dw2 = torch.zeros(N, K, device="cuda")
+    tj.gemm_nvfp4(s_dyt, s_x, alpha=2.0 ** -7, out=dw2, col_map=ni)
+    tj.gemm_mxfp8(tj.quantize_mxfp8(dY, along_cols=True), tj.requantize_mxfp8(x82), out=dw2, col_map=oi)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2) and torch.equal(dx, dx2) and torch.equal(dw, dw2)

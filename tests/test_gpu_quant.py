@@ -143,3 +143,21 @@ def test_argument_errors(tj):
     bad = tj.NVFP4.empty(64, 128)                          # wrong output shape
     with pytest.raises(tj.TjError):
         tj.quantize_nvfp4(x, out=bad)
+
+
+@pytest.mark.parametrize("rows,cols", [(256, 512), (200, 328), (4096, 921)])
+def test_requantize_bit_exact(tj, rows, cols):
+    """Transposed re-alignment (X-hat^T, W-hat^T) of forward operands, NVFP4 and FP8."""
+    x = _input(rows, cols, torch.bfloat16, rows + 3 * cols)
+    q = tj.quantize_nvfp4(x.cuda())
+    r = tj.requantize_nvfp4(q, mode=1, rht=True, seed=21, tag=3, rht_tag=0x100)
+    q8 = tj.quantize_mxfp8(x.cuda())
+    r8 = tj.requantize_mxfp8(q8)
+    torch.cuda.synchronize()
+    c, s, o = Q.quantize_nvfp4(x.float().numpy(), 0)
+    xh = Q.dequantize_nvfp4_f32(c, s, o)[:, :cols]
+    ref = _oracle_rows(np.ascontiguousarray(xh.T), 1, 21, 3, True, 0x100)
+    assert_nvfp4_equal(r, ref, "requantize nvfp4")
+    c8, s8 = Q.quantize_mxfp8(x.float().numpy())
+    xh8 = Q.dequantize_mxfp8_f32(c8, s8)[:, :cols]
+    assert_mxfp8_equal(r8, Q.quantize_mxfp8(np.ascontiguousarray(xh8.T)), "requantize mxfp8")
