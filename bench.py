@@ -255,9 +255,10 @@ class OsciState:
         self.q.reverse()
 
 
-# DRAM bytes per launch measured by ncu for the HBM-bound kernels (profiles/), valid for the
-# kernel version they were taken on; None until a capture of the current version exists.
-TRAFFIC = {}
+# DRAM bytes per element measured by ncu (dram__bytes_read + write of one capture of the
+# current kernel version, divided by its elements), for the HBM-bound kernels; kernels not
+# listed report traffic None.  k_osci_reset: 1913.3 MB over 67,108,864 weights.
+TRAFFIC_BYTES_PER_ELEM = {"k_osci_reset": 28.5}
 NV_B = 0.5 + 1.0 / 16 + 4.0 / 128      # bytes per NVFP4 element (codes + E4M3 + FP32 scales)
 MX_B = 1.0 + 1.0 / 32                   # bytes per MXFP8 element (E4M3 + UE8M0)
 LAUNCHES_PER_LINEAR = 15                # with an FP8 outlier slice: fwd 3, dX 6, dW 6
@@ -378,13 +379,20 @@ def barrier(world):
 
 
 def max_over_ranks(world, v):
+    """Largest value over the ranks (the timed region ends when the slowest replica ends)."""
     if world == 1:
         return v
     import torch.distributed as dist
 
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tflops(world, flops_per_replica_step, steps, max_ms):
+    """Throughput of the whole job: the work of every replica over the slowest replica's time."""
+    return world * flops_per_replica_step * steps / (max_ms * 1e-3) / 1e12
 
 
 def run_reference(args, world, rank):
@@ -492,7 +500,7 @@ def main():
     lin_ms = max_over_ranks(world, sum(v[0] for k, v in summ.items() if k != "osci_reset"))
     osci_ms = summ["osci_reset"][0] / summ["osci_reset"][1]
     flops_step = sum(l.flops for l in linears)
-    value = world * flops_step * args.steps / (lin_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops_step, args.steps, lin_ms)
     osci_gbs = osci.bytes / (osci_ms * 1e-3) / 1e9
     # per call: average ms and throughput against its algorithmic work
     parts = {}
@@ -542,7 +550,8 @@ def main():
     else:
         achieved = by / (ms_tot * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(achieved / hbm_peak, 3), "traffic": TRAFFIC.get(dom),
+                "frac": round(achieved / hbm_peak, 3),
+                "traffic": (round(TRAFFIC_BYTES_PER_ELEM[dom] * osci.n) if dom in TRAFFIC_BYTES_PER_ELEM else None),
                 "algorithmic_bytes_per_launch": round(by / n), "peak_source": peak_src + " hbm_gbs"}
     launches = args.steps * (LAUNCHES_PER_LINEAR * len(linears) + 1)
 
@@ -610,8 +619,7 @@ def measure_e2e(tj, linears, stream, steps, world):
     e.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(world, s.elapsed_time(e))
-    flops = world * sum(l.flops for l in linears) * steps
-    return {"value": round(flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+    return {"value": round(whole_job_tflops(world, sum(l.flops for l in linears), steps, ms), 1), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 4)}
 
 

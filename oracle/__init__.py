@@ -11,7 +11,7 @@ Oscillation Suppression and Outlier Control").  Citations below name the
 "technical summary" (gist.science nl/es/ja pages, which agree section for
 section) by its section: §2.A double-block quantization, §2.B OsciReset,
 §2.C OutControl.  Where the pages are silent, the reading taken is stated at
-the function and collected in the design doc.
+the function that relies on it.
 
 Precision.  Every decision that produces an integer (an E2M1 code, a scale
 byte, a stochastic-rounding choice, a reset bit) is taken in IEEE fp32 with

@@ -7,7 +7,7 @@ consistent (the same channels always have large norms), so the top p% of
 channels (e.g. 10%) are found once, during a short calibration window, and
 kept in higher precision from then on.
 
-Readings (DESIGN.md): channels are the input features of the linear layer;
+Readings: channels are the input features of the linear layer;
 they are ranked by the squared L2 norm summed over the calibration batches;
 k = ceil(p * K); ties go to the lower channel index; the result is returned
 in ascending order together with its ascending complement.  The fp64 sum

@@ -10,7 +10,7 @@ the transposed weight is re-grouped along the new contraction axis) and §2.C
 in FP8 in forward and backward).
 
 Notation: X [M, K], W [N, K], dY [M, N].  O = outlier channels (sorted), k = |O|;
-NC = the other channels, ascending, K_N = K - k.  Readings (DESIGN.md):
+NC = the other channels, ascending, K_N = K - k.  Readings:
   * channels are the input features K; normal channels are compacted in
     ascending order before blocking;
   * both operands of an outlier-slice product are MXFP8 (RTN, no RHT);

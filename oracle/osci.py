@@ -9,7 +9,7 @@ the learning rate is low and the risk exceeds a threshold, the master weight
 of the oscillating element is set to the centre of its current quantization
 bin.
 
-Readings (DESIGN.md):
+Readings:
   * distances are cumulative L1 path lengths in fp32, summed step by step
     from the start of tracking and zeroed on a reset;
   * Q-hat is the fp32 dequantized RTN double-block quantization of the master

@@ -9,7 +9,7 @@ nearest; backward operands use stochastic rounding so that E[round(x)] = x.
 Weight groups are 1x16, i.e. both block levels lie along one row, along the
 contraction dimension of the GEMM that consumes the operand.
 
-Readings taken where the pages are silent (each listed in the design doc):
+Readings taken where the pages are silent:
   * outer scale s_o = amax_128 / (6 * 448) in fp32 (so the largest inner block
     gets the largest inner scale); 2^-149 if that underflows to 0;
   * inner scale s_i = smallest E4M3 value >= amax_16 / (6 * s_o), clamped to 448
