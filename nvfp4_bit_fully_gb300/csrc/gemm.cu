@@ -11,22 +11,32 @@
 // The FP8 slice (kind::mxf8f6f4, UE8M0 per 32) has only power-of-two scales and
 // accumulates over its whole K into one tensor-memory buffer added at the end.
 //
-// Persistent CTAs (one per SM) walk the 128 x 128 output tiles; 10 warps:
-//   warp 0     TMA producer (one lane): operand tiles (128 B rows, 128-byte swizzle)
-//              and scale-factor tiles into a 5-stage ring, and the FP32 outer
-//              scales of every 128-K block into a 16-slot ring (bulk copies);
-//   warp 1     tensor-memory owner and MMA issuer (one lane): tcgen05.cp of the
-//              scale tiles into a 3-slot tensor-memory ring, tcgen05.mma into the
-//              double-buffered partials;
-//   warps 2-9  promotion + epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (its
-//              rows) and columns 64*((w-2)/4) .. +63, accumulates in registers
-//              (one multiply and one FMA per element and block) and writes its row
-//              segment with 16-byte stores.
-// Tensor memory (512 columns): P0 [0,128), P1 [128,256), FP8 accumulator
-// [256,384), scale factors 32 columns per slot [384,480).
+// Persistent CTAs (one per SM, grouped in clusters that share operand tiles by TMA
+// multicast) walk the 128 x 128 output tiles; 20 warps:
+//   warps 0-2   TMA producers (one lane each; stage it is issued by warp it % 3): the
+//               operand tiles (128-byte rows, 128-byte swizzle), their scale-factor
+//               tiles and the FP32 outer scales of the stage's 128-K blocks, all on the
+//               stage's barrier of a 5-stage ring;
+//   warp 3      tensor-memory owner and MMA issuer (lane 0 issues): per block,
+//               tcgen05.cp of its scale-factor tiles and two tcgen05.mma into a
+//               3-slot ring of partials, so the MMAs run up to two blocks ahead of
+//               the promotion;
+//   warps 4-19  promotion + epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (its
+//               rows) and columns 32*((w-4)/4) .. +31, accumulates in registers with
+//               packed f32x2 multiplies and FMAs, and writes its row segment with
+//               16-byte stores.
+// A thread can observe only one barrier handoff every few hundred cycles, so the
+// design keeps handoffs few: the partial slots are released through hardware named
+// barriers, the scale factors of a block share its partial slot's lifetime, and the
+// outer scales travel with the operands.
+// The FP8 slice accumulates over its whole K into the next partial slot, which the
+// promotion adds with weight 1.
+// Tensor memory (512 columns): partials [0,384) (128 per slot), FP4 scale factors
+// [384,432) (16 per partial slot), FP8 scale factors [432,496) (8 per slot).
 // Every mbarrier wait is bounded; a wait that runs out sets the sticky device
-// error flag and an abort flag that makes every role leave its loop, after which
-// in-flight copies and MMAs are drained (bounded) and tensor memory is freed.
+// error flag and an abort flag.  The roles then stop working but keep the named-
+// barrier protocol (whose counts depend only on the problem size), in-flight copies
+// and MMAs are drained (bounded) and tensor memory is freed.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -44,22 +54,32 @@ __device__ unsigned int g_tj_dev_error = 0u;
 namespace {
 
 constexpr int kStages = 5;                     // operand ring (2 x 128-K blocks per stage)
-constexpr int kSfSlots = 3;                    // tensor-memory scale-factor slots (stages in flight)
-constexpr int kScaleSlots = 16;                // FP32 outer-scale ring (one 128-K block per slot; power of 2)
-constexpr int kPromoWarps = 8;                 // 2 per TMEM lane quadrant, 64 columns each
+constexpr int kPSlots = 3;                     // tensor-memory partial slots (128-K blocks in flight)
+constexpr int kSf8Slots = 8;                   // tensor-memory scale-factor slots of FP8 stages
+constexpr int kProdWarps = 3;                  // TMA producers; stage it is issued by warp it % kProdWarps
+constexpr int kMmaWarp = kProdWarps;           // tensor-memory owner and MMA issuer
+constexpr int kPromo0 = kProdWarps + 1;        // first promotion warp
+constexpr int kPromoWarps = 16;                // 4 per TMEM lane quadrant, 32 columns each
 constexpr int kTileBytes = 128 * 128;          // one operand tile: 128 rows x 128 bytes
 constexpr int kSfStageBytes = 2048;            // 4 scale tiles of 512 bytes
 constexpr int kSmemA = 0;
 constexpr int kSmemB = kSmemA + kStages * kTileBytes;
 constexpr int kSmemSfa = kSmemB + kStages * kTileBytes;
 constexpr int kSmemSfb = kSmemSfa + kStages * kSfStageBytes;
-constexpr int kSmemOuter = kSmemSfb + kStages * kSfStageBytes;      // [slot][A 128 | B 128] floats
-constexpr int kSmemBar = kSmemOuter + kScaleSlots * 1024;
+constexpr int kScaleStageBytes = 2048;         // FP32 outer scales of a stage: [A: 2 x 128 | B: 2 x 128]
+constexpr int kSmemScale = kSmemSfb + kStages * kSfStageBytes;
+constexpr int kSmemBar = kSmemScale + kStages * kScaleStageBytes;
 constexpr int kSmemBytes = kSmemBar + 512;
-constexpr int kThreadsGemm = 32 * (2 + kPromoWarps);
-constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
+constexpr int kThreadsGemm = 32 * (kPromo0 + kPromoWarps);
+constexpr int kNamedP = 1;                     // named barriers kNamedP .. +kPSlots-1: partial slot released
+constexpr int kNamedCount = 32 * (1 + kPromoWarps);   // the MMA warp and every promotion warp
+constexpr long long kWaitClk = 4000000000ll;  // per wait: about 2 s at the maximum SM clock, longer below it
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColP = 0, kColAcc8 = 256, kColSf = 384;
+constexpr uint32_t kColP = 0;                                   // partials: 128 columns per slot
+constexpr uint32_t kColSf = 128 * kPSlots;                      // FP4 scale factors: 16 columns per partial slot
+constexpr uint32_t kColSf8 = kColSf + 16 * kPSlots;             // FP8 scale factors: 8 columns per slot
+static_assert(kColSf8 + 8 * kSf8Slots <= kTmemCols, "tensor memory budget");
+static_assert(kNamedP + kPSlots <= 16, "named barriers");
 
 struct GemmArgs {
     int64_t M, N;                 // logical output size
@@ -81,35 +101,50 @@ struct GemmArgs {
 
 struct Bars {
     uint64_t full[kStages], empty[kStages];
-    uint64_t pfull[2], pempty[2];
-    uint64_t sfull[kScaleSlots], sempty[kScaleSlots];
-    uint64_t a8full, a8empty, drain;
+    uint64_t pfull[kPSlots];
+    uint64_t f8free[kSf8Slots];
+    uint64_t drain;
     uint32_t tmem_base;
     volatile int abort_flag;
 };
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Bounded wait on an mbarrier phase: gives up after kWaitNs of wall time (or as
+// Bounded wait on an mbarrier phase: gives up after kWaitClk SM clocks (or as
 // soon as another role has aborted), setting the sticky device error flag and
-// the CTA's abort flag.  No wait in this kernel can spin forever.
+// the CTA's abort flag.  No wait in this kernel can spin forever.  The bound is
+// kept in SM clocks because the clock register is read in a few cycles.
 __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, Bars *bars) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;         // fast path: no clock read
-    const uint64_t t0 = global_ns();
-    for (uint32_t i = 0;; ++i) {
-        // sleep in hardware until the phase completes (or 20 us pass): a waiting
-        // thread takes no issue slots from the warps doing the work
-        if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (ptx::mbar_try_wait(bar, parity)) return true;         // fast path
+    const long long t0 = clock64();
+    for (;;) {
         if (bars->abort_flag) return false;
-        if ((i & 15u) == 15u && global_ns() - t0 > kWaitNs) break;
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > kWaitClk) break;
     }
     atomicOr(&g_tj_dev_error, 1u);
     bars->abort_flag = 1;
     return false;
+}
+
+// Bounded wait that ignores the abort flag: used only to drain asynchronous work
+// (copies, MMAs) that is already in flight before the CTA frees its memory.
+__device__ __forceinline__ void wait_drain(uint64_t *bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitClk) {
+            atomicOr(&g_tj_dev_error, 1u);
+            return;
+        }
+    }
+}
+
+// Hardware named barriers (ids 1..15; 0 is __syncthreads).  `count` threads, a
+// multiple of 32, take part; every warp executes them warp-uniformly.
+__device__ __forceinline__ void named_sync(int id, int count) {
+    asm volatile("barrier.cta.sync.aligned %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int count) {
+    asm volatile("barrier.cta.arrive.aligned %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Warp-uniform bounded wait: lane 0 waits, the verdict is broadcast, and
@@ -134,6 +169,28 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t sf_id) {
            (sf_id << 29);
 }
 
+// Packed pairs of fp32 (element 0 in the low half): one instruction for two lanes of work.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ float lo2(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi2(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 template <int CM, int CN>
 __global__ void __launch_bounds__(kThreadsGemm, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tm_a4, const __grid_constant__ CUtensorMap tm_b4,
@@ -142,7 +199,6 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars *bars = reinterpret_cast<Bars *>(smem + kSmemBar);
-    float *outer_s = reinterpret_cast<float *>(smem + kSmemOuter);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // cluster of CM x CN CTAs computing a (CM*128) x (CN*128) block of tiles; the CTAs
     // with the same m share the A tile, those with the same n the B tile
@@ -156,39 +212,33 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     auto tile_n0 = [&](int ct) { return (int64_t)((ct % ctn) * CN + cn) * 128; };
     const int nst4 = (args.nkb4 + 1) / 2;
     const int nstages = nst4 + args.nk8;
+    const int nblk = args.nkb4 + (args.nk8 > 0 ? 1 : 0);  // partials per tile (the FP8 slice is one)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(&bars->full[s], 1);
             ptx::mbar_init(&bars->empty[s], CS);            // every CTA of the cluster releases each stage
         }
-        for (int p = 0; p < 2; ++p) {
-            ptx::mbar_init(&bars->pfull[p], 1);
-            ptx::mbar_init(&bars->pempty[p], kPromoWarps);
-        }
-        for (int s = 0; s < kScaleSlots; ++s) {
-            ptx::mbar_init(&bars->sfull[s], 1);
-            ptx::mbar_init(&bars->sempty[s], kPromoWarps);
-        }
-        ptx::mbar_init(&bars->a8full, 1);
-        ptx::mbar_init(&bars->a8empty, kPromoWarps);
+        for (int p = 0; p < kPSlots; ++p) ptx::mbar_init(&bars->pfull[p], 1);
+        for (int f = 0; f < kSf8Slots; ++f) ptx::mbar_init(&bars->f8free[f], 1);
         ptx::mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 1) ptx::tmem_alloc(&bars->tmem_base, kTmemCols);
+    if (warp == kMmaWarp) ptx::tmem_alloc(&bars->tmem_base, kTmemCols);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     if (CS > 1) ptx::cluster_sync();                        // partners' barriers exist before any multicast
     const uint32_t tbase = bars->tmem_base;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp < kProdWarps) {
+        // ------------------------------------------------------------ producers: one thread can
+        // issue a stage only every few hundred cycles, so stages alternate between warps
         if (lane == 0) {
             if (args.nkb4 > 0) { ptx::prefetch_tmap(&tm_a4); ptx::prefetch_tmap(&tm_b4); }
             if (args.nk8 > 0) { ptx::prefetch_tmap(&tm_a8); ptx::prefetch_tmap(&tm_b8); }
-            int it = 0, sk = 0;
+            int it = 0;
             bool ok = true;
             // multicast masks: the CTAs sharing this CTA's A tile (same cm) and B tile (same cn)
             uint16_t mask_a = 0, mask_b = 0;
@@ -199,6 +249,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                 const int64_t m0 = tile_m0(tile), n0 = tile_n0(tile);
                 const int64_t rta = m0 / 128, rtb = n0 / 128;
                 for (int st = 0; st < nstages; ++st, ++it) {
+                    if (it % kProdWarps != warp) continue;
                     const int slot = it % kStages;
                     if (it >= kStages && !wait_bounded(&bars->empty[slot], ((it / kStages) - 1) & 1, bars)) {
                         ok = false;
@@ -208,217 +259,230 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     uint8_t *sb = smem + kSmemB + slot * kTileBytes;
                     uint8_t *sfa = smem + kSmemSfa + slot * kSfStageBytes;
                     uint8_t *sfb = smem + kSmemSfb + slot * kSfStageBytes;
-                    if (st < nst4) {
-                        const int nkbs = min(2, args.nkb4 - 2 * st);
-                        const uint32_t sfbytes = (uint32_t)nkbs * 1024u;
-                        ptx::mbar_arrive_expect_tx(&bars->full[slot], 2u * kTileBytes + 2u * sfbytes);
-                        if (CN > 1)
-                            ptx::tma_load_2d_multicast(sa + cn * ra * 128, &tm_a4, st * 128, (int32_t)(m0 + cn * ra),
-                                                       &bars->full[slot], mask_a);
-                        else
-                            ptx::tma_load_2d(sa, &tm_a4, st * 128, (int32_t)m0, &bars->full[slot]);
-                        if (CM > 1)
-                            ptx::tma_load_2d_multicast(sb + cm * rb * 128, &tm_b4, st * 128, (int32_t)(n0 + cm * rb),
-                                                       &bars->full[slot], mask_b);
-                        else
-                            ptx::tma_load_2d(sb, &tm_b4, st * 128, (int32_t)n0, &bars->full[slot]);
+                    const bool fp4 = st < nst4;
+                    const int k0 = fp4 ? st : st - nst4;              // 128-byte column of the operand rows
+                    const CUtensorMap *ta = fp4 ? &tm_a4 : &tm_a8;
+                    const CUtensorMap *tb = fp4 ? &tm_b4 : &tm_b8;
+                    const int nkbs = fp4 ? min(2, args.nkb4 - 2 * st) : 0;
+                    const uint32_t sfbytes = fp4 ? (uint32_t)nkbs * 1024u : 512u;
+                    // operands, their scale-factor tiles and, for FP4 stages, the FP32 outer
+                    // scales of the stage's blocks all land on one barrier
+                    ptx::mbar_arrive_expect_tx(&bars->full[slot],
+                                               2u * kTileBytes + 2u * sfbytes + (uint32_t)nkbs * 1024u);
+                    if (CN > 1)
+                        ptx::tma_load_2d_multicast(sa + cn * ra * 128, ta, k0 * 128, (int32_t)(m0 + cn * ra),
+                                                   &bars->full[slot], mask_a);
+                    else
+                        ptx::tma_load_2d(sa, ta, k0 * 128, (int32_t)m0, &bars->full[slot]);
+                    if (CM > 1)
+                        ptx::tma_load_2d_multicast(sb + cm * rb * 128, tb, k0 * 128, (int32_t)(n0 + cm * rb),
+                                                   &bars->full[slot], mask_b);
+                    else
+                        ptx::tma_load_2d(sb, tb, k0 * 128, (int32_t)n0, &bars->full[slot]);
+                    if (fp4) {
                         ptx::bulk_load(sfa, args.sfa4 + (rta * args.ntk_a4 + 4 * st) * 512, sfbytes, &bars->full[slot]);
                         ptx::bulk_load(sfb, args.sfb4 + (rtb * args.ntk_b4 + 4 * st) * 512, sfbytes, &bars->full[slot]);
-                        // the FP32 outer scales of these blocks, for the promotion warps
-                        for (int j = 0; j < nkbs && ok; ++j, ++sk) {
-                            const int ss = sk % kScaleSlots;
-                            if (sk >= kScaleSlots &&
-                                !wait_bounded(&bars->sempty[ss], ((sk / kScaleSlots) - 1) & 1, bars)) {
-                                ok = false;
-                                break;
-                            }
+                        uint8_t *so = smem + kSmemScale + slot * kScaleStageBytes;
+                        for (int j = 0; j < nkbs; ++j) {
                             const int64_t kb = 2 * st + j;
-                            ptx::mbar_arrive_expect_tx(&bars->sfull[ss], 1024u);
-                            ptx::bulk_load(outer_s + ss * 256, args.outa + kb * args.rpa + m0, 512u, &bars->sfull[ss]);
-                            ptx::bulk_load(outer_s + ss * 256 + 128, args.outb + kb * args.rpb + n0, 512u,
-                                           &bars->sfull[ss]);
+                            ptx::bulk_load(so + 512 * j, args.outa + kb * args.rpa + m0, 512u, &bars->full[slot]);
+                            ptx::bulk_load(so + 1024 + 512 * j, args.outb + kb * args.rpb + n0, 512u, &bars->full[slot]);
                         }
-                        if (!ok) { ++it; break; }
                     } else {
-                        const int s8 = st - nst4;
-                        ptx::mbar_arrive_expect_tx(&bars->full[slot], 2u * kTileBytes + 1024u);
-                        if (CN > 1)
-                            ptx::tma_load_2d_multicast(sa + cn * ra * 128, &tm_a8, s8 * 128, (int32_t)(m0 + cn * ra),
-                                                       &bars->full[slot], mask_a);
-                        else
-                            ptx::tma_load_2d(sa, &tm_a8, s8 * 128, (int32_t)m0, &bars->full[slot]);
-                        if (CM > 1)
-                            ptx::tma_load_2d_multicast(sb + cm * rb * 128, &tm_b8, s8 * 128, (int32_t)(n0 + cm * rb),
-                                                       &bars->full[slot], mask_b);
-                        else
-                            ptx::tma_load_2d(sb, &tm_b8, s8 * 128, (int32_t)n0, &bars->full[slot]);
-                        ptx::bulk_load(sfa, args.sfa8 + (rta * args.ntk_a8 + s8) * 512, 512u, &bars->full[slot]);
-                        ptx::bulk_load(sfb, args.sfb8 + (rtb * args.ntk_b8 + s8) * 512, 512u, &bars->full[slot]);
+                        ptx::bulk_load(sfa, args.sfa8 + (rta * args.ntk_a8 + k0) * 512, 512u, &bars->full[slot]);
+                        ptx::bulk_load(sfb, args.sfb8 + (rtb * args.ntk_b8 + k0) * 512, 512u, &bars->full[slot]);
                     }
                 }
             }
-            // drain: every copy issued must have landed before the CTA exits
+            // drain: every copy this warp issued must have landed before the CTA exits
             for (int j = (it > kStages ? it - kStages : 0); j < it; ++j)
-                wait_bounded(&bars->full[j % kStages], (j / kStages) & 1, bars);
-            for (int j = (sk > kScaleSlots ? sk - kScaleSlots : 0); j < sk; ++j)
-                wait_bounded(&bars->sfull[j % kScaleSlots], (j / kScaleSlots) & 1, bars);
+                if (j % kProdWarps == warp) wait_drain(&bars->full[j % kStages], (j / kStages) & 1);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc4 = idesc_nvf4();
-            int it = 0, pcount = 0, a8count = 0;
-            bool ok = true;
-            for (int tile = cid; tile < ntiles && ok; tile += ncl) {
-                for (int st = 0; st < nstages; ++st, ++it) {
-                    const int slot = it % kStages;
-                    if (!wait_bounded(&bars->full[slot], (it / kStages) & 1, bars)) { ok = false; break; }
-                    ptx::tc_fence_after();
-                    const uint32_t sa = ptx::smem_u32(smem + kSmemA + slot * kTileBytes);
-                    const uint32_t sb = ptx::smem_u32(smem + kSmemB + slot * kTileBytes);
-                    const uint32_t sfa = ptx::smem_u32(smem + kSmemSfa + slot * kSfStageBytes);
-                    const uint32_t sfb = ptx::smem_u32(smem + kSmemSfb + slot * kSfStageBytes);
-                    // scale-factor slot it % kSfSlots was last read by the MMAs of stage
-                    // it - kSfSlots; those have completed once that stage's ring slot was
-                    // released (its empty barrier phase)
-                    if (it >= kSfSlots) {
-                        const int prev = it - kSfSlots;
-                        if (!wait_bounded(&bars->empty[prev % kStages], (prev / kStages) & 1, bars)) {
-                            ok = false;
-                            break;
-                        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer (warp-uniform loop;
+        // lane 0 issues).  Before a partial slot is rewritten, the named barrier of that slot
+        // meets every promotion warp's release of the block that used it three blocks earlier;
+        // that also frees the slot's scale-factor columns, which only that block's MMAs read.
+        const uint32_t idesc4 = idesc_nvf4();
+        int it = 0, pc = 0, g8 = 0;
+        bool live = true;
+        // An FP4 stage also holds the outer scales of its blocks, which the promotion warps
+        // read after releasing a block's partial and before releasing the next one.  So the
+        // stage whose last block is b is released once the barrier of block b + 1 is met:
+        // Byte (b + 1) & 3 of `rel` holds its ring slot + 1 until then (0: nothing to release).
+        uint32_t rel = 0u;
+        auto release = [&](int idx) {
+            const int r = (int)((rel >> (8 * idx)) & 0xffu) - 1;
+            if (r >= 0 && live && lane == 0) {
+                if (CS > 1)
+                    ptx::tc_commit_multicast(&bars->empty[r], (uint16_t)((1u << CS) - 1u));
+                else
+                    ptx::tc_commit(&bars->empty[r]);
+            }
+            rel &= ~(0xffu << (8 * idx));
+        };
+        for (int tile = cid; tile < ntiles; tile += ncl) {
+            for (int st = 0; st < nstages; ++st, ++it) {
+                const int slot = it % kStages;
+                if (live) live = warp_wait_bounded(&bars->full[slot], (it / kStages) & 1, bars, lane);
+                ptx::tc_fence_after();
+                const uint32_t sa = ptx::smem_u32(smem + kSmemA + slot * kTileBytes);
+                const uint32_t sb = ptx::smem_u32(smem + kSmemB + slot * kTileBytes);
+                const uint32_t sfa = ptx::smem_u32(smem + kSmemSfa + slot * kSfStageBytes);
+                const uint32_t sfb = ptx::smem_u32(smem + kSmemSfb + slot * kSfStageBytes);
+                if (st < nst4) {
+                    const int nkbs = min(2, args.nkb4 - 2 * st);
+                    for (int kbl = 0; kbl < nkbs; ++kbl, ++pc) {
+                        const int ps = pc % kPSlots;
+                        if (pc >= kPSlots) named_sync(kNamedP + ps, kNamedCount);
+                        release((pc + 1) & 3);
                         ptx::tc_fence_after();
-                    }
-                    const uint32_t sfcol = tbase + kColSf + 32u * (uint32_t)(it % kSfSlots);
-                    if (st < nst4) {
-                        const int nkbs = min(2, args.nkb4 - 2 * st);
-                        for (int j = 0; j < 2 * nkbs; ++j) {   // one 512-byte scale tile per K = 64 MMA
-                            ptx::tc_cp_32x128b_warpx4(sfcol + 4 * j, ptx::smem_desc(sfa + 512 * j, 0, 128, 0));
-                            ptx::tc_cp_32x128b_warpx4(sfcol + 16 + 4 * j, ptx::smem_desc(sfb + 512 * j, 0, 128, 0));
-                        }
-                        for (int kbl = 0; kbl < nkbs; ++kbl) {
-                            const int pb = pcount & 1;
-                            if (pcount >= 2 && !wait_bounded(&bars->pempty[pb], ((pcount >> 1) - 1) & 1, bars)) {
-                                ok = false;
-                                break;
+                        if (live && lane == 0) {
+                            const uint32_t sfcol = tbase + kColSf + 16u * (uint32_t)ps;
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {   // one 512-byte scale tile per K = 64 MMA
+                                ptx::tc_cp_32x128b_warpx4(sfcol + 4 * j,
+                                                          ptx::smem_desc(sfa + 512 * (2 * kbl + j), 0, 128, 0));
+                                ptx::tc_cp_32x128b_warpx4(sfcol + 8 + 4 * j,
+                                                          ptx::smem_desc(sfb + 512 * (2 * kbl + j), 0, 128, 0));
                             }
-                            ptx::tc_fence_after();
 #pragma unroll
                             for (int j = 0; j < 2; ++j) {
                                 const uint32_t koff = 64u * kbl + 32u * j;
-                                ptx::mma_nvf4(tbase + kColP + 128u * pb, ptx::smem_desc(sa + koff, 16, 1024, 2),
-                                              ptx::smem_desc(sb + koff, 16, 1024, 2), idesc4,
-                                              sfcol + 4 * (2 * kbl + j), sfcol + 16 + 4 * (2 * kbl + j), (uint32_t)j);
+                                ptx::mma_nvf4(tbase + kColP + 128u * ps, ptx::smem_desc(sa + koff, 16, 1024, 2),
+                                              ptx::smem_desc(sb + koff, 16, 1024, 2), idesc4, sfcol + 4 * j,
+                                              sfcol + 8 + 4 * j, (uint32_t)j);
                             }
-                            ptx::tc_commit(&bars->pfull[pb]);
-                            ++pcount;
+                            ptx::tc_commit(&bars->pfull[ps]);
                         }
-                        if (!ok) break;
-                    } else {
-                        const int s8 = st - nst4;
-                        if (s8 == 0 && a8count >= 1 &&
-                            !wait_bounded(&bars->a8empty, (a8count - 1) & 1, bars)) {
-                            ok = false;
-                            break;
-                        }
-                        ptx::tc_fence_after();
+                        __syncwarp();
+                        if (kbl == nkbs - 1) rel |= (uint32_t)(slot + 1) << (8 * ((pc + 1) & 3));
+                    }
+                } else {
+                    // the FP8 slice: all its stages accumulate into one partial slot; their
+                    // scale factors rotate through kSf8Slots slots freed by commits
+                    const int s8 = st - nst4;
+                    const int ps = pc % kPSlots;
+                    if (s8 == 0) {
+                        if (pc >= kPSlots) named_sync(kNamedP + ps, kNamedCount);
+                        release((pc + 1) & 3);
+                    }
+                    const int f8 = g8 % kSf8Slots;
+                    if (live && g8 >= kSf8Slots)
+                        live = warp_wait_bounded(&bars->f8free[f8], ((g8 / kSf8Slots) - 1) & 1, bars, lane);
+                    ptx::tc_fence_after();
+                    if (live && lane == 0) {
+                        const uint32_t sfcol = tbase + kColSf8 + 8u * (uint32_t)f8;
                         ptx::tc_cp_32x128b_warpx4(sfcol, ptx::smem_desc(sfa, 0, 128, 0));
-                        ptx::tc_cp_32x128b_warpx4(sfcol + 16, ptx::smem_desc(sfb, 0, 128, 0));
+                        ptx::tc_cp_32x128b_warpx4(sfcol + 4, ptx::smem_desc(sfb, 0, 128, 0));
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            ptx::mma_mxf8(tbase + kColAcc8, ptx::smem_desc(sa + 32u * j, 16, 1024, 2),
+                            ptx::mma_mxf8(tbase + kColP + 128u * ps, ptx::smem_desc(sa + 32u * j, 16, 1024, 2),
                                           ptx::smem_desc(sb + 32u * j, 16, 1024, 2), idesc_mxf8((uint32_t)j), sfcol,
-                                          sfcol + 16, (uint32_t)(s8 > 0 || j > 0));
+                                          sfcol + 4, (uint32_t)(s8 > 0 || j > 0));
                         }
-                        if (s8 == args.nk8 - 1) {
-                            ptx::tc_commit(&bars->a8full);
-                            ++a8count;
-                        }
+                        ptx::tc_commit(&bars->f8free[f8]);
+                        if (s8 == args.nk8 - 1) ptx::tc_commit(&bars->pfull[ps]);
                     }
-                    // release the stage in every CTA whose shared memory this cluster's loads fill
+                    __syncwarp();
+                    ++g8;
+                    if (s8 == args.nk8 - 1) ++pc;
+                }
+                // an FP8 stage (no outer scales) is released in every CTA whose shared memory
+                // this cluster's loads fill as soon as its MMAs complete
+                if (st >= nst4 && live && lane == 0) {
                     if (CS > 1)
                         ptx::tc_commit_multicast(&bars->empty[slot], (uint16_t)((1u << CS) - 1u));
                     else
                         ptx::tc_commit(&bars->empty[slot]);
                 }
+                __syncwarp();
             }
-            // drain: all MMAs / copies issued by this thread complete before TMEM is freed
-            ptx::tc_commit(&bars->drain);
-            wait_bounded(&bars->drain, 0, bars);
         }
+        // meet the promotion warps' releases of the last blocks
+        for (int j = (pc > kPSlots ? pc - kPSlots : 0); j < pc; ++j) {
+            named_sync(kNamedP + j % kPSlots, kNamedCount);
+            release(j & 3);
+        }
+        // all MMAs / copies issued by this thread complete before TMEM is freed
+        if (lane == 0) {
+            ptx::tc_commit(&bars->drain);
+            wait_drain(&bars->drain, 0);
+        }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ promotion + epilogue
-        const int pw = warp - 2;
+        const int pw = warp - kPromo0;
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
-        const int h = pw >> 2;                  // column half: columns 64*h .. +63
-        const int row_l = 32 * q + lane;
-        const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-        int kbc = 0, a8c = 0;
-        bool ok = true;
-        for (int tile = cid; tile < ntiles && ok; tile += ncl) {
-            float acc[64];
-#pragma unroll
-            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
-            for (int kb = 0; kb < args.nkb4; ++kb, ++kbc) {
-                const int pb = kbc & 1;
-                const int ss = kbc & (kScaleSlots - 1);
-                if (!warp_wait_bounded(&bars->pfull[pb], (kbc >> 1) & 1, bars, lane)) { ok = false; break; }
-                ptx::tc_fence_after();
-                uint32_t p0[32], p1[32];
-                ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColP + 128u * pb + 64u * h, p0);
-                ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColP + 128u * pb + 64u * h + 32u, p1);
-                ptx::tmem_wait_ld();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&bars->pempty[pb]);
-                if (!warp_wait_bounded(&bars->sfull[ss], (kbc / kScaleSlots) & 1, bars, lane)) { ok = false; break; }
-                const float sa = outer_s[ss * 256 + row_l] * args.alpha;
-                const float4 *sbp = reinterpret_cast<const float4 *>(outer_s + ss * 256 + 128 + 64 * h);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float4 sb = sbp[i];                     // broadcast read: all lanes, same address
-                    const uint32_t *pp = i < 8 ? p0 : p1;
-                    const int jj = (4 * i) & 31;
-                    acc[4 * i] = fmaf(__uint_as_float(pp[jj]), sa * sb.x, acc[4 * i]);
-                    acc[4 * i + 1] = fmaf(__uint_as_float(pp[jj + 1]), sa * sb.y, acc[4 * i + 1]);
-                    acc[4 * i + 2] = fmaf(__uint_as_float(pp[jj + 2]), sa * sb.z, acc[4 * i + 2]);
-                    acc[4 * i + 3] = fmaf(__uint_as_float(pp[jj + 3]), sa * sb.w, acc[4 * i + 3]);
-                }
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&bars->sempty[ss]);
-            }
-            if (!ok) break;
-            if (args.nk8 > 0) {
-                if (!warp_wait_bounded(&bars->a8full, a8c & 1, bars, lane)) { ok = false; break; }
-                ptx::tc_fence_after();
-                uint32_t p0[32], p1[32];
-                ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColAcc8 + 64u * h, p0);
-                ptx::tmem_ld_32x32b_x32(tbase + lane_addr + kColAcc8 + 64u * h + 32u, p1);
-                ptx::tmem_wait_ld();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&bars->a8empty);
-                ++a8c;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    acc[j] += __uint_as_float(p0[j]);
-                    acc[32 + j] += __uint_as_float(p1[j]);
-                }
-            }
-            // epilogue: this thread's row segment of 64 columns, written with 16-byte stores
+        const int cq = pw >> 2;                 // column quarter: columns 32*cq .. +31
+        const uint32_t taddr0 = tbase + ((uint32_t)(32 * q) << 16) + kColP + 32u * (uint32_t)cq;
+        int it_tile = 0;                        // operand ring position of the tile's first stage
+        int ps = 0;
+        uint32_t pph = 0;                       // partial ring slot and phase
+        bool live = true;                       // false after an abort: the barrier protocol goes on, the work stops
+        for (int tile = cid; tile < ntiles; tile += ncl, it_tile += nstages) {
             const int64_t m0 = tile_m0(tile), n0 = tile_n0(tile);
-            const int64_t row = m0 + row_l;
-            const int64_t nb = n0 + 64 * h;
+            uint64_t acc[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = 0ull;
+            for (int kb = 0; kb < nblk; ++kb) {
+                uint32_t p[32];
+                if (live) live = warp_wait_bounded(&bars->pfull[ps], pph, bars, lane);
+                if (live) {
+                    ptx::tc_fence_after();
+                    ptx::tmem_ld_32x32b_x32(taddr0 + 128u * (uint32_t)ps, p);
+                    ptx::tmem_wait_ld();
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                // release the partial slot.  A live warp arrives without waiting: it reached
+                // this block only after the MMA warp had met the previous use of the slot.  A
+                // warp that has stopped waiting for partials waits here instead, so that it
+                // never arrives twice on one barrier generation.
+                if (live)
+                    named_arrive(kNamedP + ps, kNamedCount);
+                else
+                    named_sync(kNamedP + ps, kNamedCount);
+                if (++ps == kPSlots) { ps = 0; pph ^= 1u; }
+                if (kb < args.nkb4) {
+                    if (live) {
+                        // the block's outer scales, delivered with its operand stage (which is
+                        // released only after the next block's partial has been released)
+                        const float *so = reinterpret_cast<const float *>(
+                            smem + kSmemScale + ((it_tile + kb / 2) % kStages) * kScaleStageBytes);
+                        const float sa = so[128 * (kb & 1) + 32 * q + lane] * args.alpha;
+                        const uint64_t sa2 = pack2(sa, sa);
+                        const float4 *sbp = reinterpret_cast<const float4 *>(so + 256 + 128 * (kb & 1) + 32 * cq);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 sb = sbp[i];             // broadcast read: all lanes, same address
+                            const uint64_t w0 = mul2(sa2, pack2(sb.x, sb.y));
+                            const uint64_t w1 = mul2(sa2, pack2(sb.z, sb.w));
+                            acc[2 * i] = fma2((uint64_t)p[4 * i] | ((uint64_t)p[4 * i + 1] << 32), w0, acc[2 * i]);
+                            acc[2 * i + 1] =
+                                fma2((uint64_t)p[4 * i + 2] | ((uint64_t)p[4 * i + 3] << 32), w1, acc[2 * i + 1]);
+                        }
+                    }
+                } else if (live) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        acc[i] = add2(acc[i], (uint64_t)p[2 * i] | ((uint64_t)p[2 * i + 1] << 32));
+                }
+            }
+            if (!live) continue;
+            // epilogue: this thread's row segment of 32 columns, written with 16-byte stores
+            const int64_t row = m0 + 32 * q + lane;
+            const int64_t nb = n0 + 32 * cq;
             if (row < args.M) {
-                const bool fast = args.col_map == nullptr && nb + 64 <= args.N && (args.ldd & 7) == 0;
+                const bool fast = args.col_map == nullptr && nb + 32 <= args.N && (args.ldd & 7) == 0;
                 if (fast && args.out_bf16) {
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.d) + row * args.ldd + nb);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
+                    for (int i = 0; i < 4; ++i) {
                         uint32_t w4[4];
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[8 * i + 2 * k], acc[8 * i + 2 * k + 1]);
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(lo2(acc[4 * i + k]), hi2(acc[4 * i + k]));
                             w4[k] = *reinterpret_cast<uint32_t *>(&b2);
                         }
                         dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
@@ -426,18 +490,19 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                 } else if (fast) {
                     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(args.d) + row * args.ldd + nb);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(lo2(acc[2 * i]), hi2(acc[2 * i]), lo2(acc[2 * i + 1]), hi2(acc[2 * i + 1]));
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) {
+                    for (int j = 0; j < 32; ++j) {
                         const int64_t n = nb + j;
+                        const float v = (j & 1) ? hi2(acc[j >> 1]) : lo2(acc[j >> 1]);
                         if (n < args.N) {
                             const int64_t col = args.col_map ? (int64_t)args.col_map[n] : n;
                             if (args.out_bf16)
-                                static_cast<__nv_bfloat16 *>(args.d)[row * args.ldd + col] = __float2bfloat16_rn(acc[j]);
+                                static_cast<__nv_bfloat16 *>(args.d)[row * args.ldd + col] = __float2bfloat16_rn(v);
                             else
-                                static_cast<float *>(args.d)[row * args.ldd + col] = acc[j];
+                                static_cast<float *>(args.d)[row * args.ldd + col] = v;
                         }
                     }
                 }
@@ -447,7 +512,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     ptx::tc_fence_before();
     __syncthreads();
     if (CS > 1) ptx::cluster_sync();                        // no partner still writes into this CTA
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tbase, kTmemCols);
     }
