@@ -101,3 +101,31 @@ def test_gemm_fp4_plus_fp8_same_tile(tj):
     ref = OL.gemm_fp4(ra, rb) + OL.gemm_fp8(ra8, rb8)
     bound = abs_product(ra, rb) + abs_product_fp8(ra8, rb8)
     assert_gemm_close(d.cpu().numpy(), ref, bound, what="fp4+fp8")
+
+
+def test_gemm_pipeline_over_many_tiles(tj):
+    """More tiles than SMs (each CTA walks several), an odd number of FP4 blocks (a half
+    last stage) and an FP8 slice of six 128-K stages in the same tiles, so that partial
+    slots, scale-factor slots and the outer-scale ring all wrap across tile boundaries."""
+    M, N, K, k = 2048, 1536, 640, 700
+    qa, qb, ra, rb = _operands(tj, M, N, K, seed=21)
+    a8, b8, ra8, rb8 = _fp8_operands(tj, M, N, k, seed=22)
+    d = tj.gemm_nvfp4(qa, qb, a8, b8, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    tj.device_status()
+    rows = np.random.default_rng(5).choice(M, 96, replace=False)
+    sub = lambda q: tuple(x[rows] for x in q)
+    ref = OL.gemm_fp4(sub(ra), rb) + OL.gemm_fp8(sub(ra8), rb8)
+    bound = abs_product(sub(ra), rb) + abs_product_fp8(sub(ra8), rb8)
+    assert_gemm_close(d.float().cpu().numpy()[rows], ref, bound, bf16=True, what="many tiles fp4+fp8")
+
+
+def test_gemm_fp8_slice_long(tj):
+    """An FP8-only product whose K spans more stages than the FP8 scale-factor slots."""
+    M, N, k = 384, 256, 1500
+    a8, b8, ra, rb = _fp8_operands(tj, M, N, k, seed=31)
+    d = tj.gemm_mxfp8(a8, b8)
+    torch.cuda.synchronize()
+    tj.device_status()
+    ref = OL.gemm_fp8(ra, rb)
+    assert_gemm_close(d.cpu().numpy(), ref, abs_product_fp8(ra, rb), what="fp8 long")
