@@ -73,7 +73,9 @@ constexpr int kSmemSfb = kSmemSfa + kStages * kSfStageBytes;
 constexpr int kScaleSlots = 8;                 // FP32 outer-scale ring: one FP4 block per slot, [A 128 | B 128]
 constexpr int kSmemScale = kSmemSfb + kStages * kSfStageBytes;
 constexpr int kSmemBar = kSmemScale + kScaleSlots * 1024;
-constexpr int kSmemBytes = kSmemBar + 512;
+constexpr int kSmemEpi = kSmemBar + 512;       // per promotion warp: 32 rows x 33 words (epilogue staging)
+constexpr int kSmemBytes = kSmemEpi + kPromoWarps * 32 * 33 * 4;
+static_assert(kSmemBytes + 1024 <= 227 * 1024, "shared memory budget");
 constexpr int kThreadsGemm = 32 * (kPromo0 + kPromoWarps);
 constexpr int kNamedP = 1;                     // named barriers kNamedP .. +kPSlots-1: partial slot released
 constexpr int kNamedCount = 32 * (1 + kPromoWarps);   // the MMA warp and every promotion warp
@@ -493,12 +495,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                 if (kb < args.nkb4) ++f4c;
             }
             if (!live) continue;
-            // epilogue: this thread's row segment of kColsW columns, written with 16-byte stores
+            // epilogue.  Plain case: this thread's row segment of kColsW columns, written with
+            // 16-byte stores
             const int64_t row = m0 + 32 * q + lane;
             const int64_t nb = n0 + kColsW * cq;
-            if (row < args.M) {
-                const bool fast = args.col_map == nullptr && nb + kColsW <= args.N && (args.ldd & 7) == 0;
-                if (fast && args.out_bf16) {
+            const bool fast_tile = args.col_map == nullptr && nb + kColsW <= args.N && (args.ldd & 7) == 0;
+            if (fast_tile && row < args.M) {
+                if (args.out_bf16) {
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.d) + row * args.ldd + nb);
 #pragma unroll
                     for (int i = 0; i < kColsW / 8; ++i) {
@@ -510,24 +513,57 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                         }
                         dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
-                } else if (fast) {
+                } else {
                     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(args.d) + row * args.ldd + nb);
 #pragma unroll
                     for (int i = 0; i < kColsW / 4; ++i)
                         dst[i] = make_float4(lo2(acc[2 * i]), hi2(acc[2 * i]), lo2(acc[2 * i + 1]), hi2(acc[2 * i + 1]));
-                } else {
+                }
+            }
+            if (fast_tile) continue;
+            // scattered columns (col_map), a ragged right edge or an unaligned row pitch: the
+            // warp stages its 32 x kColsW slice in shared memory and writes it row by row, a
+            // lane per column, so each store instruction covers one contiguous row segment
+            uint32_t *stg = reinterpret_cast<uint32_t *>(smem + kSmemEpi) + pw * (32 * 33);
+            const int64_t rbase = m0 + 32 * q;
+            if (args.out_bf16) {
 #pragma unroll
-                    for (int j = 0; j < kColsW; ++j) {
-                        const int64_t n = nb + j;
-                        const float v = (j & 1) ? hi2(acc[j >> 1]) : lo2(acc[j >> 1]);
-                        if (n < args.N) {
-                            const int64_t col = args.col_map ? (int64_t)args.col_map[n] : n;
-                            if (args.out_bf16)
-                                static_cast<__nv_bfloat16 *>(args.d)[row * args.ldd + col] = __float2bfloat16_rn(v);
-                            else
-                                static_cast<float *>(args.d)[row * args.ldd + col] = v;
-                        }
+                for (int j = 0; j < kColsW / 2; ++j) {
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(lo2(acc[j]), hi2(acc[j]));
+                    stg[lane * 33 + j] = *reinterpret_cast<uint32_t *>(&b2);
+                }
+                __syncwarp();
+                const int64_t na = nb + 2 * lane, nz = na + 1;   // this lane's column pair
+                const bool va = na < args.N, vz = nz < args.N;
+                const int64_t ca = va ? (args.col_map ? (int64_t)args.col_map[na] : na) : 0;
+                const int64_t cz = vz ? (args.col_map ? (int64_t)args.col_map[nz] : nz) : 0;
+                const bool pair = va && vz && cz == ca + 1 && ((ca | args.ldd) & 1) == 0;
+                for (int r = 0; r < 32 && rbase + r < args.M; ++r) {
+                    const uint32_t w = stg[r * 33 + lane];
+                    __nv_bfloat16 *drow = static_cast<__nv_bfloat16 *>(args.d) + (rbase + r) * args.ldd;
+                    if (pair) {
+                        *reinterpret_cast<uint32_t *>(drow + ca) = w;
+                    } else {
+                        if (va) drow[ca] = __ushort_as_bfloat16((unsigned short)(w & 0xffffu));
+                        if (vz) drow[cz] = __ushort_as_bfloat16((unsigned short)(w >> 16));
                     }
+                }
+                __syncwarp();
+            } else {
+#pragma unroll
+                for (int h = 0; h < kColsW / 32; ++h) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int e = 32 * h + j;
+                        stg[lane * 33 + j] = __float_as_uint((e & 1) ? hi2(acc[e >> 1]) : lo2(acc[e >> 1]));
+                    }
+                    __syncwarp();
+                    const int64_t n = nb + 32 * h + lane;
+                    const bool v = n < args.N;
+                    const int64_t c = v ? (args.col_map ? (int64_t)args.col_map[n] : n) : 0;
+                    for (int r = 0; r < 32 && rbase + r < args.M; ++r)
+                        if (v) static_cast<float *>(args.d)[(rbase + r) * args.ldd + c] = __uint_as_float(stg[r * 33 + lane]);
+                    __syncwarp();
                 }
             }
         }
