@@ -27,6 +27,31 @@ struct SrcDense {
     }
     __device__ static __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
     __device__ static __forceinline__ float to_f(float v) { return v; }
+    // elem(r, c .. c+7), c a multiple of 8: one or two 16-byte loads when the octet is
+    // inside the tensor, unselected and 16-byte aligned
+    __device__ __forceinline__ void load8(int64_t r, int64_t c, float (&v)[8]) const {
+        const T *q = p + r * ld + c;
+        if (sel == nullptr && r < rows && c + 8 <= cols && (reinterpret_cast<uintptr_t>(q) & 15) == 0) {
+            vec8(q, v);
+            return;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = load(r, c + j);
+    }
+    __device__ static __forceinline__ void vec8(const __nv_bfloat16 *q, float (&v)[8]) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(q));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[2 * k] = __uint_as_float(ws[k] << 16);
+            v[2 * k + 1] = __uint_as_float(ws[k] & 0xFFFF0000u);
+        }
+    }
+    __device__ static __forceinline__ void vec8(const float *q, float (&v)[8]) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(q)), b = __ldg(reinterpret_cast<const float4 *>(q) + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
 };
 
 // NVFP4 tensor [rows, cols] read back as its fp32 dequantization (G * s_i) * s_o.
@@ -46,6 +71,28 @@ struct SrcNv {
         const float v = __fmul_rn(__fmul_rn(gv, e4m3_to_float(sb)), outer[(c >> 7) * rows_p + r]);
         return (code & 8u) ? -v : v;
     }
+    // elem(r, c .. c+7), c a multiple of 8, inside the padded tensor (whose padding holds
+    // zero codes and scales): one 4-byte code load, one scale byte, one outer scale.
+    // Two codes' magnitudes at a time are looked up as 2G in {0,1,2,3,4,6,8,12} with a
+    // byte permute, turned into fp32 exactly, and scaled as (G * s_i) * s_o.
+    __device__ __forceinline__ void load8(int64_t r, int64_t c, float (&v)[8]) const {
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(codes + r * (cols_p / 2) + (c >> 1));
+        const int64_t g = c >> 4;
+        const uint32_t sb = sf[sf_word_offset(r, g >> 2, cols_p / 64) + (g & 3)];
+        const float half_si = __fmul_rn(e4m3_to_float(sb), 0.5f);        // exact
+        const float so = outer[(c >> 7) * rows_p + r];
+        const uint32_t mag = w & 0x77777777u;
+        const uint32_t two_g[2] = {__byte_perm(0x03020100u, 0x0C080604u, mag & 0xFFFFu),
+                                   __byte_perm(0x03020100u, 0x0C080604u, mag >> 16)};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            // 0x4B0000nn = 2^23 + nn as fp32; subtracting 2^23 leaves nn = 2G exactly
+            const float gg = __fsub_rn(__uint_as_float(__byte_perm(two_g[k >> 2], 0x4B000000u, (k & 3) | 0x7440)),
+                                       8388608.0f);
+            const float a = __fmul_rn(__fmul_rn(gg, half_si), so);
+            v[k] = __uint_as_float(__float_as_uint(a) ^ ((w << (28 - 4 * k)) & 0x80000000u));
+        }
+    }
 };
 
 // MXFP8 slice [rows, cols] read back as fp32 (E4M3 value times 2^(byte-127)).
@@ -59,6 +106,15 @@ struct SrcMx {
         const int e = (int)sf[sf_word_offset(r, g >> 2, cols_p / 128) + (g & 3)] - 127;
         const float s = e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x400000u);
         return __fmul_rn(v, s);
+    }
+    // elem(r, c .. c+7), c a multiple of 8, inside the padded tensor: one 8-byte load
+    __device__ __forceinline__ void load8(int64_t r, int64_t c, float (&v)[8]) const {
+        const uint2 w = *reinterpret_cast<const uint2 *>(codes + r * cols_p + c);
+        const int64_t g = c >> 5;
+        const int e = (int)sf[sf_word_offset(r, g >> 2, cols_p / 128) + (g & 3)] - 127;
+        const float s = e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x400000u);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = __fmul_rn(e4m3_to_float(((k < 4 ? w.x : w.y) >> (8 * (k & 3))) & 0xFFu), s);
     }
 };
 
@@ -147,19 +203,22 @@ __global__ void __launch_bounds__(256) k_quant_rows(Src src, OutNv onv, OutMx om
 template <typename Src, int FMT, bool SR, bool RHT>
 __global__ void __launch_bounds__(256) k_quant_cols(Src src, OutNv onv, OutMx omx, uint64_t seed, uint32_t tag,
                                                     uint32_t rht_tag) {
-    __shared__ float tile[128 * 64];
+    __shared__ __align__(16) float tile[128 * 64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t c0 = (int64_t)blockIdx.x * 64;      // first output row of the tile
     const int64_t kb = blockIdx.y;                    // 128-block along the input rows
     const int64_t r0 = kb * 128;
-    // fill: warp w loads rows w, w+8, ...; lane l loads columns l and l+32
-    for (int rr = warp; rr < 128; rr += 8) {
-        const int sw = ((rr >> 5) & 3) << 3;
+    // fill: 128 rows x 8 column octets, one octet (8 consecutive columns of a row) per
+    // thread and pass, stored as two 16-byte words (the swizzle keeps an octet contiguous)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int cc = lane + 32 * h;
-            tile[rr * 64 + (cc ^ sw)] = src.load(r0 + rr, c0 + cc);
-        }
+    for (int i = 0; i < 4; ++i) {
+        const int idx = i * 256 + (int)threadIdx.x;
+        const int rr = idx >> 3, o = idx & 7;
+        float v[8];
+        src.load8(r0 + rr, c0 + 8 * o, v);
+        float4 *dst = reinterpret_cast<float4 *>(&tile[rr * 64 + ((8 * o) ^ (((rr >> 5) & 3) << 3))]);
+        dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+        dst[1] = make_float4(v[4], v[5], v[6], v[7]);
     }
     __syncthreads();
     const int t = lane & 3;
