@@ -142,9 +142,9 @@ class Timeline:
 
 # kernel behind each step call (for per-kernel aggregation of the live event times)
 CALL_KERNEL = {
-    "quant_x": "k_quant_rows (NVFP4)", "quant_dy_row": "k_quant_rows (NVFP4)",
-    "quant_x8": "k_quant_rows (MXFP8)", "quant_dy_row8": "k_quant_rows (MXFP8)",
-    "quant_dy_col": "k_quant_cols (NVFP4)", "quant_dy_col8": "k_quant_cols (MXFP8)",
+    "quant_x": "k_quant_rows (NVFP4)", "quant_dy_row": "k_quant_rows (NVFP4 + MXFP8 of dY)",
+    "quant_x8": "k_quant_rows (MXFP8)",
+    "quant_dy_col": "k_quant_cols (NVFP4 + MXFP8 of dY)",
     "requant_w": "k_quant_cols<SrcNv> (re-align)", "requant_x": "k_quant_cols<SrcNv> (re-align)",
     "requant_w8": "k_quant_cols<SrcMx> (re-align)", "requant_x8": "k_quant_cols<SrcMx> (re-align)",
     "gemm_fwd": "k_gemm_nvfp4", "gemm_dx": "k_gemm_nvfp4", "gemm_dw": "k_gemm_nvfp4",
@@ -191,8 +191,8 @@ class Linear:
         self.work = {
             "gemm_fwd": (f4(M, N, kn), f4(M, N, k)), "gemm_dx": (f4(M, kn, N), 0.0), "gemm_dx8": (0.0, f4(M, k, N)),
             "gemm_dw": (f4(N, kn, M), 0.0), "gemm_dw8": (0.0, f4(N, k, M)),
-            "quant_x": M * kn * (2 + NV_B), "quant_x8": M * k * (2 + MX_B), "quant_dy_row": M * N * (2 + NV_B),
-            "quant_dy_row8": M * N * (2 + MX_B), "quant_dy_col": M * N * (2 + NV_B), "quant_dy_col8": M * N * (2 + MX_B),
+            "quant_x": M * kn * (2 + NV_B), "quant_x8": M * k * (2 + MX_B),
+            "quant_dy_row": M * N * (2 + NV_B + MX_B), "quant_dy_col": M * N * (2 + NV_B + MX_B),
             "requant_w": 2 * kn * N * NV_B, "requant_w8": 2 * k * N * MX_B, "requant_x": 2 * kn * M * NV_B,
             "requant_x8": 2 * k * M * MX_B,
         }
@@ -206,23 +206,24 @@ class Linear:
         T("quant_x8", lambda: tj.quantize_mxfp8(self.X, sel=self.oi, out=self.x8, stream=s))
         T("gemm_fwd", lambda: tj.gemm_nvfp4(self.xq, self.wq, self.x8, self.w8, out=self.Y, stream=s))
         # input gradient (tj_linear_bwd_dx)
-        T("quant_dy_row", lambda: tj.quantize_nvfp4(self.dY, mode=SR, rht=True, seed=seed, tag=tj.TAG_DY_ROW,
-                                                    rht_tag=tj.TAG_RHT_DX, out=self.s_dy, stream=s))
+        # dY rows: the SR + RHT operand of dX and the MXFP8 rows of dY from one read
+        T("quant_dy_row", lambda: tj.quantize_nvfp4_mxfp8(self.dY, mode=SR, rht=True, seed=seed, tag=tj.TAG_DY_ROW,
+                                                          rht_tag=tj.TAG_RHT_DX, out=self.s_dy, out8=self.q8_dy,
+                                                          stream=s))
         T("requant_w", lambda: tj.requantize_nvfp4(self.wq, SR, True, seed, tj.TAG_WT, tj.TAG_RHT_DX, out=self.s_w,
                                                    stream=s))
         T("gemm_dx", lambda: tj.gemm_nvfp4(self.s_dy, self.s_w, alpha=2.0 ** -7, out=self.dX, col_map=self.ni,
                                            stream=s))
-        T("quant_dy_row8", lambda: tj.quantize_mxfp8(self.dY, out=self.q8_dy, stream=s))
         T("requant_w8", lambda: tj.requantize_mxfp8(self.w8, out=self.q8_w, stream=s))
         T("gemm_dx8", lambda: tj.gemm_mxfp8(self.q8_dy, self.q8_w, out=self.dX, col_map=self.oi, stream=s))
         # weight gradient (tj_linear_bwd_dw)
-        T("quant_dy_col", lambda: tj.quantize_nvfp4(self.dY, along_cols=True, mode=SR, rht=True, seed=seed,
-                                                    tag=tj.TAG_DY_COL, rht_tag=tj.TAG_RHT_DW, out=self.s_dyt, stream=s))
+        T("quant_dy_col", lambda: tj.quantize_nvfp4_mxfp8(self.dY, along_cols=True, mode=SR, rht=True, seed=seed,
+                                                          tag=tj.TAG_DY_COL, rht_tag=tj.TAG_RHT_DW, out=self.s_dyt,
+                                                          out8=self.q8_dyt, stream=s))
         T("requant_x", lambda: tj.requantize_nvfp4(self.xq, SR, True, seed, tj.TAG_XT, tj.TAG_RHT_DW, out=self.s_x,
                                                    stream=s))
         T("gemm_dw", lambda: tj.gemm_nvfp4(self.s_dyt, self.s_x, alpha=2.0 ** -7, out=self.dW, col_map=self.ni,
                                            stream=s))
-        T("quant_dy_col8", lambda: tj.quantize_mxfp8(self.dY, along_cols=True, out=self.q8_dyt, stream=s))
         T("requant_x8", lambda: tj.requantize_mxfp8(self.x8, out=self.q8_x, stream=s))
         T("gemm_dw8", lambda: tj.gemm_mxfp8(self.q8_dyt, self.q8_x, out=self.dW, col_map=self.oi, stream=s))
 

@@ -132,6 +132,18 @@ tj_status tj_quantize_mxfp8(const void *x, int dtype, int64_t rows_x, int64_t co
                             int along_cols, const int32_t *sel, int64_t n_sel,
                             tj_mxfp8 *out, void *stream);
 
+/* tj_quantize_nvfp4_mxfp8 - tj_quantize_nvfp4 and tj_quantize_mxfp8 of the same input
+ * from one read: `out` gets the NVFP4 quantization (mode / rht / seed / tags as in
+ * tj_quantize_nvfp4) and `out8` the MXFP8 quantization of the same (selected) elements
+ * without the transform, both in the same orientation and shape.  The results equal the
+ * two separate calls byte for byte.  The backward of a linear layer with outlier channels
+ * needs both of dY (§2.A SR operand, §2.C FP8 slice); this halves the reads of dY.
+ * Errors as tj_quantize_nvfp4, also when out8's shape differs. */
+tj_status tj_quantize_nvfp4_mxfp8(const void *x, int dtype, int64_t rows_x, int64_t cols_x, int64_t ld,
+                                  int along_cols, const int32_t *sel, int64_t n_sel, int mode,
+                                  int rht, uint64_t seed, uint32_t tag, uint32_t rht_tag,
+                                  tj_nvfp4 *out, tj_mxfp8 *out8, void *stream);
+
 /* tj_requantize_nvfp4 - transposed re-alignment of a forward NVFP4 operand for the
  * backward (§2.A: the backward estimates with X-hat, the dequantized forward operand, and
  * the 1x16 groups of the transposed weight are re-formed along the new contraction axis):

@@ -132,6 +132,24 @@ tj_status tj_quantize_mxfp8(const void *x, int dtype, int64_t rows_x, int64_t co
                                              static_cast<cudaStream_t>(stream)));
 }
 
+tj_status tj_quantize_nvfp4_mxfp8(const void *x, int dtype, int64_t rows_x, int64_t cols_x, int64_t ld,
+                                  int along_cols, const int32_t *sel, int64_t n_sel, int mode, int rht,
+                                  uint64_t seed, uint32_t tag, uint32_t rht_tag, tj_nvfp4 *out, tj_mxfp8 *out8,
+                                  void *stream) {
+    if (rows_x < 0 || cols_x < 0 || (mode != TJ_RTN && mode != TJ_SR) || out == nullptr || out8 == nullptr)
+        return TJ_ERR_INVALID_ARG;
+    if (!dense_ok(x, dtype, ld, cols_x)) return TJ_ERR_INVALID_ARG;
+    if (!al_elem(x, dtype)) return TJ_ERR_ALIGN;
+    const int64_t ncols = sel ? n_sel : cols_x;
+    if (sel && (n_sel < 0 || n_sel > cols_x)) return TJ_ERR_SHAPE;
+    const int64_t orows = along_cols ? ncols : rows_x, ocols = along_cols ? rows_x : ncols;
+    tj_status st = check_nv(out, orows, ocols);
+    if (st == TJ_OK) st = check_mx(out8, orows, ocols);
+    if (st != TJ_OK) return st;
+    return cuda_status(launch_quant_dual_dense(x, dtype, rows_x, ncols, ld, along_cols, sel, mode, rht, seed, tag,
+                                               rht_tag, *out, *out8, static_cast<cudaStream_t>(stream)));
+}
+
 tj_status tj_requantize_nvfp4(const tj_nvfp4 *in, int mode, int rht, uint64_t seed, uint32_t tag, uint32_t rht_tag,
                               tj_nvfp4 *out, void *stream) {
     if (in == nullptr || out == nullptr || (mode != TJ_RTN && mode != TJ_SR)) return TJ_ERR_INVALID_ARG;
@@ -253,16 +271,23 @@ tj_status tj_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, c
     uint8_t *cur = static_cast<uint8_t *>(workspace);
     tj_nvfp4 s_dy = carve_nv(cur, M, N);
     tj_nvfp4 s_w = carve_nv(cur, kn, N);
-    // dY rows: RHT along N + SR (the dX operand); W-hat^T re-aligned with the same signs
-    TJ_TRY(launch_quant_nv_dense(dy, TJ_BF16, M, N, lddy, 0, nullptr, TJ_SR, 1, seed, TJ_TAG_DY_ROW, TJ_TAG_RHT_DX,
-                                 s_dy, s));
+    tj_mxfp8 q8_dy{}, q8_w{};
+    if (k > 0) {
+        q8_dy = carve_mx(cur, M, N);
+        q8_w = carve_mx(cur, k, N);
+    }
+    // dY rows: RHT along N + SR (the dX operand), and with an outlier slice also the
+    // MXFP8 rows of dY, from one read; W-hat^T re-aligned with the same signs
+    if (k > 0)
+        TJ_TRY(launch_quant_dual_dense(dy, TJ_BF16, M, N, lddy, 0, nullptr, TJ_SR, 1, seed, TJ_TAG_DY_ROW,
+                                       TJ_TAG_RHT_DX, s_dy, q8_dy, s));
+    else
+        TJ_TRY(launch_quant_nv_dense(dy, TJ_BF16, M, N, lddy, 0, nullptr, TJ_SR, 1, seed, TJ_TAG_DY_ROW,
+                                     TJ_TAG_RHT_DX, s_dy, s));
     TJ_TRY(launch_realign_nv(*wq, s_w, TJ_SR, 1, seed, TJ_TAG_WT, TJ_TAG_RHT_DX, s));
     TJ_TRY(launch_gemm(&s_dy, &s_w, nullptr, nullptr, 0.0078125f, dx, out_dtype, lddx, M, kn,
                        k > 0 ? normal_idx : nullptr, s));
     if (k > 0) {
-        tj_mxfp8 q8_dy = carve_mx(cur, M, N);
-        tj_mxfp8 q8_w = carve_mx(cur, k, N);
-        TJ_TRY(launch_quant_mx_dense(dy, TJ_BF16, M, N, lddy, 0, nullptr, q8_dy, s));
         TJ_TRY(launch_realign_mx(*w8, q8_w, s));
         TJ_TRY(launch_gemm(nullptr, nullptr, &q8_dy, &q8_w, 1.0f, dx, out_dtype, lddx, M, k, outlier_idx, s));
     }
@@ -287,16 +312,23 @@ tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, c
     uint8_t *cur = static_cast<uint8_t *>(workspace);
     tj_nvfp4 s_dy = carve_nv(cur, N, M);
     tj_nvfp4 s_x = carve_nv(cur, kn, M);
-    // dY^T rows (RHT along M + SR) and X-hat^T re-aligned with the same signs
-    TJ_TRY(launch_quant_nv_dense(dy, TJ_BF16, M, N, lddy, 1, nullptr, TJ_SR, 1, seed, TJ_TAG_DY_COL, TJ_TAG_RHT_DW,
-                                 s_dy, s));
+    tj_mxfp8 q8_dy{}, q8_x{};
+    if (k > 0) {
+        q8_dy = carve_mx(cur, N, M);
+        q8_x = carve_mx(cur, k, M);
+    }
+    // dY^T rows (RHT along M + SR), and with an outlier slice also the MXFP8 rows of
+    // dY^T, from one read; X-hat^T re-aligned with the same signs
+    if (k > 0)
+        TJ_TRY(launch_quant_dual_dense(dy, TJ_BF16, M, N, lddy, 1, nullptr, TJ_SR, 1, seed, TJ_TAG_DY_COL,
+                                       TJ_TAG_RHT_DW, s_dy, q8_dy, s));
+    else
+        TJ_TRY(launch_quant_nv_dense(dy, TJ_BF16, M, N, lddy, 1, nullptr, TJ_SR, 1, seed, TJ_TAG_DY_COL,
+                                     TJ_TAG_RHT_DW, s_dy, s));
     TJ_TRY(launch_realign_nv(*xq, s_x, TJ_SR, 1, seed, TJ_TAG_XT, TJ_TAG_RHT_DW, s));
     TJ_TRY(launch_gemm(&s_dy, &s_x, nullptr, nullptr, 0.0078125f, dw, TJ_FP32, lddw, N, kn,
                        k > 0 ? normal_idx : nullptr, s));
     if (k > 0) {
-        tj_mxfp8 q8_dy = carve_mx(cur, N, M);
-        tj_mxfp8 q8_x = carve_mx(cur, k, M);
-        TJ_TRY(launch_quant_mx_dense(dy, TJ_BF16, M, N, lddy, 1, nullptr, q8_dy, s));
         TJ_TRY(launch_realign_mx(*x8, q8_x, s));
         TJ_TRY(launch_gemm(nullptr, nullptr, &q8_dy, &q8_x, 1.0f, dw, TJ_FP32, lddw, N, k, outlier_idx, s));
     }

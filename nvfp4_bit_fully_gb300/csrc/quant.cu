@@ -153,21 +153,22 @@ __device__ __forceinline__ void load_row32(const SrcDense<__nv_bfloat16> &src, i
 // ---------------------------------------------------------------------------
 // Row-wise kernel: output row r = input row r, quantized along the columns.
 // One quad per (row, 128-block); a warp covers 8 consecutive segments.
-// FMT 0 = NVFP4, 1 = MXFP8.
+// FMT 0 = NVFP4, 1 = MXFP8, 2 = both from one read (MXFP8 of the input, NVFP4 of
+// its optional RHT), into outputs of the same shape.
 // ---------------------------------------------------------------------------
 template <typename Src, int FMT, bool SR, bool RHT>
-__global__ void __launch_bounds__(256) k_quant_rows(Src src, OutNv onv, OutMx omx, int64_t nseg, uint64_t seed,
+__global__ void __launch_bounds__(256) k_quant_rows(Src src, OutNv onv, OutMx omx, int64_t nseg, const PhiloxKeys pk,
                                                     uint32_t tag, uint32_t rht_tag) {
     const int lane = threadIdx.x & 31;
     const int t = lane & 3;
-    const int64_t rows_p = FMT == 0 ? onv.rows_p : omx.rows_p;
-    const int64_t cols_p = FMT == 0 ? onv.cols_p : omx.cols_p;
+    const int64_t rows_p = FMT != 1 ? onv.rows_p : omx.rows_p;
+    const int64_t cols_p = FMT != 1 ? onv.cols_p : omx.cols_p;
     const int64_t total = rows_p * nseg;
     const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     uint32_t sign_word = 0u;
     if (RHT) {
-        const uint4 sb = rht_sign_bits(seed, rht_tag);
+        const uint4 sb = rht_sign_bits(pk, rht_tag);
         sign_word = t == 0 ? sb.x : (t == 1 ? sb.y : (t == 2 ? sb.z : sb.w));
     }
     for (int64_t base = warp0 * 8; base < total; base += nwarps * 8) {   // warp-uniform loop
@@ -181,9 +182,13 @@ __global__ void __launch_bounds__(256) k_quant_rows(Src src, OutNv onv, OutMx om
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[j] = 0.0f;
         }
-        if (FMT == 0) {
+        if (FMT != 1) {
+            if (FMT == 2) {
+                const MxSeg m = quant_mxfp8_group(x);
+                store_mx_seg(omx, row, kb, t, m, valid);
+            }
             if (RHT) rht128_quad(x, sign_word, t);
-            const NvSeg s = quant_nvfp4_seg<SR>(x, (uint64_t)(row * cols_p + kb * 128 + 32 * t), seed, tag);
+            const NvSeg s = quant_nvfp4_seg<SR>(x, (uint64_t)(row * cols_p + kb * 128 + 32 * t), pk, tag);
             store_nv_seg(onv, row, kb, t, s, valid);
         } else {
             const MxSeg s = quant_mxfp8_group(x);
@@ -201,7 +206,7 @@ __global__ void __launch_bounds__(256) k_quant_rows(Src src, OutNv onv, OutMx om
 // element (r, c) sits at r*64 + (c ^ (((r >> 5) & 3) << 3)).
 // ---------------------------------------------------------------------------
 template <typename Src, int FMT, bool SR, bool RHT>
-__global__ void __launch_bounds__(256) k_quant_cols(Src src, OutNv onv, OutMx omx, uint64_t seed, uint32_t tag,
+__global__ void __launch_bounds__(256) k_quant_cols(Src src, OutNv onv, OutMx omx, const PhiloxKeys pk, uint32_t tag,
                                                     uint32_t rht_tag) {
     __shared__ __align__(16) float tile[128 * 64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -227,15 +232,19 @@ __global__ void __launch_bounds__(256) k_quant_cols(Src src, OutNv onv, OutMx om
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = tile[(32 * t + j) * 64 + (cl ^ (t << 3))];
     const int64_t row = c0 + cl;
-    const int64_t rows_p = FMT == 0 ? onv.rows_p : omx.rows_p;
-    const int64_t cols_p = FMT == 0 ? onv.cols_p : omx.cols_p;
+    const int64_t rows_p = FMT != 1 ? onv.rows_p : omx.rows_p;
+    const int64_t cols_p = FMT != 1 ? onv.cols_p : omx.cols_p;
     const bool valid = row < rows_p;
-    if (FMT == 0) {
+    if (FMT != 1) {
+        if (FMT == 2) {
+            const MxSeg m = quant_mxfp8_group(x);
+            store_mx_seg(omx, row, kb, t, m, valid);
+        }
         if (RHT) {
-            const uint4 sb = rht_sign_bits(seed, rht_tag);
+            const uint4 sb = rht_sign_bits(pk, rht_tag);
             rht128_quad(x, t == 0 ? sb.x : (t == 1 ? sb.y : (t == 2 ? sb.z : sb.w)), t);
         }
-        const NvSeg s = quant_nvfp4_seg<SR>(x, (uint64_t)(row * cols_p + r0 + 32 * t), seed, tag);
+        const NvSeg s = quant_nvfp4_seg<SR>(x, (uint64_t)(row * cols_p + r0 + 32 * t), pk, tag);
         store_nv_seg(onv, row, kb, t, s, valid);
     } else {
         const MxSeg s = quant_mxfp8_group(x);
@@ -247,13 +256,13 @@ __global__ void __launch_bounds__(256) k_quant_cols(Src src, OutNv onv, OutMx om
 // Standalone RHT (fp32 -> fp32), one quad per 128-block, same butterfly as the
 // fused quantizers.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t seed,
+__global__ void __launch_bounds__(256) k_rht(const float *x, float *y, int64_t rows, int64_t cols, const PhiloxKeys pk,
                                              uint32_t tag) {
     const int lane = threadIdx.x & 31, t = lane & 3;
     const int64_t nseg = cols / 128, total = rows * nseg;
     const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const uint4 sb = rht_sign_bits(seed, tag);
+    const uint4 sb = rht_sign_bits(pk, tag);
     const uint32_t sign_word = t == 0 ? sb.x : (t == 1 ? sb.y : (t == 2 ? sb.z : sb.w));
     for (int64_t base = warp0 * 8; base < total; base += nwarps * 8) {
         const int64_t seg = base + (lane >> 2);
@@ -298,41 +307,41 @@ OutNv out_nv(const tj_nvfp4 &q) {
 }
 OutMx out_mx(const tj_mxfp8 &q) { return OutMx{q.codes, q.sf, round_up(q.rows, 128), round_up(q.cols, 128)}; }
 
-template <typename Src>
+template <typename Src, int FMT = 0>
 cudaError_t rows_nv(const Src &src, const OutNv &o, int mode, int rht, uint64_t seed, uint32_t tag,
-                    uint32_t rht_tag, cudaStream_t s) {
+                    uint32_t rht_tag, cudaStream_t s, const OutMx none = OutMx{}) {
     const int64_t nseg = o.cols_p / 128, grid = row_grid(o.rows_p * nseg);
-    const OutMx none{};
-    if (mode == TJ_SR && rht)  k_quant_rows<Src, 0, true, true><<<grid, kThreads, 0, s>>>(src, o, none, nseg, seed, tag, rht_tag);
-    else if (mode == TJ_SR)    k_quant_rows<Src, 0, true, false><<<grid, kThreads, 0, s>>>(src, o, none, nseg, seed, tag, rht_tag);
-    else if (rht)              k_quant_rows<Src, 0, false, true><<<grid, kThreads, 0, s>>>(src, o, none, nseg, seed, tag, rht_tag);
-    else                       k_quant_rows<Src, 0, false, false><<<grid, kThreads, 0, s>>>(src, o, none, nseg, seed, tag, rht_tag);
+    const PhiloxKeys pk = philox_keys(seed);
+    if (mode == TJ_SR && rht)  k_quant_rows<Src, FMT, true, true><<<grid, kThreads, 0, s>>>(src, o, none, nseg, pk, tag, rht_tag);
+    else if (mode == TJ_SR)    k_quant_rows<Src, FMT, true, false><<<grid, kThreads, 0, s>>>(src, o, none, nseg, pk, tag, rht_tag);
+    else if (rht)              k_quant_rows<Src, FMT, false, true><<<grid, kThreads, 0, s>>>(src, o, none, nseg, pk, tag, rht_tag);
+    else                       k_quant_rows<Src, FMT, false, false><<<grid, kThreads, 0, s>>>(src, o, none, nseg, pk, tag, rht_tag);
     return cudaGetLastError();
 }
 
-template <typename Src>
+template <typename Src, int FMT = 0>
 cudaError_t cols_nv(const Src &src, const OutNv &o, int mode, int rht, uint64_t seed, uint32_t tag,
-                    uint32_t rht_tag, cudaStream_t s) {
+                    uint32_t rht_tag, cudaStream_t s, const OutMx none = OutMx{}) {
     const dim3 grid((unsigned)(o.rows_p / 64), (unsigned)(o.cols_p / 128));
-    const OutMx none{};
-    if (mode == TJ_SR && rht)  k_quant_cols<Src, 0, true, true><<<grid, kThreads, 0, s>>>(src, o, none, seed, tag, rht_tag);
-    else if (mode == TJ_SR)    k_quant_cols<Src, 0, true, false><<<grid, kThreads, 0, s>>>(src, o, none, seed, tag, rht_tag);
-    else if (rht)              k_quant_cols<Src, 0, false, true><<<grid, kThreads, 0, s>>>(src, o, none, seed, tag, rht_tag);
-    else                       k_quant_cols<Src, 0, false, false><<<grid, kThreads, 0, s>>>(src, o, none, seed, tag, rht_tag);
+    const PhiloxKeys pk = philox_keys(seed);
+    if (mode == TJ_SR && rht)  k_quant_cols<Src, FMT, true, true><<<grid, kThreads, 0, s>>>(src, o, none, pk, tag, rht_tag);
+    else if (mode == TJ_SR)    k_quant_cols<Src, FMT, true, false><<<grid, kThreads, 0, s>>>(src, o, none, pk, tag, rht_tag);
+    else if (rht)              k_quant_cols<Src, FMT, false, true><<<grid, kThreads, 0, s>>>(src, o, none, pk, tag, rht_tag);
+    else                       k_quant_cols<Src, FMT, false, false><<<grid, kThreads, 0, s>>>(src, o, none, pk, tag, rht_tag);
     return cudaGetLastError();
 }
 
 template <typename Src>
 cudaError_t rows_mx(const Src &src, const OutMx &o, cudaStream_t s) {
     const int64_t nseg = o.cols_p / 128, grid = row_grid(o.rows_p * nseg);
-    k_quant_rows<Src, 1, false, false><<<grid, kThreads, 0, s>>>(src, OutNv{}, o, nseg, 0, 0, 0);
+    k_quant_rows<Src, 1, false, false><<<grid, kThreads, 0, s>>>(src, OutNv{}, o, nseg, PhiloxKeys{}, 0, 0);
     return cudaGetLastError();
 }
 
 template <typename Src>
 cudaError_t cols_mx(const Src &src, const OutMx &o, cudaStream_t s) {
     const dim3 grid((unsigned)(o.rows_p / 64), (unsigned)(o.cols_p / 128));
-    k_quant_cols<Src, 1, false, false><<<grid, kThreads, 0, s>>>(src, OutNv{}, o, 0, 0, 0);
+    k_quant_cols<Src, 1, false, false><<<grid, kThreads, 0, s>>>(src, OutNv{}, o, PhiloxKeys{}, 0, 0);
     return cudaGetLastError();
 }
 }  // namespace
@@ -358,6 +367,23 @@ cudaError_t launch_quant_nv_dense(const void *x, int dtype, int64_t rows_x, int6
     const SrcDense<float> src{static_cast<const float *>(x), ld, rows_x, n_cols_sel, sel};
     return along_cols ? cols_nv(src, o, mode, rht, seed, tag, rht_tag, s)
                       : rows_nv(src, o, mode, rht, seed, tag, rht_tag, s);
+}
+
+// Dense input -> NVFP4 (mode / rht) and MXFP8 of the same elements, one read.
+cudaError_t launch_quant_dual_dense(const void *x, int dtype, int64_t rows_x, int64_t n_cols_sel, int64_t ld,
+                                    int along_cols, const int32_t *sel, int mode, int rht, uint64_t seed,
+                                    uint32_t tag, uint32_t rht_tag, const tj_nvfp4 &out, const tj_mxfp8 &out8,
+                                    cudaStream_t s) {
+    const OutNv o = out_nv(out);
+    const OutMx m = out_mx(out8);
+    if (dtype == TJ_BF16) {
+        const SrcDense<__nv_bfloat16> src{static_cast<const __nv_bfloat16 *>(x), ld, rows_x, n_cols_sel, sel};
+        return along_cols ? cols_nv<decltype(src), 2>(src, o, mode, rht, seed, tag, rht_tag, s, m)
+                          : rows_nv<decltype(src), 2>(src, o, mode, rht, seed, tag, rht_tag, s, m);
+    }
+    const SrcDense<float> src{static_cast<const float *>(x), ld, rows_x, n_cols_sel, sel};
+    return along_cols ? cols_nv<decltype(src), 2>(src, o, mode, rht, seed, tag, rht_tag, s, m)
+                      : rows_nv<decltype(src), 2>(src, o, mode, rht, seed, tag, rht_tag, s, m);
 }
 
 cudaError_t launch_quant_mx_dense(const void *x, int dtype, int64_t rows_x, int64_t n_cols_sel, int64_t ld,
@@ -387,7 +413,7 @@ cudaError_t launch_realign_mx(const tj_mxfp8 &in, const tj_mxfp8 &out, cudaStrea
 cudaError_t launch_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,
                        cudaStream_t s) {
     const int64_t grid = row_grid(rows * (cols / 128));
-    k_rht<<<grid, kThreads, 0, s>>>(x, y, rows, cols, seed, tag);
+    k_rht<<<grid, kThreads, 0, s>>>(x, y, rows, cols, philox_keys(seed), tag);
     return cudaGetLastError();
 }
 

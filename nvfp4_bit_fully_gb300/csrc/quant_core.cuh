@@ -58,7 +58,7 @@ struct NvSeg {
 // or any element of a group whose scale is zero, gets code 0.  elem0 = index of
 // x[0] in the operand's quantized layout (row * cols_p + col), a multiple of 8.
 template <bool SR>
-__device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t elem0, uint64_t seed,
+__device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t elem0, const PhiloxKeys &pk,
                                                  uint32_t tag) {
     float a_i[2];
 #pragma unroll
@@ -80,11 +80,6 @@ __device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t 
     out.s_o = s_o;
     out.sf2 = 0u;
     uint32_t words[4] = {0u, 0u, 0u, 0u};
-    uint4 rnd[4];
-    if (SR) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) rnd[q] = sr_bits8((elem0 >> 3) + (uint64_t)q, seed, tag);
-    }
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
         uint32_t sb = 0u;
@@ -94,12 +89,13 @@ __device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t 
         const float r = s > 0.0f ? __fdiv_rn(1.0f, s) : 0.0f;
         if (!(s > 0.0f)) continue;                         // zero group: codes stay 0
         if (SR) {
+            uint4 w4;                                      // drawn just in time, 8 elements per call
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int e = 16 * g + j;
+                if ((e & 7) == 0) w4 = sr_bits8((elem0 >> 3) + (uint64_t)(e >> 3), pk, tag);
                 const float xv = x[e];
                 const float a = fminf(fabsf(__fmul_rn(xv, r)), 6.0f);
-                const uint4 w4 = rnd[e >> 3];
                 const int wi = (e & 7) >> 1;
                 const uint32_t w = wi == 0 ? w4.x : (wi == 1 ? w4.y : (wi == 2 ? w4.z : w4.w));
                 uint32_t code = e2m1_sr(a, (w >> (16 * (e & 1))) & 0xFFFFu) | (xv < 0.0f ? 8u : 0u);

@@ -29,14 +29,31 @@ __host__ __device__ inline int64_t round_up(int64_t v, int64_t m) { return (v + 
 // xored with the other counter words and the round key, the key advanced by the
 // Weyl increments 0x9E3779B9 / 0xBB67AE85 after every round.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// The ten round keys of Philox4x32-10 for one 64-bit seed (key = (lo, hi), each
+// round adds the Weyl constants 0x9E3779B9 / 0xBB67AE85).  They are the same for
+// every call of a launch, so the host computes them once and the kernels read them
+// as launch parameters instead of re-deriving them in every call.
+struct PhiloxKeys {
+    uint32_t k[20];     // k[2r], k[2r+1]: the key words of round r
+};
+inline PhiloxKeys philox_keys(uint64_t seed) {
+    PhiloxKeys pk;
+    uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        pk.k[2 * r] = k0;
+        pk.k[2 * r + 1] = k1;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return pk;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys &pk) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
         const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
         const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
+        c = make_uint4(hi1 ^ c.y ^ pk.k[2 * r], lo1, hi0 ^ c.w ^ pk.k[2 * r + 1], lo0);
     }
     return c;
 }
@@ -44,15 +61,14 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 // Random bits for stochastic rounding: element e (row * cols_p + col of the
 // quantized operand) takes 16 bits of Philox(counter = (e>>3, tag, 0), key = seed);
 // elements 8g .. 8g+7 share call g: word (e&7)>>1, low half for even e.
-__device__ __forceinline__ uint4 sr_bits8(uint64_t g, uint64_t seed, uint32_t tag) {
-    return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), tag, 0u), (uint32_t)seed,
-                         (uint32_t)(seed >> 32));
+__device__ __forceinline__ uint4 sr_bits8(uint64_t g, const PhiloxKeys &pk, uint32_t tag) {
+    return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), tag, 0u), pk);
 }
 
 // The +-1 diagonal of the RHT as 128 sign bits (bit i set -> d[i] = -1):
 // one Philox call with counter (0, 0, tag, 0) and key = seed.
-__device__ __forceinline__ uint4 rht_sign_bits(uint64_t seed, uint32_t tag) {
-    return philox4x32_10(make_uint4(0u, 0u, tag, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
+__device__ __forceinline__ uint4 rht_sign_bits(const PhiloxKeys &pk, uint32_t tag) {
+    return philox4x32_10(make_uint4(0u, 0u, tag, 0u), pk);
 }
 
 // ---------------------------------------------------------------------------

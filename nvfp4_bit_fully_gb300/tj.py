@@ -49,6 +49,8 @@ _F = ctypes.c_float
 _SIGS = {
     "tj_quantize_nvfp4": [_P, _I, _I64, _I64, _I64, _I, _P, _I64, _I, _I, _U64, _U32, _U32, ctypes.POINTER(CNvfp4), _P],
     "tj_quantize_mxfp8": [_P, _I, _I64, _I64, _I64, _I, _P, _I64, ctypes.POINTER(CMxfp8), _P],
+    "tj_quantize_nvfp4_mxfp8": [_P, _I, _I64, _I64, _I64, _I, _P, _I64, _I, _I, _U64, _U32, _U32,
+                                ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P],
     "tj_requantize_nvfp4": [ctypes.POINTER(CNvfp4), _I, _I, _U64, _U32, _U32, ctypes.POINTER(CNvfp4), _P],
     "tj_requantize_mxfp8": [ctypes.POINTER(CMxfp8), ctypes.POINTER(CMxfp8), _P],
     "tj_rht": [_P, _P, _I64, _I64, _U64, _U32, _P],
@@ -178,6 +180,21 @@ def quantize_mxfp8(x, along_cols=False, sel=None, out=None, stream=None):
     _call("tj_quantize_mxfp8", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols), _ptr(sel),
           0 if sel is None else sel.numel(), ctypes.byref(c), _stream(stream))
     return out
+
+
+def quantize_nvfp4_mxfp8(x, along_cols=False, sel=None, mode=TJ_RTN, rht=False, seed=0, tag=0, rht_tag=0,
+                         out=None, out8=None, stream=None):
+    """NVFP4 and MXFP8 of the same input from one read (tj_quantize_nvfp4_mxfp8)."""
+    rows_x, cols_x = x.shape
+    ncols = cols_x if sel is None else sel.numel()
+    orows, ocols = (ncols, rows_x) if along_cols else (rows_x, ncols)
+    out = out if out is not None else NVFP4.empty(orows, ocols, x.device)
+    out8 = out8 if out8 is not None else MXFP8.empty(orows, ocols, x.device)
+    c, c8 = out.c(), out8.c()
+    _call("tj_quantize_nvfp4_mxfp8", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols),
+          _ptr(sel), 0 if sel is None else sel.numel(), mode, int(rht), seed, tag, rht_tag, ctypes.byref(c),
+          ctypes.byref(c8), _stream(stream))
+    return out, out8
 
 
 def requantize_nvfp4(q, mode=TJ_SR, rht=True, seed=0, tag=0, rht_tag=0, out=None, stream=None):

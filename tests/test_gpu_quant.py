@@ -105,6 +105,20 @@ def test_quantize_mxfp8_bit_exact(tj, rows, cols, dtype, along):
     assert_mxfp8_equal(q8, Q.quantize_mxfp8(np.ascontiguousarray(xf.T) if along else xf), "mxfp8")
 
 
+@pytest.mark.parametrize("rows,cols,dtype", CASES)
+@pytest.mark.parametrize("along", [False, True])
+@pytest.mark.parametrize("mode,rht", [(1, True), (0, False)])
+def test_quantize_dual_bit_exact(tj, rows, cols, dtype, along, mode, rht):
+    """NVFP4 + MXFP8 of one input from one read: both outputs equal the oracle's."""
+    x = _input(rows, cols, dtype, 11 * rows + cols)
+    q, q8 = tj.quantize_nvfp4_mxfp8(x.cuda(), along_cols=along, mode=mode, rht=rht, seed=19, tag=1, rht_tag=0x100)
+    torch.cuda.synchronize()
+    xf = x.float().numpy()
+    xo = np.ascontiguousarray(xf.T) if along else xf
+    assert_nvfp4_equal(q, _oracle_rows(xo, mode, 19, 1, rht, 0x100), "dual nvfp4")
+    assert_mxfp8_equal(q8, Q.quantize_mxfp8(xo), "dual mxfp8")
+
+
 def test_rht_standalone_bit_exact(tj):
     x = torch.randn(96, 512, generator=torch.Generator().manual_seed(4))
     y = tj.rht(x.cuda(), seed=12345, tag=0x100)
