@@ -142,8 +142,7 @@ class Timeline:
 
 # kernel behind each step call (for per-kernel aggregation of the live event times)
 CALL_KERNEL = {
-    "quant_x": "k_quant_rows (NVFP4)", "quant_dy_row": "k_quant_rows (NVFP4 + MXFP8 of dY)",
-    "quant_x8": "k_quant_rows (MXFP8)",
+    "quant_x": "k_quant_split (OutControl split of X)", "quant_dy_row": "k_quant_rows (NVFP4 + MXFP8 of dY)",
     "quant_dy_col": "k_quant_cols (NVFP4 + MXFP8 of dY)",
     "requant_w": "k_quant_cols<SrcNv> (re-align)", "requant_x": "k_quant_cols<SrcNv> (re-align)",
     "requant_w8": "k_quant_cols<SrcMx> (re-align)", "requant_x8": "k_quant_cols<SrcMx> (re-align)",
@@ -191,7 +190,7 @@ class Linear:
         self.work = {
             "gemm_fwd": (f4(M, N, kn), f4(M, N, k)), "gemm_dx": (f4(M, kn, N), 0.0), "gemm_dx8": (0.0, f4(M, k, N)),
             "gemm_dw": (f4(N, kn, M), 0.0), "gemm_dw8": (0.0, f4(N, k, M)),
-            "quant_x": M * kn * (2 + NV_B), "quant_x8": M * k * (2 + MX_B),
+            "quant_x": M * kn * (2 + NV_B) + M * k * (2 + MX_B),
             "quant_dy_row": M * N * (2 + NV_B + MX_B), "quant_dy_col": M * N * (2 + NV_B + MX_B),
             "requant_w": 2 * kn * N * NV_B, "requant_w8": 2 * k * N * MX_B, "requant_x": 2 * kn * M * NV_B,
             "requant_x8": 2 * k * M * MX_B,
@@ -202,8 +201,8 @@ class Linear:
         s = stream
         SR = tj.TJ_SR
         # forward (tj_linear_fwd)
-        T("quant_x", lambda: tj.quantize_nvfp4(self.X, sel=self.ni, out=self.xq, stream=s))
-        T("quant_x8", lambda: tj.quantize_mxfp8(self.X, sel=self.oi, out=self.x8, stream=s))
+        # the OutControl split of X: NVFP4 normal channels + MXFP8 outlier channels, one read
+        T("quant_x", lambda: tj.quantize_split(self.X, self.ni, self.oi, out=self.xq, out8=self.x8, stream=s))
         T("gemm_fwd", lambda: tj.gemm_nvfp4(self.xq, self.wq, self.x8, self.w8, out=self.Y, stream=s))
         # input gradient (tj_linear_bwd_dx)
         # dY rows: the SR + RHT operand of dX and the MXFP8 rows of dY from one read

@@ -144,6 +144,18 @@ tj_status tj_quantize_nvfp4_mxfp8(const void *x, int dtype, int64_t rows_x, int6
                                   int rht, uint64_t seed, uint32_t tag, uint32_t rht_tag,
                                   tj_nvfp4 *out, tj_mxfp8 *out8, void *stream);
 
+/* tj_quantize_split - OutControl split of a forward operand (§2.C: a static set of outlier
+ * channels kept in FP8, the others in NVFP4), row-wise, from one read of x:
+ *   out  = tj_quantize_nvfp4(x, along_cols=0, sel=normal_idx, TJ_RTN, no RHT)  [rows, n_normal]
+ *   out8 = tj_quantize_mxfp8(x, along_cols=0, sel=outlier_idx)                [rows, n_outlier]
+ * byte for byte.  normal_idx / outlier_idx are the ascending complementary channel lists
+ * of tj_outlier_calibrate (n_normal + n_outlier = cols); out8 may be NULL when
+ * n_outlier = 0.  Rows longer than the kernel's shared-memory staging fall back to the two
+ * gathering passes.  Errors as tj_quantize_nvfp4. */
+tj_status tj_quantize_split(const void *x, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                            const int32_t *normal_idx, int64_t n_normal, const int32_t *outlier_idx,
+                            int64_t n_outlier, tj_nvfp4 *out, tj_mxfp8 *out8, void *stream);
+
 /* tj_requantize_nvfp4 - transposed re-alignment of a forward NVFP4 operand for the
  * backward (§2.A: the backward estimates with X-hat, the dequantized forward operand, and
  * the 1x16 groups of the transposed weight are re-formed along the new contraction axis):

@@ -150,6 +150,29 @@ tj_status tj_quantize_nvfp4_mxfp8(const void *x, int dtype, int64_t rows_x, int6
                                                rht_tag, *out, *out8, static_cast<cudaStream_t>(stream)));
 }
 
+tj_status tj_quantize_split(const void *x, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                            const int32_t *normal_idx, int64_t n_normal, const int32_t *outlier_idx,
+                            int64_t n_outlier, tj_nvfp4 *out, tj_mxfp8 *out8, void *stream) {
+    if (rows < 0 || cols < 0 || n_normal < 0 || n_outlier < 0 || out == nullptr) return TJ_ERR_INVALID_ARG;
+    if (n_normal + n_outlier != cols) return TJ_ERR_SHAPE;
+    if ((n_normal > 0 && normal_idx == nullptr) || (n_outlier > 0 && (outlier_idx == nullptr || out8 == nullptr)))
+        return TJ_ERR_INVALID_ARG;
+    if (!dense_ok(x, dtype, ld, cols)) return TJ_ERR_INVALID_ARG;
+    if (!al_elem(x, dtype)) return TJ_ERR_ALIGN;
+    tj_status st = check_nv(out, rows, n_normal);
+    if (st == TJ_OK && n_outlier > 0) st = check_mx(out8, rows, n_outlier);
+    if (st != TJ_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const tj_mxfp8 none{};
+    const cudaError_t e = launch_quant_split(x, dtype, rows, cols, ld, normal_idx, n_normal, outlier_idx, n_outlier,
+                                             *out, n_outlier > 0 ? *out8 : none, s);
+    if (e != cudaErrorNotSupported) return cuda_status(e);
+    // rows too long to stage: gather the two channel sets separately
+    TJ_TRY(launch_quant_nv_dense(x, dtype, rows, n_normal, ld, 0, normal_idx, TJ_RTN, 0, 0, 0, 0, *out, s));
+    if (n_outlier > 0) TJ_TRY(launch_quant_mx_dense(x, dtype, rows, n_outlier, ld, 0, outlier_idx, *out8, s));
+    return TJ_OK;
+}
+
 tj_status tj_requantize_nvfp4(const tj_nvfp4 *in, int mode, int rht, uint64_t seed, uint32_t tag, uint32_t rht_tag,
                               tj_nvfp4 *out, void *stream) {
     if (in == nullptr || out == nullptr || (mode != TJ_RTN && mode != TJ_SR)) return TJ_ERR_INVALID_ARG;
@@ -245,8 +268,18 @@ tj_status tj_linear_fwd(const void *x, int64_t M, int64_t K, int64_t ldx, const 
     if (st != TJ_OK) return st;
     if (ldy < N) return TJ_ERR_SHAPE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    TJ_TRY(launch_quant_nv_dense(x, TJ_BF16, M, kn, ldx, 0, k > 0 ? normal_idx : nullptr, TJ_RTN, 0, 0, 0, 0, *xq, s));
-    if (k > 0) TJ_TRY(launch_quant_mx_dense(x, TJ_BF16, M, k, ldx, 0, outlier_idx, *x8, s));
+    if (k > 0) {
+        // the OutControl split of X from one read (two gathering passes if a row is too long)
+        const cudaError_t e = launch_quant_split(x, TJ_BF16, M, K, ldx, normal_idx, kn, outlier_idx, k, *xq, *x8, s);
+        if (e != cudaErrorNotSupported) {
+            TJ_TRY(e);
+        } else {
+            TJ_TRY(launch_quant_nv_dense(x, TJ_BF16, M, kn, ldx, 0, normal_idx, TJ_RTN, 0, 0, 0, 0, *xq, s));
+            TJ_TRY(launch_quant_mx_dense(x, TJ_BF16, M, k, ldx, 0, outlier_idx, *x8, s));
+        }
+    } else {
+        TJ_TRY(launch_quant_nv_dense(x, TJ_BF16, M, kn, ldx, 0, nullptr, TJ_RTN, 0, 0, 0, 0, *xq, s));
+    }
     TJ_TRY(launch_gemm(xq, wq, k > 0 ? x8 : nullptr, k > 0 ? w8 : nullptr, 1.0f, y, out_dtype, ldy, M, N, nullptr, s));
     return TJ_OK;
 }

@@ -253,6 +253,86 @@ __global__ void __launch_bounds__(256) k_quant_cols(Src src, OutNv onv, OutMx om
 }
 
 // ---------------------------------------------------------------------------
+// OutControl split of a forward operand, row-wise, one read (§2.C): the normal
+// channels (ascending `sel_n`, compacted) -> NVFP4 RTN, the outlier channels
+// (`sel_o`) -> MXFP8.  Each warp stages whole input rows in shared memory with
+// 16-byte loads and its quads gather the selected columns from there; the
+// channel lists are staged once per CTA.  Same results as the two gathering
+// calls (tj_quantize_nvfp4 RTN with sel = normal, tj_quantize_mxfp8 with
+// sel = outliers).
+// ---------------------------------------------------------------------------
+constexpr int kSplitWarps = 4;
+
+// Shared-memory position of element e of a list: each 32-element block is rotated by
+// its block number, so the quads' reads (lanes 32 elements apart) hit 32 distinct banks.
+__device__ __forceinline__ int split_rot(int e) { return (e & ~31) | ((e + (e >> 5)) & 31); }
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kSplitWarps) k_quant_split(const T *x, int64_t ld, int64_t rows, int K,
+                                                                 const int32_t *sel_n, int kn,
+                                                                 const int32_t *sel_o, int k, OutNv onv,
+                                                                 OutMx omx) {
+    extern __shared__ __align__(16) uint8_t smem_split[];
+    const int kn32 = (kn + 31) & ~31, k32 = (k + 31) & ~31, K32 = (K + 31) & ~31;
+    int32_t *idx_n = reinterpret_cast<int32_t *>(smem_split);             // [kn32], rotated
+    int32_t *idx_o = idx_n + kn32;                                        // [k32], rotated
+    T *rowbuf = reinterpret_cast<T *>(idx_o + k32);
+    for (int i = threadIdx.x; i < kn; i += blockDim.x) idx_n[split_rot(i)] = sel_n[i];
+    for (int i = threadIdx.x; i < k; i += blockDim.x) idx_o[split_rot(i)] = sel_o[i];
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3, qd = lane >> 2;
+    T *rb = rowbuf + (size_t)warp * K32;                                  // the staged row, rotated
+    const int nseg_n = (int)(onv.cols_p / 128), nseg_o = k > 0 ? (int)(omx.cols_p / 128) : 0;
+    const int64_t rows_p = onv.rows_p;
+    const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0) && ((ld * (int64_t)sizeof(T)) % 16 == 0);
+    constexpr int kv = 16 / (int)sizeof(T);                               // elements per 16-byte word
+    for (int64_t row = (int64_t)blockIdx.x * kSplitWarps + warp; row < rows_p;
+         row += (int64_t)gridDim.x * kSplitWarps) {
+        const bool real = row < rows;
+        if (real) {
+            const T *src = x + row * ld;
+            if (vec) {
+                for (int c = lane * kv; c + kv <= K; c += 32 * kv) {
+                    const uint4 w = __ldg(reinterpret_cast<const uint4 *>(src + c));
+                    const T *e = reinterpret_cast<const T *>(&w);
+#pragma unroll
+                    for (int i = 0; i < kv; ++i) rb[split_rot(c + i)] = e[i];
+                }
+                for (int c = (K / kv) * kv + lane; c < K; c += 32) rb[split_rot(c)] = src[c];
+            } else {
+                for (int c = lane; c < K; c += 32) rb[split_rot(c)] = src[c];
+            }
+        }
+        __syncwarp();
+        // normal channels: NVFP4, one quad per 128-segment
+        for (int kb0 = 0; kb0 < nseg_n; kb0 += 8) {
+            const int kb = kb0 + qd;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int c = kb * 128 + 32 * t + j;
+                v[j] = (real && kb < nseg_n && c < kn) ? SrcDense<T>::to_f(rb[split_rot(idx_n[split_rot(c)])]) : 0.0f;
+            }
+            const NvSeg sg = quant_nvfp4_seg<false>(v, 0, PhiloxKeys{}, 0u);
+            store_nv_seg(onv, row, kb, t, sg, kb < nseg_n);
+        }
+        // outlier channels: MXFP8, one quad per 128-segment
+        for (int kb0 = 0; kb0 < nseg_o; kb0 += 8) {
+            const int kb = kb0 + qd;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int c = kb * 128 + 32 * t + j;
+                v[j] = (real && kb < nseg_o && c < k) ? SrcDense<T>::to_f(rb[split_rot(idx_o[split_rot(c)])]) : 0.0f;
+            }
+            const MxSeg m = quant_mxfp8_group(v);
+            store_mx_seg(omx, row, kb, t, m, kb < nseg_o);
+        }
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Standalone RHT (fp32 -> fp32), one quad per 128-block, same butterfly as the
 // fused quantizers.
 // ---------------------------------------------------------------------------
@@ -395,6 +475,32 @@ cudaError_t launch_quant_mx_dense(const void *x, int dtype, int64_t rows_x, int6
     }
     const SrcDense<float> src{static_cast<const float *>(x), ld, rows_x, n_cols_sel, sel};
     return along_cols ? cols_mx(src, o, s) : rows_mx(src, o, s);
+}
+
+// OutControl split of a forward operand (row-wise): NVFP4 RTN of the normal channels
+// and MXFP8 of the outlier channels from one read of x.  Returns cudaErrorNotSupported
+// when a row does not fit the shared-memory staging (the caller then gathers twice).
+cudaError_t launch_quant_split(const void *x, int dtype, int64_t rows, int64_t K, int64_t ld, const int32_t *sel_n,
+                               int64_t kn, const int32_t *sel_o, int64_t k, const tj_nvfp4 &out,
+                               const tj_mxfp8 &out8, cudaStream_t s) {
+    const size_t esz = dtype == TJ_BF16 ? 2 : 4;
+    const size_t smem = (size_t)(((kn + 31) & ~31) + ((k + 31) & ~31)) * 4 + (size_t)kSplitWarps * ((K + 31) & ~31) * esz;
+    if (smem > 200 * 1024 || K > (1 << 30)) return cudaErrorNotSupported;
+    const OutNv o = out_nv(out);
+    const OutMx m = k > 0 ? out_mx(out8) : OutMx{};
+    int64_t grid = (round_up(rows, 128) + kSplitWarps - 1) / kSplitWarps;
+    if (grid > 152 * 16) grid = 152 * 16;
+    if (dtype == TJ_BF16) {
+        cudaFuncSetAttribute(k_quant_split<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k_quant_split<__nv_bfloat16><<<(unsigned)grid, 32 * kSplitWarps, smem, s>>>(
+            static_cast<const __nv_bfloat16 *>(x), ld, rows, (int)K, sel_n, (int)kn, sel_o, (int)k, o, m);
+    } else {
+        cudaFuncSetAttribute(k_quant_split<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k_quant_split<float><<<(unsigned)grid, 32 * kSplitWarps, smem, s>>>(static_cast<const float *>(x), ld, rows,
+                                                                           (int)K, sel_n, (int)kn, sel_o, (int)k,
+                                                                           o, m);
+    }
+    return cudaGetLastError();
 }
 
 // Re-alignment of a forward NVFP4 operand for the backward (§2.A "estimate

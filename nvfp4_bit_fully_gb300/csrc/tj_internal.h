@@ -14,6 +14,9 @@ cudaError_t launch_quant_dual_dense(const void *x, int dtype, int64_t rows_x, in
                                     int along_cols, const int32_t *sel, int mode, int rht, uint64_t seed,
                                     uint32_t tag, uint32_t rht_tag, const tj_nvfp4 &out, const tj_mxfp8 &out8,
                                     cudaStream_t s);
+cudaError_t launch_quant_split(const void *x, int dtype, int64_t rows, int64_t K, int64_t ld, const int32_t *sel_n,
+                               int64_t kn, const int32_t *sel_o, int64_t k, const tj_nvfp4 &out,
+                               const tj_mxfp8 &out8, cudaStream_t s);
 cudaError_t launch_quant_mx_dense(const void *x, int dtype, int64_t rows_x, int64_t n_cols_sel, int64_t ld,
                                   int along_cols, const int32_t *sel, const tj_mxfp8 &out, cudaStream_t s);
 cudaError_t launch_realign_nv(const tj_nvfp4 &in, const tj_nvfp4 &out, int mode, int rht, uint64_t seed,

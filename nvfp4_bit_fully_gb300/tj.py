@@ -49,6 +49,8 @@ _F = ctypes.c_float
 _SIGS = {
     "tj_quantize_nvfp4": [_P, _I, _I64, _I64, _I64, _I, _P, _I64, _I, _I, _U64, _U32, _U32, ctypes.POINTER(CNvfp4), _P],
     "tj_quantize_mxfp8": [_P, _I, _I64, _I64, _I64, _I, _P, _I64, ctypes.POINTER(CMxfp8), _P],
+    "tj_quantize_split": [_P, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, ctypes.POINTER(CNvfp4),
+                          ctypes.POINTER(CMxfp8), _P],
     "tj_quantize_nvfp4_mxfp8": [_P, _I, _I64, _I64, _I64, _I, _P, _I64, _I, _I, _U64, _U32, _U32,
                                 ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P],
     "tj_requantize_nvfp4": [ctypes.POINTER(CNvfp4), _I, _I, _U64, _U32, _U32, ctypes.POINTER(CNvfp4), _P],
@@ -194,6 +196,22 @@ def quantize_nvfp4_mxfp8(x, along_cols=False, sel=None, mode=TJ_RTN, rht=False, 
     _call("tj_quantize_nvfp4_mxfp8", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols),
           _ptr(sel), 0 if sel is None else sel.numel(), mode, int(rht), seed, tag, rht_tag, ctypes.byref(c),
           ctypes.byref(c8), _stream(stream))
+    return out, out8
+
+
+def quantize_split(x, normal_idx, outlier_idx, out=None, out8=None, stream=None):
+    """OutControl split, row-wise, one read: NVFP4 RTN of the normal channels and MXFP8 of
+    the outlier channels (tj_quantize_split)."""
+    rows, cols = x.shape
+    kn, k = normal_idx.numel(), (0 if outlier_idx is None else outlier_idx.numel())
+    out = out if out is not None else NVFP4.empty(rows, kn, x.device)
+    if k > 0 and out8 is None:
+        out8 = MXFP8.empty(rows, k, x.device)
+    c = out.c()
+    c8 = out8.c() if k > 0 else None
+    _call("tj_quantize_split", _ptr(x), _dtype_code(x), rows, cols, x.stride(0), _ptr(normal_idx), kn,
+          _ptr(outlier_idx) if k > 0 else None, k, ctypes.byref(c), ctypes.byref(c8) if c8 is not None else None,
+          _stream(stream))
     return out, out8
 
 

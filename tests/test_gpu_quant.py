@@ -119,6 +119,24 @@ def test_quantize_dual_bit_exact(tj, rows, cols, dtype, along, mode, rht):
     assert_mxfp8_equal(q8, Q.quantize_mxfp8(xo), "dual mxfp8")
 
 
+@pytest.mark.parametrize("rows,cols,dtype,n_out", [(256, 520, torch.bfloat16, 52), (200, 300, torch.float32, 30),
+                                                    (130, 1024, torch.bfloat16, 103), (64, 136, torch.bfloat16, 1)])
+def test_quantize_split_bit_exact(tj, rows, cols, dtype, n_out):
+    """The OutControl split from one read equals the oracle's NVFP4 / MXFP8 of the two channel sets."""
+    x = _input(rows, cols, dtype, 13 * rows + cols)
+    outl = np.sort(np.random.default_rng(rows).choice(cols, n_out, replace=False))
+    normal = OL.normal_channels(cols, outl)
+    ni = torch.from_numpy(normal.astype(np.int32)).cuda()
+    oi = torch.from_numpy(outl.astype(np.int32)).cuda()
+    q, q8 = tj.quantize_split(x.cuda(), ni, oi)
+    torch.cuda.synchronize()
+    xf = x.float().numpy()
+    assert_nvfp4_equal(q, Q.quantize_nvfp4(np.ascontiguousarray(xf[:, normal]), 0), "split nvfp4")
+    assert_mxfp8_equal(q8, Q.quantize_mxfp8(np.ascontiguousarray(xf[:, outl])), "split mxfp8")
+    c, s, o = nvfp4_to_logical_full(q)                       # padded rows written as zero
+    assert not c[rows:].any() and not s[rows:].any() and not o[rows:].any()
+
+
 def test_rht_standalone_bit_exact(tj):
     x = torch.randn(96, 512, generator=torch.Generator().manual_seed(4))
     y = tj.rht(x.cuda(), seed=12345, tag=0x100)
