@@ -147,7 +147,6 @@ CALL_KERNEL = {
     "requant_w": "k_quant_cols<SrcNv> (re-align)", "requant_x": "k_quant_cols<SrcNv> (re-align)",
     "requant_w8": "k_quant_cols<SrcMx> (re-align)", "requant_x8": "k_quant_cols<SrcMx> (re-align)",
     "gemm_fwd": "k_gemm_nvfp4", "gemm_dx": "k_gemm_nvfp4", "gemm_dw": "k_gemm_nvfp4",
-    "gemm_dx8": "k_gemm_nvfp4", "gemm_dw8": "k_gemm_nvfp4",
     "osci_reset": "k_osci_reset",
 }
 
@@ -188,8 +187,8 @@ class Linear:
         # algorithmic work of every call: (FP4 flops, FP8 flops) or bytes
         f4 = lambda a, b, c: 2.0 * a * b * c
         self.work = {
-            "gemm_fwd": (f4(M, N, kn), f4(M, N, k)), "gemm_dx": (f4(M, kn, N), 0.0), "gemm_dx8": (0.0, f4(M, k, N)),
-            "gemm_dw": (f4(N, kn, M), 0.0), "gemm_dw8": (0.0, f4(N, k, M)),
+            "gemm_fwd": (f4(M, N, kn), f4(M, N, k)), "gemm_dx": (f4(M, kn, N), f4(M, k, N)),
+            "gemm_dw": (f4(N, kn, M), f4(N, k, M)),
             "quant_x": M * kn * (2 + NV_B) + M * k * (2 + MX_B),
             "quant_dy_row": M * N * (2 + NV_B + MX_B), "quant_dy_col": M * N * (2 + NV_B + MX_B),
             "requant_w": 2 * kn * N * NV_B, "requant_w8": 2 * k * N * MX_B, "requant_x": 2 * kn * M * NV_B,
@@ -211,20 +210,19 @@ class Linear:
                                                           stream=s))
         T("requant_w", lambda: tj.requantize_nvfp4(self.wq, SR, True, seed, tj.TAG_WT, tj.TAG_RHT_DX, out=self.s_w,
                                                    stream=s))
-        T("gemm_dx", lambda: tj.gemm_nvfp4(self.s_dy, self.s_w, alpha=2.0 ** -7, out=self.dX, col_map=self.ni,
-                                           stream=s))
         T("requant_w8", lambda: tj.requantize_mxfp8(self.w8, out=self.q8_w, stream=s))
-        T("gemm_dx8", lambda: tj.gemm_mxfp8(self.q8_dy, self.q8_w, out=self.dX, col_map=self.oi, stream=s))
+        # the FP4 product and its FP8 outlier slice in one launch
+        T("gemm_dx", lambda: tj.gemm_pair(self.s_dy, self.s_w, self.q8_dy, self.q8_w, alpha=2.0 ** -7, out=self.dX,
+                                          out8=self.dX, col_map=self.ni, col_map8=self.oi, stream=s))
         # weight gradient (tj_linear_bwd_dw)
         T("quant_dy_col", lambda: tj.quantize_nvfp4_mxfp8(self.dY, along_cols=True, mode=SR, rht=True, seed=seed,
                                                           tag=tj.TAG_DY_COL, rht_tag=tj.TAG_RHT_DW, out=self.s_dyt,
                                                           out8=self.q8_dyt, stream=s))
         T("requant_x", lambda: tj.requantize_nvfp4(self.xq, SR, True, seed, tj.TAG_XT, tj.TAG_RHT_DW, out=self.s_x,
                                                    stream=s))
-        T("gemm_dw", lambda: tj.gemm_nvfp4(self.s_dyt, self.s_x, alpha=2.0 ** -7, out=self.dW, col_map=self.ni,
-                                           stream=s))
         T("requant_x8", lambda: tj.requantize_mxfp8(self.x8, out=self.q8_x, stream=s))
-        T("gemm_dw8", lambda: tj.gemm_mxfp8(self.q8_dyt, self.q8_x, out=self.dW, col_map=self.oi, stream=s))
+        T("gemm_dw", lambda: tj.gemm_pair(self.s_dyt, self.s_x, self.q8_dyt, self.q8_x, alpha=2.0 ** -7, out=self.dW,
+                                          out8=self.dW, col_map=self.ni, col_map8=self.oi, stream=s))
 
     def run_api(self, tj, seed, stream):
         """The same step through the user-facing calls (tj_linear_fwd / bwd_dx / bwd_dw)."""

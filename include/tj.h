@@ -198,6 +198,15 @@ tj_status tj_gemm_nvfp4(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8
 tj_status tj_gemm_mxfp8(const tj_mxfp8 *a8, const tj_mxfp8 *b8, void *d, int out_dtype, int64_t ldd,
                         const int32_t *col_map, void *stream);
 
+/* tj_gemm_pair - tj_gemm_nvfp4(a, b, alpha, d, out_dtype, ldd, col_map) without an FP8
+ * slice, and tj_gemm_mxfp8(a8, b8, d8, out8_dtype, ldd8, col_map8), in one launch: the
+ * FP4 product of a backward pass and its FP8 outlier slice (§2.C) write disjoint column
+ * sets (of the same or different outputs), and the FP8 slice alone is too small to fill
+ * the GPU.  Same arguments, layouts and errors as the two calls; results are the same. */
+tj_status tj_gemm_pair(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, void *d, int out_dtype,
+                       int64_t ldd, const int32_t *col_map, const tj_mxfp8 *a8, const tj_mxfp8 *b8,
+                       void *d8, int out8_dtype, int64_t ldd8, const int32_t *col_map8, void *stream);
+
 /* ---------------------------------------------------------------------------
  * tj_linear_fwd - forward of the NVFP4 linear layer (§2: NVFP4 for activations,
  * weights and gradients of every linear layer; §2.A RTN double-block quantization;
@@ -268,6 +277,7 @@ size_t tj_noalloc_scratch_bytes(void);
 
 #define TJ_OP_BWD_DX 1
 #define TJ_OP_BWD_DW 2
+
 /* Bytes of workspace the backward call `op` needs for these sizes (K = K_N + k). */
 size_t tj_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t k);
 

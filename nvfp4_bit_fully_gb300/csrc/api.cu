@@ -236,6 +236,25 @@ tj_status tj_gemm_mxfp8(const tj_mxfp8 *a8, const tj_mxfp8 *b8, void *d, int out
                                    static_cast<cudaStream_t>(stream)));
 }
 
+tj_status tj_gemm_pair(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, void *d, int out_dtype, int64_t ldd,
+                       const int32_t *col_map, const tj_mxfp8 *a8, const tj_mxfp8 *b8, void *d8, int out8_dtype,
+                       int64_t ldd8, const int32_t *col_map8, void *stream) {
+    if (a == nullptr || b == nullptr || d == nullptr || a8 == nullptr || b8 == nullptr || d8 == nullptr)
+        return TJ_ERR_INVALID_ARG;
+    if ((out_dtype != TJ_BF16 && out_dtype != TJ_FP32) || (out8_dtype != TJ_BF16 && out8_dtype != TJ_FP32))
+        return TJ_ERR_INVALID_ARG;
+    tj_status st = check_nv(a, a->rows, a->cols);
+    if (st == TJ_OK) st = check_nv(b, b->rows, a->cols);
+    if (st == TJ_OK) st = check_mx(a8, a8->rows, a8->cols);
+    if (st == TJ_OK) st = check_mx(b8, b8->rows, a8->cols);
+    if (st != TJ_OK) return st;
+    if (ldd < (col_map ? 1 : b->rows) || ldd8 < (col_map8 ? 1 : b8->rows)) return TJ_ERR_SHAPE;
+    if (!al16(d) || !al16(d8)) return TJ_ERR_ALIGN;
+    return cuda_status(launch_gemm_pair(a, b, alpha, d, out_dtype, ldd, a->rows, b->rows, col_map, a8, b8, d8,
+                                        out8_dtype, ldd8, a8->rows, b8->rows, col_map8,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 size_t tj_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t k) {
     if (M < 0 || N < 0 || K < 0 || k < 0 || k > K) return 0;
     const int64_t kn = K - k;
@@ -318,11 +337,13 @@ tj_status tj_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, c
         TJ_TRY(launch_quant_nv_dense(dy, TJ_BF16, M, N, lddy, 0, nullptr, TJ_SR, 1, seed, TJ_TAG_DY_ROW,
                                      TJ_TAG_RHT_DX, s_dy, s));
     TJ_TRY(launch_realign_nv(*wq, s_w, TJ_SR, 1, seed, TJ_TAG_WT, TJ_TAG_RHT_DX, s));
-    TJ_TRY(launch_gemm(&s_dy, &s_w, nullptr, nullptr, 0.0078125f, dx, out_dtype, lddx, M, kn,
-                       k > 0 ? normal_idx : nullptr, s));
     if (k > 0) {
+        // the FP4 product (normal columns of dX) and the FP8 slice (outlier columns) in one launch
         TJ_TRY(launch_realign_mx(*w8, q8_w, s));
-        TJ_TRY(launch_gemm(nullptr, nullptr, &q8_dy, &q8_w, 1.0f, dx, out_dtype, lddx, M, k, outlier_idx, s));
+        TJ_TRY(launch_gemm_pair(&s_dy, &s_w, 0.0078125f, dx, out_dtype, lddx, M, kn, normal_idx, &q8_dy, &q8_w, dx,
+                                out_dtype, lddx, M, k, outlier_idx, s));
+    } else {
+        TJ_TRY(launch_gemm(&s_dy, &s_w, nullptr, nullptr, 0.0078125f, dx, out_dtype, lddx, M, kn, nullptr, s));
     }
     return TJ_OK;
 }
@@ -359,11 +380,13 @@ tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, c
         TJ_TRY(launch_quant_nv_dense(dy, TJ_BF16, M, N, lddy, 1, nullptr, TJ_SR, 1, seed, TJ_TAG_DY_COL,
                                      TJ_TAG_RHT_DW, s_dy, s));
     TJ_TRY(launch_realign_nv(*xq, s_x, TJ_SR, 1, seed, TJ_TAG_XT, TJ_TAG_RHT_DW, s));
-    TJ_TRY(launch_gemm(&s_dy, &s_x, nullptr, nullptr, 0.0078125f, dw, TJ_FP32, lddw, N, kn,
-                       k > 0 ? normal_idx : nullptr, s));
     if (k > 0) {
+        // the FP4 product (normal columns of dW) and the FP8 slice (outlier columns) in one launch
         TJ_TRY(launch_realign_mx(*x8, q8_x, s));
-        TJ_TRY(launch_gemm(nullptr, nullptr, &q8_dy, &q8_x, 1.0f, dw, TJ_FP32, lddw, N, k, outlier_idx, s));
+        TJ_TRY(launch_gemm_pair(&s_dy, &s_x, 0.0078125f, dw, TJ_FP32, lddw, N, kn, normal_idx, &q8_dy, &q8_x, dw,
+                                TJ_FP32, lddw, N, k, outlier_idx, s));
+    } else {
+        TJ_TRY(launch_gemm(&s_dy, &s_x, nullptr, nullptr, 0.0078125f, dw, TJ_FP32, lddw, N, kn, nullptr, s));
     }
     return TJ_OK;
 }

@@ -87,23 +87,54 @@ constexpr uint32_t kColSf8 = kColSf + 16 * kPSlots;             // FP8 scale fac
 static_assert(kColSf8 + 8 * kSf8Slots <= kTmemCols, "tensor memory budget");
 static_assert(kNamedP + kPSlots <= 16, "named barriers");
 
-struct GemmArgs {
+// One product D = alpha * A B^T of the launch.  A launch computes one or two of them:
+// pr[0] with FP4 blocks (and optionally an FP8 K-slice into the same tiles), and
+// optionally pr[1], an FP8-only product with its own output (the outlier slice of a
+// backward GEMM), whose tiles are scheduled first so they spread over the SMs.
+struct GemmProblem {
     int64_t M, N;                 // logical output size
-    int tiles_m, tiles_n;         // 128 x 128 output tiles
+    int tiles_m, tiles_n;         // 128 x 128 output tiles (0 x 0: absent)
     int nkb4;                     // 128-K blocks of the FP4 part (0: none)
     int nk8;                      // 128-K stages of the FP8 part (0: none)
+    float alpha;                  // applied to the FP4 part
+    void *d;
+    int out_bf16;
+    int64_t ldd;
+    const int32_t *col_map;       // output column n goes to column col_map[n] (nullptr: n)
+};
+
+struct GemmArgs {
+    GemmProblem pr[2];
     const uint8_t *sfa4, *sfb4;   // scale tiles, FP4 operands
     int64_t ntk_a4, ntk_b4;       // scale tiles per 128-row tile (cols_p / 64)
     const float *outa, *outb;     // FP32 outer scales [cols_p/128][rows_p]
     int64_t rpa, rpb;             // rows_p of A and B
-    const uint8_t *sfa8, *sfb8;   // scale tiles, FP8 operands
+    const uint8_t *sfa8, *sfb8;   // scale tiles, FP8 operands (of whichever product has FP8 stages)
     int64_t ntk_a8, ntk_b8;       // cols_p / 128
-    float alpha;
-    void *d;
-    int out_bf16;
-    int64_t ldd;
-    const int32_t *col_map;
 };
+
+// The work of one output tile: its product, origin and K schedule (FP4 stages of two
+// 128-K blocks first, then the FP8 stages, which accumulate into one partial).
+struct TileWork {
+    int p;
+    int64_t m0, n0;
+    int nkb4, nk8, nst4, nstages, nblk;
+};
+__device__ __forceinline__ TileWork tile_work(const GemmArgs &a, int t) {
+    const int t1 = a.pr[1].tiles_m * a.pr[1].tiles_n;
+    TileWork w;
+    w.p = t < t1 ? 1 : 0;
+    const int i = w.p ? t : t - t1;
+    const int tn = w.p ? a.pr[1].tiles_n : a.pr[0].tiles_n;
+    w.m0 = (int64_t)(i / tn) * 128;
+    w.n0 = (int64_t)(i % tn) * 128;
+    w.nkb4 = w.p ? a.pr[1].nkb4 : a.pr[0].nkb4;
+    w.nk8 = w.p ? a.pr[1].nk8 : a.pr[0].nk8;
+    w.nst4 = (w.nkb4 + 1) / 2;
+    w.nstages = w.nst4 + w.nk8;
+    w.nblk = w.nkb4 + (w.nk8 > 0 ? 1 : 0);
+    return w;
+}
 
 struct Bars {
     uint64_t full[kStages], empty[kStages];
@@ -198,7 +229,6 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
     return d;
 }
 
-template <int CM, int CN>
 __global__ void __launch_bounds__(kThreadsGemm, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tm_a4, const __grid_constant__ CUtensorMap tm_b4,
                  const __grid_constant__ CUtensorMap tm_a8, const __grid_constant__ CUtensorMap tm_b8,
@@ -207,24 +237,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars *bars = reinterpret_cast<Bars *>(smem + kSmemBar);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // cluster of CM x CN CTAs computing a (CM*128) x (CN*128) block of tiles; the CTAs
-    // with the same m share the A tile, those with the same n the B tile
-    constexpr int CS = CM * CN;
-    const uint32_t crank = CS > 1 ? ptx::cluster_ctarank() : 0u;
-    const int cm = (int)(crank % CM), cn = (int)(crank / CM);
-    const int cid = (int)blockIdx.x / CS, ncl = (int)gridDim.x / CS;
-    const int ctn = args.tiles_n / CN;
-    const int ntiles = (args.tiles_m / CM) * ctn;          // cluster tiles
-    auto tile_m0 = [&](int ct) { return (int64_t)((ct / ctn) * CM + cm) * 128; };
-    auto tile_n0 = [&](int ct) { return (int64_t)((ct % ctn) * CN + cn) * 128; };
-    const int nst4 = (args.nkb4 + 1) / 2;
-    const int nstages = nst4 + args.nk8;
-    const int nblk = args.nkb4 + (args.nk8 > 0 ? 1 : 0);  // partials per tile (the FP8 slice is one)
+    const int ntiles = args.pr[0].tiles_m * args.pr[0].tiles_n + args.pr[1].tiles_m * args.pr[1].tiles_n;
+    const int cta = (int)blockIdx.x, ncta = (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(&bars->full[s], 1);
-            ptx::mbar_init(&bars->empty[s], CS);            // every CTA of the cluster releases each stage
+            ptx::mbar_init(&bars->empty[s], 1);
         }
         for (int p = 0; p < kPSlots; ++p) ptx::mbar_init(&bars->pfull[p], 1);
         for (int q = 0; q < kScaleSlots; ++q) ptx::mbar_init(&bars->sempty[q], 1);
@@ -237,27 +256,20 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (CS > 1) ptx::cluster_sync();                        // partners' barriers exist before any multicast
     const uint32_t tbase = bars->tmem_base;
 
     if (warp < kProdWarps) {
         // ------------------------------------------------------------ producers: one thread can
         // issue a stage only every few hundred cycles, so stages alternate between warps
         if (lane == 0) {
-            if (args.nkb4 > 0) { ptx::prefetch_tmap(&tm_a4); ptx::prefetch_tmap(&tm_b4); }
-            if (args.nk8 > 0) { ptx::prefetch_tmap(&tm_a8); ptx::prefetch_tmap(&tm_b8); }
-            int it = 0;
+            if (args.pr[0].nkb4 > 0) { ptx::prefetch_tmap(&tm_a4); ptx::prefetch_tmap(&tm_b4); }
+            if (args.pr[0].nk8 > 0 || args.pr[1].nk8 > 0) { ptx::prefetch_tmap(&tm_a8); ptx::prefetch_tmap(&tm_b8); }
+            int it = 0, fbase = 0;                            // stages / FP4 blocks of earlier tiles
             bool ok = true;
-            // multicast masks: the CTAs sharing this CTA's A tile (same cm) and B tile (same cn)
-            uint16_t mask_a = 0, mask_b = 0;
-            for (int j = 0; j < CN; ++j) mask_a |= (uint16_t)(1u << (cm + CM * j));
-            for (int i = 0; i < CM; ++i) mask_b |= (uint16_t)(1u << (i + CM * cn));
-            constexpr int ra = 128 / CN, rb = 128 / CM;      // rows of A / B this CTA loads
-            int tcount = 0;                                   // tiles of this CTA so far
-            for (int tile = cid; tile < ntiles && ok; tile += ncl, ++tcount) {
-                const int64_t m0 = tile_m0(tile), n0 = tile_n0(tile);
-                const int64_t rta = m0 / 128, rtb = n0 / 128;
-                for (int st = 0; st < nstages; ++st, ++it) {
+            for (int tile = cta; tile < ntiles && ok; tile += ncta) {
+                const TileWork w = tile_work(args, tile);
+                const int64_t rta = w.m0 / 128, rtb = w.n0 / 128;
+                for (int st = 0; st < w.nstages; ++st, ++it) {
                     if (it % kProdWarps != warp) continue;
                     const int slot = it % kStages;
                     if (it >= kStages && !wait_bounded(&bars->empty[slot], ((it / kStages) - 1) & 1, bars)) {
@@ -268,16 +280,14 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     uint8_t *sb = smem + kSmemB + slot * kTileBytes;
                     uint8_t *sfa = smem + kSmemSfa + slot * kSfStageBytes;
                     uint8_t *sfb = smem + kSmemSfb + slot * kSfStageBytes;
-                    const bool fp4 = st < nst4;
-                    const int k0 = fp4 ? st : st - nst4;              // 128-byte column of the operand rows
-                    const CUtensorMap *ta = fp4 ? &tm_a4 : &tm_a8;
-                    const CUtensorMap *tb = fp4 ? &tm_b4 : &tm_b8;
-                    const int nkbs = fp4 ? min(2, args.nkb4 - 2 * st) : 0;
+                    const bool fp4 = st < w.nst4;
+                    const int k0 = fp4 ? st : st - w.nst4;            // 128-byte column of the operand rows
+                    const int nkbs = fp4 ? min(2, w.nkb4 - 2 * st) : 0;
                     const uint32_t sfbytes = fp4 ? (uint32_t)nkbs * 1024u : 512u;
                     // the outer-scale slots of the stage's blocks: FP4 block f (counted over this
                     // CTA's tiles) uses slot f % kScaleSlots, freed when the promotion of block
                     // f - kScaleSlots has finished with it
-                    const int f0 = tcount * args.nkb4 + 2 * st;
+                    const int f0 = fbase + 2 * st;
                     for (int j = 0; j < nkbs && ok; ++j) {
                         const int f = f0 + j;
                         if (f >= kScaleSlots &&
@@ -289,30 +299,23 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     // scales of the stage's blocks all land on one barrier
                     ptx::mbar_arrive_expect_tx(&bars->full[slot],
                                                2u * kTileBytes + 2u * sfbytes + (uint32_t)nkbs * 1024u);
-                    if (CN > 1)
-                        ptx::tma_load_2d_multicast(sa + cn * ra * 128, ta, k0 * 128, (int32_t)(m0 + cn * ra),
-                                                   &bars->full[slot], mask_a);
-                    else
-                        ptx::tma_load_2d(sa, ta, k0 * 128, (int32_t)m0, &bars->full[slot]);
-                    if (CM > 1)
-                        ptx::tma_load_2d_multicast(sb + cm * rb * 128, tb, k0 * 128, (int32_t)(n0 + cm * rb),
-                                                   &bars->full[slot], mask_b);
-                    else
-                        ptx::tma_load_2d(sb, tb, k0 * 128, (int32_t)n0, &bars->full[slot]);
+                    ptx::tma_load_2d(sa, fp4 ? &tm_a4 : &tm_a8, k0 * 128, (int32_t)w.m0, &bars->full[slot]);
+                    ptx::tma_load_2d(sb, fp4 ? &tm_b4 : &tm_b8, k0 * 128, (int32_t)w.n0, &bars->full[slot]);
                     if (fp4) {
                         ptx::bulk_load(sfa, args.sfa4 + (rta * args.ntk_a4 + 4 * st) * 512, sfbytes, &bars->full[slot]);
                         ptx::bulk_load(sfb, args.sfb4 + (rtb * args.ntk_b4 + 4 * st) * 512, sfbytes, &bars->full[slot]);
                         for (int j = 0; j < nkbs; ++j) {
                             const int64_t kb = 2 * st + j;
                             uint8_t *so = smem + kSmemScale + ((f0 + j) % kScaleSlots) * 1024;
-                            ptx::bulk_load(so, args.outa + kb * args.rpa + m0, 512u, &bars->full[slot]);
-                            ptx::bulk_load(so + 512, args.outb + kb * args.rpb + n0, 512u, &bars->full[slot]);
+                            ptx::bulk_load(so, args.outa + kb * args.rpa + w.m0, 512u, &bars->full[slot]);
+                            ptx::bulk_load(so + 512, args.outb + kb * args.rpb + w.n0, 512u, &bars->full[slot]);
                         }
                     } else {
                         ptx::bulk_load(sfa, args.sfa8 + (rta * args.ntk_a8 + k0) * 512, 512u, &bars->full[slot]);
                         ptx::bulk_load(sfb, args.sfb8 + (rtb * args.ntk_b8 + k0) * 512, 512u, &bars->full[slot]);
                     }
                 }
+                fbase += w.nkb4;
             }
             // drain: every copy this warp issued must have landed before the CTA exits
             for (int j = (it > kStages ? it - kStages : 0); j < it; ++j)
@@ -336,8 +339,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             if (r >= 0 && lane == 0) ptx::mbar_arrive(&bars->sempty[r]);
             rel &= ~(0xffu << (8 * idx));
         };
-        for (int tile = cid; tile < ntiles; tile += ncl) {
-            for (int st = 0; st < nstages; ++st, ++it) {
+        for (int tile = cta; tile < ntiles; tile += ncta) {
+            const TileWork w = tile_work(args, tile);
+            for (int st = 0; st < w.nstages; ++st, ++it) {
                 const int slot = it % kStages;
                 if (live) live = warp_wait_bounded(&bars->full[slot], (it / kStages) & 1, bars, lane);
                 ptx::tc_fence_after();
@@ -345,8 +349,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                 const uint32_t sb = ptx::smem_u32(smem + kSmemB + slot * kTileBytes);
                 const uint32_t sfa = ptx::smem_u32(smem + kSmemSfa + slot * kSfStageBytes);
                 const uint32_t sfb = ptx::smem_u32(smem + kSmemSfb + slot * kSfStageBytes);
-                if (st < nst4) {
-                    const int nkbs = min(2, args.nkb4 - 2 * st);
+                if (st < w.nst4) {
+                    const int nkbs = min(2, w.nkb4 - 2 * st);
                     for (int kbl = 0; kbl < nkbs; ++kbl, ++pc) {
                         const int ps = pc % kPSlots;
                         if (pc >= kPSlots) named_sync(kNamedP + ps, kNamedCount);
@@ -377,7 +381,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                 } else {
                     // the FP8 slice: all its stages accumulate into one partial slot; their
                     // scale factors rotate through kSf8Slots slots freed by commits
-                    const int s8 = st - nst4;
+                    const int s8 = st - w.nst4;
                     const int ps = pc % kPSlots;
                     if (s8 == 0) {
                         if (pc >= kPSlots) named_sync(kNamedP + ps, kNamedCount);
@@ -398,19 +402,14 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                                           sfcol + 4, (uint32_t)(s8 > 0 || j > 0));
                         }
                         ptx::tc_commit(&bars->f8free[f8]);
-                        if (s8 == args.nk8 - 1) ptx::tc_commit(&bars->pfull[ps]);
+                        if (s8 == w.nk8 - 1) ptx::tc_commit(&bars->pfull[ps]);
                     }
                     __syncwarp();
                     ++g8;
-                    if (s8 == args.nk8 - 1) ++pc;
+                    if (s8 == w.nk8 - 1) ++pc;
                 }
-                // release the stage in every CTA whose shared memory this cluster's loads fill
-                if (live && lane == 0) {
-                    if (CS > 1)
-                        ptx::tc_commit_multicast(&bars->empty[slot], (uint16_t)((1u << CS) - 1u));
-                    else
-                        ptx::tc_commit(&bars->empty[slot]);
-                }
+                // the stage's buffers are free once its MMAs complete
+                if (live && lane == 0) ptx::tc_commit(&bars->empty[slot]);
                 __syncwarp();
             }
         }
@@ -435,12 +434,15 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         int ps = 0;
         uint32_t pph = 0;                       // partial ring slot and phase
         bool live = true;                       // false after an abort: the barrier protocol goes on, the work stops
-        for (int tile = cid; tile < ntiles; tile += ncl) {
-            const int64_t m0 = tile_m0(tile), n0 = tile_n0(tile);
+        for (int tile = cta; tile < ntiles; tile += ncta) {
+            const TileWork w = tile_work(args, tile);
+            const GemmProblem &g = w.p ? args.pr[1] : args.pr[0];
+            const int64_t m0 = w.m0, n0 = w.n0;
+            const float alpha = g.alpha;
             uint64_t acc[kColsW / 2];
 #pragma unroll
             for (int j = 0; j < kColsW / 2; ++j) acc[j] = 0ull;
-            for (int kb = 0; kb < nblk; ++kb) {
+            for (int kb = 0; kb < w.nblk; ++kb) {
                 if (live) live = warp_wait_bounded(&bars->pfull[ps], pph, bars, lane);
                 const float *so = reinterpret_cast<const float *>(smem + kSmemScale + (f4c % kScaleSlots) * 1024);
 #pragma unroll
@@ -467,11 +469,11 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                             named_sync(kNamedP + ps, kNamedCount);
                     }
                     uint64_t *ac = acc + (kLdCols / 2) * ch;
-                    if (kb < args.nkb4) {
+                    if (kb < w.nkb4) {
                         if (live) {
                             // the block's outer scales: its slot goes back to the producers only
                             // after this warp has released the next block's partial
-                            const float sa = so[32 * q + lane] * args.alpha;
+                            const float sa = so[32 * q + lane] * alpha;
                             const uint64_t sa2 = pack2(sa, sa);
                             const float4 *sbp = reinterpret_cast<const float4 *>(
                                 so + 128 + kColsW * cq + kLdCols * ch);
@@ -492,17 +494,17 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     }
                 }
                 if (++ps == kPSlots) { ps = 0; pph ^= 1u; }
-                if (kb < args.nkb4) ++f4c;
+                if (kb < w.nkb4) ++f4c;
             }
             if (!live) continue;
             // epilogue.  Plain case: this thread's row segment of kColsW columns, written with
             // 16-byte stores
             const int64_t row = m0 + 32 * q + lane;
             const int64_t nb = n0 + kColsW * cq;
-            const bool fast_tile = args.col_map == nullptr && nb + kColsW <= args.N && (args.ldd & 7) == 0;
-            if (fast_tile && row < args.M) {
-                if (args.out_bf16) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.d) + row * args.ldd + nb);
+            const bool fast_tile = g.col_map == nullptr && nb + kColsW <= g.N && (g.ldd & 7) == 0;
+            if (fast_tile && row < g.M) {
+                if (g.out_bf16) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(g.d) + row * g.ldd + nb);
 #pragma unroll
                     for (int i = 0; i < kColsW / 8; ++i) {
                         uint32_t w4[4];
@@ -514,7 +516,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                         dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                 } else {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(args.d) + row * args.ldd + nb);
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(g.d) + row * g.ldd + nb);
 #pragma unroll
                     for (int i = 0; i < kColsW / 4; ++i)
                         dst[i] = make_float4(lo2(acc[2 * i]), hi2(acc[2 * i]), lo2(acc[2 * i + 1]), hi2(acc[2 * i + 1]));
@@ -526,7 +528,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             // lane per column, so each store instruction covers one contiguous row segment
             uint32_t *stg = reinterpret_cast<uint32_t *>(smem + kSmemEpi) + pw * (32 * 33);
             const int64_t rbase = m0 + 32 * q;
-            if (args.out_bf16) {
+            if (g.out_bf16) {
 #pragma unroll
                 for (int j = 0; j < kColsW / 2; ++j) {
                     __nv_bfloat162 b2 = __floats2bfloat162_rn(lo2(acc[j]), hi2(acc[j]));
@@ -534,13 +536,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                 }
                 __syncwarp();
                 const int64_t na = nb + 2 * lane, nz = na + 1;   // this lane's column pair
-                const bool va = na < args.N, vz = nz < args.N;
-                const int64_t ca = va ? (args.col_map ? (int64_t)args.col_map[na] : na) : 0;
-                const int64_t cz = vz ? (args.col_map ? (int64_t)args.col_map[nz] : nz) : 0;
-                const bool pair = va && vz && cz == ca + 1 && ((ca | args.ldd) & 1) == 0;
-                for (int r = 0; r < 32 && rbase + r < args.M; ++r) {
+                const bool va = na < g.N, vz = nz < g.N;
+                const int64_t ca = va ? (g.col_map ? (int64_t)g.col_map[na] : na) : 0;
+                const int64_t cz = vz ? (g.col_map ? (int64_t)g.col_map[nz] : nz) : 0;
+                const bool pair = va && vz && cz == ca + 1 && ((ca | g.ldd) & 1) == 0;
+                for (int r = 0; r < 32 && rbase + r < g.M; ++r) {
                     const uint32_t w = stg[r * 33 + lane];
-                    __nv_bfloat16 *drow = static_cast<__nv_bfloat16 *>(args.d) + (rbase + r) * args.ldd;
+                    __nv_bfloat16 *drow = static_cast<__nv_bfloat16 *>(g.d) + (rbase + r) * g.ldd;
                     if (pair) {
                         *reinterpret_cast<uint32_t *>(drow + ca) = w;
                     } else {
@@ -559,10 +561,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     }
                     __syncwarp();
                     const int64_t n = nb + 32 * h + lane;
-                    const bool v = n < args.N;
-                    const int64_t c = v ? (args.col_map ? (int64_t)args.col_map[n] : n) : 0;
-                    for (int r = 0; r < 32 && rbase + r < args.M; ++r)
-                        if (v) static_cast<float *>(args.d)[(rbase + r) * args.ldd + c] = __uint_as_float(stg[r * 33 + lane]);
+                    const bool v = n < g.N;
+                    const int64_t c = v ? (g.col_map ? (int64_t)g.col_map[n] : n) : 0;
+                    for (int r = 0; r < 32 && rbase + r < g.M; ++r)
+                        if (v) static_cast<float *>(g.d)[(rbase + r) * g.ldd + c] = __uint_as_float(stg[r * 33 + lane]);
                     __syncwarp();
                 }
             }
@@ -570,7 +572,6 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (CS > 1) ptx::cluster_sync();                        // no partner still writes into this CTA
     if (warp == kMmaWarp) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tbase, kTmemCols);
@@ -621,41 +622,62 @@ int num_sms_of_current_device() {
     return n > 0 ? n : 148;
 }
 
-// Launch one cluster shape: persistent grid of as many clusters as fit at once.
-template <int CM, int CN>
-cudaError_t launch_cluster(const CUtensorMap (&tm)[4], const GemmArgs &g, cudaStream_t s) {
-    constexpr int CS = CM * CN;
+// Persistent launch: one CTA per SM (or per tile, if fewer).
+cudaError_t launch_persistent(const CUtensorMap (&tm)[4], const GemmArgs &g, cudaStream_t s) {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_nvfp4<CM, CN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes + 1024);
+        const cudaError_t e =
+            cudaFuncSetAttribute(k_gemm_nvfp4, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes + 1024);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int nctiles = (g.tiles_m / CM) * (g.tiles_n / CN);
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreadsGemm);
-    cfg.dynamicSmemBytes = kSmemBytes + 1024;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    static int max_clusters = 0;
-    if (max_clusters == 0) {
-        cfg.gridDim = dim3(CS * 64);
-        int n = 0;
-        if (CS > 1 && cudaOccupancyMaxActiveClusters(&n, k_gemm_nvfp4<CM, CN>, &cfg) == cudaSuccess && n > 0)
-            max_clusters = n;
-        else
-            max_clusters = num_sms_of_current_device() / CS;
-    }
-    const int nclusters = nctiles < max_clusters ? nctiles : max_clusters;
-    cfg.gridDim = dim3((unsigned)(nclusters * CS));
-    return cudaLaunchKernelEx(&cfg, k_gemm_nvfp4<CM, CN>, tm[0], tm[1], tm[2], tm[3], g);
+    const int ntiles = g.pr[0].tiles_m * g.pr[0].tiles_n + g.pr[1].tiles_m * g.pr[1].tiles_n;
+    if (ntiles == 0) return cudaSuccess;
+    const int nsm = num_sms_of_current_device();
+    k_gemm_nvfp4<<<(unsigned)(ntiles < nsm ? ntiles : nsm), kThreadsGemm, kSmemBytes + 1024, s>>>(tm[0], tm[1], tm[2],
+                                                                                                tm[3], g);
+    return cudaGetLastError();
+}
+
+GemmProblem problem(int64_t M, int64_t N, float alpha, void *d, int out_dtype, int64_t ldd, const int32_t *col_map) {
+    GemmProblem p{};
+    p.M = M;
+    p.N = N;
+    p.alpha = alpha;
+    p.d = d;
+    p.out_bf16 = out_dtype == TJ_BF16;
+    p.ldd = ldd;
+    p.col_map = col_map;
+    p.tiles_m = (int)(round_up(M, 128) / 128);
+    p.tiles_n = (int)(round_up(N, 128) / 128);
+    return p;
+}
+
+// FP4 operands -> tensor maps 0/1 and the scale pointers; returns the 128-K block count.
+bool set_fp4(const tj_nvfp4 &a, const tj_nvfp4 &b, GemmArgs &g, CUtensorMap (&tm)[4], int &nkb4) {
+    const int64_t kp = round_up(a.cols, 128);
+    nkb4 = (int)(kp / 128);
+    g.sfa4 = a.sf;
+    g.sfb4 = b.sf;
+    g.ntk_a4 = kp / 64;
+    g.ntk_b4 = kp / 64;
+    g.outa = a.outer;
+    g.outb = b.outer;
+    g.rpa = round_up(a.rows, 128);
+    g.rpb = round_up(b.rows, 128);
+    return make_tile_map(&tm[0], a.codes, g.rpa, kp / 2, 128u) && make_tile_map(&tm[1], b.codes, g.rpb, kp / 2, 128u);
+}
+
+// FP8 operands -> tensor maps 2/3 and the scale pointers; returns the 128-K stage count.
+bool set_fp8(const tj_mxfp8 &a8, const tj_mxfp8 &b8, GemmArgs &g, CUtensorMap (&tm)[4], int &nk8) {
+    const int64_t kp8 = round_up(a8.cols, 128);
+    nk8 = (int)(kp8 / 128);
+    g.sfa8 = a8.sf;
+    g.sfb8 = b8.sf;
+    g.ntk_a8 = kp8 / 128;
+    g.ntk_b8 = kp8 / 128;
+    return make_tile_map(&tm[2], a8.codes, round_up(a8.rows, 128), kp8, 128u) &&
+           make_tile_map(&tm[3], b8.codes, round_up(b8.rows, 128), kp8, 128u);
 }
 
 }  // namespace
@@ -664,50 +686,29 @@ cudaError_t launch_gemm(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8
                         void *d, int out_dtype, int64_t ldd, int64_t M, int64_t N, const int32_t *col_map,
                         cudaStream_t s) {
     GemmArgs g{};
-    g.M = M;
-    g.N = N;
-    g.alpha = alpha;
-    g.d = d;
-    g.out_bf16 = out_dtype == TJ_BF16;
-    g.ldd = ldd;
-    g.col_map = col_map;
-    g.tiles_m = (int)(round_up(M, 128) / 128);
-    g.tiles_n = (int)(round_up(N, 128) / 128);
-    if (g.tiles_m == 0 || g.tiles_n == 0) return cudaSuccess;
-    // cluster shape: the kernel can pair tiles along M (sharing B) and N (sharing A) with
-    // TMA multicast, but on GB300 the L2 feeds independent CTAs fast enough and the cluster's
-    // shared stage releases only couple the CTAs' pipelines (measured ~5% slower), so every
-    // CTA runs alone
-    const int cm = 1, cn = 1;
+    g.pr[0] = problem(M, N, alpha, d, out_dtype, ldd, col_map);
+    if (g.pr[0].tiles_m == 0 || g.pr[0].tiles_n == 0) return cudaSuccess;
     CUtensorMap tm[4];
     memset(tm, 0, sizeof(tm));
-    if (a != nullptr && b != nullptr) {
-        const int64_t kp = round_up(a->cols, 128);
-        g.nkb4 = (int)(kp / 128);
-        g.sfa4 = a->sf;
-        g.sfb4 = b->sf;
-        g.ntk_a4 = kp / 64;
-        g.ntk_b4 = kp / 64;
-        g.outa = a->outer;
-        g.outb = b->outer;
-        g.rpa = round_up(a->rows, 128);
-        g.rpb = round_up(b->rows, 128);
-        if (!make_tile_map(&tm[0], a->codes, g.rpa, kp / 2, 128u / cn) ||
-            !make_tile_map(&tm[1], b->codes, g.rpb, kp / 2, 128u / cm))
-            return cudaErrorInvalidValue;
-    }
-    if (a8 != nullptr && b8 != nullptr && a8->cols > 0) {
-        const int64_t kp8 = round_up(a8->cols, 128);
-        g.nk8 = (int)(kp8 / 128);
-        g.sfa8 = a8->sf;
-        g.sfb8 = b8->sf;
-        g.ntk_a8 = kp8 / 128;
-        g.ntk_b8 = kp8 / 128;
-        if (!make_tile_map(&tm[2], a8->codes, round_up(a8->rows, 128), kp8, 128u / cn) ||
-            !make_tile_map(&tm[3], b8->codes, round_up(b8->rows, 128), kp8, 128u / cm))
-            return cudaErrorInvalidValue;
-    }
-    return launch_cluster<1, 1>(tm, g, s);
+    if (a != nullptr && b != nullptr && !set_fp4(*a, *b, g, tm, g.pr[0].nkb4)) return cudaErrorInvalidValue;
+    if (a8 != nullptr && b8 != nullptr && a8->cols > 0 && !set_fp8(*a8, *b8, g, tm, g.pr[0].nk8))
+        return cudaErrorInvalidValue;
+    return launch_persistent(tm, g, s);
+}
+
+cudaError_t launch_gemm_pair(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, void *d, int out_dtype, int64_t ldd,
+                             int64_t M, int64_t N, const int32_t *col_map, const tj_mxfp8 *a8, const tj_mxfp8 *b8,
+                             void *d8, int out8_dtype, int64_t ldd8, int64_t M8, int64_t N8, const int32_t *col_map8,
+                             cudaStream_t s) {
+    GemmArgs g{};
+    g.pr[0] = problem(M, N, alpha, d, out_dtype, ldd, col_map);
+    g.pr[1] = problem(M8, N8, 1.0f, d8, out8_dtype, ldd8, col_map8);
+    CUtensorMap tm[4];
+    memset(tm, 0, sizeof(tm));
+    if (!set_fp4(*a, *b, g, tm, g.pr[0].nkb4) || !set_fp8(*a8, *b8, g, tm, g.pr[1].nk8)) return cudaErrorInvalidValue;
+    if (g.pr[0].tiles_m * g.pr[0].tiles_n == 0) g.pr[0].tiles_m = g.pr[0].tiles_n = 0;
+    if (g.pr[1].tiles_m * g.pr[1].tiles_n == 0 || g.pr[1].nk8 == 0) g.pr[1].tiles_m = g.pr[1].tiles_n = 0;
+    return launch_persistent(tm, g, s);
 }
 
 unsigned int read_and_clear_device_error() {

@@ -30,6 +30,11 @@ cudaError_t launch_dequant_nv(const tj_nvfp4 &q, float *y, int64_t ldy, cudaStre
 cudaError_t launch_gemm(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8, const tj_mxfp8 *b8,
                         float alpha, void *d, int out_dtype, int64_t ldd, int64_t M, int64_t N,
                         const int32_t *col_map, cudaStream_t s);
+// An FP4 product and an FP8-only product (each with its own output) in one launch.
+cudaError_t launch_gemm_pair(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, void *d, int out_dtype, int64_t ldd,
+                             int64_t M, int64_t N, const int32_t *col_map, const tj_mxfp8 *a8, const tj_mxfp8 *b8,
+                             void *d8, int out8_dtype, int64_t ldd8, int64_t M8, int64_t N8, const int32_t *col_map8,
+                             cudaStream_t s);
 
 cudaError_t launch_osci_reset(float *w, float *w_prev, float *dist_q, float *dist_m, const tj_nvfp4 &q_prev,
                               const tj_nvfp4 &q_out, uint32_t *mask, int64_t rows, int64_t cols, float lr,

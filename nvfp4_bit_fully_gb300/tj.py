@@ -60,6 +60,8 @@ _SIGS = {
     "tj_gemm_nvfp4": [ctypes.POINTER(CNvfp4), ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8),
                       ctypes.POINTER(CMxfp8), _F, _P, _I, _I64, _P, _P],
     "tj_gemm_mxfp8": [ctypes.POINTER(CMxfp8), ctypes.POINTER(CMxfp8), _P, _I, _I64, _P, _P],
+    "tj_gemm_pair": [ctypes.POINTER(CNvfp4), ctypes.POINTER(CNvfp4), _F, _P, _I, _I64, _P, ctypes.POINTER(CMxfp8),
+                     ctypes.POINTER(CMxfp8), _P, _I, _I64, _P, _P],
     "tj_linear_fwd": [_P, _I64, _I64, _I64, ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P, _P, _I64,
                       ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P, _I, _I64, _P],
     "tj_linear_bwd_dx": [_P, _I64, _I64, _I64, ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P, _P, _I64, _U64,
@@ -265,6 +267,16 @@ def gemm_mxfp8(a8, b8, out=None, out_dtype=torch.float32, col_map=None, stream=N
     _call("tj_gemm_mxfp8", ctypes.byref(ca), ctypes.byref(cb), _ptr(out), _dtype_code(out), out.stride(0),
           _ptr(col_map), _stream(stream))
     return out
+
+
+def gemm_pair(a, b, a8, b8, alpha=1.0, out=None, out8=None, col_map=None, col_map8=None, stream=None):
+    """An FP4 product and an FP8-only product in one launch (tj_gemm_pair); out / out8 may be
+    the same tensor when the column maps are disjoint."""
+    ca, cb, ca8, cb8 = a.c(), b.c(), a8.c(), b8.c()
+    _call("tj_gemm_pair", ctypes.byref(ca), ctypes.byref(cb), float(alpha), _ptr(out), _dtype_code(out),
+          out.stride(0), _ptr(col_map), ctypes.byref(ca8), ctypes.byref(cb8), _ptr(out8), _dtype_code(out8),
+          out8.stride(0), _ptr(col_map8), _stream(stream))
+    return out, out8
 
 
 def workspace_size(op, M, N, K, k):

@@ -129,3 +129,27 @@ def test_gemm_fp8_slice_long(tj):
     tj.device_status()
     ref = OL.gemm_fp8(ra, rb)
     assert_gemm_close(d.cpu().numpy(), ref, abs_product_fp8(ra, rb), what="fp8 long")
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gemm_pair_equals_the_two_products(tj, out_dtype):
+    """An FP4 product and an FP8-only product in one launch, written through disjoint column
+    maps into one output: each matches the oracle, and both equal the separate calls."""
+    M, N, K, k = 384, 300, 640, 700
+    qa, qb, ra, rb = _operands(tj, M, N, K, seed=41)
+    a8, b8, ra8, rb8 = _fp8_operands(tj, M, 96, k, seed=42)
+    perm = torch.randperm(N + 96, generator=torch.Generator().manual_seed(7)).to(torch.int32)
+    cm, cm8 = perm[:N].sort().values, perm[N:].sort().values
+    out = torch.full((M, N + 96), -3.0, dtype=out_dtype, device="cuda")
+    tj.gemm_pair(qa, qb, a8, b8, alpha=2.0 ** -7, out=out, out8=out, col_map=cm.cuda(), col_map8=cm8.cuda())
+    ref_sep = torch.full_like(out, -3.0)
+    tj.gemm_nvfp4(qa, qb, alpha=2.0 ** -7, out=ref_sep, col_map=cm.cuda())
+    tj.gemm_mxfp8(a8, b8, out=ref_sep, col_map=cm8.cuda())
+    torch.cuda.synchronize()
+    tj.device_status()
+    assert torch.equal(out, ref_sep)
+    got = out.float().cpu().numpy()
+    bf = out_dtype == torch.bfloat16
+    assert_gemm_close(got[:, cm.numpy()], OL.gemm_fp4(ra, rb, 2.0 ** -7), abs_product(ra, rb, 2.0 ** -7), bf16=bf,
+                      what="pair fp4")
+    assert_gemm_close(got[:, cm8.numpy()], OL.gemm_fp8(ra8, rb8), abs_product_fp8(ra8, rb8), bf16=bf, what="pair fp8")
