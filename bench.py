@@ -259,7 +259,6 @@ class OsciState:
 TRAFFIC_BYTES_PER_ELEM = {"k_osci_reset": 28.5}
 NV_B = 0.5 + 1.0 / 16 + 4.0 / 128      # bytes per NVFP4 element (codes + E4M3 + FP32 scales)
 MX_B = 1.0 + 1.0 / 32                   # bytes per MXFP8 element (E4M3 + UE8M0)
-LAUNCHES_PER_LINEAR = 15                # with an FP8 outlier slice: fwd 3, dX 6, dW 6
 
 
 # ---------------------------------------------------------------------------
@@ -551,7 +550,10 @@ def main():
                 "frac": round(achieved / hbm_peak, 3),
                 "traffic": (round(TRAFFIC_BYTES_PER_ELEM[dom] * osci.n) if dom in TRAFFIC_BYTES_PER_ELEM else None),
                 "algorithmic_bytes_per_launch": round(by / n), "peak_source": peak_src + " hbm_gbs"}
-    launches = args.steps * (LAUNCHES_PER_LINEAR * len(linears) + 1)
+    # every recorded call of the timed region launches exactly one kernel of the library
+    # (per linear: split + GEMM, dY rows + 2 re-alignments + GEMM pair, dY columns + 2
+    # re-alignments + GEMM pair; then one OsciReset)
+    launches = len(tl.records)
 
     extras = {}
     if not args.no_extras and rank == 0:
