@@ -130,18 +130,19 @@ __device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
 // up with probability p = (a - lo) / (hi - lo), decided as float(u16) < p * 65536.
 // Integer form of that same test: for a >= 1 in the binade [2^e, 2^(e+1)) the grid
 // keeps 1 mantissa bit, so p = r / 2^22 with r the 22 lower mantissa bits and the
-// test is 64 * u16 < r; on [0.5, 1) p = m / 2^23 (test 128 * u16 < m); below 0.5
-// lo = 0 and p * 65536 = a * 2^17 exactly.  Returns the grid index (0..7).
+// test is 128 * u16 < 2 r; on [0.5, 1) p = m / 2^23 (test 128 * u16 < m); below 0.5
+// lo = 0 and p * 65536 = a * 2^17 exactly, compared with u16 converted exactly
+// (2^23 + u16 as fp32, minus 2^23).  Every case is evaluated and selected, without
+// branches.  Returns the grid index (0..7).
 __device__ __forceinline__ uint32_t e2m1_sr(float a, uint32_t u16) {
     const uint32_t A = __float_as_uint(a);
-    const bool big = A >= 0x3F800000u;             // a >= 1
-    const bool mid = A >= 0x3F000000u;             // a >= 0.5
+    const uint32_t big = A >= 0x3F800000u ? 1u : 0u;              // a >= 1
+    const bool mid = A >= 0x3F000000u;                            // a >= 0.5
+    const bool up_hi = (u16 << 7) < ((A << big) & 0x7FFFFFu);
+    const float uf = __fsub_rn(__uint_as_float(0x4B000000u | u16), 8388608.0f);
+    const bool up_lo = uf < __fmul_rn(a, 131072.0f);
     const uint32_t lo = big ? (A >> 22) - 252u : (mid ? 1u : 0u);
-    bool up;
-    if (big) up = (u16 << 6) < (A & 0x3FFFFFu);
-    else if (mid) up = (u16 << 7) < (A & 0x7FFFFFu);
-    else up = (float)u16 < __fmul_rn(a, 131072.0f);
-    return lo + (up ? 1u : 0u);
+    return lo + ((mid ? up_hi : up_lo) ? 1u : 0u);
 }
 
 // ---------------------------------------------------------------------------
