@@ -73,7 +73,10 @@ constexpr int kSmemSfb = kSmemSfa + kStages * kSfStageBytes;
 constexpr int kScaleSlots = 8;                 // FP32 outer-scale ring: one FP4 block per slot, [A 128 | B 128]
 constexpr int kSmemScale = kSmemSfb + kStages * kSfStageBytes;
 constexpr int kSmemBar = kSmemScale + kScaleSlots * 1024;
-constexpr int kSmemEpi = kSmemBar + 512;       // per promotion warp: 32 rows x 33 words (epilogue staging)
+// Epilogue staging, per promotion warp: a 4 KB 1024-aligned box for TMA stores (stride 4096)
+// or 32 rows x 33 words for the row-at-a-time writes (stride 4224).  A launch uses only one
+// of the two layouts (TMA stores only in single-product launches).
+constexpr int kSmemEpi = (kSmemBar + 512 + 1023) & ~1023;
 constexpr int kSmemBytes = kSmemEpi + kPromoWarps * 32 * 33 * 4;
 static_assert(kSmemBytes + 1024 <= 227 * 1024, "shared memory budget");
 constexpr int kThreadsGemm = 32 * (kPromo0 + kPromoWarps);
@@ -85,6 +88,7 @@ constexpr uint32_t kColP = 0;                                   // partials: 128
 constexpr uint32_t kColSf = 128 * kPSlots;                      // FP4 scale factors: 16 columns per partial slot
 constexpr uint32_t kColSf8 = kColSf + 16 * kPSlots;             // FP8 scale factors: 8 columns per slot
 static_assert(kColSf8 + 8 * kSf8Slots <= kTmemCols, "tensor memory budget");
+static_assert(kColsW == 64, "epilogue staging: 32 rows x 128 bytes (bf16) or 2 x 32 words (fp32) per warp");
 static_assert(kNamedP + kPSlots <= 16, "named barriers");
 
 // One product D = alpha * A B^T of the launch.  A launch computes one or two of them:
@@ -101,6 +105,7 @@ struct GemmProblem {
     int out_bf16;
     int64_t ldd;
     const int32_t *col_map;       // output column n goes to column col_map[n] (nullptr: n)
+    int tma_store;                // bf16, no col_map, ldd % 8 == 0: tiles leave by TMA stores (map tm_d)
 };
 
 struct GemmArgs {
@@ -232,7 +237,7 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
 __global__ void __launch_bounds__(kThreadsGemm, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tm_a4, const __grid_constant__ CUtensorMap tm_b4,
                  const __grid_constant__ CUtensorMap tm_a8, const __grid_constant__ CUtensorMap tm_b8,
-                 const GemmArgs args) {
+                 const __grid_constant__ CUtensorMap tm_d, const GemmArgs args) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars *bars = reinterpret_cast<Bars *>(smem + kSmemBar);
@@ -497,37 +502,40 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                 if (kb < w.nkb4) ++f4c;
             }
             if (!live) continue;
-            // epilogue.  Plain case: this thread's row segment of kColsW columns, written with
-            // 16-byte stores
-            const int64_t row = m0 + 32 * q + lane;
-            const int64_t nb = n0 + kColsW * cq;
-            const bool fast_tile = g.col_map == nullptr && nb + kColsW <= g.N && (g.ldd & 7) == 0;
-            if (fast_tile && row < g.M) {
-                if (g.out_bf16) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(g.d) + row * g.ldd + nb);
-#pragma unroll
-                    for (int i = 0; i < kColsW / 8; ++i) {
-                        uint32_t w4[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            __nv_bfloat162 b2 = __floats2bfloat162_rn(lo2(acc[4 * i + k]), hi2(acc[4 * i + k]));
-                            w4[k] = *reinterpret_cast<uint32_t *>(&b2);
-                        }
-                        dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                    }
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(g.d) + row * g.ldd + nb);
-#pragma unroll
-                    for (int i = 0; i < kColsW / 4; ++i)
-                        dst[i] = make_float4(lo2(acc[2 * i]), hi2(acc[2 * i]), lo2(acc[2 * i + 1]), hi2(acc[2 * i + 1]));
-                }
-            }
-            if (fast_tile) continue;
-            // scattered columns (col_map), a ragged right edge or an unaligned row pitch: the
-            // warp stages its 32 x kColsW slice in shared memory and writes it row by row, a
-            // lane per column, so each store instruction covers one contiguous row segment
-            uint32_t *stg = reinterpret_cast<uint32_t *>(smem + kSmemEpi) + pw * (32 * 33);
+            // epilogue: the warp's 32 x kColsW slice of the tile (rows 32q.., columns kColsW*cq..)
             const int64_t rbase = m0 + 32 * q;
+            const int64_t nb = n0 + kColsW * cq;
+            if (g.tma_store) {
+                uint32_t *stg = reinterpret_cast<uint32_t *>(smem + kSmemEpi + pw * 4096);
+                if (lane == 0) ptx::bulk_wait_read_all();     // this warp's previous TMA store has read it
+                __syncwarp();
+                // bf16 without scatter: each lane's 128-byte row segment goes to the staging buffer
+                // in the 128-byte swizzle of the output tensor map, and one TMA store writes the
+                // slice (clipping rows >= M and columns >= N) while the warp moves on
+                uint8_t *rowp = reinterpret_cast<uint8_t *>(stg) + lane * 128;
+#pragma unroll
+                for (int i = 0; i < kColsW / 8; ++i) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(lo2(acc[4 * i + k]), hi2(acc[4 * i + k]));
+                        w4[k] = *reinterpret_cast<uint32_t *>(&b2);
+                    }
+                    *reinterpret_cast<uint4 *>(rowp + ((i ^ (lane & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_2d(&tm_d, (int32_t)nb, (int32_t)rbase, stg);
+                    ptx::bulk_commit_group();
+                }
+                continue;
+            }
+            // fp32 outputs, scattered columns (col_map), ragged edges or unaligned row pitches: the
+            // warp stages its 32 x kColsW slice in shared memory (rows of 33 words, so row writes
+            // and column reads are both free of bank conflicts) and writes it row by row, a lane
+            // per column, so each store instruction covers one contiguous row segment
+            uint32_t *stg = reinterpret_cast<uint32_t *>(smem + kSmemEpi) + pw * (32 * 33);
             if (g.out_bf16) {
 #pragma unroll
                 for (int j = 0; j < kColsW / 2; ++j) {
@@ -569,6 +577,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                 }
             }
         }
+        // every TMA store of this warp has completed before the CTA exits
+        if (lane == 0) ptx::bulk_wait_all();
+        __syncwarp();
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -615,6 +626,20 @@ bool make_tile_map(CUtensorMap *m, const void *base, int64_t rows_p, int64_t row
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 output [M][ldd] -> boxes of 32 rows x 64 columns (128 bytes), 128-byte swizzle, for
+// the epilogue's TMA stores.
+bool make_out_map(CUtensorMap *m, void *d, int64_t M, int64_t N, int64_t ldd) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)ldd * 2u};
+    const cuuint32_t box[2] = {64u, 32u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int num_sms_of_current_device() {
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
@@ -623,7 +648,7 @@ int num_sms_of_current_device() {
 }
 
 // Persistent launch: one CTA per SM (or per tile, if fewer).
-cudaError_t launch_persistent(const CUtensorMap (&tm)[4], const GemmArgs &g, cudaStream_t s) {
+cudaError_t launch_persistent(const CUtensorMap (&tm)[5], const GemmArgs &g, cudaStream_t s) {
     static bool attr_set = false;
     if (!attr_set) {
         const cudaError_t e =
@@ -635,7 +660,7 @@ cudaError_t launch_persistent(const CUtensorMap (&tm)[4], const GemmArgs &g, cud
     if (ntiles == 0) return cudaSuccess;
     const int nsm = num_sms_of_current_device();
     k_gemm_nvfp4<<<(unsigned)(ntiles < nsm ? ntiles : nsm), kThreadsGemm, kSmemBytes + 1024, s>>>(tm[0], tm[1], tm[2],
-                                                                                                tm[3], g);
+                                                                                                tm[3], tm[4], g);
     return cudaGetLastError();
 }
 
@@ -654,7 +679,7 @@ GemmProblem problem(int64_t M, int64_t N, float alpha, void *d, int out_dtype, i
 }
 
 // FP4 operands -> tensor maps 0/1 and the scale pointers; returns the 128-K block count.
-bool set_fp4(const tj_nvfp4 &a, const tj_nvfp4 &b, GemmArgs &g, CUtensorMap (&tm)[4], int &nkb4) {
+bool set_fp4(const tj_nvfp4 &a, const tj_nvfp4 &b, GemmArgs &g, CUtensorMap (&tm)[5], int &nkb4) {
     const int64_t kp = round_up(a.cols, 128);
     nkb4 = (int)(kp / 128);
     g.sfa4 = a.sf;
@@ -669,7 +694,7 @@ bool set_fp4(const tj_nvfp4 &a, const tj_nvfp4 &b, GemmArgs &g, CUtensorMap (&tm
 }
 
 // FP8 operands -> tensor maps 2/3 and the scale pointers; returns the 128-K stage count.
-bool set_fp8(const tj_mxfp8 &a8, const tj_mxfp8 &b8, GemmArgs &g, CUtensorMap (&tm)[4], int &nk8) {
+bool set_fp8(const tj_mxfp8 &a8, const tj_mxfp8 &b8, GemmArgs &g, CUtensorMap (&tm)[5], int &nk8) {
     const int64_t kp8 = round_up(a8.cols, 128);
     nk8 = (int)(kp8 / 128);
     g.sfa8 = a8.sf;
@@ -680,6 +705,14 @@ bool set_fp8(const tj_mxfp8 &a8, const tj_mxfp8 &b8, GemmArgs &g, CUtensorMap (&
            make_tile_map(&tm[3], b8.codes, round_up(b8.rows, 128), kp8, 128u);
 }
 
+// Plain bf16 outputs (no column map, 16-byte row pitch) of a single-product launch leave the
+// kernel by TMA stores.
+void set_tma_store(GemmProblem &p, CUtensorMap &tm) {
+    p.tma_store = p.out_bf16 && p.col_map == nullptr && (p.ldd & 7) == 0 &&
+                  (reinterpret_cast<uintptr_t>(p.d) & 15) == 0 && p.M > 0 && p.N > 0 &&
+                  make_out_map(&tm, p.d, p.M, p.N, p.ldd);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8, const tj_mxfp8 *b8, float alpha,
@@ -688,11 +721,12 @@ cudaError_t launch_gemm(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8
     GemmArgs g{};
     g.pr[0] = problem(M, N, alpha, d, out_dtype, ldd, col_map);
     if (g.pr[0].tiles_m == 0 || g.pr[0].tiles_n == 0) return cudaSuccess;
-    CUtensorMap tm[4];
+    CUtensorMap tm[5];
     memset(tm, 0, sizeof(tm));
     if (a != nullptr && b != nullptr && !set_fp4(*a, *b, g, tm, g.pr[0].nkb4)) return cudaErrorInvalidValue;
     if (a8 != nullptr && b8 != nullptr && a8->cols > 0 && !set_fp8(*a8, *b8, g, tm, g.pr[0].nk8))
         return cudaErrorInvalidValue;
+    set_tma_store(g.pr[0], tm[4]);
     return launch_persistent(tm, g, s);
 }
 
@@ -703,7 +737,7 @@ cudaError_t launch_gemm_pair(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, 
     GemmArgs g{};
     g.pr[0] = problem(M, N, alpha, d, out_dtype, ldd, col_map);
     g.pr[1] = problem(M8, N8, 1.0f, d8, out8_dtype, ldd8, col_map8);
-    CUtensorMap tm[4];
+    CUtensorMap tm[5];
     memset(tm, 0, sizeof(tm));
     if (!set_fp4(*a, *b, g, tm, g.pr[0].nkb4) || !set_fp8(*a8, *b8, g, tm, g.pr[1].nk8)) return cudaErrorInvalidValue;
     if (g.pr[0].tiles_m * g.pr[0].tiles_n == 0) g.pr[0].tiles_m = g.pr[0].tiles_n = 0;
