@@ -34,7 +34,7 @@
 // The FP8 slice accumulates over its whole K into the next partial slot, which the
 // promotion adds with weight 1.
 // Tensor memory (512 columns): partials [0,384) (128 per slot), FP4 scale factors
-// [384,432) (16 per partial slot), FP8 scale factors [432,496) (8 per slot).
+// [384,432) (16 per partial slot), FP8 scale factors [432,472) (8 per operand ring slot).
 // Every mbarrier wait is bounded; a wait that runs out sets the sticky device
 // error flag and an abort flag.  The roles then stop working but keep the named-
 // barrier protocol (whose counts depend only on the problem size), in-flight copies
@@ -57,7 +57,6 @@ namespace {
 
 constexpr int kStages = 5;                     // operand ring (2 x 128-K blocks per stage)
 constexpr int kPSlots = 3;                     // tensor-memory partial slots (128-K blocks in flight)
-constexpr int kSf8Slots = 8;                   // tensor-memory scale-factor slots of FP8 stages
 constexpr int kProdWarps = 3;                  // TMA producers; stage it is issued by warp it % kProdWarps
 constexpr int kMmaWarp = kProdWarps;           // tensor-memory owner and MMA issuer
 constexpr int kPromo0 = kProdWarps + 1;        // first promotion warp
@@ -86,8 +85,8 @@ constexpr long long kWaitClk = 4000000000ll;  // per wait: about 2 s at the maxi
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColP = 0;                                   // partials: 128 columns per slot
 constexpr uint32_t kColSf = 128 * kPSlots;                      // FP4 scale factors: 16 columns per partial slot
-constexpr uint32_t kColSf8 = kColSf + 16 * kPSlots;             // FP8 scale factors: 8 columns per slot
-static_assert(kColSf8 + 8 * kSf8Slots <= kTmemCols, "tensor memory budget");
+constexpr uint32_t kColSf8 = kColSf + 16 * kPSlots;             // FP8 scale factors: 8 columns per operand slot
+static_assert(kColSf8 + 8 * kStages <= kTmemCols, "tensor memory budget");
 static_assert(kColsW == 64, "epilogue staging: 32 rows x 128 bytes (bf16) or 2 x 32 words (fp32) per warp");
 static_assert(kNamedP + kPSlots <= 16, "named barriers");
 
@@ -145,7 +144,6 @@ struct Bars {
     uint64_t full[kStages], empty[kStages];
     uint64_t pfull[kPSlots];
     uint64_t sempty[kScaleSlots];
-    uint64_t f8free[kSf8Slots];
     uint64_t drain;
     uint32_t tmem_base;
     volatile int abort_flag;
@@ -252,7 +250,6 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         }
         for (int p = 0; p < kPSlots; ++p) ptx::mbar_init(&bars->pfull[p], 1);
         for (int q = 0; q < kScaleSlots; ++q) ptx::mbar_init(&bars->sempty[q], 1);
-        for (int f = 0; f < kSf8Slots; ++f) ptx::mbar_init(&bars->f8free[f], 1);
         ptx::mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         ptx::fence_mbar_init();
@@ -332,7 +329,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         // meets every promotion warp's release of the block that used it three blocks earlier;
         // that also frees the slot's scale-factor columns, which only that block's MMAs read.
         const uint32_t idesc4 = idesc_nvf4();
-        int it = 0, pc = 0, g8 = 0, f4 = 0;
+        int it = 0, pc = 0, f4 = 0;
         bool live = true;
         // The promotion warps read the outer scales of FP4 block b after releasing its partial
         // and before releasing the next one, so b's outer-scale slot is handed back to the
@@ -384,20 +381,19 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                         ++f4;
                     }
                 } else {
-                    // the FP8 slice: all its stages accumulate into one partial slot; their
-                    // scale factors rotate through kSf8Slots slots freed by commits
+                    // the FP8 slice: all its stages accumulate into one partial slot.  A stage's
+                    // scale factors use the tensor-memory slot of its operand ring slot: the
+                    // previous user of that slot, stage it - kStages, has completed its MMAs,
+                    // because the producers refilled the ring slot only after its release
                     const int s8 = st - w.nst4;
                     const int ps = pc % kPSlots;
                     if (s8 == 0) {
                         if (pc >= kPSlots) named_sync(kNamedP + ps, kNamedCount);
                         release((pc + 1) & 3);
                     }
-                    const int f8 = g8 % kSf8Slots;
-                    if (live && g8 >= kSf8Slots)
-                        live = warp_wait_bounded(&bars->f8free[f8], ((g8 / kSf8Slots) - 1) & 1, bars, lane);
                     ptx::tc_fence_after();
                     if (live && lane == 0) {
-                        const uint32_t sfcol = tbase + kColSf8 + 8u * (uint32_t)f8;
+                        const uint32_t sfcol = tbase + kColSf8 + 8u * (uint32_t)slot;
                         ptx::tc_cp_32x128b_warpx4(sfcol, ptx::smem_desc(sfa, 0, 128, 0));
                         ptx::tc_cp_32x128b_warpx4(sfcol + 4, ptx::smem_desc(sfb, 0, 128, 0));
 #pragma unroll
@@ -406,11 +402,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                                           ptx::smem_desc(sb + 32u * j, 16, 1024, 2), idesc_mxf8((uint32_t)j), sfcol,
                                           sfcol + 4, (uint32_t)(s8 > 0 || j > 0));
                         }
-                        ptx::tc_commit(&bars->f8free[f8]);
                         if (s8 == w.nk8 - 1) ptx::tc_commit(&bars->pfull[ps]);
                     }
                     __syncwarp();
-                    ++g8;
                     if (s8 == w.nk8 - 1) ++pc;
                 }
                 // the stage's buffers are free once its MMAs complete
