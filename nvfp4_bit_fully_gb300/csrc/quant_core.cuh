@@ -23,23 +23,32 @@ __device__ __forceinline__ void rht128_quad(float (&x)[32], uint32_t sign_word, 
     for (int j = 0; j < 32; ++j)
         x[j] = __uint_as_float(__float_as_uint(x[j]) ^ ((sign_word << (31 - j)) & 0x80000000u));
 #pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
+    for (int j = 0; j < 32; j += 2) {
+        const float a = x[j], b = x[j + 1];
+        x[j] = __fadd_rn(a, b);
+        x[j + 1] = __fsub_rn(a, b);
+    }
+    // h = 2 .. 16 on packed pairs: (x[j], x[j+1]) with (x[j+h], x[j+h+1])
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+    for (int h = 2; h < 32; h <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
             if ((j & h) == 0) {
-                const float a = x[j], b = x[j + h];
-                x[j] = __fadd_rn(a, b);
-                x[j + h] = __fsub_rn(a, b);
+                const uint64_t a = f2_pack(x[j], x[j + 1]), b = f2_pack(x[j + h], x[j + h + 1]);
+                f2_unpack(f2_add(a, b), x[j], x[j + 1]);
+                f2_unpack(f2_sub(a, b), x[j + h], x[j + h + 1]);
             }
         }
     }
 #pragma unroll
     for (int m = 1; m <= 2; m <<= 1) {
         const float sgn = (t & m) ? -1.0f : 1.0f;
+        const uint64_t sgn2 = f2_pack(sgn, sgn);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float p = __shfl_xor_sync(0xffffffffu, x[j], m);
-            x[j] = __fmaf_rn(sgn, x[j], p);
+        for (int j = 0; j < 32; j += 2) {
+            const float p0 = __shfl_xor_sync(0xffffffffu, x[j], m);
+            const float p1 = __shfl_xor_sync(0xffffffffu, x[j + 1], m);
+            f2_unpack(f2_fma(sgn2, f2_pack(x[j], x[j + 1]), f2_pack(p0, p1)), x[j], x[j + 1]);
         }
     }
 }
@@ -88,8 +97,30 @@ __device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t 
         const float s = __fmul_rn(e4m3_to_float(sb), s_o);
         const float r = s > 0.0f ? __fdiv_rn(1.0f, s) : 0.0f;
         if (!(s > 0.0f)) continue;                         // zero group: codes stay 0
-        if (SR) {
-            uint4 w4;                                      // drawn just in time, 8 elements per call
+        if (SR && r <= 3.4028235e38f) {
+            // two elements at a time: y = x * r + 0 (so x = -0 gives +0 and its code 0,
+            // while a negative x whose product underflows keeps its sign), then the
+            // packed stochastic rounding; uniforms drawn just in time, 8 elements a call
+            const uint64_t r2 = f2_pack(r, r), z2 = f2_pack(0.0f, 0.0f);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint4 w4 = sr_bits8((elem0 >> 3) + (uint64_t)(2 * g + h), pk, tag);
+                const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+                uint32_t word = 0u;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int e = 16 * g + 8 * h + 2 * i;
+                    uint32_t t0, t1;
+                    e2m1x2_sr_nib(f2_fma(f2_pack(x[e], x[e + 1]), r2, z2), (ws[i] << 12) & 0x0FFFF000u,
+                                  (ws[i] >> 4) & 0x0FFFF000u, t0, t1);
+                    word |= (t0 >> (28 - 8 * i)) & (0xFu << (8 * i));
+                    word |= (t1 >> (24 - 8 * i)) & (0xF0u << (8 * i));
+                }
+                words[2 * g + h] = word;
+            }
+        } else if (SR) {
+            // a group whose 1 / s overflows (denormal inputs): element by element
+            uint4 w4;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int e = 16 * g + j;
@@ -107,7 +138,9 @@ __device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t 
             for (int j = 0; j < 16; j += 2) {
                 const int e = 16 * g + j;
                 const float x0 = x[e], x1 = x[e + 1];
-                uint32_t byte = e2m1x2_rn(__fmul_rn(x0, r), __fmul_rn(x1, r));
+                float v0, v1;
+                f2_unpack(f2_mul(f2_pack(x0, x1), f2_pack(r, r)), v0, v1);
+                uint32_t byte = e2m1x2_rn(v0, v1);
                 if (x0 == 0.0f) byte &= 0xF0u;                 // -0 or 0 input -> code 0
                 if (x1 == 0.0f) byte &= 0x0Fu;
                 words[e >> 3] |= byte << (4 * (e & 7));
@@ -152,7 +185,8 @@ __device__ __forceinline__ MxSeg quant_mxfp8_group(const float (&x)[32]) {
         uint32_t word = 0u;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const float2 f = make_float2(__fmul_rn(x[4 * i + 2 * h], inv), __fmul_rn(x[4 * i + 2 * h + 1], inv));
+            float2 f;
+            f2_unpack(f2_mul(f2_pack(x[4 * i + 2 * h], x[4 * i + 2 * h + 1]), f2_pack(inv, inv)), f.x, f.y);
             const __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
             word |= (uint32_t)p << (16 * h);
         }

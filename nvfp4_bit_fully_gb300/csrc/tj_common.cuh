@@ -157,4 +157,73 @@ __host__ __device__ __forceinline__ int64_t sf_word_offset(int64_t row, int64_t 
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
 
+// ---------------------------------------------------------------------------
+// Packed fp32 pairs (one 64-bit register, low word = first element): the sm_100+
+// f32x2 instructions round each half exactly like the scalar instruction.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// a * b + c rounded toward +infinity
+__device__ __forceinline__ uint64_t f2_fma_rp(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rp.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// Stochastic rounding of two scaled values y0, y1 (fp32, |y| may exceed 6 slightly)
+// to signed E2M1 codes, returned in bits 28..31 of the two results (bits 0..27 are
+// not part of the code).  u_lo4096 / u_hi4096 hold each element's 16-bit uniform U
+// at bits 12..27 (U << 12, other bits zero).  Same decision as e2m1_sr on
+// a = min(|y|, 6), with the sign of y:
+//   a >= 1: the float bits A of a carry the grid index in bits 22.. (index
+//           (A >> 22) - 252) and the fraction p * 2^22 in bits 0..21;
+//   a < 1:  the grid {0, .5, 1} is uniform, and 0.5 + a / 2 rounded up to a
+//           multiple of 2^-24 has the bits 0x3F000000 + ceil(a * 2^23), index *
+//           2^22 plus the fraction rounded up (exact for the test below, whose
+//           left side is a multiple of 64);
+// the larger of the two floats is the right one in each range.  Adding
+// 2^22 - 1 - 64 U to that bit pattern carries into the index exactly when the
+// fraction exceeds 64 U, which is the exact test U < p * 2^16.  The sum minus
+// 0x3F000000, times 64, puts the index in bits 28..30 (the index is <= 7, so bit
+// 31 is clear); the sign of y fills bit 31.  y = -0 gives the code of -0.
+__device__ __forceinline__ void e2m1x2_sr_nib(uint64_t y2, uint32_t u_lo4096, uint32_t u_hi4096, uint32_t &t0,
+                                              uint32_t &t1) {
+    float y0, y1;
+    f2_unpack(y2, y0, y1);
+    const float a0 = fminf(fabsf(y0), 6.0f), a1 = fminf(fabsf(y1), 6.0f);
+    float f0, f1;
+    f2_unpack(f2_fma_rp(f2_pack(a0, a1), f2_pack(0.5f, 0.5f), f2_pack(0.5f, 0.5f)), f0, f1);
+    const uint32_t s0 = __float_as_uint(fmaxf(f0, a0)), s1 = __float_as_uint(fmaxf(f1, a1));
+    // (2^22 - 1 - 64 U) * 64 - 0x3F000000 * 64 (mod 2^32) = 0x4FFFFFC0 - 4096 U, and
+    // 4096 U only has bits that 0x4FFFFFC0 has, so the subtraction is an xor
+    t0 = (s0 * 64u + (u_lo4096 ^ 0x4FFFFFC0u)) | (__float_as_uint(y0) & 0x80000000u);
+    t1 = (s1 * 64u + (u_hi4096 ^ 0x4FFFFFC0u)) | (__float_as_uint(y1) & 0x80000000u);
+}
+
 }  // namespace tj

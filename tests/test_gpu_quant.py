@@ -162,6 +162,10 @@ def test_edge_cases(tj):
     x[3, :16] = 1e-38
     x[4, :] = torch.tensor([0.0, 0.5, 1, 1.5, 2, 3, 4, 6] * 32) * 2.0 ** -3
     x[5, ::2] = -0.25
+    # signed zeros and products that underflow next to a huge group maximum: a negative
+    # element whose scaled value rounds to -0 keeps its sign bit, a -0 input gets code 0
+    x[6, :8] = torch.tensor([3.0e38, -1.4e-45, -0.0, 0.0, 1.0e-45, -3.0e-39, -1.0, 2.0e-38])
+    x[7, 16:32] = -0.0
     for mode in (0, 1):
         q = tj.quantize_nvfp4(x.cuda(), mode=mode, seed=5, tag=9)
         torch.cuda.synchronize()
