@@ -255,80 +255,131 @@ __global__ void __launch_bounds__(256) k_quant_cols(Src src, OutNv onv, OutMx om
 // ---------------------------------------------------------------------------
 // OutControl split of a forward operand, row-wise, one read (§2.C): the normal
 // channels (ascending `sel_n`, compacted) -> NVFP4 RTN, the outlier channels
-// (`sel_o`) -> MXFP8.  Each warp stages whole input rows in shared memory with
-// 16-byte loads and its quads gather the selected columns from there; the
-// channel lists are staged once per CTA.  Same results as the two gathering
-// calls (tj_quantize_nvfp4 RTN with sel = normal, tj_quantize_mxfp8 with
-// sel = outliers).
+// (`sel_o`) -> MXFP8.  Same results as the two gathering calls
+// (tj_quantize_nvfp4 RTN with sel = normal, tj_quantize_mxfp8 with sel = outliers).
+//
+// A CTA stages a tile of `tr` whole input rows in shared memory as 32-bit words,
+// one pad word after every 32, and gathers the selected columns from there
+// through two tables of byte offsets built once per CTA.  The tables list the
+// channels in output order, padded by 4 entries after every 32, so a lane reads
+// its 32 offsets with eight 16-byte loads; entries past the end of a list point
+// at a zero word of the row.  The quads of all warps take (row, segment) tasks of
+// the whole tile: first every NVFP4 task, then every MXFP8 task.
 // ---------------------------------------------------------------------------
-constexpr int kSplitWarps = 4;
+constexpr int kSplitThreads = 256;
 
-// Shared-memory position of element e of a list: each 32-element block is rotated by
-// its block number, so the quads' reads (lanes 32 elements apart) hit 32 distinct banks.
-__device__ __forceinline__ int split_rot(int e) { return (e & ~31) | ((e + (e >> 5)) & 31); }
+// words of one staged row: the data words, a pad after every 32, one zero word, 16-byte rows
+__host__ __device__ inline int split_row_words(int K, int esz) {
+    const int nw = esz == 2 ? (K + 1) / 2 : K;
+    return (int)round_up(nw + (nw + 31) / 32 + 1, 4);
+}
+__host__ __device__ inline int split_tab_words(int len) { return len + len / 8; }    // len: a multiple of 128
+__device__ __forceinline__ int split_pad_row(int w) { return w + (w >> 5); }
+__device__ __forceinline__ int split_pad_tab(int i) { return i + 4 * (i >> 5); }
 
 template <typename T>
-__global__ void __launch_bounds__(32 * kSplitWarps) k_quant_split(const T *x, int64_t ld, int64_t rows, int K,
-                                                                 const int32_t *sel_n, int kn,
-                                                                 const int32_t *sel_o, int k, OutNv onv,
-                                                                 OutMx omx) {
+__device__ __forceinline__ uint32_t split_byte_off(int c) {
+    return sizeof(T) == 2 ? 4u * (uint32_t)split_pad_row(c >> 1) + 2u * (uint32_t)(c & 1)
+                          : 4u * (uint32_t)split_pad_row(c);
+}
+
+// input word w (elements 2w, 2w+1 for bf16; element w for fp32) of row `row`, zero past the end
+template <typename T>
+__device__ __forceinline__ uint32_t split_word(const T *x, int64_t ld, int64_t row, int64_t rows, int K, int w) {
+    if (row >= rows) return 0u;
+    const T *p = x + row * ld;
+    if (sizeof(T) == 2) {
+        const uint32_t lo = 2 * w < K ? (uint32_t)__bfloat16_as_ushort(reinterpret_cast<const __nv_bfloat16 *>(p)[2 * w]) : 0u;
+        const uint32_t hi = 2 * w + 1 < K ? (uint32_t)__bfloat16_as_ushort(reinterpret_cast<const __nv_bfloat16 *>(p)[2 * w + 1]) : 0u;
+        return lo | (hi << 16);
+    }
+    return w < K ? __float_as_uint(reinterpret_cast<const float *>(p)[w]) : 0u;
+}
+
+template <typename T>
+__device__ __forceinline__ float split_elem(const uint8_t *p) {
+    if (sizeof(T) == 2) return __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(p) << 16);
+    return *reinterpret_cast<const float *>(p);
+}
+
+// 32 elements of one staged row through 32 table entries (8 x 16-byte reads)
+template <typename T>
+__device__ __forceinline__ void split_gather32(const uint8_t *rowp, const uint32_t *tab, float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 o = *reinterpret_cast<const uint4 *>(tab + 4 * i);
+        v[4 * i] = split_elem<T>(rowp + o.x);
+        v[4 * i + 1] = split_elem<T>(rowp + o.y);
+        v[4 * i + 2] = split_elem<T>(rowp + o.z);
+        v[4 * i + 3] = split_elem<T>(rowp + o.w);
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSplitThreads) k_quant_split(const T *x, int64_t ld, int64_t rows, int K,
+                                                              const int32_t *sel_n, int kn, const int32_t *sel_o,
+                                                              int k, OutNv onv, OutMx omx, int tr) {
     extern __shared__ __align__(16) uint8_t smem_split[];
-    const int kn32 = (kn + 31) & ~31, k32 = (k + 31) & ~31, K32 = (K + 31) & ~31;
-    int32_t *idx_n = reinterpret_cast<int32_t *>(smem_split);             // [kn32], rotated
-    int32_t *idx_o = idx_n + kn32;                                        // [k32], rotated
-    T *rowbuf = reinterpret_cast<T *>(idx_o + k32);
-    for (int i = threadIdx.x; i < kn; i += blockDim.x) idx_n[split_rot(i)] = sel_n[i];
-    for (int i = threadIdx.x; i < k; i += blockDim.x) idx_o[split_rot(i)] = sel_o[i];
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3, qd = lane >> 2;
-    T *rb = rowbuf + (size_t)warp * K32;                                  // the staged row, rotated
     const int nseg_n = (int)(onv.cols_p / 128), nseg_o = k > 0 ? (int)(omx.cols_p / 128) : 0;
+    const int rw = split_row_words(K, (int)sizeof(T));
+    uint32_t *tab_n = reinterpret_cast<uint32_t *>(smem_split);
+    uint32_t *tab_o = tab_n + split_tab_words(128 * nseg_n);
+    uint32_t *tile = tab_o + split_tab_words(128 * nseg_o);
+    const uint32_t zero_off = 4u * (uint32_t)(rw - 1);
+    for (int i = threadIdx.x; i < 128 * nseg_n; i += blockDim.x)
+        tab_n[split_pad_tab(i)] = i < kn ? split_byte_off<T>(sel_n[i]) : zero_off;
+    for (int i = threadIdx.x; i < 128 * nseg_o; i += blockDim.x)
+        tab_o[split_pad_tab(i)] = i < k ? split_byte_off<T>(sel_o[i]) : zero_off;
+    for (int r = threadIdx.x; r < tr; r += blockDim.x) tile[r * rw + rw - 1] = 0u;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3, qd = lane >> 2;
+    const int nwarp = blockDim.x >> 5;
     const int64_t rows_p = onv.rows_p;
+    const int64_t ntile = (rows_p + tr - 1) / tr;
     const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0) && ((ld * (int64_t)sizeof(T)) % 16 == 0);
-    constexpr int kv = 16 / (int)sizeof(T);                               // elements per 16-byte word
-    for (int64_t row = (int64_t)blockIdx.x * kSplitWarps + warp; row < rows_p;
-         row += (int64_t)gridDim.x * kSplitWarps) {
-        const bool real = row < rows;
-        if (real) {
-            const T *src = x + row * ld;
-            if (vec) {
-                for (int c = lane * kv; c + kv <= K; c += 32 * kv) {
-                    const uint4 w = __ldg(reinterpret_cast<const uint4 *>(src + c));
-                    const T *e = reinterpret_cast<const T *>(&w);
-#pragma unroll
-                    for (int i = 0; i < kv; ++i) rb[split_rot(c + i)] = e[i];
-                }
-                for (int c = (K / kv) * kv + lane; c < K; c += 32) rb[split_rot(c)] = src[c];
-            } else {
-                for (int c = lane; c < K; c += 32) rb[split_rot(c)] = src[c];
-            }
+    constexpr int kv = 16 / (int)sizeof(T);              // elements per 16-byte chunk
+    const int nch = vec ? K / kv : 0;                    // full chunks per row, loaded as vectors
+    const int nw = sizeof(T) == 2 ? (K + 1) / 2 : K;     // data words per row
+    const int wtail = 4 * nch, ntail = nw - wtail;       // words loaded one at a time
+    for (int64_t tl = blockIdx.x; tl < ntile; tl += gridDim.x) {
+        const int64_t r0 = tl * tr;
+        __syncthreads();                                 // the previous tile's gathers are done
+        for (int i = threadIdx.x; i < tr * nch; i += blockDim.x) {
+            const int r = i / nch, ch = i - r * nch;
+            const int64_t row = r0 + r;
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);
+            if (row < rows) w = __ldg(reinterpret_cast<const uint4 *>(x + row * ld) + ch);
+            uint32_t *d = tile + r * rw + split_pad_row(4 * ch);      // 4 words inside one 32-word run
+            d[0] = w.x;
+            d[1] = w.y;
+            d[2] = w.z;
+            d[3] = w.w;
         }
-        __syncwarp();
-        // normal channels: NVFP4, one quad per 128-segment
-        for (int kb0 = 0; kb0 < nseg_n; kb0 += 8) {
-            const int kb = kb0 + qd;
+        for (int i = threadIdx.x; i < tr * ntail; i += blockDim.x) {
+            const int r = i / ntail, w = wtail + (i - r * ntail);
+            tile[r * rw + split_pad_row(w)] = split_word(x, ld, r0 + r, rows, K, w);
+        }
+        __syncthreads();
+        const int nt_n = tr * nseg_n;
+        for (int b = warp * 8; b < nt_n; b += nwarp * 8) {             // warp-uniform
+            const int task = b + qd;
+            const bool ok = task < nt_n;
+            const int r = ok ? task / nseg_n : 0, kb = ok ? task - r * nseg_n : 0;
             float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int c = kb * 128 + 32 * t + j;
-                v[j] = (real && kb < nseg_n && c < kn) ? SrcDense<T>::to_f(rb[split_rot(idx_n[split_rot(c)])]) : 0.0f;
-            }
+            split_gather32<T>(reinterpret_cast<const uint8_t *>(tile + r * rw), tab_n + split_pad_tab(kb * 128 + 32 * t), v);
             const NvSeg sg = quant_nvfp4_seg<false>(v, 0, PhiloxKeys{}, 0u);
-            store_nv_seg(onv, row, kb, t, sg, kb < nseg_n);
+            store_nv_seg(onv, r0 + r, kb, t, sg, ok && r0 + r < rows_p);
         }
-        // outlier channels: MXFP8, one quad per 128-segment
-        for (int kb0 = 0; kb0 < nseg_o; kb0 += 8) {
-            const int kb = kb0 + qd;
+        const int nt_o = tr * nseg_o;
+        for (int b = warp * 8; b < nt_o; b += nwarp * 8) {
+            const int task = b + qd;
+            const bool ok = task < nt_o;
+            const int r = ok ? task / nseg_o : 0, kb = ok ? task - r * nseg_o : 0;
             float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int c = kb * 128 + 32 * t + j;
-                v[j] = (real && kb < nseg_o && c < k) ? SrcDense<T>::to_f(rb[split_rot(idx_o[split_rot(c)])]) : 0.0f;
-            }
+            split_gather32<T>(reinterpret_cast<const uint8_t *>(tile + r * rw), tab_o + split_pad_tab(kb * 128 + 32 * t), v);
             const MxSeg m = quant_mxfp8_group(v);
-            store_mx_seg(omx, row, kb, t, m, kb < nseg_o);
+            store_mx_seg(omx, r0 + r, kb, t, m, ok && r0 + r < omx.rows_p);
         }
-        __syncwarp();
     }
 }
 
@@ -483,22 +534,29 @@ cudaError_t launch_quant_mx_dense(const void *x, int dtype, int64_t rows_x, int6
 cudaError_t launch_quant_split(const void *x, int dtype, int64_t rows, int64_t K, int64_t ld, const int32_t *sel_n,
                                int64_t kn, const int32_t *sel_o, int64_t k, const tj_nvfp4 &out,
                                const tj_mxfp8 &out8, cudaStream_t s) {
-    const size_t esz = dtype == TJ_BF16 ? 2 : 4;
-    const size_t smem = (size_t)(((kn + 31) & ~31) + ((k + 31) & ~31)) * 4 + (size_t)kSplitWarps * ((K + 31) & ~31) * esz;
-    if (smem > 200 * 1024 || K > (1 << 30)) return cudaErrorNotSupported;
+    if (K > (1 << 24)) return cudaErrorNotSupported;
+    const int esz = dtype == TJ_BF16 ? 2 : 4;
     const OutNv o = out_nv(out);
     const OutMx m = k > 0 ? out_mx(out8) : OutMx{};
-    int64_t grid = (round_up(rows, 128) + kSplitWarps - 1) / kSplitWarps;
-    if (grid > 152 * 16) grid = 152 * 16;
+    const int64_t tabs = 4 * (int64_t)(split_tab_words((int)o.cols_p) + (k > 0 ? split_tab_words((int)m.cols_p) : 0));
+    const int64_t row_bytes = 4 * (int64_t)split_row_words((int)K, esz);
+    // a tile of about 48 KB of rows, so that three or four CTAs share an SM
+    int64_t tr = (48 * 1024) / row_bytes;
+    tr = tr < 1 ? 1 : (tr > 64 ? 64 : tr);
+    const size_t smem = (size_t)(tabs + tr * row_bytes);
+    if (smem > 200 * 1024) return cudaErrorNotSupported;
+    const int64_t ntile = (o.rows_p + tr - 1) / tr;
+    const int per_sm = smem <= 56 * 1024 ? 4 : (smem <= 75 * 1024 ? 3 : (smem <= 113 * 1024 ? 2 : 1));
+    const int64_t grid = ntile < 152 * per_sm ? ntile : 152 * per_sm;
     if (dtype == TJ_BF16) {
         cudaFuncSetAttribute(k_quant_split<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k_quant_split<__nv_bfloat16><<<(unsigned)grid, 32 * kSplitWarps, smem, s>>>(
-            static_cast<const __nv_bfloat16 *>(x), ld, rows, (int)K, sel_n, (int)kn, sel_o, (int)k, o, m);
+        k_quant_split<__nv_bfloat16><<<(unsigned)grid, kSplitThreads, smem, s>>>(
+            static_cast<const __nv_bfloat16 *>(x), ld, rows, (int)K, sel_n, (int)kn, sel_o, (int)k, o, m, (int)tr);
     } else {
         cudaFuncSetAttribute(k_quant_split<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k_quant_split<float><<<(unsigned)grid, 32 * kSplitWarps, smem, s>>>(static_cast<const float *>(x), ld, rows,
-                                                                           (int)K, sel_n, (int)kn, sel_o, (int)k,
-                                                                           o, m);
+        k_quant_split<float><<<(unsigned)grid, kSplitThreads, smem, s>>>(static_cast<const float *>(x), ld, rows,
+                                                                        (int)K, sel_n, (int)kn, sel_o, (int)k, o,
+                                                                        m, (int)tr);
     }
     return cudaGetLastError();
 }

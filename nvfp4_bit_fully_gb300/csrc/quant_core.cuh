@@ -133,14 +133,23 @@ __device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t 
                 if (xv == 0.0f) code = 0u;
                 words[e >> 3] |= code << (4 * (e & 7));
             }
+        } else if (r <= 3.4028235e38f) {
+            // RTN by the hardware conversion on y = x * r + 0: as above, x = -0 gives +0
+            // and code 0, a negative x whose product rounds to zero keeps its sign
+            const uint64_t r2 = f2_pack(r, r), z2 = f2_pack(0.0f, 0.0f);
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                const int e = 16 * g + j;
+                float v0, v1;
+                f2_unpack(f2_fma(f2_pack(x[e], x[e + 1]), r2, z2), v0, v1);
+                words[e >> 3] |= e2m1x2_rn(v0, v1) << (4 * (e & 7));
+            }
         } else {
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
                 const int e = 16 * g + j;
                 const float x0 = x[e], x1 = x[e + 1];
-                float v0, v1;
-                f2_unpack(f2_mul(f2_pack(x0, x1), f2_pack(r, r)), v0, v1);
-                uint32_t byte = e2m1x2_rn(v0, v1);
+                uint32_t byte = e2m1x2_rn(__fmul_rn(x0, r), __fmul_rn(x1, r));
                 if (x0 == 0.0f) byte &= 0xF0u;                 // -0 or 0 input -> code 0
                 if (x1 == 0.0f) byte &= 0x0Fu;
                 words[e >> 3] |= byte << (4 * (e & 7));

@@ -120,7 +120,8 @@ def test_quantize_dual_bit_exact(tj, rows, cols, dtype, along, mode, rht):
 
 
 @pytest.mark.parametrize("rows,cols,dtype,n_out", [(256, 520, torch.bfloat16, 52), (200, 300, torch.float32, 30),
-                                                    (130, 1024, torch.bfloat16, 103), (64, 136, torch.bfloat16, 1)])
+                                                    (130, 1024, torch.bfloat16, 103), (64, 136, torch.bfloat16, 1),
+                                                    (96, 517, torch.bfloat16, 40), (40, 4100, torch.bfloat16, 410)])
 def test_quantize_split_bit_exact(tj, rows, cols, dtype, n_out):
     """The OutControl split from one read equals the oracle's NVFP4 / MXFP8 of the two channel sets."""
     x = _input(rows, cols, dtype, 13 * rows + cols)
@@ -135,6 +136,23 @@ def test_quantize_split_bit_exact(tj, rows, cols, dtype, n_out):
     assert_mxfp8_equal(q8, Q.quantize_mxfp8(np.ascontiguousarray(xf[:, outl])), "split mxfp8")
     c, s, o = nvfp4_to_logical_full(q)                       # padded rows written as zero
     assert not c[rows:].any() and not s[rows:].any() and not o[rows:].any()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_quantize_split_unaligned_rows(tj, dtype):
+    """Rows that start off a 16-byte boundary (a column slice of a wider tensor) take the
+    element-wise staging path; same results."""
+    rows, cols, n_out = 70, 333, 33
+    big = _input(rows, cols + 3, dtype, 5)
+    x = big.cuda()[:, 1:cols + 1]
+    outl = np.sort(np.random.default_rng(7).choice(cols, n_out, replace=False))
+    normal = OL.normal_channels(cols, outl)
+    q, q8 = tj.quantize_split(x, torch.from_numpy(normal.astype(np.int32)).cuda(),
+                              torch.from_numpy(outl.astype(np.int32)).cuda())
+    torch.cuda.synchronize()
+    xf = big[:, 1:cols + 1].float().numpy()
+    assert_nvfp4_equal(q, Q.quantize_nvfp4(np.ascontiguousarray(xf[:, normal]), 0), "split nvfp4")
+    assert_mxfp8_equal(q8, Q.quantize_mxfp8(np.ascontiguousarray(xf[:, outl])), "split mxfp8")
 
 
 def test_rht_standalone_bit_exact(tj):
