@@ -24,8 +24,8 @@
 //               the promotion;
 //   warps 4-11  promotion + epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (its
 //               rows) and columns 64*((w-4)/4) .. +63, accumulates in registers with
-//               packed f32x2 multiplies and FMAs, and writes its row segment with
-//               16-byte stores.
+//               packed f32x2 multiplies and FMAs, and writes its slice (a TMA store
+//               or row-at-a-time stores).  (Sixteen warps of 32 columns measured slower.)
 // A thread can observe only one barrier handoff every few hundred cycles, so the
 // design keeps handoffs few: the partial slots are released through hardware named
 // barriers, the scale factors of a block share its partial slot's lifetime, and the
@@ -72,11 +72,14 @@ constexpr int kSmemSfb = kSmemSfa + kStages * kSfStageBytes;
 constexpr int kScaleSlots = 8;                 // FP32 outer-scale ring: one FP4 block per slot, [A 128 | B 128]
 constexpr int kSmemScale = kSmemSfb + kStages * kSfStageBytes;
 constexpr int kSmemBar = kSmemScale + kScaleSlots * 1024;
-// Epilogue staging, per promotion warp: a 4 KB 1024-aligned box for TMA stores (stride 4096)
-// or 32 rows x 33 words for the row-at-a-time writes (stride 4224).  A launch uses only one
-// of the two layouts (TMA stores only in single-product launches).
+// Epilogue staging, per promotion warp: a 32-row box of kColsW bf16 for TMA stores
+// (stride kEpiTma, 1024-aligned) or 32 rows of kColsW / 2 words plus a pad word for the
+// row-at-a-time writes (stride kEpiRow).  A launch uses only one of the two layouts (TMA
+// stores only in single-product launches).
 constexpr int kSmemEpi = (kSmemBar + 512 + 1023) & ~1023;
-constexpr int kSmemBytes = kSmemEpi + kPromoWarps * 32 * 33 * 4;
+constexpr int kEpiTma = 32 * 2 * kColsW;
+constexpr int kEpiRow = 32 * (kColsW / 2 + 1) * 4;
+constexpr int kSmemBytes = kSmemEpi + kPromoWarps * (kEpiTma > kEpiRow ? kEpiTma : kEpiRow);
 static_assert(kSmemBytes + 1024 <= 227 * 1024, "shared memory budget");
 constexpr int kThreadsGemm = 32 * (kPromo0 + kPromoWarps);
 constexpr int kNamedP = 1;                     // named barriers kNamedP .. +kPSlots-1: partial slot released
@@ -87,7 +90,8 @@ constexpr uint32_t kColP = 0;                                   // partials: 128
 constexpr uint32_t kColSf = 128 * kPSlots;                      // FP4 scale factors: 16 columns per partial slot
 constexpr uint32_t kColSf8 = kColSf + 16 * kPSlots;             // FP8 scale factors: 8 columns per operand slot
 static_assert(kColSf8 + 8 * kStages <= kTmemCols, "tensor memory budget");
-static_assert(kColsW == 64, "epilogue staging: 32 rows x 128 bytes (bf16) or 2 x 32 words (fp32) per warp");
+static_assert(kColsW == 32 || kColsW == 64, "epilogue: 64- or 128-byte bf16 rows per warp slice");
+static_assert(kEpiTma % 1024 == 0, "TMA staging boxes stay 1024-aligned");
 static_assert(kNamedP + kPSlots <= 16, "named barriers");
 
 // One product D = alpha * A B^T of the launch.  A launch computes one or two of them:
@@ -500,13 +504,15 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             const int64_t rbase = m0 + 32 * q;
             const int64_t nb = n0 + kColsW * cq;
             if (g.tma_store) {
-                uint32_t *stg = reinterpret_cast<uint32_t *>(smem + kSmemEpi + pw * 4096);
+                uint32_t *stg = reinterpret_cast<uint32_t *>(smem + kSmemEpi + pw * kEpiTma);
                 if (lane == 0) ptx::bulk_wait_read_all();     // this warp's previous TMA store has read it
                 __syncwarp();
-                // bf16 without scatter: each lane's 128-byte row segment goes to the staging buffer
-                // in the 128-byte swizzle of the output tensor map, and one TMA store writes the
-                // slice (clipping rows >= M and columns >= N) while the warp moves on
-                uint8_t *rowp = reinterpret_cast<uint8_t *>(stg) + lane * 128;
+                // bf16 without scatter: each lane's row segment (2 kColsW bytes) goes to the staging
+                // buffer in the swizzle of the output tensor map (128-byte rows: 16-byte chunk c of
+                // row r at c ^ (r & 7); 64-byte rows: c ^ ((r >> 1) & 3)), and one TMA store writes
+                // the slice (clipping rows >= M and columns >= N) while the warp moves on
+                uint8_t *rowp = reinterpret_cast<uint8_t *>(stg) + lane * (2 * kColsW);
+                const int sw = kColsW == 64 ? (lane & 7) : ((lane >> 1) & 3);
 #pragma unroll
                 for (int i = 0; i < kColsW / 8; ++i) {
                     uint32_t w4[4];
@@ -515,7 +521,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                         __nv_bfloat162 b2 = __floats2bfloat162_rn(lo2(acc[4 * i + k]), hi2(acc[4 * i + k]));
                         w4[k] = *reinterpret_cast<uint32_t *>(&b2);
                     }
-                    *reinterpret_cast<uint4 *>(rowp + ((i ^ (lane & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    *reinterpret_cast<uint4 *>(rowp + ((i ^ sw) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
@@ -526,24 +532,28 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                 continue;
             }
             // fp32 outputs, scattered columns (col_map), ragged edges or unaligned row pitches: the
-            // warp stages its 32 x kColsW slice in shared memory (rows of 33 words, so row writes
-            // and column reads are both free of bank conflicts) and writes it row by row, a lane
-            // per column, so each store instruction covers one contiguous row segment
-            uint32_t *stg = reinterpret_cast<uint32_t *>(smem + kSmemEpi) + pw * (32 * 33);
+            // warp stages its slice in shared memory, kColsW / 2 words per row plus a pad word (so
+            // row writes and column reads are both free of bank conflicts), and writes it a few
+            // rows per store instruction, a lane per word, so each instruction covers contiguous
+            // row segments.  bf16: one pass of kColsW / 2 column pairs; fp32: two passes of
+            // kColsW / 2 columns.
+            constexpr int kW = kColsW / 2, kRp = 32 / kW;      // words per staged row, rows per store
+            uint32_t *stg = reinterpret_cast<uint32_t *>(smem + kSmemEpi + pw * kEpiRow);
+            const int wl = lane % kW, rsub = lane / kW;
             if (g.out_bf16) {
 #pragma unroll
-                for (int j = 0; j < kColsW / 2; ++j) {
+                for (int j = 0; j < kW; ++j) {
                     __nv_bfloat162 b2 = __floats2bfloat162_rn(lo2(acc[j]), hi2(acc[j]));
-                    stg[lane * 33 + j] = *reinterpret_cast<uint32_t *>(&b2);
+                    stg[lane * (kW + 1) + j] = *reinterpret_cast<uint32_t *>(&b2);
                 }
                 __syncwarp();
-                const int64_t na = nb + 2 * lane, nz = na + 1;   // this lane's column pair
+                const int64_t na = nb + 2 * wl, nz = na + 1;     // this lane's column pair
                 const bool va = na < g.N, vz = nz < g.N;
                 const int64_t ca = va ? (g.col_map ? (int64_t)g.col_map[na] : na) : 0;
                 const int64_t cz = vz ? (g.col_map ? (int64_t)g.col_map[nz] : nz) : 0;
                 const bool pair = va && vz && cz == ca + 1 && ((ca | g.ldd) & 1) == 0;
-                for (int r = 0; r < 32 && rbase + r < g.M; ++r) {
-                    const uint32_t w = stg[r * 33 + lane];
+                for (int r = rsub; r < 32 && rbase + r < g.M; r += kRp) {
+                    const uint32_t w = stg[r * (kW + 1) + wl];
                     __nv_bfloat16 *drow = static_cast<__nv_bfloat16 *>(g.d) + (rbase + r) * g.ldd;
                     if (pair) {
                         *reinterpret_cast<uint32_t *>(drow + ca) = w;
@@ -555,18 +565,18 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                 __syncwarp();
             } else {
 #pragma unroll
-                for (int h = 0; h < kColsW / 32; ++h) {
+                for (int h = 0; h < 2; ++h) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int e = 32 * h + j;
-                        stg[lane * 33 + j] = __float_as_uint((e & 1) ? hi2(acc[e >> 1]) : lo2(acc[e >> 1]));
+                    for (int j = 0; j < kW; ++j) {
+                        const int e = kW * h + j;
+                        stg[lane * (kW + 1) + j] = __float_as_uint((e & 1) ? hi2(acc[e >> 1]) : lo2(acc[e >> 1]));
                     }
                     __syncwarp();
-                    const int64_t n = nb + 32 * h + lane;
+                    const int64_t n = nb + kW * h + wl;
                     const bool v = n < g.N;
                     const int64_t c = v ? (g.col_map ? (int64_t)g.col_map[n] : n) : 0;
-                    for (int r = 0; r < 32 && rbase + r < g.M; ++r)
-                        if (v) static_cast<float *>(g.d)[(rbase + r) * g.ldd + c] = __uint_as_float(stg[r * 33 + lane]);
+                    for (int r = rsub; r < 32 && rbase + r < g.M; r += kRp)
+                        if (v) static_cast<float *>(g.d)[(rbase + r) * g.ldd + c] = __uint_as_float(stg[r * (kW + 1) + wl]);
                     __syncwarp();
                 }
             }
@@ -620,17 +630,17 @@ bool make_tile_map(CUtensorMap *m, const void *base, int64_t rows_p, int64_t row
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// bf16 output [M][ldd] -> boxes of 32 rows x 64 columns (128 bytes), 128-byte swizzle, for
-// the epilogue's TMA stores.
+// bf16 output [M][ldd] -> boxes of 32 rows x kColsW columns (one promotion warp's slice),
+// swizzled to the row width (128 or 64 bytes), for the epilogue's TMA stores.
 bool make_out_map(CUtensorMap *m, void *d, int64_t M, int64_t N, int64_t ldd) {
     EncodeTiledFn enc = get_encode_fn();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)ldd * 2u};
-    const cuuint32_t box[2] = {64u, 32u};
+    const cuuint32_t box[2] = {(cuuint32_t)kColsW, 32u};
     const cuuint32_t estr[2] = {1u, 1u};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               kColsW == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

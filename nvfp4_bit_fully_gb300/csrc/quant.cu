@@ -28,29 +28,33 @@ struct SrcDense {
     __device__ static __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
     __device__ static __forceinline__ float to_f(float v) { return v; }
     // elem(r, c .. c+7), c a multiple of 8: one or two 16-byte loads when the octet is
-    // inside the tensor, unselected and 16-byte aligned
-    __device__ __forceinline__ void load8(int64_t r, int64_t c, float (&v)[8]) const {
+    // inside the tensor, unselected and 16-byte aligned.  flip = ~0u negates all eight
+    // (the RHT diagonal entry of input row r), 0 leaves them.
+    __device__ __forceinline__ void load8(int64_t r, int64_t c, float (&v)[8], uint32_t flip = 0u) const {
         const T *q = p + r * ld + c;
         if (sel == nullptr && r < rows && c + 8 <= cols && (reinterpret_cast<uintptr_t>(q) & 15) == 0) {
-            vec8(q, v);
+            vec8(q, v, flip);
             return;
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = load(r, c + j);
+        for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(__float_as_uint(load(r, c + j)) ^ (flip & 0x80000000u));
     }
-    __device__ static __forceinline__ void vec8(const __nv_bfloat16 *q, float (&v)[8]) {
+    __device__ static __forceinline__ void vec8(const __nv_bfloat16 *q, float (&v)[8], uint32_t flip) {
         const uint4 w = __ldg(reinterpret_cast<const uint4 *>(q));
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        const uint32_t f = flip & 0x80008000u;
+        const uint32_t ws[4] = {w.x ^ f, w.y ^ f, w.z ^ f, w.w ^ f};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             v[2 * k] = __uint_as_float(ws[k] << 16);
             v[2 * k + 1] = __uint_as_float(ws[k] & 0xFFFF0000u);
         }
     }
-    __device__ static __forceinline__ void vec8(const float *q, float (&v)[8]) {
+    __device__ static __forceinline__ void vec8(const float *q, float (&v)[8], uint32_t flip) {
         const float4 a = __ldg(reinterpret_cast<const float4 *>(q)), b = __ldg(reinterpret_cast<const float4 *>(q) + 1);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        const float av[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        const uint32_t f = flip & 0x80000000u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(__float_as_uint(av[k]) ^ f);
     }
 };
 
@@ -75,8 +79,9 @@ struct SrcNv {
     // zero codes and scales): one 4-byte code load, one scale byte, one outer scale.
     // Two codes' magnitudes at a time are looked up as 2G in {0,1,2,3,4,6,8,12} with a
     // byte permute, turned into fp32 exactly, and scaled as (G * s_i) * s_o.
-    __device__ __forceinline__ void load8(int64_t r, int64_t c, float (&v)[8]) const {
-        const uint32_t w = *reinterpret_cast<const uint32_t *>(codes + r * (cols_p / 2) + (c >> 1));
+    __device__ __forceinline__ void load8(int64_t r, int64_t c, float (&v)[8], uint32_t flip = 0u) const {
+        // flipping the eight code sign bits negates the eight values (zeros included)
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(codes + r * (cols_p / 2) + (c >> 1)) ^ (flip & 0x88888888u);
         const int64_t g = c >> 4;
         const uint32_t sb = sf[sf_word_offset(r, g >> 2, cols_p / 64) + (g & 3)];
         const float half_si = __fmul_rn(e4m3_to_float(sb), 0.5f);        // exact
@@ -108,7 +113,8 @@ struct SrcMx {
         return __fmul_rn(v, s);
     }
     // elem(r, c .. c+7), c a multiple of 8, inside the padded tensor: one 8-byte load
-    __device__ __forceinline__ void load8(int64_t r, int64_t c, float (&v)[8]) const {
+    // (never used with the RHT: flip must be 0)
+    __device__ __forceinline__ void load8(int64_t r, int64_t c, float (&v)[8], uint32_t flip = 0u) const {
         const uint2 w = *reinterpret_cast<const uint2 *>(codes + r * cols_p + c);
         const int64_t g = c >> 5;
         const int e = (int)sf[sf_word_offset(r, g >> 2, cols_p / 128) + (g & 3)] - 127;
@@ -157,7 +163,7 @@ __device__ __forceinline__ void load_row32(const SrcDense<__nv_bfloat16> &src, i
 // its optional RHT), into outputs of the same shape.
 // ---------------------------------------------------------------------------
 template <typename Src, int FMT, bool SR, bool RHT>
-__global__ void __launch_bounds__(256) k_quant_rows(Src src, OutNv onv, OutMx omx, int64_t nseg, const PhiloxKeys pk,
+__global__ void __launch_bounds__(256, 3) k_quant_rows(Src src, OutNv onv, OutMx omx, int64_t nseg, const PhiloxKeys pk,
                                                     uint32_t tag, uint32_t rht_tag) {
     const int lane = threadIdx.x & 31;
     const int t = lane & 3;
@@ -206,21 +212,26 @@ __global__ void __launch_bounds__(256) k_quant_rows(Src src, OutNv onv, OutMx om
 // element (r, c) sits at r*64 + (c ^ (((r >> 5) & 3) << 3)).
 // ---------------------------------------------------------------------------
 template <typename Src, int FMT, bool SR, bool RHT>
-__global__ void __launch_bounds__(256) k_quant_cols(Src src, OutNv onv, OutMx omx, const PhiloxKeys pk, uint32_t tag,
+__global__ void __launch_bounds__(256, 4) k_quant_cols(Src src, OutNv onv, OutMx omx, const PhiloxKeys pk, uint32_t tag,
                                                     uint32_t rht_tag) {
     __shared__ __align__(16) float tile[128 * 64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t c0 = (int64_t)blockIdx.x * 64;      // first output row of the tile
     const int64_t kb = blockIdx.y;                    // 128-block along the input rows
     const int64_t r0 = kb * 128;
+    // with the RHT, input row rr (element rr of every output segment) is negated while
+    // loading when its diagonal entry is -1
+    const uint4 sbits = RHT && FMT != 1 ? rht_sign_bits(pk, rht_tag) : make_uint4(0u, 0u, 0u, 0u);
     // fill: 128 rows x 8 column octets, one octet (8 consecutive columns of a row) per
     // thread and pass, stored as two 16-byte words (the swizzle keeps an octet contiguous)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int idx = i * 256 + (int)threadIdx.x;
-        const int rr = idx >> 3, o = idx & 7;
+        const int rr = idx >> 3, o = idx & 7;                   // rr = 32 i + threadIdx.x / 8
+        const uint32_t sw = i == 0 ? sbits.x : (i == 1 ? sbits.y : (i == 2 ? sbits.z : sbits.w));
+        const uint32_t flip = 0u - ((sw >> (threadIdx.x >> 3)) & 1u);
         float v[8];
-        src.load8(r0 + rr, c0 + 8 * o, v);
+        src.load8(r0 + rr, c0 + 8 * o, v, flip);
         float4 *dst = reinterpret_cast<float4 *>(&tile[rr * 64 + ((8 * o) ^ (((rr >> 5) & 3) << 3))]);
         dst[0] = make_float4(v[0], v[1], v[2], v[3]);
         dst[1] = make_float4(v[4], v[5], v[6], v[7]);
@@ -236,14 +247,13 @@ __global__ void __launch_bounds__(256) k_quant_cols(Src src, OutNv onv, OutMx om
     const int64_t cols_p = FMT != 1 ? onv.cols_p : omx.cols_p;
     const bool valid = row < rows_p;
     if (FMT != 1) {
+        const uint32_t sign_word = t == 0 ? sbits.x : (t == 1 ? sbits.y : (t == 2 ? sbits.z : sbits.w));
         if (FMT == 2) {
-            const MxSeg m = quant_mxfp8_group(x);
+            MxSeg m = quant_mxfp8_group(x);
+            if (RHT) mx_unflip(m, sign_word);
             store_mx_seg(omx, row, kb, t, m, valid);
         }
-        if (RHT) {
-            const uint4 sb = rht_sign_bits(pk, rht_tag);
-            rht128_quad(x, t == 0 ? sb.x : (t == 1 ? sb.y : (t == 2 ? sb.z : sb.w)), t);
-        }
+        if (RHT) rht128_quad<false>(x, sign_word, t);
         const NvSeg s = quant_nvfp4_seg<SR>(x, (uint64_t)(row * cols_p + r0 + 32 * t), pk, tag);
         store_nv_seg(onv, row, kb, t, s, valid);
     } else {
@@ -344,16 +354,31 @@ __global__ void __launch_bounds__(kSplitThreads) k_quant_split(const T *x, int64
     for (int64_t tl = blockIdx.x; tl < ntile; tl += gridDim.x) {
         const int64_t r0 = tl * tr;
         __syncthreads();                                 // the previous tile's gathers are done
-        for (int i = threadIdx.x; i < tr * nch; i += blockDim.x) {
-            const int r = i / nch, ch = i - r * nch;
-            const int64_t row = r0 + r;
-            uint4 w = make_uint4(0u, 0u, 0u, 0u);
-            if (row < rows) w = __ldg(reinterpret_cast<const uint4 *>(x + row * ld) + ch);
-            uint32_t *d = tile + r * rw + split_pad_row(4 * ch);      // 4 words inside one 32-word run
-            d[0] = w.x;
-            d[1] = w.y;
-            d[2] = w.z;
-            d[3] = w.w;
+        // eight 16-byte loads in flight per thread before their stores
+        constexpr int kU = 8;
+        for (int i0 = threadIdx.x; i0 < tr * nch; i0 += kU * blockDim.x) {
+            uint4 w[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = i0 + u * (int)blockDim.x;
+                w[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < tr * nch) {
+                    const int r = i / nch, ch = i - r * nch;
+                    if (r0 + r < rows) w[u] = __ldg(reinterpret_cast<const uint4 *>(x + (r0 + r) * ld) + ch);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = i0 + u * (int)blockDim.x;
+                if (i < tr * nch) {
+                    const int r = i / nch, ch = i - r * nch;
+                    uint32_t *d = tile + r * rw + split_pad_row(4 * ch);  // 4 words inside one 32-word run
+                    d[0] = w[u].x;
+                    d[1] = w[u].y;
+                    d[2] = w[u].z;
+                    d[3] = w[u].w;
+                }
+            }
         }
         for (int i = threadIdx.x; i < tr * ntail; i += blockDim.x) {
             const int r = i / ntail, w = wtail + (i - r * ntail);

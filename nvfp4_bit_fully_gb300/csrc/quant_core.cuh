@@ -18,10 +18,14 @@ namespace tj {
 // fp32, in the fixed order h = 1, 2, ..., 64 (TetraJet-v2 §2.C RHT).  The
 // cross-lane stages use one FMA with a +-1 factor: s*x + p is exact before its
 // single rounding, so it rounds exactly like x + p or p - x.
+// kFlip = false: the caller has applied the diagonal already (while loading).
+template <bool kFlip = true>
 __device__ __forceinline__ void rht128_quad(float (&x)[32], uint32_t sign_word, int t) {
+    if (kFlip) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-        x[j] = __uint_as_float(__float_as_uint(x[j]) ^ ((sign_word << (31 - j)) & 0x80000000u));
+        for (int j = 0; j < 32; ++j)
+            x[j] = __uint_as_float(__float_as_uint(x[j]) ^ ((sign_word << (31 - j)) & 0x80000000u));
+    }
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
         const float a = x[j], b = x[j + 1];
@@ -53,6 +57,14 @@ __device__ __forceinline__ void rht128_quad(float (&x)[32], uint32_t sign_word, 
     }
 }
 
+// max |x[j0 .. j0+15]| by three-input maxima
+__device__ __forceinline__ float amax16(const float (&x)[32], int j0) {
+    float m = amax3(x[j0], x[j0 + 1], x[j0 + 2]);
+#pragma unroll
+    for (int j = 3; j < 15; j += 2) m = amax3(m, x[j0 + j], x[j0 + j + 1]);
+    return fmaxf(m, fabsf(x[j0 + 15]));
+}
+
 struct NvSeg {
     uint4 codes;    // 32 E2M1 codes, element 2j in the low nibble of byte j
     uint32_t sf2;   // inner scale bytes of this lane's groups (low byte = first group)
@@ -72,10 +84,7 @@ __device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t 
     float a_i[2];
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
-        float m = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(x[16 * g + j]));
-        a_i[g] = m;
+        a_i[g] = amax16(x, 16 * g);
     }
     float a_o = fmaxf(a_i[0], a_i[1]);
     a_o = fmaxf(a_o, __shfl_xor_sync(0xffffffffu, a_o, 1));
@@ -170,9 +179,7 @@ struct MxSeg {
 // 0 for an all-zero group), values x * 2^-E rounded to nearest-even E4M3 with
 // saturation at +-448.
 __device__ __forceinline__ MxSeg quant_mxfp8_group(const float (&x)[32]) {
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(x[j]));
+    const float amax = fmaxf(amax16(x, 0), amax16(x, 16));
     int E = 0;
     if (amax > 0.0f) {
         uint32_t b = __float_as_uint(amax);
@@ -205,6 +212,22 @@ __device__ __forceinline__ MxSeg quant_mxfp8_group(const float (&x)[32]) {
     out.codes[1] = make_uint4(w[4], w[5], w[6], w[7]);
     out.e8 = (uint32_t)(E + 127);
     return out;
+}
+
+// The MXFP8 codes of a lane's 32 elements computed on sign-flipped inputs, turned
+// into the codes of the unflipped inputs: the E4M3 conversion is symmetric in the
+// sign (zeros included), so each flipped element's code byte has its sign bit
+// toggled.  Bit j of `sign_word` set = element j was negated.
+__device__ __forceinline__ void mx_unflip(MxSeg &m, uint32_t sign_word) {
+    uint32_t w[8] = {m.codes[0].x, m.codes[0].y, m.codes[0].z, m.codes[0].w,
+                     m.codes[1].x, m.codes[1].y, m.codes[1].z, m.codes[1].w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        // bits 4i .. 4i+3 -> bit 7 of bytes 0 .. 3 (the multiply spreads the four bits 7 apart)
+        w[i] ^= (((sign_word >> (4 * i)) & 0xFu) * 0x00204081u & 0x01010101u) << 7;
+    }
+    m.codes[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    m.codes[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 // Output descriptors (device pointers and padded sizes).

@@ -51,8 +51,11 @@ inline PhiloxKeys philox_keys(uint64_t seed) {
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys &pk) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        uint32_t lo0, hi0, lo1, hi1;        // both halves of each 32 x 32 -> 64-bit product at once
+        asm("{\n\t.reg .b64 p;\n\tmul.wide.u32 p, %2, 0xD2511F53;\n\tmov.b64 {%0, %1}, p;\n\t}"
+            : "=r"(lo0), "=r"(hi0) : "r"(c.x));
+        asm("{\n\t.reg .b64 p;\n\tmul.wide.u32 p, %2, 0xCD9E8D57;\n\tmov.b64 {%0, %1}, p;\n\t}"
+            : "=r"(lo1), "=r"(hi1) : "r"(c.z));
         c = make_uint4(hi1 ^ c.y ^ pk.k[2 * r], lo1, hi0 ^ c.w ^ pk.k[2 * r + 1], lo0);
     }
     return c;
@@ -156,6 +159,13 @@ __host__ __device__ __forceinline__ int64_t sf_word_offset(int64_t row, int64_t 
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
+
+// max(|a|, |b|, |c|) (one three-input maximum; NaN inputs are not propagated)
+__device__ __forceinline__ float amax3(float a, float b, float c) {
+    float d;
+    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
 
 // ---------------------------------------------------------------------------
 // Packed fp32 pairs (one 64-bit register, low word = first element): the sm_100+
