@@ -221,8 +221,8 @@ class Linear:
         T("requant_x", lambda: tj.requantize_nvfp4(self.xq, SR, True, seed, tj.TAG_XT, tj.TAG_RHT_DW, out=self.s_x,
                                                    stream=s))
         T("requant_x8", lambda: tj.requantize_mxfp8(self.x8, out=self.q8_x, stream=s))
-        T("gemm_dw", lambda: tj.gemm_pair(self.s_dyt, self.s_x, self.q8_dyt, self.q8_x, alpha=2.0 ** -7, out=self.dW,
-                                          out8=self.dW, col_map=self.ni, col_map8=self.oi, stream=s))
+        T("gemm_dw", lambda: tj.gemm_pair_f32(self.s_dyt, self.s_x, self.q8_dyt, self.q8_x, self.dW, self.ni, self.oi,
+                                              alpha=2.0 ** -7, stream=s))
 
     def run_api(self, tj, seed, stream):
         """The same step through the user-facing calls (tj_linear_fwd / bwd_dx / bwd_dw)."""

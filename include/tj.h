@@ -207,6 +207,22 @@ tj_status tj_gemm_pair(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, void *
                        int64_t ldd, const int32_t *col_map, const tj_mxfp8 *a8, const tj_mxfp8 *b8,
                        void *d8, int out8_dtype, int64_t ldd8, const int32_t *col_map8, void *stream);
 
+/* tj_gemm_pair_f32 - tj_gemm_pair for the case of a weight gradient: both products are fp32
+ * and together fill one matrix out [rows][cols] (row pitch ld floats, 16-byte aligned), the
+ * FP4 product through col_map (a->rows x b->rows) and the FP8 slice through col_map8
+ * (a8->rows x b8->rows), with rows = a->rows = a8->rows and every column of out written by
+ * exactly one product (col_map / col_map8 int32 device arrays, both required).
+ * Because the call owns all of out, it may zero it and split a long K in two: each half of
+ * a tile then adds its fp32 sum into out.  Two additions onto zero commute, so the result
+ * is deterministic.  It equals tj_gemm_pair's up to the rounding of that one extra fp32
+ * addition (the sum of the halves instead of one running sum).  The split is taken when K
+ * has at least 8 stages (2 x 128 FP4 or 128 FP8 elements each) in both products and the
+ * halves fill the GPU in fewer rounds.  Errors as tj_gemm_pair; TJ_ERR_SHAPE if the row
+ * counts differ, cols < 1 or ld < cols. */
+tj_status tj_gemm_pair_f32(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, const int32_t *col_map,
+                           const tj_mxfp8 *a8, const tj_mxfp8 *b8, const int32_t *col_map8, float *out,
+                           int64_t cols, int64_t ld, void *stream);
+
 /* ---------------------------------------------------------------------------
  * tj_linear_fwd - forward of the NVFP4 linear layer (§2: NVFP4 for activations,
  * weights and gradients of every linear layer; §2.A RTN double-block quantization;
@@ -248,7 +264,9 @@ tj_status tj_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, c
  *   dW[:, O]  = Q8(dY^T) Q8(X-hat_O^T)^T
  * xq / x8 are the saved forward context of tj_linear_fwd.  dw fp32 [N, K] (lddw).
  * The workspace then holds S_dY^T (tj_nvfp4 [N, M]), S_X (tj_nvfp4 [K_N, M]) and when
- * k > 0 Q8(dY^T) (tj_mxfp8 [N, M]) and Q8(X-hat_O^T) (tj_mxfp8 [k, M]), laid out as for dX. */
+ * k > 0 Q8(dY^T) (tj_mxfp8 [N, M]) and Q8(X-hat_O^T) (tj_mxfp8 [k, M]), laid out as for dX.
+ * The two products run as one tj_gemm_pair_f32 launch into dw, so a long M (the
+ * contraction, tokens) with few output tiles may be split in two (see there). */
 tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, const tj_nvfp4 *xq,
                            const tj_mxfp8 *x8, const int32_t *normal_idx, const int32_t *outlier_idx,
                            int64_t k, uint64_t seed, float *dw, int64_t lddw, void *workspace,

@@ -255,6 +255,24 @@ tj_status tj_gemm_pair(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, void *
                                         static_cast<cudaStream_t>(stream)));
 }
 
+tj_status tj_gemm_pair_f32(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, const int32_t *col_map,
+                           const tj_mxfp8 *a8, const tj_mxfp8 *b8, const int32_t *col_map8, float *out,
+                           int64_t cols, int64_t ld, void *stream) {
+    if (a == nullptr || b == nullptr || a8 == nullptr || b8 == nullptr || out == nullptr || col_map == nullptr ||
+        col_map8 == nullptr)
+        return TJ_ERR_INVALID_ARG;
+    tj_status st = check_nv(a, a->rows, a->cols);
+    if (st == TJ_OK) st = check_nv(b, b->rows, a->cols);
+    if (st == TJ_OK) st = check_mx(a8, a8->rows, a8->cols);
+    if (st == TJ_OK) st = check_mx(b8, b8->rows, a8->cols);
+    if (st != TJ_OK) return st;
+    if (a8->rows != a->rows || cols < 1 || ld < cols || b->rows + b8->rows > cols) return TJ_ERR_SHAPE;
+    if (!al16(out)) return TJ_ERR_ALIGN;
+    const SplitRegion whole{out, a->rows, cols, ld};
+    return cuda_status(launch_gemm_pair(a, b, alpha, out, TJ_FP32, ld, a->rows, b->rows, col_map, a8, b8, out, TJ_FP32,
+                                        ld, a8->rows, b8->rows, col_map8, static_cast<cudaStream_t>(stream), &whole));
+}
+
 size_t tj_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t k) {
     if (M < 0 || N < 0 || K < 0 || k < 0 || k > K) return 0;
     const int64_t kn = K - k;
@@ -380,13 +398,15 @@ tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, c
         TJ_TRY(launch_quant_nv_dense(dy, TJ_BF16, M, N, lddy, 1, nullptr, TJ_SR, 1, seed, TJ_TAG_DY_COL,
                                      TJ_TAG_RHT_DW, s_dy, s));
     TJ_TRY(launch_realign_nv(*xq, s_x, TJ_SR, 1, seed, TJ_TAG_XT, TJ_TAG_RHT_DW, s));
+    // dW [N][K] is fp32 and covered by the launch, so a long-K launch may split K in two
+    const SplitRegion whole_dw{dw, N, K, lddw};
     if (k > 0) {
         // the FP4 product (normal columns of dW) and the FP8 slice (outlier columns) in one launch
         TJ_TRY(launch_realign_mx(*x8, q8_x, s));
         TJ_TRY(launch_gemm_pair(&s_dy, &s_x, 0.0078125f, dw, TJ_FP32, lddw, N, kn, normal_idx, &q8_dy, &q8_x, dw,
-                                TJ_FP32, lddw, N, k, outlier_idx, s));
+                                TJ_FP32, lddw, N, k, outlier_idx, s, &whole_dw));
     } else {
-        TJ_TRY(launch_gemm(&s_dy, &s_x, nullptr, nullptr, 0.0078125f, dw, TJ_FP32, lddw, N, kn, nullptr, s));
+        TJ_TRY(launch_gemm(&s_dy, &s_x, nullptr, nullptr, 0.0078125f, dw, TJ_FP32, lddw, N, kn, nullptr, s, &whole_dw));
     }
     return TJ_OK;
 }

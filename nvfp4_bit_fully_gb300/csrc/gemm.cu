@@ -109,7 +109,10 @@ struct GemmProblem {
     int64_t ldd;
     const int32_t *col_map;       // output column n goes to column col_map[n] (nullptr: n)
     int tma_store;                // bf16, no col_map, ldd % 8 == 0: tiles leave by TMA stores (map tm_d)
+    int splits;                   // 1, or 2: each tile's K schedule is halved over two tile works whose
+                                  // fp32 sums are added into the (zeroed) output
 };
+__host__ __device__ __forceinline__ int problem_works(const GemmProblem &p) { return p.tiles_m * p.tiles_n * p.splits; }
 
 struct GemmArgs {
     GemmProblem pr[2];
@@ -121,23 +124,38 @@ struct GemmArgs {
     int64_t ntk_a8, ntk_b8;       // cols_p / 128
 };
 
-// The work of one output tile: its product, origin and K schedule (FP4 stages of two
-// 128-K blocks first, then the FP8 stages, which accumulate into one partial).
+// The work of one output tile (or, with a split, of one half of its K): its product,
+// origin and K schedule (FP4 stages of two 128-K blocks first, then the FP8 stages, which
+// accumulate into one partial).  st0 / k80: the first FP4 stage and the first FP8 stage
+// of the tile's K that this work covers.
 struct TileWork {
     int p;
     int64_t m0, n0;
-    int nkb4, nk8, nst4, nstages, nblk;
+    int nkb4, nk8, nst4, nstages, nblk, st0, k80;
 };
 __device__ __forceinline__ TileWork tile_work(const GemmArgs &a, int t) {
-    const int t1 = a.pr[1].tiles_m * a.pr[1].tiles_n;
+    const int t1 = problem_works(a.pr[1]);
     TileWork w;
     w.p = t < t1 ? 1 : 0;
     const int i = w.p ? t : t - t1;
+    const int split = w.p ? a.pr[1].splits : a.pr[0].splits;
     const int tn = w.p ? a.pr[1].tiles_n : a.pr[0].tiles_n;
-    w.m0 = (int64_t)(i / tn) * 128;
-    w.n0 = (int64_t)(i % tn) * 128;
-    w.nkb4 = w.p ? a.pr[1].nkb4 : a.pr[0].nkb4;
-    w.nk8 = w.p ? a.pr[1].nk8 : a.pr[0].nk8;
+    const int nkb4 = w.p ? a.pr[1].nkb4 : a.pr[0].nkb4, nk8 = w.p ? a.pr[1].nk8 : a.pr[0].nk8;
+    const int sp = split == 2 ? (i & 1) : 0, ti = split == 2 ? (i >> 1) : i;
+    w.m0 = (int64_t)(ti / tn) * 128;
+    w.n0 = (int64_t)(ti % tn) * 128;
+    w.st0 = 0;
+    w.k80 = 0;
+    w.nkb4 = nkb4;
+    w.nk8 = nk8;
+    if (split == 2) {
+        const int s4a = ((nkb4 + 1) / 2 + 1) / 2, k8a = (nk8 + 1) / 2;
+        const int kb4a = nkb4 < 2 * s4a ? nkb4 : 2 * s4a;
+        w.st0 = sp ? s4a : 0;
+        w.k80 = sp ? k8a : 0;
+        w.nkb4 = sp ? nkb4 - kb4a : kb4a;
+        w.nk8 = sp ? nk8 - k8a : k8a;
+    }
     w.nst4 = (w.nkb4 + 1) / 2;
     w.nstages = w.nst4 + w.nk8;
     w.nblk = w.nkb4 + (w.nk8 > 0 ? 1 : 0);
@@ -244,7 +262,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars *bars = reinterpret_cast<Bars *>(smem + kSmemBar);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ntiles = args.pr[0].tiles_m * args.pr[0].tiles_n + args.pr[1].tiles_m * args.pr[1].tiles_n;
+    const int ntiles = problem_works(args.pr[0]) + problem_works(args.pr[1]);
     const int cta = (int)blockIdx.x, ncta = (int)gridDim.x;
 
     if (threadIdx.x == 0) {
@@ -287,7 +305,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     uint8_t *sfa = smem + kSmemSfa + slot * kSfStageBytes;
                     uint8_t *sfb = smem + kSmemSfb + slot * kSfStageBytes;
                     const bool fp4 = st < w.nst4;
-                    const int k0 = fp4 ? st : st - w.nst4;            // 128-byte column of the operand rows
+                    const int k0 = fp4 ? w.st0 + st : w.k80 + st - w.nst4;   // 128-byte column of the operand rows
                     const int nkbs = fp4 ? min(2, w.nkb4 - 2 * st) : 0;
                     const uint32_t sfbytes = fp4 ? (uint32_t)nkbs * 1024u : 512u;
                     // the outer-scale slots of the stage's blocks: FP4 block f (counted over this
@@ -308,10 +326,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     ptx::tma_load_2d(sa, fp4 ? &tm_a4 : &tm_a8, k0 * 128, (int32_t)w.m0, &bars->full[slot]);
                     ptx::tma_load_2d(sb, fp4 ? &tm_b4 : &tm_b8, k0 * 128, (int32_t)w.n0, &bars->full[slot]);
                     if (fp4) {
-                        ptx::bulk_load(sfa, args.sfa4 + (rta * args.ntk_a4 + 4 * st) * 512, sfbytes, &bars->full[slot]);
-                        ptx::bulk_load(sfb, args.sfb4 + (rtb * args.ntk_b4 + 4 * st) * 512, sfbytes, &bars->full[slot]);
+                        ptx::bulk_load(sfa, args.sfa4 + (rta * args.ntk_a4 + 4 * k0) * 512, sfbytes, &bars->full[slot]);
+                        ptx::bulk_load(sfb, args.sfb4 + (rtb * args.ntk_b4 + 4 * k0) * 512, sfbytes, &bars->full[slot]);
                         for (int j = 0; j < nkbs; ++j) {
-                            const int64_t kb = 2 * st + j;
+                            const int64_t kb = 2 * k0 + j;
                             uint8_t *so = smem + kSmemScale + ((f0 + j) % kScaleSlots) * 1024;
                             ptx::bulk_load(so, args.outa + kb * args.rpa + w.m0, 512u, &bars->full[slot]);
                             ptx::bulk_load(so + 512, args.outb + kb * args.rpb + w.n0, 512u, &bars->full[slot]);
@@ -575,8 +593,14 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     const int64_t n = nb + kW * h + wl;
                     const bool v = n < g.N;
                     const int64_t c = v ? (g.col_map ? (int64_t)g.col_map[n] : n) : 0;
-                    for (int r = rsub; r < 32 && rbase + r < g.M; r += kRp)
-                        if (v) static_cast<float *>(g.d)[(rbase + r) * g.ldd + c] = __uint_as_float(stg[r * (kW + 1) + wl]);
+                    float *dcol = static_cast<float *>(g.d) + c;
+                    if (g.splits > 1) {                                  // half of a split K: add
+                        for (int r = rsub; r < 32 && rbase + r < g.M; r += kRp)
+                            if (v) atomicAdd(dcol + (rbase + r) * g.ldd, __uint_as_float(stg[r * (kW + 1) + wl]));
+                    } else {
+                        for (int r = rsub; r < 32 && rbase + r < g.M; r += kRp)
+                            if (v) dcol[(rbase + r) * g.ldd] = __uint_as_float(stg[r * (kW + 1) + wl]);
+                    }
                     __syncwarp();
                 }
             }
@@ -660,7 +684,7 @@ cudaError_t launch_persistent(const CUtensorMap (&tm)[5], const GemmArgs &g, cud
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int ntiles = g.pr[0].tiles_m * g.pr[0].tiles_n + g.pr[1].tiles_m * g.pr[1].tiles_n;
+    const int ntiles = problem_works(g.pr[0]) + problem_works(g.pr[1]);
     if (ntiles == 0) return cudaSuccess;
     const int nsm = num_sms_of_current_device();
     k_gemm_nvfp4<<<(unsigned)(ntiles < nsm ? ntiles : nsm), kThreadsGemm, kSmemBytes + 1024, s>>>(tm[0], tm[1], tm[2],
@@ -679,7 +703,28 @@ GemmProblem problem(int64_t M, int64_t N, float alpha, void *d, int out_dtype, i
     p.col_map = col_map;
     p.tiles_m = (int)(round_up(M, 128) / 128);
     p.tiles_n = (int)(round_up(N, 128) / 128);
+    p.splits = 1;
     return p;
+}
+
+// Split K in two when the caller allows it (an fp32 output region), every product of the
+// launch has at least 8 stages of K (so each half keeps 4), and the halves fill the SMs in
+// fewer rounds of half-length works than whole tiles would (e.g. 72 tiles on 152 SMs: one
+// round of halves instead of one of wholes; 216 tiles: three rounds of halves instead of two
+// of wholes).  The output region is zeroed on the stream first.
+cudaError_t maybe_split(GemmArgs &g, const SplitRegion *split, cudaStream_t s) {
+    if (split == nullptr) return cudaSuccess;
+    for (const GemmProblem &p : g.pr)
+        if (p.tiles_m * p.tiles_n > 0 && (p.out_bf16 || p.tma_store || (p.nkb4 + 1) / 2 + p.nk8 < 8)) return cudaSuccess;
+    const int nsm = num_sms_of_current_device();
+    const int t = g.pr[0].tiles_m * g.pr[0].tiles_n + g.pr[1].tiles_m * g.pr[1].tiles_n;
+    const int whole = (t + nsm - 1) / nsm, halves = (2 * t + nsm - 1) / nsm;
+    if (t == 0 || halves >= 2 * whole) return cudaSuccess;
+    const cudaError_t e = cudaMemset2DAsync(split->base, (size_t)split->ld * sizeof(float), 0,
+                                            (size_t)split->cols * sizeof(float), (size_t)split->rows, s);
+    if (e != cudaSuccess) return e;
+    g.pr[0].splits = g.pr[1].splits = 2;
+    return cudaSuccess;
 }
 
 // FP4 operands -> tensor maps 0/1 and the scale pointers; returns the 128-K block count.
@@ -721,7 +766,7 @@ void set_tma_store(GemmProblem &p, CUtensorMap &tm) {
 
 cudaError_t launch_gemm(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8, const tj_mxfp8 *b8, float alpha,
                         void *d, int out_dtype, int64_t ldd, int64_t M, int64_t N, const int32_t *col_map,
-                        cudaStream_t s) {
+                        cudaStream_t s, const SplitRegion *split) {
     GemmArgs g{};
     g.pr[0] = problem(M, N, alpha, d, out_dtype, ldd, col_map);
     if (g.pr[0].tiles_m == 0 || g.pr[0].tiles_n == 0) return cudaSuccess;
@@ -731,13 +776,15 @@ cudaError_t launch_gemm(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8
     if (a8 != nullptr && b8 != nullptr && a8->cols > 0 && !set_fp8(*a8, *b8, g, tm, g.pr[0].nk8))
         return cudaErrorInvalidValue;
     set_tma_store(g.pr[0], tm[4]);
+    const cudaError_t e = maybe_split(g, split, s);
+    if (e != cudaSuccess) return e;
     return launch_persistent(tm, g, s);
 }
 
 cudaError_t launch_gemm_pair(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, void *d, int out_dtype, int64_t ldd,
                              int64_t M, int64_t N, const int32_t *col_map, const tj_mxfp8 *a8, const tj_mxfp8 *b8,
                              void *d8, int out8_dtype, int64_t ldd8, int64_t M8, int64_t N8, const int32_t *col_map8,
-                             cudaStream_t s) {
+                             cudaStream_t s, const SplitRegion *split) {
     GemmArgs g{};
     g.pr[0] = problem(M, N, alpha, d, out_dtype, ldd, col_map);
     g.pr[1] = problem(M8, N8, 1.0f, d8, out8_dtype, ldd8, col_map8);
@@ -746,6 +793,8 @@ cudaError_t launch_gemm_pair(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, 
     if (!set_fp4(*a, *b, g, tm, g.pr[0].nkb4) || !set_fp8(*a8, *b8, g, tm, g.pr[1].nk8)) return cudaErrorInvalidValue;
     if (g.pr[0].tiles_m * g.pr[0].tiles_n == 0) g.pr[0].tiles_m = g.pr[0].tiles_n = 0;
     if (g.pr[1].tiles_m * g.pr[1].tiles_n == 0 || g.pr[1].nk8 == 0) g.pr[1].tiles_m = g.pr[1].tiles_n = 0;
+    const cudaError_t e = maybe_split(g, split, s);
+    if (e != cudaSuccess) return e;
     return launch_persistent(tm, g, s);
 }
 

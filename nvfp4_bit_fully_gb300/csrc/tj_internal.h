@@ -26,15 +26,23 @@ cudaError_t launch_rht(const float *x, float *y, int64_t rows, int64_t cols, uin
                        cudaStream_t s);
 cudaError_t launch_dequant_nv(const tj_nvfp4 &q, float *y, int64_t ldy, cudaStream_t s);
 
+// An fp32 output region [rows][cols] (row pitch ld floats) that holds every output of a GEMM
+// launch.  Passing it allows the launch to split K in two when that shortens its schedule:
+// the region is then zeroed on the stream and both halves add their sums into it (two fp32
+// additions onto zero: the result does not depend on their order).
+struct SplitRegion {
+    float *base;
+    int64_t rows, cols, ld;
+};
 // GEMM: D = alpha * A_fp4 B_fp4^T (+ A8 B8^T); a/b may be null for an FP8-only GEMM.
 cudaError_t launch_gemm(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8, const tj_mxfp8 *b8,
                         float alpha, void *d, int out_dtype, int64_t ldd, int64_t M, int64_t N,
-                        const int32_t *col_map, cudaStream_t s);
+                        const int32_t *col_map, cudaStream_t s, const SplitRegion *split = nullptr);
 // An FP4 product and an FP8-only product (each with its own output) in one launch.
 cudaError_t launch_gemm_pair(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, void *d, int out_dtype, int64_t ldd,
                              int64_t M, int64_t N, const int32_t *col_map, const tj_mxfp8 *a8, const tj_mxfp8 *b8,
                              void *d8, int out8_dtype, int64_t ldd8, int64_t M8, int64_t N8, const int32_t *col_map8,
-                             cudaStream_t s);
+                             cudaStream_t s, const SplitRegion *split = nullptr);
 
 cudaError_t launch_osci_reset(float *w, float *w_prev, float *dist_q, float *dist_m, const tj_nvfp4 &q_prev,
                               const tj_nvfp4 &q_out, uint32_t *mask, int64_t rows, int64_t cols, float lr,

@@ -62,6 +62,8 @@ _SIGS = {
     "tj_gemm_mxfp8": [ctypes.POINTER(CMxfp8), ctypes.POINTER(CMxfp8), _P, _I, _I64, _P, _P],
     "tj_gemm_pair": [ctypes.POINTER(CNvfp4), ctypes.POINTER(CNvfp4), _F, _P, _I, _I64, _P, ctypes.POINTER(CMxfp8),
                      ctypes.POINTER(CMxfp8), _P, _I, _I64, _P, _P],
+    "tj_gemm_pair_f32": [ctypes.POINTER(CNvfp4), ctypes.POINTER(CNvfp4), _F, _P, ctypes.POINTER(CMxfp8),
+                         ctypes.POINTER(CMxfp8), _P, _P, _I64, _I64, _P],
     "tj_linear_fwd": [_P, _I64, _I64, _I64, ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P, _P, _I64,
                       ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P, _I, _I64, _P],
     "tj_linear_bwd_dx": [_P, _I64, _I64, _I64, ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P, _P, _I64, _U64,
@@ -277,6 +279,15 @@ def gemm_pair(a, b, a8, b8, alpha=1.0, out=None, out8=None, col_map=None, col_ma
           out.stride(0), _ptr(col_map), ctypes.byref(ca8), ctypes.byref(cb8), _ptr(out8), _dtype_code(out8),
           out8.stride(0), _ptr(col_map8), _stream(stream))
     return out, out8
+
+
+def gemm_pair_f32(a, b, a8, b8, out, col_map, col_map8, alpha=1.0, stream=None):
+    """A pair launch whose fp32 products fill `out` through their column maps
+    (tj_gemm_pair_f32): the call may zero `out` and split a long K in two."""
+    ca, cb, ca8, cb8 = a.c(), b.c(), a8.c(), b8.c()
+    _call("tj_gemm_pair_f32", ctypes.byref(ca), ctypes.byref(cb), float(alpha), _ptr(col_map), ctypes.byref(ca8),
+          ctypes.byref(cb8), _ptr(col_map8), _ptr(out), out.shape[1], out.stride(0), _stream(stream))
+    return out
 
 
 def workspace_size(op, M, N, K, k):

@@ -153,3 +153,33 @@ def test_gemm_pair_equals_the_two_products(tj, out_dtype):
     assert_gemm_close(got[:, cm.numpy()], OL.gemm_fp4(ra, rb, 2.0 ** -7), abs_product(ra, rb, 2.0 ** -7), bf16=bf,
                       what="pair fp4")
     assert_gemm_close(got[:, cm8.numpy()], OL.gemm_fp8(ra8, rb8), abs_product_fp8(ra8, rb8), bf16=bf, what="pair fp8")
+
+
+@pytest.mark.parametrize("K,k", [(2048, 1024), (640, 256)])
+def test_gemm_pair_f32_whole_output(tj, K, k):
+    """tj_gemm_pair_f32: both fp32 products fill one matrix through their column maps.  With 8
+    or more stages of K in both products and few tiles the call zeroes the matrix and splits K
+    in two (first case); the result matches the oracle, agrees with tj_gemm_pair to fp32
+    rounding, and repeats bit for bit.  Without a split (second case) it is tj_gemm_pair's."""
+    M, N, N8 = 384, 300, 96
+    qa, qb, ra, rb = _operands(tj, M, N, K, seed=51)
+    a8, b8, ra8, rb8 = _fp8_operands(tj, M, N8, k, seed=52)
+    perm = torch.randperm(N + N8, generator=torch.Generator().manual_seed(8)).to(torch.int32)
+    cm, cm8 = perm[:N].sort().values.cuda(), perm[N:].sort().values.cuda()
+    out = torch.full((M, N + N8), 5.0, dtype=torch.float32, device="cuda")
+    tj.gemm_pair_f32(qa, qb, a8, b8, out, cm, cm8, alpha=2.0 ** -7)
+    again = torch.full_like(out, -1.0)
+    tj.gemm_pair_f32(qa, qb, a8, b8, again, cm, cm8, alpha=2.0 ** -7)
+    ref = torch.full_like(out, 5.0)
+    tj.gemm_pair(qa, qb, a8, b8, alpha=2.0 ** -7, out=ref, out8=ref, col_map=cm, col_map8=cm8)
+    torch.cuda.synchronize()
+    tj.device_status()
+    assert torch.equal(out, again)
+    if K < 2048:
+        assert torch.equal(out, ref)
+    else:
+        assert float((out - ref).abs().max()) <= 1e-5 * float(ref.abs().max())
+    got = out.cpu().numpy()
+    assert_gemm_close(got[:, cm.cpu().numpy()], OL.gemm_fp4(ra, rb, 2.0 ** -7), abs_product(ra, rb, 2.0 ** -7),
+                      what="pair_f32 fp4")
+    assert_gemm_close(got[:, cm8.cpu().numpy()], OL.gemm_fp8(ra8, rb8), abs_product_fp8(ra8, rb8), what="pair_f32 fp8")

@@ -122,6 +122,37 @@ def test_ragged_linear(tj):
     _run_and_check(tj, X, W, dY, outl, seed=17)
 
 
+@pytest.mark.parametrize("k_out", [0, 26])
+def test_long_token_dw_splits_k(tj, k_out):
+    """2048 tokens and a few output tiles: the dW launch halves its K over two works per tile
+    that add into the zeroed fp32 output (two additions onto zero, so the bits do not depend
+    on their order).  Same checks as above, and a second call gives the same bits."""
+    g = torch.Generator().manual_seed(23)
+    M, N, K = 2048, 200, 264
+    X = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    W = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16)
+    dY = (torch.randn(M, N, generator=g) * 1e-3).to(torch.bfloat16)
+    outl = np.sort(np.random.default_rng(3).choice(K, k_out, replace=False))
+    _run_and_check(tj, X, W, dY, outl, seed=29)
+    ni, oi, wq, w8 = _setup(tj, X, W, outl)
+    _, xq, x8 = tj.linear_fwd(X.cuda(), wq, w8, ni, oi)
+    dw1 = tj.linear_bwd_dw(dY.cuda(), xq, x8, ni, oi, seed=29)
+    dw2 = tj.linear_bwd_dw(dY.cuda(), xq, x8, ni, oi, seed=29)
+    torch.cuda.synchronize()
+    assert torch.equal(dw1, dw2)
+    if k_out:
+        # the same dW from the public steps, the GEMM as tj_gemm_pair_f32: bit-identical
+        dYc = dY.cuda()
+        s_dyt = tj.quantize_nvfp4(dYc, along_cols=True, mode=tj.TJ_SR, rht=True, seed=29, tag=tj.TAG_DY_COL,
+                                  rht_tag=tj.TAG_RHT_DW)
+        s_x = tj.requantize_nvfp4(xq, tj.TJ_SR, True, 29, tj.TAG_XT, tj.TAG_RHT_DW)
+        dw3 = torch.full((N, K), 7.0, device="cuda")
+        tj.gemm_pair_f32(s_dyt, s_x, tj.quantize_mxfp8(dYc, along_cols=True), tj.requantize_mxfp8(x8), dw3, ni, oi,
+                         alpha=2.0 ** -7)
+        torch.cuda.synchronize()
+        assert torch.equal(dw1, dw3)
+
+
 def test_linear_calls_equal_their_steps(tj):
     """tj_linear_fwd / bwd_dx / bwd_dw give bit-identical results to the sequence of
     public step calls (quantize, requantize, GEMM) that the benchmark times one by one."""
