@@ -97,7 +97,8 @@ static_assert(kNamedP + kPSlots <= 16, "named barriers");
 // One product D = alpha * A B^T of the launch.  A launch computes one or two of them:
 // pr[0] with FP4 blocks (and optionally an FP8 K-slice into the same tiles), and
 // optionally pr[1], an FP8-only product with its own output (the outlier slice of a
-// backward GEMM), whose tiles are scheduled first so they spread over the SMs.
+// backward GEMM).  When both cover the same output rows, the works are taken row block by
+// row block (FP8 works first), so writes to the same rows meet in L2.
 struct GemmProblem {
     int64_t M, N;                 // logical output size
     int tiles_m, tiles_n;         // 128 x 128 output tiles (0 x 0: absent)
@@ -136,8 +137,19 @@ struct TileWork {
 __device__ __forceinline__ TileWork tile_work(const GemmArgs &a, int t) {
     const int t1 = problem_works(a.pr[1]);
     TileWork w;
-    w.p = t < t1 ? 1 : 0;
-    const int i = w.p ? t : t - t1;
+    int i;
+    if (t1 > 0 && a.pr[0].tiles_m == a.pr[1].tiles_m) {
+        // both products cover the same output rows: take them row block by row block (the
+        // FP8 works of a row block, then its FP4 works), so that the two products' writes to
+        // the same output rows follow each other while those rows are still in L2
+        const int w1 = a.pr[1].tiles_n * a.pr[1].splits, w0 = a.pr[0].tiles_n * a.pr[0].splits;
+        const int mb = t / (w0 + w1), r = t - mb * (w0 + w1);
+        w.p = r < w1 ? 1 : 0;
+        i = w.p ? mb * w1 + r : mb * w0 + (r - w1);
+    } else {
+        w.p = t < t1 ? 1 : 0;
+        i = w.p ? t : t - t1;
+    }
     const int split = w.p ? a.pr[1].splits : a.pr[0].splits;
     const int tn = w.p ? a.pr[1].tiles_n : a.pr[0].tiles_n;
     const int nkb4 = w.p ? a.pr[1].nkb4 : a.pr[0].nkb4, nk8 = w.p ? a.pr[1].nk8 : a.pr[0].nk8;
