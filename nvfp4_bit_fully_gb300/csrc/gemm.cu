@@ -581,16 +581,14 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                 const bool va = na < g.N, vz = nz < g.N;
                 const int64_t ca = va ? (g.col_map ? (int64_t)g.col_map[na] : na) : 0;
                 const int64_t cz = vz ? (g.col_map ? (int64_t)g.col_map[nz] : nz) : 0;
-                const bool pair = va && vz && cz == ca + 1 && ((ca | g.ldd) & 1) == 0;
+                // two 2-byte stores per lane and row, the same for every lane: choosing a 4-byte
+                // store where a lane's pair happens to be adjacent and aligned splits the warp
+                // into divergent store instructions, which measured slower
                 for (int r = rsub; r < 32 && rbase + r < g.M; r += kRp) {
                     const uint32_t w = stg[r * (kW + 1) + wl];
                     __nv_bfloat16 *drow = static_cast<__nv_bfloat16 *>(g.d) + (rbase + r) * g.ldd;
-                    if (pair) {
-                        *reinterpret_cast<uint32_t *>(drow + ca) = w;
-                    } else {
-                        if (va) drow[ca] = __ushort_as_bfloat16((unsigned short)(w & 0xffffu));
-                        if (vz) drow[cz] = __ushort_as_bfloat16((unsigned short)(w >> 16));
-                    }
+                    if (va) drow[ca] = __ushort_as_bfloat16((unsigned short)(w & 0xffffu));
+                    if (vz) drow[cz] = __ushort_as_bfloat16((unsigned short)(w >> 16));
                 }
                 __syncwarp();
             } else {
