@@ -256,7 +256,7 @@ class OsciState:
 # DRAM bytes per element measured by ncu (dram__bytes_read + write of one capture of the
 # current kernel version, divided by its elements), for the HBM-bound kernels; kernels not
 # listed report traffic None.  k_osci_reset: 1913.3 MB over 67,108,864 weights.
-TRAFFIC_BYTES_PER_ELEM = {"k_osci_reset": 28.5}
+TRAFFIC_BYTES_PER_ELEM = {"k_osci_reset": 28.55}
 NV_B = 0.5 + 1.0 / 16 + 4.0 / 128      # bytes per NVFP4 element (codes + E4M3 + FP32 scales)
 MX_B = 1.0 + 1.0 / 32                   # bytes per MXFP8 element (E4M3 + UE8M0)
 
