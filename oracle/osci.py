@@ -61,3 +61,48 @@ def osci_reset_step(w, state, lr, lr_thr, risk_thr, track=True):
     dist_m = np.where(mask, F32(0.0), dist_m).astype(F32)
     new_state = {"w_prev": w_new.copy(), "qhat_prev": qh, "dist_q": dist_q, "dist_m": dist_m}
     return w_new, new_state, mask, q
+
+
+# ---------------------------------------------------------------------------
+# Training-step fusion around OsciReset: the optimizer update that precedes the pass.
+# The pages apply OsciReset to the master weights after the optimizer step and name no
+# optimizer; this follows AdamW (Loshchilov & Hutter, decoupled weight decay), the usual
+# choice for the OLMo-2-class models the pages train, in the form
+#     m <- beta1 m + (1 - beta1) g
+#     v <- beta2 v + (1 - beta2) g g
+#     w <- w (1 - lr wd) - (lr / (1 - beta1^t)) * m / (sqrt(v) / sqrt(1 - beta2^t) + eps)
+# with every operation an fp32 round-to-nearest step in exactly this order (products
+# before sums, no fused multiply-add), and the per-step constants formed in double
+# precision and rounded once to fp32.
+# ---------------------------------------------------------------------------
+def adamw_constants(lr, beta1, beta2, eps, weight_decay, step):
+    """The fp32 constants of one AdamW step t = step >= 1."""
+    t = int(step)
+    return {
+        "b1": F32(beta1), "b2": F32(beta2), "om1": F32(1.0 - beta1), "om2": F32(1.0 - beta2),
+        "decay": F32(1.0 - lr * weight_decay), "step_size": F32(lr / (1.0 - beta1 ** t)),
+        "bc2": F32(np.sqrt(1.0 - beta2 ** t)), "eps": F32(eps),
+    }
+
+
+def adamw_step(w, g, m, v, lr, beta1, beta2, eps, weight_decay, step):
+    """One AdamW update in fp32.  Returns (w_new, m_new, v_new)."""
+    c = adamw_constants(lr, beta1, beta2, eps, weight_decay, step)
+    w, g, m, v = (np.asarray(a, dtype=F32) for a in (w, g, m, v))
+    m1 = (c["b1"] * m).astype(F32) + (c["om1"] * g).astype(F32)
+    m1 = m1.astype(F32)
+    gg = (g * g).astype(F32)
+    v1 = ((c["b2"] * v).astype(F32) + (c["om2"] * gg).astype(F32)).astype(F32)
+    denom = ((np.sqrt(v1).astype(F32) / c["bc2"]).astype(F32) + c["eps"]).astype(F32)
+    upd = (c["step_size"] * (m1 / denom).astype(F32)).astype(F32)
+    w1 = ((w * c["decay"]).astype(F32) - upd).astype(F32)
+    return w1, m1, v1
+
+
+def adamw_osci_reset_step(w, g, m, v, state, lr, beta1, beta2, eps, weight_decay, step, lr_thr, risk_thr,
+                          track=True):
+    """The fused training-step pass: AdamW, then OsciReset of the updated weights (and their
+    forward quantization).  Returns (w_new, m_new, v_new, state_new, mask, q)."""
+    w1, m1, v1 = adamw_step(w, g, m, v, lr, beta1, beta2, eps, weight_decay, step)
+    w_new, state_new, mask, q = osci_reset_step(w1, state, lr, lr_thr, risk_thr, track)
+    return w_new, m1, v1, state_new, mask, q

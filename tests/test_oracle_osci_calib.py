@@ -128,3 +128,52 @@ def test_calibration_ties_and_exact_sums():
     out, _ = C.top_k_channels(s, 2)
     assert list(out) == [2, 5]                               # ties -> lower channel index
     assert C.outlier_count(1024, 10) == 103 and C.outlier_count(4096, 10) == 410
+
+
+# ---------------------------------------------------------------------------
+# AdamW step of the fused training-step pass, pinned against closed forms and against
+# torch.optim.AdamW (an independent implementation whose rounding order differs, so it
+# agrees within a few fp32 ulp).
+# ---------------------------------------------------------------------------
+def test_adamw_first_step_closed_form():
+    """Step 1 without weight decay: m-hat = g and v-hat = g^2, so w moves by
+    lr * g / (|g| + eps), i.e. by about lr against the sign of g."""
+    rng = np.random.default_rng(4)
+    w = (rng.standard_normal((4, 64)) * 0.02).astype(F32)
+    g = (rng.standard_normal((4, 64)) * 1e-2).astype(F32)
+    z = np.zeros_like(w)
+    lr, eps = 1e-3, 1e-8
+    w1, m1, v1 = O.adamw_step(w, g, z, z, lr, 0.9, 0.95, eps, 0.0, 1)
+    assert np.array_equal(m1, (F32(0.1) * g).astype(F32))
+    exact = w.astype(np.float64) - lr * g.astype(np.float64) / (np.abs(g.astype(np.float64)) + eps)
+    assert np.allclose(w1, exact, rtol=0, atol=4e-9)
+
+
+def test_adamw_weight_decay_alone_is_one_product():
+    """A zero gradient leaves m = v = 0 and the update is exactly w * fp32(1 - lr wd)."""
+    w = (np.random.default_rng(5).standard_normal((2, 128)) * 0.02).astype(F32)
+    z = np.zeros_like(w)
+    w1, m1, v1 = O.adamw_step(w, z, z, z, 1e-3, 0.9, 0.95, 1e-8, 0.1, 7)
+    assert not m1.any() and not v1.any()
+    assert np.array_equal(w1, (w * F32(1.0 - 1e-3 * 0.1)).astype(F32))
+
+
+def test_adamw_matches_torch_optim_adamw():
+    torch = __import__("torch")
+    rng = np.random.default_rng(6)
+    w = (rng.standard_normal((8, 96)) * 0.02).astype(F32)
+    m = np.zeros_like(w)
+    v = np.zeros_like(w)
+    p = torch.nn.Parameter(torch.from_numpy(w.copy()))
+    opt = torch.optim.AdamW([p], lr=1e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1, foreach=False)
+    for t in range(1, 9):
+        g = (rng.standard_normal(w.shape) * 1e-2).astype(F32)
+        w, m, v = O.adamw_step(w, g, m, v, 1e-3, 0.9, 0.95, 1e-8, 0.1, t)
+        p.grad = torch.from_numpy(g.copy())
+        opt.step()
+        st = opt.state[p]
+        assert np.allclose(w, p.detach().numpy(), rtol=1e-6, atol=1e-9), t
+        mt, vt = st["exp_avg"].numpy(), st["exp_avg_sq"].numpy()
+        # m can cancel to near zero, where the two rounding orders differ most in relative terms
+        assert np.allclose(m, mt, rtol=1e-5, atol=1e-6 * float(np.abs(mt).max())), t
+        assert np.allclose(v, vt, rtol=1e-5, atol=0), t
