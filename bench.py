@@ -306,6 +306,31 @@ def quantize_sweep(tj, dev, stream, hbm_peak, flush):
     return out
 
 
+def adamw_osci_alone(tj, osci, stream, hbm_peak):
+    """The fused training-step pass (AdamW + OsciReset + forward-W quantize, tj_adamw_osci_reset)
+    over the same master weights, with a synthetic gradient, timed alone.  Its state is a copy,
+    so the step's OsciReset trajectory is untouched."""
+    g = torch.randn_like(osci.w) * 1e-2
+    m = torch.zeros_like(osci.w)
+    v = torch.zeros_like(osci.w)
+    w = osci.w.clone()
+    w_prev, dq, dm = osci.w_prev.clone(), osci.dq.clone(), osci.dm.clone()
+    step = [0]
+
+    def fn():
+        step[0] += 1
+        tj.adamw_osci_reset(w, g, m, v, w_prev, dq, dm, osci.q[0], osci.q[1], osci.mask, 5e-5, 0.9, 0.95, 1e-8,
+                            0.1, step[0], LR_THR, RISK_THR, True, stream=stream)
+
+    ms = time_kernel(fn, stream, 10)
+    # read w, g, m, v, w_prev, dist_Q, dist_M + previous Q; write w, m, v, w_prev, dist_Q,
+    # dist_M + new Q + 1 mask bit
+    nbytes = osci.n * (4 * 7 + NV_B + 4 * 6 + NV_B + 1.0 / 8)
+    del g, m, v, w, w_prev, dq, dm
+    return {"params": osci.n, "ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm_peak, 3), "bytes_per_weight": round(nbytes / osci.n, 4)}
+
+
 def gemm_alone(tj, lin, stream, fp4_peak, fp8_peak):
     """The largest forward GEMM (FP4 part + FP8 slice in one tile) timed alone."""
     M, N, K, k = TOKENS, lin.N, lin.K, lin.k
@@ -562,6 +587,8 @@ def main():
         big = max(linears, key=lambda l: l.N * l.K)
         extras["gemm_fwd_alone"] = gemm_alone(tj, big, stream, fp4_peak, fp8_peak)
         del flush
+        if osci is not None:
+            extras["adamw_osci_reset"] = adamw_osci_alone(tj, osci, stream, hbm_peak)
     e2e = None
     if not args.no_extras:
         e2e = measure_e2e(tj, linears, stream, max(3, args.steps // 4), world)

@@ -330,6 +330,29 @@ tj_status tj_osci_reset(float *w, float *w_prev, float *dist_q, float *dist_m, c
                         tj_nvfp4 *q_out, uint32_t *reset_mask, int64_t rows, int64_t cols, float lr,
                         float lr_thr, float risk_thr, int track, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * tj_adamw_osci_reset - the training-step pass around OsciReset in one sweep over the
+ * master weights: the AdamW update of w from its gradient, then tj_osci_reset of the
+ * updated w (including its forward quantization into q_out).  The pages apply OsciReset
+ * after the optimizer step (§2.B) and name no optimizer; this is AdamW with decoupled
+ * weight decay, each step an fp32 round-to-nearest operation in this order:
+ *   m <- beta1 m + (1 - beta1) g
+ *   v <- beta2 v + (1 - beta2) (g g)
+ *   w <- w (1 - lr wd) - (lr / (1 - beta1^t)) (m / (sqrt(v) / sqrt(1 - beta2^t) + eps))
+ * The per-step constants (1 - beta1, 1 - beta2, 1 - lr wd, lr / (1 - beta1^t),
+ * sqrt(1 - beta2^t)) are formed in double from the fp32 arguments and rounded once.
+ * step = t >= 1.  g, m, v: fp32 [rows, cols] contiguous, 16-byte aligned (m, v updated in
+ * place; g read only).  w is always written.  The other arguments, the reset and the
+ * outputs are as for tj_osci_reset; the learning rate lr is also the one OsciReset
+ * compares with lr_thr.  Same as tj_osci_reset applied to the result of the AdamW step,
+ * bit for bit, in one pass (one read of w instead of two).
+ * ------------------------------------------------------------------------- */
+tj_status tj_adamw_osci_reset(float *w, const float *g, float *m, float *v, float *w_prev, float *dist_q,
+                              float *dist_m, const tj_nvfp4 *q_prev, tj_nvfp4 *q_out, uint32_t *reset_mask,
+                              int64_t rows, int64_t cols, float lr, float beta1, float beta2, float eps,
+                              float weight_decay, int64_t step, float lr_thr, float risk_thr, int track,
+                              void *stream);
+
 /* Reads (synchronously) and clears the sticky device error flag: TJ_OK, or
  * TJ_ERR_TIMEOUT if a bounded device wait ran out since the last query. */
 tj_status tj_get_device_status(void);

@@ -444,4 +444,24 @@ tj_status tj_osci_reset(float *w, float *w_prev, float *dist_q, float *dist_m, c
                                          lr_thr, risk_thr, track, static_cast<cudaStream_t>(stream)));
 }
 
+tj_status tj_adamw_osci_reset(float *w, const float *g, float *m, float *v, float *w_prev, float *dist_q,
+                              float *dist_m, const tj_nvfp4 *q_prev, tj_nvfp4 *q_out, uint32_t *reset_mask,
+                              int64_t rows, int64_t cols, float lr, float beta1, float beta2, float eps,
+                              float weight_decay, int64_t step, float lr_thr, float risk_thr, int track,
+                              void *stream) {
+    if (w == nullptr || g == nullptr || m == nullptr || v == nullptr || w_prev == nullptr || dist_q == nullptr ||
+        dist_m == nullptr || reset_mask == nullptr || rows < 0 || cols < 0 || step < 1)
+        return TJ_ERR_INVALID_ARG;
+    tj_status st = check_nv(q_prev, rows, cols);
+    if (st == TJ_OK) st = check_nv(q_out, rows, cols);
+    if (st != TJ_OK) return st;
+    if (!al16(w) || !al16(g) || !al16(m) || !al16(v) || !al16(w_prev) || !al16(dist_q) || !al16(dist_m) ||
+        !al16(reset_mask))
+        return TJ_ERR_ALIGN;
+    if (rows == 0 || cols == 0) return TJ_OK;
+    return cuda_status(launch_adamw_osci_reset(w, g, m, v, w_prev, dist_q, dist_m, *q_prev, *q_out, reset_mask, rows,
+                                               cols, lr, beta1, beta2, eps, weight_decay, step, lr_thr, risk_thr,
+                                               track, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

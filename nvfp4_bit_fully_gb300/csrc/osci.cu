@@ -12,6 +12,8 @@
 // The risk dist_Q / dist_M is compared without a division.  HBM-bound:
 // ~29.3 bytes per element (read w, w_prev, dist_Q, dist_M and the previous Q;
 // write w_prev, dist_Q, dist_M, the new Q and one mask bit; w only on reset).
+#include <cmath>
+
 #include "quant_core.cuh"
 #include "tj_internal.h"
 
@@ -39,13 +41,38 @@ __device__ __forceinline__ uint32_t spread4(uint32_t b) {
 
 constexpr int kBlocksPerWarp = 1;   // 128-element blocks per warp iteration (one, with 5 CTAs per SM, measured fastest)
 
+}  // namespace
+
+// The fp32 constants of one AdamW step (formed in double on the host, rounded once).
+struct AdamConsts {
+    float b1, b2, om1, om2, decay, step_size, bc2, eps;
+};
+
+namespace {
+
+// One AdamW update of an element, in the fixed fp32 order of the training-step pass:
+//   m <- b1 m + (1 - b1) g;  v <- b2 v + (1 - b2) g g;
+//   w <- w (1 - lr wd) - step_size * m / (sqrt(v) / bc2 + eps)
+// (step_size = lr / (1 - b1^t), bc2 = sqrt(1 - b2^t)); every step is rounded separately.
+__device__ __forceinline__ float adamw_elem(float w, float g, float &m, float &v, const AdamConsts &c) {
+    m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.om1, g));
+    v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.om2, __fmul_rn(g, g)));
+    const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), c.bc2), c.eps);
+    return __fsub_rn(__fmul_rn(w, c.decay), __fmul_rn(c.step_size, __fdiv_rn(m, denom)));
+}
+
 // One warp per 128-element block: lane l holds elements 4l .. 4l+3, so every
 // load and store of the fp32 state is a fully coalesced 512-byte warp access.
 // A 16-element inner group is 4 lanes; the outer block is the whole warp.
-__global__ void __launch_bounds__(256, 5) k_osci_reset(float *w, float *w_prev, float *dist_q, float *dist_m,
-                                                    const uint8_t *qp_codes, const uint8_t *qp_sf,
-                                                    const float *qp_outer, OutNv qo, uint32_t *mask, int64_t rows,
-                                                    int64_t cols, int lr_low, float risk_thr, int track) {
+// ADAMW: the training-step pass, which first applies the AdamW update to w (reading the
+// gradient and both moments, writing the moments and always writing w back).
+template <bool ADAMW>
+__global__ void __launch_bounds__(256, ADAMW ? 4 : 5) k_osci_reset(float *w, float *w_prev, float *dist_q,
+                                                                float *dist_m, const uint8_t *qp_codes,
+                                                                const uint8_t *qp_sf, const float *qp_outer, OutNv qo,
+                                                                uint32_t *mask, int64_t rows, int64_t cols, int lr_low,
+                                                                float risk_thr, int track, const float *grad,
+                                                                float *adam_m, float *adam_v, AdamConsts ac) {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2;                                  // inner group within the block
     const int64_t nblk_row = qo.cols_p / 128, total = qo.rows_p * nblk_row;
@@ -55,6 +82,7 @@ __global__ void __launch_bounds__(256, 5) k_osci_reset(float *w, float *w_prev, 
     const bool vec = (cols & 3) == 0;
     for (int64_t base = warp0 * kBlocksPerWarp; base < total; base += nwarps * kBlocksPerWarp) {
         float x[kBlocksPerWarp][4], xp[kBlocksPerWarp][4], dq[kBlocksPerWarp][4], dm[kBlocksPerWarp][4];
+        float gr[kBlocksPerWarp][4], am[kBlocksPerWarp][4], av[kBlocksPerWarp][4];   // AdamW: g, m, v
         int n_live[kBlocksPerWarp];
         uint32_t pcode[kBlocksPerWarp], psb[kBlocksPerWarp];   // previous Q: this lane's 4 codes, its group's scale byte
         float pso[kBlocksPerWarp];                              // previous Q: the block's outer scale
@@ -86,6 +114,14 @@ __global__ void __launch_bounds__(256, 5) k_osci_reset(float *w, float *w_prev, 
                 xp[b][0] = p.x; xp[b][1] = p.y; xp[b][2] = p.z; xp[b][3] = p.w;
                 dq[b][0] = q.x; dq[b][1] = q.y; dq[b][2] = q.z; dq[b][3] = q.w;
                 dm[b][0] = m.x; dm[b][1] = m.y; dm[b][2] = m.z; dm[b][3] = m.w;
+                if (ADAMW) {
+                    const float4 gg = __ldg(reinterpret_cast<const float4 *>(grad + off));
+                    const float4 mm = *reinterpret_cast<const float4 *>(adam_m + off);
+                    const float4 vv = *reinterpret_cast<const float4 *>(adam_v + off);
+                    gr[b][0] = gg.x; gr[b][1] = gg.y; gr[b][2] = gg.z; gr[b][3] = gg.w;
+                    am[b][0] = mm.x; am[b][1] = mm.y; am[b][2] = mm.z; am[b][3] = mm.w;
+                    av[b][0] = vv.x; av[b][1] = vv.y; av[b][2] = vv.z; av[b][3] = vv.w;
+                }
             } else {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -94,6 +130,11 @@ __global__ void __launch_bounds__(256, 5) k_osci_reset(float *w, float *w_prev, 
                     xp[b][i] = in ? w_prev[off + i] : 0.0f;
                     dq[b][i] = in ? dist_q[off + i] : 0.0f;
                     dm[b][i] = in ? dist_m[off + i] : 0.0f;
+                    if (ADAMW) {
+                        gr[b][i] = in ? grad[off + i] : 0.0f;
+                        am[b][i] = in ? adam_m[off + i] : 0.0f;
+                        av[b][i] = in ? adam_v[off + i] : 0.0f;
+                    }
                 }
             }
         }
@@ -105,6 +146,12 @@ __global__ void __launch_bounds__(256, 5) k_osci_reset(float *w, float *w_prev, 
             if (!valid) break;
             const int64_t row = blk / nblk_row, kb = blk % nblk_row;
             const int64_t c = kb * 128 + 4 * lane;
+            if (ADAMW) {
+                // the optimizer step first; padding elements stay 0
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (i < n_live[b]) x[b][i] = adamw_elem(x[b][i], gr[b][i], am[b][i], av[b][i], ac);
+            }
             // double-block RTN quantization (TetraJet-v2 §2.A) of the master weights
             float a = fmaxf(fmaxf(fabsf(x[b][0]), fabsf(x[b][1])), fmaxf(fabsf(x[b][2]), fabsf(x[b][3])));
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
@@ -166,6 +213,20 @@ __global__ void __launch_bounds__(256, 5) k_osci_reset(float *w, float *w_prev, 
             if (row < rows) {
                 const int64_t off = row * cols + c;
                 const int nl = n_live[b];
+                if (ADAMW && nl == 4 && vec) {
+                    *reinterpret_cast<float4 *>(w + off) = make_float4(x[b][0], x[b][1], x[b][2], x[b][3]);
+                    *reinterpret_cast<float4 *>(adam_m + off) = make_float4(am[b][0], am[b][1], am[b][2], am[b][3]);
+                    *reinterpret_cast<float4 *>(adam_v + off) = make_float4(av[b][0], av[b][1], av[b][2], av[b][3]);
+                } else if (ADAMW) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (i < nl) {
+                            w[off + i] = x[b][i];
+                            adam_m[off + i] = am[b][i];
+                            adam_v[off + i] = av[b][i];
+                        }
+                    }
+                }
                 if (nl == 4 && vec) {
                     *reinterpret_cast<float4 *>(w_prev + off) = make_float4(x[b][0], x[b][1], x[b][2], x[b][3]);
                     *reinterpret_cast<float4 *>(dist_q + off) = make_float4(dq[b][0], dq[b][1], dq[b][2], dq[b][3]);
@@ -180,9 +241,11 @@ __global__ void __launch_bounds__(256, 5) k_osci_reset(float *w, float *w_prev, 
                         }
                     }
                 }
+                if (!ADAMW) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (rs[i]) w[off + i] = x[b][i];          // master weight moves only on a reset
+                    for (int i = 0; i < 4; ++i)
+                        if (rs[i]) w[off + i] = x[b][i];      // master weight moves only on a reset
+                }
                 if (lane < 4) {
                     const int64_t word = kb * 4 + lane;        // bits of elements 32*lane .. +31 of the block
                     if (word < mw) {
@@ -199,17 +262,48 @@ __global__ void __launch_bounds__(256, 5) k_osci_reset(float *w, float *w_prev, 
 
 }  // namespace
 
-cudaError_t launch_osci_reset(float *w, float *w_prev, float *dist_q, float *dist_m, const tj_nvfp4 &q_prev,
-                              const tj_nvfp4 &q_out, uint32_t *mask, int64_t rows, int64_t cols, float lr,
-                              float lr_thr, float risk_thr, int track, cudaStream_t s) {
+namespace {
+template <bool ADAMW>
+cudaError_t launch_osci(float *w, float *w_prev, float *dist_q, float *dist_m, const tj_nvfp4 &q_prev,
+                        const tj_nvfp4 &q_out, uint32_t *mask, int64_t rows, int64_t cols, float lr, float lr_thr,
+                        float risk_thr, int track, const float *grad, float *m, float *v, const AdamConsts &ac,
+                        cudaStream_t s) {
     const OutNv qo{q_out.codes, q_out.sf, q_out.outer, round_up(rows, 128), round_up(cols, 128)};
     const int64_t total = qo.rows_p * (qo.cols_p / 128);
     int64_t grid = (total + 8 * kBlocksPerWarp - 1) / (8 * kBlocksPerWarp);
     if (grid > 152 * 12) grid = 152 * 12;
     if (grid < 1) grid = 1;
-    k_osci_reset<<<(unsigned)grid, 256, 0, s>>>(w, w_prev, dist_q, dist_m, q_prev.codes, q_prev.sf, q_prev.outer, qo,
-                                                 mask, rows, cols, (lr < lr_thr) ? 1 : 0, risk_thr, track);
+    k_osci_reset<ADAMW><<<(unsigned)grid, 256, 0, s>>>(w, w_prev, dist_q, dist_m, q_prev.codes, q_prev.sf,
+                                                        q_prev.outer, qo, mask, rows, cols, (lr < lr_thr) ? 1 : 0,
+                                                        risk_thr, track, grad, m, v, ac);
     return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_osci_reset(float *w, float *w_prev, float *dist_q, float *dist_m, const tj_nvfp4 &q_prev,
+                              const tj_nvfp4 &q_out, uint32_t *mask, int64_t rows, int64_t cols, float lr,
+                              float lr_thr, float risk_thr, int track, cudaStream_t s) {
+    return launch_osci<false>(w, w_prev, dist_q, dist_m, q_prev, q_out, mask, rows, cols, lr, lr_thr, risk_thr, track,
+                              nullptr, nullptr, nullptr, AdamConsts{}, s);
+}
+
+cudaError_t launch_adamw_osci_reset(float *w, const float *grad, float *m, float *v, float *w_prev, float *dist_q,
+                                    float *dist_m, const tj_nvfp4 &q_prev, const tj_nvfp4 &q_out, uint32_t *mask,
+                                    int64_t rows, int64_t cols, float lr, float beta1, float beta2, float eps,
+                                    float weight_decay, int64_t step, float lr_thr, float risk_thr, int track,
+                                    cudaStream_t s) {
+    const double t = (double)step;
+    AdamConsts ac;
+    ac.b1 = beta1;
+    ac.b2 = beta2;
+    ac.om1 = (float)(1.0 - (double)beta1);
+    ac.om2 = (float)(1.0 - (double)beta2);
+    ac.decay = (float)(1.0 - (double)lr * (double)weight_decay);
+    ac.step_size = (float)((double)lr / (1.0 - std::pow((double)beta1, t)));
+    ac.bc2 = (float)std::sqrt(1.0 - std::pow((double)beta2, t));
+    ac.eps = eps;
+    return launch_osci<true>(w, w_prev, dist_q, dist_m, q_prev, q_out, mask, rows, cols, lr, lr_thr, risk_thr, track,
+                             grad, m, v, ac, s);
 }
 
 }  // namespace tj

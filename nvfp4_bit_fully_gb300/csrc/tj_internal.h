@@ -44,6 +44,11 @@ cudaError_t launch_gemm_pair(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, 
                              void *d8, int out8_dtype, int64_t ldd8, int64_t M8, int64_t N8, const int32_t *col_map8,
                              cudaStream_t s, const SplitRegion *split = nullptr);
 
+cudaError_t launch_adamw_osci_reset(float *w, const float *grad, float *m, float *v, float *w_prev, float *dist_q,
+                                    float *dist_m, const tj_nvfp4 &q_prev, const tj_nvfp4 &q_out, uint32_t *mask,
+                                    int64_t rows, int64_t cols, float lr, float beta1, float beta2, float eps,
+                                    float weight_decay, int64_t step, float lr_thr, float risk_thr, int track,
+                                    cudaStream_t s);
 cudaError_t launch_osci_reset(float *w, float *w_prev, float *dist_q, float *dist_m, const tj_nvfp4 &q_prev,
                               const tj_nvfp4 &q_out, uint32_t *mask, int64_t rows, int64_t cols, float lr,
                               float lr_thr, float risk_thr, int track, cudaStream_t s);

@@ -74,6 +74,8 @@ _SIGS = {
     "tj_outlier_calibrate": [_P, _I, _I64, _I64, _I64, _P, _I, _I64, _P, _P, _P],
     "tj_osci_reset": [_P, _P, _P, _P, ctypes.POINTER(CNvfp4), ctypes.POINTER(CNvfp4), _P, _I64, _I64, _F, _F, _F,
                       _I, _P],
+    "tj_adamw_osci_reset": [_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(CNvfp4), ctypes.POINTER(CNvfp4), _P, _I64,
+                            _I64, _F, _F, _F, _F, _F, _I64, _F, _F, _I, _P],
     "tj_linear_bwd_dx_noalloc": [_P, _I64, _I64, _I64, ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P, _P, _I64,
                                  _U64, _P, _I, _I64, _P],
     "tj_noalloc_scratch_bytes": [],
@@ -382,6 +384,17 @@ def osci_reset(w, w_prev, dist_q, dist_m, q_prev, q_out, mask, lr, lr_thr, risk_
     cp, co = q_prev.c(), q_out.c()
     _call("tj_osci_reset", _ptr(w), _ptr(w_prev), _ptr(dist_q), _ptr(dist_m), ctypes.byref(cp), ctypes.byref(co),
           _ptr(mask), rows, cols, lr, lr_thr, risk_thr, int(track), _stream(stream))
+
+
+def adamw_osci_reset(w, g, m, v, w_prev, dist_q, dist_m, q_prev, q_out, mask, lr, beta1, beta2, eps, weight_decay,
+                     step, lr_thr, risk_thr, track=True, stream=None):
+    """AdamW then OsciReset in one pass (tj_adamw_osci_reset); w, m, v, w_prev and the
+    distances are updated in place."""
+    rows, cols = w.shape
+    cp, co = q_prev.c(), q_out.c()
+    _call("tj_adamw_osci_reset", _ptr(w), _ptr(g), _ptr(m), _ptr(v), _ptr(w_prev), _ptr(dist_q), _ptr(dist_m),
+          ctypes.byref(cp), ctypes.byref(co), _ptr(mask), rows, cols, lr, beta1, beta2, eps, weight_decay, int(step),
+          lr_thr, risk_thr, int(track), _stream(stream))
 
 
 def device_status():

@@ -76,12 +76,15 @@ def osci_reset_step(w, state, lr, lr_thr, risk_thr, track=True):
 # precision and rounded once to fp32.
 # ---------------------------------------------------------------------------
 def adamw_constants(lr, beta1, beta2, eps, weight_decay, step):
-    """The fp32 constants of one AdamW step t = step >= 1."""
+    """The fp32 constants of one AdamW step t = step >= 1.  The hyperparameters are fp32
+    values (as the C ABI takes them); each constant is formed from them in double precision
+    and rounded once to fp32."""
     t = int(step)
+    lr, b1, b2, wd = (float(F32(a)) for a in (lr, beta1, beta2, weight_decay))
     return {
-        "b1": F32(beta1), "b2": F32(beta2), "om1": F32(1.0 - beta1), "om2": F32(1.0 - beta2),
-        "decay": F32(1.0 - lr * weight_decay), "step_size": F32(lr / (1.0 - beta1 ** t)),
-        "bc2": F32(np.sqrt(1.0 - beta2 ** t)), "eps": F32(eps),
+        "b1": F32(b1), "b2": F32(b2), "om1": F32(1.0 - b1), "om2": F32(1.0 - b2),
+        "decay": F32(1.0 - lr * wd), "step_size": F32(lr / (1.0 - b1 ** t)),
+        "bc2": F32(np.sqrt(1.0 - b2 ** t)), "eps": F32(eps),
     }
 
 

@@ -66,6 +66,49 @@ def test_osci_reset_trajectory_bit_exact(tj, rows, cols):
     assert state["dist_m"].max() > 0
 
 
+@pytest.mark.parametrize("rows,cols", [(64, 256), (37, 200)])
+def test_adamw_osci_reset_trajectory_bit_exact(tj, rows, cols):
+    """The fused training-step pass (AdamW, then OsciReset of the updated weights) equals the
+    oracle's AdamW step followed by its OsciReset step, bit for bit, over a schedule whose
+    learning rate falls below the threshold; a low risk threshold makes resets happen."""
+    rng = np.random.default_rng(3 * rows + cols)
+    w0 = (rng.standard_normal((rows, cols)) * 0.02).astype(np.float32)
+    state = OO.init_state(w0)
+    m = np.zeros_like(w0)
+    v = np.zeros_like(w0)
+    w_dev = torch.from_numpy(w0.copy()).cuda()
+    m_dev, v_dev = torch.zeros_like(w_dev), torch.zeros_like(w_dev)
+    w_prev = w_dev.clone()
+    dq = torch.zeros_like(w_dev)
+    dm = torch.zeros_like(w_dev)
+    q_prev = tj.quantize_nvfp4(w_dev)
+    q_out = tj.NVFP4.empty(rows, cols)
+    mask = torch.empty(rows * ((cols + 31) // 32), dtype=torch.int32, device="cuda")
+    w = w0
+    osc = rng.random((rows, cols)) < 0.2
+    lrs = [1e-3, 5e-4, 2e-4, 9e-5, 5e-5, 2e-5, 1e-5, 1e-5]
+    resets = 0
+    for t, lr in enumerate(lrs, start=1):
+        g = (rng.standard_normal((rows, cols)) * 1e-2).astype(np.float32)
+        g = np.where(osc, np.float32(0.05 * (1 if t % 2 else -1)), g).astype(np.float32)
+        w, m, v, state, m_ref, q_ref = OO.adamw_osci_reset_step(w, g, m, v, state, lr, 0.9, 0.95, 1e-8, 0.1, t,
+                                                                 1e-4, 0.5)
+        tj.adamw_osci_reset(w_dev, torch.from_numpy(g).cuda(), m_dev, v_dev, w_prev, dq, dm, q_prev, q_out, mask,
+                            lr, 0.9, 0.95, 1e-8, 0.1, t, 1e-4, 0.5)
+        torch.cuda.synchronize()
+        assert np.array_equal(w_dev.cpu().numpy(), w), t
+        assert np.array_equal(m_dev.cpu().numpy(), m), t
+        assert np.array_equal(v_dev.cpu().numpy(), v), t
+        assert np.array_equal(w_prev.cpu().numpy(), state["w_prev"]), t
+        assert np.array_equal(dq.cpu().numpy(), state["dist_q"]), t
+        assert np.array_equal(dm.cpu().numpy(), state["dist_m"]), t
+        assert np.array_equal(_mask_bits(mask, rows, cols), m_ref), t
+        assert_nvfp4_equal(q_out, q_ref, "Q step %d" % t)
+        resets += int(m_ref.sum())
+        q_prev, q_out = q_out, q_prev
+    assert resets > 0
+
+
 def test_osci_reset_in_place_q(tj):
     """q_out may be the same tensor as q_prev: it then holds Q of the new weights."""
     rows, cols = 32, 128

@@ -144,7 +144,8 @@ def test_adamw_first_step_closed_form():
     z = np.zeros_like(w)
     lr, eps = 1e-3, 1e-8
     w1, m1, v1 = O.adamw_step(w, g, z, z, lr, 0.9, 0.95, eps, 0.0, 1)
-    assert np.array_equal(m1, (F32(0.1) * g).astype(F32))
+    # from m = 0 the first moment is exactly (1 - beta1) g, beta1 being the fp32 argument
+    assert np.array_equal(m1, (F32(1.0 - float(F32(0.9))) * g).astype(F32))
     exact = w.astype(np.float64) - lr * g.astype(np.float64) / (np.abs(g.astype(np.float64)) + eps)
     assert np.allclose(w1, exact, rtol=0, atol=4e-9)
 
