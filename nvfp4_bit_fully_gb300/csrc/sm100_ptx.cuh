@@ -58,16 +58,6 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, in
         "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
-// Tiled TMA load delivered to every CTA of `cta_mask` in the cluster, at the same
-// CTA-relative shared-memory offset, each signalling its own mbarrier at `bar`'s offset.
-__device__ __forceinline__ void tma_load_2d_multicast(void *smem_dst, const void *tmap, int32_t x, int32_t y,
-                                                      uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
-        : "memory");
-}
 // Tiled TMA store of a shared-memory box to global memory (elements outside the
 // tensor are not written), tracked by the issuing thread's bulk async-group.
 __device__ __forceinline__ void tma_store_2d(const void *tmap, int32_t x, int32_t y, const void *smem_src) {
@@ -114,23 +104,6 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
-}
-// Same, arriving on the mbarrier at `bar`'s offset in every CTA of `cta_mask`.
-__device__ __forceinline__ void tc_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-// Cluster-wide execution barrier (all threads of all CTAs of the cluster).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
 }
 // Copy 32 rows x 128 bits from shared memory into 4 columns of tensor memory,
 // replicated into all four 32-lane sub-partitions.
