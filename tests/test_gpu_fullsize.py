@@ -5,7 +5,8 @@ benchmark; the oracle then recomputes a sample of the outputs one by one:
 - 16384 tokens through each linear of the ~370M-class decoder-layer set, with OutControl calibrated on four batches;
 - the forward-with-OutControl case (16384 x 1024 -> 4096);
 - the backward RHT + SR case (dY 16384 x 4096, W 4096 x 1024);
-- the quantize-only sweep at 16384 x 4096.
+- the quantize-only sweep at 16384 x 4096;
+- OsciReset over the benchmark's 369,098,752 master weights.
 
 Every sampled operand row, of a quantized operand the step produced, has to match bit for bit:
 - X-hat rows and their FP8 slice;
@@ -333,3 +334,50 @@ def test_quantize_sweep_full_size_sampled(tj, along, mode):
         s = _samples(rows, 14, rng)
         ref = Q.quantize_nvfp4(xf[s], mode, seed=1, tag=1, row_ids=s)
     _rows_equal(nvfp4_to_logical(q), ref, s, "sampled %s" % ("columns" if along else "rows"))
+
+
+def test_osci_reset_full_size_sampled(tj):
+    """OsciReset over all 369,098,752 master weights of the benchmark (22 layers of the set, as
+    [n / 1024, 1024] fp32), four passes with a synthetic update before each (a random step
+    plus +-3e-4 on a fixed 5% of the weights, so that weights oscillate) and a learning rate
+    that crosses the threshold.  Sampled rows of every piece of state, the reset mask and the
+    emitted forward weight must equal the oracle's trajectory of those rows bit for bit."""
+    from oracle import osci as OO
+
+    lr_thr, risk_thr = 1e-4, 4.0
+    w = wl.device_master_weights(wl.OSCI_PARAMS, seed=3, device="cuda")
+    rows, cols = w.shape
+    rng = np.random.default_rng(23)
+    r_s = _samples(rows, 14, rng)
+    w_prev = w.clone()
+    dq = torch.zeros_like(w)
+    dm = torch.zeros_like(w)
+    q = [tj.quantize_nvfp4(w), tj.NVFP4.empty(rows, cols)]
+    mask = torch.empty(rows * ((cols + 31) // 32), dtype=torch.int32, device="cuda")
+    w_ref = _f32(w[r_s])
+    state = OO.init_state(w_ref)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(29)
+    osc = torch.rand(w.shape, generator=g, device="cuda") < 0.05
+    resets = 0
+    for t, lr in enumerate((2e-4, 8e-5, 4e-5, 1e-5)):
+        step = torch.randn(w.shape, generator=g, device="cuda") * lr
+        step = torch.where(osc, torch.full_like(step, 3e-4 * (1 if t % 2 == 0 else -1)), step)
+        w.add_(step)
+        w_ref = (w_ref + _f32(step[r_s])).astype(np.float32)
+        del step
+        tj.osci_reset(w, w_prev, dq, dm, q[0], q[1], mask, lr, lr_thr, risk_thr)
+        w_ref, state, m_ref, q_ref = OO.osci_reset_step(w_ref, state, lr, lr_thr, risk_thr)
+        torch.cuda.synchronize()
+        tj.device_status()
+        assert np.array_equal(_f32(w[r_s]), w_ref), t
+        assert np.array_equal(_f32(w_prev[r_s]), state["w_prev"]), t
+        assert np.array_equal(_f32(dq[r_s]), state["dist_q"]), t
+        assert np.array_equal(_f32(dm[r_s]), state["dist_m"]), t
+        words = mask.view(rows, -1)[r_s].cpu().numpy().view(np.uint32)
+        bits = ((words[:, :, None] >> np.arange(32, dtype=np.uint32)) & 1).reshape(len(r_s), -1)[:, :cols]
+        assert np.array_equal(bits.astype(bool), m_ref), t
+        _rows_equal(nvfp4_to_logical(q[1]), q_ref, r_s, "forward weight, pass %d" % t)
+        resets += int(m_ref.sum())
+        q.reverse()
+    assert resets > 0
