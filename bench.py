@@ -186,6 +186,13 @@ class Linear:
         self.flops = 6.0 * M * N * K
         # algorithmic work of every call: (FP4 flops, FP8 flops) or bytes
         f4 = lambda a, b, c: 2.0 * a * b * c
+        # operand and output bytes of each GEMM launch (NVFP4 / MXFP8 operands, bf16 Y and dX,
+        # fp32 dW)
+        self.gemm_bytes = {
+            "gemm_fwd": (M + N) * (kn * NV_B + k * MX_B) + M * N * 2,
+            "gemm_dx": M * N * (NV_B + MX_B) + N * (kn * NV_B + k * MX_B) + M * K * 2,
+            "gemm_dw": N * M * (NV_B + MX_B) + M * (kn * NV_B + k * MX_B) + N * K * 4,
+        }
         self.work = {
             "gemm_fwd": (f4(M, N, kn), f4(M, N, k)), "gemm_dx": (f4(M, kn, N), f4(M, k, N)),
             "gemm_dw": (f4(N, kn, M), f4(N, k, M)),
@@ -257,6 +264,10 @@ class OsciState:
 # current kernel version, divided by its elements), for the HBM-bound kernels; kernels not
 # listed report traffic None.  k_osci_reset: 1913.3 MB over 67,108,864 weights.
 TRAFFIC_BYTES_PER_ELEM = {"k_osci_reset": 28.55}
+# DRAM bytes per launch of the GEMM: the twelve launches of one timed step of the layer set
+# at 16384 tokens read 935.4 MB and wrote 363.4 MB (one-pass ncu capture of the current
+# kernel), 108.2 MB per launch on average.  Valid for the default workload only.
+TRAFFIC_BYTES_PER_LAUNCH = {"k_gemm_nvfp4": 108.2e6}
 NV_B = 0.5 + 1.0 / 16 + 4.0 / 128      # bytes per NVFP4 element (codes + E4M3 + FP32 scales)
 MX_B = 1.0 + 1.0 / 32                   # bytes per MXFP8 element (E4M3 + UE8M0)
 
@@ -543,6 +554,7 @@ def main():
                 p["TFLOP/s"] = round((w[0] + w[1]) / (ms_tot / n * 1e-3) / 1e12, 1)
                 agg[1] += w[0] * n
                 agg[2] += w[1] * n
+                agg[3] += lin.gemm_bytes[call] * n          # operands and output, for the traffic ratio
             else:
                 p["GB/s"] = round(w / (ms_tot / n * 1e-3) / 1e9, 1)
                 agg[3] += w * n
@@ -565,7 +577,9 @@ def main():
         peak_mix = (f4 + f8) / (f4 / fp4_peak + f8 / fp8_peak)           # dtype-weighted peak, TFLOP/s
         achieved = (f4 + f8) / (ms_tot * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak_mix, 1),
-                "unit": "TFLOP/s", "frac": round(achieved / peak_mix, 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(achieved / peak_mix, 4),
+                "traffic": (round(TRAFFIC_BYTES_PER_LAUNCH[dom]) if dom in TRAFFIC_BYTES_PER_LAUNCH else None),
+                "algorithmic_bytes_per_launch": round(by / n) if by else None,
                 "algorithmic_flops_per_launch": round((f4 + f8) / n),
                 "peak_source": "%s bf16 burst %.1f x nominal fp4 (x6) / fp8 (x2) ratios, weighted by the FP4 / FP8 "
                                "flop mix" % (peak_src, bf16_burst)}

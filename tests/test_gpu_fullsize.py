@@ -6,7 +6,7 @@ benchmark; the oracle then recomputes a sample of the outputs one by one:
 - the forward-with-OutControl case (16384 x 1024 -> 4096);
 - the backward RHT + SR case (dY 16384 x 4096, W 4096 x 1024);
 - the quantize-only sweep at 16384 x 4096;
-- OsciReset over the benchmark's 369,098,752 master weights.
+- OsciReset, alone and fused with the AdamW step, over the benchmark's 369,098,752 master weights.
 
 Every sampled operand row, of a quantized operand the step produced, has to match bit for bit:
 - X-hat rows and their FP8 slice;
@@ -379,5 +379,55 @@ def test_osci_reset_full_size_sampled(tj):
         assert np.array_equal(bits.astype(bool), m_ref), t
         _rows_equal(nvfp4_to_logical(q[1]), q_ref, r_s, "forward weight, pass %d" % t)
         resets += int(m_ref.sum())
+        q.reverse()
+    assert resets > 0
+
+
+def test_adamw_osci_reset_full_size_sampled(tj):
+    """The fused training-step pass (AdamW, OsciReset, forward-weight quantization) over all
+    369,098,752 master weights, four steps with a synthetic gradient (5% of the weights get an
+    alternating +-0.05, the rest N(0, 1e-2)) and a learning rate that crosses the threshold:
+    sampled rows of w, m, v, the OsciReset state, the mask and the forward weight equal the
+    oracle's AdamW step followed by its OsciReset step, bit for bit."""
+    from oracle import osci as OO
+
+    lr_thr, risk_thr, b1, b2, eps, wd = 1e-4, 0.5, 0.9, 0.95, 1e-8, 0.1
+    w = wl.device_master_weights(wl.OSCI_PARAMS, seed=3, device="cuda")
+    rows, cols = w.shape
+    rng = np.random.default_rng(31)
+    r_s = _samples(rows, 14, rng)
+    m_dev, v_dev = torch.zeros_like(w), torch.zeros_like(w)
+    w_prev = w.clone()
+    dq = torch.zeros_like(w)
+    dm = torch.zeros_like(w)
+    q = [tj.quantize_nvfp4(w), tj.NVFP4.empty(rows, cols)]
+    mask = torch.empty(rows * ((cols + 31) // 32), dtype=torch.int32, device="cuda")
+    w_ref = _f32(w[r_s])
+    m_ref = np.zeros_like(w_ref)
+    v_ref = np.zeros_like(w_ref)
+    state = OO.init_state(w_ref)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(37)
+    osc = torch.rand(w.shape, generator=gen, device="cuda") < 0.05
+    resets = 0
+    for t, lr in enumerate((2e-4, 8e-5, 4e-5, 1e-5), start=1):
+        g = torch.randn(w.shape, generator=gen, device="cuda") * 1e-2
+        g = torch.where(osc, torch.full_like(g, 0.05 * (1 if t % 2 else -1)), g)
+        tj.adamw_osci_reset(w, g, m_dev, v_dev, w_prev, dq, dm, q[0], q[1], mask, lr, b1, b2, eps, wd, t, lr_thr,
+                            risk_thr)
+        w_ref, m_ref, v_ref, state, mk_ref, q_ref = OO.adamw_osci_reset_step(
+            w_ref, _f32(g[r_s]), m_ref, v_ref, state, lr, b1, b2, eps, wd, t, lr_thr, risk_thr)
+        del g
+        torch.cuda.synchronize()
+        tj.device_status()
+        for name, got, ref in (("w", w, w_ref), ("m", m_dev, m_ref), ("v", v_dev, v_ref),
+                               ("w_prev", w_prev, state["w_prev"]), ("dist_Q", dq, state["dist_q"]),
+                               ("dist_M", dm, state["dist_m"])):
+            assert np.array_equal(_f32(got[r_s]), ref), (name, t)
+        words = mask.view(rows, -1)[r_s].cpu().numpy().view(np.uint32)
+        bits = ((words[:, :, None] >> np.arange(32, dtype=np.uint32)) & 1).reshape(len(r_s), -1)[:, :cols]
+        assert np.array_equal(bits.astype(bool), mk_ref), t
+        _rows_equal(nvfp4_to_logical(q[1]), q_ref, r_s, "forward weight, step %d" % t)
+        resets += int(mk_ref.sum())
         q.reverse()
     assert resets > 0
