@@ -177,11 +177,24 @@ __global__ void __launch_bounds__(256, 3) k_quant_rows(Src src, OutNv onv, OutMx
         const uint4 sb = rht_sign_bits(pk, rht_tag);
         sign_word = t == 0 ? sb.x : (t == 1 ? sb.y : (t == 2 ? sb.z : sb.w));
     }
-    for (int64_t base = warp0 * 8; base < total; base += nwarps * 8) {   // warp-uniform loop
-        const int64_t seg = base + (lane >> 2);
-        const bool valid = seg < total;
-        const int64_t row = valid ? seg / nseg : 0;
-        const int64_t kb = valid ? seg % nseg : 0;
+    // segment seg = row * nseg + kb of this quad; the (row, kb) pair advances by the loop
+    // stride without a division per iteration.  Segment counts fit in 32 bits: a tensor
+    // in device memory has fewer than 2^31 128-element segments.
+    const uint32_t nseg32 = (uint32_t)nseg;
+    const uint32_t stride = (uint32_t)(nwarps * 8);
+    const uint32_t seg0 = (uint32_t)(warp0 * 8) + (uint32_t)(lane >> 2);
+    const uint32_t d_row = stride / nseg32, d_kb = stride % nseg32;
+    uint32_t row_i = seg0 / nseg32, kb_i = seg0 % nseg32;
+    for (int64_t base = warp0 * 8; base < total; base += stride) {   // warp-uniform loop
+        const bool valid = (int64_t)row_i < rows_p;
+        const int64_t row = valid ? (int64_t)row_i : 0;
+        const int64_t kb = valid ? (int64_t)kb_i : 0;
+        row_i += d_row;
+        kb_i += d_kb;
+        if (kb_i >= nseg32) {
+            kb_i -= nseg32;
+            ++row_i;
+        }
         float x[32];
         if (valid) load_row32(src, row, kb * 128 + 32 * t, x);
         else {
