@@ -115,17 +115,19 @@ __device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t 
             for (int h = 0; h < 2; ++h) {
                 const uint4 w4 = sr_bits8((elem0 >> 3) + (uint64_t)(2 * g + h), pk, tag);
                 const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
-                uint32_t word = 0u;
+                // byte 3 of pb[i] = the code byte of elements 2i, 2i+1 (first in the low
+                // nibble): the top nibble of t1, and t0's top nibble shifted down by 4
+                uint32_t pb[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int e = 16 * g + 8 * h + 2 * i;
                     uint32_t t0, t1;
                     e2m1x2_sr_nib(f2_fma(f2_pack(x[e], x[e + 1]), r2, z2), (ws[i] << 12) & 0x0FFFF000u,
                                   (ws[i] >> 4) & 0x0FFFF000u, t0, t1);
-                    word |= (t0 >> (28 - 8 * i)) & (0xFu << (8 * i));
-                    word |= (t1 >> (24 - 8 * i)) & (0xF0u << (8 * i));
+                    pb[i] = (t1 & 0xF0000000u) | ((t0 >> 4) & 0x0FFFFFFFu);
                 }
-                words[2 * g + h] = word;
+                const uint32_t lo = __byte_perm(pb[0], pb[1], 0x0073u), hi = __byte_perm(pb[2], pb[3], 0x0073u);
+                words[2 * g + h] = __byte_perm(lo, hi, 0x5410u);
             }
         } else if (SR) {
             // a group whose 1 / s overflows (denormal inputs): element by element
