@@ -381,12 +381,31 @@ def oracle_sample(tokens, names=None):
     return secs, flops
 
 
+def oracle_sample_one_thread(tokens):
+    """oracle_sample in a fresh interpreter whose BLAS runs on one thread; (seconds, flops) or None."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    code = "import bench; s, f = bench.oracle_sample(%d); print(s, f)" % tokens
+    try:
+        r = subprocess.run([sys.executable, "-c", code], cwd=os.path.dirname(os.path.abspath(__file__)), env=env,
+                           capture_output=True, text=True, timeout=600)
+        s, f = r.stdout.split()[-2:]
+        return float(s), float(f)
+    except Exception:
+        return None
+
+
 def cpu_baseline():
     secs, flops = oracle_sample(128)
-    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": "oracle fwd+dX+dW (calibration, quantize, RHT+SR, re-alignment, fp64 GEMMs) of all four "
-                      "linears of the set on 128 of the 16384 tokens; %.1f s of CPU time (numpy elementwise "
-                      "single-threaded, fp64 matmul via multithreaded BLAS)" % secs}
+    out = {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+           "sample": "oracle fwd+dX+dW (calibration, quantize, RHT+SR, re-alignment, fp64 GEMMs) of all four "
+                     "linears of the set on 128 of the 16384 tokens; %.1f s of CPU time (numpy elementwise "
+                     "single-threaded, fp64 matmul via multithreaded BLAS)" % secs}
+    one = oracle_sample_one_thread(128)
+    if one is not None:
+        out["one_thread"] = {"value": round(one[1] / one[0] / 1e12, 6), "cores": 1,
+                             "sample": "the same sample with BLAS on one thread; %.1f s" % one[0]}
+    return out
 
 
 # ---------------------------------------------------------------------------
