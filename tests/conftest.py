@@ -15,7 +15,6 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
-    config.addinivalue_line("markers", "slow: full-size parity case (minutes of oracle time)")
 
 
 @pytest.fixture(scope="session")
