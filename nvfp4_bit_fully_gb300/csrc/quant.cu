@@ -163,7 +163,7 @@ __device__ __forceinline__ void load_row32(const SrcDense<__nv_bfloat16> &src, i
 // its optional RHT), into outputs of the same shape.
 // ---------------------------------------------------------------------------
 template <typename Src, int FMT, bool SR, bool RHT>
-__global__ void __launch_bounds__(256, 3) k_quant_rows(Src src, OutNv onv, OutMx omx, int64_t nseg, const PhiloxKeys pk,
+__global__ void __launch_bounds__(256, (SR || RHT) ? 3 : 4) k_quant_rows(Src src, OutNv onv, OutMx omx, int64_t nseg, const PhiloxKeys pk,
                                                     uint32_t tag, uint32_t rht_tag) {
     const int lane = threadIdx.x & 31;
     const int t = lane & 3;
