@@ -72,7 +72,10 @@ typedef enum {
 typedef enum { TJ_RTN = 0, TJ_SR = 1 } tj_round;
 typedef enum { TJ_BF16 = 0, TJ_FP32 = 1 } tj_dtype;
 
-/* NVFP4 double-block tensor (caller-owned device buffers; layout above). */
+/* NVFP4 double-block tensor (caller-owned device buffers; layout above).  Every call
+ * rejects with TJ_ERR_SHAPE an NVFP4 or MXFP8 descriptor whose padded size holds 2^31 or
+ * more 128-element blocks (roundup(rows, 128) * roundup(cols, 128) / 128); such a tensor
+ * would not fit in device memory together with its source. */
 typedef struct {
     uint8_t *codes;
     uint8_t *sf;

@@ -26,9 +26,17 @@ tj_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TJ_OK : TJ_ERR_
         if (e_ != cudaSuccess) return TJ_ERR_CUDA; \
     } while (0)
 
+// The kernels index 128-element blocks of a tensor in 32 bits.
+bool blocks_fit(int64_t rows, int64_t cols) {
+    const int64_t lim = int64_t(1) << 31;
+    if (rows > lim || cols > lim * 128) return false;
+    return round_up(rows, 128) * (round_up(cols, 128) / 128) < lim;      // both factors <= 2^31
+}
+
 tj_status check_nv(const tj_nvfp4 *q, int64_t rows, int64_t cols) {
     if (q == nullptr || q->codes == nullptr || q->sf == nullptr || q->outer == nullptr) return TJ_ERR_INVALID_ARG;
     if (q->rows != rows || q->cols != cols || rows < 0 || cols < 0) return TJ_ERR_SHAPE;
+    if (!blocks_fit(rows, cols)) return TJ_ERR_SHAPE;
     if (!al16(q->codes) || !al16(q->sf) || !al16(q->outer)) return TJ_ERR_ALIGN;
     return TJ_OK;
 }
@@ -36,6 +44,7 @@ tj_status check_nv(const tj_nvfp4 *q, int64_t rows, int64_t cols) {
 tj_status check_mx(const tj_mxfp8 *q, int64_t rows, int64_t cols) {
     if (q == nullptr || q->codes == nullptr || q->sf == nullptr) return TJ_ERR_INVALID_ARG;
     if (q->rows != rows || q->cols != cols || rows < 0 || cols < 0) return TJ_ERR_SHAPE;
+    if (!blocks_fit(rows, cols)) return TJ_ERR_SHAPE;
     if (!al16(q->codes) || !al16(q->sf)) return TJ_ERR_ALIGN;
     return TJ_OK;
 }

@@ -178,8 +178,8 @@ __global__ void __launch_bounds__(256, (SR || RHT) ? 3 : 4) k_quant_rows(Src src
         sign_word = t == 0 ? sb.x : (t == 1 ? sb.y : (t == 2 ? sb.z : sb.w));
     }
     // segment seg = row * nseg + kb of this quad; the (row, kb) pair advances by the loop
-    // stride without a division per iteration.  Segment counts fit in 32 bits: a tensor
-    // in device memory has fewer than 2^31 128-element segments.
+    // stride without a division per iteration.  Segment counts fit in 32 bits: the C ABI
+    // rejects tensors of 2^31 or more 128-element blocks.
     const uint32_t nseg32 = (uint32_t)nseg;
     const uint32_t stride = (uint32_t)(nwarps * 8);
     const uint32_t seg0 = (uint32_t)(warp0 * 8) + (uint32_t)(lane >> 2);

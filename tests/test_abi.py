@@ -87,3 +87,17 @@ def test_argument_errors_before_launch(lib):
     # calibration: k larger than K
     assert l.tj_outlier_calibrate(None, 0, 0, 8, 8, ctypes.c_void_p(256), 1, 9, ctypes.c_void_p(256),
                                   ctypes.c_void_p(256), None) == 2
+
+
+def test_block_count_limit(lib):
+    """A descriptor whose padded size holds 2^31 or more 128-element blocks is a shape error,
+    found before any launch."""
+    from nvfp4_bit_fully_gb300 import tj
+
+    l = tj.load()
+    rows, cols = 1 << 24, 1 << 14                       # 2^24 rows x 128 blocks = 2^31 blocks
+    q = tj.CNvfp4(256, 256, 256, rows, cols)
+    assert l.tj_quantize_nvfp4(ctypes.c_void_p(256), 0, rows, cols, cols, 0, None, 0, 0, 0, 0, 0, 0,
+                               ctypes.byref(q), None) == 2
+    m = tj.CMxfp8(256, 256, rows, cols)
+    assert l.tj_quantize_mxfp8(ctypes.c_void_p(256), 0, rows, cols, cols, 0, None, 0, ctypes.byref(m), None) == 2
