@@ -37,18 +37,42 @@ _E4M3_POS_BYTES = np.arange(0, 0x7F, dtype=np.uint8)          # 0x00 .. 0x7E
 _E4M3_POS_VALS = e4m3_decode(_E4M3_POS_BYTES)                  # strictly increasing
 
 
-def e4m3_ceil_byte(t):
-    """Smallest E4M3 value >= t (t >= 0, fp32), clamped to 448; returns the byte.
+# The inner scales a group may take: the normal E4M3 values 2^-6 .. 448 (bytes 0x08 .. 0x7E).
+_INNER_BYTES = np.arange(0x08, 0x7F, dtype=np.uint8)
+_INNER_VALS = e4m3_decode(_INNER_BYTES).astype(np.float32)
 
-    Reading (inner-scale rounding): the inner scale is rounded UP onto the
-    E4M3 grid so that every scaled element stays within the E2M1 range and
-    stochastic rounding needs no clipping (this keeps §2.A's E[round(x)] = x
-    exact).  t == 0 gives byte 0.
+
+def e4m3_inner_scale_byte(a_i, s_o):
+    """Inner-scale byte of 16-element groups with amax a_i inside outer blocks of scale s_o.
+
+    Reading (inner-scale rounding, technical summary §2.A): the scale is the
+    smallest normal E4M3 value sigma whose largest representable magnitude, the
+    E2M1 maximum 6 dequantized the way every consumer dequantizes it,
+    fl(fl(6 * sigma) * s_o) in fp32, is at least a_i; 448 if none is.  So:
+      * no element of the group exceeds the E2M1 range: stochastic rounding
+        never clips and stays unbiased (§2.A's E[round(x)] = x);
+      * the rule is decided on the dequantized values themselves, so a weight
+        moved onto its own dequantized value (OsciReset's reset to the bin
+        centre, §2.B) quantizes to the same scale and code again;
+      * it starts at the smallest normal E4M3 value 2^-6: with the coarser
+        subnormal steps a group maximum can round down onto the previous
+        scale's top value, and a reset would then change the group's scale.
+    a_i == 0 gives byte 0.  Brute force over all 119 candidate scales.
     """
-    t = np.asarray(t, dtype=np.float64)
-    idx = np.searchsorted(_E4M3_POS_VALS, t, side="left")
-    idx = np.minimum(idx, len(_E4M3_POS_VALS) - 1)               # clamp to 448
-    return _E4M3_POS_BYTES[idx]
+    a_i = np.asarray(a_i, dtype=np.float32)
+    s_o = np.broadcast_to(np.asarray(s_o, dtype=np.float32), a_i.shape)
+    flat_a, flat_s = a_i.reshape(-1), s_o.reshape(-1)
+    out = np.empty(flat_a.shape, dtype=np.uint8)
+    six_sigma = (np.float32(6.0) * _INNER_VALS).astype(np.float32)          # exact
+    step = 1 << 16
+    for i in range(0, flat_a.size, step):
+        a = flat_a[i:i + step]
+        with np.errstate(over="ignore"):
+            top = (six_sigma[None, :] * flat_s[i:i + step, None]).astype(np.float32)
+        ok = top >= a[:, None]
+        first = np.where(ok.any(axis=1), ok.argmax(axis=1), len(_INNER_BYTES) - 1)
+        out[i:i + step] = np.where(a > 0, _INNER_BYTES[first], 0)
+    return out.reshape(a_i.shape)
 
 
 def e4m3_rne_satfinite_byte(x):

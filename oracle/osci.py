@@ -15,8 +15,10 @@ Readings:
   * Q-hat is the fp32 dequantized RTN double-block quantization of the master
     weight, rows quantized along their length (the forward weight layout,
     without an outlier split);
-  * "bin centre" is the grid point itself, i.e. Q-hat, so a reset never
-    changes which bin the weight is in;
+  * "bin centre" is the grid point itself, i.e. Q-hat.  The quantizer decides
+    its scales on dequantized values (quant / formats.e4m3_inner_scale_byte),
+    so it is idempotent: a weight moved onto its Q-hat quantizes to the same
+    code and scales, and so do the other weights of its block;
   * reset  <=>  track and lr < lr_thr and dist_M > 0 and dist_Q > r * dist_M
     (fp32 product); 0/0 never resets;
   * after the step, w_prev <- w and Q-hat_prev <- Q-hat.

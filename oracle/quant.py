@@ -12,8 +12,11 @@ contraction dimension of the GEMM that consumes the operand.
 Readings taken where the pages are silent:
   * outer scale s_o = amax_128 / (6 * 448) in fp32 (so the largest inner block
     gets the largest inner scale); 2^-149 if that underflows to 0;
-  * inner scale s_i = smallest E4M3 value >= amax_16 / (6 * s_o), clamped to 448
-    (rounded up, so scaled elements never exceed the E2M1 maximum 6);
+  * inner scale s_i = the smallest normal E4M3 value whose dequantized top
+    value fl(fl(6 * s_i) * s_o) covers amax_16, 448 if none does (rounded up,
+    so scaled elements never exceed the E2M1 maximum 6, decided on the
+    dequantized values so that re-quantizing a dequantized tensor gives it
+    back; see formats.e4m3_inner_scale_byte);
   * element step: r = 1 / (s_i * s_o) in fp32, v = x * r, a = min(|v|, 6);
   * RTN picks the nearest grid magnitude, ties to the even code;
   * SR rounds up from the grid point below a with probability
@@ -26,7 +29,7 @@ nibble), inner scale bytes uint8 [R, Lp/16], outer scales float32 [R, Lp/128].
 """
 import numpy as np
 
-from .formats import E2M1_GRID, e2m1_decode, e4m3_ceil_byte, e4m3_decode
+from .formats import E2M1_GRID, e2m1_decode, e4m3_decode, e4m3_inner_scale_byte
 from .formats import e4m3_rne_satfinite_byte, ue8m0_decode
 from .philox import sr_uniform16
 
@@ -93,12 +96,9 @@ def quantize_nvfp4(x, mode=RTN, seed=0, tag=0, row_ids=None):
     s_o = (a_o / F32(6.0 * 448.0)).astype(F32)
     s_o = np.where((a_o > 0) & (s_o == 0), F32(2.0 ** -149), s_o).astype(F32)
 
-    # inner blocks: E4M3 scale, rounded up
+    # inner blocks: E4M3 scale, rounded up on the dequantized side
     a_i = ax.max(axis=3)                                        # [R, nb, 8]
-    m = (s_o * F32(6.0)).astype(F32)[:, :, None]
-    with np.errstate(divide="ignore", invalid="ignore"):
-        t = np.where(a_i > 0, a_i / np.where(m > 0, m, F32(1.0)), F32(0.0)).astype(F32)
-    sf = np.where(a_i > 0, e4m3_ceil_byte(t), 0).astype(np.uint8)
+    sf = e4m3_inner_scale_byte(a_i, s_o[:, :, None])
     s_i = e4m3_decode(sf).astype(F32)
 
     # element step

@@ -2,7 +2,7 @@
 
 * E4M3 decode: the OCP FP8 specification's values (golden fixture) and
   torch's independent float8_e4m3fn implementation for all 256 bytes.
-* E4M3 round-up: brute-force "smallest representable >= t".
+* Inner-scale rounding: exact (fp64) arithmetic, up to one fp32 product rounding.
 * E4M3 round-to-nearest-even: torch's fp32 -> float8_e4m3fn conversion.
 * E2M1 grid: derived from the bit-field definition (bias 1, 1 mantissa bit).
 * Philox4x32-10: the algorithm authors' published known-answer vectors.
@@ -47,28 +47,65 @@ def test_e4m3_decode_matches_torch_all_bytes():
     assert np.array_equal(ref[ok], got[ok])
 
 
-def test_e4m3_ceil_brute_force():
+def _inner_scale_cases(rng):
+    """(a_i, s_o) pairs: random magnitudes, and group maxima placed exactly on, and a few
+    fp32 ulps around, the top value 6 sigma s_o of every candidate scale sigma."""
+    s_o = np.exp2(rng.uniform(-60, 60, 4000)).astype(np.float32)
+    a = (s_o.astype(np.float64) * rng.uniform(0, 2688 * 1.2, 4000)).astype(np.float32)
+    sig = F.e4m3_decode(rng.integers(0x01, 0x7F, 6000).astype(np.uint8))
+    so2 = np.exp2(rng.uniform(-60, 60, 6000)).astype(np.float32)
+    on = (6 * sig * so2.astype(np.float64)).astype(np.float32)
+    near = [on]
+    for k in (1, 2, 3):
+        up, dn = on.copy(), on.copy()
+        for _ in range(k):
+            up = np.nextafter(up, np.float32(np.inf))
+            dn = np.nextafter(dn, np.float32(0))
+        near += [up, dn]
+    tiny = np.exp2(rng.uniform(-40, 0, 2000)) * 2688 * s_o[:2000].astype(np.float64)
+    a_all = np.concatenate([a] + near + [tiny.astype(np.float32), np.zeros(3, np.float32)])
+    s_all = np.concatenate([s_o] + [so2] * 7 + [s_o[:2000], np.ones(3, np.float32)])
+    return a_all, s_all
+
+
+def test_inner_scale_against_exact_arithmetic():
+    """The inner scale is, up to the fp32 rounding of one product, the smallest normal
+    E4M3 value sigma with 6 sigma s_o >= a_i in exact arithmetic (fp64 holds 6 sigma s_o
+    exactly: 6 sigma has at most 6 significant bits, s_o 24).  It may sit one step lower
+    only where the exact top value of that lower scale is within half an fp32 ulp below
+    a_i, so that rounding the product lifts it onto a_i."""
     rng = np.random.default_rng(0)
-    vals = np.array([F.e4m3_decode(np.uint8(b)) for b in range(0x7F)])   # 0 .. 448
-    # every representable value, its neighbours in fp32, midpoints, random values
-    t = np.concatenate([
-        vals,
-        np.nextafter(vals.astype(np.float32), np.float32(np.inf)).astype(np.float64),
-        np.nextafter(vals.astype(np.float32), np.float32(0)).astype(np.float64),
-        (vals[1:] + vals[:-1]) / 2,
-        rng.uniform(0, 448, 20000),
-        np.exp2(rng.uniform(-14, 9, 20000)),
-        [449.0, 500.0, 1e6],
-    ]).astype(np.float32).astype(np.float64)
-    t = t[t >= 0]
-    got = F.e4m3_decode(F.e4m3_ceil_byte(t))
-    for ti, gi in zip(t, got):
-        if ti > 448:
-            assert gi == 448
+    a_all, s_all = _inner_scale_cases(rng)
+    got = F.e4m3_inner_scale_byte(a_all, s_all)
+    normal = [(b, float(F.e4m3_decode(np.uint8(b)))) for b in range(0x08, 0x7F)]
+    lower = 0
+    for ai, so, gb in zip(a_all.astype(np.float64), s_all.astype(np.float64), got):
+        if ai == 0:
+            assert gb == 0
             continue
-        # brute force: the smallest representable value >= ti
-        expect = min(v for v in vals if v >= ti)
-        assert gi == expect, (ti, gi, expect)
+        fits = [b for b, v in normal if 6 * v * so >= ai]
+        exact = fits[0] if fits else 0x7E
+        if gb == exact:
+            continue
+        assert gb == exact - 1 and gb >= 0x08, (ai, so, gb, exact)
+        top = 6 * float(F.e4m3_decode(np.uint8(gb))) * so
+        assert top < ai and (ai - top) <= 0.5 * np.spacing(np.float32(ai)), (ai, so, gb)
+        lower += 1
+    assert lower > 0                     # the boundary cases were reached
+
+
+def test_inner_scale_is_normal_and_never_clips():
+    """Every nonzero group gets a normal E4M3 scale (>= 2^-6), and its maximum scaled
+    by 1/(s_i s_o) stays within the E2M1 range up to the rounding of that division."""
+    rng = np.random.default_rng(1)
+    a_all, s_all = _inner_scale_cases(rng)
+    sb = F.e4m3_inner_scale_byte(a_all, s_all)
+    nz = a_all > 0
+    assert np.all(sb[nz] >= 0x08) and np.all(sb[nz] <= 0x7E) and np.all(sb[~nz] == 0)
+    s = F.e4m3_decode(sb[nz]) * s_all[nz].astype(np.float64)
+    inside = sb[nz] < 0x7E               # 448 is a clamp: the largest amax of a block
+    v = a_all[nz].astype(np.float64) / s
+    assert np.all(v[inside] <= 6 * (1 + 2.0 ** -22))
 
 
 def test_e4m3_rne_matches_torch():

@@ -6,13 +6,18 @@ OsciReset (technical summary §2.B) is pinned by closed-form trajectories:
     reset at the first step whose learning rate is below the threshold;
   * a weight drifting monotonically away from a grid point never reaches
     risk 4 (each bin change needs at least half a bin of travel);
-  * a reset puts the master weight exactly on Q-hat and zeroes its distances.
+  * a reset puts the master weight exactly on Q-hat and zeroes its distances;
+  * a reset leaves the quantization unchanged: re-quantizing after resetting 1%,
+    50% or all of the weights, or exactly the group and block maxima, of random
+    and adversarial rows gives the same values, scales and codes (RTN is
+    idempotent), and a planted rounding slip makes this pin fail.
 Calibration (§2.C) is pinned by planted heavy channels, a full-sort brute
 force with the tie rule, and exact integer sums.
 """
 import os
 
 import numpy as np
+import pytest
 
 from oracle import calib as C
 from oracle import osci as O
@@ -98,6 +103,146 @@ def test_reset_condition_and_state_update():
             assert not mask.any()
         w = w_new
     assert state["dist_m"].max() > 0
+
+
+# ---------------------------------------------------------------------------
+# A reset lands the master weight on the centre of its current bin (technical summary
+# §2.B), so it must not move the weight's quantized value, nor that of any other weight
+# of its block: re-quantizing after any set of resets gives the same quantization.
+# ---------------------------------------------------------------------------
+def _requantize_after_reset(x, mask):
+    """Quantize x, move the masked elements onto their Q-hat, quantize again."""
+    qh, (c, s, o) = O.qhat_f32(x)
+    x2 = np.where(mask, qh, x).astype(F32)
+    qh2, (c2, s2, o2) = O.qhat_f32(x2)
+    return (qh, c, s, o), (qh2, c2, s2, o2), x2
+
+
+def _reset_invariance_failures(x, mask):
+    """Counts of everything a reset changed.  Byte for byte: the outer scales; the inner
+    scale byte of every group holding a nonzero quantized value; every code, once a
+    magnitude-0 code's sign bit is cleared (a reset element whose Q-hat is -0 becomes
+    the weight -0, which quantizes as code 0).  The only other byte that may move is the
+    scale of a group every element of which dequantizes to zero before and after: a
+    group whose elements were all reset to zero has amax 0 and scale byte 0."""
+    (qh, c, s, o), (qh2, c2, s2, o2), x2 = _requantize_after_reset(x, mask)
+    R, L = x.shape
+    zero_grp = (qh.reshape(R, -1, 16) == 0).all(axis=2) if L % 16 == 0 else None
+    live = ~zero_grp if zero_grp is not None else np.ones(s.shape, bool)[:, : L // 16]
+    strip = lambda cc: np.where((cc & 7) == 0, 0, cc)
+    return {
+        "values": int((qh2 != qh).sum()),
+        "outer": int((o2.view(np.uint32) != o.view(np.uint32)).sum()),
+        "inner": int((s2[:, : L // 16] != s[:, : L // 16])[live].sum()),
+        "codes": int((strip(c2) != strip(c)).sum()),
+        "landed": int((x2[mask] != qh[mask]).sum()),
+    }
+
+
+def _adversarial_rows(rng, R=256, L=1024):
+    """Rows built to sit on the scale rules' edges: group amaxima spread over 40 binades
+    below their block's maximum (tiny groups get the smallest normal scale), maxima
+    placed exactly on and one ulp around the top value 6 sigma s_o of a scale, ties of
+    the E2M1 grid, repeated block maxima, and signed values that round to -0."""
+    x = rng.standard_normal((R, L)).astype(F32)
+    g = np.exp2(-rng.integers(0, 40, (R, L // 16))).astype(F32)
+    x = (x.reshape(R, -1, 16) * g[:, :, None]).reshape(R, L).astype(F32)
+    qh, (c, s, o) = O.qhat_f32(x)
+    from oracle import formats as Fm
+    for r in range(0, R, 4):                       # group maxima on a scale's top value
+        b, j = rng.integers(0, L // 128), rng.integers(0, 8)
+        sig = float(Fm.e4m3_decode(np.uint8(rng.integers(0x08, 0x7E))))
+        top = F32(F32(6.0 * sig) * o[r, b])
+        seg = slice(b * 128 + j * 16, b * 128 + j * 16 + 16)
+        x[r, seg] = (x[r, seg] / np.abs(x[r, seg]).max() * top * F32(0.9)).astype(F32)
+        x[r, b * 128 + j * 16] = [top, np.nextafter(top, F32(0)), np.nextafter(top, F32(np.inf))][r % 3]
+    for r in range(1, R, 4):                       # E2M1 ties and a repeated block maximum
+        x[r, :128] = (np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0] * 16, F32) * F32(2.0 ** -5))
+        x[r, 127] = F32(6.0 * 2.0 ** -5)
+    x[2::4, 5::7] = -1e-30                         # negatives that quantize to -0
+    return x
+
+
+@pytest.mark.parametrize("frac", [0.01, 0.5, 1.0])
+def test_reset_keeps_quantization_random_weights(frac):
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((512, 1024)) * 0.02).astype(F32)
+    fails = _reset_invariance_failures(x, rng.random(x.shape) < frac)
+    assert fails == dict.fromkeys(fails, 0), fails
+
+
+@pytest.mark.parametrize("frac", [0.01, 0.5, 1.0])
+def test_reset_keeps_quantization_adversarial_rows(frac):
+    rng = np.random.default_rng(12)
+    x = _adversarial_rows(rng)
+    fails = _reset_invariance_failures(x, rng.random(x.shape) < frac)
+    assert fails == dict.fromkeys(fails, 0), fails
+
+
+def test_reset_of_group_and_block_maxima():
+    """Resetting exactly the elements that set the scales: every group maximum, and
+    every block maximum."""
+    rng = np.random.default_rng(13)
+    for x in ((rng.standard_normal((256, 1024)) * 0.02).astype(F32), _adversarial_rows(rng)):
+        ax = np.abs(x).reshape(x.shape[0], -1, 16)
+        gmax = (ax == ax.max(axis=2, keepdims=True)).reshape(x.shape)
+        bx = np.abs(x).reshape(x.shape[0], -1, 128)
+        bmax = (bx == bx.max(axis=2, keepdims=True)).reshape(x.shape)
+        for mask in (gmax, bmax):
+            fails = _reset_invariance_failures(x, mask)
+            assert fails == dict.fromkeys(fails, 0), fails
+
+
+def test_rtn_is_idempotent():
+    """Q(Q-hat(x)) = Q(x): a fully dequantized tensor quantizes back to itself (values,
+    outer scales, codes up to the sign of zero, and the scale of every live group)."""
+    rng = np.random.default_rng(14)
+    for x in ((rng.standard_normal((128, 1152)) * rng.uniform(1e-3, 1e3)).astype(F32), _adversarial_rows(rng, 64)):
+        fails = _reset_invariance_failures(x, np.ones(x.shape, bool))
+        assert fails == dict.fromkeys(fails, 0), fails
+
+
+def test_osci_reset_step_leaves_q_unchanged():
+    """Through OsciReset itself: weights oscillating across bin boundaries at a low
+    learning rate get reset, and the reset weights quantize to the Q the step emitted."""
+    rng = np.random.default_rng(15)
+    w = (rng.standard_normal((64, 512)) * 0.02).astype(F32)
+    state = O.init_state(w)
+    resets = 0
+    for t in range(12):
+        kick = (rng.standard_normal(w.shape) * 2e-3 * (1 if t % 2 == 0 else -1)).astype(F32)
+        w = (w + kick).astype(F32)
+        w, state, mask, q = O.osci_reset_step(w, state, 5e-5, 1e-4, 4.0)
+        resets += int(mask.sum())
+        _, (c2, s2, o2) = O.qhat_f32(w)
+        strip = lambda cc: np.where((cc & 7) == 0, 0, cc)
+        assert np.array_equal(strip(c2), strip(q[0])) and np.array_equal(s2, q[1])
+        assert np.array_equal(o2, q[2])
+    assert resets > 100
+
+
+def test_planted_ratio_ceiling_breaks_reset_invariance(monkeypatch):
+    """The pin above catches the rounding slip it was written for: deciding the inner
+    scale as the E4M3 ceiling of the fp32 quotient a_i / (6 s_o) (subnormal scales
+    allowed) lets a reset group maximum bump its scale one step and re-quantize its
+    neighbours.  Planted in the oracle, on the CPU."""
+    from oracle import formats as Fm
+    from oracle import quant as Qm
+    pos = np.arange(0, 0x7F, dtype=np.uint8)
+    vals = Fm.e4m3_decode(pos)
+
+    def ratio_ceiling(a_i, s_o):
+        m = (np.asarray(s_o, F32) * F32(6.0)).astype(F32)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            t = np.where(a_i > 0, (a_i / np.where(m > 0, m, F32(1))).astype(F32), F32(0))
+        idx = np.minimum(np.searchsorted(vals, t.astype(np.float64), side="left"), len(pos) - 1)
+        return np.where(a_i > 0, pos[idx], 0).astype(np.uint8)
+
+    monkeypatch.setattr(Qm, "e4m3_inner_scale_byte", ratio_ceiling)
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((512, 1024)) * 0.02).astype(F32)
+    fails = _reset_invariance_failures(x, rng.random(x.shape) < 0.01)
+    assert fails["values"] > 0 and fails["inner"] > 0
 
 
 def test_calibration_planted_channels_and_brute_force():
