@@ -45,8 +45,11 @@
  *
  * Number formats (§2.A): E2M1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}; E4M3 inner
  * scales; FP32 outer scale s_o = amax_128 / 2688 (2688 = 6 * 448); inner scale =
- * smallest E4M3 >= amax_16 / (6 s_o) (clamped to 448); elements x * (1/(s_i s_o))
- * clamped to 6, rounded to nearest-even (forward) or stochastically (backward).
+ * the smallest normal E4M3 value s_i (2^-6 .. 448) whose dequantized top value
+ * fl(fl(6 s_i) s_o) is >= amax_16, 448 if none is (decided on dequantized values, so
+ * re-quantizing a dequantized tensor gives the same codes and scales, and an OsciReset
+ * reset keeps the weight's quantized value); elements x * (1/(s_i s_o)) clamped to 6,
+ * rounded to nearest-even (forward) or stochastically (backward).
  */
 #ifndef TJ_H
 #define TJ_H
@@ -286,8 +289,10 @@ tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, c
  *     TJ_ERR_WORKSPACE before any launch.
  *   - Allocates nothing (no cudaMalloc / cudaFree, no allocating library routine).
  *   - The first call on each device looks up the scratch's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call before any
- *     stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and keeps it for later calls;
+ *     make that first call before any stream capture.  The address belongs to the
+ *     device's primary context: do not call this entry point after a cudaDeviceReset in
+ *     the same process, nor with another driver context current.
  *   - All calls share the one scratch array, which keeps the last call's contents; calls
  *     whose executions overlap on the GPU (other streams, other threads) race on it, so
  *     serialise them.  Nothing needs clearing: each call writes all scratch it reads. */

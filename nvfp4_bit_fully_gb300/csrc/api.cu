@@ -26,12 +26,18 @@ tj_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TJ_OK : TJ_ERR_
         if (e_ != cudaSuccess) return TJ_ERR_CUDA; \
     } while (0)
 
-// The kernels index 128-element blocks of a tensor in 32 bits.
+// Fewer than 2^31 128-element blocks per tensor: the row quantizers (k_quant_rows)
+// walk the (row, block) pairs of a tensor with 32-bit counters.  Every other index
+// (element, byte, scale-tile and MXFP8 group offsets) is formed in 64 bits.
 bool blocks_fit(int64_t rows, int64_t cols) {
     const int64_t lim = int64_t(1) << 31;
     if (rows > lim || cols > lim * 128) return false;
     return round_up(rows, 128) * (round_up(cols, 128) / 128) < lim;      // both factors <= 2^31
 }
+
+// The column (transposed) quantizers launch one grid row per 128 output columns, and
+// a grid has at most 65535 rows: at most 8,388,480 output columns (input rows).
+bool cols_grid_fits(int64_t out_cols) { return round_up(out_cols, 128) / 128 <= 65535; }
 
 tj_status check_nv(const tj_nvfp4 *q, int64_t rows, int64_t cols) {
     if (q == nullptr || q->codes == nullptr || q->sf == nullptr || q->outer == nullptr) return TJ_ERR_INVALID_ARG;
@@ -121,6 +127,7 @@ tj_status tj_quantize_nvfp4(const void *x, int dtype, int64_t rows_x, int64_t co
     const int64_t ncols = sel ? n_sel : cols_x;
     if (sel && (n_sel < 0 || n_sel > cols_x)) return TJ_ERR_SHAPE;
     const int64_t orows = along_cols ? ncols : rows_x, ocols = along_cols ? rows_x : ncols;
+    if (along_cols && !cols_grid_fits(ocols)) return TJ_ERR_SHAPE;
     const tj_status st = check_nv(out, orows, ocols);
     if (st != TJ_OK) return st;
     return cuda_status(launch_quant_nv_dense(x, dtype, rows_x, ncols, ld, along_cols, sel, mode, rht, seed, tag,
@@ -135,6 +142,7 @@ tj_status tj_quantize_mxfp8(const void *x, int dtype, int64_t rows_x, int64_t co
     const int64_t ncols = sel ? n_sel : cols_x;
     if (sel && (n_sel < 0 || n_sel > cols_x)) return TJ_ERR_SHAPE;
     const int64_t orows = along_cols ? ncols : rows_x, ocols = along_cols ? rows_x : ncols;
+    if (along_cols && !cols_grid_fits(ocols)) return TJ_ERR_SHAPE;
     const tj_status st = check_mx(out, orows, ocols);
     if (st != TJ_OK) return st;
     return cuda_status(launch_quant_mx_dense(x, dtype, rows_x, ncols, ld, along_cols, sel, *out,
@@ -152,6 +160,7 @@ tj_status tj_quantize_nvfp4_mxfp8(const void *x, int dtype, int64_t rows_x, int6
     const int64_t ncols = sel ? n_sel : cols_x;
     if (sel && (n_sel < 0 || n_sel > cols_x)) return TJ_ERR_SHAPE;
     const int64_t orows = along_cols ? ncols : rows_x, ocols = along_cols ? rows_x : ncols;
+    if (along_cols && !cols_grid_fits(ocols)) return TJ_ERR_SHAPE;
     tj_status st = check_nv(out, orows, ocols);
     if (st == TJ_OK) st = check_mx(out8, orows, ocols);
     if (st != TJ_OK) return st;
@@ -188,6 +197,7 @@ tj_status tj_requantize_nvfp4(const tj_nvfp4 *in, int mode, int rht, uint64_t se
     tj_status st = check_nv(in, in->rows, in->cols);
     if (st == TJ_OK) st = check_nv(out, in->cols, in->rows);
     if (st != TJ_OK) return st;
+    if (!cols_grid_fits(in->rows)) return TJ_ERR_SHAPE;
     return cuda_status(launch_realign_nv(*in, *out, mode, rht, seed, tag, rht_tag, static_cast<cudaStream_t>(stream)));
 }
 
@@ -196,6 +206,7 @@ tj_status tj_requantize_mxfp8(const tj_mxfp8 *in, tj_mxfp8 *out, void *stream) {
     tj_status st = check_mx(in, in->rows, in->cols);
     if (st == TJ_OK) st = check_mx(out, in->cols, in->rows);
     if (st != TJ_OK) return st;
+    if (!cols_grid_fits(in->rows)) return TJ_ERR_SHAPE;
     return cuda_status(launch_realign_mx(*in, *out, static_cast<cudaStream_t>(stream)));
 }
 
@@ -342,7 +353,7 @@ tj_status tj_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, c
     tj_status st = check_nv(wq, N, kn);
     if (st == TJ_OK && k > 0) st = check_mx(w8, N, k);
     if (st != TJ_OK) return st;
-    if (lddy < N || lddx < K) return TJ_ERR_SHAPE;
+    if (lddy < N || lddx < K || !cols_grid_fits(N)) return TJ_ERR_SHAPE;
     const size_t need = tj_workspace_size(TJ_OP_BWD_DX, M, N, K, k);
     if (workspace == nullptr || ws_bytes < need) return TJ_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return TJ_ERR_ALIGN;
@@ -385,7 +396,7 @@ tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, c
     tj_status st = check_nv(xq, M, kn);
     if (st == TJ_OK && k > 0) st = check_mx(x8, M, k);
     if (st != TJ_OK) return st;
-    if (lddy < N || lddw < K) return TJ_ERR_SHAPE;
+    if (lddy < N || lddw < K || !cols_grid_fits(M)) return TJ_ERR_SHAPE;
     const size_t need = tj_workspace_size(TJ_OP_BWD_DW, M, N, K, k);
     if (workspace == nullptr || ws_bytes < need) return TJ_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return TJ_ERR_ALIGN;

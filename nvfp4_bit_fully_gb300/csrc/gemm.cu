@@ -11,9 +11,8 @@
 // The FP8 slice (kind::mxf8f6f4, UE8M0 per 32) has only power-of-two scales and
 // accumulates over its whole K into one tensor-memory buffer added at the end.
 //
-// Persistent CTAs (one per SM) walk the 128 x 128 output tiles.  (A version with 2 x 2
-// clusters sharing operand tiles by TMA multicast measured slower on GB300 and was
-// removed.)  12 warps:
+// Persistent CTAs (one per SM) walk the 128 x 128 output tiles; every CTA loads its
+// own operand tiles.  12 warps:
 //   warps 0-2   TMA producers (one lane each; stage it is issued by warp it % 3): the
 //               operand tiles (128-byte rows, 128-byte swizzle) and their scale-factor
 //               tiles into a 5-stage ring, and the FP32 outer scales of the stage's

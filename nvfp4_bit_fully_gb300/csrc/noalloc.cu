@@ -15,6 +15,8 @@
 // the array's name is only a host-side stand-in, not a device address, so the
 // device address is looked up once per device with cudaGetSymbolAddress (with that
 // device current) and cached; that lookup happens on the first call on each device.
+// The cached address belongs to the device's primary context, so the entry point is
+// not for use after a cudaDeviceReset in the same process or under another context.
 // No cudaMalloc, cudaFree or allocating library routine is called.
 #include <mutex>
 

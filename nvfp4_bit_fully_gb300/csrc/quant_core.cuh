@@ -72,8 +72,9 @@ struct NvSeg {
 };
 
 // Double-block NVFP4 quantization of one 128-segment (§2.A), readings as in tj.h:
-// s_o = amax/2688 (2^-149 if that underflows), s_i = E4M3 ceiling of
-// amax_16 / (6 s_o), v = x * (1/(s_i s_o)); RTN = nearest E2M1 value, ties even,
+// s_o = amax/2688 (2^-149 if that underflows), s_i = inner_scale_byte (the
+// smallest normal E4M3 scale whose dequantized top value covers amax_16),
+// v = x * (1/(s_i s_o)); RTN = nearest E2M1 value, ties even,
 // saturated at 6 (hardware conversion); SR = exact integer test on min(|v|, 6)
 // with the 16-bit uniforms of Philox call (elem0 + 8q) >> 3.  A zero element,
 // or any element of a group whose scale is zero, gets code 0.  elem0 = index of
@@ -101,7 +102,7 @@ __device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t 
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
         uint32_t sb = 0u;
-        if (a_i[g] > 0.0f) sb = e4m3_ceil_byte(__fdiv_rn(a_i[g], m6));
+        if (a_i[g] > 0.0f) sb = inner_scale_byte(a_i[g], s_o, m6);
         out.sf2 |= sb << (8 * g);
         const float s = __fmul_rn(e4m3_to_float(sb), s_o);
         const float r = s > 0.0f ? __fdiv_rn(1.0f, s) : 0.0f;

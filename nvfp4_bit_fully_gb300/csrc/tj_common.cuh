@@ -85,8 +85,6 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t b) {
 }
 
 // Smallest E4M3 value >= t (t >= 0), clamped to 448; returns its byte.
-// Inner-scale reading: rounding the group scale UP keeps |x / s| <= 6, so no
-// element is clipped and stochastic rounding stays unbiased.
 __device__ __forceinline__ uint32_t e4m3_ceil_byte(float t) {
     if (!(t > 0.0f)) return 0u;
     if (t >= 448.0f) return 0x7Eu;
@@ -104,6 +102,24 @@ __device__ __forceinline__ uint32_t e4m3_ceil_byte(float t) {
     }
     const uint32_t byte = (eb << 3) | m3;
     return byte > 0x7Eu ? 0x7Eu : byte;
+}
+
+// Inner-scale byte of a 16-element group with amax a_i > 0 in an outer block of
+// scale s_o (m6 = fl(6 s_o)).  Reading of §2.A's group scale: the smallest normal
+// E4M3 value sigma (2^-6 .. 448) whose top value fl(fl(6 sigma) s_o), dequantized
+// the way every consumer dequantizes, is >= a_i; 448 if none is.  Rounding up keeps
+// |x / s| <= 6, so no element clips and stochastic rounding stays unbiased; deciding
+// on the dequantized value makes the quantizer idempotent, so an OsciReset reset
+// (§2.B: the weight moved onto its own Q-hat) re-quantizes to the same code and
+// scales.  The E4M3 ceiling of the quotient a_i / m6 is within one step of the
+// answer when the products are normal fp32 numbers; the two walks settle that step
+// (and go further only where the products are fp32 subnormals, at most 118 steps).
+__device__ __forceinline__ uint32_t inner_scale_byte(float a_i, float s_o, float m6) {
+    uint32_t sb = e4m3_ceil_byte(__fdiv_rn(a_i, m6));
+    if (sb < 0x08u) sb = 0x08u;                      // the smallest normal E4M3 value, 2^-6
+    while (sb < 0x7Eu && __fmul_rn(__fmul_rn(6.0f, e4m3_to_float(sb)), s_o) < a_i) ++sb;
+    while (sb > 0x08u && __fmul_rn(__fmul_rn(6.0f, e4m3_to_float(sb - 1u)), s_o) >= a_i) --sb;
+    return sb;
 }
 
 // ---------------------------------------------------------------------------

@@ -101,3 +101,24 @@ def test_block_count_limit(lib):
                                ctypes.byref(q), None) == 2
     m = tj.CMxfp8(256, 256, rows, cols)
     assert l.tj_quantize_mxfp8(ctypes.c_void_p(256), 0, rows, cols, cols, 0, None, 0, ctypes.byref(m), None) == 2
+
+
+def test_column_grid_limit(lib):
+    """The transposed quantizers launch one grid row per 128 output columns (at most
+    65535): a column quantization with more than 8,388,480 input rows, and the
+    backward calls that would need one, are shape errors found before any launch."""
+    from nvfp4_bit_fully_gb300 import tj
+
+    l = tj.load()
+    rows, cols = 65535 * 128 + 1, 128                   # one 128-block too many output columns
+    q = tj.CNvfp4(256, 256, 256, cols, rows)            # transposed output [cols, rows]
+    assert l.tj_quantize_nvfp4(ctypes.c_void_p(256), 0, rows, cols, cols, 1, None, 0, 0, 0, 0, 0, 0,
+                               ctypes.byref(q), None) == 2
+    m = tj.CMxfp8(256, 256, cols, rows)
+    assert l.tj_quantize_mxfp8(ctypes.c_void_p(256), 0, rows, cols, cols, 1, None, 0, ctypes.byref(m), None) == 2
+    src = tj.CNvfp4(256, 256, 256, rows, cols)
+    assert l.tj_requantize_nvfp4(ctypes.byref(src), 1, 1, 0, 3, 0x100, ctypes.byref(q), None) == 2
+    # dW over more tokens than the column grid holds
+    xq = tj.CNvfp4(256, 256, 256, rows, 128)
+    assert l.tj_linear_bwd_dw(ctypes.c_void_p(256), rows, 128, 128, ctypes.byref(xq), None, None, None, 0, 1,
+                              ctypes.c_void_p(256), 128, ctypes.c_void_p(256), 1 << 40, None) == 2

@@ -125,6 +125,39 @@ def test_osci_reset_in_place_q(tj):
     assert_nvfp4_equal(q, Q.quantize_nvfp4(w2_before, 0), "in-place Q")
 
 
+def test_osci_reset_keeps_q_on_the_gpu(tj):
+    """A reset moves a weight onto its bin centre without moving its quantized value
+    (§2.B): after a pass that resets many weights, the GPU quantizer applied to the
+    reset weights gives back the Q the pass emitted (codes up to the sign of zero),
+    and both equal the oracle's quantization of the pre-reset weights."""
+    rows, cols = 256, 1024
+    rng = np.random.default_rng(77)
+    w0 = (rng.standard_normal((rows, cols)) * 0.02).astype(np.float32)
+    w1 = (w0 + rng.standard_normal((rows, cols)).astype(np.float32) * np.float32(2e-3)).astype(np.float32)
+    w_dev = torch.from_numpy(w1.copy()).cuda()
+    w_prev = torch.from_numpy(w0.copy()).cuda()
+    dq = torch.zeros_like(w_dev)
+    dm = torch.zeros_like(w_dev)
+    q_prev = tj.quantize_nvfp4(w_prev)
+    q_out = tj.NVFP4.empty(rows, cols)
+    mask = torch.empty(rows * (cols // 32), dtype=torch.int32, device="cuda")
+    # risk threshold 0.5 and lr below the threshold: a large share of the weights reset
+    tj.osci_reset(w_dev, w_prev, dq, dm, q_prev, q_out, mask, 1e-5, 1e-4, 0.5)
+    q_again = tj.quantize_nvfp4(w_dev)
+    torch.cuda.synchronize()
+    m = _mask_bits(mask, rows, cols)
+    assert m.sum() > rows * cols // 100
+    ref = Q.quantize_nvfp4(w1, 0)
+    assert_nvfp4_equal(q_out, ref, "Q of the pass")
+    from layouts import nvfp4_to_logical
+    a, b = nvfp4_to_logical(q_again), nvfp4_to_logical(q_out)
+    strip = lambda c: np.where((c & 7) == 0, 0, c)
+    assert np.array_equal(strip(a[0]), strip(b[0])), "codes moved by a reset"
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2]), "scales moved by a reset"
+    qh = Q.dequantize_nvfp4_f32(*ref)
+    assert np.array_equal(w_dev.cpu().numpy()[m], qh[m])
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_calibration_bit_exact(tj, dtype):
     g = torch.Generator().manual_seed(5)

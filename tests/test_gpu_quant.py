@@ -98,7 +98,7 @@ def test_quantize_channel_selection(tj, along):
 @pytest.mark.parametrize("along", [False, True])
 def test_quantize_mxfp8_bit_exact(tj, rows, cols, dtype, along):
     x = _input(rows, cols, dtype, rows * 7 + cols)
-    x[1, 5] = 1e-30 if dtype == torch.float32 else 0.0      # tiny values -> E4M3 subnormals / zero
+    x[1, 5] = 1e-30 if dtype == torch.float32 else 0.0      # tiny values -> the smallest normal inner scale / zero
     q8 = tj.quantize_mxfp8(x.cuda(), along_cols=along)
     torch.cuda.synchronize()
     xf = x.float().numpy()

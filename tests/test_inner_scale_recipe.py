@@ -1,0 +1,88 @@
+"""CPU pin of the kernels' inner-scale recipe against the oracle's definition.
+
+The kernels do not search all 119 candidate scales.  They take the E4M3 ceiling of
+the fp32 quotient a_i / fl(6 s_o), floor it at the smallest normal value (byte
+0x08), then walk up while the top value fl(fl(6 sigma) s_o) is below a_i and down
+while the next lower scale's top value still covers a_i.  That recipe is restated
+here in numpy and checked equal to ``oracle.formats.e4m3_inner_scale_byte`` (the
+brute-force definition) on group maxima placed on and around every scale's top
+value, random magnitudes over the fp32 range, and fp32-subnormal products.
+"""
+import numpy as np
+
+from oracle import formats as F
+
+F32 = np.float32
+_ALL = np.arange(0, 0x7F, dtype=np.uint8)
+_ALL_VALS = F.e4m3_decode(_ALL)
+
+
+def _recipe(a_i, s_o):
+    m6 = (s_o * F32(6.0)).astype(F32)
+    with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
+        t = (a_i / m6).astype(F32)
+    idx = np.minimum(np.searchsorted(_ALL_VALS, t.astype(np.float64), side="left"), 0x7E)
+    sb = np.maximum(_ALL[idx].astype(np.int64), 0x08)
+
+    def top(b):
+        v = F.e4m3_decode(b.astype(np.uint8)).astype(F32)
+        with np.errstate(over="ignore"):
+            return ((F32(6.0) * v).astype(F32) * s_o).astype(F32)
+
+    for _ in range(120):
+        up = (sb < 0x7E) & (top(sb) < a_i)
+        if not up.any():
+            break
+        sb = np.where(up, sb + 1, sb)
+    for _ in range(120):
+        dn = (sb > 0x08) & (top(np.maximum(sb - 1, 0)) >= a_i)
+        if not dn.any():
+            break
+        sb = np.where(dn, sb - 1, sb)
+    return np.where(a_i > 0, sb, 0).astype(np.uint8)
+
+
+def _cases(rng, n):
+    s_o = np.exp2(rng.uniform(-126, 110, n)).astype(F32)
+    sig = F.e4m3_decode(rng.integers(0x01, 0x7F, n).astype(np.uint8))
+    on = (6 * sig * s_o.astype(np.float64)).astype(F32)
+    out_a, out_s = [on], [s_o]
+    for k in (1, 2, 5):
+        up, dn = on.copy(), on.copy()
+        for _ in range(k):
+            up, dn = np.nextafter(up, F32(np.inf)), np.nextafter(dn, F32(0))
+        out_a += [up, dn]
+        out_s += [s_o, s_o]
+    rnd = (s_o.astype(np.float64) * np.exp2(rng.uniform(-30, np.log2(2688 * 1.1), n))).astype(F32)
+    out_a.append(rnd)
+    out_s.append(s_o)
+    # fp32-subnormal products: tiny outer scales (down to 2^-149) with amaxima near them
+    s_t = np.exp2(-rng.integers(130, 150, n).astype(np.float64)).astype(F32)
+    a_t = (s_t.astype(np.float64) * rng.uniform(0, 3000, n)).astype(F32)
+    out_a.append(a_t)
+    out_s.append(s_t)
+    return np.concatenate(out_a), np.concatenate(out_s)
+
+
+def test_recipe_equals_definition():
+    rng = np.random.default_rng(21)
+    a, s = _cases(rng, 100000)
+    keep = np.isfinite(a)
+    a, s = a[keep], s[keep]
+    assert np.array_equal(_recipe(a, s), F.e4m3_inner_scale_byte(a, s))
+
+
+def test_recipe_walks_at_most_one_step_for_normal_products():
+    """Where every product is a normal fp32 number, the quotient's ceiling (floored)
+    is at most one step from the answer, so the kernels' walks take one step."""
+    rng = np.random.default_rng(22)
+    a, s = _cases(rng, 50000)
+    ok = np.isfinite(a) & (s >= F32(2.0 ** -110)) & (a > 0)
+    a, s = a[ok], s[ok]
+    m6 = (s * F32(6.0)).astype(F32)
+    t = (a / m6).astype(F32)
+    idx = np.minimum(np.searchsorted(_ALL_VALS, t.astype(np.float64), side="left"), 0x7E)
+    cand = np.maximum(_ALL[idx].astype(np.int64), 0x08)
+    got = F.e4m3_inner_scale_byte(a, s).astype(np.int64)
+    assert np.abs(got - cand).max() <= 1
+    assert (got != cand).any()

@@ -3,10 +3,13 @@ that cannot allocate device memory when the backward runs (code below the
 framework's allocator, or deployments that only use buffers registered up front).
 It uses a fixed scratch array inside the library instead of a caller workspace.
 
-Through the C ABI, two calls in a row must each give the same dX as the regular
-tj_linear_bwd_dx with a caller workspace, within the GEMM tolerance the other
-tests use (2e-3 * sum|a||b| against the oracle's operands) and in fact bit for bit;
-a problem larger than the fixed scratch is rejected before any launch.  This file
+Through the C ABI: a call of another shape, with another seed and the other
+outlier setting, first leaves the shared scratch holding unrelated bytes.  Then
+two calls in a row must each give the oracle's dX (oracle.linear.bwd_dx) within
+the GEMM tolerance the other tests use, 2e-3 * sum|a||b| over the oracle's
+quantized operands, and the same bits as tj_linear_bwd_dx with a caller
+workspace; so no byte the previous call left in the scratch reaches the result.
+A problem larger than the fixed scratch is rejected before any launch.  This file
 is named to be collected last, and passes alone or after the other tests.
 """
 import ctypes
@@ -16,7 +19,6 @@ import pytest
 import torch
 
 from layouts import abs_product, assert_gemm_close
-from nvfp4_bit_fully_gb300 import workloads
 from oracle import linear as OL
 
 pytestmark = pytest.mark.gpu
@@ -46,12 +48,13 @@ def _call_noalloc(tj, dy, wq, w8, ni, oi, seed, out):
     assert code == 0, tj.STATUS.get(code, code)
 
 
-@pytest.mark.parametrize("with_outliers", [False, True])
-def test_noalloc_matches_workspace_version_twice(tj, with_outliers):
-    X, W, dY = workloads.tiny(seed=0)
-    K = W.shape[1]
+def _problem(tj, M, N, K, with_outliers, seed):
+    """Inputs of one backward: dY, the forward-quantized weight, and the channel lists."""
+    g = torch.Generator().manual_seed(seed)
+    W = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16)
+    dY = (torch.randn(M, N, generator=g) * 1e-3).to(torch.bfloat16)
     if with_outliers:
-        outl = np.arange(3, K, 10)[:52]
+        outl = np.arange(3, K, 10)[: max(1, K // 10)]
         normal = OL.normal_channels(K, outl)
         ni = torch.from_numpy(normal.astype(np.int32)).cuda()
         oi = torch.from_numpy(outl.astype(np.int32)).cuda()
@@ -61,28 +64,37 @@ def test_noalloc_matches_workspace_version_twice(tj, with_outliers):
         outl = np.array([], dtype=np.int64)
         ni = oi = w8 = None
         wq = tj.quantize_nvfp4(W.cuda())
+    return W, dY, outl, wq, w8, ni, oi
+
+
+@pytest.mark.parametrize("with_outliers", [False, True])
+def test_noalloc_matches_oracle_and_workspace_version_twice(tj, with_outliers):
+    M, N, K, seed = 256, 512, 512, 77
+    W, dY, outl, wq, w8, ni, oi = _problem(tj, M, N, K, with_outliers, seed=0)
     dyd = dY.cuda()
-    seed = 77
     ref = tj.linear_bwd_dx(dyd, wq, w8, ni, oi, seed=seed, out_dtype=torch.float32)
+    # a call of another shape, seed and outlier setting fills the scratch with other bytes
+    W2, dY2, _, wq2, w82, ni2, oi2 = _problem(tj, 384, 640, 768, not with_outliers, seed=5)
+    junk = torch.empty(384, 768, device="cuda")
+    _call_noalloc(tj, dY2.cuda(), wq2, w82, ni2, oi2, 991, junk)
     torch.cuda.synchronize()
     ref_np = ref.cpu().numpy()
-    # tolerance as in the other GEMM tests: 2e-3 * sum|a||b| over the quantized operands
-    _, _, fw = OL.forward(X.float().numpy(), W.float().numpy(), outl)
-    s_dy, s_w, _, _ = OL.bwd_dx_operands(dY.float().numpy(), fw, seed)
+    # the oracle's dX and the tolerance of the other GEMM tests: 2e-3 * sum|a||b| over the
+    # quantized operands (FP4 product on the normal channels, FP8 slice on the outliers)
+    _, _, fw = OL.forward(np.zeros((1, K), np.float32), W.float().numpy(), outl)
+    dx_oracle = OL.bwd_dx(dY.float().numpy(), fw, outl, seed)
+    s_dy, s_w, q8_dy, q8_w = OL.bwd_dx_operands(dY.float().numpy(), fw, seed)
     bound = np.zeros(ref_np.shape)
     bound[:, OL.normal_channels(K, outl)] = abs_product(s_dy, s_w, OL.ALPHA_RHT)[:, : K - len(outl)]
     if len(outl):
         from layouts import abs_product_fp8
-        from oracle import quant as Q
-        q8_dy = Q.quantize_mxfp8(dY.float().numpy())
-        q8_w = Q.quantize_mxfp8(OL.deq_outlier_f32(fw).T)
         bound[:, outl] = abs_product_fp8(q8_dy, q8_w)[:, : len(outl)]
     for call in range(2):                                      # two calls in a row share the scratch
         out = torch.full_like(ref, float("nan"))
         _call_noalloc(tj, dyd, wq, w8, ni, oi, seed, out)
         torch.cuda.synchronize()
         got = out.cpu().numpy()
-        assert_gemm_close(got, ref_np, bound, what="noalloc call %d" % call)
+        assert_gemm_close(got, dx_oracle, bound, what="noalloc call %d" % call)
         assert np.array_equal(got, ref_np)
     tj.device_status()
 
