@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(256, ADAMW ? 4 : 5) k_osci_reset(float *w, flo
             float s_o = __fdiv_rn(a_o, 2688.0f);
             if (a_o > 0.0f && s_o == 0.0f) s_o = __uint_as_float(1u);
             uint32_t sb = 0u;
-            if (a_i > 0.0f) sb = inner_scale_byte(a_i, s_o, __fmul_rn(s_o, 6.0f));
+            if (a_i > 0.0f) sb = inner_scale_byte(a_i, s_o, rcp_approx(__fmul_rn(s_o, 6.0f)));
             const float s_i = e4m3_to_float(sb);
             const float s = __fmul_rn(s_i, s_o);
             uint32_t code16 = 0u;

@@ -93,7 +93,7 @@ __device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t 
 
     float s_o = __fdiv_rn(a_o, 2688.0f);
     if (a_o > 0.0f && s_o == 0.0f) s_o = __uint_as_float(1u);     // 2^-149
-    const float m6 = __fmul_rn(s_o, 6.0f);
+    const float inv_m6 = rcp_approx(__fmul_rn(s_o, 6.0f));    // first guess of the inner scales
 
     NvSeg out;
     out.s_o = s_o;
@@ -102,7 +102,7 @@ __device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t 
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
         uint32_t sb = 0u;
-        if (a_i[g] > 0.0f) sb = inner_scale_byte(a_i[g], s_o, m6);
+        if (a_i[g] > 0.0f) sb = inner_scale_byte(a_i[g], s_o, inv_m6);
         out.sf2 |= sb << (8 * g);
         const float s = __fmul_rn(e4m3_to_float(sb), s_o);
         const float r = s > 0.0f ? __fdiv_rn(1.0f, s) : 0.0f;

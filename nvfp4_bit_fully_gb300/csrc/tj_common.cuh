@@ -104,21 +104,35 @@ __device__ __forceinline__ uint32_t e4m3_ceil_byte(float t) {
     return byte > 0x7Eu ? 0x7Eu : byte;
 }
 
+// Value of a normal E4M3 byte (0x08 .. 0x7E): exponent and mantissa bits moved into
+// place and the exponent rebiased (7 -> 127) by one add.
+__device__ __forceinline__ float e4m3_normal_to_float(uint32_t b) { return __uint_as_float((b << 20) + 0x3C000000u); }
+
+// Approximate reciprocal (one special-function instruction); only used for a first
+// guess that inner_scale_byte corrects exactly.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // Inner-scale byte of a 16-element group with amax a_i > 0 in an outer block of
-// scale s_o (m6 = fl(6 s_o)).  Reading of §2.A's group scale: the smallest normal
-// E4M3 value sigma (2^-6 .. 448) whose top value fl(fl(6 sigma) s_o), dequantized
-// the way every consumer dequantizes, is >= a_i; 448 if none is.  Rounding up keeps
-// |x / s| <= 6, so no element clips and stochastic rounding stays unbiased; deciding
-// on the dequantized value makes the quantizer idempotent, so an OsciReset reset
-// (§2.B: the weight moved onto its own Q-hat) re-quantizes to the same code and
-// scales.  The E4M3 ceiling of the quotient a_i / m6 is within one step of the
-// answer when the products are normal fp32 numbers; the two walks settle that step
-// (and go further only where the products are fp32 subnormals, at most 118 steps).
-__device__ __forceinline__ uint32_t inner_scale_byte(float a_i, float s_o, float m6) {
-    uint32_t sb = e4m3_ceil_byte(__fdiv_rn(a_i, m6));
+// scale s_o.  Reading of §2.A's group scale: the smallest normal E4M3 value sigma
+// (2^-6 .. 448) whose top value fl(fl(6 sigma) s_o), dequantized the way every
+// consumer dequantizes, is >= a_i; 448 if none is.  Rounding up keeps |x / s| <= 6,
+// so no element clips and stochastic rounding stays unbiased; deciding on the
+// dequantized value makes the quantizer idempotent, so an OsciReset reset (§2.B: the
+// weight moved onto its own Q-hat) re-quantizes to the same code and scales.
+// The search starts from the E4M3 ceiling of a_i * inv_m6 (inv_m6 ~ 1 / fl(6 s_o),
+// any approximation), floored at the smallest normal value; the two walks then reach
+// the exact answer whatever the start (the top value grows with sigma).  From a
+// start within an ulp or two of the quotient they take at most one step; they go
+// further only where the products are fp32 subnormals (at most 118 steps).
+__device__ __forceinline__ uint32_t inner_scale_byte(float a_i, float s_o, float inv_m6) {
+    uint32_t sb = e4m3_ceil_byte(__fmul_rn(a_i, inv_m6));
     if (sb < 0x08u) sb = 0x08u;                      // the smallest normal E4M3 value, 2^-6
-    while (sb < 0x7Eu && __fmul_rn(__fmul_rn(6.0f, e4m3_to_float(sb)), s_o) < a_i) ++sb;
-    while (sb > 0x08u && __fmul_rn(__fmul_rn(6.0f, e4m3_to_float(sb - 1u)), s_o) >= a_i) --sb;
+    while (sb < 0x7Eu && __fmul_rn(__fmul_rn(6.0f, e4m3_normal_to_float(sb)), s_o) < a_i) ++sb;
+    while (sb > 0x08u && __fmul_rn(__fmul_rn(6.0f, e4m3_normal_to_float(sb - 1u)), s_o) >= a_i) --sb;
     return sb;
 }
 

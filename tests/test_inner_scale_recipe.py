@@ -1,12 +1,14 @@
 """CPU pin of the kernels' inner-scale recipe against the oracle's definition.
 
 The kernels do not search all 119 candidate scales.  They take the E4M3 ceiling of
-the fp32 quotient a_i / fl(6 s_o), floor it at the smallest normal value (byte
-0x08), then walk up while the top value fl(fl(6 sigma) s_o) is below a_i and down
-while the next lower scale's top value still covers a_i.  That recipe is restated
-here in numpy and checked equal to ``oracle.formats.e4m3_inner_scale_byte`` (the
-brute-force definition) on group maxima placed on and around every scale's top
-value, random magnitudes over the fp32 range, and fp32-subnormal products.
+a first guess of the quotient a_i / fl(6 s_o) (a_i times an approximate reciprocal),
+floor it at the smallest normal value (byte 0x08), then walk up while the top value
+fl(fl(6 sigma) s_o) is below a_i and down while the next lower scale's top value
+still covers a_i.  That recipe is restated here in numpy, from the exact quotient
+and from starts perturbed by a few ulps as an approximate reciprocal gives them, and
+checked equal to ``oracle.formats.e4m3_inner_scale_byte`` (the brute-force
+definition) on group maxima placed on and around every scale's top value, random
+magnitudes over the fp32 range, and fp32-subnormal products.
 """
 import numpy as np
 
@@ -17,10 +19,12 @@ _ALL = np.arange(0, 0x7F, dtype=np.uint8)
 _ALL_VALS = F.e4m3_decode(_ALL)
 
 
-def _recipe(a_i, s_o):
+def _recipe(a_i, s_o, rel=None):
     m6 = (s_o * F32(6.0)).astype(F32)
     with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
         t = (a_i / m6).astype(F32)
+        if rel is not None:                         # a first guess off by a few ulps
+            t = (t.astype(np.float64) * (1.0 + rel)).astype(F32)
     idx = np.minimum(np.searchsorted(_ALL_VALS, t.astype(np.float64), side="left"), 0x7E)
     sb = np.maximum(_ALL[idx].astype(np.int64), 0x08)
 
@@ -69,7 +73,10 @@ def test_recipe_equals_definition():
     a, s = _cases(rng, 100000)
     keep = np.isfinite(a)
     a, s = a[keep], s[keep]
-    assert np.array_equal(_recipe(a, s), F.e4m3_inner_scale_byte(a, s))
+    ref = F.e4m3_inner_scale_byte(a, s)
+    assert np.array_equal(_recipe(a, s), ref)
+    assert np.array_equal(_recipe(a, s, rng.uniform(-2.0 ** -20, 2.0 ** -20, a.size)), ref)
+    assert np.array_equal(_recipe(a, s, rng.uniform(-0.3, 0.3, a.size)), ref)       # any start
 
 
 def test_recipe_walks_at_most_one_step_for_normal_products():
