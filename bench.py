@@ -275,8 +275,8 @@ MX_B = 1.0 + 1.0 / 32                   # bytes per MXFP8 element (E4M3 + UE8M0)
 # ---------------------------------------------------------------------------
 # secondary measurements (outside the timed step loop)
 # ---------------------------------------------------------------------------
-def time_kernel(fn, stream, reps, flush=None, warmup=3):
-    """Average device ms of fn() over reps launches, the L2 flushed before each
+def time_kernel(fn, stream, reps=50, flush=None, warmup=10):
+    """Median device ms of fn() over reps launches, the L2 flushed before each
     (outside the events).  Every rep is enqueued before the first is waited on,
     so host launch latency never shows up as device time."""
     for _ in range(warmup):
@@ -293,7 +293,7 @@ def time_kernel(fn, stream, reps, flush=None, warmup=3):
         e.record(stream)
         evs.append((s, e))
     torch.cuda.synchronize()
-    return sum(s.elapsed_time(e) for s, e in evs) / reps
+    return float(np.median([s.elapsed_time(e) for s, e in evs]))
 
 
 def quantize_sweep(tj, dev, stream, hbm_peak, flush):
@@ -308,7 +308,7 @@ def quantize_sweep(tj, dev, stream, hbm_peak, flush):
             q = tj.NVFP4.empty(cols if along else rows, rows if along else cols, dev)
             for mode in (tj.TJ_RTN, tj.TJ_SR):
                 ms = time_kernel(lambda: tj.quantize_nvfp4(x, along_cols=along, mode=mode, seed=1, tag=1, out=q,
-                                                           stream=stream), stream, 10, flush)
+                                                           stream=stream), stream, 50, flush)
                 gbs = rows * cols * (2 + 0.59375) / (ms * 1e-3) / 1e9
                 out.append({"shape": [rows, cols], "align": "col" if along else "row",
                             "mode": "SR" if mode else "RTN", "ms": round(ms, 4), "GB/s": round(gbs, 1),
@@ -333,7 +333,7 @@ def adamw_osci_alone(tj, osci, stream, hbm_peak):
         tj.adamw_osci_reset(w, g, m, v, w_prev, dq, dm, osci.q[0], osci.q[1], osci.mask, 5e-5, 0.9, 0.95, 1e-8,
                             0.1, step[0], LR_THR, RISK_THR, True, stream=stream)
 
-    ms = time_kernel(fn, stream, 10)
+    ms = time_kernel(fn, stream, 20, warmup=3)
     # read w, g, m, v, w_prev, dist_Q, dist_M + previous Q; write w, m, v, w_prev, dist_Q,
     # dist_M + new Q + 1 mask bit
     nbytes = osci.n * (4 * 7 + NV_B + 4 * 6 + NV_B + 1.0 / 8)
@@ -345,12 +345,83 @@ def adamw_osci_alone(tj, osci, stream, hbm_peak):
 def gemm_alone(tj, lin, stream, fp4_peak, fp8_peak):
     """The largest forward GEMM (FP4 part + FP8 slice in one tile) timed alone."""
     M, N, K, k = TOKENS, lin.N, lin.K, lin.k
-    ms = time_kernel(lambda: tj.gemm_nvfp4(lin.xq, lin.wq, lin.x8, lin.w8, out=lin.Y, stream=stream), stream, 20)
+    ms = time_kernel(lambda: tj.gemm_nvfp4(lin.xq, lin.wq, lin.x8, lin.w8, out=lin.Y, stream=stream), stream, 50)
     f4 = 2.0 * M * N * (K - k)
     f8 = 2.0 * M * N * k
     t_star = f4 / (fp4_peak * 1e12) + f8 / (fp8_peak * 1e12)          # time at the dtype-weighted peak
     return {"shape": [M, N, K], "k_fp8": k, "ms": round(ms, 4), "TFLOP/s": round((f4 + f8) / (ms * 1e-3) / 1e12, 1),
             "frac_of_peak": round(t_star / (ms * 1e-3), 3)}
+
+
+def _gemm_frac(f4, f8, ms, fp4_peak, fp8_peak):
+    t_star = f4 / (fp4_peak * 1e12) + f8 / (fp8_peak * 1e12)          # time at the dtype-weighted peak
+    return {"ms": round(ms, 4), "TFLOP/s": round((f4 + f8) / (ms * 1e-3) / 1e12, 1), "frac": round(t_star / (ms * 1e-3), 4)}
+
+
+def cfg3_fwd(tj, dev, stream, fp4_peak, fp8_peak):
+    """Forward NVFP4 linear with OutControl at its own shape: X 16384 x 1024 (the fifth
+    calibration-distribution batch), W 4096 x 1024 N(0, 0.02); the 10% FP8 channels come
+    from the calibration kernel over 4 warm-up batches with 20 fixed heavy channels x40.
+    Timed through tj_linear_fwd (OutControl split of X + FP4 GEMM with its FP8 slice)."""
+    from nvfp4_bit_fully_gb300 import workloads as wl
+
+    M, K, N, seed = TOKENS, 1024, 4096, 1
+    k = (OUTLIER_PCT * K + 99) // 100
+    sumsq = torch.zeros(K, dtype=torch.float64, device=dev)
+    for b in range(4):
+        xb = wl.device_calibration_batch(K, M, 20, b, seed, 21, dev)
+        torch.cuda.synchronize()
+        tj.outlier_calibrate(xb, sumsq, stream=stream)
+        torch.cuda.synchronize()
+        del xb
+    oi, ni = tj.outlier_calibrate(None, sumsq, finalize=True, k=k, stream=stream)
+    X = wl.device_calibration_batch(K, M, 20, 4, seed, 21, dev)
+    g = wl._cuda_gen(seed, 22, dev)
+    W = (torch.randn(N, K, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    torch.cuda.synchronize()
+    wq, w8 = tj.quantize_nvfp4(W, sel=ni, stream=stream), tj.quantize_mxfp8(W, sel=oi, stream=stream)
+    xq, x8 = tj.NVFP4.empty(M, K - k, dev), tj.MXFP8.empty(M, k, dev)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    f4, f8 = 2.0 * M * N * (K - k), 2.0 * M * N * k
+    torch.cuda.synchronize()                 # inputs were drawn on torch's current stream
+    ms = time_kernel(lambda: tj.linear_fwd(X, wq, w8, ni, oi, xq=xq, x8=x8, out=Y, stream=stream), stream)
+    ms_gemm = time_kernel(lambda: tj.gemm_nvfp4(xq, wq, x8, w8, out=Y, stream=stream), stream)
+    out = {"shape": [M, N, K], "k_fp8": k, "linear_fwd": _gemm_frac(f4, f8, ms, fp4_peak, fp8_peak),
+           "gemm": _gemm_frac(f4, f8, ms_gemm, fp4_peak, fp8_peak)}
+    del X, W, xq, x8, Y, wq, w8
+    return out
+
+
+def cfg4_bwd(tj, dev, stream, fp4_peak, fp8_peak):
+    """Backward NVFP4 linear with RHT and SR at its own shape: dY 16384 x 4096 with
+    heavy-tailed rows (1e-3 |t_3| N(0, 1)), W 4096 x 1024 N(0, 0.02), X 16384 x 1024 N(0, 1)
+    with 1% of the columns x30; W-hat and X-hat from the RTN forward quantization, no
+    outlier channels.  Timed through tj_linear_bwd_dx and tj_linear_bwd_dw (each: dY
+    quantizer, operand re-alignment, FP4 GEMM)."""
+    from nvfp4_bit_fully_gb300 import workloads as wl
+
+    M, N, K, seed = TOKENS, 4096, 1024, 2
+    dY = wl.device_student_t_rows(M, N, 1e-3, 3, seed, 31, dev)
+    g = wl._cuda_gen(seed, 32, dev)
+    W = (torch.randn(N, K, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    X = wl.device_heavy_columns((M, K), 1.0, 30.0, math.ceil(K / 100), seed, 11, dev)
+    torch.cuda.synchronize()
+    wq, xq = tj.quantize_nvfp4(W, stream=stream), tj.quantize_nvfp4(X, stream=stream)
+    dX = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    dW = torch.empty(N, K, dtype=torch.float32, device=dev)
+    ws_dx = torch.empty(tj.workspace_size(tj.TJ_OP_BWD_DX, M, N, K, 0), dtype=torch.uint8, device=dev)
+    ws_dw = torch.empty(tj.workspace_size(tj.TJ_OP_BWD_DW, M, N, K, 0), dtype=torch.uint8, device=dev)
+    f4 = 2.0 * M * N * K
+    torch.cuda.synchronize()                 # inputs were drawn on torch's current stream
+    seeds = iter(range(10**6))
+    ms_dx = time_kernel(lambda: tj.linear_bwd_dx(dY, wq, seed=next(seeds), workspace=ws_dx, out=dX, stream=stream),
+                        stream)
+    ms_dw = time_kernel(lambda: tj.linear_bwd_dw(dY, xq, seed=next(seeds), workspace=ws_dw, out=dW, stream=stream),
+                        stream)
+    out = {"shape": {"dY": [M, N], "W": [N, K], "X": [M, K]}, "linear_bwd_dx": _gemm_frac(f4, 0.0, ms_dx, fp4_peak, fp8_peak),
+           "linear_bwd_dw": _gemm_frac(f4, 0.0, ms_dw, fp4_peak, fp8_peak)}
+    del dY, W, X, wq, xq, dX, dW, ws_dx, ws_dw
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -620,6 +691,8 @@ def main():
         big = max(linears, key=lambda l: l.N * l.K)
         extras["gemm_fwd_alone"] = gemm_alone(tj, big, stream, fp4_peak, fp8_peak)
         del flush
+        extras["cfg3_fwd"] = cfg3_fwd(tj, dev, stream, fp4_peak, fp8_peak)
+        extras["cfg4_bwd"] = cfg4_bwd(tj, dev, stream, fp4_peak, fp8_peak)
         if osci is not None:
             extras["adamw_osci_reset"] = adamw_osci_alone(tj, osci, stream, hbm_peak)
     e2e = None

@@ -123,16 +123,37 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // so no element clips and stochastic rounding stays unbiased; deciding on the
 // dequantized value makes the quantizer idempotent, so an OsciReset reset (§2.B: the
 // weight moved onto its own Q-hat) re-quantizes to the same code and scales.
-// The search starts from the E4M3 ceiling of a_i * inv_m6 (inv_m6 ~ 1 / fl(6 s_o),
-// any approximation), floored at the smallest normal value; the two walks then reach
-// the exact answer whatever the start (the top value grows with sigma).  From a
-// start within an ulp or two of the quotient they take at most one step; they go
-// further only where the products are fp32 subnormals (at most 118 steps).
+// The search starts from c, the E4M3 ceiling of a_i * inv_m6 (inv_m6 ~ 1 / fl(6 s_o),
+// any approximation), floored at the smallest normal value.  From a start within an
+// ulp or two of the quotient the answer is c - 1, c or c + 1 whenever the products
+// are normal fp32 numbers, and the top values of c - 2 .. c + 1, computed side by
+// side, decide it; otherwise (fp32-subnormal products, a far start) two walks reach
+// the exact answer from there, since the top value grows with sigma.
+__device__ __forceinline__ float inner_top(uint32_t b, float s_o) {
+    return __fmul_rn(__fmul_rn(6.0f, e4m3_normal_to_float(b)), s_o);   // 6 sigma is exact
+}
 __device__ __forceinline__ uint32_t inner_scale_byte(float a_i, float s_o, float inv_m6) {
-    uint32_t sb = e4m3_ceil_byte(__fmul_rn(a_i, inv_m6));
-    if (sb < 0x08u) sb = 0x08u;                      // the smallest normal E4M3 value, 2^-6
-    while (sb < 0x7Eu && __fmul_rn(__fmul_rn(6.0f, e4m3_normal_to_float(sb)), s_o) < a_i) ++sb;
-    while (sb > 0x08u && __fmul_rn(__fmul_rn(6.0f, e4m3_normal_to_float(sb - 1u)), s_o) >= a_i) --sb;
+    uint32_t c = e4m3_ceil_byte(__fmul_rn(a_i, inv_m6));
+    if (c < 0x08u) c = 0x08u;                        // the smallest normal E4M3 value, 2^-6
+    // the top values of c - 2 .. c + 1 as independent products (clamped to the normal range)
+    const uint32_t cp = c < 0x7Eu ? c + 1u : c, cm = c > 0x08u ? c - 1u : c, cmm = cm > 0x08u ? cm - 1u : cm;
+    const float tp = inner_top(cp, s_o), t0 = inner_top(c, s_o), tm = inner_top(cm, s_o), tmm = inner_top(cmm, s_o);
+    uint32_t sb;
+    bool more;
+    if (t0 < a_i) {
+        sb = cp;
+        more = cp < 0x7Eu && tp < a_i;               // still below: walk further up
+    } else if (cm < c && tm >= a_i) {
+        sb = cm;
+        more = cmm < cm && tmm >= a_i;               // the next lower scale fits too: walk down
+    } else {
+        sb = c;
+        more = false;
+    }
+    if (more) {                                      // only where the products are fp32 subnormals
+        while (sb < 0x7Eu && inner_top(sb, s_o) < a_i) ++sb;
+        while (sb > 0x08u && inner_top(sb - 1u, s_o) >= a_i) --sb;
+    }
     return sb;
 }
 

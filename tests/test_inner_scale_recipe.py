@@ -1,10 +1,10 @@
 """CPU pin of the kernels' inner-scale recipe against the oracle's definition.
 
-The kernels do not search all 119 candidate scales.  They take the E4M3 ceiling of
-a first guess of the quotient a_i / fl(6 s_o) (a_i times an approximate reciprocal),
-floor it at the smallest normal value (byte 0x08), then walk up while the top value
-fl(fl(6 sigma) s_o) is below a_i and down while the next lower scale's top value
-still covers a_i.  That recipe is restated here in numpy, from the exact quotient
+The kernels do not search all 119 candidate scales.  They take c, the E4M3 ceiling
+of a first guess of the quotient a_i / fl(6 s_o) (a_i times an approximate
+reciprocal), floored at the smallest normal value (byte 0x08), compute the top
+values fl(fl(6 sigma) s_o) of c - 2 .. c + 1, step once up or down, and walk further
+only where that step is not enough (fp32-subnormal products, or a far start).  That recipe is restated here in numpy, from the exact quotient
 and from starts perturbed by a few ulps as an approximate reciprocal gives them, and
 checked equal to ``oracle.formats.e4m3_inner_scale_byte`` (the brute-force
 definition) on group maxima placed on and around every scale's top value, random
@@ -19,30 +19,42 @@ _ALL = np.arange(0, 0x7F, dtype=np.uint8)
 _ALL_VALS = F.e4m3_decode(_ALL)
 
 
-def _recipe(a_i, s_o, rel=None):
+def _top(b, s_o):
+    v = F.e4m3_decode(np.asarray(b).astype(np.uint8)).astype(F32)
+    with np.errstate(over="ignore"):
+        return ((F32(6.0) * v).astype(F32) * s_o).astype(F32)
+
+
+def _recipe(a_i, s_o, rel=None, stats=None):
+    """The kernels' selection: start c, the top values of c - 2 .. c + 1 side by side,
+    one step up or down, and walks only where that step is not enough."""
     m6 = (s_o * F32(6.0)).astype(F32)
     with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
         t = (a_i / m6).astype(F32)
-        if rel is not None:                         # a first guess off by a few ulps
+        if rel is not None:                         # a first guess off by some ulps
             t = (t.astype(np.float64) * (1.0 + rel)).astype(F32)
     idx = np.minimum(np.searchsorted(_ALL_VALS, t.astype(np.float64), side="left"), 0x7E)
-    sb = np.maximum(_ALL[idx].astype(np.int64), 0x08)
-
-    def top(b):
-        v = F.e4m3_decode(b.astype(np.uint8)).astype(F32)
-        with np.errstate(over="ignore"):
-            return ((F32(6.0) * v).astype(F32) * s_o).astype(F32)
-
-    for _ in range(120):
-        up = (sb < 0x7E) & (top(sb) < a_i)
-        if not up.any():
+    c = np.maximum(_ALL[idx].astype(np.int64), 0x08)
+    cp = np.where(c < 0x7E, c + 1, c)
+    cm = np.where(c > 0x08, c - 1, c)
+    cmm = np.where(cm > 0x08, cm - 1, cm)
+    tp, t0, tm, tmm = _top(cp, s_o), _top(c, s_o), _top(cm, s_o), _top(cmm, s_o)
+    up = t0 < a_i
+    down = ~up & (cm < c) & (tm >= a_i)
+    sb = np.where(up, cp, np.where(down, cm, c))
+    more = (up & (cp < 0x7E) & (tp < a_i)) | (down & (cmm < cm) & (tmm >= a_i))
+    if stats is not None:
+        stats["walks"] = int(more.sum())
+    for _ in range(120):                            # the walks, on the groups that need them
+        step = more & (sb < 0x7E) & (_top(sb, s_o) < a_i)
+        if not step.any():
             break
-        sb = np.where(up, sb + 1, sb)
+        sb = np.where(step, sb + 1, sb)
     for _ in range(120):
-        dn = (sb > 0x08) & (top(np.maximum(sb - 1, 0)) >= a_i)
-        if not dn.any():
+        step = more & (sb > 0x08) & (_top(np.maximum(sb - 1, 0), s_o) >= a_i)
+        if not step.any():
             break
-        sb = np.where(dn, sb - 1, sb)
+        sb = np.where(step, sb - 1, sb)
     return np.where(a_i > 0, sb, 0).astype(np.uint8)
 
 
@@ -79,17 +91,15 @@ def test_recipe_equals_definition():
     assert np.array_equal(_recipe(a, s, rng.uniform(-0.3, 0.3, a.size)), ref)       # any start
 
 
-def test_recipe_walks_at_most_one_step_for_normal_products():
-    """Where every product is a normal fp32 number, the quotient's ceiling (floored)
-    is at most one step from the answer, so the kernels' walks take one step."""
+def test_walks_only_for_subnormal_products():
+    """Where every product is a normal fp32 number, one step from the start decides the
+    scale: the walks never run, from the exact quotient or from a start a few ulps off."""
     rng = np.random.default_rng(22)
     a, s = _cases(rng, 50000)
     ok = np.isfinite(a) & (s >= F32(2.0 ** -110)) & (a > 0)
     a, s = a[ok], s[ok]
-    m6 = (s * F32(6.0)).astype(F32)
-    t = (a / m6).astype(F32)
-    idx = np.minimum(np.searchsorted(_ALL_VALS, t.astype(np.float64), side="left"), 0x7E)
-    cand = np.maximum(_ALL[idx].astype(np.int64), 0x08)
-    got = F.e4m3_inner_scale_byte(a, s).astype(np.int64)
-    assert np.abs(got - cand).max() <= 1
-    assert (got != cand).any()
+    ref = F.e4m3_inner_scale_byte(a, s)
+    for rel in (None, rng.uniform(-2.0 ** -20, 2.0 ** -20, a.size)):
+        stats = {}
+        assert np.array_equal(_recipe(a, s, rel, stats), ref)
+        assert stats["walks"] == 0
