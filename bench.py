@@ -161,7 +161,8 @@ class Linear:
 
     def __init__(self, tj, wl, name, N, K, dev, seed):
         self.name, self.N, self.K = name, N, K
-        self.X, W, self.dY = wl.device_layer_set_linear(name, N, K, seed=seed, M=TOKENS, device=dev)
+        self.X, self.W, self.dY = wl.device_layer_set_linear(name, N, K, seed=seed, M=TOKENS, device=dev)
+        W = self.W
         self.k = (OUTLIER_PCT * K + 99) // 100
         # OutControl calibration: 4 warm-up batches with fixed heavy channels (cold path)
         sumsq = torch.zeros(K, dtype=torch.float64, device=dev)
@@ -422,6 +423,39 @@ def cfg4_bwd(tj, dev, stream, fp4_peak, fp8_peak):
            "linear_bwd_dw": _gemm_frac(f4, 0.0, ms_dw, fp4_peak, fp8_peak)}
     del dY, W, X, wq, xq, dX, dW, ws_dx, ws_dw
     return out
+
+
+def fp8_layer_set(tj, linears, stream, fp8_peak, nvfp4_linear_ms):
+    """The FP8 linear baseline (tj_fp8_linear_*: MXFP8 operands, no RHT / SR / outlier
+    split) over the same layer set, inputs and outputs: forward, dX and dW of the four
+    linears per step.  The weights' MXFP8 forms (W along K, W^T along N) are made once,
+    outside the timed region, as the NVFP4 forward weights are.  nvfp4_speedup = FP8
+    step time / NVFP4 linear step time (the pages' metric: >1 means NVFP4 is faster)."""
+    dev = linears[0].X.device
+    bufs = []
+    for lin in linears:
+        M, N, K = TOKENS, lin.N, lin.K
+        bufs.append({
+            "w8": tj.quantize_mxfp8(lin.W, stream=stream), "wt8": tj.quantize_mxfp8(lin.W, along_cols=True, stream=stream),
+            "x8": tj.MXFP8.empty(M, K, dev), "xt8": tj.MXFP8.empty(K, M, dev),
+            "ws_dx": torch.empty(tj.workspace_size(tj.TJ_OP_FP8_BWD_DX, M, N, K, 0), dtype=torch.uint8, device=dev),
+            "ws_dw": torch.empty(tj.workspace_size(tj.TJ_OP_FP8_BWD_DW, M, N, K, 0), dtype=torch.uint8, device=dev)})
+    torch.cuda.synchronize()
+
+    def step():
+        for lin, b in zip(linears, bufs):
+            tj.fp8_linear_fwd(lin.X, b["w8"], x8=b["x8"], xt8=b["xt8"], out=lin.Y, stream=stream)
+            tj.fp8_linear_bwd_dx(lin.dY, b["wt8"], workspace=b["ws_dx"], out=lin.dX, stream=stream)
+            tj.fp8_linear_bwd_dw(lin.dY, b["xt8"], workspace=b["ws_dw"], out=lin.dW, stream=stream)
+
+    ms = time_kernel(step, stream, 20, warmup=3)
+    flops = sum(l.flops for l in linears)
+    tflops = flops / (ms * 1e-3) / 1e12
+    del bufs
+    return {"ms_per_step": round(ms, 4), "TFLOP/s": round(tflops, 1), "frac_of_fp8_peak": round(tflops / fp8_peak, 4),
+            "nvfp4_speedup": round(ms / nvfp4_linear_ms, 3),
+            "recipe": "MXFP8 (E4M3, UE8M0 per 1x32 along each GEMM's contraction axis, RTN) for X, W, dY; "
+                      "fp32 accumulation; launches per linear: fwd 3 (X rows, X^T columns, GEMM), dX 2, dW 2"}
 
 
 # ---------------------------------------------------------------------------
@@ -691,6 +725,7 @@ def main():
         big = max(linears, key=lambda l: l.N * l.K)
         extras["gemm_fwd_alone"] = gemm_alone(tj, big, stream, fp4_peak, fp8_peak)
         del flush
+        extras["fp8_layer_set"] = fp8_layer_set(tj, linears, stream, fp8_peak, lin_ms / args.steps)
         extras["cfg3_fwd"] = cfg3_fwd(tj, dev, stream, fp4_peak, fp8_peak)
         extras["cfg4_bwd"] = cfg4_bwd(tj, dev, stream, fp4_peak, fp8_peak)
         if osci is not None:

@@ -301,8 +301,41 @@ tj_status tj_linear_bwd_dx_noalloc(const void *dy, int64_t M, int64_t N, int64_t
                                    int64_t k, uint64_t seed, void *dx, int out_dtype, int64_t lddx, void *stream);
 size_t tj_noalloc_scratch_bytes(void);
 
+/* ---------------------------------------------------------------------------
+ * The FP8 linear baseline (technical summary §4, efficiency: the pages measure
+ * TetraJet-v2's training speed against FP8 training with TransformerEngine).  The
+ * same linear layer with every GEMM operand in MXFP8 on the same GPU, so the NVFP4
+ * path can be timed against it:
+ *   - each operand is E4M3 with one UE8M0 scale per 1x32 block along the contraction
+ *     axis of the GEMM that reads it (the format of tj_quantize_mxfp8), rounded to
+ *     nearest, quantized from its bf16 source (X, W, dY), as an MXFP8 recipe does;
+ *   - no RHT, no stochastic rounding, no outlier channels, no double-block scale;
+ *   - the three GEMMs are FP8-only products of the library's GEMM (fp32 accumulation).
+ * ------------------------------------------------------------------------- */
+/* tj_fp8_linear_fwd:  Y[M, N] = Q8(X) Q8(W)^T.
+ * x    bf16 [M, K] (ldx).  w8: MXFP8 [N, K], W along K (tj_quantize_mxfp8(W)).
+ * x8   out: MXFP8 [M, K], X along K.  xt8: out, MXFP8 [K, M], X^T along M (the dW
+ *      operand, saved for tj_fp8_linear_bwd_dw), or NULL to skip it.
+ * y    [M, N] bf16 or fp32 (out_dtype), row stride ldy. */
+tj_status tj_fp8_linear_fwd(const void *x, int64_t M, int64_t K, int64_t ldx, const tj_mxfp8 *w8, tj_mxfp8 *x8,
+                            tj_mxfp8 *xt8, void *y, int out_dtype, int64_t ldy, void *stream);
+/* tj_fp8_linear_bwd_dx:  dX[M, K] = Q8(dY) Q8(W^T)^T, both along N.
+ * dy bf16 [M, N] (lddy); wt8 MXFP8 [K, N] = tj_quantize_mxfp8(W, along_cols = 1);
+ * dx [M, K] bf16 or fp32 (lddx).  workspace: tj_workspace_size(TJ_OP_FP8_BWD_DX, M, N, K,
+ * 0) bytes, 256-aligned; it then holds Q8(dY) (tj_mxfp8 [M, N]: codes, sf). */
+tj_status tj_fp8_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, const tj_mxfp8 *wt8, void *dx,
+                               int out_dtype, int64_t lddx, void *workspace, size_t ws_bytes, void *stream);
+/* tj_fp8_linear_bwd_dw:  dW[N, K] = Q8(dY^T) Q8(X^T)^T, both along M (tokens).
+ * xt8 from tj_fp8_linear_fwd; dw fp32 [N, K] (lddw), written whole (a long M may be
+ * split in two, as in tj_gemm_pair_f32).  workspace: tj_workspace_size(TJ_OP_FP8_BWD_DW,
+ * M, N, K, 0) bytes, 256-aligned; it then holds Q8(dY^T) (tj_mxfp8 [N, M]). */
+tj_status tj_fp8_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, const tj_mxfp8 *xt8, float *dw,
+                               int64_t lddw, void *workspace, size_t ws_bytes, void *stream);
+
 #define TJ_OP_BWD_DX 1
 #define TJ_OP_BWD_DW 2
+#define TJ_OP_FP8_BWD_DX 3
+#define TJ_OP_FP8_BWD_DW 4
 
 /* Bytes of workspace the backward call `op` needs for these sizes (K = K_N + k). */
 size_t tj_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t k);

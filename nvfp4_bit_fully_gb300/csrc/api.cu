@@ -303,6 +303,10 @@ size_t tj_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t k) {
     } else if (op == TJ_OP_BWD_DW) {
         b = nv_bytes(N, M) + nv_bytes(kn, M);
         if (k > 0) b += mx_bytes(N, M) + mx_bytes(k, M);
+    } else if (op == TJ_OP_FP8_BWD_DX) {
+        b = mx_bytes(M, N);
+    } else if (op == TJ_OP_FP8_BWD_DW) {
+        b = mx_bytes(N, M);
     }
     return (size_t)b;
 }
@@ -428,6 +432,73 @@ tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, c
     } else {
         TJ_TRY(launch_gemm(&s_dy, &s_x, nullptr, nullptr, 0.0078125f, dw, TJ_FP32, lddw, N, kn, nullptr, s, &whole_dw));
     }
+    return TJ_OK;
+}
+
+// ---------------------------------------------------------------------------
+// The FP8 linear baseline the pages compare against (technical summary §4: training
+// speed vs FP8 TransformerEngine): every GEMM operand MXFP8 (E4M3, UE8M0 per 1x32
+// along its contraction axis, round to nearest), quantized from its bf16 source; no
+// RHT, no stochastic rounding, no outlier split.  The GEMMs are FP8-only products of
+// the same kernel, whose power-of-two scales the tensor core applies itself.
+// ---------------------------------------------------------------------------
+tj_status tj_fp8_linear_fwd(const void *x, int64_t M, int64_t K, int64_t ldx, const tj_mxfp8 *w8, tj_mxfp8 *x8,
+                            tj_mxfp8 *xt8, void *y, int out_dtype, int64_t ldy, void *stream) {
+    if (x == nullptr || w8 == nullptr || x8 == nullptr || y == nullptr || M < 0 || K < 0) return TJ_ERR_INVALID_ARG;
+    if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
+    if (!al_elem(x, TJ_BF16) || !al16(y)) return TJ_ERR_ALIGN;
+    const int64_t N = w8->rows;
+    if (ldx < K || ldy < N) return TJ_ERR_SHAPE;
+    tj_status st = check_mx(w8, N, K);
+    if (st == TJ_OK) st = check_mx(x8, M, K);
+    if (st == TJ_OK && xt8 != nullptr) st = check_mx(xt8, K, M);
+    if (st != TJ_OK) return st;
+    if (xt8 != nullptr && !cols_grid_fits(M)) return TJ_ERR_SHAPE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    TJ_TRY(launch_quant_mx_dense(x, TJ_BF16, M, K, ldx, 0, nullptr, *x8, s));
+    if (xt8 != nullptr) TJ_TRY(launch_quant_mx_dense(x, TJ_BF16, M, K, ldx, 1, nullptr, *xt8, s));
+    TJ_TRY(launch_gemm(nullptr, nullptr, x8, w8, 1.0f, y, out_dtype, ldy, M, N, nullptr, s));
+    return TJ_OK;
+}
+
+tj_status tj_fp8_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, const tj_mxfp8 *wt8, void *dx,
+                               int out_dtype, int64_t lddx, void *workspace, size_t ws_bytes, void *stream) {
+    if (dy == nullptr || wt8 == nullptr || dx == nullptr || M < 0 || N < 0) return TJ_ERR_INVALID_ARG;
+    if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
+    if (!al_elem(dy, TJ_BF16) || !al16(dx)) return TJ_ERR_ALIGN;
+    const int64_t K = wt8->rows;
+    tj_status st = check_mx(wt8, K, N);
+    if (st != TJ_OK) return st;
+    if (lddy < N || lddx < K) return TJ_ERR_SHAPE;
+    const size_t need = tj_workspace_size(TJ_OP_FP8_BWD_DX, M, N, K, 0);
+    if (workspace == nullptr || ws_bytes < need) return TJ_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return TJ_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *cur = static_cast<uint8_t *>(workspace);
+    tj_mxfp8 q8_dy = carve_mx(cur, M, N);
+    TJ_TRY(launch_quant_mx_dense(dy, TJ_BF16, M, N, lddy, 0, nullptr, q8_dy, s));
+    TJ_TRY(launch_gemm(nullptr, nullptr, &q8_dy, wt8, 1.0f, dx, out_dtype, lddx, M, K, nullptr, s));
+    return TJ_OK;
+}
+
+tj_status tj_fp8_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, const tj_mxfp8 *xt8, float *dw,
+                               int64_t lddw, void *workspace, size_t ws_bytes, void *stream) {
+    if (dy == nullptr || xt8 == nullptr || dw == nullptr || M < 0 || N < 0) return TJ_ERR_INVALID_ARG;
+    if (!al_elem(dy, TJ_BF16) || !al16(dw)) return TJ_ERR_ALIGN;
+    const int64_t K = xt8->rows;
+    tj_status st = check_mx(xt8, K, M);
+    if (st != TJ_OK) return st;
+    if (lddy < N || lddw < K || !cols_grid_fits(M)) return TJ_ERR_SHAPE;
+    const size_t need = tj_workspace_size(TJ_OP_FP8_BWD_DW, M, N, K, 0);
+    if (workspace == nullptr || ws_bytes < need) return TJ_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return TJ_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *cur = static_cast<uint8_t *>(workspace);
+    tj_mxfp8 q8_dyt = carve_mx(cur, N, M);
+    TJ_TRY(launch_quant_mx_dense(dy, TJ_BF16, M, N, lddy, 1, nullptr, q8_dyt, s));
+    // dW [N][K] is fp32 and covered by the launch, so a long-K launch may split K in two
+    const SplitRegion whole_dw{dw, N, K, lddw};
+    TJ_TRY(launch_gemm(nullptr, nullptr, &q8_dyt, xt8, 1.0f, dw, TJ_FP32, lddw, N, K, nullptr, s, &whole_dw));
     return TJ_OK;
 }
 

@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(_PKG, "libtj.so")
 TJ_OK = 0
 TJ_RTN, TJ_SR = 0, 1
 TJ_BF16, TJ_FP32 = 0, 1
-TJ_OP_BWD_DX, TJ_OP_BWD_DW = 1, 2
+TJ_OP_BWD_DX, TJ_OP_BWD_DW, TJ_OP_FP8_BWD_DX, TJ_OP_FP8_BWD_DW = 1, 2, 3, 4
 TAG_DY_ROW, TAG_DY_COL, TAG_WT, TAG_XT = 1, 2, 3, 4
 TAG_RHT_DX, TAG_RHT_DW = 0x100, 0x101
 STATUS = {0: "ok", 1: "invalid argument", 2: "shape", 3: "alignment", 4: "unsupported", 5: "CUDA error",
@@ -70,6 +70,10 @@ _SIGS = {
                          _P, _I, _I64, _P, ctypes.c_size_t, _P],
     "tj_linear_bwd_dw": [_P, _I64, _I64, _I64, ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P, _P, _I64, _U64,
                          _P, _I64, _P, ctypes.c_size_t, _P],
+    "tj_fp8_linear_fwd": [_P, _I64, _I64, _I64, ctypes.POINTER(CMxfp8), ctypes.POINTER(CMxfp8), ctypes.POINTER(CMxfp8),
+                          _P, _I, _I64, _P],
+    "tj_fp8_linear_bwd_dx": [_P, _I64, _I64, _I64, ctypes.POINTER(CMxfp8), _P, _I, _I64, _P, ctypes.c_size_t, _P],
+    "tj_fp8_linear_bwd_dw": [_P, _I64, _I64, _I64, ctypes.POINTER(CMxfp8), _P, _I64, _P, ctypes.c_size_t, _P],
     "tj_workspace_size": [_I, _I64, _I64, _I64, _I64],
     "tj_outlier_calibrate": [_P, _I, _I64, _I64, _I64, _P, _I, _I64, _P, _P, _P],
     "tj_osci_reset": [_P, _P, _P, _P, ctypes.POINTER(CNvfp4), ctypes.POINTER(CNvfp4), _P, _I64, _I64, _F, _F, _F,
@@ -359,6 +363,48 @@ def linear_bwd_dx_noalloc(dy, wq, w8=None, normal_idx=None, outlier_idx=None, se
     cw8 = w8.c() if k else None
     _call("tj_linear_bwd_dx_noalloc", _ptr(dy), M, N, dy.stride(0), ctypes.byref(cw), _ref(cw8), _ptr(normal_idx),
           _ptr(outlier_idx), k, seed, _ptr(out), _dtype_code(out), out.stride(0), _stream(stream))
+    return out
+
+
+def fp8_linear_fwd(x, w8, out_dtype=torch.bfloat16, x8=None, xt8=None, save_xt=True, out=None, stream=None):
+    """FP8 baseline forward (tj_fp8_linear_fwd); returns (Y, X along K, X^T along M or None)."""
+    M, K = x.shape
+    x8 = x8 if x8 is not None else MXFP8.empty(M, K, x.device)
+    if save_xt and xt8 is None:
+        xt8 = MXFP8.empty(K, M, x.device)
+    out = out if out is not None else torch.empty(M, w8.rows, dtype=out_dtype, device=x.device)
+    cw, cx = w8.c(), x8.c()
+    cxt = xt8.c() if save_xt else None
+    _call("tj_fp8_linear_fwd", _ptr(x), M, K, x.stride(0), ctypes.byref(cw), ctypes.byref(cx), _ref(cxt), _ptr(out),
+          _dtype_code(out), out.stride(0), _stream(stream))
+    return out, x8, (xt8 if save_xt else None)
+
+
+def fp8_linear_bwd_dx(dy, wt8, out_dtype=torch.bfloat16, workspace=None, out=None, stream=None):
+    """FP8 baseline input gradient (tj_fp8_linear_bwd_dx); wt8 = MXFP8 of W^T along N."""
+    M, N = dy.shape
+    K = wt8.rows
+    ws_bytes = workspace_size(TJ_OP_FP8_BWD_DX, M, N, K, 0)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dy.device)
+    out = out if out is not None else torch.empty(M, K, dtype=out_dtype, device=dy.device)
+    cw = wt8.c()
+    _call("tj_fp8_linear_bwd_dx", _ptr(dy), M, N, dy.stride(0), ctypes.byref(cw), _ptr(out), _dtype_code(out),
+          out.stride(0), _ptr(workspace), workspace.numel(), _stream(stream))
+    return out
+
+
+def fp8_linear_bwd_dw(dy, xt8, workspace=None, out=None, stream=None):
+    """FP8 baseline weight gradient (tj_fp8_linear_bwd_dw); xt8 from fp8_linear_fwd."""
+    M, N = dy.shape
+    K = xt8.rows
+    ws_bytes = workspace_size(TJ_OP_FP8_BWD_DW, M, N, K, 0)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dy.device)
+    out = out if out is not None else torch.empty(N, K, dtype=torch.float32, device=dy.device)
+    cx = xt8.c()
+    _call("tj_fp8_linear_bwd_dw", _ptr(dy), M, N, dy.stride(0), ctypes.byref(cx), _ptr(out), out.stride(0),
+          _ptr(workspace), workspace.numel(), _stream(stream))
     return out
 
 

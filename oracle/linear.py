@@ -145,3 +145,31 @@ def bwd_dw(dY, fx, outlier_idx, seed):
     if len(o):
         dW[:, o] = gemm_fp8(q8_dy, q8_x)[:, : len(o)]
     return dW
+
+
+# ---------------------------------------------------------------------------
+# The FP8 linear baseline the pages compare against (technical summary §4: training
+# speed vs FP8 with TransformerEngine).  Reading: every GEMM operand in MXFP8 (E4M3
+# with a UE8M0 scale per 1x32 along the GEMM's contraction axis, round to nearest),
+# quantized from its unquantized source; no RHT, SR, outlier split or double-block
+# scale.  fp64 products of the exactly dequantized operands.
+# ---------------------------------------------------------------------------
+def fp8_forward(X, W):
+    """Y [M, N] = Q8(X) Q8(W)^T, both along K.  Returns (Y, Q8(X), Q8(W))."""
+    q8x = Q.quantize_mxfp8(np.asarray(X, dtype=F32))
+    q8w = Q.quantize_mxfp8(np.asarray(W, dtype=F32))
+    return gemm_fp8(q8x, q8w), q8x, q8w
+
+
+def fp8_bwd_dx(dY, W):
+    """dX [M, K] = Q8(dY) Q8(W^T)^T, both along N."""
+    q8dy = Q.quantize_mxfp8(np.asarray(dY, dtype=F32))
+    q8wt = Q.quantize_mxfp8(np.ascontiguousarray(np.asarray(W, dtype=F32).T))
+    return gemm_fp8(q8dy, q8wt), q8dy, q8wt
+
+
+def fp8_bwd_dw(dY, X):
+    """dW [N, K] = Q8(dY^T) Q8(X^T)^T, both along M."""
+    q8dyt = Q.quantize_mxfp8(np.ascontiguousarray(np.asarray(dY, dtype=F32).T))
+    q8xt = Q.quantize_mxfp8(np.ascontiguousarray(np.asarray(X, dtype=F32).T))
+    return gemm_fp8(q8dyt, q8xt), q8dyt, q8xt

@@ -131,3 +131,47 @@ def test_backward_outlier_columns_use_fp8_slice():
     # FP8 slice is deterministic (no seed dependence); FP4 columns are seeded
     assert np.array_equal(Lin.bwd_dx(dY, fw, o, 8)[:, o], dX[:, o])
     assert not np.array_equal(Lin.bwd_dx(dY, fw, o, 8)[:, 0], dX[:, 0])
+
+
+# ---------------------------------------------------------------------------
+# FP8 linear baseline (technical summary §4's comparison): exact on tensors whose
+# every 32-block, along rows and along columns, reaches +-448 with E4M3 values, so
+# that forward, dX and dW reduce to the plain matmul; otherwise within the E4M3
+# rounding bound of both operands.
+# ---------------------------------------------------------------------------
+def _exact_fp8_tensor(rng, R, C):
+    from oracle import formats as Fm
+    vals = Fm.e4m3_decode(rng.integers(0, 0x7F, (R, C)).astype(np.uint8))
+    vals *= rng.choice([-1.0, 1.0], (R, C))
+    i = np.arange(R)[:, None] % 32
+    j = np.arange(C)[None, :] % 32
+    vals = np.where(i == j, 448.0 * rng.choice([-1.0, 1.0], (R, C)), vals)
+    return (vals * 2.0 ** -9).astype(F32)       # one global power of two: still exact
+
+
+def test_fp8_baseline_exact_reduces_to_matmul():
+    rng = np.random.default_rng(31)
+    M, N, K = 96, 160, 224
+    X = _exact_fp8_tensor(rng, M, K)
+    W = _exact_fp8_tensor(rng, N, K)
+    dY = _exact_fp8_tensor(rng, M, N)
+    X64, W64, dY64 = (a.astype(np.float64) for a in (X, W, dY))
+    Y, _, _ = Lin.fp8_forward(X, W)
+    dX, _, _ = Lin.fp8_bwd_dx(dY, W)
+    dW, _, _ = Lin.fp8_bwd_dw(dY, X)
+    assert np.array_equal(Y, X64 @ W64.T)
+    assert np.array_equal(dX, dY64 @ W64)
+    assert np.array_equal(dW, dY64.T @ X64)
+
+
+def test_fp8_baseline_error_bound():
+    rng = np.random.default_rng(32)
+    M, N, K = 64, 96, 200
+    X = (rng.standard_normal((M, K)) * 3).astype(F32)
+    W = (rng.standard_normal((N, K)) * 0.02).astype(F32)
+    Y, _, _ = Lin.fp8_forward(X, W)
+    ref = X.astype(np.float64) @ W.astype(np.float64).T
+    mag = np.abs(X.astype(np.float64)) @ np.abs(W.astype(np.float64)).T
+    # each E4M3 operand is within 2^-4 relative (normal range) of its input, plus the
+    # absolute step of the block's subnormals
+    assert np.all(np.abs(Y - ref) <= mag * (2 * 2.0 ** -4 + 2.0 ** -8) + 1e-6)
