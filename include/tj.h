@@ -186,6 +186,10 @@ tj_status tj_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t 
  * [rows, cols] (row stride ldy).  The value the aligned backward re-quantizes. */
 tj_status tj_dequantize_nvfp4(const tj_nvfp4 *q, float *y, int64_t ldy, void *stream);
 
+/* tj_dequantize_mxfp8 - fp32 values (E4M3 value x 2^(e - 127)) of a tj_mxfp8 into y
+ * [rows, cols] (row stride ldy); exact.  For inspecting the FP8 slices (§2.C). */
+tj_status tj_dequantize_mxfp8(const tj_mxfp8 *q, float *y, int64_t ldy, void *stream);
+
 /* tj_gemm_nvfp4 - block-scaled FP4 GEMM with FP32 outer-scale promotion:
  *   D[m, n] = alpha * sum_kb sA[m,kb] sB[n,kb] * (sum over the 128 elements of
  *             block kb of  (a s_iA)(b s_iB))  [+ sum over the FP8 slice a8 b8]

@@ -226,6 +226,14 @@ tj_status tj_dequantize_nvfp4(const tj_nvfp4 *q, float *y, int64_t ldy, void *st
     return cuda_status(launch_dequant_nv(*q, y, ldy, static_cast<cudaStream_t>(stream)));
 }
 
+tj_status tj_dequantize_mxfp8(const tj_mxfp8 *q, float *y, int64_t ldy, void *stream) {
+    if (q == nullptr || y == nullptr) return TJ_ERR_INVALID_ARG;
+    const tj_status st = check_mx(q, q->rows, q->cols);
+    if (st != TJ_OK) return st;
+    if (ldy < q->cols) return TJ_ERR_SHAPE;
+    return cuda_status(launch_dequant_mx(*q, y, ldy, static_cast<cudaStream_t>(stream)));
+}
+
 tj_status tj_gemm_nvfp4(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8, const tj_mxfp8 *b8, float alpha,
                         void *d, int out_dtype, int64_t ldd, const int32_t *col_map, void *stream) {
     if (a == nullptr || b == nullptr || d == nullptr) return TJ_ERR_INVALID_ARG;

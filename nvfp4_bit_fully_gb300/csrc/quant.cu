@@ -460,6 +460,14 @@ __global__ void k_dequant_nv(SrcNv src, float *y, int64_t ldy) {
     y[r * ldy + c] = src.load(r, c);
 }
 
+// fp32 values of an MXFP8 tensor, one thread per element.
+__global__ void k_dequant_mx(SrcMx src, float *y, int64_t ldy) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= src.rows * src.cols) return;
+    const int64_t r = i / src.cols, c = i % src.cols;
+    y[r * ldy + c] = src.load(r, c);
+}
+
 // ---------------------------------------------------------------------------
 // Host launchers.
 // ---------------------------------------------------------------------------
@@ -623,6 +631,13 @@ cudaError_t launch_dequant_nv(const tj_nvfp4 &q, float *y, int64_t ldy, cudaStre
     const int64_t n = q.rows * q.cols;
     if (n == 0) return cudaSuccess;
     k_dequant_nv<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(src_nv(q), y, ldy);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_mx(const tj_mxfp8 &q, float *y, int64_t ldy, cudaStream_t s) {
+    const int64_t n = q.rows * q.cols;
+    if (n == 0) return cudaSuccess;
+    k_dequant_mx<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(src_mx(q), y, ldy);
     return cudaGetLastError();
 }
 

@@ -25,6 +25,7 @@ cudaError_t launch_realign_mx(const tj_mxfp8 &in, const tj_mxfp8 &out, cudaStrea
 cudaError_t launch_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,
                        cudaStream_t s);
 cudaError_t launch_dequant_nv(const tj_nvfp4 &q, float *y, int64_t ldy, cudaStream_t s);
+cudaError_t launch_dequant_mx(const tj_mxfp8 &q, float *y, int64_t ldy, cudaStream_t s);
 
 // An fp32 output region [rows][cols] (row pitch ld floats) that holds every output of a GEMM
 // launch.  Passing it allows the launch to split K in two when that shortens its schedule:

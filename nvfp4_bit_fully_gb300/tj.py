@@ -57,6 +57,7 @@ _SIGS = {
     "tj_requantize_mxfp8": [ctypes.POINTER(CMxfp8), ctypes.POINTER(CMxfp8), _P],
     "tj_rht": [_P, _P, _I64, _I64, _U64, _U32, _P],
     "tj_dequantize_nvfp4": [ctypes.POINTER(CNvfp4), _P, _I64, _P],
+    "tj_dequantize_mxfp8": [ctypes.POINTER(CMxfp8), _P, _I64, _P],
     "tj_gemm_nvfp4": [ctypes.POINTER(CNvfp4), ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8),
                       ctypes.POINTER(CMxfp8), _F, _P, _I, _I64, _P, _P],
     "tj_gemm_mxfp8": [ctypes.POINTER(CMxfp8), ctypes.POINTER(CMxfp8), _P, _I, _I64, _P, _P],
@@ -253,6 +254,13 @@ def dequantize_nvfp4(q, stream=None):
     y = torch.empty(q.rows, q.cols, dtype=torch.float32, device=q.codes.device)
     c = q.c()
     _call("tj_dequantize_nvfp4", ctypes.byref(c), _ptr(y), q.cols, _stream(stream))
+    return y
+
+
+def dequantize_mxfp8(q, stream=None):
+    y = torch.empty(q.rows, q.cols, dtype=torch.float32, device=q.codes.device)
+    c = q.c()
+    _call("tj_dequantize_mxfp8", ctypes.byref(c), _ptr(y), q.cols, _stream(stream))
     return y
 
 

@@ -215,3 +215,14 @@ def test_requantize_bit_exact(tj, rows, cols):
     c8, s8 = Q.quantize_mxfp8(x.float().numpy())
     xh8 = Q.dequantize_mxfp8_f32(c8, s8)[:, :cols]
     assert_mxfp8_equal(r8, Q.quantize_mxfp8(np.ascontiguousarray(xh8.T)), "requantize mxfp8")
+
+
+def test_dequantize_mxfp8_exact(tj):
+    """tj_dequantize_mxfp8 returns E4M3 value x 2^(e - 127) of every element, exactly."""
+    x = _input(200, 300, torch.bfloat16, 77)
+    q8 = tj.quantize_mxfp8(x.cuda())
+    y = tj.dequantize_mxfp8(q8)
+    torch.cuda.synchronize()
+    codes, sb = Q.quantize_mxfp8(x.float().numpy())
+    ref = Q.dequantize_mxfp8_f32(codes, sb)[:, :300]
+    assert np.array_equal(y.cpu().numpy(), ref)
