@@ -402,6 +402,21 @@ tj_status tj_adamw_osci_reset(float *w, const float *g, float *m, float *v, floa
  * TJ_ERR_TIMEOUT if a bounded device wait ran out since the last query. */
 tj_status tj_get_device_status(void);
 
+/* tj_debug_gemm_fault - test hook of the time-out path (not for production use).  Arms a
+ * fault for the next GEMM launch that runs (tj_gemm_*, or one inside tj_linear_* /
+ * tj_fp8_linear_*); the launch after it runs normally again:
+ *   - skip_stage >= 0: in every CTA the producers never load the operands of that stage
+ *     (its index among the CTA's stages, counted over its tiles), so the waits for it run
+ *     out; -1: no fault;
+ *   - wait_clk > 0: every mbarrier wait of the launch gives up after wait_clk SM clocks
+ *     (the default is about 2 s); 0 keeps the default.
+ * A launch whose wait runs out stops its work, keeps the protocol of its hardware
+ * barriers, drains its copies and tensor-core work, frees its tensor memory and returns;
+ * tj_get_device_status then reports TJ_ERR_TIMEOUT, the outputs of that launch are
+ * undefined, and later launches are unaffected.  Not thread-safe: arm it and launch from
+ * one host thread.  Returns TJ_ERR_INVALID_ARG for skip_stage < -1 or wait_clk < 0. */
+tj_status tj_debug_gemm_fault(int skip_stage, int64_t wait_clk);
+
 /* Static description of a status code. */
 const char *tj_status_str(tj_status s);
 

@@ -122,6 +122,8 @@ struct GemmArgs {
     int64_t rpa, rpb;             // rows_p of A and B
     const uint8_t *sfa8, *sfb8;   // scale tiles, FP8 operands (of whichever product has FP8 stages)
     int64_t ntk_a8, ntk_b8;       // cols_p / 128
+    long long wait_clk;           // bound of every mbarrier wait, in SM clocks
+    int skip_stage;               // test hook: the producers never load this stage of each CTA (-1: none)
 };
 
 // The work of one output tile (or, with a split, of one half of its K): its product,
@@ -180,6 +182,8 @@ struct Bars {
     uint64_t drain;
     uint32_t tmem_base;
     volatile int abort_flag;
+    volatile int met[kPSlots];    // generations of each slot's named barrier the MMA warp has met
+                                  // (written by the MMA warp alone, as plain stores)
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 
@@ -187,13 +191,13 @@ static_assert(sizeof(Bars) <= 512, "barrier block");
 // soon as another role has aborted), setting the sticky device error flag and
 // the CTA's abort flag.  No wait in this kernel can spin forever.  The bound is
 // kept in SM clocks because the clock register is read in a few cycles.
-__device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, Bars *bars) {
+__device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, Bars *bars, long long wait_clk) {
     if (ptx::mbar_try_wait(bar, parity)) return true;         // fast path
     const long long t0 = clock64();
     for (;;) {
         if (bars->abort_flag) return false;
         if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (clock64() - t0 > kWaitClk) break;
+        if (clock64() - t0 > wait_clk) break;
     }
     atomicOr(&g_tj_dev_error, 1u);
     bars->abort_flag = 1;
@@ -202,10 +206,10 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, Bar
 
 // Bounded wait that ignores the abort flag: used only to drain asynchronous work
 // (copies, MMAs) that is already in flight before the CTA frees its memory.
-__device__ __forceinline__ void wait_drain(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ void wait_drain(uint64_t *bar, uint32_t parity, long long wait_clk) {
     const long long t0 = clock64();
     while (!ptx::mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitClk) {
+        if (clock64() - t0 > wait_clk) {
             atomicOr(&g_tj_dev_error, 1u);
             return;
         }
@@ -227,9 +231,8 @@ __device__ __forceinline__ void named_arrive(int id, int count) {
 // handshake: 802 against 858 cycles per block).  The verdict is the lanes'
 // conjunction; a phase, once complete, stays complete, so the lanes agree unless
 // the wait ran out.
-__device__ __forceinline__ bool warp_wait_bounded(uint64_t *bar, uint32_t parity, Bars *bars, int lane) {
-    (void)lane;
-    const bool ok = wait_bounded(bar, parity, bars);
+__device__ __forceinline__ bool warp_wait_bounded(uint64_t *bar, uint32_t parity, Bars *bars, long long wait_clk) {
+    const bool ok = wait_bounded(bar, parity, bars, wait_clk);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -266,6 +269,38 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
     return d;
 }
 
+// The barrier protocol of a promotion warp that has stopped waiting for partials (a
+// wait ran out, or another role aborted), from block kb of `tile` on: it takes part in
+// every remaining generation of the partial slots' named barriers with a sync.  A live
+// warp arrives on them without waiting, which is safe because it reached each block only
+// after the MMA warp had met the slot's previous generation; a warp that stops being live
+// may have arrived on that generation already, and a second participation in one
+// generation would derail every later one.  So before each sync it waits until the MMA
+// warp has published (met[]) that it met the slot's previous generation.  The MMA warp
+// meets the generations in order and waits on nothing else once the launch has aborted,
+// so this takes microseconds; the wait is bounded by the default limit.  Not inlined: it
+// keeps the code of the working loop as it was.
+__device__ __noinline__ void promo_drain(const GemmArgs &args, Bars *bars, int tile, int kb, int ps, uint32_t pph,
+                                         int ncta, int ntiles) {
+    for (; tile < ntiles; tile += ncta, kb = 0) {
+        const TileWork w = tile_work(args, tile);
+        for (; kb < w.nblk; ++kb) {
+            // this is use u of slot ps, and met[ps] is u - 1 or u here (this warp took part in
+            // generation u - 1 already), so its parity, that of the slot's phase bit
+            // pph = u & 1, tells the two apart
+            const long long t0 = clock64();
+            while (((uint32_t)bars->met[ps] & 1u) != pph && clock64() - t0 <= kWaitClk) {
+            }
+            named_sync(kNamedP + ps, kNamedCount);
+            if (++ps == kPSlots) { ps = 0; pph ^= 1u; }
+        }
+    }
+}
+
+// kTestHook: the launch honours the test hook of tj_debug_gemm_fault (a stage the
+// producers never load, a shorter bound for every wait); production launches use the
+// instantiation without it, whose bound is the constant kWaitClk.
+template <bool kTestHook>
 __global__ void __launch_bounds__(kThreadsGemm, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tm_a4, const __grid_constant__ CUtensorMap tm_b4,
                  const __grid_constant__ CUtensorMap tm_a8, const __grid_constant__ CUtensorMap tm_b8,
@@ -274,6 +309,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars *bars = reinterpret_cast<Bars *>(smem + kSmemBar);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long wclk = kTestHook ? args.wait_clk : kWaitClk;    // bound of every mbarrier wait
     const int ntiles = problem_works(args.pr[0]) + problem_works(args.pr[1]);
     const int cta = (int)blockIdx.x, ncta = (int)gridDim.x;
 
@@ -286,6 +322,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         for (int q = 0; q < kScaleSlots; ++q) ptx::mbar_init(&bars->sempty[q], 1);
         ptx::mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
+        for (int p = 0; p < kPSlots; ++p) bars->met[p] = 0;
         ptx::fence_mbar_init();
     }
     if (warp == kMmaWarp) ptx::tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -308,7 +345,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                 for (int st = 0; st < w.nstages; ++st, ++it) {
                     if (it % kProdWarps != warp) continue;
                     const int slot = it % kStages;
-                    if (it >= kStages && !wait_bounded(&bars->empty[slot], ((it / kStages) - 1) & 1, bars)) {
+                    if (it >= kStages && !wait_bounded(&bars->empty[slot], ((it / kStages) - 1) & 1, bars, wclk)) {
                         ok = false;
                         break;
                     }
@@ -327,10 +364,12 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     for (int j = 0; j < nkbs && ok; ++j) {
                         const int f = f0 + j;
                         if (f >= kScaleSlots &&
-                            !wait_bounded(&bars->sempty[f % kScaleSlots], ((f / kScaleSlots) - 1) & 1, bars))
+                            !wait_bounded(&bars->sempty[f % kScaleSlots], ((f / kScaleSlots) - 1) & 1, bars, wclk))
                             ok = false;
                     }
                     if (!ok) break;
+                    // test hook: this stage is never loaded, so the waits for it run out
+                    if (kTestHook && it == args.skip_stage) continue;
                     // operands, their scale-factor tiles and, for FP4 stages, the FP32 outer
                     // scales of the stage's blocks all land on one barrier
                     ptx::mbar_arrive_expect_tx(&bars->full[slot],
@@ -355,7 +394,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             }
             // drain: every copy this warp issued must have landed before the CTA exits
             for (int j = (it > kStages ? it - kStages : 0); j < it; ++j)
-                if (j % kProdWarps == warp) wait_drain(&bars->full[j % kStages], (j / kStages) & 1);
+                if (j % kProdWarps == warp && (!kTestHook || j != args.skip_stage))
+                    wait_drain(&bars->full[j % kStages], (j / kStages) & 1, wclk);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer (warp-uniform loop;
@@ -379,7 +419,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             const TileWork w = tile_work(args, tile);
             for (int st = 0; st < w.nstages; ++st, ++it) {
                 const int slot = it % kStages;
-                if (live) live = warp_wait_bounded(&bars->full[slot], (it / kStages) & 1, bars, lane);
+                if (live) live = warp_wait_bounded(&bars->full[slot], (it / kStages) & 1, bars, wclk);
                 ptx::tc_fence_after();
                 const uint32_t sa = ptx::smem_u32(smem + kSmemA + slot * kTileBytes);
                 const uint32_t sb = ptx::smem_u32(smem + kSmemB + slot * kTileBytes);
@@ -411,6 +451,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                             ptx::tc_commit(&bars->pfull[ps]);
                         }
                         __syncwarp();
+                        // the generation just met, published for the promotion warps' abort path
+                        // (a plain store, after the issue so that it stays off the meet-to-issue path)
+                        if (pc >= kPSlots && lane == 0) bars->met[ps] = pc / kPSlots;
                         rel |= (uint32_t)(f4 % kScaleSlots + 1) << (8 * ((pc + 1) & 3));
                         ++f4;
                     }
@@ -439,6 +482,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                         if (s8 == w.nk8 - 1) ptx::tc_commit(&bars->pfull[ps]);
                     }
                     __syncwarp();
+                    if (s8 == 0 && pc >= kPSlots && lane == 0) bars->met[ps] = pc / kPSlots;
                     if (s8 == w.nk8 - 1) ++pc;
                 }
                 // the stage's buffers are free once its MMAs complete
@@ -449,12 +493,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         // meet the promotion warps' releases of the last blocks
         for (int j = (pc > kPSlots ? pc - kPSlots : 0); j < pc; ++j) {
             named_sync(kNamedP + j % kPSlots, kNamedCount);
+            if (lane == 0) bars->met[j % kPSlots] = j / kPSlots + 1;
             release(j & 3);
         }
         // all MMAs / copies issued by this thread complete before TMEM is freed
         if (lane == 0) {
             ptx::tc_commit(&bars->drain);
-            wait_drain(&bars->drain, 0);
+            wait_drain(&bars->drain, 0, wclk);
         }
         __syncwarp();
     } else {
@@ -466,8 +511,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         int f4c = 0;                            // FP4 blocks promoted so far (outer-scale ring position)
         int ps = 0;
         uint32_t pph = 0;                       // partial ring slot and phase
-        bool live = true;                       // false after an abort: the barrier protocol goes on, the work stops
-        for (int tile = cta; tile < ntiles; tile += ncta) {
+        bool aborted = false;                   // a wait ran out: promo_drain keeps the barrier protocol
+        for (int tile = cta; tile < ntiles && !aborted; tile += ncta) {
             const TileWork w = tile_work(args, tile);
             const GemmProblem &g = w.p ? args.pr[1] : args.pr[0];
             const int64_t m0 = w.m0, n0 = w.n0;
@@ -476,34 +521,31 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
 #pragma unroll
             for (int j = 0; j < kColsW / 2; ++j) acc[j] = 0ull;
             for (int kb = 0; kb < w.nblk; ++kb) {
-                if (live) live = warp_wait_bounded(&bars->pfull[ps], pph, bars, lane);
+                if (!warp_wait_bounded(&bars->pfull[ps], pph, bars, wclk)) {
+                    promo_drain(args, bars, tile, kb, ps, pph, ncta, ntiles);
+                    aborted = true;
+                    break;
+                }
                 const float *so = reinterpret_cast<const float *>(smem + kSmemScale + (f4c % kScaleSlots) * 1024);
 #pragma unroll
                 for (int ch = 0; ch < kColsW / kLdCols; ++ch) {
                     uint32_t p[kLdCols];
-                    if (live) {
-                        ptx::tc_fence_after();
+                    ptx::tc_fence_after();
 #pragma unroll
-                        for (int c = 0; c < kLdCols / 32; ++c)
-                            ptx::tmem_ld_32x32b_x32(taddr0 + 128u * (uint32_t)ps + (uint32_t)(kLdCols * ch + 32 * c),
-                                                    *reinterpret_cast<uint32_t(*)[32]>(p + 32 * c));
-                        ptx::tmem_wait_ld();
-                    }
+                    for (int c = 0; c < kLdCols / 32; ++c)
+                        ptx::tmem_ld_32x32b_x32(taddr0 + 128u * (uint32_t)ps + (uint32_t)(kLdCols * ch + 32 * c),
+                                                *reinterpret_cast<uint32_t(*)[32]>(p + 32 * c));
+                    ptx::tmem_wait_ld();
                     if (ch == kColsW / kLdCols - 1) {
                         ptx::tc_fence_before();
                         __syncwarp();
-                        // release the partial slot.  A live warp arrives without waiting: it reached
-                        // this block only after the MMA warp had met the previous use of the slot.
-                        // A warp that has stopped waiting for partials waits here instead, so that
-                        // it never arrives twice on one barrier generation.
-                        if (live)
-                            named_arrive(kNamedP + ps, kNamedCount);
-                        else
-                            named_sync(kNamedP + ps, kNamedCount);
+                        // release the partial slot.  The warp arrives without waiting: it reached this
+                        // block only after the MMA warp had met the previous use of the slot.
+                        named_arrive(kNamedP + ps, kNamedCount);
                     }
                     uint64_t *ac = acc + (kLdCols / 2) * ch;
                     if (kb < w.nkb4) {
-                        if (live) {
+                        {
                             // the block's outer scales: its slot goes back to the producers only
                             // after this warp has released the next block's partial
                             const float sa = so[32 * q + lane] * alpha;
@@ -520,7 +562,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                                     fma2((uint64_t)p[4 * i + 2] | ((uint64_t)p[4 * i + 3] << 32), w1, ac[2 * i + 1]);
                             }
                         }
-                    } else if (live) {
+                    } else {
 #pragma unroll
                         for (int i = 0; i < kLdCols / 2; ++i)
                             ac[i] = add2(ac[i], (uint64_t)p[2 * i] | ((uint64_t)p[2 * i + 1] << 32));
@@ -529,7 +571,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                 if (++ps == kPSlots) { ps = 0; pph ^= 1u; }
                 if (kb < w.nkb4) ++f4c;
             }
-            if (!live) continue;
+            if (aborted) break;
             // epilogue: the warp's 32 x kColsW slice of the tile (rows 32q.., columns kColsW*cq..)
             const int64_t rbase = m0 + 32 * q;
             const int64_t nb = n0 + kColsW * cq;
@@ -685,20 +727,35 @@ int num_sms_of_current_device() {
     return n > 0 ? n : 148;
 }
 
+// The test hook of tj_debug_gemm_fault, armed for the next launch that runs.
+int g_fault_skip_stage = -1;
+long long g_fault_wait_clk = 0;        // 0: the default bound kWaitClk
+
 // Persistent launch: one CTA per SM (or per tile, if fewer).
-cudaError_t launch_persistent(const CUtensorMap (&tm)[5], const GemmArgs &g, cudaStream_t s) {
+cudaError_t launch_persistent(const CUtensorMap (&tm)[5], const GemmArgs &g_in, cudaStream_t s) {
     static bool attr_set = false;
     if (!attr_set) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(k_gemm_nvfp4, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes + 1024);
+        cudaError_t e =
+            cudaFuncSetAttribute(k_gemm_nvfp4<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes + 1024);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_gemm_nvfp4<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes + 1024);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int ntiles = problem_works(g.pr[0]) + problem_works(g.pr[1]);
+    const int ntiles = problem_works(g_in.pr[0]) + problem_works(g_in.pr[1]);
     if (ntiles == 0) return cudaSuccess;
+    GemmArgs g = g_in;
+    const bool armed = g_fault_skip_stage >= 0 || g_fault_wait_clk > 0;
+    g.wait_clk = g_fault_wait_clk > 0 ? g_fault_wait_clk : kWaitClk;
+    g.skip_stage = g_fault_skip_stage;
+    g_fault_skip_stage = -1;
+    g_fault_wait_clk = 0;
     const int nsm = num_sms_of_current_device();
-    k_gemm_nvfp4<<<(unsigned)(ntiles < nsm ? ntiles : nsm), kThreadsGemm, kSmemBytes + 1024, s>>>(tm[0], tm[1], tm[2],
-                                                                                                tm[3], tm[4], g);
+    const unsigned grid = (unsigned)(ntiles < nsm ? ntiles : nsm);
+    if (armed)
+        k_gemm_nvfp4<true><<<grid, kThreadsGemm, kSmemBytes + 1024, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], g);
+    else
+        k_gemm_nvfp4<false><<<grid, kThreadsGemm, kSmemBytes + 1024, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], g);
     return cudaGetLastError();
 }
 
@@ -816,3 +873,11 @@ unsigned int read_and_clear_device_error() {
 }
 
 }  // namespace tj
+
+// Test hook: arm a fault for the next GEMM launch (see tj.h).
+extern "C" tj_status tj_debug_gemm_fault(int skip_stage, int64_t wait_clk) {
+    if (skip_stage < -1 || wait_clk < 0) return TJ_ERR_INVALID_ARG;
+    tj::g_fault_skip_stage = skip_stage;
+    tj::g_fault_wait_clk = (long long)wait_clk;
+    return TJ_OK;
+}

@@ -85,6 +85,7 @@ _SIGS = {
                                  _U64, _P, _I, _I64, _P],
     "tj_noalloc_scratch_bytes": [],
     "tj_get_device_status": [],
+    "tj_debug_gemm_fault": [_I, _I64],
     "tj_status_str": [_I],
 }
 EXPORTED = sorted(_SIGS)
