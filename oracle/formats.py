@@ -109,3 +109,80 @@ def e2m1_decode(code):
     c = np.asarray(code, dtype=np.int64)
     mag = E2M1_GRID[c & 7].astype(np.float64)
     return np.where(c & 8, -mag, mag)
+
+
+# ---------------------------------------------------------------------------
+# Element formats of an MX outlier slice.  The FP8 slice uses E4M3.  The mixed FP6 x FP4
+# variant of the slice (technical summary §5: the authors name FP6 x FP4 mixed precision
+# as a future direction, without a recipe) uses the FP6 formats E2M3 / E3M2 and the FP4
+# format E2M1.  Their definitions are those of the OCP Microscaling (MX) specification
+# v1.0, §5.3: no infinities or NaN, subnormals at the zero exponent,
+#   E2M3: bias 1, values m/8 (e = 0) and (1 + m/8) 2^(e-1), max 7.5;
+#   E3M2: bias 3, values m/4 2^-2 (e = 0) and (1 + m/4) 2^(e-3), max 28;
+#   E2M1: the grid above, max 6.
+# A code holds the sign in its top bit (bit 5 of a 6-bit code, bit 3 of a 4-bit code, bit 7
+# of an E4M3 byte).  The format numbers are the ones the tensor core uses.
+# ---------------------------------------------------------------------------
+MX_E4M3, MX_E2M3, MX_E3M2, MX_E2M1 = 0, 3, 4, 5
+MX_FORMATS = (MX_E4M3, MX_E2M3, MX_E3M2, MX_E2M1)
+MX_BITS = {MX_E4M3: 8, MX_E2M3: 6, MX_E3M2: 6, MX_E2M1: 4}
+MX_MAX = {MX_E4M3: 448.0, MX_E2M3: 7.5, MX_E3M2: 28.0, MX_E2M1: 6.0}
+
+
+def e2m3_decode(code):
+    """Signed E2M3 value of a 6-bit code, as float64."""
+    c = np.asarray(code, dtype=np.int64)
+    e = (c >> 3) & 3
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 1.0))
+    return np.where(c & 0x20, -mag, mag)
+
+
+def e3m2_decode(code):
+    """Signed E3M2 value of a 6-bit code, as float64."""
+    c = np.asarray(code, dtype=np.int64)
+    e = (c >> 2) & 7
+    m = (c & 3).astype(np.float64)
+    mag = np.where(e == 0, m / 4.0 * 0.25, (1.0 + m / 4.0) * np.exp2(e.astype(np.float64) - 3.0))
+    return np.where(c & 0x20, -mag, mag)
+
+
+def mx_elem_decode(code, fmt):
+    """Value (float64) of an MX element code of format fmt."""
+    if fmt == MX_E4M3:
+        return e4m3_decode(np.asarray(code, dtype=np.uint8))
+    if fmt == MX_E2M3:
+        return e2m3_decode(code)
+    if fmt == MX_E3M2:
+        return e3m2_decode(code)
+    if fmt == MX_E2M1:
+        return e2m1_decode(code)
+    raise ValueError("unknown MX element format %r" % (fmt,))
+
+
+def _mx_positive_codes(fmt):
+    """The non-negative finite codes of fmt in increasing order of value, and the values."""
+    n = {MX_E4M3: 0x7F, MX_E2M3: 32, MX_E3M2: 32, MX_E2M1: 8}[fmt]
+    codes = np.arange(n, dtype=np.int64)
+    return codes, mx_elem_decode(codes, fmt)
+
+
+def mx_rne_code(x, fmt):
+    """Code of the value of fmt nearest to x, ties to the even code, |x| beyond the maximum
+    -> the maximum (saturating).  Sign from the sign bit of x (so -0 and negative values
+    that round to zero give the negative zero code), as for the FP8 slice.
+
+    Brute force: the positive codes of every format here are ordered by value, and between
+    two neighbours the one with an even code has the even mantissa.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    codes, vals = _mx_positive_codes(fmt)
+    a = np.abs(x)
+    hi = np.minimum(np.searchsorted(vals, a, side="left"), len(vals) - 1)     # vals[hi] >= a
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - vals[lo], vals[hi] - a
+    pick_hi = (vals[hi] == a) | (d_hi < d_lo) | ((d_hi == d_lo) & ((codes[hi] & 1) == 0))
+    mag = np.where(pick_hi, codes[hi], codes[lo])
+    mag = np.where(a >= MX_MAX[fmt], codes[-1], mag)
+    sign = {MX_E4M3: 0x80, MX_E2M3: 0x20, MX_E3M2: 0x20, MX_E2M1: 0x8}[fmt]
+    return (mag | np.where(np.signbit(x), sign, 0)).astype(np.uint8)

@@ -14,6 +14,11 @@ NC = the other channels, ascending, K_N = K - k.  Readings:
   * channels are the input features K; normal channels are compacted in
     ascending order before blocking;
   * both operands of an outlier-slice product are MXFP8 (RTN, no RHT);
+  * the mixed FP6 x FP4 variant of the slice (technical summary §5 names FP6 x FP4 as
+    a future direction, no recipe): the slice operands take other MX element formats.
+    The forward operands choose theirs (e.g. X in E2M3, W in E2M1); in the backward the
+    re-aligned operand keeps its forward format and dY's slice takes the partner format
+    (SLICE_PARTNER), so that every slice product is FP6 x FP4 (or FP8 x FP8);
   * the backward re-quantizes the fp32 dequantized forward operands;
   * SR tags: 1 = dY rows (dX), 2 = dY^T rows (dW), 3 = W-hat^T, 4 = X-hat^T;
     RHT sign tags 0x100 (dX) and 0x101 (dW); alpha = 2^-7 undoes H^T H = 128 I.
@@ -22,6 +27,7 @@ All products are accumulated in fp64 on exactly dequantized operands.
 import numpy as np
 
 from . import quant as Q
+from .formats import MX_E2M1, MX_E2M3, MX_E3M2, MX_E4M3
 from .philox import rht_signs
 from .rht import rht_f32
 
@@ -29,6 +35,8 @@ F32 = np.float32
 TAG_DY_ROW, TAG_DY_COL, TAG_WT, TAG_XT = 1, 2, 3, 4
 TAG_RHT_DX, TAG_RHT_DW = 0x100, 0x101
 ALPHA_RHT = 2.0 ** -7
+# format of dY's slice in a backward product whose other slice operand has format f
+SLICE_PARTNER = {MX_E4M3: MX_E4M3, MX_E2M1: MX_E2M3, MX_E2M3: MX_E2M1, MX_E3M2: MX_E2M1}
 
 
 def normal_channels(K, outlier_idx):
@@ -38,19 +46,20 @@ def normal_channels(K, outlier_idx):
     return np.nonzero(mask)[0].astype(np.int64)
 
 
-def quantize_forward_operand(A, outlier_idx):
+def quantize_forward_operand(A, outlier_idx, fmt8=MX_E4M3):
     """Forward quantization of an operand [rows, K] along K (X or W).
 
     Returns dict(q=(codes, sf, outer) of the normal channels, RTN double-block,
-                 q8=(codes, scales) MXFP8 of the outlier channels or None).
+                 q8=(codes, scales) MX slice of the outlier channels in element format
+                 fmt8 (E4M3 = the FP8 slice) or None, fmt8).
     """
     A = np.asarray(A, dtype=F32)
     K = A.shape[1]
     o = np.asarray(outlier_idx, dtype=np.int64)
     nc = normal_channels(K, o)
     q = Q.quantize_nvfp4(A[:, nc], Q.RTN)
-    q8 = Q.quantize_mxfp8(A[:, o]) if len(o) else None
-    return {"q": q, "q8": q8, "K_N": len(nc), "k": len(o)}
+    q8 = Q.quantize_mx(A[:, o], fmt8) if len(o) else None
+    return {"q": q, "q8": q8, "fmt8": fmt8, "K_N": len(nc), "k": len(o)}
 
 
 def gemm_fp4(qa, qb, alpha=1.0):
@@ -65,13 +74,23 @@ def gemm_fp8(qa, qb):
     return Q.dequantize_mxfp8_f64(*qa) @ Q.dequantize_mxfp8_f64(*qb).T
 
 
-def forward(X, W, outlier_idx):
-    """Y = X-hat W-hat^T (fp64), plus the saved quantized forward operands."""
-    fx = quantize_forward_operand(X, outlier_idx)
-    fw = quantize_forward_operand(W, outlier_idx)
+def gemm_mx(qa, fmt_a, qb, fmt_b):
+    """deq(A) deq(B)^T in fp64 for two MX slice operands of element formats fmt_a, fmt_b."""
+    return Q.dequantize_mx_f64(*qa, fmt_a) @ Q.dequantize_mx_f64(*qb, fmt_b).T
+
+
+def _fmt8(fq):
+    return fq.get("fmt8", MX_E4M3)
+
+
+def forward(X, W, outlier_idx, fmt_x=MX_E4M3, fmt_w=MX_E4M3):
+    """Y = X-hat W-hat^T (fp64), plus the saved quantized forward operands.  fmt_x / fmt_w:
+    the element formats of the two outlier slices (E4M3: the FP8 slice)."""
+    fx = quantize_forward_operand(X, outlier_idx, fmt_x)
+    fw = quantize_forward_operand(W, outlier_idx, fmt_w)
     Y = gemm_fp4(fx["q"], fw["q"])
     if fx["q8"] is not None:
-        Y = Y + gemm_fp8(fx["q8"], fw["q8"])
+        Y = Y + gemm_mx(fx["q8"], fmt_x, fw["q8"], fmt_w)
     return Y, fx, fw
 
 
@@ -89,16 +108,18 @@ def deq_normal_f32(fq):
 
 def deq_outlier_f32(fq):
     """fp32 dequantized outlier slice, [rows, k]."""
-    return Q.dequantize_mxfp8_f32(*fq["q8"])[:, : fq["k"]]
+    return Q.dequantize_mx_f32(*fq["q8"], _fmt8(fq))[:, : fq["k"]]
 
 
 def bwd_dx_operands(dY, fw, seed):
-    """Quantized operands of dX: (S_dY, S_W, Q8(dY), Q8(W-hat_O^T))."""
+    """Quantized operands of dX: (S_dY, S_W, Q8(dY), Q8(W-hat_O^T)); the slices in
+    SLICE_PARTNER[f] and f, f the format of W's forward slice."""
     s_dy = sr_rht_rows(dY, seed, TAG_DY_ROW, TAG_RHT_DX)
     s_w = sr_rht_rows(deq_normal_f32(fw).T, seed, TAG_WT, TAG_RHT_DX)
     if fw["k"]:
-        q8_dy = Q.quantize_mxfp8(dY)
-        q8_w = Q.quantize_mxfp8(deq_outlier_f32(fw).T)
+        f = _fmt8(fw)
+        q8_dy = Q.quantize_mx(dY, SLICE_PARTNER[f])
+        q8_w = Q.quantize_mx(deq_outlier_f32(fw).T, f)
     else:
         q8_dy = q8_w = None
     return s_dy, s_w, q8_dy, q8_w
@@ -115,18 +136,21 @@ def bwd_dx(dY, fw, outlier_idx, seed):
     dX = np.zeros((M, K), dtype=np.float64)
     dX[:, nc] = gemm_fp4(s_dy, s_w, ALPHA_RHT)[:, : len(nc)]
     if len(o):
-        dX[:, o] = gemm_fp8(q8_dy, q8_w)[:, : len(o)]
+        f = _fmt8(fw)
+        dX[:, o] = gemm_mx(q8_dy, SLICE_PARTNER[f], q8_w, f)[:, : len(o)]
     return dX
 
 
 def bwd_dw_operands(dY, fx, seed):
-    """Quantized operands of dW: (S_dY^T, S_X, Q8(dY^T), Q8(X-hat_O^T))."""
+    """Quantized operands of dW: (S_dY^T, S_X, Q8(dY^T), Q8(X-hat_O^T)); the slices in
+    SLICE_PARTNER[f] and f, f the format of X's forward slice."""
     dYt = np.ascontiguousarray(np.asarray(dY, dtype=F32).T)
     s_dy = sr_rht_rows(dYt, seed, TAG_DY_COL, TAG_RHT_DW)
     s_x = sr_rht_rows(deq_normal_f32(fx).T, seed, TAG_XT, TAG_RHT_DW)
     if fx["k"]:
-        q8_dy = Q.quantize_mxfp8(dYt)
-        q8_x = Q.quantize_mxfp8(deq_outlier_f32(fx).T)
+        f = _fmt8(fx)
+        q8_dy = Q.quantize_mx(dYt, SLICE_PARTNER[f])
+        q8_x = Q.quantize_mx(deq_outlier_f32(fx).T, f)
     else:
         q8_dy = q8_x = None
     return s_dy, s_x, q8_dy, q8_x
@@ -143,7 +167,8 @@ def bwd_dw(dY, fx, outlier_idx, seed):
     dW = np.zeros((N, K), dtype=np.float64)
     dW[:, nc] = gemm_fp4(s_dy, s_x, ALPHA_RHT)[:, : len(nc)]
     if len(o):
-        dW[:, o] = gemm_fp8(q8_dy, q8_x)[:, : len(o)]
+        f = _fmt8(fx)
+        dW[:, o] = gemm_mx(q8_dy, SLICE_PARTNER[f], q8_x, f)[:, : len(o)]
     return dW
 
 

@@ -31,6 +31,7 @@ import numpy as np
 
 from .formats import E2M1_GRID, e2m1_decode, e4m3_decode, e4m3_inner_scale_byte
 from .formats import e4m3_rne_satfinite_byte, ue8m0_decode
+from .formats import MX_E4M3, MX_MAX, mx_elem_decode, mx_rne_code
 from .philox import sr_uniform16
 
 F32 = np.float32
@@ -188,3 +189,49 @@ def dequantize_mxfp8_f64(codes, sbytes):
 def dequantize_mxfp8_f32(codes, sbytes):
     """fp32 values of an MXFP8 slice (exact: an E4M3 value times a power of two)."""
     return dequantize_mxfp8_f64(codes, sbytes).astype(F32)
+
+
+# ---------------------------------------------------------------------------
+# The outlier slice in any MX element format (E4M3, or the FP6 / FP4 formats of the mixed
+# FP6 x FP4 variant, technical summary §5).  Reading: the FP8 slice's rule with the
+# format's own maximum: E = the smallest integer with max_fmt * 2^E >= amax_32, clamped
+# to [-127, 127] (0 for an all-zero block); elements x * 2^-E rounded to the nearest
+# value of the format, ties to even, saturating.  With E4M3 this is quantize_mxfp8.
+# ---------------------------------------------------------------------------
+def mx_exponent_fmt(amax, fmt):
+    """Smallest integer E with MX_MAX[fmt] * 2^E >= amax (amax > 0), clamped to [-127, 127]."""
+    amax = np.asarray(amax, dtype=np.float64)
+    mant, ex = np.frexp(amax)                       # amax = mant * 2^ex, mant in [0.5, 1)
+    mf, exf = np.frexp(MX_MAX[fmt])                 # the format's maximum, the same way
+    # max * 2^E >= amax  <=>  2^(exf + E - ex) >= mant / mf, and 1/2 < mant / mf < 2
+    E = np.where(mant <= mf, ex - exf, ex - exf + 1)
+    E = np.where(amax > 0, E, 0)
+    return np.clip(E, -127, 127).astype(np.int64)
+
+
+def quantize_mx(x, fmt, pad_to=128):
+    """MX quantize rows of x [R, L] along L (zero-padded to `pad_to`) in element format fmt.
+
+    Returns (codes uint8 [R, Lp], one code per element; scale bytes uint8 [R, Lp/32] UE8M0).
+    """
+    xp = pad_cols(x, pad_to)
+    R, Lp = xp.shape
+    xb = xp.reshape(R, Lp // MX, MX)
+    amax = np.abs(xb).max(axis=2)
+    E = mx_exponent_fmt(amax, fmt)
+    scale_inv = np.exp2(-E.astype(np.float64))
+    y = xb.astype(np.float64) * scale_inv[:, :, None]          # exact: a power of two
+    codes = mx_rne_code(y, fmt)
+    return codes.reshape(R, Lp), (E + 127).astype(np.uint8)
+
+
+def dequantize_mx_f64(codes, sbytes, fmt):
+    """Exact fp64 values of an MX slice of element format fmt."""
+    v = mx_elem_decode(codes, fmt)
+    s = np.repeat(ue8m0_decode(sbytes), MX, axis=1)
+    return v * s
+
+
+def dequantize_mx_f32(codes, sbytes, fmt):
+    """fp32 values of an MX slice (exact: a short-mantissa value times a power of two)."""
+    return dequantize_mx_f64(codes, sbytes, fmt).astype(F32)
