@@ -33,9 +33,15 @@
  *     outer  float [cols_p/128][rows_p] FP32 outer scales (one per 1x128 block),
  *                                        block-major so one block's scales for 128
  *                                        consecutive rows are contiguous.
- *   MXFP8 outlier slice (tj_mxfp8), logical [rows, cols] along cols:
- *     codes  uint8 [rows_p][cols_p]     E4M3 values.
+ *   MX outlier slice (tj_mxfp8), logical [rows, cols] along cols, element format fmt:
+ *     codes  uint8 [rows_p][cols_p*bits/8]  packed element codes of `bits` bits each:
+ *              E4M3 (8 bits): one byte per element;
+ *              E2M3 / E3M2 (6 bits): each row is a little-endian bit stream, element c at
+ *                bits 6c .. 6c+5 (16 elements in 12 bytes), sign in the code's bit 5;
+ *              E2M1 (4 bits): element 2j in the low nibble of byte j, sign in bit 3.
  *     sf     uint8 [rows_p*cols_p/32]   UE8M0 scales (one per 1x32 group), tile layout.
+ *   The packed FP6 / FP4 rows are the tensor core's operand order: the GEMM's TMA copies
+ *   expand each 16-element run into the 16-byte shared-memory slot the MMA reads.
  *   Scale tile layout (both formats; B = 16 for NVFP4, 32 for MXFP8): the scales
  *   form tiles of 128 rows x 4 consecutive groups; tile (rt, kt) starts at byte
  *   (rt * (cols_p / (4*B)) + kt) * 512; inside it, the scale of row
@@ -87,12 +93,23 @@ typedef struct {
     int64_t cols;
 } tj_nvfp4;
 
-/* MXFP8 outlier slice (caller-owned device buffers; layout above). */
+/* Element formats of an MX outlier slice (the tensor core's own format numbers).  E4M3 is
+ * the FP8 slice (§2.C); E2M3 / E3M2 (FP6) and E2M1 (FP4) serve the mixed FP6 x FP4
+ * variant of the slice, which the pages name as a future direction (§5).  E2M3: bias 1,
+ * max 7.5; E3M2: bias 3, max 28; E2M1: max 6; no infinities or NaN (OCP MX v1.0). */
+typedef enum { TJ_MX_E4M3 = 0, TJ_MX_E2M3 = 3, TJ_MX_E3M2 = 4, TJ_MX_E2M1 = 5 } tj_mx_format;
+
+/* MX outlier slice (caller-owned device buffers; layout above).  fmt is a tj_mx_format;
+ * a zero-initialised descriptor is E4M3.  Slices in E2M3 / E3M2 / E2M1 need 32-byte aligned
+ * codes (TJ_ERR_ALIGN otherwise); an unknown fmt is TJ_ERR_INVALID_ARG.  Every call that
+ * writes a slice writes it in its descriptor's format; every call that reads one decodes
+ * its descriptor's format. */
 typedef struct {
     uint8_t *codes;
     uint8_t *sf;
     int64_t rows;
     int64_t cols;
+    int32_t fmt;
 } tj_mxfp8;
 
 /* Philox tags used inside the backward calls (documented for reproducibility):
@@ -133,6 +150,8 @@ tj_status tj_quantize_nvfp4(const void *x, int dtype, int64_t rows_x, int64_t co
 /* tj_quantize_mxfp8 - FP8 outlier slice (§2.C "kept in higher precision, e.g.
  * FP8"): E4M3 values with a UE8M0 scale 2^E per 1x32 group, E the smallest
  * integer with 448*2^E >= amax_32, values rounded to nearest-even and saturated.
+ * With out->fmt = E2M3 / E3M2 / E2M1 the same rule with that format's maximum (7.5 / 28
+ * / 6) in place of 448 (sign of a value that rounds to zero kept, as for E4M3).
  * Same x / along_cols / sel conventions as tj_quantize_nvfp4 (no RHT, no SR). */
 tj_status tj_quantize_mxfp8(const void *x, int dtype, int64_t rows_x, int64_t cols_x, int64_t ld,
                             int along_cols, const int32_t *sel, int64_t n_sel,
@@ -172,7 +191,8 @@ tj_status tj_requantize_nvfp4(const tj_nvfp4 *in, int mode, int rht, uint64_t se
                               tj_nvfp4 *out, void *stream);
 
 /* tj_requantize_mxfp8 - the same re-alignment for an FP8 outlier slice: out[c, r] =
- * Q8(X-hat_O[:, c]) along r (RTN, no RHT), in [rows, cols] -> out [cols, rows]. */
+ * Q8(X-hat_O[:, c]) along r (RTN, no RHT), in [rows, cols] -> out [cols, rows].  X-hat_O
+ * is decoded in in->fmt and re-quantized in out->fmt. */
 tj_status tj_requantize_mxfp8(const tj_mxfp8 *in, tj_mxfp8 *out, void *stream);
 
 /* tj_rht - standalone random Hadamard transform (§2.C): for each row of x (fp32,
@@ -186,8 +206,8 @@ tj_status tj_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t 
  * [rows, cols] (row stride ldy).  The value the aligned backward re-quantizes. */
 tj_status tj_dequantize_nvfp4(const tj_nvfp4 *q, float *y, int64_t ldy, void *stream);
 
-/* tj_dequantize_mxfp8 - fp32 values (E4M3 value x 2^(e - 127)) of a tj_mxfp8 into y
- * [rows, cols] (row stride ldy); exact.  For inspecting the FP8 slices (§2.C). */
+/* tj_dequantize_mxfp8 - fp32 values (element value x 2^(e - 127), in q->fmt) of a
+ * tj_mxfp8 into y [rows, cols] (row stride ldy); exact.  For inspecting the slices (§2.C). */
 tj_status tj_dequantize_mxfp8(const tj_mxfp8 *q, float *y, int64_t ldy, void *stream);
 
 /* tj_gemm_nvfp4 - block-scaled FP4 GEMM with FP32 outer-scale promotion:
@@ -195,7 +215,8 @@ tj_status tj_dequantize_mxfp8(const tj_mxfp8 *q, float *y, int64_t ldy, void *st
  *             block kb of  (a s_iA)(b s_iB))  [+ sum over the FP8 slice a8 b8]
  * A [M, K] and B [N, K] are both quantized along K (tcgen05 kind::mxf4nvf4,
  * UE4M3 per 16; optional FP8 part kind::mxf8f6f4, UE8M0 per 32, accumulated into
- * the same tile).  a8/b8 may be NULL (no FP8 part).  D is row-major [M, N] with
+ * the same tile).  The slice operands may have any two element formats (a8->fmt,
+ * b8->fmt: e.g. E2M3 x E2M1, the FP6 x FP4 slice); this holds for every GEMM call.  a8/b8 may be NULL (no FP8 part).  D is row-major [M, N] with
  * row stride ldd, fp32 or bf16 (out_dtype); col_map (may be NULL) scatters
  * column n of the product to column col_map[n] of D.  The product of one 16-group
  * is exact; the FP32 accumulation is the only rounding (within 2e-3 sum|a||b|). */
@@ -238,6 +259,9 @@ tj_status tj_gemm_pair_f32(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, co
  * weights and gradients of every linear layer; §2.A RTN double-block quantization;
  * §2.C static outlier channels kept in FP8):
  *   Y[M, N] = Q(X[:, NC]) Q(W[:, NC])^T + Q8(X[:, O]) Q8(W[:, O])^T
+ * The slices take the formats of their descriptors: X's slice is quantized in x8->fmt, and
+ * w8 holds W's in w8->fmt (E4M3 both for the FP8 slice; e.g. E2M3 and E2M1 for the
+ * FP6 x FP4 variant).
  * x           bf16 [M, K], row stride ldx.
  * wq, w8      W's forward operands: NVFP4 [N, K_N] and FP8 slice [N, k] (w8 NULL iff
  *             k == 0), e.g. from tj_quantize_nvfp4/_mxfp8 with sel = normal_idx /
@@ -257,6 +281,9 @@ tj_status tj_linear_fwd(const void *x, int64_t M, int64_t K, int64_t ldx, const 
  * FP8 outlier columns):
  *   dX[:, NC] = 2^-7 SR(RHT(dY)) SR(RHT(W-hat_NC^T))^T   (RHT along N, tags above)
  *   dX[:, O]  = Q8(dY) Q8(W-hat_O^T)^T                   (RTN, no RHT)
+ * Slice formats: W-hat_O^T keeps w8->fmt and dY's slice takes the partner format (E4M3 for
+ * E4M3, E2M3 for E2M1, E2M1 for E2M3 or E3M2), so the slice product is FP8 x FP8 or
+ * FP6 x FP4.  The workspace reserves each slice's FP8 size whatever its format.
  * W-hat is read from the forward operands wq / w8 (never the master weight).
  * dy bf16 [M, N] (lddy); dx [M, K] bf16 or fp32 (lddx); seed = per-step Philox key.
  * workspace: at least tj_workspace_size(TJ_OP_BWD_DX, M, N, K, k) bytes, 256-aligned.
@@ -272,6 +299,8 @@ tj_status tj_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, c
 /* tj_linear_bwd_dw - weight gradient:
  *   dW[:, NC] = 2^-7 SR(RHT(dY^T)) SR(RHT(X-hat_NC^T))^T  (RHT along M)
  *   dW[:, O]  = Q8(dY^T) Q8(X-hat_O^T)^T
+ * Slice formats: X-hat_O^T keeps x8->fmt and dY^T's slice takes the partner format (as
+ * for dX).
  * xq / x8 are the saved forward context of tj_linear_fwd.  dw fp32 [N, K] (lddw).
  * The workspace then holds S_dY^T (tj_nvfp4 [N, M]), S_X (tj_nvfp4 [K_N, M]) and when
  * k > 0 Q8(dY^T) (tj_mxfp8 [N, M]) and Q8(X-hat_O^T) (tj_mxfp8 [k, M]), laid out as for dX.

@@ -47,13 +47,21 @@ tj_status check_nv(const tj_nvfp4 *q, int64_t rows, int64_t cols) {
     return TJ_OK;
 }
 
+// An MX slice: a known element format; packed FP6 / FP4 codes start on 32 bytes (the
+// tensor maps of the packed sub-byte types require it).
 tj_status check_mx(const tj_mxfp8 *q, int64_t rows, int64_t cols) {
     if (q == nullptr || q->codes == nullptr || q->sf == nullptr) return TJ_ERR_INVALID_ARG;
+    if (!mx_fmt_valid(q->fmt)) return TJ_ERR_INVALID_ARG;
     if (q->rows != rows || q->cols != cols || rows < 0 || cols < 0) return TJ_ERR_SHAPE;
     if (!blocks_fit(rows, cols)) return TJ_ERR_SHAPE;
     if (!al16(q->codes) || !al16(q->sf)) return TJ_ERR_ALIGN;
+    if (q->fmt != kMxE4M3 && (reinterpret_cast<uintptr_t>(q->codes) & 31) != 0) return TJ_ERR_ALIGN;
     return TJ_OK;
 }
+
+// Format of dY's slice in a backward product whose other slice operand has format f: the
+// FP8 slice stays FP8 x FP8, the FP6 / FP4 formats pair up as FP6 x FP4.
+int slice_partner(int f) { return f == kMxE4M3 ? kMxE4M3 : (f == kMxE2M1 ? kMxE2M3 : kMxE2M1); }
 
 int64_t nv_bytes(int64_t rows, int64_t cols) {
     const int64_t rp = round_up(rows, 128), cp = round_up(cols, 128);
@@ -78,7 +86,8 @@ tj_nvfp4 carve_nv(uint8_t *&cur, int64_t rows, int64_t cols) {
     q.cols = cols;
     return q;
 }
-tj_mxfp8 carve_mx(uint8_t *&cur, int64_t rows, int64_t cols) {
+// (the FP8 size is reserved whatever the format, so the workspace layout does not depend on it)
+tj_mxfp8 carve_mx(uint8_t *&cur, int64_t rows, int64_t cols, int fmt = kMxE4M3) {
     const int64_t rp = round_up(rows, 128), cp = round_up(cols, 128);
     tj_mxfp8 q;
     q.codes = cur;
@@ -87,6 +96,7 @@ tj_mxfp8 carve_mx(uint8_t *&cur, int64_t rows, int64_t cols) {
     cur += round_up(rp * cp / 32, 256);
     q.rows = rows;
     q.cols = cols;
+    q.fmt = fmt;
     return q;
 }
 
@@ -375,8 +385,9 @@ tj_status tj_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, c
     tj_nvfp4 s_w = carve_nv(cur, kn, N);
     tj_mxfp8 q8_dy{}, q8_w{};
     if (k > 0) {
-        q8_dy = carve_mx(cur, M, N);
-        q8_w = carve_mx(cur, k, N);
+        // W-hat_O^T keeps the forward slice's format, dY takes its partner
+        q8_dy = carve_mx(cur, M, N, slice_partner(w8->fmt));
+        q8_w = carve_mx(cur, k, N, w8->fmt);
     }
     // dY rows: RHT along N + SR (the dX operand), and with an outlier slice also the
     // MXFP8 rows of dY, from one read; W-hat^T re-aligned with the same signs
@@ -388,7 +399,7 @@ tj_status tj_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, c
                                      TJ_TAG_RHT_DX, s_dy, s));
     TJ_TRY(launch_realign_nv(*wq, s_w, TJ_SR, 1, seed, TJ_TAG_WT, TJ_TAG_RHT_DX, s));
     if (k > 0) {
-        // the FP4 product (normal columns of dX) and the FP8 slice (outlier columns) in one launch
+        // the FP4 product (normal columns of dX) and the slice (outlier columns) in one launch
         TJ_TRY(launch_realign_mx(*w8, q8_w, s));
         TJ_TRY(launch_gemm_pair(&s_dy, &s_w, 0.0078125f, dx, out_dtype, lddx, M, kn, normal_idx, &q8_dy, &q8_w, dx,
                                 out_dtype, lddx, M, k, outlier_idx, s));
@@ -418,8 +429,9 @@ tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, c
     tj_nvfp4 s_x = carve_nv(cur, kn, M);
     tj_mxfp8 q8_dy{}, q8_x{};
     if (k > 0) {
-        q8_dy = carve_mx(cur, N, M);
-        q8_x = carve_mx(cur, k, M);
+        // X-hat_O^T keeps the forward slice's format, dY^T takes its partner
+        q8_dy = carve_mx(cur, N, M, slice_partner(x8->fmt));
+        q8_x = carve_mx(cur, k, M, x8->fmt);
     }
     // dY^T rows (RHT along M + SR), and with an outlier slice also the MXFP8 rows of
     // dY^T, from one read; X-hat^T re-aligned with the same signs
@@ -433,7 +445,7 @@ tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, c
     // dW [N][K] is fp32 and covered by the launch, so a long-K launch may split K in two
     const SplitRegion whole_dw{dw, N, K, lddw};
     if (k > 0) {
-        // the FP4 product (normal columns of dW) and the FP8 slice (outlier columns) in one launch
+        // the FP4 product (normal columns of dW) and the slice (outlier columns) in one launch
         TJ_TRY(launch_realign_mx(*x8, q8_x, s));
         TJ_TRY(launch_gemm_pair(&s_dy, &s_x, 0.0078125f, dw, TJ_FP32, lddw, N, kn, normal_idx, &q8_dy, &q8_x, dw,
                                 TJ_FP32, lddw, N, k, outlier_idx, s, &whole_dw));

@@ -8,7 +8,8 @@
 // 4 scale factors per K = 64 MMA); the per-128 FP32 scales differ per row and per
 // block, so every 128-K block is accumulated into its own tensor-memory partial P
 // and promoted by CUDA cores:  acc[m, n] += sA[m, kb] * sB[n, kb] * P[m, n].
-// The FP8 slice (kind::mxf8f6f4, UE8M0 per 32) has only power-of-two scales and
+// The outlier slice (kind::mxf8f6f4, UE8M0 per 32; E4M3 operands, or the FP6 / FP4
+// formats of the FP6 x FP4 variant in any pairing) has only power-of-two scales and
 // accumulates over its whole K into one tensor-memory buffer added at the end.
 //
 // Persistent CTAs (one per SM) walk the 128 x 128 output tiles; every CTA loads its
@@ -122,6 +123,9 @@ struct GemmArgs {
     int64_t rpa, rpb;             // rows_p of A and B
     const uint8_t *sfa8, *sfb8;   // scale tiles, FP8 operands (of whichever product has FP8 stages)
     int64_t ntk_a8, ntk_b8;       // cols_p / 128
+    uint32_t tx8;                 // bytes one slice stage brings in: both operand tiles (128 rows x 128
+                                  // elements of 8, 6 or 4 bits, as stored in HBM) and two scale tiles
+    uint32_t idesc8;              // the slice's element formats in the instruction descriptor (bits 7-12)
     long long wait_clk;           // bound of every mbarrier wait, in SM clocks
     int skip_stage;               // test hook: the producers never load this stage of each CTA (-1: none)
 };
@@ -372,8 +376,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     if (kTestHook && it == args.skip_stage) continue;
                     // operands, their scale-factor tiles and, for FP4 stages, the FP32 outer
                     // scales of the stage's blocks all land on one barrier
-                    ptx::mbar_arrive_expect_tx(&bars->full[slot],
-                                               2u * kTileBytes + 2u * sfbytes + (uint32_t)nkbs * 1024u);
+                    ptx::mbar_arrive_expect_tx(&bars->full[slot], fp4 ? 2u * kTileBytes + 2u * sfbytes + (uint32_t)nkbs * 1024u
+                                                                   : args.tx8);
                     ptx::tma_load_2d(sa, fp4 ? &tm_a4 : &tm_a8, k0 * 128, (int32_t)w.m0, &bars->full[slot]);
                     ptx::tma_load_2d(sb, fp4 ? &tm_b4 : &tm_b8, k0 * 128, (int32_t)w.n0, &bars->full[slot]);
                     if (fp4) {
@@ -476,7 +480,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             ptx::mma_mxf8(tbase + kColP + 128u * ps, ptx::smem_desc(sa + 32u * j, 16, 1024, 2),
-                                          ptx::smem_desc(sb + 32u * j, 16, 1024, 2), idesc_mxf8((uint32_t)j), sfcol,
+                                          ptx::smem_desc(sb + 32u * j, 16, 1024, 2), idesc_mxf8((uint32_t)j) | args.idesc8, sfcol,
                                           sfcol + 4, (uint32_t)(s8 > 0 || j > 0));
                         }
                         if (s8 == w.nk8 - 1) ptx::tc_commit(&bars->pfull[ps]);
@@ -706,6 +710,27 @@ bool make_tile_map(CUtensorMap *m, const void *base, int64_t rows_p, int64_t row
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An MX slice operand [rows_p][cols_p] of element format fmt -> boxes of 128 rows x 128
+// elements.  E4M3 rows are plain bytes.  Packed E2M3 / E3M2 / E2M1 rows use the packed
+// sub-byte tensor-map types, whose copies expand each run of 16 codes (12 or 8 bytes in
+// HBM) into the 16-byte shared-memory slot the f8f6f4 MMA reads, so the shared tile has the
+// E4M3 tile's shape; coordinates count elements, and a box moves 128 x 96 or 128 x 64
+// bytes of HBM (the transaction count its barrier sees).
+bool make_mx_map(CUtensorMap *m, const void *base, int64_t rows_p, int64_t cols_p, int fmt) {
+    if (fmt == kMxE4M3) return make_tile_map(m, base, rows_p, cols_p, 128u);
+    EncodeTiledFn enc = get_encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols_p, (cuuint64_t)rows_p};
+    const cuuint64_t strides[1] = {(cuuint64_t)(cols_p * mx_bits(fmt) / 8)};
+    const cuuint32_t box[2] = {128u, 128u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUtensorMapDataType t =
+        fmt == kMxE2M1 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B;
+    return enc(m, t, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // bf16 output [M][ldd] -> boxes of 32 rows x kColsW columns (one promotion warp's slice),
 // swizzled to the row width (128 or 64 bytes), for the epilogue's TMA stores.
 bool make_out_map(CUtensorMap *m, void *d, int64_t M, int64_t N, int64_t ldd) {
@@ -809,7 +834,9 @@ bool set_fp4(const tj_nvfp4 &a, const tj_nvfp4 &b, GemmArgs &g, CUtensorMap (&tm
     return make_tile_map(&tm[0], a.codes, g.rpa, kp / 2, 128u) && make_tile_map(&tm[1], b.codes, g.rpb, kp / 2, 128u);
 }
 
-// FP8 operands -> tensor maps 2/3 and the scale pointers; returns the 128-K stage count.
+// Slice operands (FP8, or FP6 / FP4 in any pairing) -> tensor maps 2/3, the scale pointers,
+// the stage's transaction bytes and the formats of the instruction descriptor; returns the
+// 128-K stage count.
 bool set_fp8(const tj_mxfp8 &a8, const tj_mxfp8 &b8, GemmArgs &g, CUtensorMap (&tm)[5], int &nk8) {
     const int64_t kp8 = round_up(a8.cols, 128);
     nk8 = (int)(kp8 / 128);
@@ -817,8 +844,10 @@ bool set_fp8(const tj_mxfp8 &a8, const tj_mxfp8 &b8, GemmArgs &g, CUtensorMap (&
     g.sfb8 = b8.sf;
     g.ntk_a8 = kp8 / 128;
     g.ntk_b8 = kp8 / 128;
-    return make_tile_map(&tm[2], a8.codes, round_up(a8.rows, 128), kp8, 128u) &&
-           make_tile_map(&tm[3], b8.codes, round_up(b8.rows, 128), kp8, 128u);
+    g.tx8 = (uint32_t)(128 * 128 * (mx_bits(a8.fmt) + mx_bits(b8.fmt)) / 8 + 2 * 512);
+    g.idesc8 = ((uint32_t)a8.fmt << 7) | ((uint32_t)b8.fmt << 10);
+    return make_mx_map(&tm[2], a8.codes, round_up(a8.rows, 128), kp8, a8.fmt) &&
+           make_mx_map(&tm[3], b8.codes, round_up(b8.rows, 128), kp8, b8.fmt);
 }
 
 // Plain bf16 outputs (no column map, 16-byte row pitch) of a single-product launch leave the

@@ -100,27 +100,61 @@ struct SrcNv {
     }
 };
 
-// MXFP8 slice [rows, cols] read back as fp32 (E4M3 value times 2^(byte-127)).
+// MX slice [rows, cols] read back as fp32 (element value times 2^(byte-127)), in the
+// slice's element format (E4M3 bytes, packed 6-bit E2M3 / E3M2 or packed 4-bit E2M1).
 struct SrcMx {
     const uint8_t *codes, *sf;
     int64_t rows, cols, rows_p, cols_p;
+    int fmt;
+    __device__ __forceinline__ float scale(int64_t r, int64_t c) const {
+        const int64_t g = c >> 5;
+        const int e = (int)sf[sf_word_offset(r, g >> 2, cols_p / 128) + (g & 3)] - 127;
+        return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x400000u);
+    }
+    __device__ __forceinline__ float value(uint32_t code) const {
+        return fmt == kMxE4M3 ? e4m3_to_float(code)
+                              : (fmt == kMxE2M1 ? e2m1_to_float(code)
+                                                : (fmt == kMxE2M3 ? e2m3_to_float(code) : e3m2_to_float(code)));
+    }
     __device__ __forceinline__ float load(int64_t r, int64_t c) const {
         if (r >= rows || c >= cols) return 0.0f;
-        const float v = e4m3_to_float(codes[r * cols_p + c]);
-        const int64_t g = c >> 5;
-        const int e = (int)sf[sf_word_offset(r, g >> 2, cols_p / 128) + (g & 3)] - 127;
-        const float s = e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x400000u);
-        return __fmul_rn(v, s);
+        const uint8_t *row = codes + r * (cols_p * mx_bits(fmt) / 8);
+        uint32_t code;
+        if (fmt == kMxE4M3) {
+            code = row[c];
+        } else if (fmt == kMxE2M1) {
+            code = (row[c >> 1] >> (4 * (c & 1))) & 15u;
+        } else {                                       // bits 6c .. 6c+5 of the row
+            const int64_t b = (6 * c) >> 3;
+            const int sh = (int)((6 * c) & 7);
+            uint32_t w = row[b];
+            if (sh > 2) w |= (uint32_t)row[b + 1] << 8;   // the code spills into the next byte
+            code = (w >> sh) & 63u;
+        }
+        return __fmul_rn(value(code), scale(r, c));
     }
-    // elem(r, c .. c+7), c a multiple of 8, inside the padded tensor: one 8-byte load
-    // (never used with the RHT: flip must be 0)
+    // elem(r, c .. c+7), c a multiple of 8, inside the padded tensor: one 8-, 6- or 4-byte
+    // read of the eight codes (never used with the RHT: flip must be 0)
     __device__ __forceinline__ void load8(int64_t r, int64_t c, float (&v)[8], uint32_t flip = 0u) const {
-        const uint2 w = *reinterpret_cast<const uint2 *>(codes + r * cols_p + c);
-        const int64_t g = c >> 5;
-        const int e = (int)sf[sf_word_offset(r, g >> 2, cols_p / 128) + (g & 3)] - 127;
-        const float s = e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x400000u);
+        const float s = scale(r, c);
+        if (fmt == kMxE4M3) {
+            const uint2 w = *reinterpret_cast<const uint2 *>(codes + r * cols_p + c);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = __fmul_rn(e4m3_to_float(((k < 4 ? w.x : w.y) >> (8 * (k & 3))) & 0xFFu), s);
+            for (int k = 0; k < 8; ++k) v[k] = __fmul_rn(e4m3_to_float(((k < 4 ? w.x : w.y) >> (8 * (k & 3))) & 0xFFu), s);
+        } else if (fmt == kMxE2M1) {
+            const uint32_t w = *reinterpret_cast<const uint32_t *>(codes + r * (cols_p / 2) + (c >> 1));
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = __fmul_rn(e2m1_to_float((w >> (4 * k)) & 15u), s);
+        } else {                                       // 6 bytes at a 2-byte boundary
+            const uint16_t *p = reinterpret_cast<const uint16_t *>(codes + r * (cols_p / 4 * 3) + (c / 4) * 3);
+            const uint64_t w = (uint64_t)p[0] | ((uint64_t)p[1] << 16) | ((uint64_t)p[2] << 32);
+            const bool e3 = fmt == kMxE3M2;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t code = (uint32_t)(w >> (6 * k)) & 63u;
+                v[k] = __fmul_rn(e3 ? e3m2_to_float(code) : e2m3_to_float(code), s);
+            }
+        }
     }
 };
 
@@ -203,14 +237,14 @@ __global__ void __launch_bounds__(256, (SR || RHT) ? 3 : 4) k_quant_rows(Src src
         }
         if (FMT != 1) {
             if (FMT == 2) {
-                const MxSeg m = quant_mxfp8_group(x);
+                const MxSeg m = quant_mx_group(x, omx.fmt);
                 store_mx_seg(omx, row, kb, t, m, valid);
             }
             if (RHT) rht128_quad(x, sign_word, t);
             const NvSeg s = quant_nvfp4_seg<SR>(x, (uint64_t)(row * cols_p + kb * 128 + 32 * t), pk, tag);
             store_nv_seg(onv, row, kb, t, s, valid);
         } else {
-            const MxSeg s = quant_mxfp8_group(x);
+            const MxSeg s = quant_mx_group(x, omx.fmt);
             store_mx_seg(omx, row, kb, t, s, valid);
         }
     }
@@ -262,15 +296,14 @@ __global__ void __launch_bounds__(256, (FMT == 0 && !SR && !RHT) ? 5 : 4) k_quan
     if (FMT != 1) {
         const uint32_t sign_word = t == 0 ? sbits.x : (t == 1 ? sbits.y : (t == 2 ? sbits.z : sbits.w));
         if (FMT == 2) {
-            MxSeg m = quant_mxfp8_group(x);
-            if (RHT) mx_unflip(m, sign_word);
+            const MxSeg m = quant_mx_group<RHT>(x, omx.fmt, sign_word);
             store_mx_seg(omx, row, kb, t, m, valid);
         }
         if (RHT) rht128_quad<false>(x, sign_word, t);
         const NvSeg s = quant_nvfp4_seg<SR>(x, (uint64_t)(row * cols_p + r0 + 32 * t), pk, tag);
         store_nv_seg(onv, row, kb, t, s, valid);
     } else {
-        const MxSeg s = quant_mxfp8_group(x);
+        const MxSeg s = quant_mx_group(x, omx.fmt);
         store_mx_seg(omx, row, kb, t, s, valid);
     }
 }
@@ -415,7 +448,7 @@ __global__ void __launch_bounds__(kSplitThreads) k_quant_split(const T *x, int64
             const int r = ok ? task / nseg_o : 0, kb = ok ? task - r * nseg_o : 0;
             float v[32];
             split_gather32<T>(reinterpret_cast<const uint8_t *>(tile + r * rw), tab_o + split_pad_tab(kb * 128 + 32 * t), v);
-            const MxSeg m = quant_mxfp8_group(v);
+            const MxSeg m = quant_mx_group(v, omx.fmt);
             store_mx_seg(omx, r0 + r, kb, t, m, ok && r0 + r < omx.rows_p);
         }
     }
@@ -482,7 +515,9 @@ int64_t row_grid(int64_t total_segments) {
 OutNv out_nv(const tj_nvfp4 &q) {
     return OutNv{q.codes, q.sf, q.outer, round_up(q.rows, 128), round_up(q.cols, 128)};
 }
-OutMx out_mx(const tj_mxfp8 &q) { return OutMx{q.codes, q.sf, round_up(q.rows, 128), round_up(q.cols, 128)}; }
+OutMx out_mx(const tj_mxfp8 &q) {
+    return OutMx{q.codes, q.sf, round_up(q.rows, 128), round_up(q.cols, 128), (int)q.fmt};
+}
 
 template <typename Src, int FMT = 0>
 cudaError_t rows_nv(const Src &src, const OutNv &o, int mode, int rht, uint64_t seed, uint32_t tag,
@@ -527,7 +562,7 @@ SrcNv src_nv(const tj_nvfp4 &q) {
     return SrcNv{q.codes, q.sf, q.outer, q.rows, q.cols, round_up(q.rows, 128), round_up(q.cols, 128)};
 }
 SrcMx src_mx(const tj_mxfp8 &q) {
-    return SrcMx{q.codes, q.sf, q.rows, q.cols, round_up(q.rows, 128), round_up(q.cols, 128)};
+    return SrcMx{q.codes, q.sf, q.rows, q.cols, round_up(q.rows, 128), round_up(q.cols, 128), (int)q.fmt};
 }
 
 // Dense input (bf16 / fp32) -> NVFP4, either orientation.  n_cols_sel = number of

@@ -173,9 +173,31 @@ __device__ __forceinline__ NvSeg quant_nvfp4_seg(const float (&x)[32], uint64_t 
 }
 
 struct MxSeg {
-    uint4 codes[2];  // 32 E4M3 bytes
+    uint4 codes[2];  // the group's packed codes: 32 bytes (E4M3), 24 (E2M3 / E3M2) or 16 (E2M1)
     uint32_t e8;     // UE8M0 scale byte
 };
+
+// Block exponent of an MX group: the smallest integer E with max * 2^E >= amax, for a
+// format maximum max = (1 + f) 2^emax whose fraction bits are `manlim` (448: 8 and
+// 0x600000; 7.5: 2 and 0x700000; 28: 4 and 0x600000; 6: 2 and 0x400000), clamped to
+// [-127, 127]; 0 for an all-zero group.
+__device__ __forceinline__ int mx_block_exponent(float amax, int emax, uint32_t manlim) {
+    if (!(amax > 0.0f)) return 0;
+    uint32_t b = __float_as_uint(amax);
+    int ex = (int)(b >> 23) - 127;
+    if (ex == -127) {                                   // fp32 subnormal: renormalise
+        b = __float_as_uint(__fmul_rn(amax, 4294967296.0f));
+        ex = (int)(b >> 23) - 127 - 32;
+    }
+    const int E = ((b & 0x7FFFFFu) <= manlim) ? ex - emax : ex - emax + 1;
+    return E < -127 ? -127 : (E > 127 ? 127 : E);
+}
+
+// 2^-E as an exact fp32 (E in [-127, 127])
+__device__ __forceinline__ float mx_inv_scale(int E) {
+    const int e2 = -E;
+    return e2 >= -126 ? __uint_as_float((uint32_t)(e2 + 127) << 23) : __uint_as_float(0x400000u);
+}
 
 // MXFP8 quantization of one 32-element group (this lane's elements), §2.C FP8
 // slice: E = smallest integer with 448 * 2^E >= amax (clamped to [-127, 127],
@@ -183,20 +205,8 @@ struct MxSeg {
 // saturation at +-448.
 __device__ __forceinline__ MxSeg quant_mxfp8_group(const float (&x)[32]) {
     const float amax = fmaxf(amax16(x, 0), amax16(x, 16));
-    int E = 0;
-    if (amax > 0.0f) {
-        uint32_t b = __float_as_uint(amax);
-        int ex = (int)(b >> 23) - 127;
-        if (ex == -127) {                               // fp32 subnormal: renormalise
-            b = __float_as_uint(__fmul_rn(amax, 4294967296.0f));
-            ex = (int)(b >> 23) - 127 - 32;
-        }
-        const uint32_t man = b & 0x7FFFFFu;             // amax = 1.man * 2^ex; 448 = 1.75 * 2^8
-        E = (man <= 0x600000u) ? ex - 8 : ex - 7;
-        E = E < -127 ? -127 : (E > 127 ? 127 : E);
-    }
-    const int e2 = -E;                                  // 2^-E as an exact float
-    const float inv = e2 >= -126 ? __uint_as_float((uint32_t)(e2 + 127) << 23) : __uint_as_float(0x400000u);
+    const int E = mx_block_exponent(amax, 8, 0x600000u);          // 448 = 1.75 * 2^8
+    const float inv = mx_inv_scale(E);
     MxSeg out;
     uint32_t w[8];
 #pragma unroll
@@ -233,6 +243,71 @@ __device__ __forceinline__ void mx_unflip(MxSeg &m, uint32_t sign_word) {
     m.codes[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+// FP6 (E2M3 / E3M2) quantization of one 32-element group with the FP8 slice's rule and the
+// format's maximum (7.5 = 1.875 * 2^2, 28 = 1.75 * 2^4).  Element j is negated first when
+// bit j of `flip` is set.  The 32 6-bit codes are packed as a little-endian bit stream
+// (element j at bits 6j .. 6j+5): 24 bytes, the tensor core's FP6 operand order.
+__device__ __forceinline__ MxSeg quant_mx6_group(const float (&x)[32], bool e3m2, uint32_t flip) {
+    const float amax = fmaxf(amax16(x, 0), amax16(x, 16));
+    const int E = e3m2 ? mx_block_exponent(amax, 4, 0x600000u) : mx_block_exponent(amax, 2, 0x700000u);
+    const float inv = mx_inv_scale(E);
+    uint32_t p[8];                                      // 4 codes = 24 bits each
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float v[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+            v[h] = __uint_as_float(__float_as_uint(__fmul_rn(x[4 * i + h], inv)) ^ (((flip >> (4 * i + h)) & 1u) << 31));
+        const uint32_t w = e3m2 ? (e3m2x2_rn(v[0], v[1]) | (e3m2x2_rn(v[2], v[3]) << 16))
+                                : (e2m3x2_rn(v[0], v[1]) | (e2m3x2_rn(v[2], v[3]) << 16));
+        p[i] = (w & 0x3Fu) | ((w >> 2) & 0xFC0u) | ((w >> 4) & 0x3F000u) | ((w >> 6) & 0xFC0000u);
+    }
+    MxSeg out;
+    out.codes[0] = make_uint4(p[0] | (p[1] << 24), (p[1] >> 8) | (p[2] << 16), (p[2] >> 16) | (p[3] << 8),
+                              p[4] | (p[5] << 24));
+    out.codes[1] = make_uint4((p[5] >> 8) | (p[6] << 16), (p[6] >> 16) | (p[7] << 8), 0u, 0u);
+    out.e8 = (uint32_t)(E + 127);
+    return out;
+}
+
+// FP4 (E2M1) quantization of one 32-element group with the same rule (6 = 1.5 * 2^2):
+// codes packed two per byte, element 2j in the low nibble (16 bytes).  `flip` as above.
+__device__ __forceinline__ MxSeg quant_mx4_group(const float (&x)[32], uint32_t flip) {
+    const float amax = fmaxf(amax16(x, 0), amax16(x, 16));
+    const int E = mx_block_exponent(amax, 2, 0x400000u);
+    const float inv = mx_inv_scale(E);
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t word = 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = 8 * i + 2 * j;
+            const float a = __uint_as_float(__float_as_uint(__fmul_rn(x[e], inv)) ^ (((flip >> e) & 1u) << 31));
+            const float b = __uint_as_float(__float_as_uint(__fmul_rn(x[e + 1], inv)) ^ (((flip >> (e + 1)) & 1u) << 31));
+            word |= e2m1x2_rn(a, b) << (8 * j);
+        }
+        w[i] = word;
+    }
+    MxSeg out;
+    out.codes[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    out.codes[1] = make_uint4(0u, 0u, 0u, 0u);
+    out.e8 = (uint32_t)(E + 127);
+    return out;
+}
+
+// MX quantization of one group in the slice format fmt (uniform across the warp).  With
+// kFlip, element j is taken negated when bit j of `flip` is set (the sign-flipped rows of
+// the transposed RHT quantizer); the E4M3 path turns its codes' sign bits instead.
+template <bool kFlip = false>
+__device__ __forceinline__ MxSeg quant_mx_group(const float (&x)[32], int fmt, uint32_t flip = 0u) {
+    if (fmt == kMxE2M1) return quant_mx4_group(x, kFlip ? flip : 0u);
+    if (fmt != kMxE4M3) return quant_mx6_group(x, fmt == kMxE3M2, kFlip ? flip : 0u);
+    MxSeg m = quant_mxfp8_group(x);
+    if (kFlip) mx_unflip(m, flip);
+    return m;
+}
+
 // Output descriptors (device pointers and padded sizes).
 struct OutNv {
     uint8_t *codes;
@@ -244,6 +319,7 @@ struct OutMx {
     uint8_t *codes;
     uint8_t *sf;
     int64_t rows_p, cols_p;
+    int fmt;                  // slice element format (kMxE4M3 / kMxE2M3 / kMxE3M2 / kMxE2M1)
 };
 
 // Store one quad's NVFP4 segment (row, block kb).  Lane t writes its 16 code
@@ -261,16 +337,25 @@ __device__ __forceinline__ void store_nv_seg(const OutNv &o, int64_t row, int64_
     if (t == 0) o.outer[kb * o.rows_p + row] = s.s_o;
 }
 
-// Store one quad's MXFP8 segment (row, 128-block kb): lane t owns group 4kb+t.
+// Store one quad's MX segment (row, 128-block kb) in the slice format: lane t owns group 4kb+t.
 __device__ __forceinline__ void store_mx_seg(const OutMx &o, int64_t row, int64_t kb, int t, const MxSeg &s,
                                              bool valid) {
     const uint32_t b1 = __shfl_xor_sync(0xffffffffu, s.e8, 1);
     const uint32_t b2 = __shfl_xor_sync(0xffffffffu, s.e8, 2);
     const uint32_t b3 = __shfl_xor_sync(0xffffffffu, s.e8, 3);
     if (!valid) return;
-    uint4 *dst = reinterpret_cast<uint4 *>(o.codes + row * o.cols_p + kb * 128 + 32 * t);
-    dst[0] = s.codes[0];
-    dst[1] = s.codes[1];
+    if (o.fmt == kMxE4M3) {
+        uint4 *dst = reinterpret_cast<uint4 *>(o.codes + row * o.cols_p + kb * 128 + 32 * t);
+        dst[0] = s.codes[0];
+        dst[1] = s.codes[1];
+    } else if (o.fmt == kMxE2M1) {
+        *reinterpret_cast<uint4 *>(o.codes + row * (o.cols_p / 2) + kb * 64 + 16 * t) = s.codes[0];
+    } else {                                          // 24 bytes, 8-byte aligned
+        uint2 *dst = reinterpret_cast<uint2 *>(o.codes + row * (o.cols_p / 4 * 3) + kb * 96 + 24 * t);
+        dst[0] = make_uint2(s.codes[0].x, s.codes[0].y);
+        dst[1] = make_uint2(s.codes[0].z, s.codes[0].w);
+        dst[2] = make_uint2(s.codes[1].x, s.codes[1].y);
+    }
     if (t == 0) {
         const uint32_t word = s.e8 | (b1 << 8) | (b2 << 16) | (b3 << 24);
         *reinterpret_cast<uint32_t *>(o.sf + sf_word_offset(row, kb, o.cols_p / 128)) = word;

@@ -180,6 +180,50 @@ __device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
     return (uint32_t)r & 0xFFu;
 }
 
+// ---------------------------------------------------------------------------
+// Element formats of an MX outlier slice (tj.h tj_mx_format: the tensor core's format
+// numbers).  E2M3 (bias 1, max 7.5) and E3M2 (bias 3, max 28) are the FP6 formats, E2M1
+// the FP4 one, of the mixed FP6 x FP4 slice; E4M3 is the FP8 slice.
+// ---------------------------------------------------------------------------
+constexpr int kMxE4M3 = 0, kMxE2M3 = 3, kMxE3M2 = 4, kMxE2M1 = 5;
+__host__ __device__ constexpr int mx_bits(int fmt) { return fmt == kMxE4M3 ? 8 : (fmt == kMxE2M1 ? 4 : 6); }
+__host__ __device__ constexpr bool mx_fmt_valid(int fmt) {
+    return fmt == kMxE4M3 || fmt == kMxE2M3 || fmt == kMxE3M2 || fmt == kMxE2M1;
+}
+
+// Two signed values -> two 6-bit codes, one per byte (lo in the low byte), rounded to
+// nearest-even and saturated by cvt.rn.satfinite.{e2m3x2,e3m2x2}.f32 (which puts its
+// first operand in the high byte).
+__device__ __forceinline__ uint32_t e2m3x2_rn(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return (uint32_t)r;
+}
+__device__ __forceinline__ uint32_t e3m2x2_rn(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e3m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return (uint32_t)r;
+}
+
+// Exact fp32 value of a 6-bit E2M3 / E3M2 code (sign in bit 5): the normal values are
+// built from their exponent and mantissa bits, the subnormals as m / 8 or m / 16.
+__device__ __forceinline__ float e2m3_to_float(uint32_t c) {
+    const uint32_t e = (c >> 3) & 3u, m = c & 7u;
+    const float v = e ? __uint_as_float(((e + 126u) << 23) | (m << 20)) : __fmul_rn((float)m, 0.125f);
+    return (c & 0x20u) ? -v : v;
+}
+__device__ __forceinline__ float e3m2_to_float(uint32_t c) {
+    const uint32_t e = (c >> 2) & 7u, m = c & 3u;
+    const float v = e ? __uint_as_float(((e + 124u) << 23) | (m << 21)) : __fmul_rn((float)m, 0.0625f);
+    return (c & 0x20u) ? -v : v;
+}
+__device__ __forceinline__ float e2m1_to_float(uint32_t c) {
+    const uint32_t mag = c & 7u;
+    const float v = mag < 4u ? __fmul_rn((float)mag, 0.5f)
+                             : (mag == 4u ? 2.0f : (mag == 5u ? 3.0f : (mag == 6u ? 4.0f : 6.0f)));
+    return (c & 8u) ? -v : v;
+}
+
 // Stochastic rounding of a in [0, 6] between its grid neighbours lo <= a <= hi:
 // up with probability p = (a - lo) / (hi - lo), decided as float(u16) < p * 65536.
 // Integer form of that same test: for a >= 1 in the binade [2^e, 2^(e+1)) the grid

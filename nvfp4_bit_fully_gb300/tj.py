@@ -17,6 +17,9 @@ TJ_OK = 0
 TJ_RTN, TJ_SR = 0, 1
 TJ_BF16, TJ_FP32 = 0, 1
 TJ_OP_BWD_DX, TJ_OP_BWD_DW, TJ_OP_FP8_BWD_DX, TJ_OP_FP8_BWD_DW = 1, 2, 3, 4
+# element formats of an MX slice (E4M3 = the FP8 slice; E2M3 / E3M2 / E2M1 for FP6 x FP4)
+TJ_MX_E4M3, TJ_MX_E2M3, TJ_MX_E3M2, TJ_MX_E2M1 = 0, 3, 4, 5
+MX_BITS = {TJ_MX_E4M3: 8, TJ_MX_E2M3: 6, TJ_MX_E3M2: 6, TJ_MX_E2M1: 4}
 TAG_DY_ROW, TAG_DY_COL, TAG_WT, TAG_XT = 1, 2, 3, 4
 TAG_RHT_DX, TAG_RHT_DW = 0x100, 0x101
 STATUS = {0: "ok", 1: "invalid argument", 2: "shape", 3: "alignment", 4: "unsupported", 5: "CUDA error",
@@ -36,7 +39,7 @@ class CNvfp4(ctypes.Structure):
 
 class CMxfp8(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("sf", ctypes.c_void_p),
-                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64)]
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("fmt", ctypes.c_int32)]
 
 
 _lib = None
@@ -152,19 +155,20 @@ class NVFP4:
 
 
 class MXFP8:
-    """Device buffers of an MXFP8 outlier slice (layout documented in tj.h)."""
+    """Device buffers of an MX outlier slice in element format fmt (TJ_MX_*; E4M3 = the FP8
+    slice; layout documented in tj.h)."""
 
-    def __init__(self, codes, sf, rows, cols):
-        self.codes, self.sf, self.rows, self.cols = codes, sf, rows, cols
+    def __init__(self, codes, sf, rows, cols, fmt=TJ_MX_E4M3):
+        self.codes, self.sf, self.rows, self.cols, self.fmt = codes, sf, rows, cols, fmt
 
     @staticmethod
-    def empty(rows, cols, device="cuda"):
+    def empty(rows, cols, device="cuda", fmt=TJ_MX_E4M3):
         rp, cp = _round_up(rows, 128), _round_up(cols, 128)
-        return MXFP8(torch.empty(rp * cp, dtype=torch.uint8, device=device),
-                     torch.empty(rp * cp // 32, dtype=torch.uint8, device=device), rows, cols)
+        return MXFP8(torch.empty(rp * cp * MX_BITS[fmt] // 8, dtype=torch.uint8, device=device),
+                     torch.empty(rp * cp // 32, dtype=torch.uint8, device=device), rows, cols, fmt)
 
     def c(self):
-        return CMxfp8(self.codes.data_ptr(), self.sf.data_ptr(), self.rows, self.cols)
+        return CMxfp8(self.codes.data_ptr(), self.sf.data_ptr(), self.rows, self.cols, self.fmt)
 
 
 def _ref(obj):
@@ -184,12 +188,12 @@ def quantize_nvfp4(x, along_cols=False, sel=None, mode=TJ_RTN, rht=False, seed=0
     return out
 
 
-def quantize_mxfp8(x, along_cols=False, sel=None, out=None, stream=None):
-    """MXFP8 quantization (tj_quantize_mxfp8)."""
+def quantize_mxfp8(x, along_cols=False, sel=None, out=None, stream=None, fmt=TJ_MX_E4M3):
+    """MX slice quantization (tj_quantize_mxfp8), in `out`'s format or, when out is None, in fmt."""
     rows_x, cols_x = x.shape
     ncols = cols_x if sel is None else sel.numel()
     orows, ocols = (ncols, rows_x) if along_cols else (rows_x, ncols)
-    out = out if out is not None else MXFP8.empty(orows, ocols, x.device)
+    out = out if out is not None else MXFP8.empty(orows, ocols, x.device, fmt)
     c = out.c()
     _call("tj_quantize_mxfp8", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols), _ptr(sel),
           0 if sel is None else sel.numel(), ctypes.byref(c), _stream(stream))
@@ -197,13 +201,14 @@ def quantize_mxfp8(x, along_cols=False, sel=None, out=None, stream=None):
 
 
 def quantize_nvfp4_mxfp8(x, along_cols=False, sel=None, mode=TJ_RTN, rht=False, seed=0, tag=0, rht_tag=0,
-                         out=None, out8=None, stream=None):
-    """NVFP4 and MXFP8 of the same input from one read (tj_quantize_nvfp4_mxfp8)."""
+                         out=None, out8=None, stream=None, fmt8=TJ_MX_E4M3):
+    """NVFP4 and an MX slice (format fmt8 unless out8 is given) of the same input from one
+    read (tj_quantize_nvfp4_mxfp8)."""
     rows_x, cols_x = x.shape
     ncols = cols_x if sel is None else sel.numel()
     orows, ocols = (ncols, rows_x) if along_cols else (rows_x, ncols)
     out = out if out is not None else NVFP4.empty(orows, ocols, x.device)
-    out8 = out8 if out8 is not None else MXFP8.empty(orows, ocols, x.device)
+    out8 = out8 if out8 is not None else MXFP8.empty(orows, ocols, x.device, fmt8)
     c, c8 = out.c(), out8.c()
     _call("tj_quantize_nvfp4_mxfp8", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols),
           _ptr(sel), 0 if sel is None else sel.numel(), mode, int(rht), seed, tag, rht_tag, ctypes.byref(c),
@@ -211,14 +216,14 @@ def quantize_nvfp4_mxfp8(x, along_cols=False, sel=None, mode=TJ_RTN, rht=False, 
     return out, out8
 
 
-def quantize_split(x, normal_idx, outlier_idx, out=None, out8=None, stream=None):
-    """OutControl split, row-wise, one read: NVFP4 RTN of the normal channels and MXFP8 of
-    the outlier channels (tj_quantize_split)."""
+def quantize_split(x, normal_idx, outlier_idx, out=None, out8=None, stream=None, fmt8=TJ_MX_E4M3):
+    """OutControl split, row-wise, one read: NVFP4 RTN of the normal channels and the MX slice
+    (format fmt8 unless out8 is given) of the outlier channels (tj_quantize_split)."""
     rows, cols = x.shape
     kn, k = normal_idx.numel(), (0 if outlier_idx is None else outlier_idx.numel())
     out = out if out is not None else NVFP4.empty(rows, kn, x.device)
     if k > 0 and out8 is None:
-        out8 = MXFP8.empty(rows, k, x.device)
+        out8 = MXFP8.empty(rows, k, x.device, fmt8)
     c = out.c()
     c8 = out8.c() if k > 0 else None
     _call("tj_quantize_split", _ptr(x), _dtype_code(x), rows, cols, x.stride(0), _ptr(normal_idx), kn,
@@ -236,9 +241,10 @@ def requantize_nvfp4(q, mode=TJ_SR, rht=True, seed=0, tag=0, rht_tag=0, out=None
     return out
 
 
-def requantize_mxfp8(q, out=None, stream=None):
-    """Transposed re-alignment of an FP8 slice [rows, cols] -> [cols, rows] (RTN)."""
-    out = out if out is not None else MXFP8.empty(q.cols, q.rows, q.codes.device)
+def requantize_mxfp8(q, out=None, stream=None, fmt=None):
+    """Transposed re-alignment of a slice [rows, cols] -> [cols, rows] (RTN), in `out`'s
+    format or fmt (default: the input's)."""
+    out = out if out is not None else MXFP8.empty(q.cols, q.rows, q.codes.device, q.fmt if fmt is None else fmt)
     ci, co = q.c(), out.c()
     _call("tj_requantize_mxfp8", ctypes.byref(ci), ctypes.byref(co), _stream(stream))
     return out
@@ -310,13 +316,14 @@ def workspace_size(op, M, N, K, k):
 
 
 def linear_fwd(x, wq, w8=None, normal_idx=None, outlier_idx=None, out_dtype=torch.bfloat16, xq=None, x8=None,
-               out=None, stream=None):
-    """Forward Y = X W^T of the NVFP4 linear layer; returns (Y, X-hat NVFP4, X-hat FP8 slice)."""
+               out=None, stream=None, fmt_x8=TJ_MX_E4M3):
+    """Forward Y = X W^T of the NVFP4 linear layer; returns (Y, X-hat NVFP4, X-hat slice).
+    X's slice is quantized in x8's format, or fmt_x8 when x8 is None."""
     M, K = x.shape
     k = 0 if outlier_idx is None else outlier_idx.numel()
     xq = xq if xq is not None else NVFP4.empty(M, K - k, x.device)
     if k and x8 is None:
-        x8 = MXFP8.empty(M, k, x.device)
+        x8 = MXFP8.empty(M, k, x.device, fmt_x8)
     out = out if out is not None else torch.empty(M, wq.rows, dtype=out_dtype, device=x.device)
     cw, cx = wq.c(), xq.c()
     cw8 = w8.c() if k else None

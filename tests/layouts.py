@@ -51,10 +51,44 @@ def nvfp4_to_logical_full(q):
     return codes, sf, outer
 
 
+MX_BITS = {0: 8, 3: 6, 4: 6, 5: 4}
+
+
+def unpack_mx_codes(raw, rows_p, cols_p, fmt):
+    """Packed slice rows -> one code per element [rows_p, cols_p] (tj.h: E4M3 bytes; 6-bit
+    codes as a little-endian bit stream per row, element c at bits 6c..6c+5; 4-bit codes
+    two per byte, element 2j in the low nibble)."""
+    raw = np.asarray(raw, dtype=np.uint8).reshape(rows_p, cols_p * MX_BITS[fmt] // 8)
+    if fmt == 0:
+        return raw.copy()
+    if fmt == 5:
+        codes = np.empty((rows_p, cols_p), dtype=np.uint8)
+        codes[:, 0::2] = raw & 15
+        codes[:, 1::2] = raw >> 4
+        return codes
+    bits = np.unpackbits(raw, axis=1, bitorder="little").reshape(rows_p, cols_p, 6)
+    return (bits.astype(np.uint8) << np.arange(6, dtype=np.uint8)).sum(axis=2).astype(np.uint8)
+
+
+def pack_mx_codes(codes, fmt):
+    """Inverse of unpack_mx_codes: [rows, cols_p] codes -> packed bytes [rows, cols_p*bits/8]."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    if fmt == 0:
+        return codes.copy()
+    if fmt == 5:
+        return (codes[:, 0::2] & 15) | ((codes[:, 1::2] & 15) << 4)
+    r, c = codes.shape
+    bits = ((codes[:, :, None] >> np.arange(6, dtype=np.uint8)) & 1).reshape(r, c * 6)
+    return np.packbits(bits, axis=1, bitorder="little")
+
+
 def mxfp8_to_logical(q):
-    """tj.MXFP8 -> (codes [rows, cols_p] uint8, scale bytes [rows, cols_p/32] uint8)."""
+    """tj.MXFP8 (any slice format) -> (codes [rows, cols_p] uint8, one per element;
+    scale bytes [rows, cols_p/32] uint8)."""
     rows_p, cols_p = _round_up(q.rows, 128), _round_up(q.cols, 128)
-    codes = q.codes.cpu().numpy().reshape(rows_p, cols_p)
+    fmt = getattr(q, "fmt", 0)
+    nbytes = rows_p * cols_p * MX_BITS[fmt] // 8
+    codes = unpack_mx_codes(q.codes[:nbytes].cpu().numpy(), rows_p, cols_p, fmt)
     sb = _sf_untile(q.sf.cpu().numpy(), rows_p, cols_p // 32, cols_p // 128)
     return codes[: q.rows], sb[: q.rows]
 
@@ -124,8 +158,9 @@ def to_numpy_f32(t):
 def carve_workspace(ws, parts):
     """Views of a backward workspace, carved in the documented order.
 
-    parts: list of ("nv" | "mx", rows, cols); every buffer (codes, sf, outer)
-    starts on a 256-byte boundary.  Returns tj.NVFP4 / tj.MXFP8 objects."""
+    parts: list of ("nv" | "mx", rows, cols[, slice format]); every buffer (codes, sf,
+    outer) starts on a 256-byte boundary, and a slice reserves its FP8 size whatever its
+    format.  Returns tj.NVFP4 / tj.MXFP8 objects."""
     from nvfp4_bit_fully_gb300 import tj
 
     out, off = [], 0
@@ -136,7 +171,8 @@ def carve_workspace(ws, parts):
         off += _round_up(nbytes, 256)
         return view.view(dtype) if dtype != torch.uint8 else view
 
-    for kind, rows, cols in parts:
+    for part in parts:
+        kind, rows, cols = part[:3]
         rp, cp = _round_up(rows, 128), _round_up(cols, 128)
         if kind == "nv":
             codes = take(rp * cp // 2)
@@ -146,5 +182,5 @@ def carve_workspace(ws, parts):
         else:
             codes = take(rp * cp)
             sf = take(rp * cp // 32)
-            out.append(tj.MXFP8(codes, sf, rows, cols))
+            out.append(tj.MXFP8(codes, sf, rows, cols, part[3] if len(part) > 3 else 0))
     return out

@@ -122,3 +122,22 @@ def test_column_grid_limit(lib):
     xq = tj.CNvfp4(256, 256, 256, rows, 128)
     assert l.tj_linear_bwd_dw(ctypes.c_void_p(256), rows, 128, 128, ctypes.byref(xq), None, None, None, 0, 1,
                               ctypes.c_void_p(256), 128, ctypes.c_void_p(256), 1 << 40, None) == 2
+
+
+def test_slice_format_checks(lib):
+    """An MX slice descriptor with an unknown element format is an argument error, and packed
+    FP6 / FP4 codes that do not start on 32 bytes an alignment error, before any launch."""
+    from nvfp4_bit_fully_gb300 import tj
+
+    l = tj.load()
+    y = ctypes.c_void_p(256)
+    assert ctypes.sizeof(tj.CMxfp8) == 40
+    for fmt, want in ((1, 1), (2, 1), (6, 1), (-1, 1)):
+        m = tj.CMxfp8(256, 256, 128, 128, fmt)
+        assert l.tj_dequantize_mxfp8(ctypes.byref(m), y, 128, None) == want, fmt
+    for fmt in (tj.TJ_MX_E2M3, tj.TJ_MX_E3M2, tj.TJ_MX_E2M1):
+        m = tj.CMxfp8(256 + 16, 256, 128, 128, fmt)                 # 16- but not 32-byte aligned
+        assert l.tj_dequantize_mxfp8(ctypes.byref(m), y, 128, None) == 3
+        assert l.tj_quantize_mxfp8(ctypes.c_void_p(256), 0, 128, 128, 128, 0, None, 0, ctypes.byref(m), None) == 3
+    m = tj.CMxfp8(256 + 16, 256, 128, 128, tj.TJ_MX_E4M3)           # E4M3 needs 16 bytes only
+    assert l.tj_dequantize_mxfp8(ctypes.byref(m), y, 40, None) == 2   # (reaches the ldy check)
