@@ -389,8 +389,50 @@ def cfg3_fwd(tj, dev, stream, fp4_peak, fp8_peak):
     ms_gemm = time_kernel(lambda: tj.gemm_nvfp4(xq, wq, x8, w8, out=Y, stream=stream), stream)
     out = {"shape": [M, N, K], "k_fp8": k, "linear_fwd": _gemm_frac(f4, f8, ms, fp4_peak, fp8_peak),
            "gemm": _gemm_frac(f4, f8, ms_gemm, fp4_peak, fp8_peak)}
+    out["slice_formats"] = slice_formats(tj, dev, stream, X, W, ni, oi, k, fp4_peak, fp8_peak)
     del X, W, xq, x8, Y, wq, w8
     return out
+
+
+def slice_formats(tj, dev, stream, X, W, ni, oi, k, fp4_peak, fp8_peak):
+    """The same layer with the FP8 slice (E4M3 x E4M3) and with the FP6 x FP4 slice (X in
+    E2M3, W in E2M1; the backward gives dY the partner format, so dX's slice is E2M3 x E2M1
+    and dW's E2M1 x E2M3): forward through tj_linear_fwd, the forward GEMM alone, and the
+    two backward calls with dY 16384 x 4096 heavy-tailed rows.  The f8f6f4 MMA runs FP6 and
+    FP4 slice operands at the FP8 rate, so the peak weighting is the FP8 slice's."""
+    from nvfp4_bit_fully_gb300 import workloads as wl
+
+    M, K = X.shape
+    N = W.shape[0]
+    f4, f8 = 2.0 * M * N * (K - k), 2.0 * M * N * k
+    dY = wl.device_student_t_rows(M, N, 1e-3, 3, 3, 33, dev)
+    torch.cuda.synchronize()
+    res = {}
+    for name, fx, fw in (("fp8_x_fp8", tj.TJ_MX_E4M3, tj.TJ_MX_E4M3), ("e2m3_x_e2m1", tj.TJ_MX_E2M3, tj.TJ_MX_E2M1)):
+        wq, w8 = tj.quantize_nvfp4(W, sel=ni, stream=stream), tj.quantize_mxfp8(W, sel=oi, stream=stream, fmt=fw)
+        xq, x8 = tj.NVFP4.empty(M, K - k, dev), tj.MXFP8.empty(M, k, dev, fx)
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        dX = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        dW = torch.empty(N, K, dtype=torch.float32, device=dev)
+        ws_dx = torch.empty(tj.workspace_size(tj.TJ_OP_BWD_DX, M, N, K, k), dtype=torch.uint8, device=dev)
+        ws_dw = torch.empty(tj.workspace_size(tj.TJ_OP_BWD_DW, M, N, K, k), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+        seeds = iter(range(10**6))
+        ms_f = time_kernel(lambda: tj.linear_fwd(X, wq, w8, ni, oi, xq=xq, x8=x8, out=Y, stream=stream), stream)
+        ms_g = time_kernel(lambda: tj.gemm_nvfp4(xq, wq, x8, w8, out=Y, stream=stream), stream)
+        ms_dx = time_kernel(lambda: tj.linear_bwd_dx(dY, wq, w8, ni, oi, seed=next(seeds), workspace=ws_dx, out=dX,
+                                                     stream=stream), stream)
+        ms_dw = time_kernel(lambda: tj.linear_bwd_dw(dY, xq, x8, ni, oi, seed=next(seeds), workspace=ws_dw, out=dW,
+                                                     stream=stream), stream)
+        f4b = 2.0 * M * (K - k) * N
+        res[name] = {"linear_fwd": _gemm_frac(f4, f8, ms_f, fp4_peak, fp8_peak),
+                     "gemm_fwd": _gemm_frac(f4, f8, ms_g, fp4_peak, fp8_peak),
+                     "linear_bwd_dx": _gemm_frac(f4b, f8, ms_dx, fp4_peak, fp8_peak),
+                     "linear_bwd_dw": _gemm_frac(f4b, f8, ms_dw, fp4_peak, fp8_peak),
+                     "slice_code_bytes_x": x8.codes.numel(), "slice_code_bytes_w": w8.codes.numel()}
+        del wq, w8, xq, x8, Y, dX, dW, ws_dx, ws_dw
+    del dY
+    return res
 
 
 def cfg4_bwd(tj, dev, stream, fp4_peak, fp8_peak):

@@ -21,6 +21,11 @@ through tj_linear_fwd / tj_linear_bwd_dx / tj_linear_bwd_dw over several seeds,
 and reports the forward error against the unquantized product, and the bias (error
 of the mean over seeds) and per-seed error of dX and dW.
 
+Slice formats (§5 names FP6 x FP4 mixed precision as a future direction): at a 10%
+outlier fraction, the same layer with the FP8 slice and with FP6 x FP4 slices (X in
+E2M3 or E3M2 with W in E2M1, and the reverse), reporting the slice product's own error,
+the layer's forward error and the error of the mean dX / dW on the outlier channels.
+
 Usage:  python -m nvfp4_bit_fully_gb300.ablation [--out ablation.json] [--small]
 Needs a CUDA GPU and the built library (there is no CPU fallback).
 """
@@ -33,6 +38,8 @@ import numpy as np
 OSCI_THRESHOLDS = (2.0, 4.0, 8.0, 16.0)
 OSCI_START_STEPS = (0, 100, 150, 180)
 OUTLIER_PCTS = (0, 1, 5, 10, 20)
+# slice element formats (x, w): the FP8 slice and the FP6 x FP4 variants (tj.h tj_mx_format)
+SLICE_FORMATS = (("e4m3 x e4m3", 0, 0), ("e2m3 x e2m1", 3, 5), ("e3m2 x e2m1", 4, 5), ("e2m1 x e2m3", 5, 3))
 LR_THR = 1e-4
 
 
@@ -189,6 +196,52 @@ def run_outctl(tj, torch, M, N, K, pct, seeds, base_seed):
             "dw_vs_unquantized": rel_err(np.mean(dws, axis=0), dw_ref)}
 
 
+def run_slice_formats(tj, torch, M, N, K, pct, seeds, base_seed):
+    """The layer of run_outctl at one outlier fraction with each slice format pair."""
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(base_seed)
+    heavy = torch.randperm(K, generator=g, device=dev)[:max(1, K // 50)]
+
+    def batch():
+        x = torch.randn(M, K, generator=g, device=dev)
+        x[:, heavy] *= 40.0
+        return x.to(torch.bfloat16)
+
+    k = (pct * K + 99) // 100
+    sumsq = torch.zeros(K, dtype=torch.float64, device=dev)
+    for _ in range(2):
+        tj.outlier_calibrate(batch(), sumsq)
+    oi, ni = tj.outlier_calibrate(None, sumsq, finalize=True, k=k)
+    X = batch()
+    W = (torch.randn(N, K, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    dY = (torch.randn(M, N, generator=g, device=dev) * 1e-3).to(torch.bfloat16)
+    Xf, Wf, dYf = X.double(), W.double(), dY.double()
+    o = oi.long()
+    y_ref = (Xf @ Wf.T).cpu().numpy()
+    slice_ref = (Xf[:, o] @ Wf[:, o].T).cpu().numpy()
+    dx_ref = (dYf @ Wf[:, o]).cpu().numpy()
+    dw_ref = (dYf.T @ Xf[:, o]).cpu().numpy()
+    wq = tj.quantize_nvfp4(W, sel=ni)
+    rows = []
+    for name, fx, fw in SLICE_FORMATS:
+        w8 = tj.quantize_mxfp8(W, sel=oi, fmt=fw)
+        y, xq, x8 = tj.linear_fwd(X, wq, w8, ni, oi, out_dtype=torch.float32, fmt_x8=fx)
+        ys = tj.gemm_mxfp8(x8, w8)
+        dxs, dws = [], []
+        for s in range(seeds):
+            dxs.append(tj.linear_bwd_dx(dY, wq, w8, ni, oi, seed=base_seed * 1000 + s,
+                                        out_dtype=torch.float32)[:, o].cpu().numpy())
+            dws.append(tj.linear_bwd_dw(dY, xq, x8, ni, oi, seed=base_seed * 1000 + s)[:, o].cpu().numpy())
+        torch.cuda.synchronize()
+        rows.append({"slice": name, "k": int(k), "slice_fwd_rel_err": rel_err(ys.cpu().numpy(), slice_ref),
+                     "fwd_rel_err": rel_err(y.cpu().numpy(), y_ref),
+                     "dx_outlier_cols_vs_unquantized": rel_err(np.mean(dxs, axis=0), dx_ref),
+                     "dw_outlier_cols_vs_unquantized": rel_err(np.mean(dws, axis=0), dw_ref),
+                     "slice_code_bytes": int(x8.codes.numel() + w8.codes.numel())})
+    return rows
+
+
 def _dequant_operand(tj, torch, q, q8, ni, oi, rows, K):
     """fp64 values of a forward operand [rows, K] from its NVFP4 part (normal channels)
     and FP8 slice (outlier channels), in the original channel order."""
@@ -214,6 +267,7 @@ def run(out_path, small=False):
         rows, cols, steps, M, N, K, seeds = 1024, 1024, 200, 4096, 1024, 1024, 16
     table = {"osci_reset": [run_osci(tj, torch, rows, cols, steps, 7, c) for c in osci_configs()],
              "outcontrol": [run_outctl(tj, torch, M, N, K, p, seeds, 11) for p in OUTLIER_PCTS],
+             "slice_formats": run_slice_formats(tj, torch, M, N, K, 10, seeds, 13),
              "setup": {"osci": {"weights": rows * cols, "steps": steps, "lr": "cosine 1e-3 -> 1e-5", "lr_thr": LR_THR},
                        "outcontrol": {"M": M, "N": N, "K": K, "seeds": seeds, "heavy_channels": max(1, K // 50)}}}
     with open(out_path, "w") as f:

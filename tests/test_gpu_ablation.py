@@ -26,3 +26,21 @@ def test_small_ablation_sweep(tmp_path):
     for r in table["outcontrol"]:
         # unbiased backward estimates: the mean over seeds is closer than one seed
         assert r["dx"]["bias"] < 0.8 * r["dx"]["per_seed"] and r["dw"]["bias"] < 0.8 * r["dw"]["per_seed"]
+
+
+def test_slice_format_ablation(tmp_path):
+    """The FP6 x FP4 slices run through the layer; the FP8 slice, with three mantissa bits on
+    both sides, gives the smallest slice error."""
+    import torch
+
+    from nvfp4_bit_fully_gb300 import ablation as A
+    from nvfp4_bit_fully_gb300 import tj
+
+    tj.load()
+    rows = A.run_slice_formats(tj, torch, 256, 256, 512, 10, 4, 13)
+    errs = {r["slice"]: r["slice_fwd_rel_err"] for r in rows}
+    assert set(errs) == {n for n, _, _ in A.SLICE_FORMATS}
+    assert all(0 < e < 1 for e in errs.values())
+    assert errs["e4m3 x e4m3"] == min(errs.values())
+    sizes = {r["slice"]: r["slice_code_bytes"] for r in rows}
+    assert sizes["e2m3 x e2m1"] < sizes["e4m3 x e4m3"]
