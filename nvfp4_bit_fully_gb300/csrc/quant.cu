@@ -89,13 +89,19 @@ struct SrcNv {
         const uint32_t mag = w & 0x77777777u;
         const uint32_t two_g[2] = {__byte_perm(0x03020100u, 0x0C080604u, mag & 0xFFFFu),
                                    __byte_perm(0x03020100u, 0x0C080604u, mag >> 16)};
+        const uint64_t m2 = f2_pack(-8388608.0f, -8388608.0f), hs2 = f2_pack(half_si, half_si), so2 = f2_pack(so, so);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            // 0x4B0000nn = 2^23 + nn as fp32; subtracting 2^23 leaves nn = 2G exactly
-            const float gg = __fsub_rn(__uint_as_float(__byte_perm(two_g[k >> 2], 0x4B000000u, (k & 3) | 0x7440)),
-                                       8388608.0f);
-            const float a = __fmul_rn(__fmul_rn(gg, half_si), so);
-            v[k] = __uint_as_float(__float_as_uint(a) ^ ((w << (28 - 4 * k)) & 0x80000000u));
+        for (int k = 0; k < 8; k += 2) {
+            // 0x4B0000nn = 2^23 + nn as fp32; subtracting 2^23 leaves nn = 2G exactly.  Two
+            // elements at a time on packed f32x2 instructions, which round each half like
+            // the scalar ones: (2G * s_i / 2) * s_o
+            const uint64_t gg = f2_add(f2_pack(__uint_as_float(__byte_perm(two_g[k >> 2], 0x4B000000u, (k & 3) | 0x7440)),
+                                               __uint_as_float(__byte_perm(two_g[k >> 2], 0x4B000000u, ((k + 1) & 3) | 0x7440))),
+                                       m2);
+            float a0, a1;
+            f2_unpack(f2_mul(f2_mul(gg, hs2), so2), a0, a1);
+            v[k] = __uint_as_float(__float_as_uint(a0) ^ ((w << (28 - 4 * k)) & 0x80000000u));
+            v[k + 1] = __uint_as_float(__float_as_uint(a1) ^ ((w << (24 - 4 * k)) & 0x80000000u));
         }
     }
 };
@@ -197,7 +203,7 @@ __device__ __forceinline__ void load_row32(const SrcDense<__nv_bfloat16> &src, i
 // its optional RHT), into outputs of the same shape.
 // ---------------------------------------------------------------------------
 template <typename Src, int FMT, bool SR, bool RHT>
-__global__ void __launch_bounds__(256, (SR || RHT) ? 3 : 4) k_quant_rows(Src src, OutNv onv, OutMx omx, int64_t nseg, const PhiloxKeys pk,
+__global__ void __launch_bounds__(256, 4) k_quant_rows(Src src, OutNv onv, OutMx omx, int64_t nseg, const PhiloxKeys pk,
                                                     uint32_t tag, uint32_t rht_tag) {
     const int lane = threadIdx.x & 31;
     const int t = lane & 3;
@@ -240,7 +246,13 @@ __global__ void __launch_bounds__(256, (SR || RHT) ? 3 : 4) k_quant_rows(Src src
                 const MxSeg m = quant_mx_group(x, omx.fmt);
                 store_mx_seg(omx, row, kb, t, m, valid);
             }
-            if (RHT) rht128_quad(x, sign_word, t);
+            if (RHT) {
+                // an opaque copy per segment: otherwise the compiler hoists the 32 sign masks
+                // (sign_word << (31 - j)) out of the loop, where they spill (6% of the kernel)
+                uint32_t sw;
+                asm volatile("mov.b32 %0, %1;" : "=r"(sw) : "r"(sign_word));
+                rht128_quad(x, sw, t);
+            }
             const NvSeg s = quant_nvfp4_seg<SR>(x, (uint64_t)(row * cols_p + kb * 128 + 32 * t), pk, tag);
             store_nv_seg(onv, row, kb, t, s, valid);
         } else {
