@@ -202,6 +202,9 @@ class Linear:
             "requant_w": 2 * kn * N * NV_B, "requant_w8": 2 * k * N * MX_B, "requant_x": 2 * kn * M * NV_B,
             "requant_x8": 2 * k * M * MX_B,
         }
+        # elements each quantize call processes (for the issue roofline)
+        self.elems = {"quant_x": M * K, "quant_dy_row": M * N, "quant_dy_col": M * N, "requant_w": kn * N,
+                      "requant_w8": k * N, "requant_x": kn * M, "requant_x8": k * M}
 
     def run(self, tj, seed, tl, stream):
         T = lambda name, fn: tl.time(self.name + "." + name, fn)
@@ -266,9 +269,20 @@ class OsciState:
 # listed report traffic None.  k_osci_reset: 1913.3 MB over 67,108,864 weights.
 TRAFFIC_BYTES_PER_ELEM = {"k_osci_reset": 28.55}
 # DRAM bytes per launch of the GEMM: the twelve launches of one timed step of the layer set
-# at 16384 tokens read 935.4 MB and wrote 363.4 MB (one-pass ncu capture of the current
-# kernel), 108.2 MB per launch on average.  Valid for the default workload only.
-TRAFFIC_BYTES_PER_LAUNCH = {"k_gemm_nvfp4": 108.2e6}
+# at 16384 tokens read 940.1 MB and wrote 364.3 MB (one-pass ncu capture of the current
+# kernel), 108.7 MB per launch on average.  Valid for the default workload only.
+TRAFFIC_BYTES_PER_LAUNCH = {"k_gemm_nvfp4": 108.7e6}
+# Lane instructions per element of the issue-bound quantize kernels (smsp__thread_inst_executed
+# of one ncu capture of the current kernel versions, `bench.py --only quant`, divided by the
+# elements each launch processes: dY elements for the row / column passes, input elements of
+# X for the split, elements of the re-aligned tensor for the re-alignments).  With them each
+# kernel entry reports an issue roofline: lane instructions / (SMs x 128 lanes x SM clock x
+# time), the fraction of the SMs' instruction issue the kernel uses.
+LANE_INSTR_PER_ELEM = {
+    "k_quant_rows (NVFP4 + MXFP8 of dY)": 42.34, "k_quant_cols (NVFP4 + MXFP8 of dY)": 45.09,
+    "k_quant_split (OutControl split of X)": 29.50, "k_quant_cols<SrcNv> (re-align)": 48.98,
+    "k_quant_cols<SrcMx> (re-align)": 27.54,
+}
 NV_B = 0.5 + 1.0 / 16 + 4.0 / 128      # bytes per NVFP4 element (codes + E4M3 + FP32 scales)
 MX_B = 1.0 + 1.0 / 32                   # bytes per MXFP8 element (E4M3 + UE8M0)
 
@@ -618,6 +632,59 @@ def run_reference(args, world, rank):
     return 0
 
 
+def profiling_case(which):
+    """Small cases for profiler captures (a few hundred MB on the device), each kernel
+    launched twice: the second launch is the one to capture.
+    gemm : the gate/up forward GEMM, 16384 x 8192, K = 921 FP4 + 103 FP8 slice, bf16 out.
+    quant: at the dY shape 16384 x 4096: the row and column passes (NVFP4 SR + RHT and
+           MXFP8); at 16384 x 1024: the OutControl split of X (103 outlier channels), the
+           re-alignment of X-hat^T (921 channels, SR + RHT) and of its FP8 slice."""
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from nvfp4_bit_fully_gb300 import tj
+
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    M, K, k = TOKENS, 1024, 103
+    X = torch.randn(M, K, generator=g, device=dev).to(torch.bfloat16)
+    oi = torch.arange(0, K, 10, device=dev, dtype=torch.int32)[:k]
+    keep = torch.ones(K, dtype=torch.bool, device=dev)
+    keep[oi.long()] = False
+    ni = torch.nonzero(keep).squeeze(1).to(torch.int32)
+    xq, x8 = tj.quantize_split(X, ni, oi)
+    if which == "gemm":
+        N = 8192
+        W = (torch.randn(N, K, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        wq, w8 = tj.quantize_nvfp4(W, sel=ni), tj.quantize_mxfp8(W, sel=oi)
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        calls = [lambda: tj.gemm_nvfp4(xq, wq, x8, w8, out=Y)]
+    else:
+        N = 4096
+        dY = (torch.randn(M, N, generator=g, device=dev) * 1e-3).to(torch.bfloat16)
+        s_dy, q8 = tj.NVFP4.empty(M, N, dev), tj.MXFP8.empty(M, N, dev)
+        s_dyt, q8t = tj.NVFP4.empty(N, M, dev), tj.MXFP8.empty(N, M, dev)
+        s_x, q8x = tj.NVFP4.empty(K - k, M, dev), tj.MXFP8.empty(k, M, dev)
+        calls = [
+            lambda: tj.quantize_nvfp4_mxfp8(dY, mode=tj.TJ_SR, rht=True, seed=3, tag=tj.TAG_DY_ROW,
+                                            rht_tag=tj.TAG_RHT_DX, out=s_dy, out8=q8),
+            lambda: tj.quantize_nvfp4_mxfp8(dY, along_cols=True, mode=tj.TJ_SR, rht=True, seed=3, tag=tj.TAG_DY_COL,
+                                            rht_tag=tj.TAG_RHT_DW, out=s_dyt, out8=q8t),
+            lambda: tj.quantize_split(X, ni, oi, out=xq, out8=x8),
+            lambda: tj.requantize_nvfp4(xq, tj.TJ_SR, True, 3, tj.TAG_XT, tj.TAG_RHT_DW, out=s_x),
+            lambda: tj.requantize_mxfp8(x8, out=q8x),
+        ]
+    torch.cuda.synchronize()
+    for f in calls:
+        for _ in range(2):
+            f()
+    torch.cuda.synchronize()
+    tj.device_status()
+    print(json.dumps({"profiling_case": which, "launches": 2 * len(calls)}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -627,13 +694,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the quantize sweep / GEMM-alone / e2e parts")
     ap.add_argument("--osci-params", type=int, default=0, help="override the OsciReset size (profiling only)")
-    ap.add_argument("--only", choices=["all", "osci", "linear"], default="all",
-                    help="run one part of the step (for small profiler captures; not a bench line)")
+    ap.add_argument("--only", choices=["all", "osci", "linear", "gemm", "quant"], default="all",
+                    help="run one part of the step, or one profiling case (gemm, quant), for small profiler "
+                         "captures; not a bench line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.only in ("gemm", "quant"):
+        return profiling_case(args.only)
 
     import __graft_entry__
 
@@ -643,6 +713,7 @@ def main():
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     stream = torch.cuda.Stream(device=dev)
     peaks, peak_src = load_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
@@ -704,10 +775,15 @@ def main():
     # per call: average ms and throughput against its algorithmic work
     parts = {}
     kern = {}                       # kernel -> [total ms, flops4, flops8, bytes, launches]
+    kern_elems = {}                 # kernel -> elements processed over the timed steps
     for name, (ms_tot, n) in sorted(summ.items()):
         call = name.split(".")[-1]
         p = {"ms": round(ms_tot / n, 4)}
         agg = kern.setdefault(CALL_KERNEL[call], [0.0, 0.0, 0.0, 0.0, 0])
+        if call != "osci_reset":
+            lin_e = next(l for l in linears if l.name == name.split(".")[0]).elems.get(call)
+            if lin_e is not None:
+                kern_elems[CALL_KERNEL[call]] = kern_elems.get(CALL_KERNEL[call], 0) + lin_e * n
         agg[0] += ms_tot
         agg[4] += n
         if call == "osci_reset":
@@ -735,6 +811,11 @@ def main():
                       "frac": round(t_star / (ms_tot * 1e-3), 4)})
         else:
             e.update({"GB/s": round(by / (ms_tot * 1e-3) / 1e9, 1), "frac": round(by / (ms_tot * 1e-3) / 1e9 / hbm_peak, 3)})
+            if kname in LANE_INSTR_PER_ELEM and kname in kern_elems and clk.get("sm_mhz"):
+                lanes_per_s = num_sms * 128 * float(clk["sm_mhz"]) * 1e6
+                e["issue_roofline"] = {
+                    "lane_instr_per_elem": LANE_INSTR_PER_ELEM[kname],
+                    "frac": round(LANE_INSTR_PER_ELEM[kname] * kern_elems[kname] / (lanes_per_s * ms_tot * 1e-3), 3)}
         kernels[kname] = e
     # dominant kernel of the step (largest total time), with its roofline
     dom = max(kern.items(), key=lambda kv: kv[1][0])[0]
