@@ -124,17 +124,27 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // dequantized value makes the quantizer idempotent, so an OsciReset reset (§2.B: the
 // weight moved onto its own Q-hat) re-quantizes to the same code and scales.
 // The search starts from c, the E4M3 ceiling of a_i * inv_m6 (inv_m6 ~ 1 / fl(6 s_o),
-// any approximation), floored at the smallest normal value.  From a start within an
-// ulp or two of the quotient the answer is c - 1, c or c + 1 whenever the products
-// are normal fp32 numbers, and the top values of c - 2 .. c + 1, computed side by
-// side, decide it; otherwise (fp32-subnormal products, a far start) two walks reach
-// the exact answer from there, since the top value grows with sigma.
+// an approximate reciprocal), clamped to the normal bytes.  From a start within an ulp
+// or two of the quotient the answer is c - 1, c or c + 1 whenever the products are
+// normal fp32 numbers (s_o >= 2^-110), and the top values of c - 1 and c decide it.
+// Below that the top values of c - 2 .. c + 1, computed side by side, take one step,
+// and where that is not enough (fp32-subnormal products) two walks reach the exact
+// answer, since the top value grows with sigma.
 __device__ __forceinline__ float inner_top(uint32_t b, float s_o) {
     return __fmul_rn(__fmul_rn(6.0f, e4m3_normal_to_float(b)), s_o);   // 6 sigma is exact
 }
 __device__ __forceinline__ uint32_t inner_scale_byte(float a_i, float s_o, float inv_m6) {
-    uint32_t c = e4m3_ceil_byte(__fmul_rn(a_i, inv_m6));
-    if (c < 0x08u) c = 0x08u;                        // the smallest normal E4M3 value, 2^-6
+    // c: the E4M3 ceiling of the first guess from its fp32 bits (rounded up to 3 mantissa
+    // bits, exponent rebiased 127 -> 7), clamped to the normal bytes 0x08 .. 0x7E
+    const int cb = (int)((__float_as_uint(__fmul_rn(a_i, inv_m6)) + 0xFFFFFu) >> 20) - 960;
+    const uint32_t c = (uint32_t)min(max(cb, 0x08), 0x7E);
+    if (s_o >= 0x1p-110f) {
+        // every top value is a normal fp32 number, and the first guess is a few ulps off at
+        // most: the answer is c - 1, c or c + 1, told apart by the top values of c - 1 and c
+        const uint32_t cm = c > 0x08u ? c - 1u : c;
+        const float t0 = inner_top(c, s_o), tm = inner_top(cm, s_o);
+        return t0 < a_i ? (c < 0x7Eu ? c + 1u : c) : ((cm < c && tm >= a_i) ? cm : c);
+    }
     // the top values of c - 2 .. c + 1 as independent products (clamped to the normal range)
     const uint32_t cp = c < 0x7Eu ? c + 1u : c, cm = c > 0x08u ? c - 1u : c, cmm = cm > 0x08u ? cm - 1u : cm;
     const float tp = inner_top(cp, s_o), t0 = inner_top(c, s_o), tm = inner_top(cm, s_o), tmm = inner_top(cmm, s_o);
