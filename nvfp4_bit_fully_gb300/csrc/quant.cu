@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(256, 4) k_quant_rows(Src src, OutNv onv, OutMx
 // element (r, c) sits at r*64 + (c ^ (((r >> 5) & 3) << 3)).
 // ---------------------------------------------------------------------------
 template <typename Src, int FMT, bool SR, bool RHT>
-__global__ void __launch_bounds__(256, (FMT == 0 && !SR && !RHT) ? 5 : 4) k_quant_cols(Src src, OutNv onv, OutMx omx, const PhiloxKeys pk, uint32_t tag,
+__global__ void __launch_bounds__(256, (FMT == 2 || (FMT == 0 && !SR && !RHT)) ? 5 : 4) k_quant_cols(Src src, OutNv onv, OutMx omx, const PhiloxKeys pk, uint32_t tag,
                                                     uint32_t rht_tag) {
     __shared__ __align__(16) float tile[128 * 64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
