@@ -431,3 +431,64 @@ def test_adamw_osci_reset_full_size_sampled(tj):
         resets += int(mk_ref.sum())
         q.reverse()
     assert resets > 0
+
+
+def test_fp6_fp4_slice_full_size_sampled(tj):
+    """The FP6 x FP4 outlier slice at the forward-with-OutControl shapes (16384 x 1024 -> 4096,
+    103 outlier channels) in the calls the benchmark times: X's slice in E2M3, W's in E2M1;
+    backward with dY 16384 x 4096 (Student-t rows), whose slices take the partner formats
+    (dX: E2M3 x E2M1, dW: E2M1 x E2M3).  Sampled slice rows bit-exact; sampled Y and the
+    outlier columns of dX and dW within tolerance."""
+    from oracle import formats as F
+
+    E2M3, E2M1 = F.MX_E2M3, F.MX_E2M1
+    batches, X, W, _heavy = wl.fwd_outctl(seed=1)
+    dY = wl.bwd_rht(seed=2)[0]
+    K = X.shape[1]
+    k = OC.outlier_count(K, 10)
+    sumsq = np.zeros(K, dtype=np.float64)
+    sumsq_gpu = torch.zeros(K, dtype=torch.float64, device="cuda")
+    for xb in batches:
+        tj.outlier_calibrate(xb.cuda(), sumsq_gpu)
+        sumsq = OC.accumulate_sumsq(xb.float().numpy(), sumsq)
+    oi, ni = tj.outlier_calibrate(None, sumsq_gpu, finalize=True, k=k)
+    outl, _ = OC.top_k_channels(sumsq, k)
+    assert np.array_equal(oi.cpu().numpy().astype(np.int64), outl)
+    M, N = X.shape[0], W.shape[0]
+    wq = tj.quantize_nvfp4(W.cuda(), sel=ni)
+    w8 = tj.quantize_mxfp8(W.cuda(), sel=oi, fmt=E2M1)
+    y, xq, x8 = tj.linear_fwd(X.cuda(), wq, w8, ni, oi, fmt_x8=E2M3)
+    seed = 1001
+    dx = tj.linear_bwd_dx(dY.cuda(), wq, w8, ni, oi, seed=seed, out_dtype=torch.float32)
+    dw = tj.linear_bwd_dw(dY.cuda(), xq, x8, ni, oi, seed=seed)
+    torch.cuda.synchronize()
+    tj.device_status()
+
+    rng = np.random.default_rng(9)
+    Xf, Wf, dYf = X.float().numpy(), W.float().numpy(), dY.float().numpy()
+    m_s, n_s = _samples(M, 10, rng), _samples(N, 10, rng)
+    fx = OL.quantize_forward_operand(Xf[m_s], outl, E2M3)
+    fw = OL.quantize_forward_operand(Wf[n_s], outl, E2M1)
+    _rows_equal(mxfp8_to_logical(x8), fx["q8"], m_s, "X-hat E2M3 slice rows")
+    _rows_equal(mxfp8_to_logical(w8), fw["q8"], n_s, "W E2M1 slice rows")
+    _rows_equal(nvfp4_to_logical(xq), fx["q"], m_s, "X-hat rows")
+    abs_mx = lambda qa, fa, qb, fb: np.abs(Q.dequantize_mx_f64(*qa, fa)) @ np.abs(Q.dequantize_mx_f64(*qb, fb)).T
+    y_ref = OL.gemm_fp4(fx["q"], fw["q"]) + OL.gemm_mx(fx["q8"], E2M3, fw["q8"], E2M1)
+    y_abs = _abs_nv(fx["q"], fw["q"]) + abs_mx(fx["q8"], E2M3, fw["q8"], E2M1)
+    assert_gemm_close(_f32(y)[np.ix_(m_s, n_s)], y_ref, y_abs, bf16=True, what="Y (sampled)")
+
+    # dX on the outlier channels: Q_E2M3(dY rows) x Q_E2M1(W-hat_O^T)^T
+    w_slice = Q.quantize_mx(Wf[:, outl], E2M1)
+    q8_w = Q.quantize_mx(np.ascontiguousarray(Q.dequantize_mx_f32(*w_slice, E2M1)[:, :k].T), E2M1)
+    q8_dy = Q.quantize_mx(dYf[m_s], E2M3)
+    dx_ref = OL.gemm_mx(q8_dy, E2M3, q8_w, E2M1)[:, :k]
+    dx_abs = abs_mx(q8_dy, E2M3, q8_w, E2M1)[:, :k]
+    assert_gemm_close(_f32(dx)[np.ix_(m_s, outl)], dx_ref, dx_abs, what="dX outlier columns (sampled rows)")
+
+    # dW on the outlier channels: Q_E2M1(dY^T rows) x Q_E2M3(X-hat_O^T)^T
+    x_slice = Q.quantize_mx(Xf[:, outl], E2M3)
+    q8_x = Q.quantize_mx(np.ascontiguousarray(Q.dequantize_mx_f32(*x_slice, E2M3)[:, :k].T), E2M3)
+    q8_dyt = Q.quantize_mx(np.ascontiguousarray(dYf[:, n_s].T), E2M1)
+    dw_ref = OL.gemm_mx(q8_dyt, E2M1, q8_x, E2M3)[:, :k]
+    dw_abs = abs_mx(q8_dyt, E2M1, q8_x, E2M3)[:, :k]
+    assert_gemm_close(_f32(dw)[np.ix_(n_s, outl)], dw_ref, dw_abs, what="dW outlier columns (sampled rows)")
