@@ -232,7 +232,7 @@ __device__ __forceinline__ void named_arrive(int id, int count) {
 // Warp-uniform bounded wait.  Every lane polls the barrier: a completed phase is
 // seen several hundred cycles sooner by a warp whose lanes all wait than by one
 // that waits on lane 0 and broadcasts (measured on GB300 in the partial-slot
-// handshake: 802 against 858 cycles per block).  The verdict is the lanes'
+// handshake: 802 against 858 cycles per block).  The result is the lanes'
 // conjunction; a phase, once complete, stays complete, so the lanes agree unless
 // the wait ran out.
 __device__ __forceinline__ bool warp_wait_bounded(uint64_t *bar, uint32_t parity, Bars *bars, long long wait_clk) {
