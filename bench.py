@@ -279,8 +279,8 @@ TRAFFIC_BYTES_PER_LAUNCH = {"k_gemm_nvfp4": 108.7e6}
 # kernel entry reports an issue roofline: lane instructions / (SMs x 128 lanes x SM clock x
 # time), the fraction of the SMs' instruction issue the kernel uses.
 LANE_INSTR_PER_ELEM = {
-    "k_quant_rows (NVFP4 + MXFP8 of dY)": 42.34, "k_quant_cols (NVFP4 + MXFP8 of dY)": 45.09,
-    "k_quant_split (OutControl split of X)": 29.50, "k_quant_cols<SrcNv> (re-align)": 48.98,
+    "k_quant_rows (NVFP4 + MXFP8 of dY)": 40.89, "k_quant_cols (NVFP4 + MXFP8 of dY)": 45.81,
+    "k_quant_split (OutControl split of X)": 28.21, "k_quant_cols<SrcNv> (re-align)": 47.59,
     "k_quant_cols<SrcMx> (re-align)": 27.54,
 }
 NV_B = 0.5 + 1.0 / 16 + 4.0 / 128      # bytes per NVFP4 element (codes + E4M3 + FP32 scales)

@@ -233,5 +233,8 @@ def dequantize_mx_f64(codes, sbytes, fmt):
 
 
 def dequantize_mx_f32(codes, sbytes, fmt):
-    """fp32 values of an MX slice (exact: a short-mantissa value times a power of two)."""
-    return dequantize_mx_f64(codes, sbytes, fmt).astype(F32)
+    """fp32 values of an MX slice (exact: a short-mantissa value times a power of two).  An
+    element of a block scaled near the top of the fp32 range can round up to a grid value
+    beyond it (E2M1 6 x 2^126 = 5.1e38); its fp32 value is then infinite, as on the GPU."""
+    with np.errstate(over="ignore"):
+        return dequantize_mx_f64(codes, sbytes, fmt).astype(F32)

@@ -241,3 +241,30 @@ def test_linear_with_fp6_fp4_slice(tj, fmt_x, fmt_w):
     bw[:, nc] = abs_product(s_dyt, s_x, OL.ALPHA_RHT)[:, :K_N]
     bw[:, outl] = abs_product_mx(q8_dyt, pdw, q8_x, fmt_x)[:, :k]
     assert_gemm_close(dw.cpu().numpy(), OL.bwd_dw(dYf, fx, outl, seed), bw, what="dW")
+
+
+@pytest.mark.parametrize("fmt", [F.MX_E4M3] + SUB)
+def test_extreme_magnitudes(tj, fmt):
+    """Blocks near the top of fp32 (the scale exponent near +127), blocks of fp32-subnormal
+    values (the exponent clamped at -127, elements far below a step), blocks mixing a huge
+    maximum with tiny elements, and exact powers of two: codes and scales bit for bit, in
+    both orientations."""
+    rng = np.random.default_rng(77 + fmt)
+    rows, cols = 64, 256
+    x = rng.standard_normal((rows, cols)).astype(np.float32)
+    x[0:8] *= np.float32(1e37)                                  # amax up to ~4e37
+    x[8, :32] = np.float32(3.0e38)
+    x[8, 32:64] = -np.float32(3.3e38)
+    x[9:16] = (rng.standard_normal((7, cols)) * 1e-39).astype(np.float32)   # subnormal
+    x[16:24, ::32] = np.float32(1e30)
+    x[16:24, 1::32] = np.float32(1e-30)
+    x[24:32] = np.exp2(rng.integers(-140, 120, (8, cols))).astype(np.float32) * rng.choice([-1, 1], (8, cols))
+    t = torch.from_numpy(x).cuda()
+    q = tj.quantize_mxfp8(t, fmt=fmt)
+    qt = tj.quantize_mxfp8(t, along_cols=True, fmt=fmt)
+    y = tj.dequantize_mxfp8(q)
+    torch.cuda.synchronize()
+    ref = Q.quantize_mx(x, fmt)
+    assert_mxfp8_equal(q, ref, "rows, extreme magnitudes")
+    assert_mxfp8_equal(qt, Q.quantize_mx(np.ascontiguousarray(x.T), fmt), "columns, extreme magnitudes")
+    assert np.array_equal(y.cpu().numpy(), Q.dequantize_mx_f32(*ref, fmt)[:, :cols])
