@@ -144,8 +144,7 @@ class Timeline:
 CALL_KERNEL = {
     "quant_x": "k_quant_split (OutControl split of X)", "quant_dy_row": "k_quant_rows (NVFP4 + MXFP8 of dY)",
     "quant_dy_col": "k_quant_cols (NVFP4 + MXFP8 of dY)",
-    "requant_w": "k_quant_cols<SrcNv> (re-align)", "requant_x": "k_quant_cols<SrcNv> (re-align)",
-    "requant_w8": "k_quant_cols<SrcMx> (re-align)", "requant_x8": "k_quant_cols<SrcMx> (re-align)",
+    "requant_w": "k_realign_pair (re-align NVFP4 + slice)", "requant_x": "k_realign_pair (re-align NVFP4 + slice)",
     "gemm_fwd": "k_gemm_nvfp4", "gemm_dx": "k_gemm_nvfp4", "gemm_dw": "k_gemm_nvfp4",
     "osci_reset": "k_osci_reset",
 }
@@ -199,12 +198,15 @@ class Linear:
             "gemm_dw": (f4(N, kn, M), f4(N, k, M)),
             "quant_x": M * kn * (2 + NV_B) + M * k * (2 + MX_B),
             "quant_dy_row": M * N * (2 + NV_B + MX_B), "quant_dy_col": M * N * (2 + NV_B + MX_B),
-            "requant_w": 2 * kn * N * NV_B, "requant_w8": 2 * k * N * MX_B, "requant_x": 2 * kn * M * NV_B,
-            "requant_x8": 2 * k * M * MX_B,
+            "requant_w": 2 * kn * N * NV_B + 2 * k * N * MX_B, "requant_x": 2 * kn * M * NV_B + 2 * k * M * MX_B,
         }
-        # elements each quantize call processes (for the issue roofline)
-        self.elems = {"quant_x": M * K, "quant_dy_row": M * N, "quant_dy_col": M * N, "requant_w": kn * N,
-                      "requant_w8": k * N, "requant_x": kn * M, "requant_x8": k * M}
+        # lane instructions of each quantize call (per-element counts x elements, for the issue
+        # roofline); a re-alignment pair is the NVFP4 operand's and the slice's together
+        li = LANE_INSTR_PER_ELEM
+        self.lane_instr = {"quant_x": li["split"] * M * K, "quant_dy_row": li["rows"] * M * N,
+                           "quant_dy_col": li["cols"] * M * N,
+                           "requant_w": li["realign_nv"] * kn * N + li["realign_mx"] * k * N,
+                           "requant_x": li["realign_nv"] * kn * M + li["realign_mx"] * k * M}
 
     def run(self, tj, seed, tl, stream):
         T = lambda name, fn: tl.time(self.name + "." + name, fn)
@@ -219,9 +221,9 @@ class Linear:
         T("quant_dy_row", lambda: tj.quantize_nvfp4_mxfp8(self.dY, mode=SR, rht=True, seed=seed, tag=tj.TAG_DY_ROW,
                                                           rht_tag=tj.TAG_RHT_DX, out=self.s_dy, out8=self.q8_dy,
                                                           stream=s))
-        T("requant_w", lambda: tj.requantize_nvfp4(self.wq, SR, True, seed, tj.TAG_WT, tj.TAG_RHT_DX, out=self.s_w,
-                                                   stream=s))
-        T("requant_w8", lambda: tj.requantize_mxfp8(self.w8, out=self.q8_w, stream=s))
+        # W-hat^T and its slice re-aligned in one launch
+        T("requant_w", lambda: tj.requantize_nvfp4_mxfp8(self.wq, self.w8, SR, True, seed, tj.TAG_WT, tj.TAG_RHT_DX,
+                                                         out=self.s_w, out8=self.q8_w, stream=s))
         # the FP4 product and its FP8 outlier slice in one launch
         T("gemm_dx", lambda: tj.gemm_pair(self.s_dy, self.s_w, self.q8_dy, self.q8_w, alpha=2.0 ** -7, out=self.dX,
                                           out8=self.dX, col_map=self.ni, col_map8=self.oi, stream=s))
@@ -229,9 +231,8 @@ class Linear:
         T("quant_dy_col", lambda: tj.quantize_nvfp4_mxfp8(self.dY, along_cols=True, mode=SR, rht=True, seed=seed,
                                                           tag=tj.TAG_DY_COL, rht_tag=tj.TAG_RHT_DW, out=self.s_dyt,
                                                           out8=self.q8_dyt, stream=s))
-        T("requant_x", lambda: tj.requantize_nvfp4(self.xq, SR, True, seed, tj.TAG_XT, tj.TAG_RHT_DW, out=self.s_x,
-                                                   stream=s))
-        T("requant_x8", lambda: tj.requantize_mxfp8(self.x8, out=self.q8_x, stream=s))
+        T("requant_x", lambda: tj.requantize_nvfp4_mxfp8(self.xq, self.x8, SR, True, seed, tj.TAG_XT, tj.TAG_RHT_DW,
+                                                         out=self.s_x, out8=self.q8_x, stream=s))
         T("gemm_dw", lambda: tj.gemm_pair_f32(self.s_dyt, self.s_x, self.q8_dyt, self.q8_x, self.dW, self.ni, self.oi,
                                               alpha=2.0 ** -7, stream=s))
 
@@ -278,11 +279,7 @@ TRAFFIC_BYTES_PER_LAUNCH = {"k_gemm_nvfp4": 108.7e6}
 # X for the split, elements of the re-aligned tensor for the re-alignments).  With them each
 # kernel entry reports an issue roofline: lane instructions / (SMs x 128 lanes x SM clock x
 # time), the fraction of the SMs' instruction issue the kernel uses.
-LANE_INSTR_PER_ELEM = {
-    "k_quant_rows (NVFP4 + MXFP8 of dY)": 40.89, "k_quant_cols (NVFP4 + MXFP8 of dY)": 45.81,
-    "k_quant_split (OutControl split of X)": 28.21, "k_quant_cols<SrcNv> (re-align)": 47.59,
-    "k_quant_cols<SrcMx> (re-align)": 27.54,
-}
+LANE_INSTR_PER_ELEM = {"rows": 40.89, "cols": 45.81, "split": 28.21, "realign_nv": 47.59, "realign_mx": 27.54}
 NV_B = 0.5 + 1.0 / 16 + 4.0 / 128      # bytes per NVFP4 element (codes + E4M3 + FP32 scales)
 MX_B = 1.0 + 1.0 / 32                   # bytes per MXFP8 element (E4M3 + UE8M0)
 
@@ -775,15 +772,15 @@ def main():
     # per call: average ms and throughput against its algorithmic work
     parts = {}
     kern = {}                       # kernel -> [total ms, flops4, flops8, bytes, launches]
-    kern_elems = {}                 # kernel -> elements processed over the timed steps
+    kern_instr = {}                 # kernel -> lane instructions over the timed steps (quantize kernels)
     for name, (ms_tot, n) in sorted(summ.items()):
         call = name.split(".")[-1]
         p = {"ms": round(ms_tot / n, 4)}
         agg = kern.setdefault(CALL_KERNEL[call], [0.0, 0.0, 0.0, 0.0, 0])
         if call != "osci_reset":
-            lin_e = next(l for l in linears if l.name == name.split(".")[0]).elems.get(call)
-            if lin_e is not None:
-                kern_elems[CALL_KERNEL[call]] = kern_elems.get(CALL_KERNEL[call], 0) + lin_e * n
+            lin_i = next(l for l in linears if l.name == name.split(".")[0]).lane_instr.get(call)
+            if lin_i is not None:
+                kern_instr[CALL_KERNEL[call]] = kern_instr.get(CALL_KERNEL[call], 0.0) + lin_i * n
         agg[0] += ms_tot
         agg[4] += n
         if call == "osci_reset":
@@ -811,11 +808,10 @@ def main():
                       "frac": round(t_star / (ms_tot * 1e-3), 4)})
         else:
             e.update({"GB/s": round(by / (ms_tot * 1e-3) / 1e9, 1), "frac": round(by / (ms_tot * 1e-3) / 1e9 / hbm_peak, 3)})
-            if kname in LANE_INSTR_PER_ELEM and kname in kern_elems and clk.get("sm_mhz"):
+            if kname in kern_instr and clk.get("sm_mhz"):
                 lanes_per_s = num_sms * 128 * float(clk["sm_mhz"]) * 1e6
-                e["issue_roofline"] = {
-                    "lane_instr_per_elem": LANE_INSTR_PER_ELEM[kname],
-                    "frac": round(LANE_INSTR_PER_ELEM[kname] * kern_elems[kname] / (lanes_per_s * ms_tot * 1e-3), 3)}
+                e["issue_roofline"] = {"lane_instr_per_step": round(kern_instr[kname] / args.steps),
+                                       "frac": round(kern_instr[kname] / (lanes_per_s * ms_tot * 1e-3), 3)}
         kernels[kname] = e
     # dominant kernel of the step (largest total time), with its roofline
     dom = max(kern.items(), key=lambda kv: kv[1][0])[0]
@@ -837,8 +833,8 @@ def main():
                 "traffic": (round(TRAFFIC_BYTES_PER_ELEM[dom] * osci.n) if dom in TRAFFIC_BYTES_PER_ELEM else None),
                 "algorithmic_bytes_per_launch": round(by / n), "peak_source": peak_src + " hbm_gbs"}
     # every recorded call of the timed region launches exactly one kernel of the library
-    # (per linear: split + GEMM, dY rows + 2 re-alignments + GEMM pair, dY columns + 2
-    # re-alignments + GEMM pair; then one OsciReset)
+    # (per linear: split + GEMM, dY rows + re-alignment pair + GEMM pair, dY columns +
+    # re-alignment pair + GEMM pair; then one OsciReset)
     launches = len(tl.records)
 
     extras = {}

@@ -195,6 +195,16 @@ tj_status tj_requantize_nvfp4(const tj_nvfp4 *in, int mode, int rht, uint64_t se
  * is decoded in in->fmt and re-quantized in out->fmt. */
 tj_status tj_requantize_mxfp8(const tj_mxfp8 *in, tj_mxfp8 *out, void *stream);
 
+/* tj_requantize_nvfp4_mxfp8 - tj_requantize_nvfp4(in, mode, rht, seed, tag, rht_tag, out) and
+ * tj_requantize_mxfp8(in8, out8) in one launch: the backward re-alignment of a forward
+ * operand and of its outlier slice (§2.A, §2.C).  Alone the slice's few tiles leave the GPU
+ * mostly idle; here they run beside the operand's.  Results equal the two calls byte for
+ * byte (errors as theirs); used inside tj_linear_bwd_dx / _dw when there are outlier
+ * channels. */
+tj_status tj_requantize_nvfp4_mxfp8(const tj_nvfp4 *in, int mode, int rht, uint64_t seed, uint32_t tag,
+                                    uint32_t rht_tag, tj_nvfp4 *out, const tj_mxfp8 *in8, tj_mxfp8 *out8,
+                                    void *stream);
+
 /* tj_rht - standalone random Hadamard transform (§2.C): for each row of x (fp32,
  * [rows, cols], cols a multiple of 128, contiguous) y = H128 * (d .* x) per
  * 128-block, unnormalised, fp32 butterflies in stage order 1, 2, ..., 64.

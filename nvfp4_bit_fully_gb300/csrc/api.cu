@@ -220,6 +220,26 @@ tj_status tj_requantize_mxfp8(const tj_mxfp8 *in, tj_mxfp8 *out, void *stream) {
     return cuda_status(launch_realign_mx(*in, *out, static_cast<cudaStream_t>(stream)));
 }
 
+tj_status tj_requantize_nvfp4_mxfp8(const tj_nvfp4 *in, int mode, int rht, uint64_t seed, uint32_t tag,
+                                    uint32_t rht_tag, tj_nvfp4 *out, const tj_mxfp8 *in8, tj_mxfp8 *out8,
+                                    void *stream) {
+    if (in == nullptr || out == nullptr || in8 == nullptr || out8 == nullptr || (mode != TJ_RTN && mode != TJ_SR))
+        return TJ_ERR_INVALID_ARG;
+    tj_status st = check_nv(in, in->rows, in->cols);
+    if (st == TJ_OK) st = check_nv(out, in->cols, in->rows);
+    if (st == TJ_OK) st = check_mx(in8, in8->rows, in8->cols);
+    if (st == TJ_OK) st = check_mx(out8, in8->cols, in8->rows);
+    if (st != TJ_OK) return st;
+    if (!cols_grid_fits(in->rows) || !cols_grid_fits(in8->rows)) return TJ_ERR_SHAPE;
+    if (in->cols == 0 || in8->cols == 0) {           // an empty part: the other part alone
+        if (in->cols > 0) TJ_TRY(launch_realign_nv(*in, *out, mode, rht, seed, tag, rht_tag, static_cast<cudaStream_t>(stream)));
+        if (in8->cols > 0) TJ_TRY(launch_realign_mx(*in8, *out8, static_cast<cudaStream_t>(stream)));
+        return TJ_OK;
+    }
+    return cuda_status(launch_realign_pair(*in, *out, mode, rht, seed, tag, rht_tag, *in8, *out8,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 tj_status tj_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, void *stream) {
     if (x == nullptr || y == nullptr || rows < 0 || cols < 0) return TJ_ERR_INVALID_ARG;
     if (cols % 128 != 0) return TJ_ERR_SHAPE;
@@ -397,10 +417,15 @@ tj_status tj_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, c
     else
         TJ_TRY(launch_quant_nv_dense(dy, TJ_BF16, M, N, lddy, 0, nullptr, TJ_SR, 1, seed, TJ_TAG_DY_ROW,
                                      TJ_TAG_RHT_DX, s_dy, s));
-    TJ_TRY(launch_realign_nv(*wq, s_w, TJ_SR, 1, seed, TJ_TAG_WT, TJ_TAG_RHT_DX, s));
+    if (k > 0 && kn > 0) {
+        // W-hat^T and its slice re-aligned in one launch
+        TJ_TRY(launch_realign_pair(*wq, s_w, TJ_SR, 1, seed, TJ_TAG_WT, TJ_TAG_RHT_DX, *w8, q8_w, s));
+    } else {
+        TJ_TRY(launch_realign_nv(*wq, s_w, TJ_SR, 1, seed, TJ_TAG_WT, TJ_TAG_RHT_DX, s));
+        if (k > 0) TJ_TRY(launch_realign_mx(*w8, q8_w, s));
+    }
     if (k > 0) {
         // the FP4 product (normal columns of dX) and the slice (outlier columns) in one launch
-        TJ_TRY(launch_realign_mx(*w8, q8_w, s));
         TJ_TRY(launch_gemm_pair(&s_dy, &s_w, 0.0078125f, dx, out_dtype, lddx, M, kn, normal_idx, &q8_dy, &q8_w, dx,
                                 out_dtype, lddx, M, k, outlier_idx, s));
     } else {
@@ -441,12 +466,17 @@ tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, c
     else
         TJ_TRY(launch_quant_nv_dense(dy, TJ_BF16, M, N, lddy, 1, nullptr, TJ_SR, 1, seed, TJ_TAG_DY_COL,
                                      TJ_TAG_RHT_DW, s_dy, s));
-    TJ_TRY(launch_realign_nv(*xq, s_x, TJ_SR, 1, seed, TJ_TAG_XT, TJ_TAG_RHT_DW, s));
+    if (k > 0 && kn > 0) {
+        // X-hat^T and its slice re-aligned in one launch
+        TJ_TRY(launch_realign_pair(*xq, s_x, TJ_SR, 1, seed, TJ_TAG_XT, TJ_TAG_RHT_DW, *x8, q8_x, s));
+    } else {
+        TJ_TRY(launch_realign_nv(*xq, s_x, TJ_SR, 1, seed, TJ_TAG_XT, TJ_TAG_RHT_DW, s));
+        if (k > 0) TJ_TRY(launch_realign_mx(*x8, q8_x, s));
+    }
     // dW [N][K] is fp32 and covered by the launch, so a long-K launch may split K in two
     const SplitRegion whole_dw{dw, N, K, lddw};
     if (k > 0) {
         // the FP4 product (normal columns of dW) and the slice (outlier columns) in one launch
-        TJ_TRY(launch_realign_mx(*x8, q8_x, s));
         TJ_TRY(launch_gemm_pair(&s_dy, &s_x, 0.0078125f, dw, TJ_FP32, lddw, N, kn, normal_idx, &q8_dy, &q8_x, dw,
                                 TJ_FP32, lddw, N, k, outlier_idx, s, &whole_dw));
     } else {

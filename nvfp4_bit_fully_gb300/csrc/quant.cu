@@ -270,13 +270,13 @@ __global__ void __launch_bounds__(256, 4) k_quant_rows(Src src, OutNv onv, OutMx
 // and the column reads (lanes = 8 columns x 4 quad lanes) are conflict-free:
 // element (r, c) sits at r*64 + (c ^ (((r >> 5) & 3) << 3)).
 // ---------------------------------------------------------------------------
+// One tile (output rows 64 bx .., input-row block by), with the CTA's staging tile.
 template <typename Src, int FMT, bool SR, bool RHT>
-__global__ void __launch_bounds__(256, (FMT == 2 || (FMT == 0 && !SR && !RHT)) ? 5 : 4) k_quant_cols(Src src, OutNv onv, OutMx omx, const PhiloxKeys pk, uint32_t tag,
-                                                    uint32_t rht_tag) {
-    __shared__ __align__(16) float tile[128 * 64];
+__device__ __forceinline__ void quant_cols_tile(const Src &src, const OutNv &onv, const OutMx &omx, const PhiloxKeys &pk,
+                                                uint32_t tag, uint32_t rht_tag, int64_t bx, int64_t by, float *tile) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t c0 = (int64_t)blockIdx.x * 64;      // first output row of the tile
-    const int64_t kb = blockIdx.y;                    // 128-block along the input rows
+    const int64_t c0 = bx * 64;                       // first output row of the tile
+    const int64_t kb = by;                            // 128-block along the input rows
     const int64_t r0 = kb * 128;
     // with the RHT, input row rr (element rr of every output segment) is negated while
     // loading when its diagonal entry is -1
@@ -318,6 +318,26 @@ __global__ void __launch_bounds__(256, (FMT == 2 || (FMT == 0 && !SR && !RHT)) ?
         const MxSeg s = quant_mx_group(x, omx.fmt);
         store_mx_seg(omx, row, kb, t, s, valid);
     }
+}
+
+template <typename Src, int FMT, bool SR, bool RHT>
+__global__ void __launch_bounds__(256, (FMT == 2 || (FMT == 0 && !SR && !RHT)) ? 5 : 4) k_quant_cols(Src src, OutNv onv, OutMx omx, const PhiloxKeys pk, uint32_t tag,
+                                                    uint32_t rht_tag) {
+    __shared__ __align__(16) float tile[128 * 64];
+    quant_cols_tile<Src, FMT, SR, RHT>(src, onv, omx, pk, tag, rht_tag, blockIdx.x, blockIdx.y, tile);
+}
+
+// The backward re-alignment of a forward NVFP4 operand and of its outlier slice in one
+// launch: blocks [0, nb) take the slice's tiles (nxb per input-row block), the others the
+// NVFP4 operand's (nxa per input-row block).  Alone the slice's few tiles leave the GPU
+// mostly idle; here they run beside the operand's.
+template <bool SR, bool RHT>
+__global__ void __launch_bounds__(256, 4) k_realign_pair(SrcNv sa, OutNv oa, SrcMx sb, OutMx ob, const PhiloxKeys pk,
+                                                         uint32_t tag, uint32_t rht_tag, int nxa, int nxb, int nb) {
+    __shared__ __align__(16) float tile[128 * 64];
+    const int b = (int)blockIdx.x;
+    if (b < nb) quant_cols_tile<SrcMx, 1, false, false>(sb, OutNv{}, ob, pk, 0u, 0u, b % nxb, b / nxb, tile);
+    else quant_cols_tile<SrcNv, 0, SR, RHT>(sa, oa, OutMx{}, pk, tag, rht_tag, (b - nb) % nxa, (b - nb) / nxa, tile);
 }
 
 // ---------------------------------------------------------------------------
@@ -665,6 +685,26 @@ cudaError_t launch_realign_nv(const tj_nvfp4 &in, const tj_nvfp4 &out, int mode,
 // The FP8 outlier slice of a forward operand, transposed and re-quantized (RTN).
 cudaError_t launch_realign_mx(const tj_mxfp8 &in, const tj_mxfp8 &out, cudaStream_t s) {
     return cols_mx(src_mx(in), out_mx(out), s);
+}
+
+// Both re-alignments of a forward operand with an outlier slice, in one launch.
+cudaError_t launch_realign_pair(const tj_nvfp4 &in, const tj_nvfp4 &out, int mode, int rht, uint64_t seed,
+                                uint32_t tag, uint32_t rht_tag, const tj_mxfp8 &in8, const tj_mxfp8 &out8,
+                                cudaStream_t s) {
+    const OutNv oa = out_nv(out);
+    const OutMx ob = out_mx(out8);
+    const int64_t nxa = oa.rows_p / 64, nya = oa.cols_p / 128, nxb = ob.rows_p / 64, nyb = ob.cols_p / 128;
+    const int64_t nb = nxb * nyb, n = nb + nxa * nya;
+    if (nxa == 0 || nxb == 0 || n > 0x7fffffff) return cudaErrorInvalidValue;
+    const PhiloxKeys pk = philox_keys(seed);
+    const SrcNv sa = src_nv(in);
+    const SrcMx sb = src_mx(in8);
+    const unsigned grid = (unsigned)n;
+    if (mode == TJ_SR && rht)  k_realign_pair<true, true><<<grid, kThreads, 0, s>>>(sa, oa, sb, ob, pk, tag, rht_tag, (int)nxa, (int)nxb, (int)nb);
+    else if (mode == TJ_SR)    k_realign_pair<true, false><<<grid, kThreads, 0, s>>>(sa, oa, sb, ob, pk, tag, rht_tag, (int)nxa, (int)nxb, (int)nb);
+    else if (rht)              k_realign_pair<false, true><<<grid, kThreads, 0, s>>>(sa, oa, sb, ob, pk, tag, rht_tag, (int)nxa, (int)nxb, (int)nb);
+    else                       k_realign_pair<false, false><<<grid, kThreads, 0, s>>>(sa, oa, sb, ob, pk, tag, rht_tag, (int)nxa, (int)nxb, (int)nb);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,

@@ -22,6 +22,9 @@ cudaError_t launch_quant_mx_dense(const void *x, int dtype, int64_t rows_x, int6
 cudaError_t launch_realign_nv(const tj_nvfp4 &in, const tj_nvfp4 &out, int mode, int rht, uint64_t seed,
                               uint32_t tag, uint32_t rht_tag, cudaStream_t s);
 cudaError_t launch_realign_mx(const tj_mxfp8 &in, const tj_mxfp8 &out, cudaStream_t s);
+cudaError_t launch_realign_pair(const tj_nvfp4 &in, const tj_nvfp4 &out, int mode, int rht, uint64_t seed,
+                                uint32_t tag, uint32_t rht_tag, const tj_mxfp8 &in8, const tj_mxfp8 &out8,
+                                cudaStream_t s);
 cudaError_t launch_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,
                        cudaStream_t s);
 cudaError_t launch_dequant_nv(const tj_nvfp4 &q, float *y, int64_t ldy, cudaStream_t s);

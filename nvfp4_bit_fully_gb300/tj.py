@@ -58,6 +58,8 @@ _SIGS = {
                                 ctypes.POINTER(CNvfp4), ctypes.POINTER(CMxfp8), _P],
     "tj_requantize_nvfp4": [ctypes.POINTER(CNvfp4), _I, _I, _U64, _U32, _U32, ctypes.POINTER(CNvfp4), _P],
     "tj_requantize_mxfp8": [ctypes.POINTER(CMxfp8), ctypes.POINTER(CMxfp8), _P],
+    "tj_requantize_nvfp4_mxfp8": [ctypes.POINTER(CNvfp4), _I, _I, _U64, _U32, _U32, ctypes.POINTER(CNvfp4),
+                                  ctypes.POINTER(CMxfp8), ctypes.POINTER(CMxfp8), _P],
     "tj_rht": [_P, _P, _I64, _I64, _U64, _U32, _P],
     "tj_dequantize_nvfp4": [ctypes.POINTER(CNvfp4), _P, _I64, _P],
     "tj_dequantize_mxfp8": [ctypes.POINTER(CMxfp8), _P, _I64, _P],
@@ -248,6 +250,17 @@ def requantize_mxfp8(q, out=None, stream=None, fmt=None):
     ci, co = q.c(), out.c()
     _call("tj_requantize_mxfp8", ctypes.byref(ci), ctypes.byref(co), _stream(stream))
     return out
+
+
+def requantize_nvfp4_mxfp8(q, q8, mode=TJ_SR, rht=True, seed=0, tag=0, rht_tag=0, out=None, out8=None, stream=None):
+    """Both backward re-alignments of a forward operand (NVFP4 q [rows, cols] and its slice q8) in
+    one launch (tj_requantize_nvfp4_mxfp8); returns (out, out8)."""
+    out = out if out is not None else NVFP4.empty(q.cols, q.rows, q.codes.device)
+    out8 = out8 if out8 is not None else MXFP8.empty(q8.cols, q8.rows, q8.codes.device, q8.fmt)
+    ci, co, ci8, co8 = q.c(), out.c(), q8.c(), out8.c()
+    _call("tj_requantize_nvfp4_mxfp8", ctypes.byref(ci), mode, int(rht), seed, tag, rht_tag, ctypes.byref(co),
+          ctypes.byref(ci8), ctypes.byref(co8), _stream(stream))
+    return out, out8
 
 
 def rht(x, seed, tag, out=None, stream=None):

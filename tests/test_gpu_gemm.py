@@ -183,3 +183,19 @@ def test_gemm_pair_f32_whole_output(tj, K, k):
     assert_gemm_close(got[:, cm.cpu().numpy()], OL.gemm_fp4(ra, rb, 2.0 ** -7), abs_product(ra, rb, 2.0 ** -7),
                       what="pair_f32 fp4")
     assert_gemm_close(got[:, cm8.cpu().numpy()], OL.gemm_fp8(ra8, rb8), abs_product_fp8(ra8, rb8), what="pair_f32 fp8")
+
+
+@pytest.mark.parametrize("mode,rht,fmt", [(1, True, 0), (0, False, 5), (1, True, 3)])
+def test_realignment_pair_equals_the_two_calls(tj, mode, rht, fmt):
+    """tj_requantize_nvfp4_mxfp8: the NVFP4 operand and its slice re-aligned in one launch are
+    byte for byte the two separate calls."""
+    g = torch.Generator().manual_seed(17 + fmt)
+    X = torch.randn(300, 700, generator=g).to(torch.bfloat16)
+    q = tj.quantize_nvfp4(X[:, :597].contiguous().cuda())
+    q8 = tj.quantize_mxfp8(X[:, 597:].contiguous().cuda(), fmt=fmt)
+    a, a8 = tj.requantize_nvfp4_mxfp8(q, q8, mode, rht, 99, 4, 0x101)
+    b = tj.requantize_nvfp4(q, mode, rht, 99, 4, 0x101)
+    b8 = tj.requantize_mxfp8(q8)
+    torch.cuda.synchronize()
+    for x, y in ((a.codes, b.codes), (a.sf, b.sf), (a.outer, b.outer), (a8.codes, b8.codes), (a8.sf, b8.sf)):
+        assert torch.equal(x, y)
