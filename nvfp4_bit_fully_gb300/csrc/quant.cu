@@ -429,28 +429,39 @@ __global__ void __launch_bounds__(kSplitThreads) k_quant_split(const T *x, int64
     const int nch = vec ? K / kv : 0;                    // full chunks per row, loaded as vectors
     const int nw = sizeof(T) == 2 ? (K + 1) / 2 : K;     // data words per row
     const int wtail = 4 * nch, ntail = nw - wtail;       // words loaded one at a time
+    const int fill_dr = nch > 0 ? (int)blockDim.x / nch : 0, fill_dc = (int)blockDim.x - fill_dr * nch;
+    // the (row, segment) of a quad's task, stepped by nwarp * 8 tasks per pass
+    const int step_t = nwarp * 8;
+    const int dr_n = nseg_n > 0 ? step_t / nseg_n : 0, dk_n = step_t - dr_n * nseg_n;
+    const int dr_o = nseg_o > 0 ? step_t / nseg_o : 0, dk_o = step_t - dr_o * nseg_o;
     for (int64_t tl = blockIdx.x; tl < ntile; tl += gridDim.x) {
         const int64_t r0 = tl * tr;
         __syncthreads();                                 // the previous tile's gathers are done
-        // eight 16-byte loads in flight per thread before their stores
+        // eight 16-byte loads in flight per thread before their stores.  Chunk i of the tile is
+        // (row i / nch, chunk i % nch); the pair is stepped by blockDim.x chunks with a carry
+        // instead of dividing (the divisions were a third of the kernel's instructions)
         constexpr int kU = 8;
+        int fr = (int)threadIdx.x / (nch > 0 ? nch : 1), fc = (int)threadIdx.x - fr * nch;   // chunk threadIdx.x
         for (int i0 = threadIdx.x; i0 < tr * nch; i0 += kU * blockDim.x) {
             uint4 w[kU];
+            int rr[kU], cc[kU];
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 const int i = i0 + u * (int)blockDim.x;
+                rr[u] = fr;
+                cc[u] = fc;
+                fr += fill_dr;
+                fc += fill_dc;
+                if (fc >= nch) { fc -= nch; ++fr; }
                 w[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (i < tr * nch) {
-                    const int r = i / nch, ch = i - r * nch;
-                    if (r0 + r < rows) w[u] = __ldg(reinterpret_cast<const uint4 *>(x + (r0 + r) * ld) + ch);
-                }
+                if (i < tr * nch && r0 + rr[u] < rows)
+                    w[u] = __ldg(reinterpret_cast<const uint4 *>(x + (r0 + rr[u]) * ld) + cc[u]);
             }
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 const int i = i0 + u * (int)blockDim.x;
                 if (i < tr * nch) {
-                    const int r = i / nch, ch = i - r * nch;
-                    uint32_t *d = tile + r * rw + split_pad_row(4 * ch);  // 4 words inside one 32-word run
+                    uint32_t *d = tile + rr[u] * rw + split_pad_row(4 * cc[u]);  // 4 words inside one 32-word run
                     d[0] = w[u].x;
                     d[1] = w[u].y;
                     d[2] = w[u].z;
@@ -464,20 +475,28 @@ __global__ void __launch_bounds__(kSplitThreads) k_quant_split(const T *x, int64
         }
         __syncthreads();
         const int nt_n = tr * nseg_n;
+        int tr_n = nseg_n > 0 ? (warp * 8 + qd) / nseg_n : 0, tk_n = (warp * 8 + qd) - tr_n * nseg_n;   // task warp*8 + qd
         for (int b = warp * 8; b < nt_n; b += nwarp * 8) {             // warp-uniform
             const int task = b + qd;
             const bool ok = task < nt_n;
-            const int r = ok ? task / nseg_n : 0, kb = ok ? task - r * nseg_n : 0;
+            const int r = ok ? tr_n : 0, kb = ok ? tk_n : 0;
+            tr_n += dr_n;
+            tk_n += dk_n;
+            if (tk_n >= nseg_n) { tk_n -= nseg_n; ++tr_n; }
             float v[32];
             split_gather32<T>(reinterpret_cast<const uint8_t *>(tile + r * rw), tab_n + split_pad_tab(kb * 128 + 32 * t), v);
             const NvSeg sg = quant_nvfp4_seg<false>(v, 0, PhiloxKeys{}, 0u);
             store_nv_seg(onv, r0 + r, kb, t, sg, ok && r0 + r < rows_p);
         }
         const int nt_o = tr * nseg_o;
+        int tr_o = nseg_o > 0 ? (warp * 8 + qd) / nseg_o : 0, tk_o = (warp * 8 + qd) - tr_o * nseg_o;
         for (int b = warp * 8; b < nt_o; b += nwarp * 8) {
             const int task = b + qd;
             const bool ok = task < nt_o;
-            const int r = ok ? task / nseg_o : 0, kb = ok ? task - r * nseg_o : 0;
+            const int r = ok ? tr_o : 0, kb = ok ? tk_o : 0;
+            tr_o += dr_o;
+            tk_o += dk_o;
+            if (tk_o >= nseg_o) { tk_o -= nseg_o; ++tr_o; }
             float v[32];
             split_gather32<T>(reinterpret_cast<const uint8_t *>(tile + r * rw), tab_o + split_pad_tab(kb * 128 + 32 * t), v);
             const MxSeg m = quant_mx_group(v, omx.fmt);
