@@ -80,7 +80,18 @@ __global__ void __launch_bounds__(256, ADAMW ? 4 : 5) k_osci_reset(float *w, flo
     const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const bool vec = (cols & 3) == 0;
+    // (row, block) of the warp's block, stepped by nwarps blocks with a carry: a 64-bit
+    // division per block cost more issue slots than the block's arithmetic.  32-bit counters:
+    // the C ABI rejects tensors of 2^31 or more 128-element blocks
+    static_assert(kBlocksPerWarp == 1, "one block per warp iteration");
+    const uint32_t nbr = nblk_row > 0 ? (uint32_t)nblk_row : 1u;
+    uint32_t row_i = (uint32_t)warp0 / nbr, kb_i = (uint32_t)warp0 - row_i * nbr;
+    const uint32_t d_row = (uint32_t)nwarps / nbr, d_kb = (uint32_t)nwarps - d_row * nbr;
     for (int64_t base = warp0 * kBlocksPerWarp; base < total; base += nwarps * kBlocksPerWarp) {
+        const int64_t row_w = row_i, kb_w = kb_i;
+        row_i += d_row;
+        kb_i += d_kb;
+        if (kb_i >= nbr) { kb_i -= nbr; ++row_i; }
         float x[kBlocksPerWarp][4], xp[kBlocksPerWarp][4], dq[kBlocksPerWarp][4], dm[kBlocksPerWarp][4];
         float gr[kBlocksPerWarp][4], am[kBlocksPerWarp][4], av[kBlocksPerWarp][4];   // AdamW: g, m, v
         int n_live[kBlocksPerWarp];
@@ -90,7 +101,7 @@ __global__ void __launch_bounds__(256, ADAMW ? 4 : 5) k_osci_reset(float *w, flo
 #pragma unroll
         for (int b = 0; b < kBlocksPerWarp; ++b) {
             const int64_t blk = base + b;
-            const int64_t row = blk / nblk_row, kb = blk % nblk_row, c = kb * 128 + 4 * lane;
+            const int64_t row = row_w, kb = kb_w, c = kb * 128 + 4 * lane;
             int nl = 0;
             if (blk < total && row < rows) nl = (int)(cols - c <= 0 ? 0 : (cols - c >= 4 ? 4 : cols - c));
             n_live[b] = nl;
@@ -144,7 +155,7 @@ __global__ void __launch_bounds__(256, ADAMW ? 4 : 5) k_osci_reset(float *w, flo
             const int64_t blk = base + b;
             const bool valid = blk < total;                  // warp-uniform
             if (!valid) break;
-            const int64_t row = blk / nblk_row, kb = blk % nblk_row;
+            const int64_t row = row_w, kb = kb_w;
             const int64_t c = kb * 128 + 4 * lane;
             if (ADAMW) {
                 // the optimizer step first; padding elements stay 0
