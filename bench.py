@@ -201,12 +201,13 @@ class Linear:
             "requant_w": 2 * kn * N * NV_B + 2 * k * N * MX_B, "requant_x": 2 * kn * M * NV_B + 2 * k * M * MX_B,
         }
         # lane instructions of each quantize call (per-element counts x elements, for the issue
-        # roofline); a re-alignment pair is the NVFP4 operand's and the slice's together
+        # roofline); a re-alignment pair launch counts the elements of the NVFP4 operand and of
+        # its slice together (its count is measured at the same 10% slice share)
         li = LANE_INSTR_PER_ELEM
         self.lane_instr = {"quant_x": li["split"] * M * K, "quant_dy_row": li["rows"] * M * N,
                            "quant_dy_col": li["cols"] * M * N,
-                           "requant_w": li["realign_nv"] * kn * N + li["realign_mx"] * k * N,
-                           "requant_x": li["realign_nv"] * kn * M + li["realign_mx"] * k * M}
+                           "requant_w": li["realign_pair"] * (kn + k) * N,
+                           "requant_x": li["realign_pair"] * (kn + k) * M}
 
     def run(self, tj, seed, tl, stream):
         T = lambda name, fn: tl.time(self.name + "." + name, fn)
@@ -276,10 +277,12 @@ TRAFFIC_BYTES_PER_LAUNCH = {"k_gemm_nvfp4": 108.7e6}
 # Lane instructions per element of the issue-bound quantize kernels (smsp__thread_inst_executed
 # of one ncu capture of the current kernel versions, `bench.py --only quant`, divided by the
 # elements each launch processes: dY elements for the row / column passes, input elements of
-# X for the split, elements of the re-aligned tensor for the re-alignments).  With them each
+# X for the split, elements of the re-aligned tensors for the re-alignments: the NVFP4 operand
+# alone, its slice alone, and both for the pair launch, at 921 + 103 channels).  With them each
 # kernel entry reports an issue roofline: lane instructions / (SMs x 128 lanes x SM clock x
 # time), the fraction of the SMs' instruction issue the kernel uses.
-LANE_INSTR_PER_ELEM = {"rows": 40.89, "cols": 45.81, "split": 28.21, "realign_nv": 47.59, "realign_mx": 27.54}
+LANE_INSTR_PER_ELEM = {"rows": 40.89, "cols": 46.29, "split": 23.16, "realign_nv": 48.11, "realign_mx": 28.12,
+                      "realign_pair": 47.15}
 NV_B = 0.5 + 1.0 / 16 + 4.0 / 128      # bytes per NVFP4 element (codes + E4M3 + FP32 scales)
 MX_B = 1.0 + 1.0 / 32                   # bytes per MXFP8 element (E4M3 + UE8M0)
 
@@ -635,7 +638,8 @@ def profiling_case(which):
     gemm : the gate/up forward GEMM, 16384 x 8192, K = 921 FP4 + 103 FP8 slice, bf16 out.
     quant: at the dY shape 16384 x 4096: the row and column passes (NVFP4 SR + RHT and
            MXFP8); at 16384 x 1024: the OutControl split of X (103 outlier channels), the
-           re-alignment of X-hat^T (921 channels, SR + RHT) and of its FP8 slice."""
+           re-alignment of X-hat^T (921 channels, SR + RHT) and of its FP8 slice, as two
+           launches and as one pair launch."""
     import __graft_entry__
 
     __graft_entry__.build()
@@ -671,6 +675,7 @@ def profiling_case(which):
             lambda: tj.quantize_split(X, ni, oi, out=xq, out8=x8),
             lambda: tj.requantize_nvfp4(xq, tj.TJ_SR, True, 3, tj.TAG_XT, tj.TAG_RHT_DW, out=s_x),
             lambda: tj.requantize_mxfp8(x8, out=q8x),
+            lambda: tj.requantize_nvfp4_mxfp8(xq, x8, tj.TJ_SR, True, 3, tj.TAG_XT, tj.TAG_RHT_DW, out=s_x, out8=q8x),
         ]
     torch.cuda.synchronize()
     for f in calls:
