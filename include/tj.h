@@ -21,6 +21,11 @@
  *     TJ_ERR_CUDA.  Device-side bounded waits that run out set a sticky device
  *     flag read by tj_get_device_status().
  *   - Inputs must be finite.  Padded regions of outputs are written (zeros).
+ *   - Empty tensors: a tensor with no rows or no columns has no storage, and its
+ *     pointers may be NULL.  A call whose outputs are all empty only checks its
+ *     arguments.  A product over an empty contraction (K = 0 for a GEMM, no output
+ *     features for dX, no tokens for dW) is zero and is written as zeros.  With every
+ *     channel an outlier (k = K) normal_idx may be NULL and the NVFP4 parts are empty.
  *
  * Data layouts in HBM
  *   NVFP4 double-block tensor (tj_nvfp4), logical [rows, cols] quantized along
@@ -133,6 +138,8 @@ typedef struct {
  *                 input rows.
  *   sel, n_sel optional (sel may be NULL -> all columns, n_sel ignored): ascending
  *              int32 input-column indices to keep (OutControl's normal channels).
+ *              A non-NULL sel with n_sel = 0 keeps no column (the output is empty and
+ *              sel is not read).
  *              along_cols=0: they form the compacted contraction (out->cols = n_sel);
  *              along_cols=1: they are the output rows (out->rows = n_sel).
  *   mode       TJ_RTN or TJ_SR.  SR draws 16 bits per element from Philox4x32-10

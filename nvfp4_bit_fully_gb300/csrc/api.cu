@@ -39,9 +39,13 @@ bool blocks_fit(int64_t rows, int64_t cols) {
 // a grid has at most 65535 rows: at most 8,388,480 output columns (input rows).
 bool cols_grid_fits(int64_t out_cols) { return round_up(out_cols, 128) / 128 <= 65535; }
 
+// An empty tensor (no rows or no columns) has no storage: its pointers may be null.
 tj_status check_nv(const tj_nvfp4 *q, int64_t rows, int64_t cols) {
-    if (q == nullptr || q->codes == nullptr || q->sf == nullptr || q->outer == nullptr) return TJ_ERR_INVALID_ARG;
+    if (q == nullptr) return TJ_ERR_INVALID_ARG;
+    const bool empty = q->rows == 0 || q->cols == 0;
+    if (!empty && (q->codes == nullptr || q->sf == nullptr || q->outer == nullptr)) return TJ_ERR_INVALID_ARG;
     if (q->rows != rows || q->cols != cols || rows < 0 || cols < 0) return TJ_ERR_SHAPE;
+    if (empty) return TJ_OK;
     if (!blocks_fit(rows, cols)) return TJ_ERR_SHAPE;
     if (!al16(q->codes) || !al16(q->sf) || !al16(q->outer)) return TJ_ERR_ALIGN;
     return TJ_OK;
@@ -50,9 +54,12 @@ tj_status check_nv(const tj_nvfp4 *q, int64_t rows, int64_t cols) {
 // An MX slice: a known element format; packed FP6 / FP4 codes start on 32 bytes (the
 // tensor maps of the packed sub-byte types require it).
 tj_status check_mx(const tj_mxfp8 *q, int64_t rows, int64_t cols) {
-    if (q == nullptr || q->codes == nullptr || q->sf == nullptr) return TJ_ERR_INVALID_ARG;
+    if (q == nullptr) return TJ_ERR_INVALID_ARG;
+    const bool empty = q->rows == 0 || q->cols == 0;
+    if (!empty && (q->codes == nullptr || q->sf == nullptr)) return TJ_ERR_INVALID_ARG;
     if (!mx_fmt_valid(q->fmt)) return TJ_ERR_INVALID_ARG;
     if (q->rows != rows || q->cols != cols || rows < 0 || cols < 0) return TJ_ERR_SHAPE;
+    if (empty) return TJ_OK;
     if (!blocks_fit(rows, cols)) return TJ_ERR_SHAPE;
     if (!al16(q->codes) || !al16(q->sf)) return TJ_ERR_ALIGN;
     if (q->fmt != kMxE4M3 && (reinterpret_cast<uintptr_t>(q->codes) & 31) != 0) return TJ_ERR_ALIGN;
@@ -100,8 +107,9 @@ tj_mxfp8 carve_mx(uint8_t *&cur, int64_t rows, int64_t cols, int fmt = kMxE4M3) 
     return q;
 }
 
-bool dense_ok(const void *x, int dtype, int64_t ld, int64_t cols) {
-    return x != nullptr && (dtype == TJ_BF16 || dtype == TJ_FP32) && ld >= cols;
+// A dense input: x may be null only when it has no elements.
+bool dense_ok(const void *x, int dtype, int64_t ld, int64_t rows, int64_t cols) {
+    return (x != nullptr || rows == 0 || cols == 0) && (dtype == TJ_BF16 || dtype == TJ_FP32) && ld >= cols;
 }
 
 }  // namespace
@@ -132,7 +140,7 @@ tj_status tj_quantize_nvfp4(const void *x, int dtype, int64_t rows_x, int64_t co
                             const int32_t *sel, int64_t n_sel, int mode, int rht, uint64_t seed, uint32_t tag,
                             uint32_t rht_tag, tj_nvfp4 *out, void *stream) {
     if (rows_x < 0 || cols_x < 0 || (mode != TJ_RTN && mode != TJ_SR) || out == nullptr) return TJ_ERR_INVALID_ARG;
-    if (!dense_ok(x, dtype, ld, cols_x)) return TJ_ERR_INVALID_ARG;
+    if (!dense_ok(x, dtype, ld, rows_x, cols_x)) return TJ_ERR_INVALID_ARG;
     if (!al_elem(x, dtype)) return TJ_ERR_ALIGN;
     const int64_t ncols = sel ? n_sel : cols_x;
     if (sel && (n_sel < 0 || n_sel > cols_x)) return TJ_ERR_SHAPE;
@@ -140,6 +148,7 @@ tj_status tj_quantize_nvfp4(const void *x, int dtype, int64_t rows_x, int64_t co
     if (along_cols && !cols_grid_fits(ocols)) return TJ_ERR_SHAPE;
     const tj_status st = check_nv(out, orows, ocols);
     if (st != TJ_OK) return st;
+    if (orows == 0 || ocols == 0) return TJ_OK;
     return cuda_status(launch_quant_nv_dense(x, dtype, rows_x, ncols, ld, along_cols, sel, mode, rht, seed, tag,
                                              rht_tag, *out, static_cast<cudaStream_t>(stream)));
 }
@@ -147,7 +156,7 @@ tj_status tj_quantize_nvfp4(const void *x, int dtype, int64_t rows_x, int64_t co
 tj_status tj_quantize_mxfp8(const void *x, int dtype, int64_t rows_x, int64_t cols_x, int64_t ld, int along_cols,
                             const int32_t *sel, int64_t n_sel, tj_mxfp8 *out, void *stream) {
     if (rows_x < 0 || cols_x < 0 || out == nullptr) return TJ_ERR_INVALID_ARG;
-    if (!dense_ok(x, dtype, ld, cols_x)) return TJ_ERR_INVALID_ARG;
+    if (!dense_ok(x, dtype, ld, rows_x, cols_x)) return TJ_ERR_INVALID_ARG;
     if (!al_elem(x, dtype)) return TJ_ERR_ALIGN;
     const int64_t ncols = sel ? n_sel : cols_x;
     if (sel && (n_sel < 0 || n_sel > cols_x)) return TJ_ERR_SHAPE;
@@ -155,6 +164,7 @@ tj_status tj_quantize_mxfp8(const void *x, int dtype, int64_t rows_x, int64_t co
     if (along_cols && !cols_grid_fits(ocols)) return TJ_ERR_SHAPE;
     const tj_status st = check_mx(out, orows, ocols);
     if (st != TJ_OK) return st;
+    if (orows == 0 || ocols == 0) return TJ_OK;
     return cuda_status(launch_quant_mx_dense(x, dtype, rows_x, ncols, ld, along_cols, sel, *out,
                                              static_cast<cudaStream_t>(stream)));
 }
@@ -165,7 +175,7 @@ tj_status tj_quantize_nvfp4_mxfp8(const void *x, int dtype, int64_t rows_x, int6
                                   void *stream) {
     if (rows_x < 0 || cols_x < 0 || (mode != TJ_RTN && mode != TJ_SR) || out == nullptr || out8 == nullptr)
         return TJ_ERR_INVALID_ARG;
-    if (!dense_ok(x, dtype, ld, cols_x)) return TJ_ERR_INVALID_ARG;
+    if (!dense_ok(x, dtype, ld, rows_x, cols_x)) return TJ_ERR_INVALID_ARG;
     if (!al_elem(x, dtype)) return TJ_ERR_ALIGN;
     const int64_t ncols = sel ? n_sel : cols_x;
     if (sel && (n_sel < 0 || n_sel > cols_x)) return TJ_ERR_SHAPE;
@@ -174,6 +184,7 @@ tj_status tj_quantize_nvfp4_mxfp8(const void *x, int dtype, int64_t rows_x, int6
     tj_status st = check_nv(out, orows, ocols);
     if (st == TJ_OK) st = check_mx(out8, orows, ocols);
     if (st != TJ_OK) return st;
+    if (orows == 0 || ocols == 0) return TJ_OK;
     return cuda_status(launch_quant_dual_dense(x, dtype, rows_x, ncols, ld, along_cols, sel, mode, rht, seed, tag,
                                                rht_tag, *out, *out8, static_cast<cudaStream_t>(stream)));
 }
@@ -185,11 +196,12 @@ tj_status tj_quantize_split(const void *x, int dtype, int64_t rows, int64_t cols
     if (n_normal + n_outlier != cols) return TJ_ERR_SHAPE;
     if ((n_normal > 0 && normal_idx == nullptr) || (n_outlier > 0 && (outlier_idx == nullptr || out8 == nullptr)))
         return TJ_ERR_INVALID_ARG;
-    if (!dense_ok(x, dtype, ld, cols)) return TJ_ERR_INVALID_ARG;
+    if (!dense_ok(x, dtype, ld, rows, cols)) return TJ_ERR_INVALID_ARG;
     if (!al_elem(x, dtype)) return TJ_ERR_ALIGN;
     tj_status st = check_nv(out, rows, n_normal);
     if (st == TJ_OK && n_outlier > 0) st = check_mx(out8, rows, n_outlier);
     if (st != TJ_OK) return st;
+    if (rows == 0 || cols == 0) return TJ_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const tj_mxfp8 none{};
     const cudaError_t e = launch_quant_split(x, dtype, rows, cols, ld, normal_idx, n_normal, outlier_idx, n_outlier,
@@ -208,6 +220,7 @@ tj_status tj_requantize_nvfp4(const tj_nvfp4 *in, int mode, int rht, uint64_t se
     if (st == TJ_OK) st = check_nv(out, in->cols, in->rows);
     if (st != TJ_OK) return st;
     if (!cols_grid_fits(in->rows)) return TJ_ERR_SHAPE;
+    if (in->rows == 0 || in->cols == 0) return TJ_OK;
     return cuda_status(launch_realign_nv(*in, *out, mode, rht, seed, tag, rht_tag, static_cast<cudaStream_t>(stream)));
 }
 
@@ -217,6 +230,7 @@ tj_status tj_requantize_mxfp8(const tj_mxfp8 *in, tj_mxfp8 *out, void *stream) {
     if (st == TJ_OK) st = check_mx(out, in->cols, in->rows);
     if (st != TJ_OK) return st;
     if (!cols_grid_fits(in->rows)) return TJ_ERR_SHAPE;
+    if (in->rows == 0 || in->cols == 0) return TJ_OK;
     return cuda_status(launch_realign_mx(*in, *out, static_cast<cudaStream_t>(stream)));
 }
 
@@ -231,17 +245,13 @@ tj_status tj_requantize_nvfp4_mxfp8(const tj_nvfp4 *in, int mode, int rht, uint6
     if (st == TJ_OK) st = check_mx(out8, in8->cols, in8->rows);
     if (st != TJ_OK) return st;
     if (!cols_grid_fits(in->rows) || !cols_grid_fits(in8->rows)) return TJ_ERR_SHAPE;
-    if (in->cols == 0 || in8->cols == 0) {           // an empty part: the other part alone
-        if (in->cols > 0) TJ_TRY(launch_realign_nv(*in, *out, mode, rht, seed, tag, rht_tag, static_cast<cudaStream_t>(stream)));
-        if (in8->cols > 0) TJ_TRY(launch_realign_mx(*in8, *out8, static_cast<cudaStream_t>(stream)));
-        return TJ_OK;
-    }
+    // (an empty part leaves the other part alone in the launch)
     return cuda_status(launch_realign_pair(*in, *out, mode, rht, seed, tag, rht_tag, *in8, *out8,
                                            static_cast<cudaStream_t>(stream)));
 }
 
 tj_status tj_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, void *stream) {
-    if (x == nullptr || y == nullptr || rows < 0 || cols < 0) return TJ_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || ((x == nullptr || y == nullptr) && rows > 0 && cols > 0)) return TJ_ERR_INVALID_ARG;
     if (cols % 128 != 0) return TJ_ERR_SHAPE;
     if (!al16(x) || !al16(y)) return TJ_ERR_ALIGN;
     if (rows == 0 || cols == 0) return TJ_OK;
@@ -249,7 +259,7 @@ tj_status tj_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t 
 }
 
 tj_status tj_dequantize_nvfp4(const tj_nvfp4 *q, float *y, int64_t ldy, void *stream) {
-    if (q == nullptr || y == nullptr) return TJ_ERR_INVALID_ARG;
+    if (q == nullptr || (y == nullptr && q->rows > 0 && q->cols > 0)) return TJ_ERR_INVALID_ARG;
     const tj_status st = check_nv(q, q->rows, q->cols);
     if (st != TJ_OK) return st;
     if (ldy < q->cols) return TJ_ERR_SHAPE;
@@ -257,7 +267,7 @@ tj_status tj_dequantize_nvfp4(const tj_nvfp4 *q, float *y, int64_t ldy, void *st
 }
 
 tj_status tj_dequantize_mxfp8(const tj_mxfp8 *q, float *y, int64_t ldy, void *stream) {
-    if (q == nullptr || y == nullptr) return TJ_ERR_INVALID_ARG;
+    if (q == nullptr || (y == nullptr && q->rows > 0 && q->cols > 0)) return TJ_ERR_INVALID_ARG;
     const tj_status st = check_mx(q, q->rows, q->cols);
     if (st != TJ_OK) return st;
     if (ldy < q->cols) return TJ_ERR_SHAPE;
@@ -266,7 +276,7 @@ tj_status tj_dequantize_mxfp8(const tj_mxfp8 *q, float *y, int64_t ldy, void *st
 
 tj_status tj_gemm_nvfp4(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8, const tj_mxfp8 *b8, float alpha,
                         void *d, int out_dtype, int64_t ldd, const int32_t *col_map, void *stream) {
-    if (a == nullptr || b == nullptr || d == nullptr) return TJ_ERR_INVALID_ARG;
+    if (a == nullptr || b == nullptr || (d == nullptr && a->rows > 0 && b->rows > 0)) return TJ_ERR_INVALID_ARG;
     if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
     tj_status st = check_nv(a, a->rows, a->cols);
     if (st == TJ_OK) st = check_nv(b, b->rows, a->cols);
@@ -284,7 +294,7 @@ tj_status tj_gemm_nvfp4(const tj_nvfp4 *a, const tj_nvfp4 *b, const tj_mxfp8 *a8
 
 tj_status tj_gemm_mxfp8(const tj_mxfp8 *a8, const tj_mxfp8 *b8, void *d, int out_dtype, int64_t ldd,
                         const int32_t *col_map, void *stream) {
-    if (a8 == nullptr || b8 == nullptr || d == nullptr) return TJ_ERR_INVALID_ARG;
+    if (a8 == nullptr || b8 == nullptr || (d == nullptr && a8->rows > 0 && b8->rows > 0)) return TJ_ERR_INVALID_ARG;
     if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
     tj_status st = check_mx(a8, a8->rows, a8->cols);
     if (st == TJ_OK) st = check_mx(b8, b8->rows, a8->cols);
@@ -297,7 +307,8 @@ tj_status tj_gemm_mxfp8(const tj_mxfp8 *a8, const tj_mxfp8 *b8, void *d, int out
 tj_status tj_gemm_pair(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, void *d, int out_dtype, int64_t ldd,
                        const int32_t *col_map, const tj_mxfp8 *a8, const tj_mxfp8 *b8, void *d8, int out8_dtype,
                        int64_t ldd8, const int32_t *col_map8, void *stream) {
-    if (a == nullptr || b == nullptr || d == nullptr || a8 == nullptr || b8 == nullptr || d8 == nullptr)
+    if (a == nullptr || b == nullptr || a8 == nullptr || b8 == nullptr) return TJ_ERR_INVALID_ARG;
+    if ((d == nullptr && a->rows > 0 && b->rows > 0) || (d8 == nullptr && a8->rows > 0 && b8->rows > 0))
         return TJ_ERR_INVALID_ARG;
     if ((out_dtype != TJ_BF16 && out_dtype != TJ_FP32) || (out8_dtype != TJ_BF16 && out8_dtype != TJ_FP32))
         return TJ_ERR_INVALID_ARG;
@@ -316,15 +327,16 @@ tj_status tj_gemm_pair(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, void *
 tj_status tj_gemm_pair_f32(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, const int32_t *col_map,
                            const tj_mxfp8 *a8, const tj_mxfp8 *b8, const int32_t *col_map8, float *out,
                            int64_t cols, int64_t ld, void *stream) {
-    if (a == nullptr || b == nullptr || a8 == nullptr || b8 == nullptr || out == nullptr || col_map == nullptr ||
-        col_map8 == nullptr)
+    if (a == nullptr || b == nullptr || a8 == nullptr || b8 == nullptr) return TJ_ERR_INVALID_ARG;
+    if ((col_map == nullptr && b->rows > 0) || (col_map8 == nullptr && b8->rows > 0) ||
+        (out == nullptr && a->rows > 0 && cols > 0))
         return TJ_ERR_INVALID_ARG;
     tj_status st = check_nv(a, a->rows, a->cols);
     if (st == TJ_OK) st = check_nv(b, b->rows, a->cols);
     if (st == TJ_OK) st = check_mx(a8, a8->rows, a8->cols);
     if (st == TJ_OK) st = check_mx(b8, b8->rows, a8->cols);
     if (st != TJ_OK) return st;
-    if (a8->rows != a->rows || cols < 1 || ld < cols || b->rows + b8->rows > cols) return TJ_ERR_SHAPE;
+    if (a8->rows != a->rows || cols < 0 || ld < cols || b->rows + b8->rows > cols) return TJ_ERR_SHAPE;
     if (!al16(out)) return TJ_ERR_ALIGN;
     const SplitRegion whole{out, a->rows, cols, ld};
     return cuda_status(launch_gemm_pair(a, b, alpha, out, TJ_FP32, ld, a->rows, b->rows, col_map, a8, b8, out, TJ_FP32,
@@ -352,10 +364,11 @@ size_t tj_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t k) {
 tj_status tj_linear_fwd(const void *x, int64_t M, int64_t K, int64_t ldx, const tj_nvfp4 *wq, const tj_mxfp8 *w8,
                         const int32_t *normal_idx, const int32_t *outlier_idx, int64_t k, tj_nvfp4 *xq,
                         tj_mxfp8 *x8, void *y, int out_dtype, int64_t ldy, void *stream) {
-    if (x == nullptr || wq == nullptr || xq == nullptr || y == nullptr || M < 0 || K < 0 || k < 0 || k > K)
-        return TJ_ERR_INVALID_ARG;
+    if (wq == nullptr || xq == nullptr || M < 0 || K < 0 || k < 0 || k > K) return TJ_ERR_INVALID_ARG;
+    if ((x == nullptr && M > 0 && K > 0) || (y == nullptr && M > 0 && wq->rows > 0)) return TJ_ERR_INVALID_ARG;
     if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
-    if (k > 0 && (normal_idx == nullptr || outlier_idx == nullptr || w8 == nullptr || x8 == nullptr))
+    // (every channel an outlier: there is no normal channel to list)
+    if (k > 0 && ((k < K && normal_idx == nullptr) || outlier_idx == nullptr || w8 == nullptr || x8 == nullptr))
         return TJ_ERR_INVALID_ARG;
     if (!al_elem(x, TJ_BF16) || !al16(y)) return TJ_ERR_ALIGN;
     if (ldx < K) return TJ_ERR_SHAPE;
@@ -366,6 +379,7 @@ tj_status tj_linear_fwd(const void *x, int64_t M, int64_t K, int64_t ldx, const 
     if (st == TJ_OK && k > 0) st = check_mx(x8, M, k);
     if (st != TJ_OK) return st;
     if (ldy < N) return TJ_ERR_SHAPE;
+    if (M == 0) return TJ_OK;                          // no tokens: nothing to quantize or write
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (k > 0) {
         // the OutControl split of X from one read (two gathering passes if a row is too long)
@@ -387,18 +401,21 @@ tj_status tj_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, c
                            const tj_mxfp8 *w8, const int32_t *normal_idx, const int32_t *outlier_idx, int64_t k,
                            uint64_t seed, void *dx, int out_dtype, int64_t lddx, void *workspace, size_t ws_bytes,
                            void *stream) {
-    if (dy == nullptr || wq == nullptr || dx == nullptr || M < 0 || N < 0 || k < 0) return TJ_ERR_INVALID_ARG;
-    if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
-    if (k > 0 && (normal_idx == nullptr || outlier_idx == nullptr || w8 == nullptr)) return TJ_ERR_INVALID_ARG;
-    if (!al_elem(dy, TJ_BF16) || !al16(dx)) return TJ_ERR_ALIGN;
+    if (wq == nullptr || M < 0 || N < 0 || k < 0) return TJ_ERR_INVALID_ARG;
     const int64_t kn = wq->cols, K = kn + k;
+    if ((dy == nullptr && M > 0 && N > 0) || (dx == nullptr && M > 0 && K > 0)) return TJ_ERR_INVALID_ARG;
+    if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
+    if (k > 0 && ((kn > 0 && normal_idx == nullptr) || outlier_idx == nullptr || w8 == nullptr))
+        return TJ_ERR_INVALID_ARG;
+    if (!al_elem(dy, TJ_BF16) || !al16(dx)) return TJ_ERR_ALIGN;
     tj_status st = check_nv(wq, N, kn);
     if (st == TJ_OK && k > 0) st = check_mx(w8, N, k);
     if (st != TJ_OK) return st;
     if (lddy < N || lddx < K || !cols_grid_fits(N)) return TJ_ERR_SHAPE;
     const size_t need = tj_workspace_size(TJ_OP_BWD_DX, M, N, K, k);
-    if (workspace == nullptr || ws_bytes < need) return TJ_ERR_WORKSPACE;
+    if ((workspace == nullptr && need > 0) || ws_bytes < need) return TJ_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return TJ_ERR_ALIGN;
+    if (M == 0 || K == 0) return TJ_OK;                // dX is empty (N = 0: dX = 0, an empty contraction)
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *cur = static_cast<uint8_t *>(workspace);
     tj_nvfp4 s_dy = carve_nv(cur, M, N);
@@ -437,17 +454,20 @@ tj_status tj_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, c
 tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, const tj_nvfp4 *xq,
                            const tj_mxfp8 *x8, const int32_t *normal_idx, const int32_t *outlier_idx, int64_t k,
                            uint64_t seed, float *dw, int64_t lddw, void *workspace, size_t ws_bytes, void *stream) {
-    if (dy == nullptr || xq == nullptr || dw == nullptr || M < 0 || N < 0 || k < 0) return TJ_ERR_INVALID_ARG;
-    if (k > 0 && (normal_idx == nullptr || outlier_idx == nullptr || x8 == nullptr)) return TJ_ERR_INVALID_ARG;
-    if (!al_elem(dy, TJ_BF16) || !al16(dw)) return TJ_ERR_ALIGN;
+    if (xq == nullptr || M < 0 || N < 0 || k < 0) return TJ_ERR_INVALID_ARG;
     const int64_t kn = xq->cols, K = kn + k;
+    if ((dy == nullptr && M > 0 && N > 0) || (dw == nullptr && N > 0 && K > 0)) return TJ_ERR_INVALID_ARG;
+    if (k > 0 && ((kn > 0 && normal_idx == nullptr) || outlier_idx == nullptr || x8 == nullptr))
+        return TJ_ERR_INVALID_ARG;
+    if (!al_elem(dy, TJ_BF16) || !al16(dw)) return TJ_ERR_ALIGN;
     tj_status st = check_nv(xq, M, kn);
     if (st == TJ_OK && k > 0) st = check_mx(x8, M, k);
     if (st != TJ_OK) return st;
     if (lddy < N || lddw < K || !cols_grid_fits(M)) return TJ_ERR_SHAPE;
     const size_t need = tj_workspace_size(TJ_OP_BWD_DW, M, N, K, k);
-    if (workspace == nullptr || ws_bytes < need) return TJ_ERR_WORKSPACE;
+    if ((workspace == nullptr && need > 0) || ws_bytes < need) return TJ_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return TJ_ERR_ALIGN;
+    if (N == 0 || K == 0) return TJ_OK;                // dW is empty (M = 0: dW = 0, an empty contraction)
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *cur = static_cast<uint8_t *>(workspace);
     tj_nvfp4 s_dy = carve_nv(cur, N, M);
@@ -494,16 +514,18 @@ tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, c
 // ---------------------------------------------------------------------------
 tj_status tj_fp8_linear_fwd(const void *x, int64_t M, int64_t K, int64_t ldx, const tj_mxfp8 *w8, tj_mxfp8 *x8,
                             tj_mxfp8 *xt8, void *y, int out_dtype, int64_t ldy, void *stream) {
-    if (x == nullptr || w8 == nullptr || x8 == nullptr || y == nullptr || M < 0 || K < 0) return TJ_ERR_INVALID_ARG;
+    if (w8 == nullptr || x8 == nullptr || M < 0 || K < 0) return TJ_ERR_INVALID_ARG;
+    const int64_t N = w8->rows;
+    if ((x == nullptr && M > 0 && K > 0) || (y == nullptr && M > 0 && N > 0)) return TJ_ERR_INVALID_ARG;
     if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
     if (!al_elem(x, TJ_BF16) || !al16(y)) return TJ_ERR_ALIGN;
-    const int64_t N = w8->rows;
     if (ldx < K || ldy < N) return TJ_ERR_SHAPE;
     tj_status st = check_mx(w8, N, K);
     if (st == TJ_OK) st = check_mx(x8, M, K);
     if (st == TJ_OK && xt8 != nullptr) st = check_mx(xt8, K, M);
     if (st != TJ_OK) return st;
     if (xt8 != nullptr && !cols_grid_fits(M)) return TJ_ERR_SHAPE;
+    if (M == 0) return TJ_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     TJ_TRY(launch_quant_mx_dense(x, TJ_BF16, M, K, ldx, 0, nullptr, *x8, s));
     if (xt8 != nullptr) TJ_TRY(launch_quant_mx_dense(x, TJ_BF16, M, K, ldx, 1, nullptr, *xt8, s));
@@ -513,16 +535,18 @@ tj_status tj_fp8_linear_fwd(const void *x, int64_t M, int64_t K, int64_t ldx, co
 
 tj_status tj_fp8_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t lddy, const tj_mxfp8 *wt8, void *dx,
                                int out_dtype, int64_t lddx, void *workspace, size_t ws_bytes, void *stream) {
-    if (dy == nullptr || wt8 == nullptr || dx == nullptr || M < 0 || N < 0) return TJ_ERR_INVALID_ARG;
+    if (wt8 == nullptr || M < 0 || N < 0) return TJ_ERR_INVALID_ARG;
+    const int64_t K = wt8->rows;
+    if ((dy == nullptr && M > 0 && N > 0) || (dx == nullptr && M > 0 && K > 0)) return TJ_ERR_INVALID_ARG;
     if (out_dtype != TJ_BF16 && out_dtype != TJ_FP32) return TJ_ERR_INVALID_ARG;
     if (!al_elem(dy, TJ_BF16) || !al16(dx)) return TJ_ERR_ALIGN;
-    const int64_t K = wt8->rows;
     tj_status st = check_mx(wt8, K, N);
     if (st != TJ_OK) return st;
     if (lddy < N || lddx < K) return TJ_ERR_SHAPE;
     const size_t need = tj_workspace_size(TJ_OP_FP8_BWD_DX, M, N, K, 0);
-    if (workspace == nullptr || ws_bytes < need) return TJ_ERR_WORKSPACE;
+    if ((workspace == nullptr && need > 0) || ws_bytes < need) return TJ_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return TJ_ERR_ALIGN;
+    if (M == 0 || K == 0) return TJ_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *cur = static_cast<uint8_t *>(workspace);
     tj_mxfp8 q8_dy = carve_mx(cur, M, N);
@@ -533,15 +557,17 @@ tj_status tj_fp8_linear_bwd_dx(const void *dy, int64_t M, int64_t N, int64_t ldd
 
 tj_status tj_fp8_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, const tj_mxfp8 *xt8, float *dw,
                                int64_t lddw, void *workspace, size_t ws_bytes, void *stream) {
-    if (dy == nullptr || xt8 == nullptr || dw == nullptr || M < 0 || N < 0) return TJ_ERR_INVALID_ARG;
-    if (!al_elem(dy, TJ_BF16) || !al16(dw)) return TJ_ERR_ALIGN;
+    if (xt8 == nullptr || M < 0 || N < 0) return TJ_ERR_INVALID_ARG;
     const int64_t K = xt8->rows;
+    if ((dy == nullptr && M > 0 && N > 0) || (dw == nullptr && N > 0 && K > 0)) return TJ_ERR_INVALID_ARG;
+    if (!al_elem(dy, TJ_BF16) || !al16(dw)) return TJ_ERR_ALIGN;
     tj_status st = check_mx(xt8, K, M);
     if (st != TJ_OK) return st;
     if (lddy < N || lddw < K || !cols_grid_fits(M)) return TJ_ERR_SHAPE;
     const size_t need = tj_workspace_size(TJ_OP_FP8_BWD_DW, M, N, K, 0);
-    if (workspace == nullptr || ws_bytes < need) return TJ_ERR_WORKSPACE;
+    if ((workspace == nullptr && need > 0) || ws_bytes < need) return TJ_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return TJ_ERR_ALIGN;
+    if (N == 0 || K == 0) return TJ_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *cur = static_cast<uint8_t *>(workspace);
     tj_mxfp8 q8_dyt = carve_mx(cur, N, M);
@@ -573,8 +599,9 @@ tj_status tj_outlier_calibrate(const void *x, int dtype, int64_t M, int64_t K, i
 tj_status tj_osci_reset(float *w, float *w_prev, float *dist_q, float *dist_m, const tj_nvfp4 *q_prev,
                         tj_nvfp4 *q_out, uint32_t *reset_mask, int64_t rows, int64_t cols, float lr, float lr_thr,
                         float risk_thr, int track, void *stream) {
-    if (w == nullptr || w_prev == nullptr || dist_q == nullptr || dist_m == nullptr || reset_mask == nullptr ||
-        rows < 0 || cols < 0)
+    if (rows < 0 || cols < 0) return TJ_ERR_INVALID_ARG;
+    if ((w == nullptr || w_prev == nullptr || dist_q == nullptr || dist_m == nullptr || reset_mask == nullptr) &&
+        rows > 0 && cols > 0)
         return TJ_ERR_INVALID_ARG;
     tj_status st = check_nv(q_prev, rows, cols);
     if (st == TJ_OK) st = check_nv(q_out, rows, cols);
@@ -590,8 +617,10 @@ tj_status tj_adamw_osci_reset(float *w, const float *g, float *m, float *v, floa
                               int64_t rows, int64_t cols, float lr, float beta1, float beta2, float eps,
                               float weight_decay, int64_t step, float lr_thr, float risk_thr, int track,
                               void *stream) {
-    if (w == nullptr || g == nullptr || m == nullptr || v == nullptr || w_prev == nullptr || dist_q == nullptr ||
-        dist_m == nullptr || reset_mask == nullptr || rows < 0 || cols < 0 || step < 1)
+    if (rows < 0 || cols < 0 || step < 1) return TJ_ERR_INVALID_ARG;
+    if ((w == nullptr || g == nullptr || m == nullptr || v == nullptr || w_prev == nullptr || dist_q == nullptr ||
+         dist_m == nullptr || reset_mask == nullptr) &&
+        rows > 0 && cols > 0)
         return TJ_ERR_INVALID_ARG;
     tj_status st = check_nv(q_prev, rows, cols);
     if (st == TJ_OK) st = check_nv(q_out, rows, cols);

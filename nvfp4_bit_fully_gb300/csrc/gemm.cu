@@ -823,6 +823,7 @@ cudaError_t maybe_split(GemmArgs &g, const SplitRegion *split, cudaStream_t s) {
 bool set_fp4(const tj_nvfp4 &a, const tj_nvfp4 &b, GemmArgs &g, CUtensorMap (&tm)[5], int &nkb4) {
     const int64_t kp = round_up(a.cols, 128);
     nkb4 = (int)(kp / 128);
+    if (nkb4 == 0 || a.rows == 0 || b.rows == 0) { nkb4 = 0; return true; }   // no FP4 blocks: no loads
     g.sfa4 = a.sf;
     g.sfb4 = b.sf;
     g.ntk_a4 = kp / 64;
@@ -840,6 +841,7 @@ bool set_fp4(const tj_nvfp4 &a, const tj_nvfp4 &b, GemmArgs &g, CUtensorMap (&tm
 bool set_fp8(const tj_mxfp8 &a8, const tj_mxfp8 &b8, GemmArgs &g, CUtensorMap (&tm)[5], int &nk8) {
     const int64_t kp8 = round_up(a8.cols, 128);
     nk8 = (int)(kp8 / 128);
+    if (nk8 == 0 || a8.rows == 0 || b8.rows == 0) { nk8 = 0; return true; }   // no slice stages: no loads
     g.sfa8 = a8.sf;
     g.sfb8 = b8.sf;
     g.ntk_a8 = kp8 / 128;
@@ -888,7 +890,8 @@ cudaError_t launch_gemm_pair(const tj_nvfp4 *a, const tj_nvfp4 *b, float alpha, 
     memset(tm, 0, sizeof(tm));
     if (!set_fp4(*a, *b, g, tm, g.pr[0].nkb4) || !set_fp8(*a8, *b8, g, tm, g.pr[1].nk8)) return cudaErrorInvalidValue;
     if (g.pr[0].tiles_m * g.pr[0].tiles_n == 0) g.pr[0].tiles_m = g.pr[0].tiles_n = 0;
-    if (g.pr[1].tiles_m * g.pr[1].tiles_n == 0 || g.pr[1].nk8 == 0) g.pr[1].tiles_m = g.pr[1].tiles_n = 0;
+    // a product over an empty contraction is zero: its tiles run with no blocks and write zeros
+    if (g.pr[1].tiles_m * g.pr[1].tiles_n == 0) g.pr[1].tiles_m = g.pr[1].tiles_n = 0;
     const cudaError_t e = maybe_split(g, split, s);
     if (e != cudaSuccess) return e;
     return launch_persistent(tm, g, s);

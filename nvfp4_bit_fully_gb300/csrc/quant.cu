@@ -585,6 +585,7 @@ cudaError_t rows_nv(const Src &src, const OutNv &o, int mode, int rht, uint64_t 
 template <typename Src, int FMT = 0>
 cudaError_t cols_nv(const Src &src, const OutNv &o, int mode, int rht, uint64_t seed, uint32_t tag,
                     uint32_t rht_tag, cudaStream_t s, const OutMx none = OutMx{}) {
+    if (o.rows_p == 0 || o.cols_p == 0) return cudaSuccess;          // an empty output
     const dim3 grid((unsigned)(o.rows_p / 64), (unsigned)(o.cols_p / 128));
     const PhiloxKeys pk = philox_keys(seed);
     if (mode == TJ_SR && rht)  k_quant_cols<Src, FMT, true, true><<<grid, kThreads, 0, s>>>(src, o, none, pk, tag, rht_tag);
@@ -603,6 +604,7 @@ cudaError_t rows_mx(const Src &src, const OutMx &o, cudaStream_t s) {
 
 template <typename Src>
 cudaError_t cols_mx(const Src &src, const OutMx &o, cudaStream_t s) {
+    if (o.rows_p == 0 || o.cols_p == 0) return cudaSuccess;          // an empty output
     const dim3 grid((unsigned)(o.rows_p / 64), (unsigned)(o.cols_p / 128));
     k_quant_cols<Src, 1, false, false><<<grid, kThreads, 0, s>>>(src, OutNv{}, o, PhiloxKeys{}, 0, 0);
     return cudaGetLastError();
@@ -667,6 +669,7 @@ cudaError_t launch_quant_split(const void *x, int dtype, int64_t rows, int64_t K
                                int64_t kn, const int32_t *sel_o, int64_t k, const tj_nvfp4 &out,
                                const tj_mxfp8 &out8, cudaStream_t s) {
     if (K > (1 << 24)) return cudaErrorNotSupported;
+    if (rows == 0 || K == 0) return cudaSuccess;                      // empty outputs
     const int esz = dtype == TJ_BF16 ? 2 : 4;
     const OutNv o = out_nv(out);
     const OutMx m = k > 0 ? out_mx(out8) : OutMx{};
@@ -713,8 +716,13 @@ cudaError_t launch_realign_pair(const tj_nvfp4 &in, const tj_nvfp4 &out, int mod
     const OutNv oa = out_nv(out);
     const OutMx ob = out_mx(out8);
     const int64_t nxa = oa.rows_p / 64, nya = oa.cols_p / 128, nxb = ob.rows_p / 64, nyb = ob.cols_p / 128;
+    if (nxa * nya == 0 || nxb * nyb == 0) {          // an empty part: the other one alone
+        if (nxa * nya > 0) return launch_realign_nv(in, out, mode, rht, seed, tag, rht_tag, s);
+        if (nxb * nyb > 0) return launch_realign_mx(in8, out8, s);
+        return cudaSuccess;
+    }
     const int64_t nb = nxb * nyb, n = nb + nxa * nya;
-    if (nxa == 0 || nxb == 0 || n > 0x7fffffff) return cudaErrorInvalidValue;
+    if (n > 0x7fffffff) return cudaErrorInvalidValue;
     const PhiloxKeys pk = philox_keys(seed);
     const SrcNv sa = src_nv(in);
     const SrcMx sb = src_mx(in8);
@@ -728,6 +736,7 @@ cudaError_t launch_realign_pair(const tj_nvfp4 &in, const tj_nvfp4 &out, int mod
 
 cudaError_t launch_rht(const float *x, float *y, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,
                        cudaStream_t s) {
+    if (rows == 0 || cols == 0) return cudaSuccess;
     const int64_t grid = row_grid(rows * (cols / 128));
     k_rht<<<grid, kThreads, 0, s>>>(x, y, rows, cols, philox_keys(seed), tag);
     return cudaGetLastError();

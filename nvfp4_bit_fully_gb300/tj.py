@@ -122,6 +122,17 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_NO_COLUMN = ctypes.c_int32(0)
+
+
+def _sel_ptr(sel):
+    """A channel selection: None -> NULL (all columns); an empty index tensor, whose data
+    pointer is NULL, -> a non-NULL address that the library does not read (no column)."""
+    if sel is None:
+        return None
+    return ctypes.c_void_p(sel.data_ptr()) if sel.numel() else ctypes.cast(ctypes.byref(_NO_COLUMN), ctypes.c_void_p)
+
+
 def _stream(stream=None):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
@@ -185,7 +196,7 @@ def quantize_nvfp4(x, along_cols=False, sel=None, mode=TJ_RTN, rht=False, seed=0
     orows, ocols = (ncols, rows_x) if along_cols else (rows_x, ncols)
     out = out if out is not None else NVFP4.empty(orows, ocols, x.device)
     c = out.c()
-    _call("tj_quantize_nvfp4", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols), _ptr(sel),
+    _call("tj_quantize_nvfp4", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols), _sel_ptr(sel),
           0 if sel is None else sel.numel(), mode, int(rht), seed, tag, rht_tag, ctypes.byref(c), _stream(stream))
     return out
 
@@ -197,7 +208,7 @@ def quantize_mxfp8(x, along_cols=False, sel=None, out=None, stream=None, fmt=TJ_
     orows, ocols = (ncols, rows_x) if along_cols else (rows_x, ncols)
     out = out if out is not None else MXFP8.empty(orows, ocols, x.device, fmt)
     c = out.c()
-    _call("tj_quantize_mxfp8", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols), _ptr(sel),
+    _call("tj_quantize_mxfp8", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols), _sel_ptr(sel),
           0 if sel is None else sel.numel(), ctypes.byref(c), _stream(stream))
     return out
 
@@ -213,7 +224,7 @@ def quantize_nvfp4_mxfp8(x, along_cols=False, sel=None, mode=TJ_RTN, rht=False, 
     out8 = out8 if out8 is not None else MXFP8.empty(orows, ocols, x.device, fmt8)
     c, c8 = out.c(), out8.c()
     _call("tj_quantize_nvfp4_mxfp8", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols),
-          _ptr(sel), 0 if sel is None else sel.numel(), mode, int(rht), seed, tag, rht_tag, ctypes.byref(c),
+          _sel_ptr(sel), 0 if sel is None else sel.numel(), mode, int(rht), seed, tag, rht_tag, ctypes.byref(c),
           ctypes.byref(c8), _stream(stream))
     return out, out8
 

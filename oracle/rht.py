@@ -24,8 +24,8 @@ def fwht128_f32(x):
     """Unnormalised Walsh-Hadamard transform of each 128-block of the last axis (fp32)."""
     y = np.array(x, dtype=F32, copy=True)
     assert y.shape[-1] % RHT_N == 0
-    lead = y.shape[:-1]
-    y = y.reshape(*lead, -1, RHT_N)
+    lead, nblk = y.shape[:-1], y.shape[-1] // RHT_N
+    y = y.reshape(*lead, nblk, RHT_N)          # (an explicit block count: rows may be empty)
     h = 1
     while h < RHT_N:
         idx = np.arange(RHT_N)
@@ -35,7 +35,7 @@ def fwht128_f32(x):
         y[..., i] = (a + b).astype(F32)
         y[..., i + h] = (a - b).astype(F32)
         h *= 2
-    return y.reshape(*lead, -1)
+    return y.reshape(*lead, nblk * RHT_N)
 
 
 def rht_f32(x, d):

@@ -112,6 +112,17 @@ def test_tiny_linear_with_outcontrol(tj):
     _run_and_check(tj, X, W, dY, outl, seed=5)
 
 
+def test_every_channel_an_outlier(tj):
+    """The degenerate OutControl split with p = 100%: no NVFP4 channels, the whole layer in
+    the FP8 slice (the empty NVFP4 parts are skipped, the products are the slice's alone)."""
+    g = torch.Generator().manual_seed(29)
+    M, N, K = 200, 136, 256
+    X = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    W = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16)
+    dY = (torch.randn(M, N, generator=g) * 1e-3).to(torch.bfloat16)
+    _run_and_check(tj, X, W, dY, np.arange(K), seed=9)
+
+
 def test_ragged_linear(tj):
     g = torch.Generator().manual_seed(11)
     M, N, K = 200, 136, 328
