@@ -29,8 +29,8 @@
 // A thread can observe only one barrier handoff every few hundred cycles, so the
 // design keeps handoffs few: the partial slots are released through hardware named
 // barriers, the scale factors of a block share its partial slot's lifetime, and the
-// outer scales travel with the operands and are handed back by the MMA warp when it
-// meets the promotion warps' next release.
+// outer scales travel with the operands and are handed back by the promotion warps once
+// their math is done with them.
 // The FP8 slice accumulates over its whole K into the next partial slot, which the
 // promotion adds with weight 1.
 // Tensor memory (512 columns): partials [0,384) (128 per slot), FP4 scale factors
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             ptx::mbar_init(&bars->empty[s], 1);
         }
         for (int p = 0; p < kPSlots; ++p) ptx::mbar_init(&bars->pfull[p], 1);
-        for (int q = 0; q < kScaleSlots; ++q) ptx::mbar_init(&bars->sempty[q], 1);
+        for (int q = 0; q < kScaleSlots; ++q) ptx::mbar_init(&bars->sempty[q], kPromoWarps);
         ptx::mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         for (int p = 0; p < kPSlots; ++p) bars->met[p] = 0;
@@ -407,18 +407,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         // meets every promotion warp's release of the block that used it three blocks earlier;
         // that also frees the slot's scale-factor columns, which only that block's MMAs read.
         const uint32_t idesc4 = idesc_nvf4();
-        int it = 0, pc = 0, f4 = 0;
+        int it = 0, pc = 0;
         bool live = true;
-        // The promotion warps read the outer scales of FP4 block b after releasing its partial
-        // and before releasing the next one, so b's outer-scale slot is handed back to the
-        // producers once the barrier of block b + 1 is met: byte (b + 1) & 3 of `rel` holds
-        // that slot + 1 until then (0: nothing to hand back).
-        uint32_t rel = 0u;
-        auto release = [&](int idx) {
-            const int r = (int)((rel >> (8 * idx)) & 0xffu) - 1;
-            if (r >= 0 && lane == 0) ptx::mbar_arrive(&bars->sempty[r]);
-            rel &= ~(0xffu << (8 * idx));
-        };
         for (int tile = cta; tile < ntiles; tile += ncta) {
             const TileWork w = tile_work(args, tile);
             for (int st = 0; st < w.nstages; ++st, ++it) {
@@ -434,7 +424,6 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     for (int kbl = 0; kbl < nkbs; ++kbl, ++pc) {
                         const int ps = pc % kPSlots;
                         if (pc >= kPSlots) named_sync(kNamedP + ps, kNamedCount);
-                        release((pc + 1) & 3);
                         ptx::tc_fence_after();
                         if (live && lane == 0) {
                             const uint32_t sfcol = tbase + kColSf + 16u * (uint32_t)ps;
@@ -458,8 +447,6 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                         // the generation just met, published for the promotion warps' abort path
                         // (a plain store, after the issue so that it stays off the meet-to-issue path)
                         if (pc >= kPSlots && lane == 0) bars->met[ps] = pc / kPSlots;
-                        rel |= (uint32_t)(f4 % kScaleSlots + 1) << (8 * ((pc + 1) & 3));
-                        ++f4;
                     }
                 } else {
                     // the FP8 slice: all its stages accumulate into one partial slot.  A stage's
@@ -468,10 +455,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     // because the producers refilled the ring slot only after its release
                     const int s8 = st - w.nst4;
                     const int ps = pc % kPSlots;
-                    if (s8 == 0) {
-                        if (pc >= kPSlots) named_sync(kNamedP + ps, kNamedCount);
-                        release((pc + 1) & 3);
-                    }
+                    if (s8 == 0 && pc >= kPSlots) named_sync(kNamedP + ps, kNamedCount);
                     ptx::tc_fence_after();
                     if (live && lane == 0) {
                         const uint32_t sfcol = tbase + kColSf8 + 8u * (uint32_t)slot;
@@ -498,7 +482,6 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         for (int j = (pc > kPSlots ? pc - kPSlots : 0); j < pc; ++j) {
             named_sync(kNamedP + j % kPSlots, kNamedCount);
             if (lane == 0) bars->met[j % kPSlots] = j / kPSlots + 1;
-            release(j & 3);
         }
         // all MMAs / copies issued by this thread complete before TMEM is freed
         if (lane == 0) {
@@ -572,8 +555,14 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                             ac[i] = add2(ac[i], (uint64_t)p[2 * i] | ((uint64_t)p[2 * i + 1] << 32));
                     }
                 }
+                if (kb < w.nkb4) {
+                    // this warp is done with the block's outer scales: its share of handing their
+                    // slot back to the producers (the slot's barrier counts the promotion warps)
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&bars->sempty[f4c % kScaleSlots]);
+                    ++f4c;
+                }
                 if (++ps == kPSlots) { ps = 0; pph ^= 1u; }
-                if (kb < w.nkb4) ++f4c;
             }
             if (aborted) break;
             // epilogue: the warp's 32 x kColsW slice of the tile (rows 32q.., columns kColsW*cq..)

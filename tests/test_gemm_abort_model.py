@@ -5,7 +5,9 @@ ring (mbarriers full / empty, outer-scale slots sempty), the MMA warp turns each
 block into a tensor-memory partial in a 3-slot ring (commit -> mbarrier pfull), and
 eight promotion warps read each partial and release its slot through hardware named
 barriers (one per slot, 9 warps per generation: the MMA warp meets it with a sync
-before it reuses the slot; a live promotion warp arrives without waiting).  Every
+before it reuses the slot; a live promotion warp arrives without waiting).  Each
+promotion warp also hands an FP4 block's outer-scale slot back once its math is done
+(sempty completes a phase after eight arrivals).  Every
 mbarrier wait is bounded; a wait that runs out sets the CTA's abort flag, after which
 the roles stop working but keep the named-barrier protocol, which has no time bound.
 
@@ -44,7 +46,8 @@ class Model:
         self.full = [0] * STAGES             # completed phases per mbarrier
         self.empty = [0] * STAGES
         self.pfull = [0] * PSLOTS
-        self.sempty = [0] * SSLOTS
+        self.sempty = [0] * SSLOTS             # completed phases of each outer-scale slot
+        self.sempty_arrivals = [0] * SSLOTS
         self.met = [0] * PSLOTS              # generations the MMA warp has met per slot
         self.bar = {s: {"gen": 0, "members": set()} for s in range(PSLOTS)}
 
@@ -123,13 +126,7 @@ class Model:
         # drain: the copies it issued have landed (they complete by themselves in the model)
 
     def mma(self):
-        it, pc, f4, live = 0, 0, 0, True
-        rel = [None] * 4                     # outer-scale slot to hand back, by (block + 1) & 3
-
-        def release(idx):
-            if rel[idx] is not None:
-                self.sempty[rel[idx] % SSLOTS] += 1
-                rel[idx] = None
+        it, pc, live = 0, 0, True
         for w, st, nst4 in self.stages():
             nkb4, nk8 = w
             slot = it % STAGES
@@ -141,20 +138,15 @@ class Model:
                     if pc >= PSLOTS:
                         yield from self.sync(ps, "mma")
                         self.met[ps] += 1
-                    release((pc + 1) & 3)
                     if live:
                         self.pfull[ps] += 1       # MMAs complete, commit arrives
-                    rel[(pc + 1) & 3] = f4
-                    f4 += 1
                     pc += 1
             else:
                 s8 = st - nst4
                 ps = pc % PSLOTS
-                if s8 == 0:
-                    if pc >= PSLOTS:
-                        yield from self.sync(ps, "mma")
-                        self.met[ps] += 1
-                    release((pc + 1) & 3)
+                if s8 == 0 and pc >= PSLOTS:
+                    yield from self.sync(ps, "mma")
+                    self.met[ps] += 1
                 if live and s8 == nk8 - 1:
                     self.pfull[ps] += 1
                 if s8 == nk8 - 1:
@@ -165,10 +157,9 @@ class Model:
         for j in range(max(pc - PSLOTS, 0), pc):
             yield from self.sync(j % PSLOTS, "mma")
             self.met[j % PSLOTS] += 1
-            release(j & 3)
 
     def promo(self, warp):
-        live, blk = True, 0
+        live, blk, f4c = True, 0, 0
         for w in self.works:
             nkb4, nk8 = w
             nblk = nkb4 + (1 if nk8 else 0)
@@ -178,6 +169,12 @@ class Model:
                     live = yield from self.wait_bounded(self.pfull, ps, blk // PSLOTS)
                 if live:
                     self.arrive(ps, warp)
+                    if kb < nkb4:                 # the math is done with the block's outer scales
+                        s = f4c % SSLOTS
+                        self.sempty_arrivals[s] += 1
+                        if self.sempty_arrivals[s] % PROMO == 0:
+                            self.sempty[s] += 1
+                        f4c += 1
                 else:
                     if self.gate:
                         # the slot's previous generation must have been met by the MMA warp.  The
@@ -226,7 +223,8 @@ class Model:
         return self
 
     def snapshot(self):
-        return (tuple(self.full), tuple(self.empty), tuple(self.pfull), tuple(self.met), self.abort,
+        return (tuple(self.full), tuple(self.empty), tuple(self.pfull), tuple(self.met), tuple(self.sempty),
+                tuple(self.sempty_arrivals), self.abort,
                 tuple((b["gen"], len(b["members"])) for b in self.bar.values()))
 
 
