@@ -195,3 +195,25 @@ def test_linear_calls_equal_their_steps(tj):
     tj.gemm_mxfp8(tj.quantize_mxfp8(dY, along_cols=True), tj.requantize_mxfp8(x82), out=dw2, col_map=oi)
     torch.cuda.synchronize()
     assert torch.equal(y, y2) and torch.equal(dx, dx2) and torch.equal(dw, dw2)
+
+
+def test_linear_is_deterministic(tj):
+    """Every output of the layer is a fixed function of its inputs: two runs over 4096 tokens
+    (many tiles per CTA, split-K dW, the FP8 slice) give the same bytes."""
+    g = torch.Generator().manual_seed(31)
+    M, N, K = 4096, 1536, 1024
+    X = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    W = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16)
+    dY = (torch.randn(M, N, generator=g) * 1e-3).to(torch.bfloat16).cuda()
+    outl = np.sort(np.random.default_rng(5).choice(K, 103, replace=False))
+    ni, oi, wq, w8 = _setup(tj, X.cpu(), W, outl)
+    runs = []
+    for _ in range(2):
+        y, xq, x8 = tj.linear_fwd(X, wq, w8, ni, oi)
+        dx = tj.linear_bwd_dx(dY, wq, w8, ni, oi, seed=17)
+        dw = tj.linear_bwd_dw(dY, xq, x8, ni, oi, seed=17)
+        runs.append([y, xq.codes, xq.sf, xq.outer, x8.codes, x8.sf, dx, dw])
+    torch.cuda.synchronize()
+    tj.device_status()
+    for a, b in zip(*runs):
+        assert torch.equal(a, b)
