@@ -346,9 +346,11 @@ __global__ void __launch_bounds__(256, 4) k_realign_pair(SrcNv sa, OutNv oa, Src
 // (`sel_o`) -> MXFP8.  Same results as the two gathering calls
 // (tj_quantize_nvfp4 RTN with sel = normal, tj_quantize_mxfp8 with sel = outliers).
 //
-// A CTA stages a tile of `tr` whole input rows in shared memory as 32-bit words,
-// one pad word after every 32, and gathers the selected columns from there
-// through two tables of byte offsets built once per CTA.  The tables list the
+// A CTA stages tiles of `tr` whole input rows in shared memory as 32-bit words,
+// two pad words after every 32, and gathers the selected columns from there
+// through two tables of byte offsets built once per CTA.  Two staging buffers: the
+// rows of the next tile arrive by asynchronous copies (cp.async, 8 bytes each, which
+// the two-word pad keeps aligned) while the current tile is gathered and quantized.  The tables list the
 // channels in output order, padded by 4 entries after every 32, so a lane reads
 // its 32 offsets with eight 16-byte loads; entries past the end of a list point
 // at a zero word of the row.  The quads of all warps take (row, segment) tasks of
@@ -356,13 +358,23 @@ __global__ void __launch_bounds__(256, 4) k_realign_pair(SrcNv sa, OutNv oa, Src
 // ---------------------------------------------------------------------------
 constexpr int kSplitThreads = 256;
 
-// words of one staged row: the data words, a pad after every 32, one zero word, 16-byte rows
+// words of one staged row: the data words, two pads after every 32, one zero word, 16-byte rows
 __host__ __device__ inline int split_row_words(int K, int esz) {
     const int nw = esz == 2 ? (K + 1) / 2 : K;
-    return (int)round_up(nw + (nw + 31) / 32 + 1, 4);
+    return (int)round_up(nw + 2 * ((nw + 31) / 32) + 1, 4);
 }
 __host__ __device__ inline int split_tab_words(int len) { return len + len / 8; }    // len: a multiple of 128
-__device__ __forceinline__ int split_pad_row(int w) { return w + (w >> 5); }
+__device__ __forceinline__ int split_pad_row(int w) { return w + 2 * (w >> 5); }
+
+// 8-byte asynchronous copy global -> shared; src_bytes 0 writes zeros and reads nothing
+__device__ __forceinline__ void cp_async8(void *smem_dst, const void *gsrc, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+                 "l"(gsrc), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ int split_pad_tab(int i) { return i + 4 * (i >> 5); }
 
 template <typename T>
@@ -412,13 +424,15 @@ __global__ void __launch_bounds__(kSplitThreads) k_quant_split(const T *x, int64
     const int rw = split_row_words(K, (int)sizeof(T));
     uint32_t *tab_n = reinterpret_cast<uint32_t *>(smem_split);
     uint32_t *tab_o = tab_n + split_tab_words(128 * nseg_n);
-    uint32_t *tile = tab_o + split_tab_words(128 * nseg_o);
+    uint32_t *tiles[2];
+    tiles[0] = tab_o + split_tab_words(128 * nseg_o);
+    tiles[1] = tiles[0] + tr * rw;
     const uint32_t zero_off = 4u * (uint32_t)(rw - 1);
     for (int i = threadIdx.x; i < 128 * nseg_n; i += blockDim.x)
         tab_n[split_pad_tab(i)] = i < kn ? split_byte_off<T>(sel_n[i]) : zero_off;
     for (int i = threadIdx.x; i < 128 * nseg_o; i += blockDim.x)
         tab_o[split_pad_tab(i)] = i < k ? split_byte_off<T>(sel_o[i]) : zero_off;
-    for (int r = threadIdx.x; r < tr; r += blockDim.x) tile[r * rw + rw - 1] = 0u;
+    for (int r = threadIdx.x; r < 2 * tr; r += blockDim.x) tiles[0][r * rw + rw - 1] = 0u;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3, qd = lane >> 2;
     const int nwarp = blockDim.x >> 5;
@@ -426,7 +440,7 @@ __global__ void __launch_bounds__(kSplitThreads) k_quant_split(const T *x, int64
     const int64_t ntile = (rows_p + tr - 1) / tr;
     const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0) && ((ld * (int64_t)sizeof(T)) % 16 == 0);
     constexpr int kv = 16 / (int)sizeof(T);              // elements per 16-byte chunk
-    const int nch = vec ? K / kv : 0;                    // full chunks per row, loaded as vectors
+    const int nch = vec ? K / kv : 0;                    // full chunks per row, copied asynchronously
     const int nw = sizeof(T) == 2 ? (K + 1) / 2 : K;     // data words per row
     const int wtail = 4 * nch, ntail = nw - wtail;       // words loaded one at a time
     const int fill_dr = nch > 0 ? (int)blockDim.x / nch : 0, fill_dc = (int)blockDim.x - fill_dr * nch;
@@ -434,50 +448,43 @@ __global__ void __launch_bounds__(kSplitThreads) k_quant_split(const T *x, int64
     const int step_t = nwarp * 8;
     const int dr_n = nseg_n > 0 ? step_t / nseg_n : 0, dk_n = step_t - dr_n * nseg_n;
     const int dr_o = nseg_o > 0 ? step_t / nseg_o : 0, dk_o = step_t - dr_o * nseg_o;
-    for (int64_t tl = blockIdx.x; tl < ntile; tl += gridDim.x) {
+
+    // Start the copies of tile tl's rows into buf: chunk i of the tile is (row i / nch, chunk
+    // i % nch), stepped by blockDim.x chunks with a carry instead of dividing; rows past the end
+    // are filled with zeros.  The words past a row's last full chunk are loaded and stored here.
+    auto stage = [&](int64_t tl, uint32_t *buf) {
         const int64_t r0 = tl * tr;
-        __syncthreads();                                 // the previous tile's gathers are done
-        // eight 16-byte loads in flight per thread before their stores.  Chunk i of the tile is
-        // (row i / nch, chunk i % nch); the pair is stepped by blockDim.x chunks with a carry
-        // instead of dividing (the divisions were a third of the kernel's instructions)
-        constexpr int kU = 8;
         int fr = (int)threadIdx.x / (nch > 0 ? nch : 1), fc = (int)threadIdx.x - fr * nch;   // chunk threadIdx.x
-        for (int i0 = threadIdx.x; i0 < tr * nch; i0 += kU * blockDim.x) {
-            uint4 w[kU];
-            int rr[kU], cc[kU];
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int i = i0 + u * (int)blockDim.x;
-                rr[u] = fr;
-                cc[u] = fc;
-                fr += fill_dr;
-                fc += fill_dc;
-                if (fc >= nch) { fc -= nch; ++fr; }
-                w[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (i < tr * nch && r0 + rr[u] < rows)
-                    w[u] = __ldg(reinterpret_cast<const uint4 *>(x + (r0 + rr[u]) * ld) + cc[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int i = i0 + u * (int)blockDim.x;
-                if (i < tr * nch) {
-                    uint32_t *d = tile + rr[u] * rw + split_pad_row(4 * cc[u]);  // 4 words inside one 32-word run
-                    d[0] = w[u].x;
-                    d[1] = w[u].y;
-                    d[2] = w[u].z;
-                    d[3] = w[u].w;
-                }
-            }
+        for (int i = threadIdx.x; i < tr * nch; i += blockDim.x) {
+            const int rr = fr, cc = fc;
+            fr += fill_dr;
+            fc += fill_dc;
+            if (fc >= nch) { fc -= nch; ++fr; }
+            const bool in = r0 + rr < rows;
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(in ? x + (r0 + rr) * ld + (int64_t)cc * kv : x);
+            uint32_t *d = buf + rr * rw + split_pad_row(4 * cc);       // 4 words inside one 32-word run
+            cp_async8(d, src, in ? 8u : 0u);
+            cp_async8(d + 2, src + (in ? 8 : 0), in ? 8u : 0u);
         }
         for (int i = threadIdx.x; i < tr * ntail; i += blockDim.x) {
             const int r = i / ntail, w = wtail + (i - r * ntail);
-            tile[r * rw + split_pad_row(w)] = split_word(x, ld, r0 + r, rows, K, w);
+            buf[r * rw + split_pad_row(w)] = split_word(x, ld, r0 + r, rows, K, w);
         }
-        __syncthreads();
+    };
+    int64_t tl = blockIdx.x;
+    if (tl < ntile) stage(tl, tiles[0]);
+    cp_async_commit();
+    for (int b = 0; tl < ntile; tl += gridDim.x, b ^= 1) {
+        const int64_t r0 = tl * tr;
+        const uint32_t *tile = tiles[b];
+        if (tl + gridDim.x < ntile) stage(tl + gridDim.x, tiles[b ^ 1]);   // lands during this tile
+        cp_async_commit();
+        cp_async_wait_one();                             // this thread's copies of tile tl have landed
+        __syncthreads();                                 // ... and every thread's
         const int nt_n = tr * nseg_n;
         int tr_n = nseg_n > 0 ? (warp * 8 + qd) / nseg_n : 0, tk_n = (warp * 8 + qd) - tr_n * nseg_n;   // task warp*8 + qd
-        for (int b = warp * 8; b < nt_n; b += nwarp * 8) {             // warp-uniform
-            const int task = b + qd;
+        for (int q0 = warp * 8; q0 < nt_n; q0 += nwarp * 8) {          // warp-uniform
+            const int task = q0 + qd;
             const bool ok = task < nt_n;
             const int r = ok ? tr_n : 0, kb = ok ? tk_n : 0;
             tr_n += dr_n;
@@ -490,8 +497,8 @@ __global__ void __launch_bounds__(kSplitThreads) k_quant_split(const T *x, int64
         }
         const int nt_o = tr * nseg_o;
         int tr_o = nseg_o > 0 ? (warp * 8 + qd) / nseg_o : 0, tk_o = (warp * 8 + qd) - tr_o * nseg_o;
-        for (int b = warp * 8; b < nt_o; b += nwarp * 8) {
-            const int task = b + qd;
+        for (int q0 = warp * 8; q0 < nt_o; q0 += nwarp * 8) {
+            const int task = q0 + qd;
             const bool ok = task < nt_o;
             const int r = ok ? tr_o : 0, kb = ok ? tk_o : 0;
             tr_o += dr_o;
@@ -502,6 +509,7 @@ __global__ void __launch_bounds__(kSplitThreads) k_quant_split(const T *x, int64
             const MxSeg m = quant_mx_group(v, omx.fmt);
             store_mx_seg(omx, r0 + r, kb, t, m, ok && r0 + r < omx.rows_p);
         }
+        __syncthreads();                                 // the gathers are done before the buffer is refilled
     }
 }
 
@@ -675,10 +683,11 @@ cudaError_t launch_quant_split(const void *x, int dtype, int64_t rows, int64_t K
     const OutMx m = k > 0 ? out_mx(out8) : OutMx{};
     const int64_t tabs = 4 * (int64_t)(split_tab_words((int)o.cols_p) + (k > 0 ? split_tab_words((int)m.cols_p) : 0));
     const int64_t row_bytes = 4 * (int64_t)split_row_words((int)K, esz);
-    // a tile of about 48 KB of rows, so that three or four CTAs share an SM
-    int64_t tr = (48 * 1024) / row_bytes;
+    // two staging buffers of about 24 KB of rows each, so that three or four CTAs share an SM
+    int64_t tr = (24 * 1024) / row_bytes;
     tr = tr < 1 ? 1 : (tr > 64 ? 64 : tr);
-    const size_t smem = (size_t)(tabs + tr * row_bytes);
+    if (tr >= 8) tr -= tr % 8;     // whole passes of the 64 quads when a row has 8 segments
+    const size_t smem = (size_t)(tabs + 2 * tr * row_bytes);
     if (smem > 200 * 1024) return cudaErrorNotSupported;
     const int64_t ntile = (o.rows_p + tr - 1) / tr;
     const int per_sm = smem <= 56 * 1024 ? 4 : (smem <= 75 * 1024 ? 3 : (smem <= 113 * 1024 ? 2 : 1));
