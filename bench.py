@@ -281,7 +281,7 @@ TRAFFIC_BYTES_PER_LAUNCH = {"k_gemm_nvfp4": 108.8e6}
 # alone, its slice alone, and both for the pair launch, at 921 + 103 channels).  With them each
 # kernel entry reports an issue roofline: lane instructions / (SMs x 128 lanes x SM clock x
 # time), the fraction of the SMs' instruction issue the kernel uses.
-LANE_INSTR_PER_ELEM = {"rows": 40.89, "cols": 46.29, "split": 23.16, "realign_nv": 48.11, "realign_mx": 28.12,
+LANE_INSTR_PER_ELEM = {"rows": 40.89, "cols": 46.29, "split": 27.11, "realign_nv": 48.11, "realign_mx": 28.12,
                       "realign_pair": 47.15}
 NV_B = 0.5 + 1.0 / 16 + 4.0 / 128      # bytes per NVFP4 element (codes + E4M3 + FP32 scales)
 MX_B = 1.0 + 1.0 / 32                   # bytes per MXFP8 element (E4M3 + UE8M0)
