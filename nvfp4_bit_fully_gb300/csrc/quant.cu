@@ -350,11 +350,11 @@ __global__ void __launch_bounds__(256, 4) k_realign_pair(SrcNv sa, OutNv oa, Src
 // two pad words after every 32, and gathers the selected columns from there
 // through two tables of byte offsets built once per CTA.  Two staging buffers: the
 // rows of the next tile arrive by asynchronous copies (cp.async, 8 bytes each, which
-// the two-word pad keeps aligned) while the current tile is gathered and quantized.  The tables list the
-// channels in output order, padded by 4 entries after every 32, so a lane reads
-// its 32 offsets with eight 16-byte loads; entries past the end of a list point
-// at a zero word of the row.  The quads of all warps take (row, segment) tasks of
-// the whole tile: first every NVFP4 task, then every MXFP8 task.
+// the two-word pad keeps aligned) while the current tile is gathered and quantized.
+// The tables list the channels in output order, padded by 4 entries after every 32,
+// so a lane reads its 32 offsets with eight 16-byte loads; entries past the end of a
+// list point at a zero word of the row.  The quads of all warps take (row, segment)
+// tasks of the whole tile: first every NVFP4 task, then every MXFP8 task.
 // ---------------------------------------------------------------------------
 constexpr int kSplitThreads = 256;
 
