@@ -217,3 +217,32 @@ def test_linear_is_deterministic(tj):
     tj.device_status()
     for a, b in zip(*runs):
         assert torch.equal(a, b)
+
+
+def test_strided_inputs_and_outputs(tj):
+    """X, dY and the outputs as column slices of wider buffers (row strides K + 40, N + 24,
+    N + 16, K + 8): every result equals the contiguous call byte for byte, and the columns
+    beyond each view are left untouched."""
+    g = torch.Generator().manual_seed(37)
+    M, N, K = 300, 200, 328
+    outl = np.sort(np.random.default_rng(7).choice(K, 33, replace=False))
+    Xw = torch.randn(M, K + 40, generator=g).to(torch.bfloat16).cuda()
+    dYw = (torch.randn(M, N + 24, generator=g) * 1e-3).to(torch.bfloat16).cuda()
+    W = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16)
+    ni, oi, wq, w8 = _setup(tj, Xw[:, :K].cpu(), W, outl)
+    X, dY = Xw[:, :K], dYw[:, :N]
+    y_ref, xq_ref, x8_ref = tj.linear_fwd(X.contiguous(), wq, w8, ni, oi)
+    dx_ref = tj.linear_bwd_dx(dY.contiguous(), wq, w8, ni, oi, seed=3)
+    dw_ref = tj.linear_bwd_dw(dY.contiguous(), xq_ref, x8_ref, ni, oi, seed=3)
+    yw = torch.full((M, N + 16), 5.0, dtype=torch.bfloat16, device="cuda")
+    dxw = torch.full((M, K + 8), 5.0, dtype=torch.bfloat16, device="cuda")
+    dww = torch.full((N, K + 8), 5.0, device="cuda")
+    y, xq, x8 = tj.linear_fwd(X, wq, w8, ni, oi, out=yw[:, :N])
+    dx = tj.linear_bwd_dx(dY, wq, w8, ni, oi, seed=3, out=dxw[:, :K])
+    dw = tj.linear_bwd_dw(dY, xq, x8, ni, oi, seed=3, out=dww[:, :K])
+    torch.cuda.synchronize()
+    tj.device_status()
+    for a, b in ((y, y_ref), (dx, dx_ref), (dw, dw_ref), (xq.codes, xq_ref.codes), (xq.sf, xq_ref.sf),
+                 (xq.outer, xq_ref.outer), (x8.codes, x8_ref.codes), (x8.sf, x8_ref.sf)):
+        assert torch.equal(a, b)
+    assert bool((yw[:, N:] == 5.0).all()) and bool((dxw[:, K:] == 5.0).all()) and bool((dww[:, K:] == 5.0).all())
