@@ -246,3 +246,40 @@ def test_strided_inputs_and_outputs(tj):
                  (xq.outer, xq_ref.outer), (x8.codes, x8_ref.codes), (x8.sf, x8_ref.sf)):
         assert torch.equal(a, b)
     assert bool((yw[:, N:] == 5.0).all()) and bool((dxw[:, K:] == 5.0).all()) and bool((dww[:, K:] == 5.0).all())
+
+
+def test_concurrent_streams(tj):
+    """Two layers forward and backward on two streams at once equal the same calls run one
+    after the other: the launches share no hidden state and honour their stream."""
+    g = torch.Generator().manual_seed(41)
+    M, N, K = 2048, 640, 512
+    outl = np.sort(np.random.default_rng(9).choice(K, 52, replace=False))
+    layers = []
+    for _ in range(2):
+        X = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+        W = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16)
+        dY = (torch.randn(M, N, generator=g) * 1e-3).to(torch.bfloat16).cuda()
+        ni, oi, wq, w8 = _setup(tj, X.cpu(), W, outl)
+        layers.append((X, dY, ni, oi, wq, w8))
+
+    def run(L, stream=None):
+        X, dY, ni, oi, wq, w8 = L
+        y, xq, x8 = tj.linear_fwd(X, wq, w8, ni, oi, stream=stream)
+        dx = tj.linear_bwd_dx(dY, wq, w8, ni, oi, seed=5, stream=stream)
+        dw = tj.linear_bwd_dw(dY, xq, x8, ni, oi, seed=5, stream=stream)
+        return [y, dx, dw, xq.codes, xq.sf, xq.outer, x8.codes, x8.sf]
+
+    ref = [run(L) for L in layers]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    got = []
+    for L, s in zip(layers, streams):
+        with torch.cuda.stream(s):
+            got.append(run(L, stream=s))
+    torch.cuda.synchronize()
+    tj.device_status()
+    for r, o in zip(ref, got):
+        for a, b in zip(r, o):
+            assert torch.equal(a, b)
