@@ -283,3 +283,60 @@ def test_concurrent_streams(tj):
     for r, o in zip(ref, got):
         for a, b in zip(r, o):
             assert torch.equal(a, b)
+
+
+def test_cuda_graph_capture(tj):
+    """The layer's launches (forward, dX, dW) captured into one CUDA graph and replayed give
+    the eager calls' bytes; a replay after the inputs change gives the new results."""
+    g = torch.Generator().manual_seed(43)
+    M, N, K = 1024, 512, 512
+    k = 52
+    outl = np.sort(np.random.default_rng(11).choice(K, k, replace=False))
+    X = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    W = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16)
+    dY = (torch.randn(M, N, generator=g) * 1e-3).to(torch.bfloat16).cuda()
+    ni, oi, wq, w8 = _setup(tj, X.cpu(), W, outl)
+    # buffers the graph writes, allocated up front
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    xq, x8 = tj.NVFP4.empty(M, K - k), tj.MXFP8.empty(M, k)
+    dx = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty(N, K, dtype=torch.float32, device="cuda")
+    ws_dx = torch.empty(tj.workspace_size(tj.TJ_OP_BWD_DX, M, N, K, k), dtype=torch.uint8, device="cuda")
+    ws_dw = torch.empty(tj.workspace_size(tj.TJ_OP_BWD_DW, M, N, K, k), dtype=torch.uint8, device="cuda")
+
+    def layer():
+        tj.linear_fwd(X, wq, w8, ni, oi, xq=xq, x8=x8, out=y)
+        tj.linear_bwd_dx(dY, wq, w8, ni, oi, seed=13, workspace=ws_dx, out=dx)
+        tj.linear_bwd_dw(dY, xq, x8, ni, oi, seed=13, workspace=ws_dw, out=dw)
+
+    def snapshot():
+        return [t.clone() for t in (y, dx, dw, xq.codes, xq.sf, xq.outer, x8.codes, x8.sf)]
+
+    layer()                                  # eager (also sets the kernels' launch attributes)
+    torch.cuda.synchronize()
+    eager = snapshot()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            layer()
+    torch.cuda.current_stream().wait_stream(s)
+    for t in (y, dx, dw):
+        t.fill_(7.0)
+    graph.replay()
+    torch.cuda.synchronize()
+    tj.device_status()
+    for a, b in zip(eager, snapshot()):
+        assert torch.equal(a, b)
+    # new inputs in the same buffers: the replay computes them
+    X.copy_(torch.randn(M, K, generator=g).to(torch.bfloat16))
+    dY.mul_(-2.0)
+    layer()
+    torch.cuda.synchronize()
+    eager2 = snapshot()
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager2, snapshot()):
+        assert torch.equal(a, b)
+    assert not torch.equal(eager[0], eager2[0])
