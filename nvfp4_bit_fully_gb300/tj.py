@@ -122,6 +122,68 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_DENSE = (torch.bfloat16, torch.float32)
+_BF16 = (torch.bfloat16,)
+_FP32 = (torch.float32,)
+_MASK = (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
+
+
+def _cuda(t, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s: a CUDA tensor is expected, got %s" % (name, type(t).__name__ if not
+                                                                     isinstance(t, torch.Tensor) else t.device))
+
+
+def _mat(t, name, dtypes=_DENSE):
+    """Pointer to a 2-D CUDA matrix in one of `dtypes`.  The library addresses element (r, c)
+    at r * ld + c, so the columns must be adjacent (stride(1) == 1); the row stride is free."""
+    if t is None:
+        return None
+    _cuda(t, name)
+    if t.dim() != 2:
+        raise ValueError("%s: a 2-D tensor is expected, got shape %s" % (name, tuple(t.shape)))
+    if t.dtype not in dtypes:
+        raise ValueError("%s: dtype %s, expected %s" % (name, t.dtype, " or ".join(map(str, dtypes))))
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError("%s: the columns must be adjacent in memory (stride %s); pass .contiguous()"
+                         % (name, tuple(t.stride())))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _ld(t):
+    """Row stride of a matrix checked by _mat; a single row has no row stride of its own."""
+    return t.stride(0) if t.shape[0] > 1 else t.shape[1]
+
+
+def _arr(t, name, dtypes, numel=None, at_least=False):
+    """Pointer to a contiguous CUDA array in one of `dtypes` with `numel` elements (or at
+    least that many): index lists, column maps, optimizer state, masks."""
+    if t is None:
+        return None
+    _cuda(t, name)
+    if t.dtype not in dtypes:
+        raise ValueError("%s: dtype %s, expected %s" % (name, t.dtype, " or ".join(map(str, dtypes))))
+    if not t.is_contiguous():
+        raise ValueError("%s: a contiguous tensor is expected (stride %s)" % (name, tuple(t.stride())))
+    if numel is not None and (t.numel() < numel if at_least else t.numel() != numel):
+        raise ValueError("%s: %d elements, expected %s%d" % (name, t.numel(), "at least " if at_least else "",
+                                                              numel))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _idx(t, name, numel=None):
+    """An int32 index list (channel selection, column map)."""
+    if t is not None and t.dim() != 1:
+        raise ValueError("%s: a 1-D index tensor is expected, got shape %s" % (name, tuple(t.shape)))
+    return _arr(t, name, (torch.int32,), numel, at_least=True)
+
+
+def _workspace(t, name="workspace"):
+    """(pointer, size in bytes) of a contiguous CUDA scratch buffer of any dtype."""
+    _arr(t, name, (t.dtype,))
+    return ctypes.c_void_p(t.data_ptr()), t.numel() * t.element_size()
+
+
 _NO_COLUMN = ctypes.c_int32(0)
 
 
@@ -130,7 +192,8 @@ def _sel_ptr(sel):
     pointer is NULL, -> a non-NULL address that the library does not read (no column)."""
     if sel is None:
         return None
-    return ctypes.c_void_p(sel.data_ptr()) if sel.numel() else ctypes.cast(ctypes.byref(_NO_COLUMN), ctypes.c_void_p)
+    p = _idx(sel, "sel")
+    return p if sel.numel() else ctypes.cast(ctypes.byref(_NO_COLUMN), ctypes.c_void_p)
 
 
 def _stream(stream=None):
@@ -150,6 +213,14 @@ def _dtype_code(t):
     raise TypeError("bf16 or fp32 tensor expected, got %s" % t.dtype)
 
 
+def _buf(t, name, dtype, numel):
+    """Address of a packed buffer of a quantized tensor: contiguous, CUDA, at least the
+    padded size of its layout."""
+    if t.dtype != dtype:
+        raise ValueError("%s: dtype %s, expected %s" % (name, t.dtype, dtype))
+    return _arr(t, name, (dtype,), numel, at_least=True).value
+
+
 class NVFP4:
     """Device buffers of a double-block NVFP4 tensor (layout documented in tj.h)."""
 
@@ -164,7 +235,10 @@ class NVFP4:
                      torch.empty((cp // 128) * rp, dtype=torch.float32, device=device), rows, cols)
 
     def c(self):
-        return CNvfp4(self.codes.data_ptr(), self.sf.data_ptr(), self.outer.data_ptr(), self.rows, self.cols)
+        rp, cp = _round_up(self.rows, 128), _round_up(self.cols, 128)
+        return CNvfp4(_buf(self.codes, "NVFP4 codes", torch.uint8, rp * cp // 2),
+                      _buf(self.sf, "NVFP4 inner scales", torch.uint8, rp * cp // 16),
+                      _buf(self.outer, "NVFP4 outer scales", torch.float32, (cp // 128) * rp), self.rows, self.cols)
 
 
 class MXFP8:
@@ -181,7 +255,11 @@ class MXFP8:
                      torch.empty(rp * cp // 32, dtype=torch.uint8, device=device), rows, cols, fmt)
 
     def c(self):
-        return CMxfp8(self.codes.data_ptr(), self.sf.data_ptr(), self.rows, self.cols, self.fmt)
+        if self.fmt not in MX_BITS:
+            raise ValueError("MX slice: unknown element format %r" % (self.fmt,))
+        rp, cp = _round_up(self.rows, 128), _round_up(self.cols, 128)
+        return CMxfp8(_buf(self.codes, "MX slice codes", torch.uint8, rp * cp * MX_BITS[self.fmt] // 8),
+                      _buf(self.sf, "MX slice scales", torch.uint8, rp * cp // 32), self.rows, self.cols, self.fmt)
 
 
 def _ref(obj):
@@ -196,7 +274,7 @@ def quantize_nvfp4(x, along_cols=False, sel=None, mode=TJ_RTN, rht=False, seed=0
     orows, ocols = (ncols, rows_x) if along_cols else (rows_x, ncols)
     out = out if out is not None else NVFP4.empty(orows, ocols, x.device)
     c = out.c()
-    _call("tj_quantize_nvfp4", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols), _sel_ptr(sel),
+    _call("tj_quantize_nvfp4", _mat(x, "x"), _dtype_code(x), rows_x, cols_x, _ld(x), int(along_cols), _sel_ptr(sel),
           0 if sel is None else sel.numel(), mode, int(rht), seed, tag, rht_tag, ctypes.byref(c), _stream(stream))
     return out
 
@@ -208,7 +286,7 @@ def quantize_mxfp8(x, along_cols=False, sel=None, out=None, stream=None, fmt=TJ_
     orows, ocols = (ncols, rows_x) if along_cols else (rows_x, ncols)
     out = out if out is not None else MXFP8.empty(orows, ocols, x.device, fmt)
     c = out.c()
-    _call("tj_quantize_mxfp8", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols), _sel_ptr(sel),
+    _call("tj_quantize_mxfp8", _mat(x, "x"), _dtype_code(x), rows_x, cols_x, _ld(x), int(along_cols), _sel_ptr(sel),
           0 if sel is None else sel.numel(), ctypes.byref(c), _stream(stream))
     return out
 
@@ -223,7 +301,7 @@ def quantize_nvfp4_mxfp8(x, along_cols=False, sel=None, mode=TJ_RTN, rht=False, 
     out = out if out is not None else NVFP4.empty(orows, ocols, x.device)
     out8 = out8 if out8 is not None else MXFP8.empty(orows, ocols, x.device, fmt8)
     c, c8 = out.c(), out8.c()
-    _call("tj_quantize_nvfp4_mxfp8", _ptr(x), _dtype_code(x), rows_x, cols_x, x.stride(0), int(along_cols),
+    _call("tj_quantize_nvfp4_mxfp8", _mat(x, "x"), _dtype_code(x), rows_x, cols_x, _ld(x), int(along_cols),
           _sel_ptr(sel), 0 if sel is None else sel.numel(), mode, int(rht), seed, tag, rht_tag, ctypes.byref(c),
           ctypes.byref(c8), _stream(stream))
     return out, out8
@@ -239,8 +317,8 @@ def quantize_split(x, normal_idx, outlier_idx, out=None, out8=None, stream=None,
         out8 = MXFP8.empty(rows, k, x.device, fmt8)
     c = out.c()
     c8 = out8.c() if k > 0 else None
-    _call("tj_quantize_split", _ptr(x), _dtype_code(x), rows, cols, x.stride(0), _ptr(normal_idx), kn,
-          _ptr(outlier_idx) if k > 0 else None, k, ctypes.byref(c), ctypes.byref(c8) if c8 is not None else None,
+    _call("tj_quantize_split", _mat(x, "x"), _dtype_code(x), rows, cols, _ld(x), _idx(normal_idx, "normal_idx"), kn,
+          _idx(outlier_idx, "outlier_idx") if k > 0 else None, k, ctypes.byref(c), ctypes.byref(c8) if c8 is not None else None,
           _stream(stream))
     return out, out8
 
@@ -276,8 +354,11 @@ def requantize_nvfp4_mxfp8(q, q8, mode=TJ_SR, rht=True, seed=0, tag=0, rht_tag=0
 
 def rht(x, seed, tag, out=None, stream=None):
     """128-point random Hadamard transform of each 128-block of the rows of x (fp32)."""
+    _arr(x, "x", _FP32)
+    if x.dim() != 2:
+        raise ValueError("x: a 2-D tensor is expected, got shape %s" % (tuple(x.shape),))
     out = out if out is not None else torch.empty_like(x)
-    _call("tj_rht", _ptr(x), _ptr(out), x.shape[0], x.shape[1], seed, tag, _stream(stream))
+    _call("tj_rht", _ptr(x), _arr(out, "out", _FP32, x.numel()), x.shape[0], x.shape[1], seed, tag, _stream(stream))
     return out
 
 
@@ -302,8 +383,8 @@ def gemm_nvfp4(a, b, a8=None, b8=None, alpha=1.0, out=None, out_dtype=torch.floa
     ca, cb = a.c(), b.c()
     c8a = a8.c() if a8 is not None else None
     c8b = b8.c() if b8 is not None else None
-    _call("tj_gemm_nvfp4", ctypes.byref(ca), ctypes.byref(cb), _ref(c8a), _ref(c8b), alpha, _ptr(out),
-          _dtype_code(out), out.stride(0), _ptr(col_map), _stream(stream))
+    _call("tj_gemm_nvfp4", ctypes.byref(ca), ctypes.byref(cb), _ref(c8a), _ref(c8b), alpha, _mat(out, "out"),
+          _dtype_code(out), _ld(out), _idx(col_map, "col_map", b.rows), _stream(stream))
     return out
 
 
@@ -311,8 +392,8 @@ def gemm_mxfp8(a8, b8, out=None, out_dtype=torch.float32, col_map=None, stream=N
     if out is None:
         out = torch.empty(a8.rows, b8.rows, dtype=out_dtype, device=a8.codes.device)
     ca, cb = a8.c(), b8.c()
-    _call("tj_gemm_mxfp8", ctypes.byref(ca), ctypes.byref(cb), _ptr(out), _dtype_code(out), out.stride(0),
-          _ptr(col_map), _stream(stream))
+    _call("tj_gemm_mxfp8", ctypes.byref(ca), ctypes.byref(cb), _mat(out, "out"), _dtype_code(out), _ld(out),
+          _idx(col_map, "col_map", b8.rows), _stream(stream))
     return out
 
 
@@ -320,9 +401,9 @@ def gemm_pair(a, b, a8, b8, alpha=1.0, out=None, out8=None, col_map=None, col_ma
     """An FP4 product and an FP8-only product in one launch (tj_gemm_pair); out / out8 may be
     the same tensor when the column maps are disjoint."""
     ca, cb, ca8, cb8 = a.c(), b.c(), a8.c(), b8.c()
-    _call("tj_gemm_pair", ctypes.byref(ca), ctypes.byref(cb), float(alpha), _ptr(out), _dtype_code(out),
-          out.stride(0), _ptr(col_map), ctypes.byref(ca8), ctypes.byref(cb8), _ptr(out8), _dtype_code(out8),
-          out8.stride(0), _ptr(col_map8), _stream(stream))
+    _call("tj_gemm_pair", ctypes.byref(ca), ctypes.byref(cb), float(alpha), _mat(out, "out"), _dtype_code(out),
+          _ld(out), _idx(col_map, "col_map", b.rows), ctypes.byref(ca8), ctypes.byref(cb8), _mat(out8, "out8"),
+          _dtype_code(out8), _ld(out8), _idx(col_map8, "col_map8", b8.rows), _stream(stream))
     return out, out8
 
 
@@ -330,8 +411,9 @@ def gemm_pair_f32(a, b, a8, b8, out, col_map, col_map8, alpha=1.0, stream=None):
     """A pair launch whose fp32 products fill `out` through their column maps
     (tj_gemm_pair_f32): the call may zero `out` and split a long K in two."""
     ca, cb, ca8, cb8 = a.c(), b.c(), a8.c(), b8.c()
-    _call("tj_gemm_pair_f32", ctypes.byref(ca), ctypes.byref(cb), float(alpha), _ptr(col_map), ctypes.byref(ca8),
-          ctypes.byref(cb8), _ptr(col_map8), _ptr(out), out.shape[1], out.stride(0), _stream(stream))
+    _call("tj_gemm_pair_f32", ctypes.byref(ca), ctypes.byref(cb), float(alpha), _idx(col_map, "col_map", b.rows),
+          ctypes.byref(ca8), ctypes.byref(cb8), _idx(col_map8, "col_map8", b8.rows), _mat(out, "out", _FP32),
+          out.shape[1], _ld(out), _stream(stream))
     return out
 
 
@@ -352,9 +434,9 @@ def linear_fwd(x, wq, w8=None, normal_idx=None, outlier_idx=None, out_dtype=torc
     cw, cx = wq.c(), xq.c()
     cw8 = w8.c() if k else None
     cx8 = x8.c() if k else None
-    _call("tj_linear_fwd", _ptr(x), M, K, x.stride(0), ctypes.byref(cw), _ref(cw8), _ptr(normal_idx),
-          _ptr(outlier_idx), k, ctypes.byref(cx), _ref(cx8), _ptr(out), _dtype_code(out), out.stride(0),
-          _stream(stream))
+    _call("tj_linear_fwd", _mat(x, "x", _BF16), M, K, _ld(x), ctypes.byref(cw), _ref(cw8),
+          _idx(normal_idx, "normal_idx", K - k), _idx(outlier_idx, "outlier_idx", k), k, ctypes.byref(cx), _ref(cx8),
+          _mat(out, "out"), _dtype_code(out), _ld(out), _stream(stream))
     return out, xq, (x8 if k else None)
 
 
@@ -369,9 +451,9 @@ def linear_bwd_dx(dy, wq, w8=None, normal_idx=None, outlier_idx=None, seed=0, ou
     out = out if out is not None else torch.empty(M, K, dtype=out_dtype, device=dy.device)
     cw = wq.c()
     cw8 = w8.c() if k else None
-    _call("tj_linear_bwd_dx", _ptr(dy), M, N, dy.stride(0), ctypes.byref(cw), _ref(cw8), _ptr(normal_idx),
-          _ptr(outlier_idx), k, seed, _ptr(out), _dtype_code(out), out.stride(0), _ptr(workspace),
-          workspace.numel(), _stream(stream))
+    _call("tj_linear_bwd_dx", _mat(dy, "dy", _BF16), M, N, _ld(dy), ctypes.byref(cw), _ref(cw8),
+          _idx(normal_idx, "normal_idx", K - k), _idx(outlier_idx, "outlier_idx", k), k, seed, _mat(out, "out"),
+          _dtype_code(out), _ld(out), *_workspace(workspace), _stream(stream))
     return out
 
 
@@ -386,9 +468,9 @@ def linear_bwd_dw(dy, xq, x8=None, normal_idx=None, outlier_idx=None, seed=0, wo
     out = out if out is not None else torch.empty(N, K, dtype=torch.float32, device=dy.device)
     cx = xq.c()
     cx8 = x8.c() if k else None
-    _call("tj_linear_bwd_dw", _ptr(dy), M, N, dy.stride(0), ctypes.byref(cx), _ref(cx8), _ptr(normal_idx),
-          _ptr(outlier_idx), k, seed, _ptr(out), out.stride(0), _ptr(workspace), workspace.numel(),
-          _stream(stream))
+    _call("tj_linear_bwd_dw", _mat(dy, "dy", _BF16), M, N, _ld(dy), ctypes.byref(cx), _ref(cx8),
+          _idx(normal_idx, "normal_idx", K - k), _idx(outlier_idx, "outlier_idx", k), k, seed,
+          _mat(out, "out", _FP32), _ld(out), *_workspace(workspace), _stream(stream))
     return out
 
 
@@ -401,8 +483,10 @@ def linear_bwd_dx_noalloc(dy, wq, w8=None, normal_idx=None, outlier_idx=None, se
     out = out if out is not None else torch.empty(M, wq.cols + k, dtype=out_dtype, device=dy.device)
     cw = wq.c()
     cw8 = w8.c() if k else None
-    _call("tj_linear_bwd_dx_noalloc", _ptr(dy), M, N, dy.stride(0), ctypes.byref(cw), _ref(cw8), _ptr(normal_idx),
-          _ptr(outlier_idx), k, seed, _ptr(out), _dtype_code(out), out.stride(0), _stream(stream))
+    K = wq.cols + k
+    _call("tj_linear_bwd_dx_noalloc", _mat(dy, "dy", _BF16), M, N, _ld(dy), ctypes.byref(cw), _ref(cw8),
+          _idx(normal_idx, "normal_idx", K - k), _idx(outlier_idx, "outlier_idx", k), k, seed, _mat(out, "out"),
+          _dtype_code(out), _ld(out), _stream(stream))
     return out
 
 
@@ -415,8 +499,8 @@ def fp8_linear_fwd(x, w8, out_dtype=torch.bfloat16, x8=None, xt8=None, save_xt=T
     out = out if out is not None else torch.empty(M, w8.rows, dtype=out_dtype, device=x.device)
     cw, cx = w8.c(), x8.c()
     cxt = xt8.c() if save_xt else None
-    _call("tj_fp8_linear_fwd", _ptr(x), M, K, x.stride(0), ctypes.byref(cw), ctypes.byref(cx), _ref(cxt), _ptr(out),
-          _dtype_code(out), out.stride(0), _stream(stream))
+    _call("tj_fp8_linear_fwd", _mat(x, "x", _BF16), M, K, _ld(x), ctypes.byref(cw), ctypes.byref(cx), _ref(cxt),
+          _mat(out, "out"), _dtype_code(out), _ld(out), _stream(stream))
     return out, x8, (xt8 if save_xt else None)
 
 
@@ -429,8 +513,8 @@ def fp8_linear_bwd_dx(dy, wt8, out_dtype=torch.bfloat16, workspace=None, out=Non
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dy.device)
     out = out if out is not None else torch.empty(M, K, dtype=out_dtype, device=dy.device)
     cw = wt8.c()
-    _call("tj_fp8_linear_bwd_dx", _ptr(dy), M, N, dy.stride(0), ctypes.byref(cw), _ptr(out), _dtype_code(out),
-          out.stride(0), _ptr(workspace), workspace.numel(), _stream(stream))
+    _call("tj_fp8_linear_bwd_dx", _mat(dy, "dy", _BF16), M, N, _ld(dy), ctypes.byref(cw), _mat(out, "out"),
+          _dtype_code(out), _ld(out), *_workspace(workspace), _stream(stream))
     return out
 
 
@@ -443,8 +527,8 @@ def fp8_linear_bwd_dw(dy, xt8, workspace=None, out=None, stream=None):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dy.device)
     out = out if out is not None else torch.empty(N, K, dtype=torch.float32, device=dy.device)
     cx = xt8.c()
-    _call("tj_fp8_linear_bwd_dw", _ptr(dy), M, N, dy.stride(0), ctypes.byref(cx), _ptr(out), out.stride(0),
-          _ptr(workspace), workspace.numel(), _stream(stream))
+    _call("tj_fp8_linear_bwd_dw", _mat(dy, "dy", _BF16), M, N, _ld(dy), ctypes.byref(cx), _mat(out, "out", _FP32),
+          _ld(out), *_workspace(workspace), _stream(stream))
     return out
 
 
@@ -455,11 +539,11 @@ def outlier_calibrate(x, sumsq, finalize=False, k=0, stream=None):
     outl = torch.empty(max(k, 1), dtype=torch.int32, device=sumsq.device)
     norm = torch.empty(max(K - k, 1), dtype=torch.int32, device=sumsq.device)
     if x is not None:
-        _call("tj_outlier_calibrate", _ptr(x), _dtype_code(x), x.shape[0], x.shape[1], x.stride(0), _ptr(sumsq), 0,
-              0, None, None, _stream(stream))
+        _call("tj_outlier_calibrate", _mat(x, "x"), _dtype_code(x), x.shape[0], x.shape[1], _ld(x),
+              _arr(sumsq, "sumsq", (torch.float64,)), 0, 0, None, None, _stream(stream))
     if finalize:
-        _call("tj_outlier_calibrate", None, TJ_BF16, 0, K, K, _ptr(sumsq), 1, k, _ptr(outl), _ptr(norm),
-              _stream(stream))
+        _call("tj_outlier_calibrate", None, TJ_BF16, 0, K, K, _arr(sumsq, "sumsq", (torch.float64,)), 1, k,
+              _ptr(outl), _ptr(norm), _stream(stream))
         return outl[:k], norm[:K - k]
     return None
 
@@ -467,9 +551,12 @@ def outlier_calibrate(x, sumsq, finalize=False, k=0, stream=None):
 def osci_reset(w, w_prev, dist_q, dist_m, q_prev, q_out, mask, lr, lr_thr, risk_thr, track=True, stream=None):
     """One OsciReset pass (tj_osci_reset); w, w_prev, dist_q, dist_m updated in place."""
     rows, cols = w.shape
+    n = w.numel()
     cp, co = q_prev.c(), q_out.c()
-    _call("tj_osci_reset", _ptr(w), _ptr(w_prev), _ptr(dist_q), _ptr(dist_m), ctypes.byref(cp), ctypes.byref(co),
-          _ptr(mask), rows, cols, lr, lr_thr, risk_thr, int(track), _stream(stream))
+    _call("tj_osci_reset", _arr(w, "w", _FP32, n), _arr(w_prev, "w_prev", _FP32, n), _arr(dist_q, "dist_q", _FP32, n),
+          _arr(dist_m, "dist_m", _FP32, n), ctypes.byref(cp), ctypes.byref(co),
+          _arr(mask, "mask", _MASK, rows * ((cols + 31) // 32), at_least=True), rows, cols, lr, lr_thr, risk_thr,
+          int(track), _stream(stream))
 
 
 def adamw_osci_reset(w, g, m, v, w_prev, dist_q, dist_m, q_prev, q_out, mask, lr, beta1, beta2, eps, weight_decay,
@@ -477,9 +564,12 @@ def adamw_osci_reset(w, g, m, v, w_prev, dist_q, dist_m, q_prev, q_out, mask, lr
     """AdamW then OsciReset in one pass (tj_adamw_osci_reset); w, m, v, w_prev and the
     distances are updated in place."""
     rows, cols = w.shape
+    n = w.numel()
     cp, co = q_prev.c(), q_out.c()
-    _call("tj_adamw_osci_reset", _ptr(w), _ptr(g), _ptr(m), _ptr(v), _ptr(w_prev), _ptr(dist_q), _ptr(dist_m),
-          ctypes.byref(cp), ctypes.byref(co), _ptr(mask), rows, cols, lr, beta1, beta2, eps, weight_decay, int(step),
+    _call("tj_adamw_osci_reset", _arr(w, "w", _FP32, n), _arr(g, "g", _FP32, n), _arr(m, "m", _FP32, n),
+          _arr(v, "v", _FP32, n), _arr(w_prev, "w_prev", _FP32, n), _arr(dist_q, "dist_q", _FP32, n),
+          _arr(dist_m, "dist_m", _FP32, n), ctypes.byref(cp), ctypes.byref(co),
+          _arr(mask, "mask", _MASK, rows * ((cols + 31) // 32), at_least=True), rows, cols, lr, beta1, beta2, eps, weight_decay, int(step),
           lr_thr, risk_thr, int(track), _stream(stream))
 
 

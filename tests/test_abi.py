@@ -141,3 +141,19 @@ def test_slice_format_checks(lib):
         assert l.tj_quantize_mxfp8(ctypes.c_void_p(256), 0, 128, 128, 128, 0, None, 0, ctypes.byref(m), None) == 3
     m = tj.CMxfp8(256 + 16, 256, 128, 128, tj.TJ_MX_E4M3)           # E4M3 needs 16 bytes only
     assert l.tj_dequantize_mxfp8(ctypes.byref(m), y, 40, None) == 2   # (reaches the ldy check)
+
+
+def test_binding_refuses_host_tensors(lib):
+    """The binding marshals device tensors only: a host tensor, or a quantized tensor whose
+    buffers live on the host, raises ValueError before any library call."""
+    import torch
+
+    from nvfp4_bit_fully_gb300 import tj
+
+    x = torch.zeros(128, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        tj.quantize_nvfp4(x)
+    with pytest.raises(ValueError, match="CUDA"):
+        tj.dequantize_mxfp8(tj.MXFP8.empty(128, 256, device="cpu"))
+    with pytest.raises(ValueError, match="CUDA"):
+        tj.rht(torch.zeros(4, 128), 1, 2)
