@@ -338,11 +338,10 @@ tj_status tj_linear_bwd_dw(const void *dy, int64_t M, int64_t N, int64_t lddy, c
  *   - Problems whose tj_workspace_size(TJ_OP_BWD_DX, ...) exceeds it return
  *     TJ_ERR_WORKSPACE before any launch.
  *   - Allocates nothing (no cudaMalloc / cudaFree, no allocating library routine).
- *   - The first call on each device looks up the scratch's device address
- *     (cudaGetSymbolAddress, with that device current) and keeps it for later calls;
- *     make that first call before any stream capture.  The address belongs to the
- *     device's primary context: do not call this entry point after a cudaDeviceReset in
- *     the same process, nor with another driver context current.
+ *   - Each call looks up the scratch's device address in the current context
+ *     (cudaGetSymbolAddress, a host call); nothing is cached, so the call stays valid
+ *     after a cudaDeviceReset and under any context, and it may be captured into a
+ *     CUDA graph.
  *   - All calls share the one scratch array, which keeps the last call's contents; calls
  *     whose executions overlap on the GPU (other streams, other threads) race on it, so
  *     serialise them.  Nothing needs clearing: each call writes all scratch it reads. */

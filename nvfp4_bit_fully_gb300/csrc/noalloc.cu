@@ -12,14 +12,11 @@
 //
 // The scratch is a file-scope __device__ array of kNoAllocScratchBytes.  Every GPU
 // that loads the library keeps it resident until the process exits.  In host code
-// the array's name is only a host-side stand-in, not a device address, so the
-// device address is looked up once per device with cudaGetSymbolAddress (with that
-// device current) and cached; that lookup happens on the first call on each device.
-// The cached address belongs to the device's primary context, so the entry point is
-// not for use after a cudaDeviceReset in the same process or under another context.
-// No cudaMalloc, cudaFree or allocating library routine is called.
-#include <mutex>
-
+// the array's name is only a host-side stand-in, not a device address, so every call
+// looks the device address up with cudaGetSymbolAddress in the current context (a host
+// call of a few microseconds).  Nothing is cached, so the address stays right after a
+// cudaDeviceReset and under any context.  No cudaMalloc, cudaFree or allocating
+// library routine is called.
 #include "tj_common.cuh"
 #include "tj_internal.h"
 
@@ -28,21 +25,10 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;      // 16 MiB
 static __device__ __align__(256) uint8_t g_bwd_dx_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (nullptr on failure).
+// Device address of the scratch array in the current context (nullptr on failure).
 void *scratch_on_current_device() {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_bwd_dx_scratch) != cudaSuccess) return nullptr;
-        g_scratch_ptr[dev] = p;
-    }
-    return g_scratch_ptr[dev];
+    void *p = nullptr;
+    return cudaGetSymbolAddress(&p, g_bwd_dx_scratch) == cudaSuccess ? p : nullptr;
 }
 
 }  // namespace

@@ -9,7 +9,8 @@ two calls in a row must each give the oracle's dX (oracle.linear.bwd_dx) within
 the GEMM tolerance the other tests use, 2e-3 * sum|a||b| over the oracle's
 quantized operands, and the same bits as tj_linear_bwd_dx with a caller
 workspace; so no byte the previous call left in the scratch reaches the result.
-A problem larger than the fixed scratch is rejected before any launch.  This file
+A problem larger than the fixed scratch is rejected before any launch.  The call
+also works inside a captured CUDA graph, whose replays give the same bits.  This file
 is named to be collected last, and passes alone or after the other tests.
 """
 import ctypes
@@ -109,3 +110,30 @@ def test_noalloc_rejects_problems_beyond_the_scratch(tj):
     code = lib.tj_linear_bwd_dx_noalloc(ctypes.c_void_p(256), M, N, N, ctypes.byref(wq), None, None, None, 0, 1,
                                         ctypes.c_void_p(256), tj.TJ_FP32, K, None)
     assert code == 7                                           # TJ_ERR_WORKSPACE, before any launch
+
+
+def test_noalloc_in_a_cuda_graph(tj):
+    """Captured into a CUDA graph (the scratch address is looked up while capturing) and
+    replayed, the call writes the workspace version's dX byte for byte; after the scratch
+    has been overwritten by an eager call of another shape, a replay still does."""
+    M, N, K, seed = 256, 512, 512, 31
+    W, dY, outl, wq, w8, ni, oi = _problem(tj, M, N, K, True, seed=2)
+    dyd = dY.cuda()
+    ref = tj.linear_bwd_dx(dyd, wq, w8, ni, oi, seed=seed, out_dtype=torch.float32)
+    out = torch.empty_like(ref)
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            tj.linear_bwd_dx_noalloc(dyd, wq, w8, ni, oi, seed=seed, out_dtype=torch.float32, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+        W2, dY2, _, wq2, w82, ni2, oi2 = _problem(tj, 384, 640, 768, False, seed=5)
+        tj.linear_bwd_dx_noalloc(dY2.cuda(), wq2, w82, ni2, oi2, seed=991, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+    tj.device_status()
