@@ -21,6 +21,11 @@
  *     TJ_ERR_CUDA.  Device-side bounded waits that run out set a sticky device
  *     flag read by tj_get_device_status().
  *   - Inputs must be finite.  Padded regions of outputs are written (zeros).
+ *   - Index arrays (sel, normal_idx, outlier_idx, col_map) are device data: the host
+ *     checks their pointers and lengths, not their values.  Their values must lie in
+ *     range (a channel index < the input's columns, a col_map entry < the output's
+ *     columns) and be distinct, as tj_outlier_calibrate writes them; the kernels read
+ *     and write through them unchecked.
  *   - Empty tensors: a tensor with no rows or no columns has no storage, and its
  *     pointers may be NULL.  A call whose outputs are all empty only checks its
  *     arguments.  A product over an empty contraction (K = 0 for a GEMM, no output
