@@ -12,10 +12,12 @@ mbarrier wait is bounded; a wait that runs out sets the CTA's abort flag, after 
 the roles stop working but keep the named-barrier protocol, which has no time bound.
 
 This model restates that protocol at the level of the barriers (one actor per warp, a
-random interleaving per trial) and checks, over thousands of interleavings with and
-without an injected fault (a stage whose loads are never issued, or a wait that runs
-out at a random moment), that every actor finishes and that no warp takes part twice
-in one named-barrier generation.  A promotion warp that stops being live must first
+random interleaving and random relative speeds per trial) and checks, over thousands of
+interleavings with and without an injected fault (a stage whose loads are never issued,
+or a wait that runs out at a random moment), that every actor finishes, that no warp
+takes part twice in one named-barrier generation, and that no block's outer scales are
+overwritten before its promotion (a planted mistake, producers that do not wait for the
+slot's hand-back, is caught).  A promotion warp that stops being live must first
 see the MMA warp meet the slot's previous generation (the kernel's `met` counters,
 compared by parity with the slot's phase, which the model checks is enough);
 without that gate the model finds the double participation that would derail the
@@ -34,8 +36,9 @@ class Violation(Exception):
 
 
 class Model:
-    def __init__(self, works, skip_stage=None, gate=True, rng=None, timeout_at=None):
+    def __init__(self, works, skip_stage=None, gate=True, rng=None, timeout_at=None, wait_sempty=True):
         self.works = works                   # per CTA work list: (nkb4, nk8)
+        self.wait_sempty = wait_sempty       # False: planted mistake, outer-scale slots reloaded unasked
         self.skip = skip_stage
         self.gate = gate
         self.rng = rng or random.Random(0)
@@ -48,6 +51,7 @@ class Model:
         self.pfull = [0] * PSLOTS
         self.sempty = [0] * SSLOTS             # completed phases of each outer-scale slot
         self.sempty_arrivals = [0] * SSLOTS
+        self.sload = [0] * SSLOTS              # outer-scale loads landed per slot
         self.met = [0] * PSLOTS              # generations the MMA warp has met per slot
         self.bar = {s: {"gen": 0, "members": set()} for s in range(PSLOTS)}
 
@@ -114,12 +118,14 @@ class Model:
                 nkbs = min(2, nkb4 - 2 * st) if st < nst4 else 0
                 for j in range(nkbs):
                     f = fbase + 2 * st + j
-                    if f >= SSLOTS and ok:
+                    if f >= SSLOTS and ok and self.wait_sempty:
                         ok = yield from self.wait_bounded(self.sempty, f % SSLOTS, f // SSLOTS - 1)
                 if not ok:
                     break
                 if it != self.skip:
                     self.full[slot] += 1          # expect_tx + copies land
+                    for j in range(nkbs):         # with the outer scales of the stage's blocks
+                        self.sload[(fbase + 2 * st + j) % SSLOTS] += 1
                     issued.add(it)
                 it += 1
             fbase += nkb4
@@ -167,6 +173,8 @@ class Model:
                 ps = blk % PSLOTS
                 if live:
                     live = yield from self.wait_bounded(self.pfull, ps, blk // PSLOTS)
+                if live and kb < nkb4 and self.sload[f4c % SSLOTS] != f4c // SSLOTS + 1:
+                    raise Violation("outer scales of block %d overwritten before their promotion" % f4c)
                 if live:
                     self.arrive(ps, warp)
                     if kb < nkb4:                 # the math is done with the block's outer scales
@@ -195,6 +203,9 @@ class Model:
         actors["mma"] = self.mma()
         actors.update({("promo", q): self.promo(("promo", q)) for q in range(PROMO)})
         pending = dict(actors)
+        # each actor takes 1 to 3 steps per round (drawn per trial), so that some trials run
+        # a role several blocks ahead of another
+        speed = {name: self.rng.choice((1, 1, 2, 3)) for name in actors}
         blocked_rounds = 0
         while pending:
             self.steps += 1
@@ -202,15 +213,16 @@ class Model:
                 raise Violation("no progress: " + str(sorted(map(str, pending))))
             progressed = False
             for name in self.rng.sample(list(pending), len(pending)):
-                before = self.snapshot()
-                try:
-                    next(pending[name])
-                except StopIteration:
-                    del pending[name]
-                    progressed = True
-                    continue
-                if self.snapshot() != before:
-                    progressed = True
+                for _ in range(speed[name]):
+                    before = self.snapshot()
+                    try:
+                        next(pending[name])
+                    except StopIteration:
+                        del pending[name]
+                        progressed = True
+                        break
+                    if self.snapshot() != before:
+                        progressed = True
             if progressed:
                 blocked_rounds = 0
             else:
@@ -223,7 +235,8 @@ class Model:
         return self
 
     def snapshot(self):
-        return (tuple(self.full), tuple(self.empty), tuple(self.pfull), tuple(self.met), tuple(self.sempty),
+        return (tuple(self.full), tuple(self.empty), tuple(self.pfull), tuple(self.met), tuple(self.sload),
+                tuple(self.sempty),
                 tuple(self.sempty_arrivals), self.abort,
                 tuple((b["gen"], len(b["members"])) for b in self.bar.values()))
 
@@ -272,6 +285,21 @@ def test_without_the_gate_a_warp_can_take_part_twice():
             Model([(8, 0), (8, 0)], gate=False, rng=rng, timeout_at=rng.randrange(1, 300)).run()
         except Violation as e:
             found = "twice" in str(e) or "deadlock" in str(e)
+            if found:
+                break
+    assert found
+
+
+def test_outer_scale_slots_need_the_hand_back():
+    """Planted in the model: the producers load a stage without waiting for its blocks'
+    outer-scale slots to be handed back.  Some interleaving then overwrites a block's outer
+    scales before every promotion warp has used them."""
+    found = False
+    for seed in range(500):
+        try:
+            Model([(16, 0), (16, 0)], rng=random.Random(seed), wait_sempty=False).run()
+        except Violation as e:
+            found = "overwritten" in str(e)
             if found:
                 break
     assert found
