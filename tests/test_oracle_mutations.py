@@ -17,9 +17,11 @@ import types
 import pytest
 
 import test_oracle_formats as TF
+import test_oracle_mx_formats as TM
 import test_oracle_osci_calib as TO
 import test_oracle_quant as TQ
 import test_oracle_rht_linear as TR
+from oracle import formats as F
 from oracle import quant as Q
 
 
@@ -116,6 +118,29 @@ CASES = [
     ("AdamW without the first-moment bias correction", "oracle.osci",
      '"step_size": F32(lr / (1.0 - b1 ** t))', '"step_size": F32(lr)',
      [TO.test_adamw_first_step_closed_form, TO.test_adamw_matches_torch_optim_adamw]),
+    ("outlier channels kept among the normal ones", "oracle.linear",
+     "mask[np.asarray(outlier_idx, dtype=np.int64)] = False", "mask[np.asarray(outlier_idx, dtype=np.int64)] = True",
+     [TR.test_forward_with_outlier_slice_on_representable_inputs]),
+    ("dW slice operands not transposed", "oracle.linear",
+     "dYt = np.ascontiguousarray(np.asarray(dY, dtype=F32).T)", "dYt = np.ascontiguousarray(np.asarray(dY, dtype=F32))",
+     [TR.test_backward_is_unbiased_over_seeds]),
+    ("dist_Q accumulates the step of the weight, not of Q-hat", "oracle.osci",
+     "dist_q = (state[\"dist_q\"] + np.abs((qh - state[\"qhat_prev\"]).astype(F32))).astype(F32)",
+     "dist_q = (state[\"dist_q\"] + np.abs((w - state[\"w_prev\"]).astype(F32))).astype(F32)",
+     [lambda: TO.test_pages_oscillation_example_resets_on_schedule(_golden()), TO.test_reset_condition_and_state_update]),
+    ("calibration sums |x| instead of x^2", "oracle.calib",
+     "chunk = chunk + x[t] * x[t]", "chunk = chunk + np.abs(x[t])",
+     [TO.test_calibration_ties_and_exact_sums, TO.test_calibration_planted_channels_and_brute_force]),
+    ("E2M3 exponent bias 2", "oracle.formats",
+     "(1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 1.0))", "(1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 2.0))",
+     [lambda: TM.test_decode_matches_the_hand_tables(F.MX_E2M3)]),
+    ("MX element ties away from zero", "oracle.formats",
+     "((d_hi == d_lo) & ((codes[hi] & 1) == 0))", "(d_hi == d_lo)",
+     [lambda: TM.test_rne_by_brute_force(F.MX_E3M2), lambda: TM.test_rne_by_brute_force(F.MX_E2M3)]),
+    ("MX block scale applied the wrong way", "oracle.quant",
+     "scale_inv = np.exp2(-E.astype(np.float64))\n    y = xb.astype(np.float64)",
+     "scale_inv = np.exp2(E.astype(np.float64))\n    y = xb.astype(np.float64)",
+     [lambda: TM.test_grid_inputs_quantize_exactly_and_the_product_is_a_matmul(F.MX_E2M3)]),
 ]
 
 
