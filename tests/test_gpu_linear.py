@@ -123,6 +123,29 @@ def test_every_channel_an_outlier(tj):
     _run_and_check(tj, X, W, dY, np.arange(K), seed=9)
 
 
+def _random_case(case):
+    """A seeded random layer: M, N, K anywhere from one element to a few tiles (so every
+    dimension is ragged in its own way), and 0 to 80 outlier channels at random positions
+    (every channel, when K is that small)."""
+    rng = np.random.default_rng(4000 + case)
+    M, N, K = int(rng.integers(1, 520)), int(rng.integers(1, 400)), int(rng.integers(1, 600))
+    k = int(rng.integers(0, min(K, 80) + 1))
+    outl = np.sort(rng.choice(K, k, replace=False)).astype(np.int64)
+    g = torch.Generator().manual_seed(4000 + case)
+    X = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    W = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16)
+    dY = (torch.randn(M, N, generator=g) * 1e-3).to(torch.bfloat16)
+    return X, W, dY, outl
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_random_ragged_shapes(tj, case):
+    """Twelve seeded random shapes and outlier sets through forward, dX and dW, checked like
+    the fixed cases: every quantized operand bit for bit, the products within tolerance."""
+    X, W, dY, outl = _random_case(case)
+    _run_and_check(tj, X, W, dY, outl, seed=17 + case)
+
+
 def test_ragged_linear(tj):
     g = torch.Generator().manual_seed(11)
     M, N, K = 200, 136, 328
