@@ -271,9 +271,9 @@ class OsciState:
 # listed report traffic None.  k_osci_reset: 1913.3 MB over 67,108,864 weights.
 TRAFFIC_BYTES_PER_ELEM = {"k_osci_reset": 28.55}
 # DRAM bytes per launch of the GEMM: the twelve launches of one timed step of the layer set
-# at 16384 tokens read 940.9 MB and wrote 365.1 MB (one-pass ncu capture of the current
-# kernel), 108.8 MB per launch on average.  Valid for the default workload only.
-TRAFFIC_BYTES_PER_LAUNCH = {"k_gemm_nvfp4": 108.8e6}
+# at 16384 tokens read 939.9 MB and wrote 363.6 MB (one-pass ncu capture of the current
+# kernel), 108.6 MB per launch on average.  Valid for the default workload only.
+TRAFFIC_BYTES_PER_LAUNCH = {"k_gemm_nvfp4": 108.6e6}
 # Lane instructions per element of the issue-bound quantize kernels (smsp__thread_inst_executed
 # of one ncu capture of the current kernel versions, `bench.py --only quant`, divided by the
 # elements each launch processes: dY elements for the row / column passes, input elements of

@@ -273,6 +273,18 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
     return d;
 }
 
+// A 16-byte shared-memory load issued where it stands in the program: each of the
+// promotion's column-scale loads then sits right before the math that uses it.  Left to
+// the compiler, the same loads were scheduled otherwise and the layer set's GEMMs took 5%
+// longer (1.88 against 1.78 ms per step).
+__device__ __forceinline__ float4 lds128_in_order(const float4 *p) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(ptx::smem_u32(p)));
+    return v;
+}
+
 // The barrier protocol of a promotion warp that has stopped waiting for partials (a
 // wait ran out, or another role aborted), from block kb of `tile` on: it takes part in
 // every remaining generation of the partial slots' named barriers with a sync.  A live
@@ -541,7 +553,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                                 so + 128 + kColsW * cq + kLdCols * ch);
 #pragma unroll
                             for (int i = 0; i < kLdCols / 4; ++i) {
-                                const float4 sb = sbp[i];         // broadcast read: all lanes, same address
+                                const float4 sb = lds128_in_order(sbp + i);   // broadcast: all lanes, one address
                                 const uint64_t w0 = mul2(sa2, pack2(sb.x, sb.y));
                                 const uint64_t w1 = mul2(sa2, pack2(sb.z, sb.w));
                                 ac[2 * i] = fma2((uint64_t)p[4 * i] | ((uint64_t)p[4 * i + 1] << 32), w0, ac[2 * i]);
