@@ -545,8 +545,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     uint64_t *ac = acc + (kLdCols / 2) * ch;
                     if (kb < w.nkb4) {
                         {
-                            // the block's outer scales: its slot goes back to the producers only
-                            // after this warp has released the next block's partial
+                            // the block's outer scales: their slot goes back to the producers once
+                            // every promotion warp has done this math (the arrivals below)
                             const float sa = so[32 * q + lane] * alpha;
                             const uint64_t sa2 = pack2(sa, sa);
                             const float4 *sbp = reinterpret_cast<const float4 *>(
