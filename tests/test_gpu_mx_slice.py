@@ -191,16 +191,41 @@ def test_pair_launches_with_fp6_fp4_slice(tj):
         assert_gemm_close(g_[:, cm8.cpu().numpy()], ref8, b8_, what=what + " fp4 x fp6 slice")
 
 
-@pytest.mark.parametrize("fmt_x,fmt_w", [(F.MX_E2M3, F.MX_E2M1), (F.MX_E3M2, F.MX_E2M1), (F.MX_E2M1, F.MX_E2M3)])
-def test_linear_with_fp6_fp4_slice(tj, fmt_x, fmt_w):
-    rng = np.random.default_rng(fmt_x * 7 + fmt_w)
-    M, N, K, seed = 256, 320, 512, 21
+SLICE_PAIRS = [(F.MX_E2M3, F.MX_E2M1), (F.MX_E3M2, F.MX_E2M1), (F.MX_E2M1, F.MX_E2M3)]
+
+
+def _slice_layer(rng, M, N, K, k):
     X = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32))
-    outl = np.sort(rng.choice(K, 40, replace=False))
+    outl = np.sort(rng.choice(K, k, replace=False))
     X[:, torch.from_numpy(outl)] *= 20
     X = X.to(torch.bfloat16)
     W = torch.from_numpy((rng.standard_normal((N, K)) * 0.05).astype(np.float32)).to(torch.bfloat16)
     dY = torch.from_numpy(rng.standard_normal((M, N)).astype(np.float32)).to(torch.bfloat16)
+    return X, W, dY, outl
+
+
+@pytest.mark.parametrize("fmt_x,fmt_w", SLICE_PAIRS)
+def test_linear_with_fp6_fp4_slice(tj, fmt_x, fmt_w):
+    rng = np.random.default_rng(fmt_x * 7 + fmt_w)
+    X, W, dY, outl = _slice_layer(rng, 256, 320, 512, 40)
+    _check_slice_linear(tj, X, W, dY, outl, fmt_x, fmt_w, 21)
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_linear_with_fp6_fp4_slice_random_shapes(tj, case):
+    """Six seeded random layers (M, N, K from one element to a few tiles, 1 to 80 outlier
+    channels), each with a random FP6 x FP4 slice pairing, under the same checks."""
+    rng = np.random.default_rng(5000 + case)
+    M, N, K = int(rng.integers(1, 520)), int(rng.integers(1, 400)), int(rng.integers(2, 600))
+    k = int(rng.integers(1, min(K, 80) + 1))
+    fmt_x, fmt_w = SLICE_PAIRS[int(rng.integers(0, len(SLICE_PAIRS)))]
+    X, W, dY, outl = _slice_layer(rng, M, N, K, k)
+    _check_slice_linear(tj, X, W, dY, outl, fmt_x, fmt_w, 31 + case)
+
+
+def _check_slice_linear(tj, X, W, dY, outl, fmt_x, fmt_w, seed):
+    M, K = X.shape
+    N = W.shape[0]
     k = len(outl)
     nc = OL.normal_channels(K, outl)
     ni, oi = torch.from_numpy(nc.astype(np.int32)).cuda(), torch.from_numpy(outl.astype(np.int32)).cuda()
