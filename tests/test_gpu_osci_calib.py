@@ -32,7 +32,12 @@ def _mask_bits(mask_words, rows, cols):
     return bits.reshape(rows, -1)[:, :cols].astype(bool)
 
 
-@pytest.mark.parametrize("rows,cols", [(64, 256), (100, 200)])
+# the odd column counts take the kernel's scalar path (rows not 16-byte aligned) and leave a
+# ragged last mask word and a ragged last 128-element block
+ODD_SHAPES = [(1, 1), (3, 130), (129, 33), (50, 517)]
+
+
+@pytest.mark.parametrize("rows,cols", [(64, 256), (100, 200)] + ODD_SHAPES)
 def test_osci_reset_trajectory_bit_exact(tj, rows, cols):
     rng = np.random.default_rng(rows + cols)
     w0 = (rng.standard_normal((rows, cols)) * 0.02).astype(np.float32)
@@ -66,7 +71,7 @@ def test_osci_reset_trajectory_bit_exact(tj, rows, cols):
     assert state["dist_m"].max() > 0
 
 
-@pytest.mark.parametrize("rows,cols", [(64, 256), (37, 200)])
+@pytest.mark.parametrize("rows,cols", [(64, 256), (37, 200)] + ODD_SHAPES)
 def test_adamw_osci_reset_trajectory_bit_exact(tj, rows, cols):
     """The fused training-step pass (AdamW, then OsciReset of the updated weights) equals the
     oracle's AdamW step followed by its OsciReset step, bit for bit, over a schedule whose
@@ -106,7 +111,8 @@ def test_adamw_osci_reset_trajectory_bit_exact(tj, rows, cols):
         assert_nvfp4_equal(q_out, q_ref, "Q step %d" % t)
         resets += int(m_ref.sum())
         q_prev, q_out = q_out, q_prev
-    assert resets > 0
+    if rows * cols >= 1024:                   # enough weights for some of them to oscillate
+        assert resets > 0
 
 
 def test_osci_reset_in_place_q(tj):
