@@ -157,3 +157,52 @@ def test_binding_refuses_host_tensors(lib):
         tj.dequantize_mxfp8(tj.MXFP8.empty(128, 256, device="cpu"))
     with pytest.raises(ValueError, match="CUDA"):
         tj.rht(torch.zeros(4, 128), 1, 2)
+
+
+def test_binding_layout_dtype_and_length_rules(monkeypatch):
+    """The binding's argument rules on host tensors, with its device check stubbed out: a
+    matrix needs adjacent columns and a call's dtype; a single row is passed with its length
+    as row stride; index lists are 1-D contiguous int32 with enough entries; state arrays
+    are contiguous with the weight's size; a quantized tensor's buffers have their padded
+    sizes."""
+    import torch
+
+    from nvfp4_bit_fully_gb300 import tj
+
+    monkeypatch.setattr(tj, "_cuda", lambda t, name: None)
+    x = torch.zeros(64, 256, dtype=torch.bfloat16)
+    assert tj._mat(x, "x") is not None and tj._ld(x) == 256
+    assert tj._ld(x[:, 8:72]) == 256                                     # a column slice keeps its row stride
+    for bad, what in ((x.t(), "adjacent"), (x[:, ::2], "adjacent"), (x.float()[0], "2-D"),
+                      (x.half(), "dtype")):
+        with pytest.raises(ValueError, match=what):
+            tj._mat(bad, "x")
+    with pytest.raises(ValueError, match="dtype"):
+        tj._mat(x, "x", tj._FP32)
+    col = torch.zeros(256, 1, dtype=torch.bfloat16)
+    assert tj._mat(col.t(), "x") is not None and tj._ld(col.t()) == 256   # one row: its own length
+    idx = torch.arange(10, dtype=torch.int32)
+    assert tj._idx(idx, "i", 10) is not None
+    for bad, n, what in ((idx.long(), None, "dtype"), (idx[::2], None, "contiguous"), (idx.view(2, 5), None, "1-D"),
+                         (idx, 11, "at least 11")):
+        with pytest.raises(ValueError, match=what):
+            tj._idx(bad, "i", n)
+    st = torch.zeros(64, 256)
+    assert tj._arr(st, "w", tj._FP32, st.numel()) is not None
+    with pytest.raises(ValueError, match="elements"):
+        tj._arr(st[:32], "w", tj._FP32, st.numel())
+    with pytest.raises(ValueError, match="contiguous"):
+        tj._arr(torch.zeros(64, 512)[:, :256], "w", tj._FP32, st.numel())
+    q = tj.NVFP4.empty(100, 300, device="cpu")
+    assert (q.codes.numel(), q.sf.numel(), q.outer.numel()) == (128 * 384 // 2, 128 * 384 // 16, 3 * 128)
+    q.c()
+    with pytest.raises(ValueError, match="codes"):
+        tj.NVFP4(q.codes[:-1], q.sf, q.outer, 100, 300).c()
+    with pytest.raises(ValueError, match="outer"):
+        tj.NVFP4(q.codes, q.sf, q.outer.view(torch.int32), 100, 300).c()
+    m = tj.MXFP8.empty(100, 300, device="cpu", fmt=tj.TJ_MX_E2M3)
+    assert m.codes.numel() == 128 * 384 * 6 // 8
+    m.c()
+    m.fmt = 2
+    with pytest.raises(ValueError, match="format"):
+        m.c()
